@@ -1,0 +1,378 @@
+"""Benchmark of the MLA hot path on GB300 (one JSON line on rank 0).
+
+Workload: absorbed MLA speculative decode, batch 4, q_len 4, 16 heads, 32768 cached tokens
+per request, 64-token pages scattered in a shared pool, bf16 (synthetic, seeded).  One
+step = one mla_decode call (plan cached; split-KV partial kernel + LSE combine kernel).
+Inputs are rotated over several independent input sets whose KV totals more than twice
+the L2 size, so every step streams its KV from HBM.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+N > 1 runs under torchrun: every rank runs an independent replica (the path has no
+exchange step); value = all ranks' KV bytes / max-over-ranks time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from mla_attention_paged_gb300.inputs import decode_workloads, make_decode_inputs  # noqa: E402
+
+METRIC = "MLA decode KV-read GB/s & µs/call vs 8 TB/s; varlen prefill TFLOP/s"
+WORKLOAD = "decode_b4_q4_h16_l32k"
+L2_BYTES = 129 * 1024 * 1024
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                "source": "measured"}
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+def decode_bytes(wl):
+    """Algorithmic bytes of one decode call: each request's latent rows once, its page-table
+    entries, and the query / output / lse rows."""
+    e = 1 if wl.kv_dtype == "e4m3" else 2
+    kv = sum(L * 576 * e for L in wl.seq_lens)
+    pt = sum(((L + wl.page_size - 1) // wl.page_size) * 4 for L in wl.seq_lens)
+    io = wl.batch * wl.q_len * wl.heads * (576 * 2 + 512 * 2 + 4)
+    return kv, kv + pt + io
+
+
+def decode_flops(wl):
+    return 2 * sum(wl.q_len * wl.heads * L * (576 + 512) for L in wl.seq_lens)
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200",
+                 "-i", str(device_index)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out = ""
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend)
+    return ws, rank, local
+
+
+def _barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def _max_over_ranks(x, ws, device):
+    if ws == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def _sum_over_ranks(x, ws, device):
+    if ws == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def _traffic_record(kernel_src):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on the
+    current kernel source; otherwise None."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "decode_partial_traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+        src = open(os.path.join(ROOT, "mla_attention_paged_gb300", "csrc", kernel_src), "rb").read()
+        if rec.get("source_sha256") != hashlib.sha256(src).hexdigest():
+            return None
+        return rec
+    except Exception:
+        return None
+
+
+def cpu_baseline(wl, inp_cpu, budget_s=15.0):
+    """The fp64 oracle, as it stands, on a bounded sample of this workload's rows."""
+    import numpy as np
+
+    import oracle
+    oracle.build()
+    rows_total = wl.batch * wl.q_len * wl.heads
+    rng = np.random.default_rng(0)
+    n = 8
+    done_rows, elapsed = 0, 0.0
+    while True:
+        rows = rng.choice(rows_total, size=min(n, rows_total), replace=False)
+        t0 = time.perf_counter()
+        oracle.mla_decode(inp_cpu.q, inp_cpu.kv_pool, inp_cpu.page_table, inp_cpu.seq_lens, inp_cpu.scale,
+                          kv_scale=inp_cpu.kv_scale, rows=rows)
+        dt = time.perf_counter() - t0
+        done_rows += len(rows)
+        elapsed += dt
+        if elapsed >= budget_s or done_rows >= rows_total:
+            break
+        per_row = elapsed / done_rows
+        n = int(max(8, min(rows_total, (budget_s - elapsed) / max(per_row, 1e-9))))
+    kv_bytes, _ = decode_bytes(wl)
+    step_s = elapsed * rows_total / done_rows
+    return {"value": kv_bytes / step_s / 1e9, "unit": "GB/s", "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"{done_rows} of {rows_total} (request, draft, head) rows of {wl.name}, fp64, "
+                      f"{elapsed:.1f} s; step time scaled by rows", "seconds": round(elapsed, 2)}
+
+
+def run_reference(args, ws, rank):
+    """Reference arm: the CPU fp64 oracle timed on bounded samples of the same workload."""
+    if rank != 0:
+        return
+    import numpy as np
+
+    import oracle
+    oracle.build()
+    wl = decode_workloads()[WORKLOAD]
+    inp = make_decode_inputs(wl, "cpu")
+    rows_total = wl.batch * wl.q_len * wl.heads
+    rng = np.random.default_rng(1)
+    rows_per_step = 4
+    for _ in range(args.warmup):
+        oracle.mla_decode(inp.q, inp.kv_pool, inp.page_table, inp.seq_lens, inp.scale,
+                          rows=rng.choice(rows_total, rows_per_step, replace=False))
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.mla_decode(inp.q, inp.kv_pool, inp.page_table, inp.seq_lens, inp.scale,
+                          rows=rng.choice(rows_total, rows_per_step, replace=False))
+    el = time.perf_counter() - t0
+    kv_bytes, _ = decode_bytes(wl)
+    step_s = el / args.steps * rows_total / rows_per_step
+    val = kv_bytes / step_s / 1e9
+    line = {"impl": "reference", "metric": METRIC, "value": val, "unit": "GB/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_s * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "batch": wl.batch, "q_len": wl.q_len, "heads": wl.heads,
+                       "kv_len": wl.seq_lens[0], "page_size": wl.page_size, "kv_dtype": wl.kv_dtype},
+            "cpu_baseline": {"value": val, "unit": "GB/s", "cores": oracle.num_threads(), "kind": "oracle",
+                             "sample": f"{rows_per_step} of {rows_total} rows per step, step time scaled by rows"},
+            "e2e": {"value": val, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="mine", choices=["mine", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    ws, rank, local = _dist()
+    if args.impl == "reference":
+        run_reference(args, ws, rank)
+        return
+
+    from mla_attention_paged_gb300 import build
+    if rank == 0 or ws == 1:
+        build.build()
+    _barrier(ws)
+    from mla_attention_paged_gb300 import mla
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    wl = decode_workloads()[WORKLOAD]
+    kv_bytes, alg_bytes = decode_bytes(wl)
+    n_sets = max(2, math.ceil(2.5 * L2_BYTES / kv_bytes) + 1)
+    sets = []
+    for i in range(n_sets):
+        wl_i = decode_workloads()[WORKLOAD]
+        wl_i.seed = wl.seed + 97 * i + 1000 * rank
+        sets.append(make_decode_inputs(wl_i, dev))
+    s0 = sets[0]
+    plan = mla.decode_plan(wl.seq_lens, wl.q_len, wl.heads, wl.page_size, s0.page_table.shape[1],
+                           s0.kv_pool.shape[0], mla.MLA_KV_BF16)
+    ws_buf = mla.workspace_for(plan, dev)
+    outs = [torch.empty(wl.batch, wl.q_len, wl.heads, 512, dtype=torch.bfloat16, device=dev) for _ in sets]
+    lses = [torch.empty(wl.batch, wl.q_len, wl.heads, dtype=torch.float32, device=dev) for _ in sets]
+    stream = torch.cuda.Stream(device=dev)
+
+    def step(i, st):
+        s = sets[i % n_sets]
+        mla.decode(plan, s.q, s.kv_pool, s.page_table, s.seq_lens, s.scale, 1.0, out=outs[i % n_sets],
+                   lse=lses[i % n_sets], workspace=ws_buf, stream=st)
+
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            step(i, stream)
+    stream.synchronize()
+    assert mla.get_status(stream) == mla.MLA_OK
+
+    # Timed region: one CUDA graph holding exactly K steps; the first (up to) 256 steps
+    # carry event pairs around the split-KV partial kernel.
+    n_ev = min(args.steps, 256)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_ev)]
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        for i in range(args.steps):
+            if i < n_ev:
+                mla.set_profile_events(ev[i][0], ev[i][1])
+            elif i == n_ev:
+                mla.set_profile_events(None, None)
+            step(i, stream)
+    mla.set_profile_events(None, None)
+    stream.synchronize()
+    # pre-roll under the clock sampler, then the timed replay
+    sampler = ClockSampler(local)
+    t_end = time.perf_counter() + 1.0
+    with torch.cuda.stream(stream):
+        while time.perf_counter() < t_end:
+            graph.replay()
+            stream.synchronize()
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    _barrier(ws)
+    torch.cuda.synchronize(dev)
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        graph.replay()
+        stop.record(stream)
+    stream.synchronize()
+    torch.cuda.synchronize(dev)
+    _barrier(ws)
+    clocks = sampler.stop()
+    status = mla.get_status(stream)
+    if status != mla.MLA_OK:
+        raise RuntimeError(f"device status {mla.status_string(status)}")
+    ms = start.elapsed_time(stop)
+    ms_max = _max_over_ranks(ms, ws, dev)
+    total_bytes = _sum_over_ranks(kv_bytes * args.steps, ws, dev)
+    value = total_bytes / (ms_max / 1e3) / 1e9
+    part_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    peaks = _peaks()
+    achieved = alg_bytes / (part_ms / 1e3) / 1e9
+    traffic = _traffic_record("mla_decode_sm103a.cu")
+
+    # End to end through the public API: pinned host q/page_table/seq_lens -> device each
+    # step, decode, out+lse -> pinned host each step.  The latent cache is device-resident.
+    host_in = [(s.q.cpu().pin_memory(), s.page_table.cpu().pin_memory(), s.seq_lens.cpu().pin_memory()) for s in sets]
+    dev_in = [(torch.empty_like(s.q), torch.empty_like(s.page_table), torch.empty_like(s.seq_lens)) for s in sets]
+    host_out = [(torch.empty(o.shape, dtype=o.dtype).pin_memory(), torch.empty(l.shape, dtype=l.dtype).pin_memory())
+                for o, l in zip(outs, lses)]
+    h2d = sum(t.numel() * t.element_size() for t in host_in[0])
+    d2h = sum(t.numel() * t.element_size() for t in host_out[0])
+    e2e_steps = min(args.steps, 500)
+
+    def e2e_step(i):
+        k = i % n_sets
+        s = sets[k]
+        for d, h in zip(dev_in[k], host_in[k]):
+            d.copy_(h, non_blocking=True)
+        mla.decode(plan, dev_in[k][0], s.kv_pool, dev_in[k][1], dev_in[k][2], s.scale, 1.0, out=outs[k],
+                   lse=lses[k], workspace=ws_buf, stream=stream)
+        host_out[k][0].copy_(outs[k], non_blocking=True)
+        host_out[k][1].copy_(lses[k], non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            e2e_step(i)
+        stream.synchronize()
+        _barrier(ws)
+        t0 = time.perf_counter()
+        for i in range(e2e_steps):
+            e2e_step(i)
+        stream.synchronize()
+        e2e_s = time.perf_counter() - t0
+    e2e_s = _max_over_ranks(e2e_s, ws, dev)
+    e2e_val = _sum_over_ranks(kv_bytes * e2e_steps, ws, dev) / e2e_s / 1e9
+
+    launches_per_step = 1 + (1 if plan.max_splits > 1 else 0)
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_max / args.steps, "us_per_call": ms_max / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1)/sqrt(576) latents, shuffled 64-token pages)",
+        "config": {"workload": WORKLOAD, "batch": wl.batch, "q_len": wl.q_len, "heads": wl.heads,
+                   "kv_len": wl.seq_lens[0], "page_size": wl.page_size, "kv_dtype": wl.kv_dtype,
+                   "parallelism": f"replicas x{ws}", "l2": f"inputs rotated over {n_sets} sets "
+                   f"({n_sets * kv_bytes / 2**20:.0f} MiB KV > 2.5x L2)",
+                   "timing": "one CUDA graph of K steps, CUDA events on the launch stream",
+                   "splits": plan.max_splits, "chunk_tokens": plan.chunk_tokens},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": achieved / peaks["hbm_gbs"],
+                     "traffic": (traffic["dram_bytes_per_launch"] if traffic else None),
+                     "kernel": "decode_partial_bf16_kernel", "kernel_us": part_ms * 1e3,
+                     "alg_bytes_per_launch": alg_bytes, "peak_source": peaks["source"]},
+        "e2e": {"value": e2e_val, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "steps": e2e_steps, "us_per_call": e2e_s / e2e_steps * 1e6},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clocks,
+    }
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        inp_cpu = make_decode_inputs(decode_workloads()[WORKLOAD], "cpu")
+        line["cpu_baseline"] = cpu_baseline(wl, inp_cpu)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

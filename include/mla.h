@@ -1,0 +1,166 @@
+/*
+ * mla.h -- C ABI of libmla: Multi-head Latent Attention (MLA) over a paged latent KV
+ * cache on GB300 (sm_103a).
+ *
+ * Sources.  The operations follow the TokenSpeed pages:
+ *  [TALK]  "构建面向 Agentic 推理的下一代 LLM 推理引擎" (AICon 2026 Shenzhen talk
+ *          transcript), section "Kernel：让 MLA 真正跑满 GPU": MLA keeps one latent
+ *          state shared by all heads; decode's first matmul is query x latent key with a
+ *          query length of one, so query tokens are folded into the head axis; the KV
+ *          loop is split into a partial stage and a reduction stage whose split count
+ *          and workspace size are computed automatically at run time and cached; the
+ *          prefill path is a ragged no-padding batch whose Q and KV lengths differ
+ *          because a long prefix (>90% hit rate) is cached and only a few hundred tokens
+ *          are appended.  Even with 8-bit KV, loading KV is the bottleneck.
+ *  [BLOG]  "英偉達力薦，小團隊兩個月開源一款「光速級」智能體推理引擎" (Synced repost of the
+ *          TokenSpeed launch blog), sections "TokenSpeed 技術簡介" and "TokenSpeed 性能
+ *          預覽": the decode kernel folds the query-sequence axis into the head axis to
+ *          fill the M tile of the first batched matmul; decode is benchmarked with
+ *          speculative decoding at batch 4/8/16 over long prefixes; prefill is "prefill
+ *          with a long prefix KV cache".
+ *  [READ]  "TokenSpeed 深度解析" (gitread.org), section "核心技术揭秘": KV is managed in
+ *          fixed-size blocks reached through a table (paged KV).
+ *
+ * Shapes used throughout: B requests, T = q_len draft tokens per request (1..8), H heads,
+ * D = 576 latent columns (512 latent + 64 rope), Dv = 512 (the value is the first 512
+ * latent columns).  Prefill: 16-bit q/k with Dqk = 192 and v with Dv' = 128.
+ *
+ * Conventions shared by every call:
+ *  - Every pointer argument that is not documented as host memory is DEVICE memory owned
+ *    by the caller.  The library never allocates or frees device memory and never
+ *    synchronises the stream in mla_decode / mla_prefill_varlen.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *  - Tensors are dense and row-major (last index fastest), with the layouts given below.
+ *  - Every call returns an mla_status_t code; no C++ exception crosses this ABI.
+ *    Host-side argument checks run before anything is enqueued; on a non-zero return
+ *    nothing was launched unless the code is MLA_ERR_CUDA.
+ *  - Device-side failures (a bounded wait that ran out, a length beyond the plan) are
+ *    recorded in a per-device status word that mla_get_status() reads and clears.
+ */
+#ifndef MLA_GB300_MLA_H_
+#define MLA_GB300_MLA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum mla_status_t {
+  MLA_OK = 0,
+  MLA_ERR_INVALID_ARG = 1,         /* null pointer, negative size, inconsistent shapes   */
+  MLA_ERR_UNSUPPORTED = 2,         /* shape the kernels do not implement (see each call) */
+  MLA_ERR_WORKSPACE_TOO_SMALL = 3, /* workspace_bytes < plan->workspace_bytes            */
+  MLA_ERR_CUDA = 4,                /* a CUDA runtime/driver call or launch failed        */
+  MLA_ERR_TIMEOUT = 5,             /* a device-side bounded wait expired (status word)   */
+  MLA_ERR_DEVICE_ARG = 6           /* device-side argument check failed (status word)    */
+} mla_status_t;
+
+typedef enum mla_kv_dtype_t {
+  MLA_KV_BF16 = 0, /* latent pool stored as bfloat16                                     */
+  MLA_KV_E4M3 = 1  /* latent pool stored as OCP FP8 e4m3fn codes times one kv_scale      */
+} mla_kv_dtype_t;
+
+/* Decode plan: a plain value struct filled by mla_decode_plan(); callers treat the
+ * fields as read-only.  It fixes the launch shape of mla_decode for one batch layout. */
+typedef struct mla_decode_plan_t {
+  int32_t batch;             /* B                                                        */
+  int32_t q_len;             /* T, draft tokens per request                              */
+  int32_t num_heads;         /* H                                                        */
+  int32_t page_size;         /* tokens per page                                          */
+  int32_t max_pages_per_seq; /* row stride of page_table                                 */
+  int32_t kv_dtype;          /* mla_kv_dtype_t                                           */
+  int64_t num_pages;         /* pages in the pool (first dimension of kv_pages)          */
+  int32_t num_sms;           /* SMs the split count was sized for                        */
+  int32_t rows;              /* T*H folded query rows per request                        */
+  int32_t head_groups;       /* CTAs along the folded row axis (64 rows each)            */
+  int32_t chunk_tokens;      /* keys per split (multiple of 64)                          */
+  int32_t max_splits;        /* splits of the longest request                            */
+  int32_t max_seq_len;       /* longest planned request; device seq_lens must not exceed */
+  size_t workspace_bytes;    /* bytes mla_decode needs in `workspace` (0 = none)         */
+} mla_decode_plan_t;
+
+/* Plan one decode launch: pick the keys-per-split chunk so that the partial kernel
+ * fills the GPU's SMs in one wave (one CTA per SM per (request, split, 64-row group)),
+ * and size the workspace for the split partials.  Plans are memoised on all arguments
+ * (the split count and workspace are "computed automatically at run time and cached",
+ * [TALK] Kernel section).
+ *   seq_lens_host : HOST int32[batch], tokens cached per request INCLUDING the q_len
+ *                   draft tokens (the drafts are the last q_len positions).
+ *   num_sms       : SMs to plan for; 0 = query the current device.
+ * Errors: MLA_ERR_INVALID_ARG (null pointers, batch < 1, a length < q_len or beyond
+ * max_pages_per_seq*page_size), MLA_ERR_UNSUPPORTED (q_len > 8, page_size not one of
+ * 8,16,32,64,128,256, or more than 1024 folded rows), MLA_ERR_CUDA (device query). */
+int mla_decode_plan(int batch, const int32_t* seq_lens_host, int q_len, int num_heads,
+                    int page_size, int max_pages_per_seq, int64_t num_pages, int kv_dtype,
+                    int num_sms, mla_decode_plan_t* plan_out);
+
+/* Absorbed MLA decode with speculative draft tokens over the paged latent cache.
+ *   q          : [B, T, H, 576] bf16.  Folded row m = t*H + h of request b.
+ *   kv_pages   : [num_pages, page_size, 576] bf16 or e4m3 bytes (plan->kv_dtype).
+ *   page_table : [B, max_pages_per_seq] int32; latent row j of request b is
+ *                kv_pages[page_table[b, j / page_size], j % page_size, :].
+ *   seq_lens   : [B] int32 device copy of the planned lengths (each <= max_seq_len).
+ *   scale      : softmax scale applied to q . k.
+ *   kv_scale   : per-tensor dequantisation scale of an e4m3 pool (ignored for bf16).
+ *   out        : [B, T, H, 512] bf16, out[b,t,h] = sum_j softmax_j(scale q.k_j) v_j with
+ *                draft t seeing keys 0 .. L_b - T + t and v_j = k_j[:512].
+ *   lse        : [B, T, H] fp32, natural-log log-sum-exp of the scaled scores.
+ *   workspace  : device scratch of workspace_bytes >= plan->workspace_bytes, 256-byte
+ *                aligned; may be NULL when plan->workspace_bytes == 0.  Its contents are
+ *                overwritten; calls that share one workspace must be stream-ordered.
+ * Enqueues the split-KV partial kernel and, when any request has more than one split,
+ * the LSE-merge combine kernel on `stream`.  No allocation, no host synchronisation.
+ * Errors: MLA_ERR_INVALID_ARG (null pointers, q_len/num_heads differ from the plan,
+ * misaligned pointers: q, kv_pages 16-byte, out 16-byte), MLA_ERR_WORKSPACE_TOO_SMALL,
+ * MLA_ERR_CUDA (tensor-map encoding or launch failure). */
+int mla_decode(const mla_decode_plan_t* plan, const void* q, const void* kv_pages,
+               const int32_t* page_table, const int32_t* seq_lens, int q_len, int num_heads,
+               float scale, float kv_scale, void* out, float* lse, void* workspace,
+               size_t workspace_bytes, void* stream);
+
+/* Ragged (no padding) causal MLA prefill on top of a cached prefix.
+ *   q             : [total_q, H, 192] bf16; request b's n_b new tokens are rows
+ *                   cu_seqlens_q[b] .. cu_seqlens_q[b+1]-1.
+ *   k             : [total_kv, H, 192] bf16; request b's p_b + n_b keys (prefix first) are
+ *                   rows cu_seqlens_kv[b] .. cu_seqlens_kv[b+1]-1.
+ *   v             : [total_kv, H, 128] bf16, same rows as k.
+ *   cu_seqlens_q, cu_seqlens_kv : [batch+1] int32 prefix sums (device).
+ *   prefix_lens   : [batch] int32 p_b (device); kv length must equal p_b + n_b.
+ *   max_seqlen_q  : host bound on n_b (sizes the grid).
+ *   total_q, total_kv : host row counts of q and k/v (bounds of the tensor maps).
+ *   out           : [total_q, H, 128] bf16; new token i of request b attends to keys
+ *                   0 .. p_b + i of its own request.
+ *   lse           : [total_q, H] fp32 natural-log log-sum-exp.
+ * Errors: MLA_ERR_INVALID_ARG, MLA_ERR_UNSUPPORTED (num_heads < 1 or > 256),
+ * MLA_ERR_CUDA. */
+int mla_prefill_varlen(const void* q, const void* k, const void* v, const int32_t* cu_seqlens_q,
+                       const int32_t* cu_seqlens_kv, const int32_t* prefix_lens, int batch,
+                       int num_heads, int max_seqlen_q, int total_q, int total_kv, float scale,
+                       void* out, float* lse, void* stream);
+
+/* Read and clear the current device's status word after synchronising `stream`.
+ * Returns MLA_OK, MLA_ERR_TIMEOUT or MLA_ERR_DEVICE_ARG (first recorded), or
+ * MLA_ERR_CUDA if the read itself fails.  This call synchronises: keep it off the hot
+ * path. */
+int mla_get_status(void* stream);
+
+/* Measurement hook: when start/stop are non-NULL cudaEvent_t handles, subsequent
+ * mla_decode calls made from the calling host thread record `start` immediately before
+ * and `stop` immediately after the split-KV partial kernel (on the call's stream), and
+ * mla_prefill_varlen records them around its kernel.  NULL, NULL turns recording off.
+ * The library does not own the events.  Returns MLA_OK. */
+int mla_set_profile_events(void* start_event, void* stop_event);
+
+/* Static, human-readable name of a status code. */
+const char* mla_status_string(int status);
+
+/* Library version as major*10000 + minor*100 + patch. */
+int mla_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MLA_GB300_MLA_H_ */

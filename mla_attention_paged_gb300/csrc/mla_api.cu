@@ -1,0 +1,307 @@
+// mla_api.cu -- host side of the libmla C ABI (include/mla.h): argument validation, the
+// memoised decode plan (split count + workspace size, computed at run time and cached as
+// the TokenSpeed talk "构建面向 Agentic 推理的下一代 LLM 推理引擎", section
+// "Kernel：让 MLA 真正跑满 GPU", describes), TMA tensor-map encoding and kernel launches.
+// No device memory is allocated here and no call synchronises the stream, except
+// mla_get_status which exists to read the device status word.
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+#include <unordered_map>
+#include <vector>
+
+#include "../../include/mla.h"
+#include "mla_internal.h"
+
+namespace mla {
+
+// Per-device status word written by the kernels (bit 0 timeout, bit 1 device argument).
+__device__ unsigned int g_status_word = 0;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+unsigned* status_ptr() {
+  static std::mutex mu;
+  static unsigned* ptrs[kMaxDevices] = {nullptr};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!ptrs[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return nullptr;
+    ptrs[dev] = static_cast<unsigned*>(p);
+  }
+  return ptrs[dev];
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = []() -> PFN_cuTensorMapEncodeTiled_v12000 {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return nullptr;
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  }();
+  return fn;
+}
+
+// Tiled tensor map with 128-byte swizzle.  dims/strides innermost first; strides in bytes
+// for dims 1..rank-1.
+bool make_map(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void* base, const uint64_t* dims,
+              const uint64_t* strides, const uint32_t* box) {
+  PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t d[5];
+  cuuint64_t s[4];
+  cuuint32_t bx[5];
+  cuuint32_t es[5];
+  for (int i = 0; i < rank; ++i) {
+    d[i] = dims[i];
+    bx[i] = box[i];
+    es[i] = 1;
+    if (i + 1 < rank) s[i] = strides[i];
+  }
+  CUresult r = fn(m, dt, static_cast<cuuint32_t>(rank), const_cast<void*>(base), d, s, bx, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+bool page_size_ok(int P) { return P == 8 || P == 16 || P == 32 || P == 64 || P == 128 || P == 256; }
+
+thread_local cudaEvent_t g_prof_start = nullptr;
+thread_local cudaEvent_t g_prof_stop = nullptr;
+
+// Inside stream capture an event must be recorded as an external node to be observable
+// when the graph runs.
+cudaError_t record_event(cudaEvent_t ev, cudaStream_t s) {
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  cudaError_t e = cudaStreamIsCapturing(s, &cs);
+  if (e != cudaSuccess) return e;
+  if (cs == cudaStreamCaptureStatusActive) return cudaEventRecordWithFlags(ev, s, cudaEventRecordExternal);
+  return cudaEventRecord(ev, s);
+}
+
+std::mutex g_plan_mu;
+std::unordered_map<std::string, mla_decode_plan_t> g_plan_cache;
+
+// Smallest keys-per-split chunk (whole 64-key tiles, at least 4 tiles when the request is
+// that long) for which the partial kernel needs no more CTAs than the GPU has SMs.
+int choose_chunk_tiles(const std::vector<int>& lens, int groups, int sms) {
+  int max_tiles = 1;
+  for (int L : lens) max_tiles = std::max(max_tiles, (L + kTileKeys - 1) / kTileKeys);
+  auto ctas = [&](int ct) {
+    long long n = 0;
+    for (int L : lens) n += ((L + kTileKeys - 1) / kTileKeys + ct - 1) / ct;
+    return n * groups;
+  };
+  int lo = std::min(4, max_tiles), hi = max_tiles;
+  if (ctas(hi) > sms) return hi;  // one split per request already exceeds one wave
+  while (lo < hi) {
+    int mid = (lo + hi) / 2;
+    if (ctas(mid) <= sms)
+      hi = mid;
+    else
+      lo = mid + 1;
+  }
+  return lo;
+}
+
+}  // namespace
+}  // namespace mla
+
+using namespace mla;
+
+extern "C" {
+
+int mla_version(void) { return 100; }
+
+const char* mla_status_string(int status) {
+  switch (status) {
+    case MLA_OK: return "MLA_OK";
+    case MLA_ERR_INVALID_ARG: return "MLA_ERR_INVALID_ARG";
+    case MLA_ERR_UNSUPPORTED: return "MLA_ERR_UNSUPPORTED";
+    case MLA_ERR_WORKSPACE_TOO_SMALL: return "MLA_ERR_WORKSPACE_TOO_SMALL";
+    case MLA_ERR_CUDA: return "MLA_ERR_CUDA";
+    case MLA_ERR_TIMEOUT: return "MLA_ERR_TIMEOUT";
+    case MLA_ERR_DEVICE_ARG: return "MLA_ERR_DEVICE_ARG";
+    default: return "MLA_ERR_UNKNOWN";
+  }
+}
+
+int mla_decode_plan(int batch, const int32_t* seq_lens_host, int q_len, int num_heads, int page_size,
+                    int max_pages_per_seq, int64_t num_pages, int kv_dtype, int num_sms,
+                    mla_decode_plan_t* plan_out) {
+  if (!seq_lens_host || !plan_out || batch < 1 || q_len < 1 || num_heads < 1 || max_pages_per_seq < 1 ||
+      num_pages < 1)
+    return MLA_ERR_INVALID_ARG;
+  if (kv_dtype != MLA_KV_BF16 && kv_dtype != MLA_KV_E4M3) return MLA_ERR_INVALID_ARG;
+  if (q_len > 8 || !page_size_ok(page_size) || q_len * num_heads > 1024) return MLA_ERR_UNSUPPORTED;
+  if (batch > 65535) return MLA_ERR_UNSUPPORTED;
+  std::vector<int> lens(seq_lens_host, seq_lens_host + batch);
+  int max_len = 0;
+  for (int L : lens) {
+    if (L < q_len || static_cast<int64_t>(L) > static_cast<int64_t>(max_pages_per_seq) * page_size)
+      return MLA_ERR_INVALID_ARG;
+    max_len = std::max(max_len, L);
+  }
+  if (num_sms <= 0) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return MLA_ERR_CUDA;
+    if (cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return MLA_ERR_CUDA;
+  }
+  std::string key;
+  key.reserve(64 + 4 * lens.size());
+  char head[160];
+  snprintf(head, sizeof head, "%d,%d,%d,%d,%d,%lld,%d,%d|", batch, q_len, num_heads, page_size, max_pages_per_seq,
+           static_cast<long long>(num_pages), kv_dtype, num_sms);
+  key += head;
+  key.append(reinterpret_cast<const char*>(lens.data()), lens.size() * sizeof(int));
+  {
+    std::lock_guard<std::mutex> lock(g_plan_mu);
+    auto it = g_plan_cache.find(key);
+    if (it != g_plan_cache.end()) {
+      *plan_out = it->second;
+      return MLA_OK;
+    }
+  }
+  mla_decode_plan_t pl;
+  memset(&pl, 0, sizeof pl);
+  pl.batch = batch;
+  pl.q_len = q_len;
+  pl.num_heads = num_heads;
+  pl.page_size = page_size;
+  pl.max_pages_per_seq = max_pages_per_seq;
+  pl.kv_dtype = kv_dtype;
+  pl.num_pages = num_pages;
+  pl.num_sms = num_sms;
+  pl.rows = q_len * num_heads;
+  pl.head_groups = (pl.rows + kGroupRows - 1) / kGroupRows;
+  const int ct = choose_chunk_tiles(lens, pl.head_groups, num_sms);
+  pl.chunk_tokens = ct * kTileKeys;
+  pl.max_seq_len = max_len;
+  pl.max_splits = (max_len + pl.chunk_tokens - 1) / pl.chunk_tokens;
+  if (pl.max_splits > 65535) return MLA_ERR_UNSUPPORTED;
+  if (pl.max_splits > 1) {
+    const size_t parts = static_cast<size_t>(batch) * pl.max_splits * pl.rows;
+    pl.workspace_bytes = 256 + parts * kValueDim * sizeof(float) + parts * sizeof(float);
+  } else {
+    pl.workspace_bytes = 0;
+  }
+  {
+    std::lock_guard<std::mutex> lock(g_plan_mu);
+    if (g_plan_cache.size() > 4096) g_plan_cache.clear();
+    g_plan_cache.emplace(key, pl);
+  }
+  *plan_out = pl;
+  return MLA_OK;
+}
+
+int mla_decode(const mla_decode_plan_t* plan, const void* q, const void* kv_pages, const int32_t* page_table,
+               const int32_t* seq_lens, int q_len, int num_heads, float scale, float kv_scale, void* out,
+               float* lse, void* workspace, size_t workspace_bytes, void* stream) {
+  if (!plan || !q || !kv_pages || !page_table || !seq_lens || !out || !lse) return MLA_ERR_INVALID_ARG;
+  if (q_len != plan->q_len || num_heads != plan->num_heads || plan->rows != q_len * num_heads)
+    return MLA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(kv_pages, 16) || !aligned(out, 16) || !aligned(lse, 4))
+    return MLA_ERR_INVALID_ARG;
+  if (!(scale > 0.f) || !(kv_scale > 0.f)) return MLA_ERR_INVALID_ARG;
+  if (plan->workspace_bytes > 0) {
+    if (!workspace) return MLA_ERR_INVALID_ARG;
+    if (workspace_bytes < plan->workspace_bytes) return MLA_ERR_WORKSPACE_TOO_SMALL;
+    if (!aligned(workspace, 256)) return MLA_ERR_INVALID_ARG;
+  }
+  if (plan->kv_dtype == MLA_KV_E4M3) return MLA_ERR_UNSUPPORTED;
+  unsigned* status = status_ptr();
+  if (!status) return MLA_ERR_CUDA;
+
+  const uint64_t row_bytes = kLatentDim * 2;
+  CUtensorMap tm_q, tm_kv;
+  {
+    const uint64_t dims[2] = {static_cast<uint64_t>(kLatentDim), static_cast<uint64_t>(plan->batch) * plan->rows};
+    const uint64_t strides[1] = {row_bytes};
+    const uint32_t box[2] = {64, static_cast<uint32_t>(kGroupRows)};
+    if (!make_map(&tm_q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, q, dims, strides, box)) return MLA_ERR_CUDA;
+  }
+  {
+    const uint64_t dims[2] = {static_cast<uint64_t>(kLatentDim),
+                              static_cast<uint64_t>(plan->num_pages) * plan->page_size};
+    const uint64_t strides[1] = {row_bytes};
+    const uint32_t box[2] = {64, static_cast<uint32_t>(std::min(plan->page_size, kTileKeys))};
+    if (!make_map(&tm_kv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kv_pages, dims, strides, box)) return MLA_ERR_CUDA;
+  }
+  DecodeParams p;
+  memset(&p, 0, sizeof p);
+  p.B = plan->batch;
+  p.T = q_len;
+  p.H = num_heads;
+  p.R = plan->rows;
+  p.page_size = plan->page_size;
+  p.max_pages = plan->max_pages_per_seq;
+  p.chunk = plan->chunk_tokens;
+  p.max_splits = plan->max_splits;
+  p.max_seq = plan->max_seq_len;
+  p.kv_fp8 = plan->kv_dtype == MLA_KV_E4M3;
+  p.scale_log2 = scale * 1.4426950408889634f * (p.kv_fp8 ? kv_scale : 1.f);
+  p.v_scale = p.kv_fp8 ? kv_scale : 1.f;
+  p.page_table = page_table;
+  p.seq_lens = seq_lens;
+  p.kv_pool = static_cast<const uint8_t*>(kv_pages);
+  p.out = static_cast<__nv_bfloat16*>(out);
+  p.lse = lse;
+  if (plan->max_splits > 1) {
+    const size_t parts = static_cast<size_t>(plan->batch) * plan->max_splits * plan->rows;
+    p.ws_o = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + 256);
+    p.ws_lse = p.ws_o + parts * kValueDim;
+  }
+  p.status = status;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (g_prof_start && record_event(g_prof_start, s) != cudaSuccess) return MLA_ERR_CUDA;
+  if (launch_decode_partial(p, tm_q, tm_kv, plan->head_groups, s) != cudaSuccess) return MLA_ERR_CUDA;
+  if (g_prof_stop && record_event(g_prof_stop, s) != cudaSuccess) return MLA_ERR_CUDA;
+  if (plan->max_splits > 1) {
+    if (launch_decode_combine(p, s) != cudaSuccess) return MLA_ERR_CUDA;
+  }
+  return MLA_OK;
+}
+
+int mla_prefill_varlen(const void* q, const void* k, const void* v, const int32_t* cu_seqlens_q,
+                       const int32_t* cu_seqlens_kv, const int32_t* prefix_lens, int batch, int num_heads,
+                       int max_seqlen_q, int total_q, int total_kv, float scale, void* out, float* lse,
+                       void* stream) {
+  (void)q; (void)k; (void)v; (void)cu_seqlens_q; (void)cu_seqlens_kv; (void)prefix_lens; (void)batch;
+  (void)num_heads; (void)max_seqlen_q; (void)total_q; (void)total_kv; (void)scale; (void)out; (void)lse;
+  (void)stream;
+  return MLA_ERR_UNSUPPORTED;
+}
+
+int mla_set_profile_events(void* start_event, void* stop_event) {
+  g_prof_start = static_cast<cudaEvent_t>(start_event);
+  g_prof_stop = static_cast<cudaEvent_t>(stop_event);
+  return MLA_OK;
+}
+
+int mla_get_status(void* stream) {
+  unsigned* status = status_ptr();
+  if (!status) return MLA_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  unsigned host = 0;
+  if (cudaMemcpyAsync(&host, status, sizeof host, cudaMemcpyDeviceToHost, s) != cudaSuccess) return MLA_ERR_CUDA;
+  if (cudaMemsetAsync(status, 0, sizeof host, s) != cudaSuccess) return MLA_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return MLA_ERR_CUDA;
+  if (host & kStatusTimeout) return MLA_ERR_TIMEOUT;
+  if (host & kStatusDeviceArg) return MLA_ERR_DEVICE_ARG;
+  return MLA_OK;
+}
+
+}  // extern "C"

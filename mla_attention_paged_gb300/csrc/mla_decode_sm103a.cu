@@ -1,0 +1,511 @@
+// mla_decode_sm103a.cu -- absorbed MLA decode over a paged latent KV cache, sm_103a.
+//
+// What it computes (per request b, draft t, head h; keys j = 0 .. L_b - T + t):
+//   out[b,t,h,:] = sum_j softmax_j(scale * q[b,t,h,:] . k_j) * k_j[:512]
+// where k_j is the 576-wide latent row j of request b, found through the page table.
+// TokenSpeed pages: "构建面向 Agentic 推理的下一代 LLM 推理引擎" (AICon talk), section
+// "Kernel：让 MLA 真正跑满 GPU" (latent state shared by all heads, fold factor, split-KV
+// partial + reduction stages, TMEM accumulators); launch-blog repost
+// "英偉達力薦，小團隊兩個月開源一款「光速級」智能體推理引擎", section "TokenSpeed 性能預覽"
+// (query-sequence axis folded into the head axis to fill the first matmul's M tile).
+//
+// Design on sm_103a (one CTA per (64-row group, split, request); one CTA per SM):
+//  * Fold: the T*H query rows of a request are one matrix with row m = t*H + h; a CTA
+//    takes 64 consecutive rows, so all heads and drafts share each latent tile load.
+//  * Producer warp: TMA (128-byte swizzled boxes of 64 columns) gathers one 64-key tile
+//    per stage from the pages named by the page table into a 2-stage ring (mbarriers).
+//  * MMA warp (one thread): BMM1  S[rows, keys]  = Q . K^T  (M=128, N=64, K=576;
+//    rows 64..127 of the M tile are don't-care) into TMEM, double-buffered;
+//    BMM2  O^T[dims, rows] += V^T . P^T  (M=128 per 128 value columns, N=rows, K=64
+//    keys) with V^T read MN-major from the same shared-memory tile as K.  O^T lives in
+//    TMEM for the whole split (256 columns); S takes 2 x 64 columns.
+//  * Softmax warps (2): one thread per folded row reads its 64 scores from TMEM, applies
+//    the causal/length mask, keeps a running max in the log2 domain with a lazy rescale
+//    (O is rescaled only when the max grows by more than 2^8), writes P (bf16) to
+//    shared memory as the K-major B operand of BMM2.
+//  * Epilogue (4 warps over the 128 TMEM lanes = value columns): normalise by the row
+//    sum and write either the final bf16 output (single split) or the fp32 partial and
+//    its log-sum-exp for the combine kernel.
+// Every wait is bounded; on expiry the CTA records a timeout in the status word, drains
+// its in-flight copies and MMAs, frees TMEM and returns.
+#include "mla_internal.h"
+#include "sm103a_ptx.cuh"
+
+namespace mla {
+namespace {
+
+constexpr int kDimBlocks = kLatentDim / 64;          // 9 blocks of 64 columns (128 bytes)
+constexpr int kBlockBytes = 64 * 128;                // 64 rows x 128 bytes, swizzled
+constexpr int kTileBytes = kDimBlocks * kBlockBytes; // 73728: one bf16 64-key latent tile
+constexpr int kStages = 2;
+constexpr int kThreads = 192;                        // warps 0-3 softmax/epilogue, 4 TMA, 5 MMA
+
+constexpr int kOffQ = 0;
+constexpr int kOffKV = kOffQ + kTileBytes;
+constexpr int kOffP = kOffKV + kStages * kTileBytes;
+constexpr int kOffCtrl = kOffP + kBlockBytes;
+
+struct DecodeCtrl {
+  uint64_t q_full;
+  uint64_t kv_full[kStages];
+  uint64_t kv_empty[kStages];
+  uint64_t s_full[2];
+  uint64_t s_free[2];
+  uint64_t p_full;
+  uint64_t o_done;
+  uint64_t mma_drain;
+  uint32_t tmem_base;
+  int abort_flag;
+  int rescale_flag[2];
+  float alpha[kGroupRows];
+  float row_scale[kGroupRows];
+};
+constexpr int kSmemBytes = kOffCtrl + 1024 + 1024;  // + control block + alignment slack
+static_assert(sizeof(DecodeCtrl) <= 1024, "control block");
+
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kTmemS = 256;   // S buffers at columns 256 and 320; O^T chunks at 0,64,128,192
+constexpr float kRescaleThreshold = 8.0f;  // log2 units
+
+__device__ __forceinline__ bool bar_or(int id, int nthreads, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 q, %1, 0;\n\t"
+      "bar.red.or.pred p, %2, %3, q;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(pred)), "r"(id), "r"(nthreads)
+      : "memory");
+  return r != 0;
+}
+
+// Bounded wait that ignores the abort flag: used only to drain work already in flight.
+__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
+  const unsigned long long t0 = global_timer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (global_timer_ns() - t0 > kWaitLimitNs) return;
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+decode_partial_bf16_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kv,
+                           const DecodeParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  DecodeCtrl* ctrl = reinterpret_cast<DecodeCtrl*>(smem + kOffCtrl);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int group = blockIdx.x;
+  const int split = blockIdx.y;
+  const int b = blockIdx.z;
+
+  const int L = p.seq_lens[b];
+  if (L < p.T || L > p.max_seq || L > p.max_pages * p.page_size) {
+    if (threadIdx.x == 0 && split == 0 && group == 0) atomicOr(p.status, kStatusDeviceArg);
+    return;
+  }
+  const int kv_start = split * p.chunk;
+  if (kv_start >= L) return;  // this request needs fewer splits
+  const int kv_end = min(L, kv_start + p.chunk);
+  const int ntiles = (kv_end - kv_start + kTileKeys - 1) / kTileKeys;
+  const int nsplit_b = (L + p.chunk - 1) / p.chunk;
+  const int row0 = group * kGroupRows;
+  const int nrows = min(kGroupRows, p.R - row0);
+  const int nq = (nrows + 15) & ~15;  // BMM2 N (multiple of 16)
+
+  if (threadIdx.x == 0) {
+    mbar_init(&ctrl->q_full, 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&ctrl->kv_full[s], 1);
+      mbar_init(&ctrl->kv_empty[s], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&ctrl->s_full[i], 1);
+      mbar_init(&ctrl->s_free[i], 64);
+    }
+    mbar_init(&ctrl->p_full, 128);
+    mbar_init(&ctrl->o_done, 1);
+    mbar_init(&ctrl->mma_drain, 1);
+    ctrl->abort_flag = 0;
+    ctrl->rescale_flag[0] = ctrl->rescale_flag[1] = 0;
+    fence_mbarrier_init();
+  }
+  if (warp == 5) {
+    tmem_alloc(&ctrl->tmem_base, kTmemCols);
+    tmem_relinquish();
+  }
+  if (warp == 4 && lane == 0) {
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_kv);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = ctrl->tmem_base;
+  volatile int* abort_flag = &ctrl->abort_flag;
+
+  if (warp == 4) {
+    // ------------------------------------------------------------------ TMA producer
+    const int P = p.page_size;
+    const int sub = P < kTileKeys ? kTileKeys / P : 1;  // pages per tile
+    const int box_rows = P < kTileKeys ? P : kTileKeys;
+    const int32_t* pt = p.page_table + static_cast<int64_t>(b) * p.max_pages;
+    const int first_page = kv_start / P;
+    const int last_page = (kv_end - 1) / P;
+    int batch_base = first_page;
+    int cur = (first_page + lane <= last_page) ? __ldg(pt + first_page + lane) : 0;
+    int nxt = (first_page + 32 + lane <= last_page) ? __ldg(pt + first_page + 32 + lane) : 0;
+    const uint64_t pol_kv = policy_evict_first();
+    const uint64_t pol_q = policy_evict_last();
+    if (lane == 0) {
+      mbar_arrive_expect_tx(&ctrl->q_full, kTileBytes);
+      for (int c = 0; c < kDimBlocks; ++c)
+        tma_load_2d(smem + kOffQ + c * kBlockBytes, &tm_q, &ctrl->q_full, c * 64, b * p.R + row0, pol_q);
+    }
+    int last_issued[kStages] = {-1, -1};
+    bool ok = true;
+    for (int j = 0; j < ntiles; ++j) {
+      const int s = j % kStages;
+      if (j >= kStages) {
+        bool w = true;
+        if (lane == 0) w = mbar_wait(&ctrl->kv_empty[s], ((j / kStages) - 1) & 1, abort_flag);
+        ok = __shfl_sync(0xffffffffu, w, 0);
+        if (!ok) break;
+      }
+      const int k0 = kv_start + j * kTileKeys;
+      const int pg0 = k0 / P;
+      const int tile_end = min(k0 + kTileKeys, L);
+      const int npg = (P < kTileKeys) ? ((tile_end - 1) / P - pg0 + 1) : 1;
+      uint8_t* stage = smem + kOffKV + s * kTileBytes;
+      int pids[8];
+#pragma unroll
+      for (int pp = 0; pp < 8; ++pp) {
+        int pi = pg0 + pp;
+        if (pp < sub) {
+          while (pi - batch_base >= 32) {  // advance the page-id window (warp-uniform)
+            batch_base += 32;
+            cur = nxt;
+            const int nb = batch_base + 32 + lane;
+            nxt = (nb <= last_page) ? __ldg(pt + nb) : 0;
+          }
+          pids[pp] = __shfl_sync(0xffffffffu, cur, (pi - batch_base) & 31);
+        } else {
+          pids[pp] = 0;
+        }
+      }
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&ctrl->kv_full[s], static_cast<uint32_t>(npg * box_rows * 128 * kDimBlocks));
+        for (int pp = 0; pp < npg; ++pp) {
+          const int y = pids[pp] * P + (P > kTileKeys ? (k0 % P) : 0);
+          for (int c = 0; c < kDimBlocks; ++c)
+            tma_load_2d(stage + c * kBlockBytes + pp * box_rows * 128, &tm_kv, &ctrl->kv_full[s], c * 64, y, pol_kv);
+        }
+      }
+      last_issued[s] = j;
+      __syncwarp();
+    }
+    if (!ok && lane == 0) {
+      // drain copies still in flight before the CTA exits
+      drain_wait(&ctrl->q_full, 0);
+      for (int s = 0; s < kStages; ++s)
+        if (last_issued[s] >= 0) drain_wait(&ctrl->kv_full[s], (last_issued[s] / kStages) & 1);
+    }
+  } else if (warp == 5) {
+    // ------------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc1 = make_idesc_bf16(128, 64, false, false);
+      const uint32_t idesc2 = make_idesc_bf16(128, nq, true, false);
+      const uint32_t q_base = smem_u32(smem + kOffQ);
+      const uint32_t p_base = smem_u32(smem + kOffP);
+      bool ok = mbar_wait(&ctrl->q_full, 0, abort_flag);
+      for (int j = 0; j <= ntiles && ok; ++j) {
+        if (j < ntiles) {
+          const int s = j % kStages, sb = j & 1;
+          ok = mbar_wait(&ctrl->kv_full[s], (j / kStages) & 1, abort_flag);
+          if (ok && j >= 2) ok = mbar_wait(&ctrl->s_free[sb], ((j - 2) >> 1) & 1, abort_flag);
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t kv_base = smem_u32(smem + kOffKV + s * kTileBytes);
+          const uint32_t d = tmem + kTmemS + sb * 64;
+#pragma unroll 1
+          for (int c = 0; c < kDimBlocks; ++c) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const uint64_t a = make_smem_desc(q_base + c * kBlockBytes + k * 32, 16, 1024);
+              const uint64_t bb = make_smem_desc(kv_base + c * kBlockBytes + k * 32, 16, 1024);
+              umma_bf16(d, a, bb, idesc1, (c | k) != 0);
+            }
+          }
+          umma_commit(&ctrl->s_full[sb]);
+        }
+        if (j >= 1) {
+          const int jj = j - 1, s = jj % kStages;
+          ok = mbar_wait(&ctrl->p_full, jj & 1, abort_flag);
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t kv_base = smem_u32(smem + kOffKV + s * kTileBytes);
+#pragma unroll
+          for (int qc = 0; qc < 4; ++qc) {
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+              // V^T: 128 value columns (two 64-column blocks, LBO apart) x 16 keys (two
+              // 8-key groups, SBO apart), MN-major.  P^T: rows x 16 keys, K-major.
+              const uint64_t a = make_smem_desc(kv_base + (2 * qc) * kBlockBytes + kk * 2048, kBlockBytes, 1024);
+              const uint64_t bb = make_smem_desc(p_base + kk * 32, 16, 1024);
+              umma_bf16(tmem + qc * 64, a, bb, idesc2, (jj > 0 || kk > 0) ? 1u : 0u);
+            }
+          }
+          umma_commit(&ctrl->o_done);
+          umma_commit(&ctrl->kv_empty[s]);
+        }
+      }
+      // every MMA issued so far completes before TMEM is released
+      umma_commit(&ctrl->mma_drain);
+      drain_wait(&ctrl->mma_drain, 0);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------------ softmax + epilogue (warps 0-3)
+    const bool is_sm = warp < 2;
+    const int r = warp * 32 + lane;  // folded row within the group (softmax warps)
+    const bool row_active = is_sm && r < nrows;
+    const int t = (row0 + r) / p.H;
+    const int lim_abs = L - p.T + t;  // last visible key of this row
+    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    float m_used = -INFINITY;
+    float l_sum = 0.f;
+    bool failed = false;
+
+    for (int j = 0; j < ntiles; ++j) {
+      const int sb = j & 1;
+      const int k0 = kv_start + j * kTileKeys;
+      bool fail = false;
+      bool need_rescale = false;
+      float alpha = 1.f;
+      uint32_t packed[32];
+      if (is_sm) {
+        fail = !mbar_wait(&ctrl->s_full[sb], (j >> 1) & 1, abort_flag);
+        fail = __any_sync(0xffffffffu, fail);
+        if (!fail) {
+          tc_fence_after();
+          uint32_t sr[64];
+          tmem_ld32(tmem + lane_base + kTmemS + sb * 64, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
+          tmem_ld32(tmem + lane_base + kTmemS + sb * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
+          tmem_ld_wait();
+          tc_fence_before();
+          mbar_arrive(&ctrl->s_free[sb]);
+          const int lim = row_active ? (min(kv_end - 1, lim_abs) - k0) : -1;  // keys i <= lim are valid
+          float x[64];
+          float mt = -INFINITY;
+#pragma unroll
+          for (int i = 0; i < 64; ++i) {
+            x[i] = __uint_as_float(sr[i]) * p.scale_log2;
+            if (i <= lim) mt = fmaxf(mt, x[i]);
+          }
+          if (m_used == -INFINITY) {
+            m_used = mt;  // first contributing tile: O^T column is still zero
+          } else if (mt > m_used + kRescaleThreshold) {
+            alpha = ex2_approx(m_used - mt);
+            need_rescale = true;
+            l_sum *= alpha;
+            m_used = mt;
+          }
+          const float msub = (m_used == -INFINITY) ? 0.f : m_used;
+#pragma unroll
+          for (int i = 0; i < 64; i += 2) {
+            const float p0 = (i <= lim) ? ex2_approx(x[i] - msub) : 0.f;
+            const float p1 = (i + 1 <= lim) ? ex2_approx(x[i + 1] - msub) : 0.f;
+            l_sum += p0 + p1;
+            packed[i >> 1] = pack_bf16x2(p0, p1);
+          }
+        }
+      }
+      if (!fail && j >= 1) {
+        fail = !mbar_wait(&ctrl->o_done, (j - 1) & 1, abort_flag);
+        fail = __any_sync(0xffffffffu, fail);
+      }
+      if (!fail && is_sm) {
+        // P row r (64 keys, 128 bytes) into the 128-byte-swizzled K-major block
+        const uint32_t row_addr = smem_u32(smem + kOffP) + r * 128;
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+          st_shared_v4(row_addr + ((c ^ (r & 7)) << 4), packed[4 * c], packed[4 * c + 1], packed[4 * c + 2],
+                       packed[4 * c + 3]);
+        ctrl->alpha[r] = alpha;
+        const bool any = __any_sync(0xffffffffu, need_rescale);
+        if (lane == 0) ctrl->rescale_flag[warp] = any ? 1 : 0;
+      }
+      fence_proxy_async_smem();
+      if (bar_or(1, 128, fail || (*abort_flag != 0))) {
+        failed = true;
+        break;
+      }
+      // zero value rows past the request's end in the last tile (stale or unloaded rows
+      // would otherwise meet P = 0 in BMM2 and could carry NaN/Inf bit patterns)
+      const int valid_rows = L - k0;
+      if (valid_rows < kTileKeys) {
+        uint8_t* stage = smem + kOffKV + (j % kStages) * kTileBytes;
+        const int nzero = (kTileKeys - valid_rows) * 8;  // 16-byte chunks per block
+        for (int idx = threadIdx.x; idx < nzero * 8; idx += 128) {
+          const int blk = idx / nzero;
+          const int rem = idx % nzero;
+          const int row = valid_rows + rem / 8;
+          const uint32_t a = smem_u32(stage + blk * kBlockBytes + row * 128 + (rem % 8) * 16);
+          st_shared_v4(a, 0u, 0u, 0u, 0u);
+        }
+        fence_proxy_async_smem();
+      }
+      if (ctrl->rescale_flag[0] | ctrl->rescale_flag[1]) {
+        // O^T[dim, row] *= alpha[row] for all 512 value columns; this thread owns TMEM lane
+        // (warp*32 + lane) of each 128-column chunk.
+        tc_fence_after();
+#pragma unroll 1
+        for (int qc = 0; qc < 4; ++qc) {
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            uint32_t v[32];
+            const uint32_t addr = tmem + lane_base + qc * 64 + h * 32;
+            tmem_ld32(addr, v);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * ctrl->alpha[h * 32 + i]);
+            tmem_st32(addr, v);
+          }
+        }
+        tmem_st_wait();
+      }
+      tc_fence_before();
+      mbar_arrive(&ctrl->p_full);
+    }
+
+    if (!failed) {
+      failed = !mbar_wait(&ctrl->o_done, (ntiles - 1) & 1, abort_flag);
+    }
+    if (bar_or(1, 128, failed || (*abort_flag != 0))) {
+      failed = true;
+    } else {
+      tc_fence_after();
+      const bool final_out = (nsplit_b == 1);
+      if (is_sm) {
+        const float lse2 = (l_sum > 0.f) ? (m_used + __log2f(l_sum)) : -INFINITY;
+        const float lse_nat = lse2 * 0.69314718055994530942f;
+        ctrl->row_scale[r] = (l_sum > 0.f) ? (p.v_scale / l_sum) : 0.f;
+        if (row_active) {
+          const int64_t grow = static_cast<int64_t>(b) * p.R + row0 + r;
+          if (final_out)
+            p.lse[grow] = lse_nat;
+          else
+            p.ws_lse[(static_cast<int64_t>(b) * p.max_splits + split) * p.R + row0 + r] = lse_nat;
+        }
+      }
+      named_bar_sync(1, 128);
+#pragma unroll 1
+      for (int qc = 0; qc < 4; ++qc) {
+        const int dim = qc * 128 + warp * 32 + lane;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          uint32_t v[32];
+          tmem_ld32(tmem + lane_base + qc * 64 + h * 32, v);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const int rr = h * 32 + i;
+            if (rr < nrows) {
+              const float val = __uint_as_float(v[i]) * ctrl->row_scale[rr];
+              if (final_out) {
+                p.out[(static_cast<int64_t>(b) * p.R + row0 + rr) * kValueDim + dim] = __float2bfloat16_rn(val);
+              } else {
+                p.ws_o[((static_cast<int64_t>(b) * p.max_splits + split) * p.R + row0 + rr) * kValueDim + dim] = val;
+              }
+            }
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (threadIdx.x == 0 && ctrl->abort_flag) atomicOr(p.status, kStatusTimeout);
+  if (warp == 5) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// --------------------------------------------------------------------------------------
+// Combine: out[b, row] = sum_s exp(lse_s - lse) * O_s,  lse = log sum_s exp(lse_s).
+// One warp per folded row, each lane owns 16 of the 512 value columns.
+// --------------------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) decode_combine_kernel(const DecodeParams p) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int row = blockIdx.x * 8 + warp;
+  const int b = blockIdx.y;
+  if (row >= p.R) return;
+  const int L = p.seq_lens[b];
+  if (L < p.T || L > p.max_seq) return;
+  const int ns = (L + p.chunk - 1) / p.chunk;
+  if (ns <= 1) return;
+  const float* lse_s = p.ws_lse + static_cast<int64_t>(b) * p.max_splits * p.R + row;
+  float mx = -INFINITY;
+  for (int s = lane; s < ns; s += 32) mx = fmaxf(mx, lse_s[static_cast<int64_t>(s) * p.R]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  float acc[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) acc[i] = 0.f;
+  float wsum = 0.f;
+  if (mx != -INFINITY) {
+    for (int s = 0; s < ns; ++s) {
+      const float w = __expf(lse_s[static_cast<int64_t>(s) * p.R] - mx);
+      wsum += w;
+      const float4* src = reinterpret_cast<const float4*>(
+          p.ws_o + ((static_cast<int64_t>(b) * p.max_splits + s) * p.R + row) * kValueDim + lane * 16);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float4 v = __ldg(src + i);
+        acc[4 * i + 0] += w * v.x;
+        acc[4 * i + 1] += w * v.y;
+        acc[4 * i + 2] += w * v.z;
+        acc[4 * i + 3] += w * v.w;
+      }
+    }
+  }
+  const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+  uint32_t pk[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) pk[i] = pack_bf16x2(acc[2 * i] * inv, acc[2 * i + 1] * inv);
+  uint4* dst = reinterpret_cast<uint4*>(p.out + (static_cast<int64_t>(b) * p.R + row) * kValueDim + lane * 16);
+  dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+  dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+  if (lane == 0) p.lse[static_cast<int64_t>(b) * p.R + row] = (wsum > 0.f) ? (mx + __logf(wsum)) : -INFINITY;
+}
+
+}  // namespace
+
+cudaError_t launch_decode_partial(const DecodeParams& p, const CUtensorMap& tm_q, const CUtensorMap& tm_kv,
+                                  int head_groups, cudaStream_t stream) {
+  static thread_local int configured_device = -1;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (configured_device != dev) {
+    e = cudaFuncSetAttribute(decode_partial_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e != cudaSuccess) return e;
+    configured_device = dev;
+  }
+  if (p.kv_fp8) return cudaErrorNotSupported;
+  dim3 grid(head_groups, p.max_splits, p.B);
+  decode_partial_bf16_kernel<<<grid, kThreads, kSmemBytes, stream>>>(tm_q, tm_kv, p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_decode_combine(const DecodeParams& p, cudaStream_t stream) {
+  dim3 grid((p.R + 7) / 8, p.B);
+  decode_combine_kernel<<<grid, 256, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace mla

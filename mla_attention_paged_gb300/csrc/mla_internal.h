@@ -1,0 +1,59 @@
+// mla_internal.h -- launch parameter blocks and launcher declarations shared by the host
+// API (mla_api.cu) and the kernel translation units.  Not part of the public ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace mla {
+
+constexpr int kLatentDim = 576;  // 512 latent + 64 rope columns
+constexpr int kValueDim = 512;   // value = first 512 latent columns
+constexpr int kTileKeys = 64;    // keys per decode tile
+constexpr int kGroupRows = 64;   // folded query rows per decode CTA
+
+// Device status word bits (OR-ed by kernels, read and cleared by mla_get_status).
+constexpr unsigned kStatusTimeout = 1u;
+constexpr unsigned kStatusDeviceArg = 2u;
+
+struct DecodeParams {
+  int B, T, H, R;               // R = T*H folded rows per request
+  int page_size, max_pages;     // page geometry and page_table row stride
+  int chunk, max_splits, max_seq;
+  int kv_fp8;                   // 0: bf16 pool, 1: e4m3 pool
+  float scale_log2;             // softmax scale * log2(e) (* kv_scale for e4m3)
+  float v_scale;                // 1, or kv_scale for e4m3 (applied in the epilogue)
+  const int32_t* page_table;
+  const int32_t* seq_lens;
+  const uint8_t* kv_pool;       // pool base (e4m3 path copies raw pages from here)
+  __nv_bfloat16* out;           // [B, T, H, 512]
+  float* lse;                   // [B, T, H]
+  float* ws_o;                  // [B, max_splits, R, 512] partial outputs (normalised)
+  float* ws_lse;                // [B, max_splits, R] partial log-sum-exp (natural log)
+  unsigned* status;             // device status word
+};
+
+struct PrefillParams {
+  int B, H, max_q_blocks;
+  float scale_log2;
+  const int32_t* cu_q;
+  const int32_t* cu_kv;
+  const int32_t* prefix_lens;
+  __nv_bfloat16* out;           // [total_q, H, 128]
+  float* lse;                   // [total_q, H]
+  int total_q;
+  unsigned* status;
+};
+
+// Decode: split-KV partial kernel (tensor maps over q and the latent pool).
+cudaError_t launch_decode_partial(const DecodeParams& p, const CUtensorMap& tm_q, const CUtensorMap& tm_kv,
+                                  int head_groups, cudaStream_t stream);
+// Decode: LSE-merge of the split partials for requests with more than one split.
+cudaError_t launch_decode_combine(const DecodeParams& p, cudaStream_t stream);
+// Prefill: ragged causal prefill with prefix offset.
+cudaError_t launch_prefill(const PrefillParams& p, const CUtensorMap& tm_q, const CUtensorMap& tm_k,
+                           const CUtensorMap& tm_v, cudaStream_t stream);
+
+}  // namespace mla

@@ -1,0 +1,170 @@
+"""GPU parity of mla_decode (through the C ABI) against the fp64 CPU oracle.
+
+Tolerances (bf16 output): max-abs 2e-2 and relative L2 5e-3 over the compared outputs,
+LSE within 1e-3 absolute; FP8 KV: max-abs 6e-2 against the oracle run on the same e4m3
+codes and scale.  Small cases are compared element by element over every output; the
+full-size workloads are compared on sampled rows the oracle computes one by one, in the
+same launch configuration the benchmark times.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from mla_attention_paged_gb300.inputs import DecodeWorkload, decode_workloads, make_decode_inputs
+
+pytestmark = pytest.mark.gpu
+
+MAX_ABS = 2e-2
+REL_L2 = 5e-3
+LSE_ABS = 1e-3
+MAX_ABS_FP8 = 6e-2
+
+
+@pytest.fixture(scope="module")
+def mla():
+    if not torch.cuda.is_available():
+        pytest.fail("GPU test collected on a machine without CUDA")
+    from mla_attention_paged_gb300 import build
+    build.build()
+    from mla_attention_paged_gb300 import mla as m
+    return m
+
+
+def run_gpu(mla, inp, num_sms=0, dev="cuda"):
+    wl = inp.wl
+    q = inp.q.to(dev)
+    pool = inp.kv_pool.to(dev)
+    pt = inp.page_table.to(dev)
+    sl = inp.seq_lens.to(dev)
+    kvd = mla.MLA_KV_E4M3 if pool.dtype == torch.uint8 else mla.MLA_KV_BF16
+    plan = mla.decode_plan(inp.seq_lens.cpu(), wl.q_len, wl.heads, wl.page_size, pt.shape[1], pool.shape[0],
+                           kvd, num_sms)
+    out, lse = mla.decode(plan, q, pool, pt, sl, inp.scale, inp.kv_scale)
+    torch.cuda.synchronize()
+    assert mla.get_status() == mla.MLA_OK
+    return out.float().cpu().numpy(), lse.cpu().numpy(), plan
+
+
+def check(out, lse, ref_out, ref_lse, fp8=False):
+    out = out.reshape(ref_out.shape)
+    lse = lse.reshape(ref_lse.shape)
+    assert np.isfinite(out).all() and np.isfinite(lse).all()
+    err = np.abs(out - ref_out)
+    assert err.max() <= (MAX_ABS_FP8 if fp8 else MAX_ABS), f"max-abs {err.max():.3e}"
+    rel = np.linalg.norm(out - ref_out) / max(np.linalg.norm(ref_out), 1e-30)
+    if not fp8:
+        assert rel <= REL_L2, f"rel-L2 {rel:.3e}"
+    else:
+        assert rel <= 2 * REL_L2, f"rel-L2 {rel:.3e}"
+    lerr = np.abs(lse - ref_lse).max()
+    assert lerr <= LSE_ABS, f"lse abs {lerr:.3e}"
+
+
+def _full_check(mla, oracle_mod, wl, num_sms=0):
+    inp = make_decode_inputs(wl, "cpu")
+    out, lse, plan = run_gpu(mla, inp, num_sms)
+    ref_out, ref_lse = oracle_mod.mla_decode(inp.q, inp.kv_pool, inp.page_table, inp.seq_lens, inp.scale,
+                                             kv_scale=inp.kv_scale)
+    check(out, lse, ref_out, ref_lse, fp8=(wl.kv_dtype == "e4m3"))
+    return out, lse, plan
+
+
+# ------------------------------------------------------------------------------------
+# small cases, every output compared
+# ------------------------------------------------------------------------------------
+SMALL = [
+    # name, B, T, H, lens, page, kv
+    ("one_key", 1, 1, 16, [1], 64, "bf16"),
+    ("ragged_tails", 6, 1, 16, [1, 63, 64, 65, 127, 200], 64, "bf16"),
+    ("drafts4", 3, 4, 16, [4, 70, 333], 64, "bf16"),
+    ("drafts2_h8", 2, 2, 8, [129, 1000], 64, "bf16"),
+    ("rows_not_mult16", 2, 3, 5, [90, 257], 64, "bf16"),
+    ("two_groups", 2, 3, 40, [300, 77], 64, "bf16"),
+    ("h128", 2, 2, 128, [520, 1999], 64, "bf16"),
+    ("page8", 2, 4, 16, [45, 300], 8, "bf16"),
+    ("page16", 2, 2, 16, [500, 17], 16, "bf16"),
+    ("page32", 1, 4, 16, [1025], 32, "bf16"),
+    ("page128", 2, 1, 16, [700, 129], 128, "bf16"),
+    ("page256", 1, 4, 16, [2000], 256, "bf16"),
+    ("long_single", 1, 1, 16, [20000], 64, "bf16"),
+]
+
+
+@pytest.mark.parametrize("name,B,T,H,lens,P,kv", SMALL, ids=[c[0] for c in SMALL])
+@pytest.mark.parametrize("peaked", [False, True], ids=["plain", "peaked"])
+def test_decode_small(mla, oracle_mod, name, B, T, H, lens, P, kv, peaked):
+    wl = DecodeWorkload(name, B, T, H, lens, page_size=P, kv_dtype=kv, seed=100 + len(name), peaked=peaked,
+                        extra_pages=2)
+    _full_check(mla, oracle_mod, wl)
+
+
+@pytest.mark.parametrize("num_sms", [1, 3, 16, 152, 100000])
+def test_decode_split_counts_agree(mla, oracle_mod, num_sms):
+    """Different split counts (one split per request up to the minimum chunk) give the
+    oracle's result; the LSE merge of the partials is exercised whenever splits > 1."""
+    wl = DecodeWorkload("splits", 3, 4, 16, [3000, 65, 9000], seed=77, peaked=True)
+    _, _, plan = _full_check(mla, oracle_mod, wl, num_sms=num_sms)
+    if num_sms >= 152:
+        assert plan.max_splits > 1
+
+
+def test_decode_page_shuffle_invariance_bitwise(mla):
+    wl = DecodeWorkload("shuffle", 2, 4, 16, [1500, 777], seed=5, extra_pages=7)
+    inp = make_decode_inputs(wl, "cpu")
+    out1, lse1, _ = run_gpu(mla, inp)
+    n = inp.kv_pool.shape[0]
+    perm = torch.randperm(n, generator=torch.Generator().manual_seed(3))
+    pool2 = torch.empty_like(inp.kv_pool)
+    pool2[perm] = inp.kv_pool
+    inp.kv_pool = pool2
+    inp.page_table = perm[inp.page_table.long()].to(torch.int32)
+    out2, lse2, _ = run_gpu(mla, inp)
+    np.testing.assert_array_equal(out1, out2)
+    np.testing.assert_array_equal(lse1, lse2)
+
+
+def test_decode_fold_neutrality(mla):
+    """T drafts folded into one launch equal T single-token launches whose cache ends at
+    each draft's own position."""
+    wl = DecodeWorkload("fold", 2, 4, 16, [700, 1300], seed=9)
+    inp = make_decode_inputs(wl, "cpu")
+    out, lse, _ = run_gpu(mla, inp)
+    out = out.reshape(2, 4, 16, 512)
+    for t in range(4):
+        w1 = DecodeWorkload("fold1", 2, 1, 16, [700 - 3 + t, 1300 - 3 + t], seed=9)
+        one = make_decode_inputs(w1, "cpu")
+        one.q = inp.q[:, t:t + 1].contiguous()
+        one.kv_pool, one.page_table = inp.kv_pool, inp.page_table
+        o1, l1, _ = run_gpu(mla, one)
+        err = np.abs(o1.reshape(2, 1, 16, 512)[:, 0] - out[:, t]).max()
+        assert err <= MAX_ABS / 4
+
+
+# ------------------------------------------------------------------------------------
+# full-size workloads, sampled rows
+# ------------------------------------------------------------------------------------
+def _sample_rows(wl, per_request=8, seed=0):
+    g = np.random.default_rng(seed)
+    rows = []
+    for b in range(wl.batch):
+        picks = {(0, 0), (wl.q_len - 1, wl.heads - 1)}
+        while len(picks) < per_request:
+            picks.add((int(g.integers(wl.q_len)), int(g.integers(wl.heads))))
+        for t, h in sorted(picks):
+            rows.append((b * wl.q_len + t) * wl.heads + h)
+    return rows
+
+
+@pytest.mark.parametrize("name", list(decode_workloads().keys()))
+def test_decode_full_size_sampled(mla, oracle_mod, name):
+    wl = decode_workloads()[name]
+    inp = make_decode_inputs(wl, "cuda")
+    out, lse, plan = run_gpu(mla, inp)
+    rows = _sample_rows(wl, per_request=16 if wl.batch <= 4 else 6)
+    ref_out, ref_lse = oracle_mod.mla_decode(inp.q.cpu(), inp.kv_pool.cpu(), inp.page_table.cpu(),
+                                             inp.seq_lens.cpu(), inp.scale, kv_scale=inp.kv_scale, rows=rows)
+    check(out.reshape(-1, 512)[rows], lse.reshape(-1)[rows], ref_out, ref_lse, fp8=(wl.kv_dtype == "e4m3"))
+    # every output finite, including rows not sampled
+    assert np.isfinite(out).all() and np.isfinite(lse).all()

@@ -193,7 +193,13 @@ def run_reference(args, ws, rank):
     inp = make_decode_inputs(wl, "cpu")
     rows_total = wl.batch * wl.q_len * wl.heads
     rng = np.random.default_rng(1)
-    rows_per_step = 4
+    # size each step's row sample so that warm-up + K steps take about a minute
+    t0 = time.perf_counter()
+    oracle.mla_decode(inp.q, inp.kv_pool, inp.page_table, inp.seq_lens, inp.scale, rows=[0])
+    per_row = max(time.perf_counter() - t0, 1e-4)
+    threads = oracle.num_threads()
+    budget = 60.0 / max(1, args.steps + args.warmup)
+    rows_per_step = int(max(1, min(threads, rows_total, budget / per_row * threads)))
     for _ in range(args.warmup):
         oracle.mla_decode(inp.q, inp.kv_pool, inp.page_table, inp.seq_lens, inp.scale,
                           rows=rng.choice(rows_total, rows_per_step, replace=False))
@@ -304,7 +310,7 @@ def main():
     ms_max = _max_over_ranks(ms, ws, dev)
     total_bytes = _sum_over_ranks(kv_bytes * args.steps, ws, dev)
     value = total_bytes / (ms_max / 1e3) / 1e9
-    part_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    part_ms = statistics.mean(mla.profile_elapsed_ms(a, b) for a, b in ev)
     peaks = _peaks()
     achieved = alg_bytes / (part_ms / 1e3) / 1e9
     traffic = _traffic_record("mla_decode_sm103a.cu")

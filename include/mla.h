@@ -153,6 +153,11 @@ int mla_get_status(void* stream);
  * The library does not own the events.  Returns MLA_OK. */
 int mla_set_profile_events(void* start_event, void* stop_event);
 
+/* Elapsed milliseconds between two events recorded through the hook above (including
+ * event nodes replayed from a captured CUDA graph).  Returns MLA_ERR_CUDA if either event
+ * has not completed. */
+int mla_profile_elapsed_ms(void* start_event, void* stop_event, float* ms_out);
+
 /* Static, human-readable name of a status code. */
 const char* mla_status_string(int status);
 

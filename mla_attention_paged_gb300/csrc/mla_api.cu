@@ -279,15 +279,67 @@ int mla_prefill_varlen(const void* q, const void* k, const void* v, const int32_
                        const int32_t* cu_seqlens_kv, const int32_t* prefix_lens, int batch, int num_heads,
                        int max_seqlen_q, int total_q, int total_kv, float scale, void* out, float* lse,
                        void* stream) {
-  (void)q; (void)k; (void)v; (void)cu_seqlens_q; (void)cu_seqlens_kv; (void)prefix_lens; (void)batch;
-  (void)num_heads; (void)max_seqlen_q; (void)total_q; (void)total_kv; (void)scale; (void)out; (void)lse;
-  (void)stream;
-  return MLA_ERR_UNSUPPORTED;
+  if (!q || !k || !v || !cu_seqlens_q || !cu_seqlens_kv || !prefix_lens || !out || !lse) return MLA_ERR_INVALID_ARG;
+  if (batch < 1 || batch > 65535 || max_seqlen_q < 0 || total_q < 0 || total_kv < 0) return MLA_ERR_INVALID_ARG;
+  if (num_heads < 1 || num_heads > 256) return MLA_ERR_UNSUPPORTED;
+  if (!(scale > 0.f)) return MLA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16) || !aligned(lse, 4))
+    return MLA_ERR_INVALID_ARG;
+  if (total_q == 0 || max_seqlen_q == 0) return MLA_OK;
+  if (total_kv < 1) return MLA_ERR_INVALID_ARG;
+  unsigned* status = status_ptr();
+  if (!status) return MLA_ERR_CUDA;
+  const uint64_t H = static_cast<uint64_t>(num_heads);
+  CUtensorMap tm_q, tm_k, tm_v;
+  {
+    const uint64_t dims[3] = {192, H, static_cast<uint64_t>(total_q)};
+    const uint64_t strides[2] = {192 * 2, H * 192 * 2};
+    const uint32_t box[3] = {64, 1, 128};
+    if (!make_map(&tm_q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, q, dims, strides, box)) return MLA_ERR_CUDA;
+  }
+  {
+    const uint64_t dims[3] = {192, H, static_cast<uint64_t>(total_kv)};
+    const uint64_t strides[2] = {192 * 2, H * 192 * 2};
+    const uint32_t box[3] = {64, 1, 64};
+    if (!make_map(&tm_k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, k, dims, strides, box)) return MLA_ERR_CUDA;
+  }
+  {
+    const uint64_t dims[3] = {128, H, static_cast<uint64_t>(total_kv)};
+    const uint64_t strides[2] = {128 * 2, H * 128 * 2};
+    const uint32_t box[3] = {64, 1, 64};
+    if (!make_map(&tm_v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, v, dims, strides, box)) return MLA_ERR_CUDA;
+  }
+  PrefillParams p;
+  memset(&p, 0, sizeof p);
+  p.B = batch;
+  p.H = num_heads;
+  p.max_q_blocks = (max_seqlen_q + 127) / 128;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.cu_q = cu_seqlens_q;
+  p.cu_kv = cu_seqlens_kv;
+  p.prefix_lens = prefix_lens;
+  p.out = static_cast<__nv_bfloat16*>(out);
+  p.lse = lse;
+  p.total_q = total_q;
+  p.status = status;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (g_prof_start && record_event(g_prof_start, s) != cudaSuccess) return MLA_ERR_CUDA;
+  if (launch_prefill(p, tm_q, tm_k, tm_v, s) != cudaSuccess) return MLA_ERR_CUDA;
+  if (g_prof_stop && record_event(g_prof_stop, s) != cudaSuccess) return MLA_ERR_CUDA;
+  return MLA_OK;
 }
 
 int mla_set_profile_events(void* start_event, void* stop_event) {
   g_prof_start = static_cast<cudaEvent_t>(start_event);
   g_prof_stop = static_cast<cudaEvent_t>(stop_event);
+  return MLA_OK;
+}
+
+int mla_profile_elapsed_ms(void* start_event, void* stop_event, float* ms_out) {
+  if (!start_event || !stop_event || !ms_out) return MLA_ERR_INVALID_ARG;
+  if (cudaEventElapsedTime(ms_out, static_cast<cudaEvent_t>(start_event), static_cast<cudaEvent_t>(stop_event)) !=
+      cudaSuccess)
+    return MLA_ERR_CUDA;
   return MLA_OK;
 }
 

@@ -1,11 +1,373 @@
-// mla_prefill_sm103a.cu -- ragged causal MLA prefill with a cached-prefix offset (sm_103a).
+// mla_prefill_sm103a.cu -- ragged (no padding) causal MLA prefill on top of a cached
+// prefix, sm_103a.
+//
+// What it computes: request b has p_b cached prefix tokens followed by n_b new tokens; for
+// new token i and head h,
+//   out[i,h,:] = sum_{j <= p_b + i} softmax_j(scale * q[i,h,:] . k[j,h,:]) * v[j,h,:]
+// with q/k 192 wide (128 no-rope + 64 rope) and v 128 wide.  TokenSpeed pages:
+// "构建面向 Agentic 推理的下一代 LLM 推理引擎" (AICon talk), section "Kernel：让 MLA 真正跑满
+// GPU", last paragraph (agent prefill hits a cached prefix >90% of the time and appends a
+// few hundred tokens, so Q and KV lengths differ and the batch is variable-length without
+// padding); launch-blog repost "英偉達力薦，小團隊兩個月開源一款「光速級」智能體推理引擎",
+// section "TokenSpeed 性能預覽" (prefill with a long prefix KV cache, tuned softmax).
+//
+// Design on sm_103a (one CTA per (128-row query block, head, request), one CTA per SM):
+//  * Producer warp: TMA (128-byte swizzled, 3-D maps over [rows, heads, columns]) loads the
+//    query block once and streams 64-key K (192 wide) and V (128 wide) tiles of the same
+//    head through a 3-stage mbarrier ring.
+//  * MMA warp (one thread): S = Q . K^T (M=128 rows, N=64 keys, K=192) into a double-
+//    buffered TMEM S; O += P . V (M=128, N=128, K=64; V read MN-major) into TMEM O.
+//  * Softmax warps (4, one thread per query row = TMEM lane): causal mask offset by the
+//    prefix only on tiles that cross the diagonal, running max in the log2 domain with a
+//    lazy rescale of the thread's own O row (only when the max grows by more than 2^8),
+//    exp2 on the MUFU unit, P (bf16) to shared memory as the K-major A operand.
+//  * Epilogue: O / l to bf16 and the natural-log LSE, straight from TMEM.
+// Every wait is bounded; on expiry the CTA records a timeout in the status word, drains
+// its in-flight copies and MMAs, frees TMEM and returns.
 #include "mla_internal.h"
 #include "sm103a_ptx.cuh"
 
 namespace mla {
+namespace {
+
+constexpr int kDqk = 192;
+constexpr int kDv = 128;
+constexpr int kBM = 128;     // query rows per CTA
+constexpr int kBN = 64;      // keys per tile
+constexpr int kStages = 3;
+constexpr int kThreads = 192;
+
+constexpr int kQBlockBytes = kBM * 128;                // 16 KB per 64-column block
+constexpr int kQBytes = (kDqk / 64) * kQBlockBytes;    // 48 KB
+constexpr int kKVBlockBytes = kBN * 128;               // 8 KB
+constexpr int kKBytes = (kDqk / 64) * kKVBlockBytes;   // 24 KB
+constexpr int kVBytes = (kDv / 64) * kKVBlockBytes;    // 16 KB
+constexpr int kStageBytes = kKBytes + kVBytes;         // 40 KB
+constexpr int kPBytes = kBM * 128;                     // 16 KB: 128 rows x 64 keys bf16
+
+constexpr int kOffQ = 0;
+constexpr int kOffKV = kOffQ + kQBytes;
+constexpr int kOffP = kOffKV + kStages * kStageBytes;
+constexpr int kOffCtrl = kOffP + kPBytes;
+
+struct PrefillCtrl {
+  uint64_t q_full;
+  uint64_t kv_full[kStages];
+  uint64_t kv_empty[kStages];
+  uint64_t s_full[2];
+  uint64_t s_free[2];
+  uint64_t p_full;
+  uint64_t o_done;
+  uint64_t mma_drain;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+constexpr int kSmemBytes = kOffCtrl + 1024 + 1024;
+static_assert(sizeof(PrefillCtrl) <= 1024, "control block");
+
+constexpr uint32_t kTmemCols = 256;  // O at 0..127, S buffers at 128 and 192
+constexpr uint32_t kTmemO = 0;
+constexpr uint32_t kTmemS = 128;
+constexpr float kRescaleThreshold = 8.0f;
+
+__device__ __forceinline__ bool bar_or(int id, int nthreads, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 q, %1, 0;\n\t"
+      "bar.red.or.pred p, %2, %3, q;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(pred)), "r"(id), "r"(nthreads)
+      : "memory");
+  return r != 0;
+}
+
+__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
+  const unsigned long long t0 = global_timer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (global_timer_ns() - t0 > kWaitLimitNs) return;
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+               const __grid_constant__ CUtensorMap tm_v, const PrefillParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  PrefillCtrl* ctrl = reinterpret_cast<PrefillCtrl*>(smem + kOffCtrl);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int qb = blockIdx.x;
+  const int h = blockIdx.y;
+  const int b = blockIdx.z;
+
+  const int q_start = p.cu_q[b];
+  const int n_b = p.cu_q[b + 1] - q_start;
+  const int kv_start = p.cu_kv[b];
+  const int kv_total = p.cu_kv[b + 1] - kv_start;
+  const int pre = p.prefix_lens[b];
+  if (n_b < 0 || pre < 0 || kv_total != pre + n_b) {
+    if (threadIdx.x == 0 && qb == 0 && h == 0) atomicOr(p.status, kStatusDeviceArg);
+    return;
+  }
+  const int row_begin = qb * kBM;
+  if (row_begin >= n_b) return;
+  const int rows = min(kBM, n_b - row_begin);
+  const int kv_len = pre + row_begin + rows;  // keys any row of this block can see
+  const int ntiles = (kv_len + kBN - 1) / kBN;
+  const int diag_tile = (pre + row_begin) / kBN;  // first tile that may need the causal mask
+
+  if (threadIdx.x == 0) {
+    mbar_init(&ctrl->q_full, 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&ctrl->kv_full[s], 1);
+      mbar_init(&ctrl->kv_empty[s], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&ctrl->s_full[i], 1);
+      mbar_init(&ctrl->s_free[i], 128);
+    }
+    mbar_init(&ctrl->p_full, 128);
+    mbar_init(&ctrl->o_done, 1);
+    mbar_init(&ctrl->mma_drain, 1);
+    ctrl->abort_flag = 0;
+    fence_mbarrier_init();
+  }
+  if (warp == 5) {
+    tmem_alloc(&ctrl->tmem_base, kTmemCols);
+    tmem_relinquish();
+  }
+  if (warp == 4 && lane == 0) {
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_v);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = ctrl->tmem_base;
+  volatile int* abort_flag = &ctrl->abort_flag;
+
+  if (warp == 4) {
+    // ------------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      const uint64_t pol_q = policy_evict_first();
+      const uint64_t pol_kv = policy_evict_last();  // re-read by the other query blocks of this head
+      mbar_arrive_expect_tx(&ctrl->q_full, kQBytes);
+      for (int c = 0; c < kDqk / 64; ++c)
+        tma_load_3d(smem + kOffQ + c * kQBlockBytes, &tm_q, &ctrl->q_full, c * 64, h, q_start + row_begin, pol_q);
+      int last_issued[kStages] = {-1, -1, -1};
+      bool ok = true;
+      for (int j = 0; j < ntiles; ++j) {
+        const int s = j % kStages;
+        if (j >= kStages) {
+          ok = mbar_wait(&ctrl->kv_empty[s], ((j / kStages) - 1) & 1, abort_flag);
+          if (!ok) break;
+        }
+        uint8_t* st = smem + kOffKV + s * kStageBytes;
+        const int row = kv_start + j * kBN;
+        mbar_arrive_expect_tx(&ctrl->kv_full[s], kStageBytes);
+        for (int c = 0; c < kDqk / 64; ++c)
+          tma_load_3d(st + c * kKVBlockBytes, &tm_k, &ctrl->kv_full[s], c * 64, h, row, pol_kv);
+        for (int c = 0; c < kDv / 64; ++c)
+          tma_load_3d(st + kKBytes + c * kKVBlockBytes, &tm_v, &ctrl->kv_full[s], c * 64, h, row, pol_kv);
+        last_issued[s] = j;
+      }
+      if (!ok) {
+        drain_wait(&ctrl->q_full, 0);
+        for (int s = 0; s < kStages; ++s)
+          if (last_issued[s] >= 0) drain_wait(&ctrl->kv_full[s], (last_issued[s] / kStages) & 1);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 5) {
+    // ------------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc1 = make_idesc_bf16(kBM, kBN, false, false);
+      const uint32_t idesc2 = make_idesc_bf16(kBM, kDv, false, true);
+      const uint32_t q_base = smem_u32(smem + kOffQ);
+      const uint32_t p_base = smem_u32(smem + kOffP);
+      bool ok = mbar_wait(&ctrl->q_full, 0, abort_flag);
+      for (int j = 0; j <= ntiles && ok; ++j) {
+        if (j < ntiles) {
+          const int s = j % kStages, sb = j & 1;
+          ok = mbar_wait(&ctrl->kv_full[s], (j / kStages) & 1, abort_flag);
+          if (ok && j >= 2) ok = mbar_wait(&ctrl->s_free[sb], ((j - 2) >> 1) & 1, abort_flag);
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t k_base = smem_u32(smem + kOffKV + s * kStageBytes);
+#pragma unroll
+          for (int c = 0; c < kDqk / 64; ++c) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const uint64_t a = make_smem_desc(q_base + c * kQBlockBytes + k * 32, 16, 1024);
+              const uint64_t bb = make_smem_desc(k_base + c * kKVBlockBytes + k * 32, 16, 1024);
+              umma_bf16(tmem + kTmemS + sb * 64, a, bb, idesc1, (c | k) != 0);
+            }
+          }
+          umma_commit(&ctrl->s_full[sb]);
+        }
+        if (j >= 1) {
+          const int jj = j - 1, s = jj % kStages;
+          ok = mbar_wait(&ctrl->p_full, jj & 1, abort_flag);
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t v_base = smem_u32(smem + kOffKV + s * kStageBytes + kKBytes);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            // P: 128 rows x 16 keys, K-major.  V: 16 keys (two 8-key groups, SBO apart) x 128
+            // value columns (two 64-column blocks, LBO apart), MN-major.
+            const uint64_t a = make_smem_desc(p_base + kk * 32, 16, 1024);
+            const uint64_t bb = make_smem_desc(v_base + kk * 2048, kKVBlockBytes, 1024);
+            umma_bf16(tmem + kTmemO, a, bb, idesc2, (jj > 0 || kk > 0) ? 1u : 0u);
+          }
+          umma_commit(&ctrl->o_done);
+          umma_commit(&ctrl->kv_empty[s]);
+        }
+      }
+      umma_commit(&ctrl->mma_drain);
+      drain_wait(&ctrl->mma_drain, 0);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------------ softmax + epilogue (warps 0-3)
+    const int r = warp * 32 + lane;          // query row within the block = TMEM lane
+    const bool row_active = r < rows;
+    const int vis_last = pre + row_begin + r;  // last visible key of this row
+    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    float m_used = -INFINITY;
+    float l_sum = 0.f;
+    bool failed = false;
+    for (int j = 0; j < ntiles; ++j) {
+      const int sb = j & 1;
+      const int k0 = j * kBN;
+      bool fail = !mbar_wait(&ctrl->s_full[sb], (j >> 1) & 1, abort_flag);
+      fail = __any_sync(0xffffffffu, fail);
+      uint32_t packed[32];
+      bool need_rescale = false;
+      float alpha = 1.f;
+      if (!fail) {
+        tc_fence_after();
+        uint32_t sr[64];
+        tmem_ld32(tmem + lane_base + kTmemS + sb * 64, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
+        tmem_ld32(tmem + lane_base + kTmemS + sb * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
+        tmem_ld_wait();
+        tc_fence_before();
+        mbar_arrive(&ctrl->s_free[sb]);
+        const int lim = (j >= diag_tile) ? (row_active ? vis_last - k0 : -1) : (row_active ? kBN - 1 : -1);
+        float x[64];
+        float mt = -INFINITY;
+#pragma unroll
+        for (int i = 0; i < 64; ++i) {
+          x[i] = __uint_as_float(sr[i]) * p.scale_log2;
+          if (i <= lim) mt = fmaxf(mt, x[i]);
+        }
+        if (m_used == -INFINITY) {
+          m_used = mt;
+        } else if (mt > m_used + kRescaleThreshold) {
+          alpha = ex2_approx(m_used - mt);
+          need_rescale = true;
+          l_sum *= alpha;
+          m_used = mt;
+        }
+        const float msub = (m_used == -INFINITY) ? 0.f : m_used;
+#pragma unroll
+        for (int i = 0; i < 64; i += 2) {
+          const float p0 = (i <= lim) ? ex2_approx(x[i] - msub) : 0.f;
+          const float p1 = (i + 1 <= lim) ? ex2_approx(x[i + 1] - msub) : 0.f;
+          l_sum += p0 + p1;
+          packed[i >> 1] = pack_bf16x2(p0, p1);
+        }
+      }
+      if (!fail && j >= 1) {
+        fail = !mbar_wait(&ctrl->o_done, (j - 1) & 1, abort_flag);
+        fail = __any_sync(0xffffffffu, fail);
+      }
+      if (!fail) {
+        const uint32_t row_addr = smem_u32(smem + kOffP) + r * 128;
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+          st_shared_v4(row_addr + ((c ^ (r & 7)) << 4), packed[4 * c], packed[4 * c + 1], packed[4 * c + 2],
+                       packed[4 * c + 3]);
+        if (__any_sync(0xffffffffu, need_rescale) && j >= 1) {
+          // rescale this thread's own O row (TMEM lane r, 128 columns)
+          tc_fence_after();
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            uint32_t v[32];
+            tmem_ld32(tmem + lane_base + kTmemO + c * 32, v);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
+            tmem_st32(tmem + lane_base + kTmemO + c * 32, v);
+          }
+          tmem_st_wait();
+        }
+      }
+      fence_proxy_async_smem();
+      if (bar_or(1, 128, fail || (*abort_flag != 0))) {
+        failed = true;
+        break;
+      }
+      tc_fence_before();
+      mbar_arrive(&ctrl->p_full);
+    }
+    if (!failed) failed = !mbar_wait(&ctrl->o_done, (ntiles - 1) & 1, abort_flag);
+    if (!bar_or(1, 128, failed || (*abort_flag != 0))) {
+      tc_fence_after();
+      const float inv = (l_sum > 0.f) ? 1.f / l_sum : 0.f;
+      const int64_t tok = static_cast<int64_t>(q_start) + row_begin + r;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t v[32];
+        tmem_ld32(tmem + lane_base + kTmemO + c * 32, v);
+        tmem_ld_wait();
+        if (row_active) {
+          uint4* dst = reinterpret_cast<uint4*>(p.out + (tok * p.H + h) * kDv + c * 32);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            dst[i] = make_uint4(pack_bf16x2(__uint_as_float(v[8 * i + 0]) * inv, __uint_as_float(v[8 * i + 1]) * inv),
+                                pack_bf16x2(__uint_as_float(v[8 * i + 2]) * inv, __uint_as_float(v[8 * i + 3]) * inv),
+                                pack_bf16x2(__uint_as_float(v[8 * i + 4]) * inv, __uint_as_float(v[8 * i + 5]) * inv),
+                                pack_bf16x2(__uint_as_float(v[8 * i + 6]) * inv, __uint_as_float(v[8 * i + 7]) * inv));
+          }
+        }
+      }
+      if (row_active) {
+        const float lse2 = (l_sum > 0.f) ? (m_used + __log2f(l_sum)) : -INFINITY;
+        p.lse[tok * p.H + h] = lse2 * 0.69314718055994530942f;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (threadIdx.x == 0 && ctrl->abort_flag) atomicOr(p.status, kStatusTimeout);
+  if (warp == 5) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+}  // namespace
+
 cudaError_t launch_prefill(const PrefillParams& p, const CUtensorMap& tm_q, const CUtensorMap& tm_k,
                            const CUtensorMap& tm_v, cudaStream_t stream) {
-  (void)p; (void)tm_q; (void)tm_k; (void)tm_v; (void)stream;
-  return cudaErrorNotSupported;
+  static thread_local int configured_device = -1;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (configured_device != dev) {
+    e = cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e != cudaSuccess) return e;
+    configured_device = dev;
+  }
+  if (p.max_q_blocks < 1) return cudaSuccess;
+  dim3 grid(p.max_q_blocks, p.H, p.B);
+  prefill_kernel<<<grid, kThreads, kSmemBytes, stream>>>(tm_q, tm_k, tm_v, p);
+  return cudaGetLastError();
 }
+
 }  // namespace mla

@@ -25,7 +25,7 @@ MLA_KV_BF16 = 0
 MLA_KV_E4M3 = 1
 
 EXPORTED = ["mla_decode_plan", "mla_decode", "mla_prefill_varlen", "mla_get_status",
-            "mla_status_string", "mla_version", "mla_set_profile_events"]
+            "mla_status_string", "mla_version", "mla_set_profile_events", "mla_profile_elapsed_ms"]
 
 
 class MlaError(RuntimeError):
@@ -64,6 +64,8 @@ def _load() -> ctypes.CDLL:
     lib.mla_version.restype = i32
     lib.mla_set_profile_events.restype = i32
     lib.mla_set_profile_events.argtypes = [P, P]
+    lib.mla_profile_elapsed_ms.restype = i32
+    lib.mla_profile_elapsed_ms.argtypes = [P, P, ctypes.POINTER(ctypes.c_float)]
     return lib
 
 
@@ -147,6 +149,14 @@ def set_profile_events(start=None, stop=None) -> None:
     """Record torch.cuda.Event pairs around the main kernel of later calls (this thread)."""
     lib.mla_set_profile_events(ctypes.c_void_p(start.cuda_event) if start is not None else None,
                                ctypes.c_void_p(stop.cuda_event) if stop is not None else None)
+
+
+def profile_elapsed_ms(start, stop) -> float:
+    """Milliseconds between two torch.cuda.Event objects recorded through the hook."""
+    ms = ctypes.c_float()
+    _check(lib.mla_profile_elapsed_ms(ctypes.c_void_p(start.cuda_event), ctypes.c_void_p(stop.cuda_event),
+                                      ctypes.byref(ms)), "mla_profile_elapsed_ms")
+    return ms.value
 
 
 def get_status(stream=None) -> int:

@@ -275,6 +275,10 @@ def main():
     # carry event pairs around the split-KV partial kernel.
     n_ev = min(args.steps, 256)
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_ev)]
+    for a, b in ev:  # torch creates the CUDA events lazily, on first record
+        a.record(stream)
+        b.record(stream)
+    stream.synchronize()
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph, stream=stream):
         for i in range(args.steps):

@@ -221,7 +221,6 @@ int mla_decode(const mla_decode_plan_t* plan, const void* q, const void* kv_page
     if (workspace_bytes < plan->workspace_bytes) return MLA_ERR_WORKSPACE_TOO_SMALL;
     if (!aligned(workspace, 256)) return MLA_ERR_INVALID_ARG;
   }
-  if (plan->kv_dtype == MLA_KV_E4M3) return MLA_ERR_UNSUPPORTED;
   unsigned* status = status_ptr();
   if (!status) return MLA_ERR_CUDA;
 
@@ -233,7 +232,8 @@ int mla_decode(const mla_decode_plan_t* plan, const void* q, const void* kv_page
     const uint32_t box[2] = {64, static_cast<uint32_t>(kGroupRows)};
     if (!make_map(&tm_q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, q, dims, strides, box)) return MLA_ERR_CUDA;
   }
-  {
+  memset(&tm_kv, 0, sizeof tm_kv);
+  if (plan->kv_dtype == MLA_KV_BF16) {  // e4m3 pages are fetched with untiled bulk copies
     const uint64_t dims[2] = {static_cast<uint64_t>(kLatentDim),
                               static_cast<uint64_t>(plan->num_pages) * plan->page_size};
     const uint64_t strides[1] = {row_bytes};
@@ -279,13 +279,13 @@ int mla_prefill_varlen(const void* q, const void* k, const void* v, const int32_
                        const int32_t* cu_seqlens_kv, const int32_t* prefix_lens, int batch, int num_heads,
                        int max_seqlen_q, int total_q, int total_kv, float scale, void* out, float* lse,
                        void* stream) {
-  if (!q || !k || !v || !cu_seqlens_q || !cu_seqlens_kv || !prefix_lens || !out || !lse) return MLA_ERR_INVALID_ARG;
   if (batch < 1 || batch > 65535 || max_seqlen_q < 0 || total_q < 0 || total_kv < 0) return MLA_ERR_INVALID_ARG;
   if (num_heads < 1 || num_heads > 256) return MLA_ERR_UNSUPPORTED;
   if (!(scale > 0.f)) return MLA_ERR_INVALID_ARG;
+  if (total_q == 0 || max_seqlen_q == 0) return MLA_OK;  // no new tokens: nothing to compute
+  if (!q || !k || !v || !cu_seqlens_q || !cu_seqlens_kv || !prefix_lens || !out || !lse) return MLA_ERR_INVALID_ARG;
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16) || !aligned(lse, 4))
     return MLA_ERR_INVALID_ARG;
-  if (total_q == 0 || max_seqlen_q == 0) return MLA_OK;
   if (total_kv < 1) return MLA_ERR_INVALID_ARG;
   unsigned* status = status_ptr();
   if (!status) return MLA_ERR_CUDA;

@@ -2,18 +2,22 @@
 //
 // What it computes (per request b, draft t, head h; keys j = 0 .. L_b - T + t):
 //   out[b,t,h,:] = sum_j softmax_j(scale * q[b,t,h,:] . k_j) * k_j[:512]
-// where k_j is the 576-wide latent row j of request b, found through the page table.
-// TokenSpeed pages: "构建面向 Agentic 推理的下一代 LLM 推理引擎" (AICon talk), section
-// "Kernel：让 MLA 真正跑满 GPU" (latent state shared by all heads, fold factor, split-KV
-// partial + reduction stages, TMEM accumulators); launch-blog repost
-// "英偉達力薦，小團隊兩個月開源一款「光速級」智能體推理引擎", section "TokenSpeed 性能預覽"
-// (query-sequence axis folded into the head axis to fill the first matmul's M tile).
+// where k_j is the 576-wide latent row j of request b, found through the page table (an
+// e4m3 pool is decoded exactly to bf16 and its per-tensor scale folded into the softmax
+// scale and the output).  TokenSpeed pages: "构建面向 Agentic 推理的下一代 LLM 推理引擎"
+// (AICon talk), section "Kernel：让 MLA 真正跑满 GPU" (latent state shared by all heads,
+// fold factor, split-KV partial + reduction stages, TMEM accumulators, KV bandwidth as the
+// limit even with 8-bit KV); launch-blog repost "英偉達力薦，小團隊兩個月開源一款「光速級」
+// 智能體推理引擎", section "TokenSpeed 性能預覽" (query-sequence axis folded into the head
+// axis to fill the first matmul's M tile).
 //
 // Design on sm_103a (one CTA per (64-row group, split, request); one CTA per SM):
 //  * Fold: the T*H query rows of a request are one matrix with row m = t*H + h; a CTA
 //    takes 64 consecutive rows, so all heads and drafts share each latent tile load.
-//  * Producer warp: TMA (128-byte swizzled boxes of 64 columns) gathers one 64-key tile
-//    per stage from the pages named by the page table into a 2-stage ring (mbarriers).
+//  * Producer warp: bf16 pools are gathered by TMA (128-byte swizzled boxes of 64
+//    columns) one 64-key tile per stage from the pages named by the page table, into a
+//    2-stage ring; e4m3 pools are gathered by bulk copies of whole page rows into a 2-stage
+//    raw ring and decoded to the bf16 swizzled tile by two dequant warps.
 //  * MMA warp (one thread): BMM1  S[rows, keys]  = Q . K^T  (M=128, N=64, K=576;
 //    rows 64..127 of the M tile are don't-care) into TMEM, double-buffered;
 //    BMM2  O^T[dims, rows] += V^T . P^T  (M=128 per 128 value columns, N=rows, K=64
@@ -28,6 +32,9 @@
 //    its log-sum-exp for the combine kernel.
 // Every wait is bounded; on expiry the CTA records a timeout in the status word, drains
 // its in-flight copies and MMAs, frees TMEM and returns.
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+
 #include "mla_internal.h"
 #include "sm103a_ptx.cuh"
 
@@ -37,13 +44,18 @@ namespace {
 constexpr int kDimBlocks = kLatentDim / 64;          // 9 blocks of 64 columns (128 bytes)
 constexpr int kBlockBytes = 64 * 128;                // 64 rows x 128 bytes, swizzled
 constexpr int kTileBytes = kDimBlocks * kBlockBytes; // 73728: one bf16 64-key latent tile
+constexpr int kRawBytes = kTileKeys * kLatentDim;    // 36864: one e4m3 64-key tile
 constexpr int kStages = 2;
 constexpr int kThreads = 192;                        // warps 0-3 softmax/epilogue, 4 TMA, 5 MMA
 
+// Shared memory map.  bf16: Q | stage0 | stage1 | P | ctrl.
+//                     e4m3: Q | raw0 | raw1 | bf16 tile | P | ctrl  (same total).
 constexpr int kOffQ = 0;
-constexpr int kOffKV = kOffQ + kTileBytes;
-constexpr int kOffP = kOffKV + kStages * kTileBytes;
+constexpr int kOffStages = kOffQ + kTileBytes;
+constexpr int kOffTileFp8 = kOffStages + kStages * kRawBytes;
+constexpr int kOffP = kOffStages + kStages * kTileBytes;
 constexpr int kOffCtrl = kOffP + kBlockBytes;
+static_assert(kOffTileFp8 + kTileBytes == kOffP, "e4m3 layout must match the bf16 footprint");
 
 struct DecodeCtrl {
   uint64_t q_full;
@@ -53,6 +65,7 @@ struct DecodeCtrl {
   uint64_t s_free[2];
   uint64_t p_full;
   uint64_t o_done;
+  uint64_t tile_full;   // e4m3: dequantised tile ready
   uint64_t mma_drain;
   uint32_t tmem_base;
   int abort_flag;
@@ -88,9 +101,48 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
   }
 }
 
+// Two e4m3 codes -> two bf16 (exact: every e4m3 value is a bf16 value).
+__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint16_t two) {
+  const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(two), __NV_E4M3);
+  const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h));
+  return pack_bf16x2(f.x, f.y);
+}
+
+// Decode one raw e4m3 tile (64 rows x 576 bytes, row-major) into the 128-byte-swizzled
+// bf16 tile (9 blocks of 64 rows x 64 columns); rows >= valid_rows become zero.  Run by
+// 64 threads (t = 0..63).
+__device__ __forceinline__ void dequant_tile(const uint8_t* raw, uint8_t* tile, int valid_rows, int t) {
+  const uint32_t raw_s = smem_u32(raw);
+  const uint32_t tile_s = smem_u32(tile);
+#pragma unroll 4
+  for (int i = 0; i < kTileKeys * (kLatentDim / 16) / 64; ++i) {
+    const int item = t + 64 * i;
+    const int row = item / (kLatentDim / 16);
+    const int c16 = item % (kLatentDim / 16);
+    uint32_t w[4] = {0u, 0u, 0u, 0u};
+    if (row < valid_rows) {
+      asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                   : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
+                   : "r"(raw_s + row * kLatentDim + c16 * 16));
+    }
+    uint32_t o[8];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      o[2 * k] = e4m3x2_to_bf16x2(static_cast<uint16_t>(w[k] & 0xFFFFu));
+      o[2 * k + 1] = e4m3x2_to_bf16x2(static_cast<uint16_t>(w[k] >> 16));
+    }
+    const int blk = c16 >> 2;
+    const int cc = (c16 & 3) * 2;
+    const uint32_t rbase = tile_s + blk * kBlockBytes + row * 128;
+    st_shared_v4(rbase + ((cc ^ (row & 7)) << 4), o[0], o[1], o[2], o[3]);
+    st_shared_v4(rbase + (((cc + 1) ^ (row & 7)) << 4), o[4], o[5], o[6], o[7]);
+  }
+}
+
+template <bool kFp8>
 __global__ void __launch_bounds__(kThreads, 1)
-decode_partial_bf16_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kv,
-                           const DecodeParams p) {
+decode_partial_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kv,
+                      const DecodeParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   DecodeCtrl* ctrl = reinterpret_cast<DecodeCtrl*>(smem + kOffCtrl);
@@ -119,7 +171,7 @@ decode_partial_bf16_kernel(const __grid_constant__ CUtensorMap tm_q, const __gri
     mbar_init(&ctrl->q_full, 1);
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&ctrl->kv_full[s], 1);
-      mbar_init(&ctrl->kv_empty[s], 1);
+      mbar_init(&ctrl->kv_empty[s], kFp8 ? 64 : 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&ctrl->s_full[i], 1);
@@ -127,6 +179,7 @@ decode_partial_bf16_kernel(const __grid_constant__ CUtensorMap tm_q, const __gri
     }
     mbar_init(&ctrl->p_full, 128);
     mbar_init(&ctrl->o_done, 1);
+    mbar_init(&ctrl->tile_full, 64);
     mbar_init(&ctrl->mma_drain, 1);
     ctrl->abort_flag = 0;
     ctrl->rescale_flag[0] = ctrl->rescale_flag[1] = 0;
@@ -138,7 +191,7 @@ decode_partial_bf16_kernel(const __grid_constant__ CUtensorMap tm_q, const __gri
   }
   if (warp == 4 && lane == 0) {
     tma_prefetch_desc(&tm_q);
-    tma_prefetch_desc(&tm_kv);
+    if (!kFp8) tma_prefetch_desc(&tm_kv);
   }
   tc_fence_before();
   __syncthreads();
@@ -147,7 +200,7 @@ decode_partial_bf16_kernel(const __grid_constant__ CUtensorMap tm_q, const __gri
   volatile int* abort_flag = &ctrl->abort_flag;
 
   if (warp == 4) {
-    // ------------------------------------------------------------------ TMA producer
+    // ------------------------------------------------------------------ producer
     const int P = p.page_size;
     const int sub = P < kTileKeys ? kTileKeys / P : 1;  // pages per tile
     const int box_rows = P < kTileKeys ? P : kTileKeys;
@@ -178,11 +231,10 @@ decode_partial_bf16_kernel(const __grid_constant__ CUtensorMap tm_q, const __gri
       const int pg0 = k0 / P;
       const int tile_end = min(k0 + kTileKeys, L);
       const int npg = (P < kTileKeys) ? ((tile_end - 1) / P - pg0 + 1) : 1;
-      uint8_t* stage = smem + kOffKV + s * kTileBytes;
       int pids[8];
 #pragma unroll
       for (int pp = 0; pp < 8; ++pp) {
-        int pi = pg0 + pp;
+        const int pi = pg0 + pp;
         if (pp < sub) {
           while (pi - batch_base >= 32) {  // advance the page-id window (warp-uniform)
             batch_base += 32;
@@ -196,11 +248,24 @@ decode_partial_bf16_kernel(const __grid_constant__ CUtensorMap tm_q, const __gri
         }
       }
       if (lane == 0) {
-        mbar_arrive_expect_tx(&ctrl->kv_full[s], static_cast<uint32_t>(npg * box_rows * 128 * kDimBlocks));
-        for (int pp = 0; pp < npg; ++pp) {
-          const int y = pids[pp] * P + (P > kTileKeys ? (k0 % P) : 0);
-          for (int c = 0; c < kDimBlocks; ++c)
-            tma_load_2d(stage + c * kBlockBytes + pp * box_rows * 128, &tm_kv, &ctrl->kv_full[s], c * 64, y, pol_kv);
+        const int row_in_page = (P > kTileKeys) ? (k0 % P) : 0;
+        if (!kFp8) {
+          uint8_t* stage = smem + kOffStages + s * kTileBytes;
+          mbar_arrive_expect_tx(&ctrl->kv_full[s], static_cast<uint32_t>(npg * box_rows * 128 * kDimBlocks));
+          for (int pp = 0; pp < npg; ++pp) {
+            const int y = pids[pp] * P + row_in_page;
+            for (int c = 0; c < kDimBlocks; ++c)
+              tma_load_2d(stage + c * kBlockBytes + pp * box_rows * 128, &tm_kv, &ctrl->kv_full[s], c * 64, y,
+                          pol_kv);
+          }
+        } else {
+          uint8_t* stage = smem + kOffStages + s * kRawBytes;
+          const uint32_t bytes = static_cast<uint32_t>(box_rows * kLatentDim);
+          mbar_arrive_expect_tx(&ctrl->kv_full[s], bytes * npg);
+          for (int pp = 0; pp < npg; ++pp) {
+            const uint8_t* src = p.kv_pool + (static_cast<int64_t>(pids[pp]) * P + row_in_page) * kLatentDim;
+            bulk_load(stage + pp * box_rows * kLatentDim, src, bytes, &ctrl->kv_full[s], pol_kv);
+          }
         }
       }
       last_issued[s] = j;
@@ -220,45 +285,56 @@ decode_partial_bf16_kernel(const __grid_constant__ CUtensorMap tm_q, const __gri
       const uint32_t q_base = smem_u32(smem + kOffQ);
       const uint32_t p_base = smem_u32(smem + kOffP);
       bool ok = mbar_wait(&ctrl->q_full, 0, abort_flag);
-      for (int j = 0; j <= ntiles && ok; ++j) {
-        if (j < ntiles) {
-          const int s = j % kStages, sb = j & 1;
-          ok = mbar_wait(&ctrl->kv_full[s], (j / kStages) & 1, abort_flag);
-          if (ok && j >= 2) ok = mbar_wait(&ctrl->s_free[sb], ((j - 2) >> 1) & 1, abort_flag);
-          if (!ok) break;
-          tc_fence_after();
-          const uint32_t kv_base = smem_u32(smem + kOffKV + s * kTileBytes);
-          const uint32_t d = tmem + kTmemS + sb * 64;
+      auto bmm1 = [&](int j) -> bool {
+        const int s = j % kStages, sb = j & 1;
+        bool w = kFp8 ? mbar_wait(&ctrl->tile_full, j & 1, abort_flag)
+                      : mbar_wait(&ctrl->kv_full[s], (j / kStages) & 1, abort_flag);
+        if (w && j >= 2) w = mbar_wait(&ctrl->s_free[sb], ((j - 2) >> 1) & 1, abort_flag);
+        if (!w) return false;
+        tc_fence_after();
+        const uint32_t kv_base = kFp8 ? smem_u32(smem + kOffTileFp8) : smem_u32(smem + kOffStages + s * kTileBytes);
+        const uint32_t d = tmem + kTmemS + sb * 64;
 #pragma unroll 1
-          for (int c = 0; c < kDimBlocks; ++c) {
+        for (int c = 0; c < kDimBlocks; ++c) {
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              const uint64_t a = make_smem_desc(q_base + c * kBlockBytes + k * 32, 16, 1024);
-              const uint64_t bb = make_smem_desc(kv_base + c * kBlockBytes + k * 32, 16, 1024);
-              umma_bf16(d, a, bb, idesc1, (c | k) != 0);
-            }
+          for (int k = 0; k < 4; ++k) {
+            const uint64_t a = make_smem_desc(q_base + c * kBlockBytes + k * 32, 16, 1024);
+            const uint64_t bb = make_smem_desc(kv_base + c * kBlockBytes + k * 32, 16, 1024);
+            umma_bf16(d, a, bb, idesc1, (c | k) != 0);
           }
-          umma_commit(&ctrl->s_full[sb]);
         }
-        if (j >= 1) {
-          const int jj = j - 1, s = jj % kStages;
-          ok = mbar_wait(&ctrl->p_full, jj & 1, abort_flag);
-          if (!ok) break;
-          tc_fence_after();
-          const uint32_t kv_base = smem_u32(smem + kOffKV + s * kTileBytes);
+        umma_commit(&ctrl->s_full[sb]);
+        return true;
+      };
+      auto bmm2 = [&](int jj) -> bool {
+        const int s = jj % kStages;
+        if (!mbar_wait(&ctrl->p_full, jj & 1, abort_flag)) return false;
+        tc_fence_after();
+        const uint32_t kv_base = kFp8 ? smem_u32(smem + kOffTileFp8) : smem_u32(smem + kOffStages + s * kTileBytes);
 #pragma unroll
-          for (int qc = 0; qc < 4; ++qc) {
+        for (int qc = 0; qc < 4; ++qc) {
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-              // V^T: 128 value columns (two 64-column blocks, LBO apart) x 16 keys (two
-              // 8-key groups, SBO apart), MN-major.  P^T: rows x 16 keys, K-major.
-              const uint64_t a = make_smem_desc(kv_base + (2 * qc) * kBlockBytes + kk * 2048, kBlockBytes, 1024);
-              const uint64_t bb = make_smem_desc(p_base + kk * 32, 16, 1024);
-              umma_bf16(tmem + qc * 64, a, bb, idesc2, (jj > 0 || kk > 0) ? 1u : 0u);
-            }
+          for (int kk = 0; kk < 4; ++kk) {
+            // V^T: 128 value columns (two 64-column blocks, LBO apart) x 16 keys (two
+            // 8-key groups, SBO apart), MN-major.  P^T: rows x 16 keys, K-major.
+            const uint64_t a = make_smem_desc(kv_base + (2 * qc) * kBlockBytes + kk * 2048, kBlockBytes, 1024);
+            const uint64_t bb = make_smem_desc(p_base + kk * 32, 16, 1024);
+            umma_bf16(tmem + qc * 64, a, bb, idesc2, (jj > 0 || kk > 0) ? 1u : 0u);
           }
-          umma_commit(&ctrl->o_done);
-          umma_commit(&ctrl->kv_empty[s]);
+        }
+        umma_commit(&ctrl->o_done);
+        if (!kFp8) umma_commit(&ctrl->kv_empty[s]);
+        return true;
+      };
+      for (int j = 0; j <= ntiles && ok; ++j) {
+        if (kFp8) {
+          // the single bf16 tile is rewritten for tile j only after BMM2(j-1) has read it
+          if (j >= 1) ok = bmm2(j - 1);
+          if (ok && j < ntiles) ok = bmm1(j);
+        } else {
+          // BMM1 of the next tile runs on the tensor core while the softmax works on this one
+          if (j < ntiles) ok = bmm1(j);
+          if (ok && j >= 1) ok = bmm2(j - 1);
         }
       }
       // every MMA issued so far completes before TMEM is released
@@ -267,7 +343,7 @@ decode_partial_bf16_kernel(const __grid_constant__ CUtensorMap tm_q, const __gri
     }
     __syncwarp();
   } else {
-    // ------------------------------------------------------------------ softmax + epilogue (warps 0-3)
+    // ------------------------------------------------------------------ softmax / dequant / epilogue (warps 0-3)
     const bool is_sm = warp < 2;
     const int r = warp * 32 + lane;  // folded row within the group (softmax warps)
     const bool row_active = is_sm && r < nrows;
@@ -277,11 +353,26 @@ decode_partial_bf16_kernel(const __grid_constant__ CUtensorMap tm_q, const __gri
     float m_used = -INFINITY;
     float l_sum = 0.f;
     bool failed = false;
+    bool carry_fail = false;  // dequant warps: a wait that failed after the last barrier
+
+    auto dequant = [&](int j) -> bool {  // warps 2-3: raw stage of tile j -> bf16 tile
+      const int s = j % kStages;
+      bool w = mbar_wait(&ctrl->kv_full[s], (j / kStages) & 1, abort_flag);
+      w = !__any_sync(0xffffffffu, !w);
+      if (!w) return false;
+      dequant_tile(smem + kOffStages + s * kRawBytes, smem + kOffTileFp8, L - (kv_start + j * kTileKeys),
+                   threadIdx.x - 64);
+      fence_proxy_async_smem();
+      mbar_arrive(&ctrl->tile_full);
+      mbar_arrive(&ctrl->kv_empty[s]);
+      return true;
+    };
+    if (kFp8 && !is_sm) carry_fail = !dequant(0);
 
     for (int j = 0; j < ntiles; ++j) {
       const int sb = j & 1;
       const int k0 = kv_start + j * kTileKeys;
-      bool fail = false;
+      bool fail = carry_fail;
       bool need_rescale = false;
       float alpha = 1.f;
       uint32_t packed[32];
@@ -342,20 +433,21 @@ decode_partial_bf16_kernel(const __grid_constant__ CUtensorMap tm_q, const __gri
         failed = true;
         break;
       }
-      // zero value rows past the request's end in the last tile (stale or unloaded rows
-      // would otherwise meet P = 0 in BMM2 and could carry NaN/Inf bit patterns)
-      const int valid_rows = L - k0;
-      if (valid_rows < kTileKeys) {
-        uint8_t* stage = smem + kOffKV + (j % kStages) * kTileBytes;
-        const int nzero = (kTileKeys - valid_rows) * 8;  // 16-byte chunks per block
-        for (int idx = threadIdx.x; idx < nzero * 8; idx += 128) {
-          const int blk = idx / nzero;
-          const int rem = idx % nzero;
-          const int row = valid_rows + rem / 8;
-          const uint32_t a = smem_u32(stage + blk * kBlockBytes + row * 128 + (rem % 8) * 16);
-          st_shared_v4(a, 0u, 0u, 0u, 0u);
+      if (!kFp8) {
+        // zero value rows past the request's end in the last tile (stale or unloaded rows
+        // would otherwise meet P = 0 in BMM2 and could carry NaN/Inf bit patterns)
+        const int valid_rows = L - k0;
+        if (valid_rows < kTileKeys) {
+          uint8_t* stage = smem + kOffStages + (j % kStages) * kTileBytes;
+          const int nzero = (kTileKeys - valid_rows) * 8;  // 16-byte chunks per block
+          for (int idx = threadIdx.x; idx < nzero * 8; idx += 128) {
+            const int blk = idx / nzero;
+            const int rem = idx % nzero;
+            const int row = valid_rows + rem / 8;
+            st_shared_v4(smem_u32(stage + blk * kBlockBytes + row * 128 + (rem % 8) * 16), 0u, 0u, 0u, 0u);
+          }
+          fence_proxy_async_smem();
         }
-        fence_proxy_async_smem();
       }
       if (ctrl->rescale_flag[0] | ctrl->rescale_flag[1]) {
         // O^T[dim, row] *= alpha[row] for all 512 value columns; this thread owns TMEM lane
@@ -364,13 +456,13 @@ decode_partial_bf16_kernel(const __grid_constant__ CUtensorMap tm_q, const __gri
 #pragma unroll 1
         for (int qc = 0; qc < 4; ++qc) {
 #pragma unroll
-          for (int h = 0; h < 2; ++h) {
+          for (int hh = 0; hh < 2; ++hh) {
             uint32_t v[32];
-            const uint32_t addr = tmem + lane_base + qc * 64 + h * 32;
+            const uint32_t addr = tmem + lane_base + qc * 64 + hh * 32;
             tmem_ld32(addr, v);
             tmem_ld_wait();
 #pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * ctrl->alpha[h * 32 + i]);
+            for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * ctrl->alpha[hh * 32 + i]);
             tmem_st32(addr, v);
           }
         }
@@ -378,6 +470,12 @@ decode_partial_bf16_kernel(const __grid_constant__ CUtensorMap tm_q, const __gri
       }
       tc_fence_before();
       mbar_arrive(&ctrl->p_full);
+      if (kFp8 && !is_sm && j + 1 < ntiles) {
+        // the bf16 tile is free once BMM2(j) has completed
+        bool w = mbar_wait(&ctrl->o_done, j & 1, abort_flag);
+        w = !__any_sync(0xffffffffu, !w);
+        carry_fail = !(w && dequant(j + 1));
+      }
     }
 
     if (!failed) {
@@ -405,13 +503,13 @@ decode_partial_bf16_kernel(const __grid_constant__ CUtensorMap tm_q, const __gri
       for (int qc = 0; qc < 4; ++qc) {
         const int dim = qc * 128 + warp * 32 + lane;
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
+        for (int hh = 0; hh < 2; ++hh) {
           uint32_t v[32];
-          tmem_ld32(tmem + lane_base + qc * 64 + h * 32, v);
+          tmem_ld32(tmem + lane_base + qc * 64 + hh * 32, v);
           tmem_ld_wait();
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
-            const int rr = h * 32 + i;
+            const int rr = hh * 32 + i;
             if (rr < nrows) {
               const float val = __uint_as_float(v[i]) * ctrl->row_scale[rr];
               if (final_out) {
@@ -483,23 +581,29 @@ __global__ void __launch_bounds__(256) decode_combine_kernel(const DecodeParams 
   if (lane == 0) p.lse[static_cast<int64_t>(b) * p.R + row] = (wsum > 0.f) ? (mx + __logf(wsum)) : -INFINITY;
 }
 
-}  // namespace
-
-cudaError_t launch_decode_partial(const DecodeParams& p, const CUtensorMap& tm_q, const CUtensorMap& tm_kv,
-                                  int head_groups, cudaStream_t stream) {
+template <bool kFp8>
+cudaError_t launch_partial_impl(const DecodeParams& p, const CUtensorMap& tm_q, const CUtensorMap& tm_kv,
+                                int head_groups, cudaStream_t stream) {
   static thread_local int configured_device = -1;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (configured_device != dev) {
-    e = cudaFuncSetAttribute(decode_partial_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    e = cudaFuncSetAttribute(decode_partial_kernel<kFp8>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return e;
     configured_device = dev;
   }
-  if (p.kv_fp8) return cudaErrorNotSupported;
   dim3 grid(head_groups, p.max_splits, p.B);
-  decode_partial_bf16_kernel<<<grid, kThreads, kSmemBytes, stream>>>(tm_q, tm_kv, p);
+  decode_partial_kernel<kFp8><<<grid, kThreads, kSmemBytes, stream>>>(tm_q, tm_kv, p);
   return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_decode_partial(const DecodeParams& p, const CUtensorMap& tm_q, const CUtensorMap& tm_kv,
+                                  int head_groups, cudaStream_t stream) {
+  return p.kv_fp8 ? launch_partial_impl<true>(p, tm_q, tm_kv, head_groups, stream)
+                  : launch_partial_impl<false>(p, tm_q, tm_kv, head_groups, stream);
 }
 
 cudaError_t launch_decode_combine(const DecodeParams& p, cudaStream_t stream) {

@@ -89,6 +89,11 @@ SMALL = [
     ("page128", 2, 1, 16, [700, 129], 128, "bf16"),
     ("page256", 1, 4, 16, [2000], 256, "bf16"),
     ("long_single", 1, 1, 16, [20000], 64, "bf16"),
+    ("fp8_drafts4", 2, 4, 16, [300, 1000], 64, "e4m3"),
+    ("fp8_ragged", 3, 1, 16, [1, 65, 130], 64, "e4m3"),
+    ("fp8_page16", 2, 2, 16, [77, 500], 16, "e4m3"),
+    ("fp8_page128", 1, 3, 16, [700], 128, "e4m3"),
+    ("fp8_h128", 1, 2, 128, [900], 64, "e4m3"),
 ]
 
 

@@ -158,6 +158,14 @@ int mla_set_profile_events(void* start_event, void* stop_event);
  * has not completed. */
 int mla_profile_elapsed_ms(void* start_event, void* stop_event, float* ms_out);
 
+/* Watchdog self-test: enqueue a one-warp kernel that waits, through the same bounded
+ * mbarrier wait every MLA kernel uses, on a barrier nothing ever arrives on.  The wait
+ * gives up after its limit (1 s) and records MLA_ERR_TIMEOUT in the status word, which
+ * the next mla_get_status() returns; the CUDA context stays usable.  Returns MLA_OK once
+ * enqueued.  (No counterpart on the pages: it exercises the failure-detection path of
+ * this library without faulting or hanging the GPU.) */
+int mla_selftest_wait_timeout(void* stream);
+
 /* Static, human-readable name of a status code. */
 const char* mla_status_string(int status);
 

@@ -343,6 +343,13 @@ int mla_profile_elapsed_ms(void* start_event, void* stop_event, float* ms_out) {
   return MLA_OK;
 }
 
+int mla_selftest_wait_timeout(void* stream) {
+  unsigned* status = status_ptr();
+  if (!status) return MLA_ERR_CUDA;
+  if (launch_selftest_timeout(status, static_cast<cudaStream_t>(stream)) != cudaSuccess) return MLA_ERR_CUDA;
+  return MLA_OK;
+}
+
 int mla_get_status(void* stream) {
   unsigned* status = status_ptr();
   if (!status) return MLA_ERR_CUDA;

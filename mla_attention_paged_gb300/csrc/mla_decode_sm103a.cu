@@ -581,6 +581,22 @@ __global__ void __launch_bounds__(256) decode_combine_kernel(const DecodeParams 
   if (lane == 0) p.lse[static_cast<int64_t>(b) * p.R + row] = (wsum > 0.f) ? (mx + __logf(wsum)) : -INFINITY;
 }
 
+// Watchdog self-test: wait on an mbarrier that nothing ever arrives on, through the same
+// bounded wait the kernels above use; the wait must give up and record a timeout.
+__global__ void selftest_timeout_kernel(unsigned* status) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    fence_mbarrier_init();
+  }
+  __syncthreads();
+  const bool ok = mbar_wait(&bar, 0, &abort_flag);
+  __syncthreads();
+  if (threadIdx.x == 0 && (!ok || abort_flag)) atomicOr(status, kStatusTimeout);
+}
+
 template <bool kFp8>
 cudaError_t launch_partial_impl(const DecodeParams& p, const CUtensorMap& tm_q, const CUtensorMap& tm_kv,
                                 int head_groups, cudaStream_t stream) {
@@ -604,6 +620,11 @@ cudaError_t launch_decode_partial(const DecodeParams& p, const CUtensorMap& tm_q
                                   int head_groups, cudaStream_t stream) {
   return p.kv_fp8 ? launch_partial_impl<true>(p, tm_q, tm_kv, head_groups, stream)
                   : launch_partial_impl<false>(p, tm_q, tm_kv, head_groups, stream);
+}
+
+cudaError_t launch_selftest_timeout(unsigned* status, cudaStream_t stream) {
+  selftest_timeout_kernel<<<1, 32, 0, stream>>>(status);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_decode_combine(const DecodeParams& p, cudaStream_t stream) {

@@ -52,6 +52,8 @@ cudaError_t launch_decode_partial(const DecodeParams& p, const CUtensorMap& tm_q
                                   int head_groups, cudaStream_t stream);
 // Decode: LSE-merge of the split partials for requests with more than one split.
 cudaError_t launch_decode_combine(const DecodeParams& p, cudaStream_t stream);
+// Watchdog self-test kernel (a wait nothing satisfies; must time out and report).
+cudaError_t launch_selftest_timeout(unsigned* status, cudaStream_t stream);
 // Prefill: ragged causal prefill with prefix offset.
 cudaError_t launch_prefill(const PrefillParams& p, const CUtensorMap& tm_q, const CUtensorMap& tm_k,
                            const CUtensorMap& tm_v, cudaStream_t stream);

@@ -25,7 +25,8 @@ MLA_KV_BF16 = 0
 MLA_KV_E4M3 = 1
 
 EXPORTED = ["mla_decode_plan", "mla_decode", "mla_prefill_varlen", "mla_get_status",
-            "mla_status_string", "mla_version", "mla_set_profile_events", "mla_profile_elapsed_ms"]
+            "mla_status_string", "mla_version", "mla_set_profile_events", "mla_profile_elapsed_ms",
+            "mla_selftest_wait_timeout"]
 
 
 class MlaError(RuntimeError):
@@ -65,6 +66,8 @@ def _load() -> ctypes.CDLL:
     lib.mla_set_profile_events.restype = i32
     lib.mla_set_profile_events.argtypes = [P, P]
     lib.mla_profile_elapsed_ms.restype = i32
+    lib.mla_selftest_wait_timeout.restype = i32
+    lib.mla_selftest_wait_timeout.argtypes = [P]
     lib.mla_profile_elapsed_ms.argtypes = [P, P, ctypes.POINTER(ctypes.c_float)]
     return lib
 
@@ -157,6 +160,11 @@ def profile_elapsed_ms(start, stop) -> float:
     _check(lib.mla_profile_elapsed_ms(ctypes.c_void_p(start.cuda_event), ctypes.c_void_p(stop.cuda_event),
                                       ctypes.byref(ms)), "mla_profile_elapsed_ms")
     return ms.value
+
+
+def selftest_wait_timeout(stream=None) -> None:
+    """Enqueue the watchdog self-test kernel (its bounded wait must expire)."""
+    _check(lib.mla_selftest_wait_timeout(_stream_handle(stream)), "mla_selftest_wait_timeout")
 
 
 def get_status(stream=None) -> int:

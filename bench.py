@@ -60,6 +60,96 @@ def decode_flops(wl):
     return 2 * sum(wl.q_len * wl.heads * L * (576 + 512) for L in wl.seq_lens)
 
 
+def prefill_flops(wl):
+    """2 * H * (192 + 128) * sum over new tokens of the keys each one sees."""
+    keys = sum(n * p + n * (n + 1) // 2 for p, n in zip(wl.prefix_lens, wl.new_lens))
+    return 2 * wl.heads * (192 + 128) * keys
+
+
+def measure_decode_extra(mla, name, dev, steps=50):
+    """Secondary decode measurement (device time per call, partial-kernel roofline)."""
+    wl = decode_workloads()[name]
+    kv_bytes, alg_bytes = decode_bytes(wl)
+    n_sets = max(2, math.ceil(2.5 * L2_BYTES / kv_bytes) + 1) if kv_bytes < 2.5 * L2_BYTES else 1
+    sets = []
+    for i in range(n_sets):
+        w = decode_workloads()[name]
+        w.seed = replica_seed(wl.seed, i, 0)
+        sets.append(make_decode_inputs(w, dev))
+    kvd = mla.MLA_KV_E4M3 if wl.kv_dtype == "e4m3" else mla.MLA_KV_BF16
+    plan = mla.decode_plan(wl.seq_lens, wl.q_len, wl.heads, wl.page_size, sets[0].page_table.shape[1],
+                           sets[0].kv_pool.shape[0], kvd)
+    ws_buf = mla.workspace_for(plan, dev)
+    out = torch.empty(wl.batch, wl.q_len, wl.heads, 512, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty(wl.batch, wl.q_len, wl.heads, dtype=torch.float32, device=dev)
+    st = torch.cuda.Stream(device=dev)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    with torch.cuda.stream(st):
+        for a, b in ev:
+            a.record(st)
+            b.record(st)
+        for i in range(5):
+            s = sets[i % n_sets]
+            mla.decode(plan, s.q, s.kv_pool, s.page_table, s.seq_lens, s.scale, s.kv_scale, out=out, lse=lse,
+                       workspace=ws_buf, stream=st)
+        st.synchronize()
+        start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        start.record(st)
+        for i in range(steps):
+            s = sets[i % n_sets]
+            mla.set_profile_events(ev[i][0], ev[i][1])
+            mla.decode(plan, s.q, s.kv_pool, s.page_table, s.seq_lens, s.scale, s.kv_scale, out=out, lse=lse,
+                       workspace=ws_buf, stream=st)
+        mla.set_profile_events(None, None)
+        stop.record(st)
+    st.synchronize()
+    assert mla.get_status(st) == mla.MLA_OK
+    call_ms = start.elapsed_time(stop) / steps
+    part_ms = statistics.median(mla.profile_elapsed_ms(a, b) for a, b in ev)
+    peak = _peaks()
+    del sets
+    return {"workload": name, "us_per_call": call_ms * 1e3, "kv_gbs": kv_bytes / (call_ms / 1e3) / 1e9,
+            "partial_us": part_ms * 1e3, "partial_gbs": alg_bytes / (part_ms / 1e3) / 1e9,
+            "hbm_frac": alg_bytes / (part_ms / 1e3) / 1e9 / peak["hbm_gbs"],
+            "tflops": decode_flops(wl) / (call_ms / 1e3) / 1e12, "splits": plan.max_splits,
+            "timing": "eager calls, L2 " + ("rotated sets" if n_sets > 1 else "inputs > L2")}
+
+
+def measure_prefill(mla, dev, steps=5):
+    from mla_attention_paged_gb300.inputs import make_prefill_inputs, prefill_workloads
+    wl = prefill_workloads()["prefill_b5_h16_prefix"]
+    inp = make_prefill_inputs(wl, dev)
+    out = torch.empty(inp.q.shape[0], wl.heads, 128, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty(inp.q.shape[0], wl.heads, dtype=torch.float32, device=dev)
+    st = torch.cuda.Stream(device=dev)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+
+    def call():
+        mla.prefill_varlen(inp.q, inp.k, inp.v, inp.cu_seqlens_q, inp.cu_seqlens_kv, inp.prefix_lens,
+                           inp.max_seqlen_q, inp.scale, out=out, lse=lse, stream=st)
+
+    with torch.cuda.stream(st):
+        for a, b in ev:
+            a.record(st)
+            b.record(st)
+        for _ in range(2):
+            call()
+        st.synchronize()
+        for i in range(steps):
+            mla.set_profile_events(ev[i][0], ev[i][1])
+            call()
+        mla.set_profile_events(None, None)
+    st.synchronize()
+    assert mla.get_status(st) == mla.MLA_OK
+    ms = statistics.median(mla.profile_elapsed_ms(a, b) for a, b in ev)
+    fl = prefill_flops(wl)
+    peak = _peaks()
+    tf = fl / (ms / 1e3) / 1e12
+    return {"workload": wl.name, "ms_per_call": ms, "tflops": tf, "flops_per_call": fl,
+            "roofline": {"bound": "tensor", "achieved": tf, "peak": peak["bf16_tflops"], "unit": "TFLOP/s",
+                         "frac": tf / peak["bf16_tflops"], "peak_source": peak["source"] + " bf16 dense burst"}}
+
+
 class ClockSampler:
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -136,6 +226,11 @@ def _sum_over_ranks(x, ws, device):
     return float(t.item())
 
 
+def replica_seed(base_seed, set_index, rank):
+    """Seed of input set `set_index` on replica `rank`: every rank and set draws its own data."""
+    return base_seed + 97 * set_index + 100003 * rank
+
+
 def _traffic_record(kernel_src):
     """DRAM bytes per launch from the committed ncu summary, if it was taken on the
     current kernel source; otherwise None."""
@@ -163,7 +258,8 @@ def cpu_baseline(wl, inp_cpu, budget_s=15.0):
     n = 8
     done_rows, elapsed = 0, 0.0
     while True:
-        rows = rng.choice(rows_total, size=min(n, rows_total), replace=False)
+        n = min(n, rows_total - done_rows) if done_rows < rows_total else n
+        rows = rng.choice(rows_total, size=max(1, min(n, rows_total)), replace=False)
         t0 = time.perf_counter()
         oracle.mla_decode(inp_cpu.q, inp_cpu.kv_pool, inp_cpu.page_table, inp_cpu.seq_lens, inp_cpu.scale,
                           kv_scale=inp_cpu.kv_scale, rows=rows)
@@ -229,6 +325,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="mine", choices=["mine", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extra", action="store_true", help="skip the secondary prefill / batch-16 decode lines")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     ws, rank, local = _dist()
@@ -250,7 +347,7 @@ def main():
     sets = []
     for i in range(n_sets):
         wl_i = decode_workloads()[WORKLOAD]
-        wl_i.seed = wl.seed + 97 * i + 1000 * rank
+        wl_i.seed = replica_seed(wl.seed, i, rank)
         sets.append(make_decode_inputs(wl_i, dev))
     s0 = sets[0]
     plan = mla.decode_plan(wl.seq_lens, wl.q_len, wl.heads, wl.page_size, s0.page_table.shape[1],
@@ -377,6 +474,14 @@ def main():
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         inp_cpu = make_decode_inputs(decode_workloads()[WORKLOAD], "cpu")
         line["cpu_baseline"] = cpu_baseline(wl, inp_cpu)
+    if not args.no_extra:
+        # the other hot-path rows, measured on their own (not part of `value`)
+        del sets, host_in, dev_in, host_out, graph
+        torch.cuda.empty_cache()
+        line["extra"] = {"prefill": measure_prefill(mla, dev)}
+        for name in ["decode_bf16_b16_q4_h16_l64k", "decode_fp8_b16_q4_h16_l64k"]:
+            line["extra"][name] = measure_decode_extra(mla, name, dev)
+            torch.cuda.empty_cache()
     if rank == 0:
         print(json.dumps(line), flush=True)
     if ws > 1:

@@ -285,56 +285,76 @@ decode_partial_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
       const uint32_t q_base = smem_u32(smem + kOffQ);
       const uint32_t p_base = smem_u32(smem + kOffP);
       bool ok = mbar_wait(&ctrl->q_full, 0, abort_flag);
-      auto bmm1 = [&](int j) -> bool {
+      // Descriptors are built once; each MMA advances the start-address field by a
+      // compile-time offset (addresses stay below 256 KB, so no carry leaves the field).
+      const uint64_t q_desc = make_smem_desc(q_base, 16, 1024);
+      const uint64_t p_desc = make_smem_desc(p_base, 16, 1024);
+      auto bmm1 = [&](int j) {
         const int s = j % kStages, sb = j & 1;
-        bool w = kFp8 ? mbar_wait(&ctrl->tile_full, j & 1, abort_flag)
-                      : mbar_wait(&ctrl->kv_full[s], (j / kStages) & 1, abort_flag);
-        if (w && j >= 2) w = mbar_wait(&ctrl->s_free[sb], ((j - 2) >> 1) & 1, abort_flag);
-        if (!w) return false;
-        tc_fence_after();
         const uint32_t kv_base = kFp8 ? smem_u32(smem + kOffTileFp8) : smem_u32(smem + kOffStages + s * kTileBytes);
+        const uint64_t k_desc = make_smem_desc(kv_base, 16, 1024);
         const uint32_t d = tmem + kTmemS + sb * 64;
-#pragma unroll 1
+#pragma unroll
         for (int c = 0; c < kDimBlocks; ++c) {
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
-            const uint64_t a = make_smem_desc(q_base + c * kBlockBytes + k * 32, 16, 1024);
-            const uint64_t bb = make_smem_desc(kv_base + c * kBlockBytes + k * 32, 16, 1024);
-            umma_bf16(d, a, bb, idesc1, (c | k) != 0);
+            const uint64_t off = static_cast<uint64_t>((c * kBlockBytes + k * 32) >> 4);
+            umma_bf16(d, q_desc + off, k_desc + off, idesc1, (c | k) != 0);
           }
         }
         umma_commit(&ctrl->s_full[sb]);
-        return true;
       };
-      auto bmm2 = [&](int jj) -> bool {
+      auto bmm2 = [&](int jj) {
         const int s = jj % kStages;
-        if (!mbar_wait(&ctrl->p_full, jj & 1, abort_flag)) return false;
-        tc_fence_after();
         const uint32_t kv_base = kFp8 ? smem_u32(smem + kOffTileFp8) : smem_u32(smem + kOffStages + s * kTileBytes);
+        // V^T: 128 value columns (two 64-column blocks, LBO apart) x 16 keys (two 8-key
+        // groups, SBO apart), MN-major.  P^T: rows x 16 keys, K-major.
+        const uint64_t v_desc = make_smem_desc(kv_base, kBlockBytes, 1024);
 #pragma unroll
         for (int qc = 0; qc < 4; ++qc) {
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
-            // V^T: 128 value columns (two 64-column blocks, LBO apart) x 16 keys (two
-            // 8-key groups, SBO apart), MN-major.  P^T: rows x 16 keys, K-major.
-            const uint64_t a = make_smem_desc(kv_base + (2 * qc) * kBlockBytes + kk * 2048, kBlockBytes, 1024);
-            const uint64_t bb = make_smem_desc(p_base + kk * 32, 16, 1024);
-            umma_bf16(tmem + qc * 64, a, bb, idesc2, (jj > 0 || kk > 0) ? 1u : 0u);
+            const uint64_t voff = static_cast<uint64_t>((2 * qc * kBlockBytes + kk * 2048) >> 4);
+            const uint64_t poff = static_cast<uint64_t>((kk * 32) >> 4);
+            umma_bf16(tmem + qc * 64, v_desc + voff, p_desc + poff, idesc2, (jj > 0 || kk > 0) ? 1u : 0u);
           }
         }
         umma_commit(&ctrl->o_done);
         if (!kFp8) umma_commit(&ctrl->kv_empty[s]);
-        return true;
       };
-      for (int j = 0; j <= ntiles && ok; ++j) {
-        if (kFp8) {
-          // the single bf16 tile is rewritten for tile j only after BMM2(j-1) has read it
-          if (j >= 1) ok = bmm2(j - 1);
-          if (ok && j < ntiles) ok = bmm1(j);
+      // Issue whichever GEMM is ready: BMM2(n2) first (it frees a stage), else BMM1(n1)
+      // for a tile whose data has landed and whose S buffer is free.  BMM1 may run up to
+      // two tiles ahead of BMM2 (double-buffered S).
+      int n1 = 0, n2 = 0;
+      unsigned long long idle_since = 0;
+      while (ok && n2 < ntiles) {
+        bool progressed = false;
+        if (n2 < n1 && mbar_test_wait(&ctrl->p_full, n2 & 1)) {
+          tc_fence_after();
+          bmm2(n2);
+          ++n2;
+          progressed = true;
+        } else if (n1 < ntiles && n1 < n2 + 2) {
+          const int s = n1 % kStages, sb = n1 & 1;
+          const bool data = kFp8 ? mbar_test_wait(&ctrl->tile_full, n1 & 1)
+                                 : mbar_test_wait(&ctrl->kv_full[s], (n1 / kStages) & 1);
+          if (data && (n1 < 2 || mbar_test_wait(&ctrl->s_free[sb], ((n1 - 2) >> 1) & 1))) {
+            tc_fence_after();
+            bmm1(n1);
+            ++n1;
+            progressed = true;
+          }
+        }
+        if (progressed) {
+          idle_since = 0;
         } else {
-          // BMM1 of the next tile runs on the tensor core while the softmax works on this one
-          if (j < ntiles) ok = bmm1(j);
-          if (ok && j >= 1) ok = bmm2(j - 1);
+          const unsigned long long now = global_timer_ns();
+          if (idle_since == 0) {
+            idle_since = now;
+          } else if (*abort_flag || now - idle_since > kWaitLimitNs) {
+            *abort_flag = 1;
+            ok = false;
+          }
         }
       }
       // every MMA issued so far completes before TMEM is released
@@ -499,6 +519,10 @@ decode_partial_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
         }
       }
       named_bar_sync(1, 128);
+      // Normalised O is transposed through shared memory (the KV stage area is free once
+      // the last BMM2 has completed) so that global stores are whole 16-byte row chunks.
+      float* stage_f = reinterpret_cast<float*>(smem + kOffStages);                   // [64][512] fp32
+      __nv_bfloat16* stage_h = reinterpret_cast<__nv_bfloat16*>(smem + kOffStages);   // [64][512] bf16
 #pragma unroll 1
       for (int qc = 0; qc < 4; ++qc) {
         const int dim = qc * 128 + warp * 32 + lane;
@@ -510,15 +534,29 @@ decode_partial_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
             const int rr = hh * 32 + i;
-            if (rr < nrows) {
-              const float val = __uint_as_float(v[i]) * ctrl->row_scale[rr];
-              if (final_out) {
-                p.out[(static_cast<int64_t>(b) * p.R + row0 + rr) * kValueDim + dim] = __float2bfloat16_rn(val);
-              } else {
-                p.ws_o[((static_cast<int64_t>(b) * p.max_splits + split) * p.R + row0 + rr) * kValueDim + dim] = val;
-              }
-            }
+            const float val = __uint_as_float(v[i]) * ctrl->row_scale[rr];
+            if (final_out)
+              stage_h[rr * kValueDim + dim] = __float2bfloat16_rn(val);
+            else
+              stage_f[rr * kValueDim + dim] = val;
           }
+        }
+      }
+      named_bar_sync(1, 128);
+      if (final_out) {
+        constexpr int kChunksPerRow = kValueDim * 2 / 16;
+        for (int c = threadIdx.x; c < nrows * kChunksPerRow; c += 128) {
+          const int rr = c / kChunksPerRow, cc = c % kChunksPerRow;
+          const uint4 v = *reinterpret_cast<const uint4*>(stage_h + rr * kValueDim + cc * 8);
+          *reinterpret_cast<uint4*>(p.out + (static_cast<int64_t>(b) * p.R + row0 + rr) * kValueDim + cc * 8) = v;
+        }
+      } else {
+        constexpr int kChunksPerRow = kValueDim * 4 / 16;
+        float* dst = p.ws_o + ((static_cast<int64_t>(b) * p.max_splits + split) * p.R + row0) * kValueDim;
+        for (int c = threadIdx.x; c < nrows * kChunksPerRow; c += 128) {
+          const int rr = c / kChunksPerRow, cc = c % kChunksPerRow;
+          const float4 v = *reinterpret_cast<const float4*>(stage_f + rr * kValueDim + cc * 4);
+          *reinterpret_cast<float4*>(dst + rr * kValueDim + cc * 4) = v;
         }
       }
     }
@@ -535,50 +573,93 @@ decode_partial_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
 
 // --------------------------------------------------------------------------------------
 // Combine: out[b, row] = sum_s exp(lse_s - lse) * O_s,  lse = log sum_s exp(lse_s).
-// One warp per folded row, each lane owns 16 of the 512 value columns.
+// One 128-thread CTA per (request, folded row); thread i owns value columns 4i..4i+3.
+// The split weights are computed once into shared memory; the partial rows are then read
+// as independent 16-byte loads, several splits in flight per thread.
 // --------------------------------------------------------------------------------------
-__global__ void __launch_bounds__(256) decode_combine_kernel(const DecodeParams p) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int row = blockIdx.x * 8 + warp;
+constexpr int kCombineThreads = 128;
+constexpr int kCombineMaxSplitsSmem = 1024;
+
+__global__ void __launch_bounds__(kCombineThreads) decode_combine_kernel(const DecodeParams p) {
+  __shared__ float w_s[kCombineMaxSplitsSmem];
+  __shared__ float red[kCombineThreads / 32];
+  __shared__ float stat[2];
+  const int row = blockIdx.x;
   const int b = blockIdx.y;
-  if (row >= p.R) return;
+  const int tid = threadIdx.x;
   const int L = p.seq_lens[b];
   if (L < p.T || L > p.max_seq) return;
   const int ns = (L + p.chunk - 1) / p.chunk;
   if (ns <= 1) return;
-  const float* lse_s = p.ws_lse + static_cast<int64_t>(b) * p.max_splits * p.R + row;
+  const int64_t base = static_cast<int64_t>(b) * p.max_splits;
+  const float* lse_s = p.ws_lse + base * p.R + row;
+  // max over splits
   float mx = -INFINITY;
-  for (int s = lane; s < ns; s += 32) mx = fmaxf(mx, lse_s[static_cast<int64_t>(s) * p.R]);
+  for (int s = tid; s < ns; s += kCombineThreads) mx = fmaxf(mx, __ldg(lse_s + static_cast<int64_t>(s) * p.R));
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-  float acc[16];
+  if ((tid & 31) == 0) red[tid >> 5] = mx;
+  __syncthreads();
+  if (tid == 0) {
+    float m = red[0];
+    for (int i = 1; i < kCombineThreads / 32; ++i) m = fmaxf(m, red[i]);
+    stat[0] = m;
+  }
+  __syncthreads();
+  mx = stat[0];
+  // weights (and their sum) into shared memory
+  float part = 0.f;
+  for (int s = tid; s < ns; s += kCombineThreads) {
+    const float w = (mx == -INFINITY) ? 0.f : __expf(__ldg(lse_s + static_cast<int64_t>(s) * p.R) - mx);
+    if (s < kCombineMaxSplitsSmem) w_s[s] = w;
+    part += w;
+  }
 #pragma unroll
-  for (int i = 0; i < 16; ++i) acc[i] = 0.f;
-  float wsum = 0.f;
-  if (mx != -INFINITY) {
-    for (int s = 0; s < ns; ++s) {
-      const float w = __expf(lse_s[static_cast<int64_t>(s) * p.R] - mx);
-      wsum += w;
-      const float4* src = reinterpret_cast<const float4*>(
-          p.ws_o + ((static_cast<int64_t>(b) * p.max_splits + s) * p.R + row) * kValueDim + lane * 16);
+  for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+  __syncthreads();
+  if ((tid & 31) == 0) red[tid >> 5] = part;
+  __syncthreads();
+  if (tid == 0) {
+    float t = 0.f;
+    for (int i = 0; i < kCombineThreads / 32; ++i) t += red[i];
+    stat[1] = t;
+  }
+  __syncthreads();
+  const float wsum = stat[1];
+  const float4* src = reinterpret_cast<const float4*>(p.ws_o + (base * p.R + row) * kValueDim) + tid;
+  const int64_t stride4 = static_cast<int64_t>(p.R) * kValueDim / 4;  // float4s between splits
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  int s = 0;
+  for (; s + 4 <= ns; s += 4) {
+    float4 v[4];
+    float w[4];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float4 v = __ldg(src + i);
-        acc[4 * i + 0] += w * v.x;
-        acc[4 * i + 1] += w * v.y;
-        acc[4 * i + 2] += w * v.z;
-        acc[4 * i + 3] += w * v.w;
-      }
+    for (int u = 0; u < 4; ++u) v[u] = __ldg(src + (s + u) * stride4);
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      w[u] = (s + u < kCombineMaxSplitsSmem) ? w_s[s + u] : __expf(__ldg(lse_s + static_cast<int64_t>(s + u) * p.R) - mx);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      acc.x += w[u] * v[u].x;
+      acc.y += w[u] * v[u].y;
+      acc.z += w[u] * v[u].z;
+      acc.w += w[u] * v[u].w;
     }
   }
+  for (; s < ns; ++s) {
+    const float4 v = __ldg(src + s * stride4);
+    const float w = (s < kCombineMaxSplitsSmem) ? w_s[s] : __expf(__ldg(lse_s + static_cast<int64_t>(s) * p.R) - mx);
+    acc.x += w * v.x;
+    acc.y += w * v.y;
+    acc.z += w * v.z;
+    acc.w += w * v.w;
+  }
   const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
-  uint32_t pk[8];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) pk[i] = pack_bf16x2(acc[2 * i] * inv, acc[2 * i + 1] * inv);
-  uint4* dst = reinterpret_cast<uint4*>(p.out + (static_cast<int64_t>(b) * p.R + row) * kValueDim + lane * 16);
-  dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-  dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
-  if (lane == 0) p.lse[static_cast<int64_t>(b) * p.R + row] = (wsum > 0.f) ? (mx + __logf(wsum)) : -INFINITY;
+  uint2 pk;
+  pk.x = pack_bf16x2(acc.x * inv, acc.y * inv);
+  pk.y = pack_bf16x2(acc.z * inv, acc.w * inv);
+  *reinterpret_cast<uint2*>(p.out + (static_cast<int64_t>(b) * p.R + row) * kValueDim + tid * 4) = pk;
+  if (tid == 0) p.lse[static_cast<int64_t>(b) * p.R + row] = (wsum > 0.f) ? (mx + __logf(wsum)) : -INFINITY;
 }
 
 // Watchdog self-test: wait on an mbarrier that nothing ever arrives on, through the same
@@ -628,8 +709,8 @@ cudaError_t launch_selftest_timeout(unsigned* status, cudaStream_t stream) {
 }
 
 cudaError_t launch_decode_combine(const DecodeParams& p, cudaStream_t stream) {
-  dim3 grid((p.R + 7) / 8, p.B);
-  decode_combine_kernel<<<grid, 256, 0, stream>>>(p);
+  dim3 grid(p.R, p.B);
+  decode_combine_kernel<<<grid, kCombineThreads, 0, stream>>>(p);
   return cudaGetLastError();
 }
 

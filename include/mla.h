@@ -120,6 +120,27 @@ int mla_decode(const mla_decode_plan_t* plan, const void* q, const void* kv_page
                float scale, float kv_scale, void* out, float* lse, void* workspace,
                size_t workspace_bytes, void* stream);
 
+/* mla_decode for callers that cannot allocate device memory.  (The pages have no
+ * counterpart: this is a library convenience.)  Some callers cannot call cudaMalloc, e.g.
+ * a serving engine whose memory manager gives every free byte of the device to its
+ * KV-cache pool at start-up and refuses later allocations, or a plugin loaded into a host
+ * program that offers it no allocator.  This entry point takes the same arguments as
+ * mla_decode minus the workspace, and uses as scratch a fixed 32 MiB buffer that lives in
+ * the library's own device data: every GPU that loads libmla holds those 32 MiB until the
+ * process exits.  It allocates and frees nothing.
+ *  - Limit: plan->workspace_bytes must be <= 32 MiB (33554432); larger plans are rejected
+ *    with MLA_ERR_WORKSPACE_TOO_SMALL before anything is enqueued.
+ *  - The first call on each device looks up the buffer's device address (with that device
+ *    current); make that first call before any stream capture.
+ *  - All calls on a device share the one buffer, which keeps the previous call's
+ *    contents.  Nothing in it has to start at zero: each call writes every partial it
+ *    later reads.  Calls whose kernels overlap on the GPU (other streams, other threads)
+ *    race on the buffer and corrupt each other's results: order them on one stream.
+ * Errors: as mla_decode, plus MLA_ERR_WORKSPACE_TOO_SMALL for plans beyond the limit. */
+int mla_decode_noalloc(const mla_decode_plan_t* plan, const void* q, const void* kv_pages,
+                       const int32_t* page_table, const int32_t* seq_lens, int q_len, int num_heads,
+                       float scale, float kv_scale, void* out, float* lse, void* stream);
+
 /* Ragged (no padding) causal MLA prefill on top of a cached prefix.
  *   q             : [total_q, H, 192] bf16; request b's n_b new tokens are rows
  *                   cu_seqlens_q[b] .. cu_seqlens_q[b+1]-1.

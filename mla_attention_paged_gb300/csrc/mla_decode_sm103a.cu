@@ -17,16 +17,18 @@
 //  * Producer warp: bf16 pools are gathered by TMA (128-byte swizzled boxes of 64
 //    columns) one 64-key tile per stage from the pages named by the page table, into a
 //    2-stage ring; e4m3 pools are gathered by bulk copies of whole page rows into a 2-stage
-//    raw ring and decoded to the bf16 swizzled tile by two dequant warps.
-//  * MMA warp (one thread): BMM1  S[rows, keys]  = Q . K^T  (M=128, N=64, K=576;
-//    rows 64..127 of the M tile are don't-care) into TMEM, double-buffered;
-//    BMM2  O^T[dims, rows] += V^T . P^T  (M=128 per 128 value columns, N=rows, K=64
-//    keys) with V^T read MN-major from the same shared-memory tile as K.  O^T lives in
-//    TMEM for the whole split (256 columns); S takes 2 x 64 columns.
-//  * Softmax warps (2): one thread per folded row reads its 64 scores from TMEM, applies
-//    the causal/length mask, keeps a running max in the log2 domain with a lazy rescale
-//    (O is rescaled only when the max grows by more than 2^8), writes P (bf16) to
-//    shared memory as the K-major B operand of BMM2.
+//    raw ring and decoded to the bf16 swizzled tile by two dequant warps (6-7).
+//  * MMA warp (uniform control flow, one elected thread issues): BMM1  S[rows, keys] =
+//    Q . K^T  (M=64, N=64, K=576) into TMEM, double-buffered; BMM2  O^T[dims, rows] +=
+//    V^T . P^T  (M=128 per 128 value columns, N=rows, K=64 keys) with V^T read MN-major
+//    from the same shared-memory tile as K.  O^T lives in TMEM for the whole split (256
+//    columns); S takes 2 x 64 columns.  GEMMs are issued in whichever order their inputs
+//    become ready.
+//  * Softmax warps (4): the M=64 accumulator puts row 16w+i in TMEM lane 32w+i, so each
+//    warp serves 16 rows, one thread per row; it reads the row's 64 scores, applies the
+//    causal/length mask, keeps a running max in the log2 domain with a lazy rescale (O is
+//    rescaled only when the max grows by more than 2^8), and writes P (bf16) to shared
+//    memory as the K-major B operand of BMM2.
 //  * Epilogue (4 warps over the 128 TMEM lanes = value columns): normalise by the row
 //    sum and write either the final bf16 output (single split) or the fp32 partial and
 //    its log-sum-exp for the combine kernel.
@@ -46,7 +48,8 @@ constexpr int kBlockBytes = 64 * 128;                // 64 rows x 128 bytes, swi
 constexpr int kTileBytes = kDimBlocks * kBlockBytes; // 73728: one bf16 64-key latent tile
 constexpr int kRawBytes = kTileKeys * kLatentDim;    // 36864: one e4m3 64-key tile
 constexpr int kStages = 2;
-constexpr int kThreads = 192;                        // warps 0-3 softmax/epilogue, 4 TMA, 5 MMA
+constexpr int kThreads = 256;        // warps 0-3 softmax/epilogue, 4 producer, 5 MMA, 6-7 e4m3 dequant
+constexpr int kDequantThreads = 64;  // warps 6-7
 
 // Shared memory map.  bf16: Q | stage0 | stage1 | P | ctrl.
 //                     e4m3: Q | raw0 | raw1 | bf16 tile | P | ctrl  (same total).
@@ -69,7 +72,7 @@ struct DecodeCtrl {
   uint64_t mma_drain;
   uint32_t tmem_base;
   int abort_flag;
-  int rescale_flag[2];
+  int rescale_flag[4];
   float alpha[kGroupRows];
   float row_scale[kGroupRows];
 };
@@ -171,18 +174,18 @@ decode_partial_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
     mbar_init(&ctrl->q_full, 1);
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&ctrl->kv_full[s], 1);
-      mbar_init(&ctrl->kv_empty[s], kFp8 ? 64 : 1);
+      mbar_init(&ctrl->kv_empty[s], kFp8 ? kDequantThreads : 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&ctrl->s_full[i], 1);
-      mbar_init(&ctrl->s_free[i], 64);
+      mbar_init(&ctrl->s_free[i], 128);
     }
     mbar_init(&ctrl->p_full, 128);
     mbar_init(&ctrl->o_done, 1);
-    mbar_init(&ctrl->tile_full, 64);
+    mbar_init(&ctrl->tile_full, kDequantThreads);
     mbar_init(&ctrl->mma_drain, 1);
     ctrl->abort_flag = 0;
-    ctrl->rescale_flag[0] = ctrl->rescale_flag[1] = 0;
+    for (int w = 0; w < 4; ++w) ctrl->rescale_flag[w] = 0;
     fence_mbarrier_init();
   }
   if (warp == 5) {
@@ -278,173 +281,171 @@ decode_partial_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
         if (last_issued[s] >= 0) drain_wait(&ctrl->kv_full[s], (last_issued[s] / kStages) & 1);
     }
   } else if (warp == 5) {
-    // ------------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      const uint32_t idesc1 = make_idesc_bf16(128, 64, false, false);
-      const uint32_t idesc2 = make_idesc_bf16(128, nq, true, false);
-      const uint32_t q_base = smem_u32(smem + kOffQ);
-      const uint32_t p_base = smem_u32(smem + kOffP);
-      bool ok = mbar_wait(&ctrl->q_full, 0, abort_flag);
-      // Descriptors are built once; each MMA advances the start-address field by a
-      // compile-time offset (addresses stay below 256 KB, so no carry leaves the field).
-      const uint64_t q_desc = make_smem_desc(q_base, 16, 1024);
-      const uint64_t p_desc = make_smem_desc(p_base, 16, 1024);
-      auto bmm1 = [&](int j) {
-        const int s = j % kStages, sb = j & 1;
-        const uint32_t kv_base = kFp8 ? smem_u32(smem + kOffTileFp8) : smem_u32(smem + kOffStages + s * kTileBytes);
-        const uint64_t k_desc = make_smem_desc(kv_base, 16, 1024);
-        const uint32_t d = tmem + kTmemS + sb * 64;
-#pragma unroll
-        for (int c = 0; c < kDimBlocks; ++c) {
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const uint64_t off = static_cast<uint64_t>((c * kBlockBytes + k * 32) >> 4);
-            umma_bf16(d, q_desc + off, k_desc + off, idesc1, (c | k) != 0);
-          }
-        }
-        umma_commit(&ctrl->s_full[sb]);
-      };
-      auto bmm2 = [&](int jj) {
-        const int s = jj % kStages;
+    // ------------------------------------------------------------------ MMA issuer (whole warp,
+    // uniform control flow; one elected thread issues each GEMM's MMAs and their commit)
+    const uint32_t idesc1 = make_idesc_bf16(64, 64, false, false);
+    const uint32_t idesc2 = make_idesc_bf16(128, nq, true, false);
+    // Descriptors are built once; each MMA advances the start-address field by a
+    // compile-time offset (addresses stay below 256 KB, so no carry leaves the field).
+    const uint64_t q_desc = make_smem_desc(smem_u32(smem + kOffQ), 16, 1024);
+    const uint64_t p_desc = make_smem_desc(smem_u32(smem + kOffP), 16, 1024);
+    auto poll = [&](uint64_t* bar, uint32_t parity) -> bool {
+      uint32_t v = 0;
+      if (lane == 0) v = mbar_test_wait(bar, parity) ? 1u : 0u;
+      return __shfl_sync(0xffffffffu, v, 0) != 0;
+    };
+    bool ok = mbar_wait(&ctrl->q_full, 0, abort_flag);
+    ok = __all_sync(0xffffffffu, ok);
+    // Issue whichever GEMM is ready: BMM2(n2) first (it frees a stage), else BMM1(n1) for a
+    // tile whose data has landed and whose S buffer is free.  BMM1 runs at most two tiles
+    // ahead of BMM2 (double-buffered S).
+    int n1 = 0, n2 = 0;
+    unsigned long long idle_since = 0;
+    while (ok && n2 < ntiles) {
+      bool progressed = false;
+      if (n2 < n1 && poll(&ctrl->p_full, n2 & 1)) {
+        tc_fence_after();
+        const int s = n2 % kStages;
         const uint32_t kv_base = kFp8 ? smem_u32(smem + kOffTileFp8) : smem_u32(smem + kOffStages + s * kTileBytes);
         // V^T: 128 value columns (two 64-column blocks, LBO apart) x 16 keys (two 8-key
         // groups, SBO apart), MN-major.  P^T: rows x 16 keys, K-major.
         const uint64_t v_desc = make_smem_desc(kv_base, kBlockBytes, 1024);
+        if (elect_one()) {
 #pragma unroll
-        for (int qc = 0; qc < 4; ++qc) {
+          for (int qc = 0; qc < 4; ++qc) {
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const uint64_t voff = static_cast<uint64_t>((2 * qc * kBlockBytes + kk * 2048) >> 4);
-            const uint64_t poff = static_cast<uint64_t>((kk * 32) >> 4);
-            umma_bf16(tmem + qc * 64, v_desc + voff, p_desc + poff, idesc2, (jj > 0 || kk > 0) ? 1u : 0u);
+            for (int kk = 0; kk < 4; ++kk) {
+              const uint64_t voff = static_cast<uint64_t>((2 * qc * kBlockBytes + kk * 2048) >> 4);
+              const uint64_t poff = static_cast<uint64_t>((kk * 32) >> 4);
+              umma_bf16(tmem + qc * 64, v_desc + voff, p_desc + poff, idesc2, (n2 > 0 || kk > 0) ? 1u : 0u);
+            }
           }
+          umma_commit(&ctrl->o_done);
+          if (!kFp8) umma_commit(&ctrl->kv_empty[s]);
         }
-        umma_commit(&ctrl->o_done);
-        if (!kFp8) umma_commit(&ctrl->kv_empty[s]);
-      };
-      // Issue whichever GEMM is ready: BMM2(n2) first (it frees a stage), else BMM1(n1)
-      // for a tile whose data has landed and whose S buffer is free.  BMM1 may run up to
-      // two tiles ahead of BMM2 (double-buffered S).
-      int n1 = 0, n2 = 0;
-      unsigned long long idle_since = 0;
-      while (ok && n2 < ntiles) {
-        bool progressed = false;
-        if (n2 < n1 && mbar_test_wait(&ctrl->p_full, n2 & 1)) {
+        __syncwarp();
+        ++n2;
+        progressed = true;
+      } else if (n1 < ntiles && n1 < n2 + 2) {
+        const int s = n1 % kStages, sb = n1 & 1;
+        const bool data = kFp8 ? poll(&ctrl->tile_full, n1 & 1) : poll(&ctrl->kv_full[s], (n1 / kStages) & 1);
+        if (data && (n1 < 2 || poll(&ctrl->s_free[sb], ((n1 - 2) >> 1) & 1))) {
           tc_fence_after();
-          bmm2(n2);
-          ++n2;
-          progressed = true;
-        } else if (n1 < ntiles && n1 < n2 + 2) {
-          const int s = n1 % kStages, sb = n1 & 1;
-          const bool data = kFp8 ? mbar_test_wait(&ctrl->tile_full, n1 & 1)
-                                 : mbar_test_wait(&ctrl->kv_full[s], (n1 / kStages) & 1);
-          if (data && (n1 < 2 || mbar_test_wait(&ctrl->s_free[sb], ((n1 - 2) >> 1) & 1))) {
-            tc_fence_after();
-            bmm1(n1);
-            ++n1;
-            progressed = true;
+          const uint32_t kv_base =
+              kFp8 ? smem_u32(smem + kOffTileFp8) : smem_u32(smem + kOffStages + s * kTileBytes);
+          const uint64_t k_desc = make_smem_desc(kv_base, 16, 1024);
+          const uint32_t d = tmem + kTmemS + sb * 64;
+          if (elect_one()) {
+#pragma unroll
+            for (int c = 0; c < kDimBlocks; ++c) {
+#pragma unroll
+              for (int k = 0; k < 4; ++k) {
+                const uint64_t off = static_cast<uint64_t>((c * kBlockBytes + k * 32) >> 4);
+                umma_bf16(d, q_desc + off, k_desc + off, idesc1, (c | k) != 0);
+              }
+            }
+            umma_commit(&ctrl->s_full[sb]);
           }
+          __syncwarp();
+          ++n1;
+          progressed = true;
         }
-        if (progressed) {
-          idle_since = 0;
-        } else {
+      }
+      if (progressed) {
+        idle_since = 0;
+      } else {
+        uint32_t give_up = 0;
+        if (lane == 0) {
           const unsigned long long now = global_timer_ns();
           if (idle_since == 0) {
             idle_since = now;
           } else if (*abort_flag || now - idle_since > kWaitLimitNs) {
             *abort_flag = 1;
-            ok = false;
+            give_up = 1;
           }
         }
+        ok = __shfl_sync(0xffffffffu, give_up, 0) == 0;
       }
-      // every MMA issued so far completes before TMEM is released
+    }
+    // every MMA issued so far completes before TMEM is released
+    if (elect_one()) {
       umma_commit(&ctrl->mma_drain);
       drain_wait(&ctrl->mma_drain, 0);
     }
     __syncwarp();
+  } else if (warp >= 6) {
+    // ------------------------------------------------------------------ e4m3 dequant (warps 6-7)
+    if (kFp8) {
+      const int td = threadIdx.x - 6 * 32;
+      auto dequant = [&](int j) -> bool {  // raw stage of tile j -> the bf16 tile
+        const int s = j % kStages;
+        bool w = mbar_wait(&ctrl->kv_full[s], (j / kStages) & 1, abort_flag);
+        w = __all_sync(0xffffffffu, w);
+        if (!w) return false;
+        dequant_tile(smem + kOffStages + s * kRawBytes, smem + kOffTileFp8, L - (kv_start + j * kTileKeys), td);
+        fence_proxy_async_smem();
+        mbar_arrive(&ctrl->tile_full);
+        mbar_arrive(&ctrl->kv_empty[s]);
+        return true;
+      };
+      bool ok = dequant(0);
+      for (int j = 0; ok && j + 1 < ntiles; ++j) {
+        // the bf16 tile is free once BMM2(j) has read it
+        bool w = mbar_wait(&ctrl->o_done, j & 1, abort_flag);
+        ok = __all_sync(0xffffffffu, w) && dequant(j + 1);
+      }
+    }
   } else {
-    // ------------------------------------------------------------------ softmax / dequant / epilogue (warps 0-3)
-    const bool is_sm = warp < 2;
-    const int r = warp * 32 + lane;  // folded row within the group (softmax warps)
-    const bool row_active = is_sm && r < nrows;
+    // ------------------------------------------------------------------ softmax + epilogue (warps 0-3)
+    // BMM1 runs with M = 64: folded row r lives in TMEM lane 32*(r/16) + r%16, so warp w
+    // owns rows 16w .. 16w+15.  Each row is split between lanes i and i+16 of its warp:
+    // lane i takes keys 0-31 of every tile, lane i+16 keys 32-63.
+    const int half = lane >> 4;
+    const bool row_lane = half == 0;  // the lane that writes per-row results
+    const int r = warp * 16 + (lane & 15);
+    const bool row_active = r < nrows;
     const int t = (row0 + r) / p.H;
     const int lim_abs = L - p.T + t;  // last visible key of this row
     const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
     float m_used = -INFINITY;
     float l_sum = 0.f;
     bool failed = false;
-    bool carry_fail = false;  // dequant warps: a wait that failed after the last barrier
-
-    auto dequant = [&](int j) -> bool {  // warps 2-3: raw stage of tile j -> bf16 tile
-      const int s = j % kStages;
-      bool w = mbar_wait(&ctrl->kv_full[s], (j / kStages) & 1, abort_flag);
-      w = !__any_sync(0xffffffffu, !w);
-      if (!w) return false;
-      dequant_tile(smem + kOffStages + s * kRawBytes, smem + kOffTileFp8, L - (kv_start + j * kTileKeys),
-                   threadIdx.x - 64);
-      fence_proxy_async_smem();
-      mbar_arrive(&ctrl->tile_full);
-      mbar_arrive(&ctrl->kv_empty[s]);
-      return true;
-    };
-    if (kFp8 && !is_sm) carry_fail = !dequant(0);
 
     for (int j = 0; j < ntiles; ++j) {
       const int sb = j & 1;
       const int k0 = kv_start + j * kTileKeys;
-      bool fail = carry_fail;
       bool need_rescale = false;
       float alpha = 1.f;
-      uint32_t packed[32];
-      if (is_sm) {
-        fail = !mbar_wait(&ctrl->s_full[sb], (j >> 1) & 1, abort_flag);
-        fail = __any_sync(0xffffffffu, fail);
-        if (!fail) {
-          tc_fence_after();
-          uint32_t sr[64];
-          tmem_ld32(tmem + lane_base + kTmemS + sb * 64, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
-          tmem_ld32(tmem + lane_base + kTmemS + sb * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
-          tmem_ld_wait();
-          tc_fence_before();
-          mbar_arrive(&ctrl->s_free[sb]);
-          const int lim = row_active ? (min(kv_end - 1, lim_abs) - k0) : -1;  // keys i <= lim are valid
-          float x[64];
-          float mt = -INFINITY;
-#pragma unroll
-          for (int i = 0; i < 64; ++i) {
-            x[i] = __uint_as_float(sr[i]) * p.scale_log2;
-            if (i <= lim) mt = fmaxf(mt, x[i]);
-          }
-          if (m_used == -INFINITY) {
-            m_used = mt;  // first contributing tile: O^T column is still zero
-          } else if (mt > m_used + kRescaleThreshold) {
-            alpha = ex2_approx(m_used - mt);
-            need_rescale = true;
-            l_sum *= alpha;
-            m_used = mt;
-          }
-          const float msub = (m_used == -INFINITY) ? 0.f : m_used;
-#pragma unroll
-          for (int i = 0; i < 64; i += 2) {
-            const float p0 = (i <= lim) ? ex2_approx(x[i] - msub) : 0.f;
-            const float p1 = (i + 1 <= lim) ? ex2_approx(x[i + 1] - msub) : 0.f;
-            l_sum += p0 + p1;
-            packed[i >> 1] = pack_bf16x2(p0, p1);
-          }
-        }
+      uint32_t packed[16];
+      bool fail = !mbar_wait(&ctrl->s_full[sb], (j >> 1) & 1, abort_flag);
+      fail = __any_sync(0xffffffffu, fail);
+      if (!fail) {
+        tc_fence_after();
+        uint32_t sr[32];
+        tmem_ld16x32bx2_32(tmem + lane_base + kTmemS + sb * 64, sr);
+        tmem_ld_wait();
+        tc_fence_before();
+        mbar_arrive(&ctrl->s_free[sb]);
+        // keys i <= lim of this lane's 32-key half are visible
+        const int lim = row_active ? (min(kv_end - 1, lim_abs) - k0 - 32 * half) : -1;
+        online_softmax_step<32, true>(sr, lim, p.scale_log2, kRescaleThreshold, m_used, l_sum, packed, alpha,
+                                      need_rescale);
       }
       if (!fail && j >= 1) {
         fail = !mbar_wait(&ctrl->o_done, (j - 1) & 1, abort_flag);
         fail = __any_sync(0xffffffffu, fail);
       }
-      if (!fail && is_sm) {
-        // P row r (64 keys, 128 bytes) into the 128-byte-swizzled K-major block
+      if (!fail) {
+        // this lane's half of P row r (32 keys = four 16-byte chunks) into the
+        // 128-byte-swizzled K-major block
         const uint32_t row_addr = smem_u32(smem + kOffP) + r * 128;
 #pragma unroll
-        for (int c = 0; c < 8; ++c)
-          st_shared_v4(row_addr + ((c ^ (r & 7)) << 4), packed[4 * c], packed[4 * c + 1], packed[4 * c + 2],
+        for (int c = 0; c < 4; ++c) {
+          const int chunk = 4 * half + c;
+          st_shared_v4(row_addr + ((chunk ^ (r & 7)) << 4), packed[4 * c], packed[4 * c + 1], packed[4 * c + 2],
                        packed[4 * c + 3]);
-        ctrl->alpha[r] = alpha;
+        }
+        if (row_lane) ctrl->alpha[r] = alpha;
         const bool any = __any_sync(0xffffffffu, need_rescale);
         if (lane == 0) ctrl->rescale_flag[warp] = any ? 1 : 0;
       }
@@ -469,7 +470,7 @@ decode_partial_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
           fence_proxy_async_smem();
         }
       }
-      if (ctrl->rescale_flag[0] | ctrl->rescale_flag[1]) {
+      if (ctrl->rescale_flag[0] | ctrl->rescale_flag[1] | ctrl->rescale_flag[2] | ctrl->rescale_flag[3]) {
         // O^T[dim, row] *= alpha[row] for all 512 value columns; this thread owns TMEM lane
         // (warp*32 + lane) of each 128-column chunk.
         tc_fence_after();
@@ -490,12 +491,6 @@ decode_partial_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
       }
       tc_fence_before();
       mbar_arrive(&ctrl->p_full);
-      if (kFp8 && !is_sm && j + 1 < ntiles) {
-        // the bf16 tile is free once BMM2(j) has completed
-        bool w = mbar_wait(&ctrl->o_done, j & 1, abort_flag);
-        w = !__any_sync(0xffffffffu, !w);
-        carry_fail = !(w && dequant(j + 1));
-      }
     }
 
     if (!failed) {
@@ -506,7 +501,8 @@ decode_partial_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
     } else {
       tc_fence_after();
       const bool final_out = (nsplit_b == 1);
-      if (is_sm) {
+      l_sum += __shfl_xor_sync(0xffffffffu, l_sum, 16);  // the two halves' partial row sums
+      if (row_lane) {
         const float lse2 = (l_sum > 0.f) ? (m_used + __log2f(l_sum)) : -INFINITY;
         const float lse_nat = lse2 * 0.69314718055994530942f;
         ctrl->row_scale[r] = (l_sum > 0.f) ? (p.v_scale / l_sum) : 0.f;

@@ -183,50 +183,79 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     }
     __syncwarp();
   } else if (warp == 5) {
-    // ------------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      const uint32_t idesc1 = make_idesc_bf16(kBM, kBN, false, false);
-      const uint32_t idesc2 = make_idesc_bf16(kBM, kDv, false, true);
-      const uint32_t q_base = smem_u32(smem + kOffQ);
-      const uint32_t p_base = smem_u32(smem + kOffP);
-      bool ok = mbar_wait(&ctrl->q_full, 0, abort_flag);
-      for (int j = 0; j <= ntiles && ok; ++j) {
-        if (j < ntiles) {
-          const int s = j % kStages, sb = j & 1;
-          ok = mbar_wait(&ctrl->kv_full[s], (j / kStages) & 1, abort_flag);
-          if (ok && j >= 2) ok = mbar_wait(&ctrl->s_free[sb], ((j - 2) >> 1) & 1, abort_flag);
-          if (!ok) break;
-          tc_fence_after();
-          const uint32_t k_base = smem_u32(smem + kOffKV + s * kStageBytes);
+    // ------------------------------------------------------------------ MMA issuer (whole warp,
+    // uniform control flow; one elected thread issues each GEMM's MMAs and their commit)
+    const uint32_t idesc1 = make_idesc_bf16(kBM, kBN, false, false);
+    const uint32_t idesc2 = make_idesc_bf16(kBM, kDv, false, true);
+    const uint64_t q_desc = make_smem_desc(smem_u32(smem + kOffQ), 16, 1024);
+    const uint64_t p_desc = make_smem_desc(smem_u32(smem + kOffP), 16, 1024);
+    auto poll = [&](uint64_t* bar, uint32_t parity) -> bool {
+      uint32_t v = 0;
+      if (lane == 0) v = mbar_test_wait(bar, parity) ? 1u : 0u;
+      return __shfl_sync(0xffffffffu, v, 0) != 0;
+    };
+    bool ok = mbar_wait(&ctrl->q_full, 0, abort_flag);
+    ok = __all_sync(0xffffffffu, ok);
+    // BMM2(n2) as soon as P(n2) is ready (it frees a stage), else BMM1(n1) once its K/V
+    // tile has landed and its S buffer is free; BMM1 runs at most two tiles ahead.
+    int n1 = 0, n2 = 0;
+    unsigned long long idle_since = 0;
+    while (ok && n2 < ntiles) {
+      bool progressed = false;
+      if (n2 < n1 && poll(&ctrl->p_full, n2 & 1)) {
+        tc_fence_after();
+        const int s = n2 % kStages;
+        // P: 128 rows x 16 keys, K-major.  V: 16 keys (two 8-key groups, SBO apart) x 128
+        // value columns (two 64-column blocks, LBO apart), MN-major.
+        const uint64_t v_desc = make_smem_desc(smem_u32(smem + kOffKV + s * kStageBytes + kKBytes), kKVBlockBytes, 1024);
+        if (elect_one()) {
 #pragma unroll
-          for (int c = 0; c < kDqk / 64; ++c) {
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              const uint64_t a = make_smem_desc(q_base + c * kQBlockBytes + k * 32, 16, 1024);
-              const uint64_t bb = make_smem_desc(k_base + c * kKVBlockBytes + k * 32, 16, 1024);
-              umma_bf16(tmem + kTmemS + sb * 64, a, bb, idesc1, (c | k) != 0);
-            }
-          }
-          umma_commit(&ctrl->s_full[sb]);
-        }
-        if (j >= 1) {
-          const int jj = j - 1, s = jj % kStages;
-          ok = mbar_wait(&ctrl->p_full, jj & 1, abort_flag);
-          if (!ok) break;
-          tc_fence_after();
-          const uint32_t v_base = smem_u32(smem + kOffKV + s * kStageBytes + kKBytes);
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            // P: 128 rows x 16 keys, K-major.  V: 16 keys (two 8-key groups, SBO apart) x 128
-            // value columns (two 64-column blocks, LBO apart), MN-major.
-            const uint64_t a = make_smem_desc(p_base + kk * 32, 16, 1024);
-            const uint64_t bb = make_smem_desc(v_base + kk * 2048, kKVBlockBytes, 1024);
-            umma_bf16(tmem + kTmemO, a, bb, idesc2, (jj > 0 || kk > 0) ? 1u : 0u);
-          }
+          for (int kk = 0; kk < 4; ++kk)
+            umma_bf16(tmem + kTmemO, p_desc + static_cast<uint64_t>((kk * 32) >> 4),
+                      v_desc + static_cast<uint64_t>((kk * 2048) >> 4), idesc2, (n2 > 0 || kk > 0) ? 1u : 0u);
           umma_commit(&ctrl->o_done);
           umma_commit(&ctrl->kv_empty[s]);
         }
+        __syncwarp();
+        ++n2;
+        progressed = true;
+      } else if (n1 < ntiles && n1 < n2 + 2) {
+        const int s = n1 % kStages, sb = n1 & 1;
+        if (poll(&ctrl->kv_full[s], (n1 / kStages) & 1) && (n1 < 2 || poll(&ctrl->s_free[sb], ((n1 - 2) >> 1) & 1))) {
+          tc_fence_after();
+          const uint64_t k_desc = make_smem_desc(smem_u32(smem + kOffKV + s * kStageBytes), 16, 1024);
+          if (elect_one()) {
+#pragma unroll
+            for (int c = 0; c < kDqk / 64; ++c) {
+#pragma unroll
+              for (int k = 0; k < 4; ++k)
+                umma_bf16(tmem + kTmemS + sb * 64, q_desc + static_cast<uint64_t>((c * kQBlockBytes + k * 32) >> 4),
+                          k_desc + static_cast<uint64_t>((c * kKVBlockBytes + k * 32) >> 4), idesc1, (c | k) != 0);
+            }
+            umma_commit(&ctrl->s_full[sb]);
+          }
+          __syncwarp();
+          ++n1;
+          progressed = true;
+        }
       }
+      if (progressed) {
+        idle_since = 0;
+      } else {
+        uint32_t give_up = 0;
+        if (lane == 0) {
+          const unsigned long long now = global_timer_ns();
+          if (idle_since == 0) {
+            idle_since = now;
+          } else if (*abort_flag || now - idle_since > kWaitLimitNs) {
+            *abort_flag = 1;
+            give_up = 1;
+          }
+        }
+        ok = __shfl_sync(0xffffffffu, give_up, 0) == 0;
+      }
+    }
+    if (elect_one()) {
       umma_commit(&ctrl->mma_drain);
       drain_wait(&ctrl->mma_drain, 0);
     }
@@ -257,29 +286,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         tc_fence_before();
         mbar_arrive(&ctrl->s_free[sb]);
         const int lim = (j >= diag_tile) ? (row_active ? vis_last - k0 : -1) : (row_active ? kBN - 1 : -1);
-        float x[64];
-        float mt = -INFINITY;
-#pragma unroll
-        for (int i = 0; i < 64; ++i) {
-          x[i] = __uint_as_float(sr[i]) * p.scale_log2;
-          if (i <= lim) mt = fmaxf(mt, x[i]);
-        }
-        if (m_used == -INFINITY) {
-          m_used = mt;
-        } else if (mt > m_used + kRescaleThreshold) {
-          alpha = ex2_approx(m_used - mt);
-          need_rescale = true;
-          l_sum *= alpha;
-          m_used = mt;
-        }
-        const float msub = (m_used == -INFINITY) ? 0.f : m_used;
-#pragma unroll
-        for (int i = 0; i < 64; i += 2) {
-          const float p0 = (i <= lim) ? ex2_approx(x[i] - msub) : 0.f;
-          const float p1 = (i + 1 <= lim) ? ex2_approx(x[i + 1] - msub) : 0.f;
-          l_sum += p0 + p1;
-          packed[i >> 1] = pack_bf16x2(p0, p1);
-        }
+        online_softmax_step<64>(sr, lim, p.scale_log2, kRescaleThreshold, m_used, l_sum, packed, alpha,
+                                need_rescale);
       }
       if (!fail && j >= 1) {
         fail = !mbar_wait(&ctrl->o_done, (j - 1) & 1, abort_flag);

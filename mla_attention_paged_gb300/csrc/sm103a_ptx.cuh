@@ -93,6 +93,18 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// One thread of a fully active warp (elect.sync): the warp keeps uniform control flow
+// while a single lane issues tcgen05 MMAs and commits.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred = 0;
+  asm volatile(
+      "{\n\t.reg .b32 r;\n\t.reg .pred p;\n\t"
+      "elect.sync r|p, 0xffffffff;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(pred));
+  return pred != 0;
+}
+
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
@@ -241,6 +253,21 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
       : "memory");
 }
 
+// Shape 16x32bx2 with a 32-column split: thread i (< 16) reads lane (lane_base + i)
+// columns [c, c+32); thread i+16 reads the same lane, columns [c+32, c+64).  Used for
+// accumulators whose rows occupy lanes 0-15 of each 32-lane quarter (M = 64).
+__device__ __forceinline__ void tmem_ld16x32bx2_32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.16x32bx2.x32.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32], 32;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+}
+
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
@@ -257,6 +284,65 @@ __device__ __forceinline__ float ex2_approx(float x) {
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// One online-softmax step for one row over N raw scores s[] (fp32 bit patterns of q.k).
+// Keys i <= lim are visible (lim >= N-1: all).  The running max m_used lives in the log2
+// domain of the scaled score (x = s * scale_log2); it only moves when a tile's max exceeds
+// it by more than `threshold`, and then alpha = 2^(m_old - m_new) rescales l_sum here and
+// must rescale the row's O accumulator (need_rescale).  P = 2^(x - m_used) is returned as
+// packed bf16 pairs; l_sum accumulates the fp32 P.
+// kPairMax: the row is split between lanes l and l^16 (each holds N of its scores); the
+// tile max is exchanged between them, so both take identical running-state decisions and
+// each keeps the partial row sum of its own half.
+template <int N, bool kPairMax = false>
+__device__ __forceinline__ void online_softmax_step(const uint32_t (&s)[N], int lim, float scale_log2,
+                                                    float threshold, float& m_used, float& l_sum,
+                                                    uint32_t (&packed)[N / 2], float& alpha, bool& need_rescale) {
+  const bool all = lim >= N - 1;
+  float mx = -INFINITY;
+  if (all) {
+#pragma unroll
+    for (int i = 0; i < N; ++i) mx = fmaxf(mx, __uint_as_float(s[i]));
+  } else {
+#pragma unroll
+    for (int i = 0; i < N; ++i)
+      if (i <= lim) mx = fmaxf(mx, __uint_as_float(s[i]));
+  }
+  if (kPairMax) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+  const float mt = mx * scale_log2;  // scale > 0: max commutes with the scaling; -inf stays -inf
+  alpha = 1.f;
+  need_rescale = false;
+  if (m_used == -INFINITY) {
+    m_used = mt;  // first contributing tile: nothing accumulated yet
+  } else if (mt > m_used + threshold) {
+    alpha = ex2_approx(m_used - mt);
+    need_rescale = true;
+    l_sum *= alpha;
+    m_used = mt;
+  }
+  const float neg_m = (m_used == -INFINITY) ? 0.f : -m_used;
+  float l0 = 0.f, l1 = 0.f;
+  if (all) {
+#pragma unroll
+    for (int i = 0; i < N; i += 2) {
+      const float p0 = ex2_approx(fmaf(__uint_as_float(s[i]), scale_log2, neg_m));
+      const float p1 = ex2_approx(fmaf(__uint_as_float(s[i + 1]), scale_log2, neg_m));
+      l0 += p0;
+      l1 += p1;
+      packed[i >> 1] = pack_bf16x2(p0, p1);
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < N; i += 2) {
+      const float p0 = (i <= lim) ? ex2_approx(fmaf(__uint_as_float(s[i]), scale_log2, neg_m)) : 0.f;
+      const float p1 = (i + 1 <= lim) ? ex2_approx(fmaf(__uint_as_float(s[i + 1]), scale_log2, neg_m)) : 0.f;
+      l0 += p0;
+      l1 += p1;
+      packed[i >> 1] = pack_bf16x2(p0, p1);
+    }
+  }
+  l_sum += l0 + l1;
 }
 
 __device__ __forceinline__ void st_shared_v4(uint32_t saddr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {

@@ -194,7 +194,7 @@ int mla_decode_plan(int batch, const int32_t* seq_lens_host, int q_len, int num_
   if (pl.max_splits > 65535) return MLA_ERR_UNSUPPORTED;
   if (pl.max_splits > 1) {
     const size_t parts = static_cast<size_t>(batch) * pl.max_splits * pl.rows;
-    pl.workspace_bytes = 256 + parts * kValueDim * sizeof(float) + parts * sizeof(float);
+    pl.workspace_bytes = 256 + parts * kValueDim * sizeof(__nv_bfloat16) + parts * sizeof(float);
   } else {
     pl.workspace_bytes = 0;
   }
@@ -261,8 +261,8 @@ int mla_decode(const mla_decode_plan_t* plan, const void* q, const void* kv_page
   p.lse = lse;
   if (plan->max_splits > 1) {
     const size_t parts = static_cast<size_t>(plan->batch) * plan->max_splits * plan->rows;
-    p.ws_o = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + 256);
-    p.ws_lse = p.ws_o + parts * kValueDim;
+    p.ws_o = reinterpret_cast<__nv_bfloat16*>(static_cast<uint8_t*>(workspace) + 256);
+    p.ws_lse = reinterpret_cast<float*>(p.ws_o + parts * kValueDim);
   }
   p.status = status;
   cudaStream_t s = static_cast<cudaStream_t>(stream);

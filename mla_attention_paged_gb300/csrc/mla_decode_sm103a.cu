@@ -25,13 +25,13 @@
 //    columns); S takes 2 x 64 columns.  GEMMs are issued in whichever order their inputs
 //    become ready.
 //  * Softmax warps (4): the M=64 accumulator puts row 16w+i in TMEM lane 32w+i, so each
-//    warp serves 16 rows, one thread per row; it reads the row's 64 scores, applies the
-//    causal/length mask, keeps a running max in the log2 domain with a lazy rescale (O is
-//    rescaled only when the max grows by more than 2^8), and writes P (bf16) to shared
-//    memory as the K-major B operand of BMM2.
+//    warp serves 16 rows, each row split between lanes i and i+16 (32 keys apiece); it
+//    applies the causal/length mask, keeps a running max in the log2 domain with a lazy
+//    rescale (O is rescaled only when the max grows by more than 2^8), and writes P
+//    (bf16) to shared memory as the K-major B operand of BMM2.
 //  * Epilogue (4 warps over the 128 TMEM lanes = value columns): normalise by the row
-//    sum and write either the final bf16 output (single split) or the fp32 partial and
-//    its log-sum-exp for the combine kernel.
+//    sum and write either the final bf16 output (single split) or the bf16 partial and
+//    its fp32 log-sum-exp for the combine kernel.
 // Every wait is bounded; on expiry the CTA records a timeout in the status word, drains
 // its in-flight copies and MMAs, frees TMEM and returns.
 #include <cuda_fp16.h>
@@ -48,6 +48,7 @@ constexpr int kBlockBytes = 64 * 128;                // 64 rows x 128 bytes, swi
 constexpr int kTileBytes = kDimBlocks * kBlockBytes; // 73728: one bf16 64-key latent tile
 constexpr int kRawBytes = kTileKeys * kLatentDim;    // 36864: one e4m3 64-key tile
 constexpr int kStages = 2;
+constexpr int kPrefetchTiles = 4;  // L2 prefetch distance beyond the shared-memory ring
 constexpr int kThreads = 256;        // warps 0-3 softmax/epilogue, 4 producer, 5 MMA, 6-7 e4m3 dequant
 constexpr int kDequantThreads = 64;  // warps 6-7
 
@@ -220,6 +221,30 @@ decode_partial_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
       for (int c = 0; c < kDimBlocks; ++c)
         tma_load_2d(smem + kOffQ + c * kBlockBytes, &tm_q, &ctrl->q_full, c * 64, b * p.R + row0, pol_q);
     }
+    // L2 prefetch runs kPrefetch tiles ahead of the shared-memory ring, so a stage's TMA
+    // load is served from L2 rather than waiting a full HBM round trip.  Page ids come from
+    // the two 32-entry windows (cur, nxt); the lookahead stays inside them.
+    const uint32_t row_bytes = kFp8 ? kLatentDim : kLatentDim * 2;
+    const int prefetch_dist = min(kPrefetchTiles, 32 / sub - 1);
+    auto pid_at = [&](int pi) -> int {  // page id of page index pi in [batch_base, batch_base + 64)
+      const int rel = pi - batch_base;
+      const int a = __shfl_sync(0xffffffffu, cur, rel & 31);
+      const int c = __shfl_sync(0xffffffffu, nxt, rel & 31);
+      return rel < 32 ? a : c;
+    };
+    auto prefetch_tile = [&](int jt) {  // warp-uniform call
+      const int k0t = kv_start + jt * kTileKeys;
+      const int pg = k0t / P;
+      const int np = (P < kTileKeys) ? ((min(k0t + kTileKeys, L) - 1) / P - pg + 1) : 1;
+      for (int pp = 0; pp < sub; ++pp) {
+        const int pid = pid_at(pg + pp);
+        if (lane == 0 && pp < np) {
+          const int rip = (P > kTileKeys) ? (k0t % P) : 0;
+          prefetch_l2_bulk(p.kv_pool + (static_cast<int64_t>(pid) * P + rip) * row_bytes, box_rows * row_bytes);
+        }
+      }
+    };
+    for (int jt = kStages; jt < min(ntiles, kStages + prefetch_dist); ++jt) prefetch_tile(jt);
     int last_issued[kStages] = {-1, -1};
     bool ok = true;
     for (int j = 0; j < ntiles; ++j) {
@@ -250,6 +275,7 @@ decode_partial_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
           pids[pp] = 0;
         }
       }
+      if (j + kStages + prefetch_dist < ntiles) prefetch_tile(j + kStages + prefetch_dist);
       if (lane == 0) {
         const int row_in_page = (P > kTileKeys) ? (k0 % P) : 0;
         if (!kFp8) {
@@ -515,9 +541,10 @@ decode_partial_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
         }
       }
       named_bar_sync(1, 128);
-      // Normalised O is transposed through shared memory (the KV stage area is free once
-      // the last BMM2 has completed) so that global stores are whole 16-byte row chunks.
-      float* stage_f = reinterpret_cast<float*>(smem + kOffStages);                   // [64][512] fp32
+      // Normalised O (bf16) is transposed through shared memory (the KV stage area is free
+      // once the last BMM2 has completed) so that global stores are whole 16-byte row
+      // chunks.  Split partials are kept in bf16 too: they are averaged by the combine and
+      // rounded to the bf16 output anyway, and half the bytes is half the extra traffic.
       __nv_bfloat16* stage_h = reinterpret_cast<__nv_bfloat16*>(smem + kOffStages);   // [64][512] bf16
 #pragma unroll 1
       for (int qc = 0; qc < 4; ++qc) {
@@ -530,30 +557,19 @@ decode_partial_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
             const int rr = hh * 32 + i;
-            const float val = __uint_as_float(v[i]) * ctrl->row_scale[rr];
-            if (final_out)
-              stage_h[rr * kValueDim + dim] = __float2bfloat16_rn(val);
-            else
-              stage_f[rr * kValueDim + dim] = val;
+            stage_h[rr * kValueDim + dim] = __float2bfloat16_rn(__uint_as_float(v[i]) * ctrl->row_scale[rr]);
           }
         }
       }
       named_bar_sync(1, 128);
-      if (final_out) {
-        constexpr int kChunksPerRow = kValueDim * 2 / 16;
-        for (int c = threadIdx.x; c < nrows * kChunksPerRow; c += 128) {
-          const int rr = c / kChunksPerRow, cc = c % kChunksPerRow;
-          const uint4 v = *reinterpret_cast<const uint4*>(stage_h + rr * kValueDim + cc * 8);
-          *reinterpret_cast<uint4*>(p.out + (static_cast<int64_t>(b) * p.R + row0 + rr) * kValueDim + cc * 8) = v;
-        }
-      } else {
-        constexpr int kChunksPerRow = kValueDim * 4 / 16;
-        float* dst = p.ws_o + ((static_cast<int64_t>(b) * p.max_splits + split) * p.R + row0) * kValueDim;
-        for (int c = threadIdx.x; c < nrows * kChunksPerRow; c += 128) {
-          const int rr = c / kChunksPerRow, cc = c % kChunksPerRow;
-          const float4 v = *reinterpret_cast<const float4*>(stage_f + rr * kValueDim + cc * 4);
-          *reinterpret_cast<float4*>(dst + rr * kValueDim + cc * 4) = v;
-        }
+      constexpr int kChunksPerRow = kValueDim * 2 / 16;
+      __nv_bfloat16* dst = final_out
+                               ? p.out + (static_cast<int64_t>(b) * p.R + row0) * kValueDim
+                               : p.ws_o + ((static_cast<int64_t>(b) * p.max_splits + split) * p.R + row0) * kValueDim;
+      for (int c = threadIdx.x; c < nrows * kChunksPerRow; c += 128) {
+        const int rr = c / kChunksPerRow, cc = c % kChunksPerRow;
+        const uint4 v = *reinterpret_cast<const uint4*>(stage_h + rr * kValueDim + cc * 8);
+        *reinterpret_cast<uint4*>(dst + rr * kValueDim + cc * 8) = v;
       }
     }
   }
@@ -622,34 +638,30 @@ __global__ void __launch_bounds__(kCombineThreads) decode_combine_kernel(const D
   }
   __syncthreads();
   const float wsum = stat[1];
-  const float4* src = reinterpret_cast<const float4*>(p.ws_o + (base * p.R + row) * kValueDim) + tid;
-  const int64_t stride4 = static_cast<int64_t>(p.R) * kValueDim / 4;  // float4s between splits
+  // thread tid owns value columns 4*tid .. 4*tid+3: one 8-byte bf16 load per split
+  const uint2* src = reinterpret_cast<const uint2*>(p.ws_o + (base * p.R + row) * kValueDim) + tid;
+  const int64_t stride2 = static_cast<int64_t>(p.R) * kValueDim / 4;  // uint2s between splits
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  auto fma4 = [&](float w, uint2 v) {
+    const float2 lo = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v.x));
+    const float2 hi = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v.y));
+    acc.x += w * lo.x;
+    acc.y += w * lo.y;
+    acc.z += w * hi.x;
+    acc.w += w * hi.y;
+  };
+  auto weight = [&](int s) -> float {
+    return (s < kCombineMaxSplitsSmem) ? w_s[s] : __expf(__ldg(lse_s + static_cast<int64_t>(s) * p.R) - mx);
+  };
   int s = 0;
-  for (; s + 4 <= ns; s += 4) {
-    float4 v[4];
-    float w[4];
+  for (; s + 8 <= ns; s += 8) {  // eight independent loads in flight per thread
+    uint2 v[8];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) v[u] = __ldg(src + (s + u) * stride4);
+    for (int u = 0; u < 8; ++u) v[u] = __ldg(src + (s + u) * stride2);
 #pragma unroll
-    for (int u = 0; u < 4; ++u)
-      w[u] = (s + u < kCombineMaxSplitsSmem) ? w_s[s + u] : __expf(__ldg(lse_s + static_cast<int64_t>(s + u) * p.R) - mx);
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      acc.x += w[u] * v[u].x;
-      acc.y += w[u] * v[u].y;
-      acc.z += w[u] * v[u].z;
-      acc.w += w[u] * v[u].w;
-    }
+    for (int u = 0; u < 8; ++u) fma4(weight(s + u), v[u]);
   }
-  for (; s < ns; ++s) {
-    const float4 v = __ldg(src + s * stride4);
-    const float w = (s < kCombineMaxSplitsSmem) ? w_s[s] : __expf(__ldg(lse_s + static_cast<int64_t>(s) * p.R) - mx);
-    acc.x += w * v.x;
-    acc.y += w * v.y;
-    acc.z += w * v.z;
-    acc.w += w * v.w;
-  }
+  for (; s < ns; ++s) fma4(weight(s), __ldg(src + s * stride2));
   const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
   uint2 pk;
   pk.x = pack_bf16x2(acc.x * inv, acc.y * inv);

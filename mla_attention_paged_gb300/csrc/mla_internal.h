@@ -30,7 +30,7 @@ struct DecodeParams {
   const uint8_t* kv_pool;       // pool base (e4m3 path copies raw pages from here)
   __nv_bfloat16* out;           // [B, T, H, 512]
   float* lse;                   // [B, T, H]
-  float* ws_o;                  // [B, max_splits, R, 512] partial outputs (normalised)
+  __nv_bfloat16* ws_o;          // [B, max_splits, R, 512] partial outputs (normalised, bf16)
   float* ws_lse;                // [B, max_splits, R] partial log-sum-exp (natural log)
   unsigned* status;             // device status word
 };

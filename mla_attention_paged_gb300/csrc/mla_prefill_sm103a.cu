@@ -13,14 +13,16 @@
 //
 // Design on sm_103a (one CTA per (128-row query block, head, request), one CTA per SM):
 //  * Producer warp: TMA (128-byte swizzled, 3-D maps over [rows, heads, columns]) loads the
-//    query block once and streams 64-key K (192 wide) and V (128 wide) tiles of the same
-//    head through a 3-stage mbarrier ring.
-//  * MMA warp (one thread): S = Q . K^T (M=128 rows, N=64 keys, K=192) into a double-
-//    buffered TMEM S; O += P . V (M=128, N=128, K=64; V read MN-major) into TMEM O.
+//    query block once and streams 128-key K (192 wide) and V (128 wide) tiles of the same
+//    head through a 2-stage mbarrier ring.
+//  * MMA warp (uniform control flow, one elected thread issues): S = Q . K^T (M=128 rows,
+//    N=128 keys, K=192) into one of two TMEM S buffers; O += P . V (M=128, N=128, K=128)
+//    with P read straight from TMEM (the A operand) and V MN-major from shared memory.
 //  * Softmax warps (4, one thread per query row = TMEM lane): causal mask offset by the
 //    prefix only on tiles that cross the diagonal, running max in the log2 domain with a
 //    lazy rescale of the thread's own O row (only when the max grows by more than 2^8),
-//    exp2 on the MUFU unit, P (bf16) to shared memory as the K-major A operand.
+//    exp2 on the MUFU unit; P (bf16) is written back into the first 64 columns of the
+//    tile's own S buffer, so it never touches shared memory.
 //  * Epilogue: O / l to bf16 and the natural-log LSE, straight from TMEM.
 // Every wait is bounded; on expiry the CTA records a timeout in the status word, drains
 // its in-flight copies and MMAs, frees TMEM and returns.
@@ -33,29 +35,28 @@ namespace {
 constexpr int kDqk = 192;
 constexpr int kDv = 128;
 constexpr int kBM = 128;     // query rows per CTA
-constexpr int kBN = 64;      // keys per tile
-constexpr int kStages = 3;
+constexpr int kBN = 128;     // keys per tile
+constexpr int kBox = 64;     // rows per TMA box (the tensor maps' box height)
+constexpr int kStages = 2;
 constexpr int kThreads = 192;
 
 constexpr int kQBlockBytes = kBM * 128;                // 16 KB per 64-column block
 constexpr int kQBytes = (kDqk / 64) * kQBlockBytes;    // 48 KB
-constexpr int kKVBlockBytes = kBN * 128;               // 8 KB
-constexpr int kKBytes = (kDqk / 64) * kKVBlockBytes;   // 24 KB
-constexpr int kVBytes = (kDv / 64) * kKVBlockBytes;    // 16 KB
-constexpr int kStageBytes = kKBytes + kVBytes;         // 40 KB
-constexpr int kPBytes = kBM * 128;                     // 16 KB: 128 rows x 64 keys bf16
+constexpr int kKVBlockBytes = kBN * 128;               // 16 KB
+constexpr int kKBytes = (kDqk / 64) * kKVBlockBytes;   // 48 KB
+constexpr int kVBytes = (kDv / 64) * kKVBlockBytes;    // 32 KB
+constexpr int kStageBytes = kKBytes + kVBytes;         // 80 KB
 
 constexpr int kOffQ = 0;
 constexpr int kOffKV = kOffQ + kQBytes;
-constexpr int kOffP = kOffKV + kStages * kStageBytes;
-constexpr int kOffCtrl = kOffP + kPBytes;
+constexpr int kOffCtrl = kOffKV + kStages * kStageBytes;
 
 struct PrefillCtrl {
   uint64_t q_full;
   uint64_t kv_full[kStages];
   uint64_t kv_empty[kStages];
   uint64_t s_full[2];
-  uint64_t s_free[2];
+  uint64_t s_consumed[2];  // BMM2 has read the P held in this S buffer
   uint64_t p_full;
   uint64_t o_done;
   uint64_t mma_drain;
@@ -65,7 +66,7 @@ struct PrefillCtrl {
 constexpr int kSmemBytes = kOffCtrl + 1024 + 1024;
 static_assert(sizeof(PrefillCtrl) <= 1024, "control block");
 
-constexpr uint32_t kTmemCols = 256;  // O at 0..127, S buffers at 128 and 192
+constexpr uint32_t kTmemCols = 512;  // O at 0..127, S/P buffers at 128..255 and 256..383
 constexpr uint32_t kTmemO = 0;
 constexpr uint32_t kTmemS = 128;
 constexpr float kRescaleThreshold = 8.0f;
@@ -88,6 +89,18 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
   while (!mbar_try_wait(bar, parity)) {
     if (global_timer_ns() - t0 > kWaitLimitNs) return;
   }
+}
+
+// D[tmem] (+)= A[tmem] * B[smem desc]: the A operand (M rows x 16 K elements, bf16 packed
+// two per 32-bit column, row = lane) is read from Tensor Memory.
+__device__ __forceinline__ void umma_ts_bf16(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                             uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -127,7 +140,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&ctrl->s_full[i], 1);
-      mbar_init(&ctrl->s_free[i], 128);
+      mbar_init(&ctrl->s_consumed[i], 1);
     }
     mbar_init(&ctrl->p_full, 128);
     mbar_init(&ctrl->o_done, 1);
@@ -156,9 +169,9 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       const uint64_t pol_q = policy_evict_first();
       const uint64_t pol_kv = policy_evict_last();  // re-read by the other query blocks of this head
       mbar_arrive_expect_tx(&ctrl->q_full, kQBytes);
-      for (int c = 0; c < kDqk / 64; ++c)
+      for (int c = 0; c < kDqk / 64; ++c)  // the query map's box is 64 columns x 128 rows
         tma_load_3d(smem + kOffQ + c * kQBlockBytes, &tm_q, &ctrl->q_full, c * 64, h, q_start + row_begin, pol_q);
-      int last_issued[kStages] = {-1, -1, -1};
+      int last_issued[kStages] = {-1, -1};
       bool ok = true;
       for (int j = 0; j < ntiles; ++j) {
         const int s = j % kStages;
@@ -169,10 +182,14 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         uint8_t* st = smem + kOffKV + s * kStageBytes;
         const int row = kv_start + j * kBN;
         mbar_arrive_expect_tx(&ctrl->kv_full[s], kStageBytes);
-        for (int c = 0; c < kDqk / 64; ++c)
-          tma_load_3d(st + c * kKVBlockBytes, &tm_k, &ctrl->kv_full[s], c * 64, h, row, pol_kv);
-        for (int c = 0; c < kDv / 64; ++c)
-          tma_load_3d(st + kKBytes + c * kKVBlockBytes, &tm_v, &ctrl->kv_full[s], c * 64, h, row, pol_kv);
+        for (int hb = 0; hb < kBN / kBox; ++hb) {
+          for (int c = 0; c < kDqk / 64; ++c)
+            tma_load_3d(st + c * kKVBlockBytes + hb * kBox * 128, &tm_k, &ctrl->kv_full[s], c * 64, h,
+                        row + hb * kBox, pol_kv);
+          for (int c = 0; c < kDv / 64; ++c)
+            tma_load_3d(st + kKBytes + c * kKVBlockBytes + hb * kBox * 128, &tm_v, &ctrl->kv_full[s], c * 64, h,
+                        row + hb * kBox, pol_kv);
+        }
         last_issued[s] = j;
       }
       if (!ok) {
@@ -184,11 +201,10 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     __syncwarp();
   } else if (warp == 5) {
     // ------------------------------------------------------------------ MMA issuer (whole warp,
-    // uniform control flow; one elected thread issues each GEMM's MMAs and their commit)
+    // uniform control flow; one elected thread issues each GEMM's MMAs and their commits)
     const uint32_t idesc1 = make_idesc_bf16(kBM, kBN, false, false);
     const uint32_t idesc2 = make_idesc_bf16(kBM, kDv, false, true);
     const uint64_t q_desc = make_smem_desc(smem_u32(smem + kOffQ), 16, 1024);
-    const uint64_t p_desc = make_smem_desc(smem_u32(smem + kOffP), 16, 1024);
     auto poll = [&](uint64_t* bar, uint32_t parity) -> bool {
       uint32_t v = 0;
       if (lane == 0) v = mbar_test_wait(bar, parity) ? 1u : 0u;
@@ -196,32 +212,36 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     };
     bool ok = mbar_wait(&ctrl->q_full, 0, abort_flag);
     ok = __all_sync(0xffffffffu, ok);
-    // BMM2(n2) as soon as P(n2) is ready (it frees a stage), else BMM1(n1) once its K/V
-    // tile has landed and its S buffer is free; BMM1 runs at most two tiles ahead.
+    // BMM2(n2) as soon as P(n2) is ready (it frees a K/V stage and an S buffer), else
+    // BMM1(n1) once its K/V tile has landed and BMM2(n1-2) has read the P in its S buffer.
     int n1 = 0, n2 = 0;
     unsigned long long idle_since = 0;
     while (ok && n2 < ntiles) {
       bool progressed = false;
       if (n2 < n1 && poll(&ctrl->p_full, n2 & 1)) {
         tc_fence_after();
-        const int s = n2 % kStages;
-        // P: 128 rows x 16 keys, K-major.  V: 16 keys (two 8-key groups, SBO apart) x 128
-        // value columns (two 64-column blocks, LBO apart), MN-major.
-        const uint64_t v_desc = make_smem_desc(smem_u32(smem + kOffKV + s * kStageBytes + kKBytes), kKVBlockBytes, 1024);
+        const int s = n2 % kStages, sb = n2 & 1;
+        // P: 128 rows x 16 keys per MMA, 8 TMEM columns apart.  V: 16 keys (two 8-key groups,
+        // SBO apart) x 128 value columns (two 64-column blocks, LBO apart), MN-major.
+        const uint64_t v_desc =
+            make_smem_desc(smem_u32(smem + kOffKV + s * kStageBytes + kKBytes), kKVBlockBytes, 1024);
+        const uint32_t p_tmem = tmem + kTmemS + sb * 128;
         if (elect_one()) {
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            umma_bf16(tmem + kTmemO, p_desc + static_cast<uint64_t>((kk * 32) >> 4),
-                      v_desc + static_cast<uint64_t>((kk * 2048) >> 4), idesc2, (n2 > 0 || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < kBN / 16; ++kk)
+            umma_ts_bf16(tmem + kTmemO, p_tmem + kk * 8, v_desc + static_cast<uint64_t>((kk * 2048) >> 4), idesc2,
+                         (n2 > 0 || kk > 0) ? 1u : 0u);
           umma_commit(&ctrl->o_done);
           umma_commit(&ctrl->kv_empty[s]);
+          umma_commit(&ctrl->s_consumed[sb]);
         }
         __syncwarp();
         ++n2;
         progressed = true;
       } else if (n1 < ntiles && n1 < n2 + 2) {
         const int s = n1 % kStages, sb = n1 & 1;
-        if (poll(&ctrl->kv_full[s], (n1 / kStages) & 1) && (n1 < 2 || poll(&ctrl->s_free[sb], ((n1 - 2) >> 1) & 1))) {
+        if (poll(&ctrl->kv_full[s], (n1 / kStages) & 1) &&
+            (n1 < 2 || poll(&ctrl->s_consumed[sb], ((n1 - 2) >> 1) & 1))) {
           tc_fence_after();
           const uint64_t k_desc = make_smem_desc(smem_u32(smem + kOffKV + s * kStageBytes), 16, 1024);
           if (elect_one()) {
@@ -229,7 +249,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             for (int c = 0; c < kDqk / 64; ++c) {
 #pragma unroll
               for (int k = 0; k < 4; ++k)
-                umma_bf16(tmem + kTmemS + sb * 64, q_desc + static_cast<uint64_t>((c * kQBlockBytes + k * 32) >> 4),
+                umma_bf16(tmem + kTmemS + sb * 128, q_desc + static_cast<uint64_t>((c * kQBlockBytes + k * 32) >> 4),
                           k_desc + static_cast<uint64_t>((c * kKVBlockBytes + k * 32) >> 4), idesc1, (c | k) != 0);
             }
             umma_commit(&ctrl->s_full[sb]);
@@ -272,49 +292,44 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     for (int j = 0; j < ntiles; ++j) {
       const int sb = j & 1;
       const int k0 = j * kBN;
+      const uint32_t s_tmem = tmem + lane_base + kTmemS + sb * 128;
       bool fail = !mbar_wait(&ctrl->s_full[sb], (j >> 1) & 1, abort_flag);
       fail = __any_sync(0xffffffffu, fail);
-      uint32_t packed[32];
       bool need_rescale = false;
       float alpha = 1.f;
       if (!fail) {
         tc_fence_after();
-        uint32_t sr[64];
-        tmem_ld32(tmem + lane_base + kTmemS + sb * 64, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
-        tmem_ld32(tmem + lane_base + kTmemS + sb * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
+        uint32_t sr[128];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tmem_ld32(s_tmem + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32 * c]));
         tmem_ld_wait();
-        tc_fence_before();
-        mbar_arrive(&ctrl->s_free[sb]);
         const int lim = (j >= diag_tile) ? (row_active ? vis_last - k0 : -1) : (row_active ? kBN - 1 : -1);
-        online_softmax_step<64>(sr, lim, p.scale_log2, kRescaleThreshold, m_used, l_sum, packed, alpha,
-                                need_rescale);
+        uint32_t packed[64];
+        online_softmax_step<128>(sr, lim, p.scale_log2, kRescaleThreshold, m_used, l_sum, packed, alpha,
+                                 need_rescale);
+        // P (bf16 pairs) over the first 64 columns of this tile's S buffer
+        tmem_st32(s_tmem, *reinterpret_cast<uint32_t(*)[32]>(&packed[0]));
+        tmem_st32(s_tmem + 32, *reinterpret_cast<uint32_t(*)[32]>(&packed[32]));
       }
       if (!fail && j >= 1) {
+        // O may only be rescaled once BMM2(j-1) has finished accumulating into it
         fail = !mbar_wait(&ctrl->o_done, (j - 1) & 1, abort_flag);
         fail = __any_sync(0xffffffffu, fail);
       }
-      if (!fail) {
-        const uint32_t row_addr = smem_u32(smem + kOffP) + r * 128;
+      if (!fail && __any_sync(0xffffffffu, need_rescale) && j >= 1) {
+        // rescale this thread's own O row (TMEM lane r, 128 columns)
+        tc_fence_after();
 #pragma unroll
-        for (int c = 0; c < 8; ++c)
-          st_shared_v4(row_addr + ((c ^ (r & 7)) << 4), packed[4 * c], packed[4 * c + 1], packed[4 * c + 2],
-                       packed[4 * c + 3]);
-        if (__any_sync(0xffffffffu, need_rescale) && j >= 1) {
-          // rescale this thread's own O row (TMEM lane r, 128 columns)
-          tc_fence_after();
+        for (int c = 0; c < 4; ++c) {
+          uint32_t v[32];
+          tmem_ld32(tmem + lane_base + kTmemO + c * 32, v);
+          tmem_ld_wait();
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            uint32_t v[32];
-            tmem_ld32(tmem + lane_base + kTmemO + c * 32, v);
-            tmem_ld_wait();
-#pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
-            tmem_st32(tmem + lane_base + kTmemO + c * 32, v);
-          }
-          tmem_st_wait();
+          for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
+          tmem_st32(tmem + lane_base + kTmemO + c * 32, v);
         }
       }
-      fence_proxy_async_smem();
+      tmem_st_wait();
       if (bar_or(1, 128, fail || (*abort_flag != 0))) {
         failed = true;
         break;

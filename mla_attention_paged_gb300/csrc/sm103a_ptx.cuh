@@ -144,6 +144,12 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
       : "memory");
 }
 
+// Bulk prefetch of a contiguous global range into L2 (16-byte aligned, multiple of 16 bytes).
+__device__ __forceinline__ void prefetch_l2_bulk(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(src)), "r"(bytes)
+               : "memory");
+}
+
 // L2 cache policies (createpolicy): streamed-once data vs. data re-read by other CTAs.
 __device__ __forceinline__ uint64_t policy_evict_first() {
   uint64_t p;

@@ -48,7 +48,7 @@ constexpr int kBlockBytes = 64 * 128;                // 64 rows x 128 bytes, swi
 constexpr int kTileBytes = kDimBlocks * kBlockBytes; // 73728: one bf16 64-key latent tile
 constexpr int kRawBytes = kTileKeys * kLatentDim;    // 36864: one e4m3 64-key tile
 constexpr int kStages = 2;
-constexpr int kPrefetchTiles = 4;  // L2 prefetch distance beyond the shared-memory ring
+constexpr int kPrefetchTiles = 4;  // e4m3 L2 prefetch distance beyond the shared-memory ring
 constexpr int kThreads = 256;        // warps 0-3 softmax/epilogue, 4 producer, 5 MMA, 6-7 e4m3 dequant
 constexpr int kDequantThreads = 64;  // warps 6-7
 
@@ -74,8 +74,8 @@ struct DecodeCtrl {
   uint32_t tmem_base;
   int abort_flag;
   int rescale_flag[4];
-  float alpha[kGroupRows];
-  float row_scale[kGroupRows];
+  alignas(16) float alpha[kGroupRows];
+  alignas(16) float row_scale[kGroupRows];
 };
 constexpr int kSmemBytes = kOffCtrl + 1024 + 1024;  // + control block + alignment slack
 static_assert(sizeof(DecodeCtrl) <= 1024, "control block");
@@ -221,11 +221,13 @@ decode_partial_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
       for (int c = 0; c < kDimBlocks; ++c)
         tma_load_2d(smem + kOffQ + c * kBlockBytes, &tm_q, &ctrl->q_full, c * 64, b * p.R + row0, pol_q);
     }
-    // L2 prefetch runs kPrefetch tiles ahead of the shared-memory ring, so a stage's TMA
-    // load is served from L2 rather than waiting a full HBM round trip.  Page ids come from
-    // the two 32-entry windows (cur, nxt); the lookahead stays inside them.
+    // e4m3 only: an L2 prefetch runs kPrefetchTiles tiles ahead of the shared-memory ring
+    // (that path is bound by the dequant warps, and the prefetch hides part of each raw
+    // tile's HBM round trip).  The bf16 path measured faster without it: the extra requests
+    // queue ahead of the ring's own loads.  Page ids come from the two 32-entry windows
+    // (cur, nxt); the lookahead stays inside them.
     const uint32_t row_bytes = kFp8 ? kLatentDim : kLatentDim * 2;
-    const int prefetch_dist = min(kPrefetchTiles, 32 / sub - 1);
+    const int prefetch_dist = kFp8 ? min(kPrefetchTiles, 32 / sub - 1) : 0;
     auto pid_at = [&](int pi) -> int {  // page id of page index pi in [batch_base, batch_base + 64)
       const int rel = pi - batch_base;
       const int a = __shfl_sync(0xffffffffu, cur, rel & 31);
@@ -275,7 +277,7 @@ decode_partial_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
           pids[pp] = 0;
         }
       }
-      if (j + kStages + prefetch_dist < ntiles) prefetch_tile(j + kStages + prefetch_dist);
+      if (prefetch_dist > 0 && j + kStages + prefetch_dist < ntiles) prefetch_tile(j + kStages + prefetch_dist);
       if (lane == 0) {
         const int row_in_page = (P > kTileKeys) ? (k0 % P) : 0;
         if (!kFp8) {
@@ -545,7 +547,18 @@ decode_partial_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
       // once the last BMM2 has completed) so that global stores are whole 16-byte row
       // chunks.  Split partials are kept in bf16 too: they are averaged by the combine and
       // rounded to the bf16 output anyway, and half the bytes is half the extra traffic.
-      __nv_bfloat16* stage_h = reinterpret_cast<__nv_bfloat16*>(smem + kOffStages);   // [64][512] bf16
+      // The 64 row scales go to registers first: shared-memory loads interleaved with the
+      // staging stores below would each have to wait for the stores before them.
+      float rs[kGroupRows];
+#pragma unroll
+      for (int i = 0; i < kGroupRows; i += 4) {
+        const float4 f = *reinterpret_cast<const float4*>(&ctrl->row_scale[i]);
+        rs[i] = f.x;
+        rs[i + 1] = f.y;
+        rs[i + 2] = f.z;
+        rs[i + 3] = f.w;
+      }
+      const uint32_t stage_s = smem_u32(smem + kOffStages);  // [64][512] bf16
 #pragma unroll 1
       for (int qc = 0; qc < 4; ++qc) {
         const int dim = qc * 128 + warp * 32 + lane;
@@ -557,10 +570,13 @@ decode_partial_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
             const int rr = hh * 32 + i;
-            stage_h[rr * kValueDim + dim] = __float2bfloat16_rn(__uint_as_float(v[i]) * ctrl->row_scale[rr]);
+            const __nv_bfloat16 o = __float2bfloat16_rn(__uint_as_float(v[i]) * rs[rr]);
+            asm volatile("st.shared.b16 [%0], %1;" ::"r"(stage_s + (rr * kValueDim + dim) * 2),
+                         "h"(*reinterpret_cast<const uint16_t*>(&o)));
           }
         }
       }
+      __nv_bfloat16* stage_h = reinterpret_cast<__nv_bfloat16*>(smem + kOffStages);
       named_bar_sync(1, 128);
       constexpr int kChunksPerRow = kValueDim * 2 / 16;
       __nv_bfloat16* dst = final_out

@@ -225,20 +225,30 @@ int mla_decode(const mla_decode_plan_t* plan, const void* q, const void* kv_page
   if (!status) return MLA_ERR_CUDA;
 
   const uint64_t row_bytes = kLatentDim * 2;
+  // Latent rows are viewed as [rows][9 blocks][64 columns] (block stride 128 bytes), so one
+  // 3-D box {64 columns, n rows, 9 blocks} lands a whole row range as the nine 128-byte
+  // swizzled column blocks the MMAs read, in a single TMA instruction.
   CUtensorMap tm_q, tm_kv;
   {
-    const uint64_t dims[2] = {static_cast<uint64_t>(kLatentDim), static_cast<uint64_t>(plan->batch) * plan->rows};
-    const uint64_t strides[1] = {row_bytes};
-    const uint32_t box[2] = {64, static_cast<uint32_t>(kGroupRows)};
-    if (!make_map(&tm_q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, q, dims, strides, box)) return MLA_ERR_CUDA;
+    const uint64_t dims[3] = {64, static_cast<uint64_t>(plan->batch) * plan->rows, kLatentDim / 64};
+    const uint64_t strides[2] = {row_bytes, 128};
+    const uint32_t box[3] = {64, static_cast<uint32_t>(kGroupRows), kLatentDim / 64};
+    if (!make_map(&tm_q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, q, dims, strides, box)) return MLA_ERR_CUDA;
   }
   memset(&tm_kv, 0, sizeof tm_kv);
   if (plan->kv_dtype == MLA_KV_BF16) {  // e4m3 pages are fetched with untiled bulk copies
-    const uint64_t dims[2] = {static_cast<uint64_t>(kLatentDim),
-                              static_cast<uint64_t>(plan->num_pages) * plan->page_size};
-    const uint64_t strides[1] = {row_bytes};
-    const uint32_t box[2] = {64, static_cast<uint32_t>(std::min(plan->page_size, kTileKeys))};
-    if (!make_map(&tm_kv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kv_pages, dims, strides, box)) return MLA_ERR_CUDA;
+    const uint64_t rows = static_cast<uint64_t>(plan->num_pages) * plan->page_size;
+    if (plan->page_size >= kTileKeys) {  // a 64-key tile is one row range of one page
+      const uint64_t dims[3] = {64, rows, kLatentDim / 64};
+      const uint64_t strides[2] = {row_bytes, 128};
+      const uint32_t box[3] = {64, static_cast<uint32_t>(kTileKeys), kLatentDim / 64};
+      if (!make_map(&tm_kv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, kv_pages, dims, strides, box)) return MLA_ERR_CUDA;
+    } else {  // smaller pages: one 2-D box per (page, column block)
+      const uint64_t dims[2] = {static_cast<uint64_t>(kLatentDim), rows};
+      const uint64_t strides[1] = {row_bytes};
+      const uint32_t box[2] = {64, static_cast<uint32_t>(plan->page_size)};
+      if (!make_map(&tm_kv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kv_pages, dims, strides, box)) return MLA_ERR_CUDA;
+    }
   }
   DecodeParams p;
   memset(&p, 0, sizeof p);

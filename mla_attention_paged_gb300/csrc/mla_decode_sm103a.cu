@@ -218,8 +218,7 @@ decode_partial_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
     const uint64_t pol_q = policy_evict_last();
     if (lane == 0) {
       mbar_arrive_expect_tx(&ctrl->q_full, kTileBytes);
-      for (int c = 0; c < kDimBlocks; ++c)
-        tma_load_2d(smem + kOffQ + c * kBlockBytes, &tm_q, &ctrl->q_full, c * 64, b * p.R + row0, pol_q);
+      tma_load_3d(smem + kOffQ, &tm_q, &ctrl->q_full, 0, b * p.R + row0, 0, pol_q);  // all 9 column blocks
     }
     // e4m3 only: an L2 prefetch runs kPrefetchTiles tiles ahead of the shared-memory ring
     // (that path is bound by the dequant warps, and the prefetch hides part of each raw
@@ -251,12 +250,6 @@ decode_partial_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
     bool ok = true;
     for (int j = 0; j < ntiles; ++j) {
       const int s = j % kStages;
-      if (j >= kStages) {
-        bool w = true;
-        if (lane == 0) w = mbar_wait(&ctrl->kv_empty[s], ((j / kStages) - 1) & 1, abort_flag);
-        ok = __shfl_sync(0xffffffffu, w, 0);
-        if (!ok) break;
-      }
       const int k0 = kv_start + j * kTileKeys;
       const int pg0 = k0 / P;
       const int tile_end = min(k0 + kTileKeys, L);
@@ -277,17 +270,30 @@ decode_partial_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
           pids[pp] = 0;
         }
       }
+      // The page ids above are resolved before waiting for the stage, so that only the
+      // copies are left once it frees up (resolving them after the wait was measured to
+      // delay each tile's copies by ~1.5k cycles).
+      if (j >= kStages) {
+        bool w = true;
+        if (lane == 0) w = mbar_wait(&ctrl->kv_empty[s], ((j / kStages) - 1) & 1, abort_flag);
+        ok = __shfl_sync(0xffffffffu, w, 0);
+        if (!ok) break;
+      }
       if (prefetch_dist > 0 && j + kStages + prefetch_dist < ntiles) prefetch_tile(j + kStages + prefetch_dist);
       if (lane == 0) {
         const int row_in_page = (P > kTileKeys) ? (k0 % P) : 0;
         if (!kFp8) {
           uint8_t* stage = smem + kOffStages + s * kTileBytes;
           mbar_arrive_expect_tx(&ctrl->kv_full[s], static_cast<uint32_t>(npg * box_rows * 128 * kDimBlocks));
-          for (int pp = 0; pp < npg; ++pp) {
-            const int y = pids[pp] * P + row_in_page;
-            for (int c = 0; c < kDimBlocks; ++c)
-              tma_load_2d(stage + c * kBlockBytes + pp * box_rows * 128, &tm_kv, &ctrl->kv_full[s], c * 64, y,
-                          pol_kv);
+          if (P >= kTileKeys) {  // one 3-D box: 64 rows x all 9 column blocks
+            tma_load_3d(stage, &tm_kv, &ctrl->kv_full[s], 0, pids[0] * P + row_in_page, 0, pol_kv);
+          } else {
+            for (int pp = 0; pp < npg; ++pp) {
+              const int y = pids[pp] * P;
+              for (int c = 0; c < kDimBlocks; ++c)
+                tma_load_2d(stage + c * kBlockBytes + pp * box_rows * 128, &tm_kv, &ctrl->kv_full[s], c * 64, y,
+                            pol_kv);
+            }
           }
         } else {
           uint8_t* stage = smem + kOffStages + s * kRawBytes;

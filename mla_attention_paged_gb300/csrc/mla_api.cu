@@ -300,24 +300,27 @@ int mla_prefill_varlen(const void* q, const void* k, const void* v, const int32_
   unsigned* status = status_ptr();
   if (!status) return MLA_ERR_CUDA;
   const uint64_t H = static_cast<uint64_t>(num_heads);
+  // q/k/v rows are viewed as [token][column block][64 columns] per head, 4-D
+  // (columns, token, block, head): one box {64 columns, n tokens, all blocks, 1 head}
+  // lands every 128-byte swizzled column block of a tile in a single TMA instruction.
   CUtensorMap tm_q, tm_k, tm_v;
   {
-    const uint64_t dims[3] = {192, H, static_cast<uint64_t>(total_q)};
-    const uint64_t strides[2] = {192 * 2, H * 192 * 2};
-    const uint32_t box[3] = {64, 1, 128};
-    if (!make_map(&tm_q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, q, dims, strides, box)) return MLA_ERR_CUDA;
+    const uint64_t dims[4] = {64, static_cast<uint64_t>(total_q), 3, H};
+    const uint64_t strides[3] = {H * 192 * 2, 128, 192 * 2};
+    const uint32_t box[4] = {64, 128, 3, 1};
+    if (!make_map(&tm_q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, q, dims, strides, box)) return MLA_ERR_CUDA;
   }
   {
-    const uint64_t dims[3] = {192, H, static_cast<uint64_t>(total_kv)};
-    const uint64_t strides[2] = {192 * 2, H * 192 * 2};
-    const uint32_t box[3] = {64, 1, 64};
-    if (!make_map(&tm_k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, k, dims, strides, box)) return MLA_ERR_CUDA;
+    const uint64_t dims[4] = {64, static_cast<uint64_t>(total_kv), 3, H};
+    const uint64_t strides[3] = {H * 192 * 2, 128, 192 * 2};
+    const uint32_t box[4] = {64, 128, 3, 1};
+    if (!make_map(&tm_k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, k, dims, strides, box)) return MLA_ERR_CUDA;
   }
   {
-    const uint64_t dims[3] = {128, H, static_cast<uint64_t>(total_kv)};
-    const uint64_t strides[2] = {128 * 2, H * 128 * 2};
-    const uint32_t box[3] = {64, 1, 64};
-    if (!make_map(&tm_v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, v, dims, strides, box)) return MLA_ERR_CUDA;
+    const uint64_t dims[4] = {64, static_cast<uint64_t>(total_kv), 2, H};
+    const uint64_t strides[3] = {H * 128 * 2, 128, 128 * 2};
+    const uint32_t box[4] = {64, 128, 2, 1};
+    if (!make_map(&tm_v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, v, dims, strides, box)) return MLA_ERR_CUDA;
   }
   PrefillParams p;
   memset(&p, 0, sizeof p);

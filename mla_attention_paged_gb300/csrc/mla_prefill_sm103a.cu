@@ -36,7 +36,6 @@ constexpr int kDqk = 192;
 constexpr int kDv = 128;
 constexpr int kBM = 128;     // query rows per CTA
 constexpr int kBN = 128;     // keys per tile
-constexpr int kBox = 64;     // rows per TMA box (the tensor maps' box height)
 constexpr int kStages = 2;
 constexpr int kThreads = 192;
 
@@ -169,8 +168,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       const uint64_t pol_q = policy_evict_first();
       const uint64_t pol_kv = policy_evict_last();  // re-read by the other query blocks of this head
       mbar_arrive_expect_tx(&ctrl->q_full, kQBytes);
-      for (int c = 0; c < kDqk / 64; ++c)  // the query map's box is 64 columns x 128 rows
-        tma_load_3d(smem + kOffQ + c * kQBlockBytes, &tm_q, &ctrl->q_full, c * 64, h, q_start + row_begin, pol_q);
+      // one box: 128 rows x all three 64-column blocks of head h
+      tma_load_4d(smem + kOffQ, &tm_q, &ctrl->q_full, 0, q_start + row_begin, 0, h, pol_q);
       int last_issued[kStages] = {-1, -1};
       bool ok = true;
       for (int j = 0; j < ntiles; ++j) {
@@ -182,14 +181,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         uint8_t* st = smem + kOffKV + s * kStageBytes;
         const int row = kv_start + j * kBN;
         mbar_arrive_expect_tx(&ctrl->kv_full[s], kStageBytes);
-        for (int hb = 0; hb < kBN / kBox; ++hb) {
-          for (int c = 0; c < kDqk / 64; ++c)
-            tma_load_3d(st + c * kKVBlockBytes + hb * kBox * 128, &tm_k, &ctrl->kv_full[s], c * 64, h,
-                        row + hb * kBox, pol_kv);
-          for (int c = 0; c < kDv / 64; ++c)
-            tma_load_3d(st + kKBytes + c * kKVBlockBytes + hb * kBox * 128, &tm_v, &ctrl->kv_full[s], c * 64, h,
-                        row + hb * kBox, pol_kv);
-        }
+        tma_load_4d(st, &tm_k, &ctrl->kv_full[s], 0, row, 0, h, pol_kv);            // K: 128 rows x 3 blocks
+        tma_load_4d(st + kKBytes, &tm_v, &ctrl->kv_full[s], 0, row, 0, h, pol_kv);  // V: 128 rows x 2 blocks
         last_issued[s] = j;
       }
       if (!ok) {

@@ -49,8 +49,9 @@ constexpr int kTileBytes = kDimBlocks * kBlockBytes; // 73728: one bf16 64-key l
 constexpr int kRawBytes = kTileKeys * kLatentDim;    // 36864: one e4m3 64-key tile
 constexpr int kStages = 2;
 constexpr int kPrefetchTiles = 4;  // e4m3 L2 prefetch distance beyond the shared-memory ring
-constexpr int kThreads = 256;        // warps 0-3 softmax/epilogue, 4 producer, 5 MMA, 6-7 e4m3 dequant
-constexpr int kDequantThreads = 64;  // warps 6-7
+// warps 0-3 softmax/epilogue, 4 producer, 5 MMA; the e4m3 variant adds warps 6-9 (dequant)
+constexpr int kDequantThreads = 128;
+__host__ __device__ constexpr int threads_for(bool fp8) { return fp8 ? 192 + kDequantThreads : 192; }
 
 // Shared memory map.  bf16: Q | stage0 | stage1 | P | ctrl.
 //                     e4m3: Q | raw0 | raw1 | bf16 tile | P | ctrl  (same total).
@@ -69,7 +70,9 @@ struct DecodeCtrl {
   uint64_t s_free[2];
   uint64_t p_full;
   uint64_t o_done;
-  uint64_t tile_full;   // e4m3: dequantised tile ready
+  uint64_t q_ready;                 // e4m3: Q converted to f16 in place
+  uint64_t blk_ready[kDimBlocks];   // e4m3: 64-column block of the f16 tile written
+  uint64_t blk_free[5];             // e4m3: f16 blocks 2g, 2g+1 (g < 4) / block 8 (g = 4) read
   uint64_t mma_drain;
   uint32_t tmem_base;
   int abort_flag;
@@ -105,24 +108,35 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
   }
 }
 
-// Two e4m3 codes -> two bf16 (exact: every e4m3 value is a bf16 value).
-__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint16_t two) {
-  const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(two), __NV_E4M3);
-  const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h));
-  return pack_bf16x2(f.x, f.y);
+// Four e4m3 codes (bytes of w) -> four f16 holding the codes' values times 2^-8, exactly,
+// with integer ops only.  An e4m3 code s.eeee.mmm moved to f16 bit positions s.0eeee.mmm0000000
+// reads as the same significand with exponent bias 15 instead of 7, i.e. the value times
+// 2^-8; e4m3 subnormals land on f16 subnormals with the same factor.  (The finite e4m3 range,
+// |v| <= 448, becomes |v| <= 1.75.)  The kernel folds 2^8 back into the softmax and output
+// scales.
+__device__ __forceinline__ void e4m3x4_to_f16x4_scaled(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  const uint32_t h0 = __byte_perm(w, 0u, 0x1404);  // code 0 in bits 8-15, code 1 in bits 24-31
+  const uint32_t h1 = __byte_perm(w, 0u, 0x3424);  // codes 2 and 3
+  lo = (h0 & 0x80008000u) | ((h0 >> 1) & 0x3F803F80u);
+  hi = (h1 & 0x80008000u) | ((h1 >> 1) & 0x3F803F80u);
 }
 
-// Decode one raw e4m3 tile (64 rows x 576 bytes, row-major) into the 128-byte-swizzled
-// bf16 tile (9 blocks of 64 rows x 64 columns); rows >= valid_rows become zero.  Run by
-// 64 threads (t = 0..63).
-__device__ __forceinline__ void dequant_tile(const uint8_t* raw, uint8_t* tile, int valid_rows, int t) {
-  const uint32_t raw_s = smem_u32(raw);
-  const uint32_t tile_s = smem_u32(tile);
-#pragma unroll 4
-  for (int i = 0; i < kTileKeys * (kLatentDim / 16) / 64; ++i) {
-    const int item = t + 64 * i;
-    const int row = item / (kLatentDim / 16);
-    const int c16 = item % (kLatentDim / 16);
+// Two bf16 -> two f16, round to nearest (exact for magnitudes in f16's normal range).
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t v) {
+  return pack_f16x2(__uint_as_float(v << 16), __uint_as_float(v & 0xFFFF0000u));
+}
+
+// Decode rows [r0, r0 + nr) of 64-column block c of one raw e4m3 tile (64 rows x 576 bytes,
+// row-major) into block c of the 128-byte-swizzled f16 tile (64 rows x 128 bytes), as values
+// times 2^-8; rows >= valid_rows become zero.  Run by `nt` threads (t = 0 .. nt-1); each
+// item is 16 raw bytes (16 columns) -> two 16-byte f16 chunks.
+__device__ __forceinline__ void dequant_rows(const uint8_t* raw, uint8_t* tile, int c, int r0, int nr,
+                                             int valid_rows, int t, int nt) {
+  const uint32_t raw_s = smem_u32(raw) + c * 64;
+  const uint32_t blk_s = smem_u32(tile) + c * kBlockBytes;
+  for (int item = t; item < nr * 4; item += nt) {
+    const int row = r0 + (item >> 2);
+    const int c16 = item & 3;
     uint32_t w[4] = {0u, 0u, 0u, 0u};
     if (row < valid_rows) {
       asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
@@ -131,20 +145,21 @@ __device__ __forceinline__ void dequant_tile(const uint8_t* raw, uint8_t* tile, 
     }
     uint32_t o[8];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      o[2 * k] = e4m3x2_to_bf16x2(static_cast<uint16_t>(w[k] & 0xFFFFu));
-      o[2 * k + 1] = e4m3x2_to_bf16x2(static_cast<uint16_t>(w[k] >> 16));
-    }
-    const int blk = c16 >> 2;
-    const int cc = (c16 & 3) * 2;
-    const uint32_t rbase = tile_s + blk * kBlockBytes + row * 128;
+    for (int k = 0; k < 4; ++k) e4m3x4_to_f16x4_scaled(w[k], o[2 * k], o[2 * k + 1]);
+    const int cc = c16 * 2;
+    const uint32_t rbase = blk_s + row * 128;
     st_shared_v4(rbase + ((cc ^ (row & 7)) << 4), o[0], o[1], o[2], o[3]);
     st_shared_v4(rbase + (((cc + 1) ^ (row & 7)) << 4), o[4], o[5], o[6], o[7]);
   }
 }
 
+// The e4m3 path fills and consumes the f16 tile's column blocks in this order: block 8 (the
+// rope columns, free as soon as the previous tile's BMM1 is done) first, then 0..7 in the
+// order the previous tile's BMM2 frees them.
+__device__ __forceinline__ int fp8_block_order(int i) { return i == 0 ? kDimBlocks - 1 : i - 1; }
+
 template <bool kFp8>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(threads_for(kFp8), 1)
 decode_partial_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kv,
                       const DecodeParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -183,7 +198,10 @@ decode_partial_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
     }
     mbar_init(&ctrl->p_full, 128);
     mbar_init(&ctrl->o_done, 1);
-    mbar_init(&ctrl->tile_full, kDequantThreads);
+    mbar_init(&ctrl->q_ready, kDequantThreads);
+    // block 8 is written by all dequant warps, blocks 0-7 by one warp each
+    for (int c = 0; c < kDimBlocks; ++c) mbar_init(&ctrl->blk_ready[c], c == kDimBlocks - 1 ? kDequantThreads : 32);
+    for (int g = 0; g < 5; ++g) mbar_init(&ctrl->blk_free[g], 1);
     mbar_init(&ctrl->mma_drain, 1);
     ctrl->abort_flag = 0;
     for (int w = 0; w < 4; ++w) ctrl->rescale_flag[w] = 0;
@@ -317,8 +335,9 @@ decode_partial_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
   } else if (warp == 5) {
     // ------------------------------------------------------------------ MMA issuer (whole warp,
     // uniform control flow; one elected thread issues each GEMM's MMAs and their commit)
-    const uint32_t idesc1 = make_idesc_bf16(64, 64, false, false);
-    const uint32_t idesc2 = make_idesc_bf16(128, nq, true, false);
+    // the e4m3 path multiplies f16 operands (Q converted once, K/V decoded to f16, P in f16)
+    const uint32_t idesc1 = kFp8 ? make_idesc_f16(64, 64, false, false) : make_idesc_bf16(64, 64, false, false);
+    const uint32_t idesc2 = kFp8 ? make_idesc_f16(128, nq, true, false) : make_idesc_bf16(128, nq, true, false);
     // Descriptors are built once; each MMA advances the start-address field by a
     // compile-time offset (addresses stay below 256 KB, so no carry leaves the field).
     const uint64_t q_desc = make_smem_desc(smem_u32(smem + kOffQ), 16, 1024);
@@ -328,8 +347,9 @@ decode_partial_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
       if (lane == 0) v = mbar_test_wait(bar, parity) ? 1u : 0u;
       return __shfl_sync(0xffffffffu, v, 0) != 0;
     };
-    bool ok = mbar_wait(&ctrl->q_full, 0, abort_flag);
+    bool ok = kFp8 ? mbar_wait(&ctrl->q_ready, 0, abort_flag) : mbar_wait(&ctrl->q_full, 0, abort_flag);
     ok = __all_sync(0xffffffffu, ok);
+    int c1 = 0;  // e4m3: blocks of BMM1(n1) already issued, in fp8_block_order
     // Issue whichever GEMM is ready: BMM2(n2) first (it frees a stage), else BMM1(n1) for a
     // tile whose data has landed and whose S buffer is free.  BMM1 runs at most two tiles
     // ahead of BMM2 (double-buffered S).
@@ -353,6 +373,7 @@ decode_partial_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
               const uint64_t poff = static_cast<uint64_t>((kk * 32) >> 4);
               umma_bf16(tmem + qc * 64, v_desc + voff, p_desc + poff, idesc2, (n2 > 0 || kk > 0) ? 1u : 0u);
             }
+            if (kFp8) umma_commit(&ctrl->blk_free[qc]);  // f16 value blocks 2qc, 2qc+1 read
           }
           umma_commit(&ctrl->o_done);
           if (!kFp8) umma_commit(&ctrl->kv_empty[s]);
@@ -360,14 +381,47 @@ decode_partial_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
         __syncwarp();
         ++n2;
         progressed = true;
-      } else if (n1 < ntiles && n1 < n2 + 2) {
+      } else if (kFp8 && n1 < ntiles && n1 < n2 + 2) {
+        // e4m3: BMM1 follows the dequant warps block by block (lanes test the block
+        // barriers in parallel; consecutive decoded blocks are issued together)
+        const int sb = n1 & 1;
+        const bool r = lane >= c1 && lane < kDimBlocks &&
+                       mbar_test_wait(&ctrl->blk_ready[fp8_block_order(lane)], n1 & 1);
+        const uint32_t ready = __ballot_sync(0xffffffffu, r);
+        const int nb = __ffs(~(ready >> c1)) - 1;
+        if (nb > 0 && (c1 > 0 || n1 < 2 || poll(&ctrl->s_free[sb], ((n1 - 2) >> 1) & 1))) {
+          tc_fence_after();
+          const uint64_t k_desc = make_smem_desc(smem_u32(smem + kOffTileFp8), 16, 1024);
+          const uint32_t d = tmem + kTmemS + sb * 64;
+          const int i_end = c1 + nb;
+          if (elect_one()) {
+            for (int i = c1; i < i_end; ++i) {
+              const uint64_t boff = static_cast<uint64_t>((fp8_block_order(i) * kBlockBytes) >> 4);
+#pragma unroll
+              for (int k = 0; k < 4; ++k) {
+                const uint64_t off = boff + static_cast<uint64_t>((k * 32) >> 4);
+                umma_bf16(d, q_desc + off, k_desc + off, idesc1, (i | k) != 0);
+              }
+            }
+            if (i_end == kDimBlocks) {
+              umma_commit(&ctrl->s_full[sb]);
+              umma_commit(&ctrl->blk_free[4]);  // the rope block is only read by BMM1
+            }
+          }
+          __syncwarp();
+          c1 = i_end;
+          if (c1 == kDimBlocks) {
+            c1 = 0;
+            ++n1;
+          }
+          progressed = true;
+        }
+      } else if (!kFp8 && n1 < ntiles && n1 < n2 + 2) {
         const int s = n1 % kStages, sb = n1 & 1;
-        const bool data = kFp8 ? poll(&ctrl->tile_full, n1 & 1) : poll(&ctrl->kv_full[s], (n1 / kStages) & 1);
+        const bool data = poll(&ctrl->kv_full[s], (n1 / kStages) & 1);
         if (data && (n1 < 2 || poll(&ctrl->s_free[sb], ((n1 - 2) >> 1) & 1))) {
           tc_fence_after();
-          const uint32_t kv_base =
-              kFp8 ? smem_u32(smem + kOffTileFp8) : smem_u32(smem + kOffStages + s * kTileBytes);
-          const uint64_t k_desc = make_smem_desc(kv_base, 16, 1024);
+          const uint64_t k_desc = make_smem_desc(smem_u32(smem + kOffStages + s * kTileBytes), 16, 1024);
           const uint32_t d = tmem + kTmemS + sb * 64;
           if (elect_one()) {
 #pragma unroll
@@ -408,25 +462,48 @@ decode_partial_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
     }
     __syncwarp();
   } else if (warp >= 6) {
-    // ------------------------------------------------------------------ e4m3 dequant (warps 6-7)
+    // ------------------------------------------------------------------ e4m3 dequant (warps 6-9):
+    // Q to f16 in place once, then each raw tile into the f16 tile block by block, each block
+    // as soon as the previous tile has finished reading it
     if (kFp8) {
       const int td = threadIdx.x - 6 * 32;
-      auto dequant = [&](int j) -> bool {  // raw stage of tile j -> the bf16 tile
-        const int s = j % kStages;
-        bool w = mbar_wait(&ctrl->kv_full[s], (j / kStages) & 1, abort_flag);
-        w = __all_sync(0xffffffffu, w);
-        if (!w) return false;
-        dequant_tile(smem + kOffStages + s * kRawBytes, smem + kOffTileFp8, L - (kv_start + j * kTileKeys), td);
+      bool ok = mbar_wait(&ctrl->q_full, 0, abort_flag);
+      if (ok) {
+        const uint32_t q_s = smem_u32(smem + kOffQ);
+        for (int c = td; c < kTileBytes / 16; c += kDequantThreads) {
+          uint32_t w0, w1, w2, w3;
+          asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                       : "=r"(w0), "=r"(w1), "=r"(w2), "=r"(w3)
+                       : "r"(q_s + c * 16));
+          st_shared_v4(q_s + c * 16, bf16x2_to_f16x2(w0), bf16x2_to_f16x2(w1), bf16x2_to_f16x2(w2),
+                       bf16x2_to_f16x2(w3));
+        }
         fence_proxy_async_smem();
-        mbar_arrive(&ctrl->tile_full);
-        mbar_arrive(&ctrl->kv_empty[s]);
-        return true;
-      };
-      bool ok = dequant(0);
-      for (int j = 0; ok && j + 1 < ntiles; ++j) {
-        // the bf16 tile is free once BMM2(j) has read it
-        bool w = mbar_wait(&ctrl->o_done, j & 1, abort_flag);
-        ok = __all_sync(0xffffffffu, w) && dequant(j + 1);
+        mbar_arrive(&ctrl->q_ready);
+      }
+      // Per tile: block 8 (free once the previous tile's BMM1 is done) by all four warps, 16
+      // rows each; then warp w decodes blocks w and w + 4, each as soon as the previous tile's
+      // BMM2 has read it, so the four warps work on different blocks at once.
+      const int dw = td >> 5, dl = td & 31;
+      for (int j = 0; ok && j < ntiles; ++j) {
+        const int s = j % kStages;
+        ok = mbar_wait(&ctrl->kv_full[s], (j / kStages) & 1, abort_flag);
+        const uint8_t* raw = smem + kOffStages + s * kRawBytes;
+        const int valid_rows = L - (kv_start + j * kTileKeys);
+        if (ok && j >= 1) ok = mbar_wait(&ctrl->blk_free[4], (j - 1) & 1, abort_flag);
+        if (ok) {
+          dequant_rows(raw, smem + kOffTileFp8, kDimBlocks - 1, 16 * dw, 16, valid_rows, dl, 32);
+          fence_proxy_async_smem();
+          mbar_arrive(&ctrl->blk_ready[kDimBlocks - 1]);
+        }
+        for (int c = dw; ok && c < 8; c += 4) {
+          if (j >= 1) ok = mbar_wait(&ctrl->blk_free[c / 2], (j - 1) & 1, abort_flag);
+          if (!ok) break;
+          dequant_rows(raw, smem + kOffTileFp8, c, 0, kTileKeys, valid_rows, dl, 32);
+          fence_proxy_async_smem();
+          mbar_arrive(&ctrl->blk_ready[c]);
+        }
+        if (ok) mbar_arrive(&ctrl->kv_empty[s]);  // the raw stage may be refilled
       }
     }
   } else {
@@ -444,6 +521,9 @@ decode_partial_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
     float m_used = -INFINITY;
     float l_sum = 0.f;
     bool failed = false;
+    // e4m3 tiles are decoded as values times 2^-8 (exact); the factor returns here
+    const float scale_log2 = kFp8 ? p.scale_log2 * 256.f : p.scale_log2;
+    const float v_scale = kFp8 ? p.v_scale * 256.f : p.v_scale;
 
     for (int j = 0; j < ntiles; ++j) {
       const int sb = j & 1;
@@ -462,8 +542,9 @@ decode_partial_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
         mbar_arrive(&ctrl->s_free[sb]);
         // keys i <= lim of this lane's 32-key half are visible
         const int lim = row_active ? (min(kv_end - 1, lim_abs) - k0 - 32 * half) : -1;
-        online_softmax_step<32, true>(sr, lim, p.scale_log2, kRescaleThreshold, m_used, l_sum, packed, alpha,
-                                      need_rescale);
+        // the e4m3 path multiplies P in f16 (P <= 2^8 here, where f16 keeps more bits than bf16)
+        online_softmax_step<32, true, kFp8>(sr, lim, scale_log2, kRescaleThreshold, m_used, l_sum, packed, alpha,
+                                            need_rescale);
       }
       if (!fail && j >= 1) {
         fail = !mbar_wait(&ctrl->o_done, (j - 1) & 1, abort_flag);
@@ -539,7 +620,7 @@ decode_partial_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
       if (row_lane) {
         const float lse2 = (l_sum > 0.f) ? (m_used + __log2f(l_sum)) : -INFINITY;
         const float lse_nat = lse2 * 0.69314718055994530942f;
-        ctrl->row_scale[r] = (l_sum > 0.f) ? (p.v_scale / l_sum) : 0.f;
+        ctrl->row_scale[r] = (l_sum > 0.f) ? (v_scale / l_sum) : 0.f;
         if (row_active) {
           const int64_t grow = static_cast<int64_t>(b) * p.R + row0 + r;
           if (final_out)
@@ -721,7 +802,7 @@ cudaError_t launch_partial_impl(const DecodeParams& p, const CUtensorMap& tm_q, 
     configured_device = dev;
   }
   dim3 grid(head_groups, p.max_splits, p.B);
-  decode_partial_kernel<kFp8><<<grid, kThreads, kSmemBytes, stream>>>(tm_q, tm_kv, p);
+  decode_partial_kernel<kFp8><<<grid, threads_for(kFp8), kSmemBytes, stream>>>(tm_q, tm_kv, p);
   return cudaGetLastError();
 }
 

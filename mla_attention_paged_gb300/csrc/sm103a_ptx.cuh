@@ -6,6 +6,7 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <stdint.h>
 
 namespace mla {
@@ -222,7 +223,14 @@ __host__ __device__ constexpr uint32_t make_idesc_bf16(int M, int N, bool a_mn_m
          (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
 }
 
-// D[tmem] (+)= A[smem desc] * B[smem desc]; issued by a single thread.
+// The same with f16 A and B (format code 0 in bits 7-9 and 10-12).
+__host__ __device__ constexpr uint32_t make_idesc_f16(int M, int N, bool a_mn_major, bool b_mn_major) {
+  return (1u << 4) | ((a_mn_major ? 1u : 0u) << 15) | ((b_mn_major ? 1u : 0u) << 16) |
+         (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// D[tmem] (+)= A[smem desc] * B[smem desc]; issued by a single thread.  kind::f16 covers
+// both 16-bit input types; the instruction descriptor says which.
 __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                                           uint32_t accumulate) {
   asm volatile(
@@ -301,16 +309,21 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  const __half2 v = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+
 // One online-softmax step for one row over N raw scores s[] (fp32 bit patterns of q.k).
 // Keys i <= lim are visible (lim >= N-1: all).  The running max m_used lives in the log2
 // domain of the scaled score (x = s * scale_log2); it only moves when a tile's max exceeds
 // it by more than `threshold`, and then alpha = 2^(m_old - m_new) rescales l_sum here and
 // must rescale the row's O accumulator (need_rescale).  P = 2^(x - m_used) is returned as
-// packed bf16 pairs; l_sum accumulates the fp32 P.
+// packed bf16 pairs (f16 pairs with kHalfP); l_sum accumulates the fp32 P.
 // kPairMax: the row is split between lanes l and l^16 (each holds N of its scores); the
 // tile max is exchanged between them, so both take identical running-state decisions and
 // each keeps the partial row sum of its own half.
-template <int N, bool kPairMax = false>
+template <int N, bool kPairMax = false, bool kHalfP = false>
 __device__ __forceinline__ void online_softmax_step(const uint32_t (&s)[N], int lim, float scale_log2,
                                                     float threshold, float& m_used, float& l_sum,
                                                     uint32_t (&packed)[N / 2], float& alpha, bool& need_rescale) {
@@ -345,7 +358,7 @@ __device__ __forceinline__ void online_softmax_step(const uint32_t (&s)[N], int 
       const float p1 = ex2_approx(fmaf(__uint_as_float(s[i + 1]), scale_log2, neg_m));
       l0 += p0;
       l1 += p1;
-      packed[i >> 1] = pack_bf16x2(p0, p1);
+      packed[i >> 1] = kHalfP ? pack_f16x2(p0, p1) : pack_bf16x2(p0, p1);
     }
   } else {
 #pragma unroll
@@ -354,7 +367,7 @@ __device__ __forceinline__ void online_softmax_step(const uint32_t (&s)[N], int 
       const float p1 = (i + 1 <= lim) ? ex2_approx(fmaf(__uint_as_float(s[i + 1]), scale_log2, neg_m)) : 0.f;
       l0 += p0;
       l1 += p1;
-      packed[i >> 1] = pack_bf16x2(p0, p1);
+      packed[i >> 1] = kHalfP ? pack_f16x2(p0, p1) : pack_bf16x2(p0, p1);
     }
   }
   l_sum += l0 + l1;

@@ -126,27 +126,34 @@ __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t v) {
   return pack_f16x2(__uint_as_float(v << 16), __uint_as_float(v & 0xFFFF0000u));
 }
 
-// Decode rows [r0, r0 + nr) of 64-column block c of one raw e4m3 tile (64 rows x 576 bytes,
-// row-major) into block c of the 128-byte-swizzled f16 tile (64 rows x 128 bytes), as values
-// times 2^-8; rows >= valid_rows become zero.  Run by `nt` threads (t = 0 .. nt-1); each
-// item is 16 raw bytes (16 columns) -> two 16-byte f16 chunks.
-__device__ __forceinline__ void dequant_rows(const uint8_t* raw, uint8_t* tile, int c, int r0, int nr,
-                                             int valid_rows, int t, int nt) {
-  const uint32_t raw_s = smem_u32(raw) + c * 64;
-  const uint32_t blk_s = smem_u32(tile) + c * kBlockBytes;
-  for (int item = t; item < nr * 4; item += nt) {
-    const int row = r0 + (item >> 2);
-    const int c16 = item & 3;
-    uint32_t w[4] = {0u, 0u, 0u, 0u};
-    if (row < valid_rows) {
-      asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                   : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
-                   : "r"(raw_s + row * kLatentDim + c16 * 16));
-    }
-    uint32_t o[8];
+// Decode rows [r0, r0 + 8*NI) of 64-column block c of one raw e4m3 tile (64 rows x 576
+// bytes, row-major) into block c of the 128-byte-swizzled f16 tile (64 rows x 128 bytes), as
+// values times 2^-8; rows >= valid_rows become zero.  One warp (lane = 0..31); each item is
+// 16 raw bytes (16 columns) -> two 16-byte f16 chunks, NI items per lane, all loads issued
+// before the first conversion.
+template <int NI>
+__device__ __forceinline__ void dequant_rows(const uint8_t* raw, uint8_t* tile, int c, int r0, int valid_rows,
+                                             int lane) {
+  uint4 w[NI];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) e4m3x4_to_f16x4_scaled(w[k], o[2 * k], o[2 * k + 1]);
-    const int cc = c16 * 2;
+  for (int i = 0; i < NI; ++i) {
+    const int item = lane + 32 * i;
+    const int row = r0 + (item >> 2);
+    w[i] = (row < valid_rows)
+               ? *reinterpret_cast<const uint4*>(raw + row * kLatentDim + c * 64 + (item & 3) * 16)
+               : make_uint4(0u, 0u, 0u, 0u);
+  }
+  const uint32_t blk_s = smem_u32(tile) + c * kBlockBytes;
+#pragma unroll
+  for (int i = 0; i < NI; ++i) {
+    const int item = lane + 32 * i;
+    const int row = r0 + (item >> 2);
+    uint32_t o[8];
+    e4m3x4_to_f16x4_scaled(w[i].x, o[0], o[1]);
+    e4m3x4_to_f16x4_scaled(w[i].y, o[2], o[3]);
+    e4m3x4_to_f16x4_scaled(w[i].z, o[4], o[5]);
+    e4m3x4_to_f16x4_scaled(w[i].w, o[6], o[7]);
+    const int cc = (item & 3) * 2;
     const uint32_t rbase = blk_s + row * 128;
     st_shared_v4(rbase + ((cc ^ (row & 7)) << 4), o[0], o[1], o[2], o[3]);
     st_shared_v4(rbase + (((cc + 1) ^ (row & 7)) << 4), o[4], o[5], o[6], o[7]);
@@ -492,14 +499,14 @@ decode_partial_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
         const int valid_rows = L - (kv_start + j * kTileKeys);
         if (ok && j >= 1) ok = mbar_wait(&ctrl->blk_free[4], (j - 1) & 1, abort_flag);
         if (ok) {
-          dequant_rows(raw, smem + kOffTileFp8, kDimBlocks - 1, 16 * dw, 16, valid_rows, dl, 32);
+          dequant_rows<2>(raw, smem + kOffTileFp8, kDimBlocks - 1, 16 * dw, valid_rows, dl);
           fence_proxy_async_smem();
           mbar_arrive(&ctrl->blk_ready[kDimBlocks - 1]);
         }
         for (int c = dw; ok && c < 8; c += 4) {
           if (j >= 1) ok = mbar_wait(&ctrl->blk_free[c / 2], (j - 1) & 1, abort_flag);
           if (!ok) break;
-          dequant_rows(raw, smem + kOffTileFp8, c, 0, kTileKeys, valid_rows, dl, 32);
+          dequant_rows<8>(raw, smem + kOffTileFp8, c, 0, valid_rows, dl);
           fence_proxy_async_smem();
           mbar_arrive(&ctrl->blk_ready[c]);
         }

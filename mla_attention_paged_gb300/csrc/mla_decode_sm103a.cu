@@ -121,6 +121,23 @@ __device__ __forceinline__ void e4m3x4_to_f16x4_scaled(uint32_t w, uint32_t& lo,
   hi = (h1 & 0x80008000u) | ((h1 >> 1) & 0x3F803F80u);
 }
 
+// The same four codes through the conversion unit (cvt e4m3x2 -> f16x2, exact), scaled by
+// 2^-8 on the FMA pipe (exact: a power of two, and every result stays an f16 value).  The
+// dequant warps decode half of each chunk this way and half with the integer ops above, so
+// that the conversion and integer pipes share the work.
+__device__ __forceinline__ void e4m3x4_to_f16x4_scaled_cvt(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  uint32_t a, b;
+  asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, l;\n\tcvt.rn.f16x2.e4m3x2 %1, h;\n\t}"
+      : "=r"(a), "=r"(b)
+      : "r"(w));
+  const __half2 k = __half2half2(__ushort_as_half(0x1C00));  // 2^-8
+  const __half2 ra = __hmul2(*reinterpret_cast<const __half2*>(&a), k);
+  const __half2 rb = __hmul2(*reinterpret_cast<const __half2*>(&b), k);
+  lo = *reinterpret_cast<const uint32_t*>(&ra);
+  hi = *reinterpret_cast<const uint32_t*>(&rb);
+}
+
 // Two bf16 -> two f16, round to nearest (exact for magnitudes in f16's normal range).
 __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t v) {
   return pack_f16x2(__uint_as_float(v << 16), __uint_as_float(v & 0xFFFF0000u));
@@ -149,8 +166,8 @@ __device__ __forceinline__ void dequant_rows(const uint8_t* raw, uint8_t* tile, 
     const int item = lane + 32 * i;
     const int row = r0 + (item >> 2);
     uint32_t o[8];
-    e4m3x4_to_f16x4_scaled(w[i].x, o[0], o[1]);
-    e4m3x4_to_f16x4_scaled(w[i].y, o[2], o[3]);
+    e4m3x4_to_f16x4_scaled_cvt(w[i].x, o[0], o[1]);
+    e4m3x4_to_f16x4_scaled_cvt(w[i].y, o[2], o[3]);
     e4m3x4_to_f16x4_scaled(w[i].z, o[4], o[5]);
     e4m3x4_to_f16x4_scaled(w[i].w, o[6], o[7]);
     const int cc = (item & 3) * 2;

@@ -12,9 +12,11 @@
 // section "TokenSpeed 性能預覽" (prefill with a long prefix KV cache, tuned softmax).
 //
 // Design on sm_103a (one CTA per (128-row query block, head, request), one CTA per SM):
-//  * Producer warp: TMA (128-byte swizzled, 3-D maps over [rows, heads, columns]) loads the
-//    query block once and streams 128-key K (192 wide) and V (128 wide) tiles of the same
-//    head through a 2-stage mbarrier ring.
+//  * Producer warp: TMA (128-byte swizzled, 4-D maps over (columns, token, column block,
+//    head), one box per operand tile) loads the query block once and streams 128-key K (192
+//    wide) and V (128 wide) tiles of the same head through two separate 2-stage mbarrier
+//    rings: a K stage is refilled as soon as its BMM1 is done, a V stage once its BMM2 is,
+//    so the K loads run ahead of the softmax instead of waiting for the whole tile.
 //  * MMA warp (uniform control flow, one elected thread issues): S = Q . K^T (M=128 rows,
 //    N=128 keys, K=192) into one of two TMEM S buffers; O += P . V (M=128, N=128, K=128)
 //    with P read straight from TMEM (the A operand) and V MN-major from shared memory.
@@ -44,16 +46,18 @@ constexpr int kQBytes = (kDqk / 64) * kQBlockBytes;    // 48 KB
 constexpr int kKVBlockBytes = kBN * 128;               // 16 KB
 constexpr int kKBytes = (kDqk / 64) * kKVBlockBytes;   // 48 KB
 constexpr int kVBytes = (kDv / 64) * kKVBlockBytes;    // 32 KB
-constexpr int kStageBytes = kKBytes + kVBytes;         // 80 KB
 
 constexpr int kOffQ = 0;
-constexpr int kOffKV = kOffQ + kQBytes;
-constexpr int kOffCtrl = kOffKV + kStages * kStageBytes;
+constexpr int kOffK = kOffQ + kQBytes;               // K ring: 2 x 48 KB
+constexpr int kOffV = kOffK + kStages * kKBytes;     // V ring: 2 x 32 KB
+constexpr int kOffCtrl = kOffV + kStages * kVBytes;
 
 struct PrefillCtrl {
   uint64_t q_full;
-  uint64_t kv_full[kStages];
-  uint64_t kv_empty[kStages];
+  uint64_t k_full[kStages];
+  uint64_t k_empty[kStages];   // BMM1 of the tile in this K stage has completed
+  uint64_t v_full[kStages];
+  uint64_t v_empty[kStages];   // BMM2 of the tile in this V stage has completed
   uint64_t s_full[2];
   uint64_t s_consumed[2];  // BMM2 has read the P held in this S buffer
   uint64_t p_full;
@@ -134,8 +138,10 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
   if (threadIdx.x == 0) {
     mbar_init(&ctrl->q_full, 1);
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(&ctrl->kv_full[s], 1);
-      mbar_init(&ctrl->kv_empty[s], 1);
+      mbar_init(&ctrl->k_full[s], 1);
+      mbar_init(&ctrl->k_empty[s], 1);
+      mbar_init(&ctrl->v_full[s], 1);
+      mbar_init(&ctrl->v_empty[s], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&ctrl->s_full[i], 1);
@@ -164,31 +170,39 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
 
   if (warp == 4) {
     // ------------------------------------------------------------------ TMA producer
-    if (lane == 0) {
-      const uint64_t pol_q = policy_evict_first();
+    // lane 0 streams the K ring, lane 1 the V ring (independent waits in divergent lanes)
+    if (lane < 2) {
+      const bool is_k = lane == 0;
       const uint64_t pol_kv = policy_evict_last();  // re-read by the other query blocks of this head
-      mbar_arrive_expect_tx(&ctrl->q_full, kQBytes);
-      // one box: 128 rows x all three 64-column blocks of head h
-      tma_load_4d(smem + kOffQ, &tm_q, &ctrl->q_full, 0, q_start + row_begin, 0, h, pol_q);
+      if (is_k) {
+        mbar_arrive_expect_tx(&ctrl->q_full, kQBytes);
+        // one box: 128 rows x all three 64-column blocks of head h
+        tma_load_4d(smem + kOffQ, &tm_q, &ctrl->q_full, 0, q_start + row_begin, 0, h, policy_evict_first());
+      }
+      uint64_t* full = is_k ? ctrl->k_full : ctrl->v_full;
+      uint64_t* empty = is_k ? ctrl->k_empty : ctrl->v_empty;
       int last_issued[kStages] = {-1, -1};
       bool ok = true;
       for (int j = 0; j < ntiles; ++j) {
         const int s = j % kStages;
         if (j >= kStages) {
-          ok = mbar_wait(&ctrl->kv_empty[s], ((j / kStages) - 1) & 1, abort_flag);
+          ok = mbar_wait(&empty[s], ((j / kStages) - 1) & 1, abort_flag);
           if (!ok) break;
         }
-        uint8_t* st = smem + kOffKV + s * kStageBytes;
         const int row = kv_start + j * kBN;
-        mbar_arrive_expect_tx(&ctrl->kv_full[s], kStageBytes);
-        tma_load_4d(st, &tm_k, &ctrl->kv_full[s], 0, row, 0, h, pol_kv);            // K: 128 rows x 3 blocks
-        tma_load_4d(st + kKBytes, &tm_v, &ctrl->kv_full[s], 0, row, 0, h, pol_kv);  // V: 128 rows x 2 blocks
+        if (is_k) {
+          mbar_arrive_expect_tx(&full[s], kKBytes);
+          tma_load_4d(smem + kOffK + s * kKBytes, &tm_k, &full[s], 0, row, 0, h, pol_kv);  // 128 rows x 3 blocks
+        } else {
+          mbar_arrive_expect_tx(&full[s], kVBytes);
+          tma_load_4d(smem + kOffV + s * kVBytes, &tm_v, &full[s], 0, row, 0, h, pol_kv);  // 128 rows x 2 blocks
+        }
         last_issued[s] = j;
       }
       if (!ok) {
-        drain_wait(&ctrl->q_full, 0);
+        if (is_k) drain_wait(&ctrl->q_full, 0);
         for (int s = 0; s < kStages; ++s)
-          if (last_issued[s] >= 0) drain_wait(&ctrl->kv_full[s], (last_issued[s] / kStages) & 1);
+          if (last_issued[s] >= 0) drain_wait(&full[s], (last_issued[s] / kStages) & 1);
       }
     }
     __syncwarp();
@@ -205,19 +219,19 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     };
     bool ok = mbar_wait(&ctrl->q_full, 0, abort_flag);
     ok = __all_sync(0xffffffffu, ok);
-    // BMM2(n2) as soon as P(n2) is ready (it frees a K/V stage and an S buffer), else
-    // BMM1(n1) once its K/V tile has landed and BMM2(n1-2) has read the P in its S buffer.
+    // BMM2(n2) as soon as P(n2) and V(n2) are ready (it frees a V stage and an S buffer),
+    // else BMM1(n1) once K(n1) has landed and BMM2(n1-2) has read the P in its S buffer.
     int n1 = 0, n2 = 0;
     unsigned long long idle_since = 0;
     while (ok && n2 < ntiles) {
       bool progressed = false;
-      if (n2 < n1 && poll(&ctrl->p_full, n2 & 1)) {
+      if (n2 < n1 && poll(&ctrl->p_full, n2 & 1) && poll(&ctrl->v_full[n2 % kStages], (n2 / kStages) & 1)) {
         tc_fence_after();
         const int s = n2 % kStages, sb = n2 & 1;
         // P: 128 rows x 16 keys per MMA, 8 TMEM columns apart.  V: 16 keys (two 8-key groups,
         // SBO apart) x 128 value columns (two 64-column blocks, LBO apart), MN-major.
         const uint64_t v_desc =
-            make_smem_desc(smem_u32(smem + kOffKV + s * kStageBytes + kKBytes), kKVBlockBytes, 1024);
+            make_smem_desc(smem_u32(smem + kOffV + s * kVBytes), kKVBlockBytes, 1024);
         const uint32_t p_tmem = tmem + kTmemS + sb * 128;
         if (elect_one()) {
 #pragma unroll
@@ -225,7 +239,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             umma_ts_bf16(tmem + kTmemO, p_tmem + kk * 8, v_desc + static_cast<uint64_t>((kk * 2048) >> 4), idesc2,
                          (n2 > 0 || kk > 0) ? 1u : 0u);
           umma_commit(&ctrl->o_done);
-          umma_commit(&ctrl->kv_empty[s]);
+          umma_commit(&ctrl->v_empty[s]);
           umma_commit(&ctrl->s_consumed[sb]);
         }
         __syncwarp();
@@ -233,10 +247,10 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         progressed = true;
       } else if (n1 < ntiles && n1 < n2 + 2) {
         const int s = n1 % kStages, sb = n1 & 1;
-        if (poll(&ctrl->kv_full[s], (n1 / kStages) & 1) &&
+        if (poll(&ctrl->k_full[s], (n1 / kStages) & 1) &&
             (n1 < 2 || poll(&ctrl->s_consumed[sb], ((n1 - 2) >> 1) & 1))) {
           tc_fence_after();
-          const uint64_t k_desc = make_smem_desc(smem_u32(smem + kOffKV + s * kStageBytes), 16, 1024);
+          const uint64_t k_desc = make_smem_desc(smem_u32(smem + kOffK + s * kKBytes), 16, 1024);
           if (elect_one()) {
 #pragma unroll
             for (int c = 0; c < kDqk / 64; ++c) {
@@ -246,6 +260,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                           k_desc + static_cast<uint64_t>((c * kKVBlockBytes + k * 32) >> 4), idesc1, (c | k) != 0);
             }
             umma_commit(&ctrl->s_full[sb]);
+            umma_commit(&ctrl->k_empty[s]);
           }
           __syncwarp();
           ++n1;

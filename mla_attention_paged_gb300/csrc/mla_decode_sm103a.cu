@@ -14,10 +14,13 @@
 // Design on sm_103a (one CTA per (64-row group, split, request); one CTA per SM):
 //  * Fold: the T*H query rows of a request are one matrix with row m = t*H + h; a CTA
 //    takes 64 consecutive rows, so all heads and drafts share each latent tile load.
-//  * Producer warp: bf16 pools are gathered by TMA (128-byte swizzled boxes of 64
-//    columns) one 64-key tile per stage from the pages named by the page table, into a
-//    2-stage ring; e4m3 pools are gathered by bulk copies of whole page rows into a 2-stage
-//    raw ring and decoded to the bf16 swizzled tile by two dequant warps (6-7).
+//  * Producer warp: bf16 pools are gathered by TMA (one 3-D box per 64-key tile: 64 rows x
+//    nine 128-byte-swizzled column blocks) from the pages named by the page table, into a
+//    2-stage ring.  For e4m3 pools, four dequant warps (6-9) read each tile's rows from the
+//    page pool into registers, wait for the stage, and write them as f16 into the same
+//    swizzled layout (exact decode, values times 2^-8; the factor is folded into the
+//    scales); the producer then only prefetches rows into L2 ahead of them.  The e4m3
+//    GEMMs run on f16 operands (Q converted once per CTA, P in f16).
 //  * MMA warp (uniform control flow, one elected thread issues): BMM1  S[rows, keys] =
 //    Q . K^T  (M=64, N=64, K=576) into TMEM, double-buffered; BMM2  O^T[dims, rows] +=
 //    V^T . P^T  (M=128 per 128 value columns, N=rows, K=64 keys) with V^T read MN-major
@@ -46,33 +49,29 @@ namespace {
 constexpr int kDimBlocks = kLatentDim / 64;          // 9 blocks of 64 columns (128 bytes)
 constexpr int kBlockBytes = 64 * 128;                // 64 rows x 128 bytes, swizzled
 constexpr int kTileBytes = kDimBlocks * kBlockBytes; // 73728: one bf16 64-key latent tile
-constexpr int kRawBytes = kTileKeys * kLatentDim;    // 36864: one e4m3 64-key tile
 constexpr int kStages = 2;
-constexpr int kPrefetchTiles = 4;  // e4m3 L2 prefetch distance beyond the shared-memory ring
+constexpr int kPrefetchTiles = 2;  // e4m3: tiles ahead of the decode that are prefetched into L2
 // warps 0-3 softmax/epilogue, 4 producer, 5 MMA; the e4m3 variant adds warps 6-9 (dequant)
 constexpr int kDequantThreads = 128;
 __host__ __device__ constexpr int threads_for(bool fp8) { return fp8 ? 192 + kDequantThreads : 192; }
 
-// Shared memory map.  bf16: Q | stage0 | stage1 | P | ctrl.
-//                     e4m3: Q | raw0 | raw1 | bf16 tile | P | ctrl  (same total).
+// Shared memory map: Q | stage0 | stage1 | P | ctrl.  A stage holds one 64-key tile as nine
+// 128-byte-swizzled column blocks: bf16 as loaded by TMA, or (e4m3) f16 as decoded by the
+// dequant warps from rows they read straight from global memory.
 constexpr int kOffQ = 0;
 constexpr int kOffStages = kOffQ + kTileBytes;
-constexpr int kOffTileFp8 = kOffStages + kStages * kRawBytes;
 constexpr int kOffP = kOffStages + kStages * kTileBytes;
 constexpr int kOffCtrl = kOffP + kBlockBytes;
-static_assert(kOffTileFp8 + kTileBytes == kOffP, "e4m3 layout must match the bf16 footprint");
 
 struct DecodeCtrl {
   uint64_t q_full;
-  uint64_t kv_full[kStages];
-  uint64_t kv_empty[kStages];
+  uint64_t kv_full[kStages];   // tile landed (bf16: TMA bytes; e4m3: dequant threads)
+  uint64_t kv_empty[kStages];  // BMM2 of the tile in this stage completed
   uint64_t s_full[2];
   uint64_t s_free[2];
   uint64_t p_full;
   uint64_t o_done;
-  uint64_t q_ready;                 // e4m3: Q converted to f16 in place
-  uint64_t blk_ready[kDimBlocks];   // e4m3: 64-column block of the f16 tile written
-  uint64_t blk_free[5];             // e4m3: f16 blocks 2g, 2g+1 (g < 4) / block 8 (g = 4) read
+  uint64_t q_ready;            // e4m3: Q converted to f16 in place
   uint64_t mma_drain;
   uint32_t tmem_base;
   int abort_flag;
@@ -143,44 +142,25 @@ __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t v) {
   return pack_f16x2(__uint_as_float(v << 16), __uint_as_float(v & 0xFFFF0000u));
 }
 
-// Decode rows [r0, r0 + 8*NI) of 64-column block c of one raw e4m3 tile (64 rows x 576
-// bytes, row-major) into block c of the 128-byte-swizzled f16 tile (64 rows x 128 bytes), as
-// values times 2^-8; rows >= valid_rows become zero.  One warp (lane = 0..31); each item is
-// 16 raw bytes (16 columns) -> two 16-byte f16 chunks, NI items per lane, all loads issued
-// before the first conversion.
-template <int NI>
-__device__ __forceinline__ void dequant_rows(const uint8_t* raw, uint8_t* tile, int c, int r0, int valid_rows,
-                                             int lane) {
-  uint4 w[NI];
-#pragma unroll
-  for (int i = 0; i < NI; ++i) {
-    const int item = lane + 32 * i;
-    const int row = r0 + (item >> 2);
-    w[i] = (row < valid_rows)
-               ? *reinterpret_cast<const uint4*>(raw + row * kLatentDim + c * 64 + (item & 3) * 16)
-               : make_uint4(0u, 0u, 0u, 0u);
-  }
-  const uint32_t blk_s = smem_u32(tile) + c * kBlockBytes;
-#pragma unroll
-  for (int i = 0; i < NI; ++i) {
-    const int item = lane + 32 * i;
-    const int row = r0 + (item >> 2);
-    uint32_t o[8];
-    e4m3x4_to_f16x4_scaled_cvt(w[i].x, o[0], o[1]);
-    e4m3x4_to_f16x4_scaled_cvt(w[i].y, o[2], o[3]);
-    e4m3x4_to_f16x4_scaled(w[i].z, o[4], o[5]);
-    e4m3x4_to_f16x4_scaled(w[i].w, o[6], o[7]);
-    const int cc = (item & 3) * 2;
-    const uint32_t rbase = blk_s + row * 128;
-    st_shared_v4(rbase + ((cc ^ (row & 7)) << 4), o[0], o[1], o[2], o[3]);
-    st_shared_v4(rbase + (((cc + 1) ^ (row & 7)) << 4), o[4], o[5], o[6], o[7]);
-  }
+// Decode 16 e4m3 codes (one 16-byte chunk of a row: 16 consecutive columns) into two 16-byte
+// f16 chunks (values times 2^-8) of a 128-byte-swizzled row.  rbase: shared address of the
+// row's 128-byte line plus 32 bytes per chunk index (chunk pair 2m, 2m+1 of the row);
+// sw: the row's swizzle (row mod 8, times 16).  Half of the codes go through the conversion
+// unit, half through the integer path, so that both pipes share the work.
+__device__ __forceinline__ void store_f16_chunk(uint32_t rbase, int sw, uint4 w) {
+  uint32_t o[8];
+  e4m3x4_to_f16x4_scaled_cvt(w.x, o[0], o[1]);
+  e4m3x4_to_f16x4_scaled_cvt(w.y, o[2], o[3]);
+  e4m3x4_to_f16x4_scaled(w.z, o[4], o[5]);
+  e4m3x4_to_f16x4_scaled(w.w, o[6], o[7]);
+  // the chunk pair sits at byte offsets 32m and 32m + 16 of the unswizzled row; rbase
+  // already holds row base + 32m
+  const uint32_t row0 = rbase & ~127u;
+  const uint32_t c0 = (rbase & 127u);
+  st_shared_v4(row0 + (c0 ^ sw), o[0], o[1], o[2], o[3]);
+  st_shared_v4(row0 + ((c0 + 16) ^ sw), o[4], o[5], o[6], o[7]);
 }
 
-// The e4m3 path fills and consumes the f16 tile's column blocks in this order: block 8 (the
-// rope columns, free as soon as the previous tile's BMM1 is done) first, then 0..7 in the
-// order the previous tile's BMM2 frees them.
-__device__ __forceinline__ int fp8_block_order(int i) { return i == 0 ? kDimBlocks - 1 : i - 1; }
 
 template <bool kFp8>
 __global__ void __launch_bounds__(threads_for(kFp8), 1)
@@ -213,8 +193,8 @@ decode_partial_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
   if (threadIdx.x == 0) {
     mbar_init(&ctrl->q_full, 1);
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(&ctrl->kv_full[s], 1);
-      mbar_init(&ctrl->kv_empty[s], kFp8 ? kDequantThreads : 1);
+      mbar_init(&ctrl->kv_full[s], kFp8 ? kDequantThreads : 1);
+      mbar_init(&ctrl->kv_empty[s], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&ctrl->s_full[i], 1);
@@ -223,9 +203,6 @@ decode_partial_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
     mbar_init(&ctrl->p_full, 128);
     mbar_init(&ctrl->o_done, 1);
     mbar_init(&ctrl->q_ready, kDequantThreads);
-    // block 8 is written by all dequant warps, blocks 0-7 by one warp each
-    for (int c = 0; c < kDimBlocks; ++c) mbar_init(&ctrl->blk_ready[c], c == kDimBlocks - 1 ? kDequantThreads : 32);
-    for (int g = 0; g < 5; ++g) mbar_init(&ctrl->blk_free[g], 1);
     mbar_init(&ctrl->mma_drain, 1);
     ctrl->abort_flag = 0;
     for (int w = 0; w < 4; ++w) ctrl->rescale_flag[w] = 0;
@@ -262,11 +239,11 @@ decode_partial_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
       mbar_arrive_expect_tx(&ctrl->q_full, kTileBytes);
       tma_load_3d(smem + kOffQ, &tm_q, &ctrl->q_full, 0, b * p.R + row0, 0, pol_q);  // all 9 column blocks
     }
-    // e4m3 only: an L2 prefetch runs kPrefetchTiles tiles ahead of the shared-memory ring
-    // (that path is bound by the dequant warps, and the prefetch hides part of each raw
-    // tile's HBM round trip).  The bf16 path measured faster without it: the extra requests
-    // queue ahead of the ring's own loads.  Page ids come from the two 32-entry windows
-    // (cur, nxt); the lookahead stays inside them.
+    // e4m3 only: the dequant warps read their rows from global memory themselves; this warp
+    // prefetches those rows into L2 kPrefetchTiles tiles ahead of the stage being refilled.
+    // (The bf16 path measured faster without any prefetch: the extra requests queue ahead of
+    // the ring's own TMA loads.)  Page ids come from the two 32-entry windows (cur, nxt); the
+    // lookahead stays inside them.
     const uint32_t row_bytes = kFp8 ? kLatentDim : kLatentDim * 2;
     const int prefetch_dist = kFp8 ? min(kPrefetchTiles, 32 / sub - 1) : 0;
     auto pid_at = [&](int pi) -> int {  // page id of page index pi in [batch_base, batch_base + 64)
@@ -337,14 +314,6 @@ decode_partial_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
                             pol_kv);
             }
           }
-        } else {
-          uint8_t* stage = smem + kOffStages + s * kRawBytes;
-          const uint32_t bytes = static_cast<uint32_t>(box_rows * kLatentDim);
-          mbar_arrive_expect_tx(&ctrl->kv_full[s], bytes * npg);
-          for (int pp = 0; pp < npg; ++pp) {
-            const uint8_t* src = p.kv_pool + (static_cast<int64_t>(pids[pp]) * P + row_in_page) * kLatentDim;
-            bulk_load(stage + pp * box_rows * kLatentDim, src, bytes, &ctrl->kv_full[s], pol_kv);
-          }
         }
       }
       last_issued[s] = j;
@@ -354,7 +323,7 @@ decode_partial_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
       // drain copies still in flight before the CTA exits
       drain_wait(&ctrl->q_full, 0);
       for (int s = 0; s < kStages; ++s)
-        if (last_issued[s] >= 0) drain_wait(&ctrl->kv_full[s], (last_issued[s] / kStages) & 1);
+        if (!kFp8 && last_issued[s] >= 0) drain_wait(&ctrl->kv_full[s], (last_issued[s] / kStages) & 1);
     }
   } else if (warp == 5) {
     // ------------------------------------------------------------------ MMA issuer (whole warp,
@@ -373,7 +342,6 @@ decode_partial_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
     };
     bool ok = kFp8 ? mbar_wait(&ctrl->q_ready, 0, abort_flag) : mbar_wait(&ctrl->q_full, 0, abort_flag);
     ok = __all_sync(0xffffffffu, ok);
-    int c1 = 0;  // e4m3: blocks of BMM1(n1) already issued, in fp8_block_order
     // Issue whichever GEMM is ready: BMM2(n2) first (it frees a stage), else BMM1(n1) for a
     // tile whose data has landed and whose S buffer is free.  BMM1 runs at most two tiles
     // ahead of BMM2 (double-buffered S).
@@ -384,7 +352,7 @@ decode_partial_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
       if (n2 < n1 && poll(&ctrl->p_full, n2 & 1)) {
         tc_fence_after();
         const int s = n2 % kStages;
-        const uint32_t kv_base = kFp8 ? smem_u32(smem + kOffTileFp8) : smem_u32(smem + kOffStages + s * kTileBytes);
+        const uint32_t kv_base = smem_u32(smem + kOffStages + s * kTileBytes);
         // V^T: 128 value columns (two 64-column blocks, LBO apart) x 16 keys (two 8-key
         // groups, SBO apart), MN-major.  P^T: rows x 16 keys, K-major.
         const uint64_t v_desc = make_smem_desc(kv_base, kBlockBytes, 1024);
@@ -397,50 +365,14 @@ decode_partial_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
               const uint64_t poff = static_cast<uint64_t>((kk * 32) >> 4);
               umma_bf16(tmem + qc * 64, v_desc + voff, p_desc + poff, idesc2, (n2 > 0 || kk > 0) ? 1u : 0u);
             }
-            if (kFp8) umma_commit(&ctrl->blk_free[qc]);  // f16 value blocks 2qc, 2qc+1 read
           }
           umma_commit(&ctrl->o_done);
-          if (!kFp8) umma_commit(&ctrl->kv_empty[s]);
+          umma_commit(&ctrl->kv_empty[s]);
         }
         __syncwarp();
         ++n2;
         progressed = true;
-      } else if (kFp8 && n1 < ntiles && n1 < n2 + 2) {
-        // e4m3: BMM1 follows the dequant warps block by block (lanes test the block
-        // barriers in parallel; consecutive decoded blocks are issued together)
-        const int sb = n1 & 1;
-        const bool r = lane >= c1 && lane < kDimBlocks &&
-                       mbar_test_wait(&ctrl->blk_ready[fp8_block_order(lane)], n1 & 1);
-        const uint32_t ready = __ballot_sync(0xffffffffu, r);
-        const int nb = __ffs(~(ready >> c1)) - 1;
-        if (nb > 0 && (c1 > 0 || n1 < 2 || poll(&ctrl->s_free[sb], ((n1 - 2) >> 1) & 1))) {
-          tc_fence_after();
-          const uint64_t k_desc = make_smem_desc(smem_u32(smem + kOffTileFp8), 16, 1024);
-          const uint32_t d = tmem + kTmemS + sb * 64;
-          const int i_end = c1 + nb;
-          if (elect_one()) {
-            for (int i = c1; i < i_end; ++i) {
-              const uint64_t boff = static_cast<uint64_t>((fp8_block_order(i) * kBlockBytes) >> 4);
-#pragma unroll
-              for (int k = 0; k < 4; ++k) {
-                const uint64_t off = boff + static_cast<uint64_t>((k * 32) >> 4);
-                umma_bf16(d, q_desc + off, k_desc + off, idesc1, (i | k) != 0);
-              }
-            }
-            if (i_end == kDimBlocks) {
-              umma_commit(&ctrl->s_full[sb]);
-              umma_commit(&ctrl->blk_free[4]);  // the rope block is only read by BMM1
-            }
-          }
-          __syncwarp();
-          c1 = i_end;
-          if (c1 == kDimBlocks) {
-            c1 = 0;
-            ++n1;
-          }
-          progressed = true;
-        }
-      } else if (!kFp8 && n1 < ntiles && n1 < n2 + 2) {
+      } else if (n1 < ntiles && n1 < n2 + 2) {
         const int s = n1 % kStages, sb = n1 & 1;
         const bool data = poll(&ctrl->kv_full[s], (n1 / kStages) & 1);
         if (data && (n1 < 2 || poll(&ctrl->s_free[sb], ((n1 - 2) >> 1) & 1))) {
@@ -487,8 +419,11 @@ decode_partial_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
     __syncwarp();
   } else if (warp >= 6) {
     // ------------------------------------------------------------------ e4m3 dequant (warps 6-9):
-    // Q to f16 in place once, then each raw tile into the f16 tile block by block, each block
-    // as soon as the previous tile has finished reading it
+    // Q to f16 in place once; then, per tile, each lane reads its rows' e4m3 bytes straight
+    // from the page pool into registers (issued before waiting for the stage, so the reads
+    // overlap the previous tile's GEMMs), waits for the stage, and writes them as f16 into
+    // the swizzled tile.  Lane dl of warp dw owns rows dl/4 + 8i (i < 8) and 16-byte chunk
+    // dl % 4 of column blocks dw and dw + 4, plus rows 16dw + dl/4 + 8i' (i' < 2) of block 8.
     if (kFp8) {
       const int td = threadIdx.x - 6 * 32;
       bool ok = mbar_wait(&ctrl->q_full, 0, abort_flag);
@@ -505,29 +440,52 @@ decode_partial_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
         fence_proxy_async_smem();
         mbar_arrive(&ctrl->q_ready);
       }
-      // Per tile: block 8 (free once the previous tile's BMM1 is done) by all four warps, 16
-      // rows each; then warp w decodes blocks w and w + 4, each as soon as the previous tile's
-      // BMM2 has read it, so the four warps work on different blocks at once.
       const int dw = td >> 5, dl = td & 31;
+      const int P = p.page_size;
+      const int32_t* pt = p.page_table + static_cast<int64_t>(b) * p.max_pages;
+      // page id of each owned row of tile j (0 past the request end: the row is not read)
+      auto row_pids = [&](int j, int (&pid)[8]) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int k = kv_start + j * kTileKeys + (dl >> 2) + 8 * i;
+          pid[i] = (k < L) ? __ldg(pt + k / P) : 0;
+        }
+      };
+      int pid_cur[8];
+      row_pids(0, pid_cur);
       for (int j = 0; ok && j < ntiles; ++j) {
         const int s = j % kStages;
-        ok = mbar_wait(&ctrl->kv_full[s], (j / kStages) & 1, abort_flag);
-        const uint8_t* raw = smem + kOffStages + s * kRawBytes;
-        const int valid_rows = L - (kv_start + j * kTileKeys);
-        if (ok && j >= 1) ok = mbar_wait(&ctrl->blk_free[4], (j - 1) & 1, abort_flag);
-        if (ok) {
-          dequant_rows<2>(raw, smem + kOffTileFp8, kDimBlocks - 1, 16 * dw, valid_rows, dl);
-          fence_proxy_async_smem();
-          mbar_arrive(&ctrl->blk_ready[kDimBlocks - 1]);
+        const int k0 = kv_start + j * kTileKeys;
+        uint4 wa[8], wb[8], w8[2];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int k = k0 + (dl >> 2) + 8 * i;
+          const uint8_t* row = p.kv_pool + (static_cast<int64_t>(pid_cur[i]) * P + k % P) * kLatentDim + (dl & 3) * 16;
+          const bool valid = k < L;
+          wa[i] = valid ? __ldg(reinterpret_cast<const uint4*>(row + dw * 64)) : make_uint4(0u, 0u, 0u, 0u);
+          wb[i] = valid ? __ldg(reinterpret_cast<const uint4*>(row + (dw + 4) * 64)) : make_uint4(0u, 0u, 0u, 0u);
+          if (i >> 1 == dw)
+            w8[i & 1] = valid ? __ldg(reinterpret_cast<const uint4*>(row + 8 * 64)) : make_uint4(0u, 0u, 0u, 0u);
         }
-        for (int c = dw; ok && c < 8; c += 4) {
-          if (j >= 1) ok = mbar_wait(&ctrl->blk_free[c / 2], (j - 1) & 1, abort_flag);
-          if (!ok) break;
-          dequant_rows<8>(raw, smem + kOffTileFp8, c, 0, valid_rows, dl);
-          fence_proxy_async_smem();
-          mbar_arrive(&ctrl->blk_ready[c]);
+        int pid_nxt[8];
+        if (j + 1 < ntiles) row_pids(j + 1, pid_nxt);
+        // the stage is free once BMM2(j - 2) has completed
+        if (j >= kStages) ok = mbar_wait(&ctrl->kv_empty[s], ((j / kStages) - 1) & 1, abort_flag);
+        if (!ok) break;
+        const uint32_t st = smem_u32(smem + kOffStages + s * kTileBytes) + (dl & 3) * 32;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int row = (dl >> 2) + 8 * i;
+          const uint32_t rbase = st + row * 128;
+          const int sw = (row & 7) << 4;
+          store_f16_chunk(rbase + dw * kBlockBytes, sw, wa[i]);
+          store_f16_chunk(rbase + (dw + 4) * kBlockBytes, sw, wb[i]);
+          if (i >> 1 == dw) store_f16_chunk(rbase + 8 * kBlockBytes, sw, w8[i & 1]);
         }
-        if (ok) mbar_arrive(&ctrl->kv_empty[s]);  // the raw stage may be refilled
+        fence_proxy_async_smem();
+        mbar_arrive(&ctrl->kv_full[s]);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) pid_cur[i] = pid_nxt[i];
       }
     }
   } else {

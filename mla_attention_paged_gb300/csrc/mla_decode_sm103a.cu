@@ -50,10 +50,11 @@ constexpr int kDimBlocks = kLatentDim / 64;          // 9 blocks of 64 columns (
 constexpr int kBlockBytes = 64 * 128;                // 64 rows x 128 bytes, swizzled
 constexpr int kTileBytes = kDimBlocks * kBlockBytes; // 73728: one bf16 64-key latent tile
 constexpr int kStages = 2;
-constexpr int kPrefetchTiles = 2;  // e4m3: tiles ahead of the decode that are prefetched into L2
-// warps 0-3 softmax/epilogue, 4 producer, 5 MMA; the e4m3 variant adds warps 6-9 (dequant)
-constexpr int kDequantThreads = 128;
-__host__ __device__ constexpr int threads_for(bool fp8) { return fp8 ? 192 + kDequantThreads : 192; }
+constexpr int kPrefetchTiles = 3;  // e4m3: tiles ahead of the decode that are prefetched into L2
+// Warps 0-3 softmax/epilogue, 5 MMA; bf16: warp 4 producer (192 threads); e4m3: warps 4, 6
+// and 7 decode (256 threads: eight warps keep the register budget at 255 per thread).
+constexpr int kDequantThreads = 96;
+__host__ __device__ constexpr int threads_for(bool fp8) { return fp8 ? 256 : 192; }
 
 // Shared memory map: Q | stage0 | stage1 | P | ctrl.  A stage holds one 64-key tile as nine
 // 128-byte-swizzled column blocks: bf16 as loaded by TMA, or (e4m3) f16 as decoded by the
@@ -215,6 +216,8 @@ decode_partial_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
   if (warp == 4 && lane == 0) {
     tma_prefetch_desc(&tm_q);
     if (!kFp8) tma_prefetch_desc(&tm_kv);
+    mbar_arrive_expect_tx(&ctrl->q_full, kTileBytes);
+    tma_load_3d(smem + kOffQ, &tm_q, &ctrl->q_full, 0, b * p.R + row0, 0, policy_evict_last());  // 9 blocks
   }
   tc_fence_before();
   __syncthreads();
@@ -222,8 +225,8 @@ decode_partial_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
   const uint32_t tmem = ctrl->tmem_base;
   volatile int* abort_flag = &ctrl->abort_flag;
 
-  if (warp == 4) {
-    // ------------------------------------------------------------------ producer
+  if (warp == 4 && !kFp8) {
+    // ------------------------------------------------------------------ producer (bf16)
     const int P = p.page_size;
     const int sub = P < kTileKeys ? kTileKeys / P : 1;  // pages per tile
     const int box_rows = P < kTileKeys ? P : kTileKeys;
@@ -234,37 +237,6 @@ decode_partial_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
     int cur = (first_page + lane <= last_page) ? __ldg(pt + first_page + lane) : 0;
     int nxt = (first_page + 32 + lane <= last_page) ? __ldg(pt + first_page + 32 + lane) : 0;
     const uint64_t pol_kv = policy_evict_first();
-    const uint64_t pol_q = policy_evict_last();
-    if (lane == 0) {
-      mbar_arrive_expect_tx(&ctrl->q_full, kTileBytes);
-      tma_load_3d(smem + kOffQ, &tm_q, &ctrl->q_full, 0, b * p.R + row0, 0, pol_q);  // all 9 column blocks
-    }
-    // e4m3 only: the dequant warps read their rows from global memory themselves; this warp
-    // prefetches those rows into L2 kPrefetchTiles tiles ahead of the stage being refilled.
-    // (The bf16 path measured faster without any prefetch: the extra requests queue ahead of
-    // the ring's own TMA loads.)  Page ids come from the two 32-entry windows (cur, nxt); the
-    // lookahead stays inside them.
-    const uint32_t row_bytes = kFp8 ? kLatentDim : kLatentDim * 2;
-    const int prefetch_dist = kFp8 ? min(kPrefetchTiles, 32 / sub - 1) : 0;
-    auto pid_at = [&](int pi) -> int {  // page id of page index pi in [batch_base, batch_base + 64)
-      const int rel = pi - batch_base;
-      const int a = __shfl_sync(0xffffffffu, cur, rel & 31);
-      const int c = __shfl_sync(0xffffffffu, nxt, rel & 31);
-      return rel < 32 ? a : c;
-    };
-    auto prefetch_tile = [&](int jt) {  // warp-uniform call
-      const int k0t = kv_start + jt * kTileKeys;
-      const int pg = k0t / P;
-      const int np = (P < kTileKeys) ? ((min(k0t + kTileKeys, L) - 1) / P - pg + 1) : 1;
-      for (int pp = 0; pp < sub; ++pp) {
-        const int pid = pid_at(pg + pp);
-        if (lane == 0 && pp < np) {
-          const int rip = (P > kTileKeys) ? (k0t % P) : 0;
-          prefetch_l2_bulk(p.kv_pool + (static_cast<int64_t>(pid) * P + rip) * row_bytes, box_rows * row_bytes);
-        }
-      }
-    };
-    for (int jt = kStages; jt < min(ntiles, kStages + prefetch_dist); ++jt) prefetch_tile(jt);
     int last_issued[kStages] = {-1, -1};
     bool ok = true;
     for (int j = 0; j < ntiles; ++j) {
@@ -298,10 +270,9 @@ decode_partial_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
         ok = __shfl_sync(0xffffffffu, w, 0);
         if (!ok) break;
       }
-      if (prefetch_dist > 0 && j + kStages + prefetch_dist < ntiles) prefetch_tile(j + kStages + prefetch_dist);
       if (lane == 0) {
         const int row_in_page = (P > kTileKeys) ? (k0 % P) : 0;
-        if (!kFp8) {
+        {
           uint8_t* stage = smem + kOffStages + s * kTileBytes;
           mbar_arrive_expect_tx(&ctrl->kv_full[s], static_cast<uint32_t>(npg * box_rows * 128 * kDimBlocks));
           if (P >= kTileKeys) {  // one 3-D box: 64 rows x all 9 column blocks
@@ -323,7 +294,7 @@ decode_partial_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
       // drain copies still in flight before the CTA exits
       drain_wait(&ctrl->q_full, 0);
       for (int s = 0; s < kStages; ++s)
-        if (!kFp8 && last_issued[s] >= 0) drain_wait(&ctrl->kv_full[s], (last_issued[s] / kStages) & 1);
+        if (last_issued[s] >= 0) drain_wait(&ctrl->kv_full[s], (last_issued[s] / kStages) & 1);
     }
   } else if (warp == 5) {
     // ------------------------------------------------------------------ MMA issuer (whole warp,
@@ -417,76 +388,101 @@ decode_partial_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
       drain_wait(&ctrl->mma_drain, 0);
     }
     __syncwarp();
-  } else if (warp >= 6) {
-    // ------------------------------------------------------------------ e4m3 dequant (warps 6-9):
+  } else if (kFp8 && warp >= 4) {
+    // ------------------------------------------------------------------ e4m3 dequant (warps 4, 6, 7):
     // Q to f16 in place once; then, per tile, each lane reads its rows' e4m3 bytes straight
     // from the page pool into registers (issued before waiting for the stage, so the reads
     // overlap the previous tile's GEMMs), waits for the stage, and writes them as f16 into
-    // the swizzled tile.  Lane dl of warp dw owns rows dl/4 + 8i (i < 8) and 16-byte chunk
-    // dl % 4 of column blocks dw and dw + 4, plus rows 16dw + dl/4 + 8i' (i' < 2) of block 8.
-    if (kFp8) {
-      const int td = threadIdx.x - 6 * 32;
-      bool ok = mbar_wait(&ctrl->q_full, 0, abort_flag);
-      if (ok) {
-        const uint32_t q_s = smem_u32(smem + kOffQ);
-        for (int c = td; c < kTileBytes / 16; c += kDequantThreads) {
-          uint32_t w0, w1, w2, w3;
-          asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                       : "=r"(w0), "=r"(w1), "=r"(w2), "=r"(w3)
-                       : "r"(q_s + c * 16));
-          st_shared_v4(q_s + c * 16, bf16x2_to_f16x2(w0), bf16x2_to_f16x2(w1), bf16x2_to_f16x2(w2),
-                       bf16x2_to_f16x2(w3));
-        }
-        fence_proxy_async_smem();
-        mbar_arrive(&ctrl->q_ready);
+    // the swizzled tile.  Lane dl of decode warp dw (0..2) owns rows dl/4 + 8i (i < 8) and
+    // 16-byte chunk dl % 4 of column blocks dw, dw + 3 and dw + 6.  Warp 4 also prefetches
+    // the rows kPrefetchTiles tiles ahead into L2.
+    const int dw = (warp == 4) ? 0 : warp - 5;
+    const int dl = lane;
+    const int td = dw * 32 + dl;
+    bool ok = mbar_wait(&ctrl->q_full, 0, abort_flag);
+    if (ok) {
+      const uint32_t q_s = smem_u32(smem + kOffQ);
+      for (int c = td; c < kTileBytes / 16; c += kDequantThreads) {
+        uint32_t w0, w1, w2, w3;
+        asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(w0), "=r"(w1), "=r"(w2), "=r"(w3)
+                     : "r"(q_s + c * 16));
+        st_shared_v4(q_s + c * 16, bf16x2_to_f16x2(w0), bf16x2_to_f16x2(w1), bf16x2_to_f16x2(w2),
+                     bf16x2_to_f16x2(w3));
       }
-      const int dw = td >> 5, dl = td & 31;
-      const int P = p.page_size;
-      const int32_t* pt = p.page_table + static_cast<int64_t>(b) * p.max_pages;
-      // page id of each owned row of tile j (0 past the request end: the row is not read)
-      auto row_pids = [&](int j, int (&pid)[8]) {
+      fence_proxy_async_smem();
+      mbar_arrive(&ctrl->q_ready);
+    }
+    const int P = p.page_size;
+    const int sub = P < kTileKeys ? kTileKeys / P : 1;  // pages per tile
+    const int32_t* pt = p.page_table + static_cast<int64_t>(b) * p.max_pages;
+    // page id of each owned row of tile j (0 past the request end: the row is not read)
+    auto row_pids = [&](int j, int (&pid)[8]) {
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const int k = kv_start + j * kTileKeys + (dl >> 2) + 8 * i;
-          pid[i] = (k < L) ? __ldg(pt + k / P) : 0;
-        }
-      };
-      int pid_cur[8];
-      row_pids(0, pid_cur);
-      for (int j = 0; ok && j < ntiles; ++j) {
-        const int s = j % kStages;
-        const int k0 = kv_start + j * kTileKeys;
-        uint4 wa[8], wb[8], w8[2];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const int k = k0 + (dl >> 2) + 8 * i;
-          const uint8_t* row = p.kv_pool + (static_cast<int64_t>(pid_cur[i]) * P + k % P) * kLatentDim + (dl & 3) * 16;
-          const bool valid = k < L;
-          wa[i] = valid ? __ldg(reinterpret_cast<const uint4*>(row + dw * 64)) : make_uint4(0u, 0u, 0u, 0u);
-          wb[i] = valid ? __ldg(reinterpret_cast<const uint4*>(row + (dw + 4) * 64)) : make_uint4(0u, 0u, 0u, 0u);
-          if (i >> 1 == dw)
-            w8[i & 1] = valid ? __ldg(reinterpret_cast<const uint4*>(row + 8 * 64)) : make_uint4(0u, 0u, 0u, 0u);
-        }
-        int pid_nxt[8];
-        if (j + 1 < ntiles) row_pids(j + 1, pid_nxt);
-        // the stage is free once BMM2(j - 2) has completed
-        if (j >= kStages) ok = mbar_wait(&ctrl->kv_empty[s], ((j / kStages) - 1) & 1, abort_flag);
-        if (!ok) break;
-        const uint32_t st = smem_u32(smem + kOffStages + s * kTileBytes) + (dl & 3) * 32;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const int row = (dl >> 2) + 8 * i;
-          const uint32_t rbase = st + row * 128;
-          const int sw = (row & 7) << 4;
-          store_f16_chunk(rbase + dw * kBlockBytes, sw, wa[i]);
-          store_f16_chunk(rbase + (dw + 4) * kBlockBytes, sw, wb[i]);
-          if (i >> 1 == dw) store_f16_chunk(rbase + 8 * kBlockBytes, sw, w8[i & 1]);
-        }
-        fence_proxy_async_smem();
-        mbar_arrive(&ctrl->kv_full[s]);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) pid_cur[i] = pid_nxt[i];
+      for (int i = 0; i < 8; ++i) {
+        const int k = kv_start + j * kTileKeys + (dl >> 2) + 8 * i;
+        pid[i] = (k < L) ? __ldg(pt + k / P) : 0;
       }
+    };
+    // L2 prefetch of tile jt's pages: lane pp < sub takes page pp (rows of this split only)
+    auto page_of = [&](int jt) -> int {  // page index of this lane's page of tile jt, or -1
+      const int k = kv_start + jt * kTileKeys + dl * P;
+      return (dw == 0 && dl < sub && jt < ntiles && k < kv_end) ? k / P : -1;
+    };
+    auto prefetch = [&](int jt, int pid) {
+      if (pid < 0) return;
+      const int k = kv_start + jt * kTileKeys + dl * P;
+      const int rows = min(min(P, kTileKeys), kv_end - k);
+      prefetch_l2_bulk(p.kv_pool + (static_cast<int64_t>(pid) * P + k % P) * kLatentDim,
+                       static_cast<uint32_t>(rows * kLatentDim));
+    };
+    int pid_cur[8];
+    row_pids(0, pid_cur);
+    int pf_pid = -1;  // page id for the prefetch of tile j + kPrefetchTiles, looked up a tile early
+    for (int jt = 1; jt <= kPrefetchTiles; ++jt) {
+      const int pg = page_of(jt);
+      if (pg >= 0) prefetch(jt, __ldg(pt + pg));
+    }
+    {
+      const int pg = page_of(1 + kPrefetchTiles);
+      pf_pid = (pg >= 0) ? __ldg(pt + pg) : -1;
+    }
+    for (int j = 0; ok && j < ntiles; ++j) {
+      const int s = j % kStages;
+      const int k0 = kv_start + j * kTileKeys;
+      uint4 w[3][8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int k = k0 + (dl >> 2) + 8 * i;
+        const uint8_t* row = p.kv_pool + (static_cast<int64_t>(pid_cur[i]) * P + k % P) * kLatentDim + (dl & 3) * 16;
+        const bool valid = k < L;
+#pragma unroll
+        for (int m = 0; m < 3; ++m)
+          w[m][i] = valid ? __ldg(reinterpret_cast<const uint4*>(row + (dw + 3 * m) * 64)) : make_uint4(0u, 0u, 0u, 0u);
+      }
+      int pid_nxt[8];
+      if (j + 1 < ntiles) row_pids(j + 1, pid_nxt);
+      prefetch(j + 1 + kPrefetchTiles, pf_pid);
+      {
+        const int pg = page_of(j + 2 + kPrefetchTiles);
+        pf_pid = (pg >= 0) ? __ldg(pt + pg) : -1;
+      }
+      // the stage is free once BMM2(j - 2) has completed
+      if (j >= kStages) ok = mbar_wait(&ctrl->kv_empty[s], ((j / kStages) - 1) & 1, abort_flag);
+      if (!ok) break;
+      const uint32_t st = smem_u32(smem + kOffStages + s * kTileBytes) + (dl & 3) * 32;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int row = (dl >> 2) + 8 * i;
+        const uint32_t rbase = st + row * 128;
+        const int sw = (row & 7) << 4;
+#pragma unroll
+        for (int m = 0; m < 3; ++m) store_f16_chunk(rbase + (dw + 3 * m) * kBlockBytes, sw, w[m][i]);
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(&ctrl->kv_full[s]);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) pid_cur[i] = pid_nxt[i];
     }
   } else {
     // ------------------------------------------------------------------ softmax + epilogue (warps 0-3)

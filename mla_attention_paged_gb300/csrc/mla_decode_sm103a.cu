@@ -311,6 +311,32 @@ decode_partial_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
       if (lane == 0) v = mbar_test_wait(bar, parity) ? 1u : 0u;
       return __shfl_sync(0xffffffffu, v, 0) != 0;
     };
+    // e4m3: lanes < sub (pages per tile) prefetch their page of tile n1 + 1 + kPrefetchTiles
+    // into L2 each time BMM1(n1) is issued, with the page id looked up one BMM1 earlier.
+    const int P = p.page_size;
+    const int sub = P < kTileKeys ? kTileKeys / P : 1;
+    const int32_t* pt = p.page_table + static_cast<int64_t>(b) * p.max_pages;
+    auto page_of = [&](int jt) -> int {  // page index of this lane's page of tile jt, or -1
+      const int k = kv_start + jt * kTileKeys + lane * P;
+      return (lane < sub && jt < ntiles && k < kv_end) ? k / P : -1;
+    };
+    auto prefetch = [&](int jt, int pid) {
+      if (pid < 0) return;
+      const int k = kv_start + jt * kTileKeys + lane * P;
+      const int rows = min(min(P, kTileKeys), kv_end - k);
+      prefetch_l2_bulk(p.kv_pool + (static_cast<int64_t>(pid) * P + k % P) * kLatentDim,
+                       static_cast<uint32_t>(rows * kLatentDim));
+    };
+    int pf_pid = -1;
+    if (kFp8) {
+      for (int jt = 1; jt <= kPrefetchTiles; ++jt) {
+        const int pg = page_of(jt);
+        if (pg >= 0) prefetch(jt, __ldg(pt + pg));
+      }
+      const int pg = page_of(1 + kPrefetchTiles);
+      pf_pid = (pg >= 0) ? __ldg(pt + pg) : -1;
+      __syncwarp();
+    }
     bool ok = kFp8 ? mbar_wait(&ctrl->q_ready, 0, abort_flag) : mbar_wait(&ctrl->q_full, 0, abort_flag);
     ok = __all_sync(0xffffffffu, ok);
     // Issue whichever GEMM is ready: BMM2(n2) first (it frees a stage), else BMM1(n1) for a
@@ -362,6 +388,12 @@ decode_partial_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
             umma_commit(&ctrl->s_full[sb]);
           }
           __syncwarp();
+          if (kFp8) {
+            prefetch(n1 + 1 + kPrefetchTiles, pf_pid);
+            const int pg = page_of(n1 + 2 + kPrefetchTiles);
+            pf_pid = (pg >= 0) ? __ldg(pt + pg) : -1;
+            __syncwarp();
+          }
           ++n1;
           progressed = true;
         }
@@ -394,8 +426,8 @@ decode_partial_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
     // from the page pool into registers (issued before waiting for the stage, so the reads
     // overlap the previous tile's GEMMs), waits for the stage, and writes them as f16 into
     // the swizzled tile.  Lane dl of decode warp dw (0..2) owns rows dl/4 + 8i (i < 8) and
-    // 16-byte chunk dl % 4 of column blocks dw, dw + 3 and dw + 6.  Warp 4 also prefetches
-    // the rows kPrefetchTiles tiles ahead into L2.
+    // 16-byte chunk dl % 4 of column blocks dw, dw + 3 and dw + 6.  (The MMA warp prefetches
+    // the rows into L2 kPrefetchTiles tiles ahead.)
     const int dw = (warp == 4) ? 0 : warp - 5;
     const int dl = lane;
     const int td = dw * 32 + dl;
@@ -414,7 +446,6 @@ decode_partial_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
       mbar_arrive(&ctrl->q_ready);
     }
     const int P = p.page_size;
-    const int sub = P < kTileKeys ? kTileKeys / P : 1;  // pages per tile
     const int32_t* pt = p.page_table + static_cast<int64_t>(b) * p.max_pages;
     // page id of each owned row of tile j (0 past the request end: the row is not read)
     auto row_pids = [&](int j, int (&pid)[8]) {
@@ -424,29 +455,8 @@ decode_partial_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
         pid[i] = (k < L) ? __ldg(pt + k / P) : 0;
       }
     };
-    // L2 prefetch of tile jt's pages: lane pp < sub takes page pp (rows of this split only)
-    auto page_of = [&](int jt) -> int {  // page index of this lane's page of tile jt, or -1
-      const int k = kv_start + jt * kTileKeys + dl * P;
-      return (dw == 0 && dl < sub && jt < ntiles && k < kv_end) ? k / P : -1;
-    };
-    auto prefetch = [&](int jt, int pid) {
-      if (pid < 0) return;
-      const int k = kv_start + jt * kTileKeys + dl * P;
-      const int rows = min(min(P, kTileKeys), kv_end - k);
-      prefetch_l2_bulk(p.kv_pool + (static_cast<int64_t>(pid) * P + k % P) * kLatentDim,
-                       static_cast<uint32_t>(rows * kLatentDim));
-    };
     int pid_cur[8];
     row_pids(0, pid_cur);
-    int pf_pid = -1;  // page id for the prefetch of tile j + kPrefetchTiles, looked up a tile early
-    for (int jt = 1; jt <= kPrefetchTiles; ++jt) {
-      const int pg = page_of(jt);
-      if (pg >= 0) prefetch(jt, __ldg(pt + pg));
-    }
-    {
-      const int pg = page_of(1 + kPrefetchTiles);
-      pf_pid = (pg >= 0) ? __ldg(pt + pg) : -1;
-    }
     for (int j = 0; ok && j < ntiles; ++j) {
       const int s = j % kStages;
       const int k0 = kv_start + j * kTileKeys;
@@ -462,11 +472,6 @@ decode_partial_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
       }
       int pid_nxt[8];
       if (j + 1 < ntiles) row_pids(j + 1, pid_nxt);
-      prefetch(j + 1 + kPrefetchTiles, pf_pid);
-      {
-        const int pg = page_of(j + 2 + kPrefetchTiles);
-        pf_pid = (pg >= 0) ? __ldg(pt + pg) : -1;
-      }
       // the stage is free once BMM2(j - 2) has completed
       if (j >= kStages) ok = mbar_wait(&ctrl->kv_empty[s], ((j / kStages) - 1) & 1, abort_flag);
       if (!ok) break;

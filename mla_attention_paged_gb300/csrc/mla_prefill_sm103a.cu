@@ -115,9 +115,28 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int qb = blockIdx.x;
   const int h = blockIdx.y;
-  const int b = blockIdx.z;
+  // Longest work first: blockIdx.z is the rank of the request by its key count (descending,
+  // ties by index) and blockIdx.x counts q blocks down from the last one, so the in-order
+  // dispatch of the grid starts the longest CTAs first and the shorter ones fill in behind
+  // them (per-CTA work spans a few hundred to a few thousand tiles across requests).
+  __shared__ int s_req;
+  int b = blockIdx.z;
+  if (p.B <= kThreads) {
+    if (threadIdx.x < p.B) {
+      const int t = threadIdx.x;
+      const int len_t = p.cu_kv[t + 1] - p.cu_kv[t];
+      int rank = 0;
+      for (int u = 0; u < p.B; ++u) {
+        const int len_u = p.cu_kv[u + 1] - p.cu_kv[u];
+        rank += (len_u > len_t || (len_u == len_t && u < t)) ? 1 : 0;
+      }
+      if (rank == static_cast<int>(blockIdx.z)) s_req = t;
+    }
+    __syncthreads();
+    b = s_req;
+  }
+  const int qb = static_cast<int>(gridDim.x) - 1 - static_cast<int>(blockIdx.x);
 
   const int q_start = p.cu_q[b];
   const int n_b = p.cu_q[b + 1] - q_start;

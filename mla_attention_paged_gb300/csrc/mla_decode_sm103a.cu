@@ -16,10 +16,10 @@
 //    takes 64 consecutive rows, so all heads and drafts share each latent tile load.
 //  * Producer warp: bf16 pools are gathered by TMA (one 3-D box per 64-key tile: 64 rows x
 //    nine 128-byte-swizzled column blocks) from the pages named by the page table, into a
-//    2-stage ring.  For e4m3 pools, four dequant warps (6-9) read each tile's rows from the
-//    page pool into registers, wait for the stage, and write them as f16 into the same
-//    swizzled layout (exact decode, values times 2^-8; the factor is folded into the
-//    scales); the producer then only prefetches rows into L2 ahead of them.  The e4m3
+//    2-stage ring.  For e4m3 pools, three dequant warps (4, 6, 7) read each tile's rows
+//    from the page pool into registers, wait for the stage, and write them as f16 into the
+//    same swizzled layout (exact decode, values times 2^-8; the factor is folded into the
+//    scales); the MMA warp prefetches rows into L2 a few tiles ahead of them.  The e4m3
 //    GEMMs run on f16 operands (Q converted once per CTA, P in f16).
 //  * MMA warp (uniform control flow, one elected thread issues): BMM1  S[rows, keys] =
 //    Q . K^T  (M=64, N=64, K=576) into TMEM, double-buffered; BMM2  O^T[dims, rows] +=

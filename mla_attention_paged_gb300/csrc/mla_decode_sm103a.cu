@@ -672,88 +672,79 @@ decode_partial_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
 // --------------------------------------------------------------------------------------
 // Combine: out[b, row] = sum_s exp(lse_s - lse) * O_s,  lse = log sum_s exp(lse_s).
 // One 128-thread CTA per (request, folded row); thread i owns value columns 4i..4i+3.
-// The split weights are computed once into shared memory; the partial rows are then read
-// as independent 16-byte loads, several splits in flight per thread.
+// Splits are taken in batches of kCombineBatch (16, or 64 when a request has more than 16
+// splits): every partial row of a batch and its log-sum-exp are loaded before any is used
+// (one memory round trip per batch), each warp reduces the batch's weights with shuffles
+// (no block-wide synchronisation), and a running maximum rescales what earlier batches
+// accumulated.  The small batch keeps registers low so that many CTAs share an SM.
 // --------------------------------------------------------------------------------------
 constexpr int kCombineThreads = 128;
-constexpr int kCombineMaxSplitsSmem = 1024;
 
+template <int kCombineBatch>
 __global__ void __launch_bounds__(kCombineThreads) decode_combine_kernel(const DecodeParams p) {
-  __shared__ float w_s[kCombineMaxSplitsSmem];
-  __shared__ float red[kCombineThreads / 32];
-  __shared__ float stat[2];
+  static_assert(kCombineBatch <= 64, "a lane holds at most two splits' log-sum-exp");
   const int row = blockIdx.x;
   const int b = blockIdx.y;
   const int tid = threadIdx.x;
+  const int lane = tid & 31;
   const int L = p.seq_lens[b];
   if (L < p.T || L > p.max_seq) return;
   const int ns = (L + p.chunk - 1) / p.chunk;
   if (ns <= 1) return;
   const int64_t base = static_cast<int64_t>(b) * p.max_splits;
   const float* lse_s = p.ws_lse + base * p.R + row;
-  // max over splits
-  float mx = -INFINITY;
-  for (int s = tid; s < ns; s += kCombineThreads) mx = fmaxf(mx, __ldg(lse_s + static_cast<int64_t>(s) * p.R));
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-  if ((tid & 31) == 0) red[tid >> 5] = mx;
-  __syncthreads();
-  if (tid == 0) {
-    float m = red[0];
-    for (int i = 1; i < kCombineThreads / 32; ++i) m = fmaxf(m, red[i]);
-    stat[0] = m;
-  }
-  __syncthreads();
-  mx = stat[0];
-  // weights (and their sum) into shared memory
-  float part = 0.f;
-  for (int s = tid; s < ns; s += kCombineThreads) {
-    const float w = (mx == -INFINITY) ? 0.f : __expf(__ldg(lse_s + static_cast<int64_t>(s) * p.R) - mx);
-    if (s < kCombineMaxSplitsSmem) w_s[s] = w;
-    part += w;
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
-  __syncthreads();
-  if ((tid & 31) == 0) red[tid >> 5] = part;
-  __syncthreads();
-  if (tid == 0) {
-    float t = 0.f;
-    for (int i = 0; i < kCombineThreads / 32; ++i) t += red[i];
-    stat[1] = t;
-  }
-  __syncthreads();
-  const float wsum = stat[1];
   // thread tid owns value columns 4*tid .. 4*tid+3: one 8-byte bf16 load per split
   const uint2* src = reinterpret_cast<const uint2*>(p.ws_o + (base * p.R + row) * kValueDim) + tid;
   const int64_t stride2 = static_cast<int64_t>(p.R) * kValueDim / 4;  // uint2s between splits
+  float m_run = -INFINITY, w_run = 0.f;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  auto fma4 = [&](float w, uint2 v) {
-    const float2 lo = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v.x));
-    const float2 hi = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v.y));
-    acc.x += w * lo.x;
-    acc.y += w * lo.y;
-    acc.z += w * hi.x;
-    acc.w += w * hi.y;
-  };
-  auto weight = [&](int s) -> float {
-    return (s < kCombineMaxSplitsSmem) ? w_s[s] : __expf(__ldg(lse_s + static_cast<int64_t>(s) * p.R) - mx);
-  };
-  int s = 0;
-  for (; s + 8 <= ns; s += 8) {  // eight independent loads in flight per thread
-    uint2 v[8];
+  for (int s0 = 0; s0 < ns; s0 += kCombineBatch) {
+    const int nb = min(kCombineBatch, ns - s0);
+    uint2 v[kCombineBatch];
 #pragma unroll
-    for (int u = 0; u < 8; ++u) v[u] = __ldg(src + (s + u) * stride2);
+    for (int u = 0; u < kCombineBatch; ++u)
+      v[u] = (u < nb) ? __ldg(src + (s0 + u) * stride2) : make_uint2(0u, 0u);
+    // lane l holds the log-sum-exp of splits s0 + l and s0 + 32 + l
+    const float l0 = (lane < nb) ? __ldg(lse_s + static_cast<int64_t>(s0 + lane) * p.R) : -INFINITY;
+    const float l1 = (kCombineBatch > 32 && lane + 32 < nb) ? __ldg(lse_s + static_cast<int64_t>(s0 + 32 + lane) * p.R) : -INFINITY;
+    float bm = fmaxf(l0, l1);
 #pragma unroll
-    for (int u = 0; u < 8; ++u) fma4(weight(s + u), v[u]);
+    for (int o = 16; o > 0; o >>= 1) bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, o));
+    const float m_new = fmaxf(m_run, bm);
+    if (m_new != -INFINITY) {
+      const float c = __expf(m_run - m_new);  // 0 while nothing has been accumulated
+      acc.x *= c;
+      acc.y *= c;
+      acc.z *= c;
+      acc.w *= c;
+      w_run *= c;
+      m_run = m_new;
+    }
+    const float w0 = (m_new == -INFINITY) ? 0.f : __expf(l0 - m_new);
+    const float w1 = (m_new == -INFINITY) ? 0.f : __expf(l1 - m_new);
+    float ws = w0 + w1;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ws += __shfl_xor_sync(0xffffffffu, ws, o);
+    w_run += ws;
+#pragma unroll
+    for (int u = 0; u < kCombineBatch; ++u) {
+      if (u < nb) {  // nb is uniform across the CTA
+        const float w = __shfl_sync(0xffffffffu, u < 32 ? w0 : w1, u & 31);
+        const float2 lo = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v[u].x));
+        const float2 hi = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v[u].y));
+        acc.x += w * lo.x;
+        acc.y += w * lo.y;
+        acc.z += w * hi.x;
+        acc.w += w * hi.y;
+      }
+    }
   }
-  for (; s < ns; ++s) fma4(weight(s), __ldg(src + s * stride2));
-  const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+  const float inv = w_run > 0.f ? 1.f / w_run : 0.f;
   uint2 pk;
   pk.x = pack_bf16x2(acc.x * inv, acc.y * inv);
   pk.y = pack_bf16x2(acc.z * inv, acc.w * inv);
   *reinterpret_cast<uint2*>(p.out + (static_cast<int64_t>(b) * p.R + row) * kValueDim + tid * 4) = pk;
-  if (tid == 0) p.lse[static_cast<int64_t>(b) * p.R + row] = (wsum > 0.f) ? (mx + __logf(wsum)) : -INFINITY;
+  if (tid == 0) p.lse[static_cast<int64_t>(b) * p.R + row] = (w_run > 0.f) ? (m_run + __logf(w_run)) : -INFINITY;
 }
 
 // Watchdog self-test: wait on an mbarrier that nothing ever arrives on, through the same
@@ -804,7 +795,10 @@ cudaError_t launch_selftest_timeout(unsigned* status, cudaStream_t stream) {
 
 cudaError_t launch_decode_combine(const DecodeParams& p, cudaStream_t stream) {
   dim3 grid(p.R, p.B);
-  decode_combine_kernel<<<grid, kCombineThreads, 0, stream>>>(p);
+  if (p.max_splits <= 16)
+    decode_combine_kernel<16><<<grid, kCombineThreads, 0, stream>>>(p);
+  else
+    decode_combine_kernel<64><<<grid, kCombineThreads, 0, stream>>>(p);
   return cudaGetLastError();
 }
 

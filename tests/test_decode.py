@@ -115,6 +115,15 @@ def test_decode_split_counts_agree(mla, oracle_mod, num_sms):
         assert plan.max_splits > 1
 
 
+@pytest.mark.parametrize("kv", ["bf16", "e4m3"])
+def test_decode_combine_many_splits(mla, oracle_mod, kv):
+    """More than 64 splits per request: the combine takes its splits in several batches and
+    rescales the running sum between them; a ragged batch mixes 2 to ~80 splits."""
+    wl = DecodeWorkload("manysplits", 3, 2, 16, [20000, 300, 17000], kv_dtype=kv, seed=78, peaked=True)
+    _, _, plan = _full_check(mla, oracle_mod, wl, num_sms=100000)
+    assert plan.max_splits > 64
+
+
 def test_decode_page_shuffle_invariance_bitwise(mla):
     wl = DecodeWorkload("shuffle", 2, 4, 16, [1500, 777], seed=5, extra_pages=7)
     inp = make_decode_inputs(wl, "cpu")

@@ -66,7 +66,28 @@ def prefill_flops(wl):
     return 2 * wl.heads * (192 + 128) * keys
 
 
-def measure_decode_extra(mla, name, dev, steps=50):
+def graph_ms_per_call(fn, n, stream):
+    """Capture fn(0..n-1) into one CUDA graph, replay it once to warm up, then time one
+    replay between two CUDA events on `stream`; returns milliseconds per call.  (Events
+    between kernels inside a graph were measured to add ~6 us each on this part, so a
+    kernel's duration is taken over n back-to-back launches instead.)"""
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for i in range(n):
+            fn(i)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        g.replay()
+        a.record(stream)
+        g.replay()
+        b.record(stream)
+    stream.synchronize()
+    ms = a.elapsed_time(b) / n
+    del g
+    return ms
+
+
+def measure_decode_extra(mla, name, dev, steps=200):
     """Secondary decode measurement (device time per call, partial-kernel roofline)."""
     wl = decode_workloads()[name]
     kv_bytes, alg_bytes = decode_bytes(wl)
@@ -83,65 +104,52 @@ def measure_decode_extra(mla, name, dev, steps=50):
     out = torch.empty(wl.batch, wl.q_len, wl.heads, 512, dtype=torch.bfloat16, device=dev)
     lse = torch.empty(wl.batch, wl.q_len, wl.heads, dtype=torch.float32, device=dev)
     st = torch.cuda.Stream(device=dev)
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+
+    def call(i):
+        s = sets[i % n_sets]
+        mla.decode(plan, s.q, s.kv_pool, s.page_table, s.seq_lens, s.scale, s.kv_scale, out=out, lse=lse,
+                   workspace=ws_buf, stream=st)
+
+    def partial(i):
+        s = sets[i % n_sets]
+        mla.decode_partial(plan, s.q, s.kv_pool, s.page_table, s.seq_lens, s.scale, s.kv_scale, out=out, lse=lse,
+                           workspace=ws_buf, stream=st)
+
     with torch.cuda.stream(st):
-        for a, b in ev:
-            a.record(st)
-            b.record(st)
         for i in range(5):
-            s = sets[i % n_sets]
-            mla.decode(plan, s.q, s.kv_pool, s.page_table, s.seq_lens, s.scale, s.kv_scale, out=out, lse=lse,
-                       workspace=ws_buf, stream=st)
-        st.synchronize()
-        start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        start.record(st)
-        for i in range(steps):
-            s = sets[i % n_sets]
-            mla.set_profile_events(ev[i][0], ev[i][1])
-            mla.decode(plan, s.q, s.kv_pool, s.page_table, s.seq_lens, s.scale, s.kv_scale, out=out, lse=lse,
-                       workspace=ws_buf, stream=st)
-        mla.set_profile_events(None, None)
-        stop.record(st)
+            call(i)
     st.synchronize()
+    call_ms = graph_ms_per_call(call, steps, st)
+    part_ms = graph_ms_per_call(partial, steps, st)
     assert mla.get_status(st) == mla.MLA_OK
-    call_ms = start.elapsed_time(stop) / steps
-    part_ms = statistics.median(mla.profile_elapsed_ms(a, b) for a, b in ev)
     peak = _peaks()
     del sets
     return {"workload": name, "us_per_call": call_ms * 1e3, "kv_gbs": kv_bytes / (call_ms / 1e3) / 1e9,
             "partial_us": part_ms * 1e3, "partial_gbs": alg_bytes / (part_ms / 1e3) / 1e9,
             "hbm_frac": alg_bytes / (part_ms / 1e3) / 1e9 / peak["hbm_gbs"],
             "tflops": decode_flops(wl) / (call_ms / 1e3) / 1e12, "splits": plan.max_splits,
-            "timing": "eager calls, L2 " + ("rotated sets" if n_sets > 1 else "inputs > L2")}
+            "timing": "CUDA graph of back-to-back calls (partial: of partial-kernel launches alone), "
+                      "L2 " + ("rotated sets" if n_sets > 1 else "inputs > L2")}
 
 
-def measure_prefill(mla, dev, steps=5):
+def measure_prefill(mla, dev, steps=10):
     from mla_attention_paged_gb300.inputs import make_prefill_inputs, prefill_workloads
     wl = prefill_workloads()["prefill_b5_h16_prefix"]
     inp = make_prefill_inputs(wl, dev)
     out = torch.empty(inp.q.shape[0], wl.heads, 128, dtype=torch.bfloat16, device=dev)
     lse = torch.empty(inp.q.shape[0], wl.heads, dtype=torch.float32, device=dev)
     st = torch.cuda.Stream(device=dev)
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
 
-    def call():
+    def call(i=0):
         mla.prefill_varlen(inp.q, inp.k, inp.v, inp.cu_seqlens_q, inp.cu_seqlens_kv, inp.prefix_lens,
                            inp.max_seqlen_q, inp.scale, out=out, lse=lse, stream=st)
 
     with torch.cuda.stream(st):
-        for a, b in ev:
-            a.record(st)
-            b.record(st)
         for _ in range(2):
             call()
-        st.synchronize()
-        for i in range(steps):
-            mla.set_profile_events(ev[i][0], ev[i][1])
-            call()
-        mla.set_profile_events(None, None)
     st.synchronize()
+    ms = graph_ms_per_call(call, steps, st)
     assert mla.get_status(st) == mla.MLA_OK
-    ms = statistics.median(mla.profile_elapsed_ms(a, b) for a, b in ev)
     fl = prefill_flops(wl)
     peak = _peaks()
     tf = fl / (ms / 1e3) / 1e12
@@ -368,23 +376,28 @@ def main():
     stream.synchronize()
     assert mla.get_status(stream) == mla.MLA_OK
 
-    # Timed region: one CUDA graph holding exactly K steps; the first (up to) 256 steps
-    # carry event pairs around the split-KV partial kernel.
-    n_ev = min(args.steps, 256)
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_ev)]
-    for a, b in ev:  # torch creates the CUDA events lazily, on first record
-        a.record(stream)
-        b.record(stream)
-    stream.synchronize()
+    # Timed region: one CUDA graph holding exactly K steps (no event nodes inside it: an
+    # event recorded between two kernels of a graph was measured to add ~6 us per call).
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph, stream=stream):
         for i in range(args.steps):
-            if i < n_ev:
-                mla.set_profile_events(ev[i][0], ev[i][1])
-            elif i == n_ev:
-                mla.set_profile_events(None, None)
             step(i, stream)
-    mla.set_profile_events(None, None)
+    stream.synchronize()
+
+    # Duration of the dominant kernel: the split-KV partial kernel alone, launched back to
+    # back (same rotated inputs) in a second graph, timed between one pair of CUDA events on
+    # the launch stream, right after the timed replay and under the same clock sampling.
+    n_k = min(args.steps, 400)
+
+    def partial_step(i):
+        s = sets[i % n_sets]
+        mla.decode_partial(plan, s.q, s.kv_pool, s.page_table, s.seq_lens, s.scale, 1.0, out=outs[i % n_sets],
+                           lse=lses[i % n_sets], workspace=ws_buf, stream=stream)
+
+    kgraph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(kgraph, stream=stream):
+        for i in range(n_k):
+            partial_step(i)
     stream.synchronize()
     # pre-roll under the clock sampler, then the timed replay
     sampler = ClockSampler(local)
@@ -394,6 +407,7 @@ def main():
             graph.replay()
             stream.synchronize()
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    kstart, kstop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     _barrier(ws)
     torch.cuda.synchronize(dev)
     with torch.cuda.stream(stream):
@@ -403,6 +417,12 @@ def main():
     stream.synchronize()
     torch.cuda.synchronize(dev)
     _barrier(ws)
+    with torch.cuda.stream(stream):
+        kgraph.replay()  # warm
+        kstart.record(stream)
+        kgraph.replay()
+        kstop.record(stream)
+    stream.synchronize()
     clocks = sampler.stop()
     status = mla.get_status(stream)
     if status != mla.MLA_OK:
@@ -411,7 +431,7 @@ def main():
     ms_max = _max_over_ranks(ms, ws, dev)
     total_bytes = _sum_over_ranks(kv_bytes * args.steps, ws, dev)
     value = total_bytes / (ms_max / 1e3) / 1e9
-    part_ms = statistics.mean(mla.profile_elapsed_ms(a, b) for a, b in ev)
+    part_ms = kstart.elapsed_time(kstop) / n_k
     peaks = _peaks()
     achieved = alg_bytes / (part_ms / 1e3) / 1e9
     traffic = _traffic_record("mla_decode_sm103a.cu")
@@ -465,6 +485,8 @@ def main():
                      "frac": achieved / peaks["hbm_gbs"],
                      "traffic": (traffic["dram_bytes_per_launch"] if traffic else None),
                      "kernel": "decode_partial_bf16_kernel", "kernel_us": part_ms * 1e3,
+                     "kernel_timing": f"{n_k} back-to-back launches of the partial kernel in one CUDA graph "
+                                      "between two CUDA events on the launch stream",
                      "alg_bytes_per_launch": alg_bytes, "peak_source": peaks["source"]},
         "e2e": {"value": e2e_val, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "steps": e2e_steps, "us_per_call": e2e_s / e2e_steps * 1e6},
@@ -476,7 +498,7 @@ def main():
         line["cpu_baseline"] = cpu_baseline(wl, inp_cpu)
     if not args.no_extra:
         # the other hot-path rows, measured on their own (not part of `value`)
-        del sets, host_in, dev_in, host_out, graph
+        del sets, host_in, dev_in, host_out, graph, kgraph
         torch.cuda.empty_cache()
         line["extra"] = {"prefill": measure_prefill(mla, dev)}
         for name in ["decode_bf16_b16_q4_h16_l64k", "decode_fp8_b16_q4_h16_l64k"]:

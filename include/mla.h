@@ -120,6 +120,33 @@ int mla_decode(const mla_decode_plan_t* plan, const void* q, const void* kv_page
                float scale, float kv_scale, void* out, float* lse, void* workspace,
                size_t workspace_bytes, void* stream);
 
+/* The two stages of mla_decode, for callers that schedule them apart (e.g. to put other
+ * work between them, or to time the split-KV partial kernel on its own).  The TokenSpeed
+ * talk ("构建面向 Agentic 推理的下一代 LLM 推理引擎", section "Kernel：让 MLA 真正跑满 GPU")
+ * describes the kernel as a split-KV partial stage followed by a reduction stage; these
+ * calls expose that split.  mla_decode(...) is exactly mla_decode_partial(...) followed by
+ * mla_decode_combine(...) on the same stream with the same plan, workspace, out and lse.
+ *
+ * mla_decode_partial: arguments, layouts and errors as mla_decode.  Enqueues the split-KV
+ * partial kernel only.  Requests whose plan gives them one split get their final out/lse
+ * rows; the others leave per-split bf16 partial outputs and fp32 log-sum-exps in the
+ * workspace, which stay valid until the workspace is next written.
+ *
+ * mla_decode_combine: merges those partials into out/lse (log-sum-exp weighted mean over
+ * the splits of each request).  plan, seq_lens, q_len, num_heads, out, lse and workspace
+ * must be the ones given to the mla_decode_partial call it completes, stream-ordered
+ * after it.  Enqueues nothing when no request has more than one split.  Errors:
+ * MLA_ERR_INVALID_ARG (null plan/seq_lens/out/lse, q_len/num_heads differ from the plan,
+ * out not 16-byte or lse not 4-byte aligned, workspace missing or not 256-byte aligned),
+ * MLA_ERR_WORKSPACE_TOO_SMALL, MLA_ERR_CUDA (launch failure). */
+int mla_decode_partial(const mla_decode_plan_t* plan, const void* q, const void* kv_pages,
+                       const int32_t* page_table, const int32_t* seq_lens, int q_len, int num_heads,
+                       float scale, float kv_scale, void* out, float* lse, void* workspace,
+                       size_t workspace_bytes, void* stream);
+int mla_decode_combine(const mla_decode_plan_t* plan, const int32_t* seq_lens, int q_len,
+                       int num_heads, void* out, float* lse, void* workspace,
+                       size_t workspace_bytes, void* stream);
+
 /* mla_decode for callers that cannot allocate device memory.  (The pages have no
  * counterpart: this is a library convenience.)  Some callers cannot call cudaMalloc, e.g.
  * a serving engine whose memory manager gives every free byte of the device to its

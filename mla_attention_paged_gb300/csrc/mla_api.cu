@@ -207,15 +207,26 @@ int mla_decode_plan(int batch, const int32_t* seq_lens_host, int q_len, int num_
   return MLA_OK;
 }
 
-int mla_decode(const mla_decode_plan_t* plan, const void* q, const void* kv_pages, const int32_t* page_table,
-               const int32_t* seq_lens, int q_len, int num_heads, float scale, float kv_scale, void* out,
-               float* lse, void* workspace, size_t workspace_bytes, void* stream) {
-  if (!plan || !q || !kv_pages || !page_table || !seq_lens || !out || !lse) return MLA_ERR_INVALID_ARG;
+}  // extern "C"
+
+namespace {
+
+constexpr int kStagePartial = 1;
+constexpr int kStageCombine = 2;
+
+// The two stages of a decode call.  The partial stage needs q, the pages and the page table;
+// the combine stage reads only the lengths, the workspace and writes out/lse.
+int decode_stages(const mla_decode_plan_t* plan, const void* q, const void* kv_pages, const int32_t* page_table,
+                  const int32_t* seq_lens, int q_len, int num_heads, float scale, float kv_scale, void* out,
+                  float* lse, void* workspace, size_t workspace_bytes, void* stream, int stages) {
+  const bool partial = (stages & kStagePartial) != 0;
+  if (!plan || !seq_lens || !out || !lse) return MLA_ERR_INVALID_ARG;
+  if (partial && (!q || !kv_pages || !page_table)) return MLA_ERR_INVALID_ARG;
   if (q_len != plan->q_len || num_heads != plan->num_heads || plan->rows != q_len * num_heads)
     return MLA_ERR_INVALID_ARG;
-  if (!aligned(q, 16) || !aligned(kv_pages, 16) || !aligned(out, 16) || !aligned(lse, 4))
-    return MLA_ERR_INVALID_ARG;
-  if (!(scale > 0.f) || !(kv_scale > 0.f)) return MLA_ERR_INVALID_ARG;
+  if (!aligned(out, 16) || !aligned(lse, 4)) return MLA_ERR_INVALID_ARG;
+  if (partial && (!aligned(q, 16) || !aligned(kv_pages, 16))) return MLA_ERR_INVALID_ARG;
+  if (partial && (!(scale > 0.f) || !(kv_scale > 0.f))) return MLA_ERR_INVALID_ARG;
   if (plan->workspace_bytes > 0) {
     if (!workspace) return MLA_ERR_INVALID_ARG;
     if (workspace_bytes < plan->workspace_bytes) return MLA_ERR_WORKSPACE_TOO_SMALL;
@@ -229,14 +240,15 @@ int mla_decode(const mla_decode_plan_t* plan, const void* q, const void* kv_page
   // 3-D box {64 columns, n rows, 9 blocks} lands a whole row range as the nine 128-byte
   // swizzled column blocks the MMAs read, in a single TMA instruction.
   CUtensorMap tm_q, tm_kv;
-  {
+  memset(&tm_q, 0, sizeof tm_q);
+  if (partial) {
     const uint64_t dims[3] = {64, static_cast<uint64_t>(plan->batch) * plan->rows, kLatentDim / 64};
     const uint64_t strides[2] = {row_bytes, 128};
     const uint32_t box[3] = {64, static_cast<uint32_t>(kGroupRows), kLatentDim / 64};
     if (!make_map(&tm_q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, q, dims, strides, box)) return MLA_ERR_CUDA;
   }
   memset(&tm_kv, 0, sizeof tm_kv);
-  if (plan->kv_dtype == MLA_KV_BF16) {  // e4m3 pages are fetched with untiled bulk copies
+  if (partial && plan->kv_dtype == MLA_KV_BF16) {  // e4m3 pages are fetched with untiled bulk copies
     const uint64_t rows = static_cast<uint64_t>(plan->num_pages) * plan->page_size;
     if (plan->page_size >= kTileKeys) {  // a 64-key tile is one row range of one page
       const uint64_t dims[3] = {64, rows, kLatentDim / 64};
@@ -276,13 +288,40 @@ int mla_decode(const mla_decode_plan_t* plan, const void* q, const void* kv_page
   }
   p.status = status;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (g_prof_start && record_event(g_prof_start, s) != cudaSuccess) return MLA_ERR_CUDA;
-  if (launch_decode_partial(p, tm_q, tm_kv, plan->head_groups, s) != cudaSuccess) return MLA_ERR_CUDA;
-  if (g_prof_stop && record_event(g_prof_stop, s) != cudaSuccess) return MLA_ERR_CUDA;
-  if (plan->max_splits > 1) {
+  if (partial) {
+    if (g_prof_start && record_event(g_prof_start, s) != cudaSuccess) return MLA_ERR_CUDA;
+    if (launch_decode_partial(p, tm_q, tm_kv, plan->head_groups, s) != cudaSuccess) return MLA_ERR_CUDA;
+    if (g_prof_stop && record_event(g_prof_stop, s) != cudaSuccess) return MLA_ERR_CUDA;
+  }
+  if ((stages & kStageCombine) && plan->max_splits > 1) {
     if (launch_decode_combine(p, s) != cudaSuccess) return MLA_ERR_CUDA;
   }
   return MLA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int mla_decode(const mla_decode_plan_t* plan, const void* q, const void* kv_pages, const int32_t* page_table,
+               const int32_t* seq_lens, int q_len, int num_heads, float scale, float kv_scale, void* out,
+               float* lse, void* workspace, size_t workspace_bytes, void* stream) {
+  return decode_stages(plan, q, kv_pages, page_table, seq_lens, q_len, num_heads, scale, kv_scale, out, lse,
+                       workspace, workspace_bytes, stream, kStagePartial | kStageCombine);
+}
+
+int mla_decode_partial(const mla_decode_plan_t* plan, const void* q, const void* kv_pages,
+                       const int32_t* page_table, const int32_t* seq_lens, int q_len, int num_heads, float scale,
+                       float kv_scale, void* out, float* lse, void* workspace, size_t workspace_bytes,
+                       void* stream) {
+  return decode_stages(plan, q, kv_pages, page_table, seq_lens, q_len, num_heads, scale, kv_scale, out, lse,
+                       workspace, workspace_bytes, stream, kStagePartial);
+}
+
+int mla_decode_combine(const mla_decode_plan_t* plan, const int32_t* seq_lens, int q_len, int num_heads,
+                       void* out, float* lse, void* workspace, size_t workspace_bytes, void* stream) {
+  return decode_stages(plan, nullptr, nullptr, nullptr, seq_lens, q_len, num_heads, 1.f, 1.f, out, lse, workspace,
+                       workspace_bytes, stream, kStageCombine);
 }
 
 int mla_prefill_varlen(const void* q, const void* k, const void* v, const int32_t* cu_seqlens_q,

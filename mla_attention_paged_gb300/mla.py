@@ -24,7 +24,7 @@ MLA_ERR_DEVICE_ARG = 6
 MLA_KV_BF16 = 0
 MLA_KV_E4M3 = 1
 
-EXPORTED = ["mla_decode_plan", "mla_decode", "mla_prefill_varlen", "mla_get_status",
+EXPORTED = ["mla_decode_plan", "mla_decode", "mla_decode_partial", "mla_decode_combine", "mla_prefill_varlen", "mla_get_status",
             "mla_status_string", "mla_version", "mla_set_profile_events", "mla_profile_elapsed_ms",
             "mla_selftest_wait_timeout"]
 
@@ -56,6 +56,10 @@ def _load() -> ctypes.CDLL:
     lib.mla_decode_plan.argtypes = [i32, P, i32, i32, i32, i32, i64, i32, i32, ctypes.POINTER(DecodePlan)]
     lib.mla_decode.restype = i32
     lib.mla_decode.argtypes = [ctypes.POINTER(DecodePlan), P, P, P, P, i32, i32, f32, f32, P, P, P, sz, P]
+    lib.mla_decode_partial.restype = i32
+    lib.mla_decode_partial.argtypes = [ctypes.POINTER(DecodePlan), P, P, P, P, i32, i32, f32, f32, P, P, P, sz, P]
+    lib.mla_decode_combine.restype = i32
+    lib.mla_decode_combine.argtypes = [ctypes.POINTER(DecodePlan), P, i32, i32, P, P, P, sz, P]
     lib.mla_prefill_varlen.restype = i32
     lib.mla_prefill_varlen.argtypes = [P, P, P, P, P, P, i32, i32, i32, i32, i32, f32, P, P, P]
     lib.mla_get_status.restype = i32
@@ -129,6 +133,38 @@ def decode(plan: DecodePlan, q: torch.Tensor, kv_pages: torch.Tensor, page_table
                         int(H), float(scale), float(kv_scale), _ptr(out), _ptr(lse), _ptr(workspace),
                         int(ws_bytes), _stream_handle(stream))
     _check(rc, "mla_decode")
+    return out, lse
+
+
+def decode_partial(plan: DecodePlan, q: torch.Tensor, kv_pages: torch.Tensor, page_table: torch.Tensor,
+                   seq_lens: torch.Tensor, scale: float, kv_scale: float = 1.0, out=None, lse=None,
+                   workspace=None, stream=None):
+    """mla_decode_partial through the C ABI (stage 1 of decode): returns (out, lse, workspace);
+    multi-split requests are finished by decode_combine with the same out/lse/workspace."""
+    B, T, H, D = q.shape
+    if out is None:
+        out = torch.empty(B, T, H, 512, dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.empty(B, T, H, dtype=torch.float32, device=q.device)
+    if workspace is None and plan.workspace_bytes:
+        workspace = workspace_for(plan, q.device)
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    rc = lib.mla_decode_partial(ctypes.byref(plan), _ptr(q), _ptr(kv_pages), _ptr(page_table), _ptr(seq_lens),
+                                int(T), int(H), float(scale), float(kv_scale), _ptr(out), _ptr(lse),
+                                _ptr(workspace), int(ws_bytes), _stream_handle(stream))
+    _check(rc, "mla_decode_partial")
+    return out, lse, workspace
+
+
+def decode_combine(plan: DecodePlan, seq_lens: torch.Tensor, out: torch.Tensor, lse: torch.Tensor, workspace=None,
+                   stream=None):
+    """mla_decode_combine through the C ABI (stage 2 of decode): merges the split partials
+    left in `workspace` by decode_partial into out/lse."""
+    B, T, H, _ = out.shape
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    rc = lib.mla_decode_combine(ctypes.byref(plan), _ptr(seq_lens), int(T), int(H), _ptr(out), _ptr(lse),
+                                _ptr(workspace), int(ws_bytes), _stream_handle(stream))
+    _check(rc, "mla_decode_combine")
     return out, lse
 
 

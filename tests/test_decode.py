@@ -124,6 +124,26 @@ def test_decode_combine_many_splits(mla, oracle_mod, kv):
     assert plan.max_splits > 64
 
 
+@pytest.mark.parametrize("kv,num_sms", [("bf16", 0), ("e4m3", 0), ("bf16", 1)], ids=["bf16", "e4m3", "one_split"])
+def test_decode_stages_equal_decode_bitwise(mla, kv, num_sms):
+    """mla_decode_partial then mla_decode_combine gives mla_decode's bits (multi-split and
+    single-split plans; the combine enqueues nothing for the latter)."""
+    wl = DecodeWorkload("stages", 3, 4, 16, [5000, 130, 2999], kv_dtype=kv, seed=79, peaked=True)
+    inp = make_decode_inputs(wl, "cuda")
+    kvd = mla.MLA_KV_E4M3 if kv == "e4m3" else mla.MLA_KV_BF16
+    plan = mla.decode_plan(wl.seq_lens, wl.q_len, wl.heads, wl.page_size, inp.page_table.shape[1],
+                           inp.kv_pool.shape[0], kvd, num_sms)
+    assert (plan.max_splits > 1) == (num_sms == 0)
+    out1, lse1 = mla.decode(plan, inp.q, inp.kv_pool, inp.page_table, inp.seq_lens, inp.scale, inp.kv_scale)
+    out2, lse2, ws = mla.decode_partial(plan, inp.q, inp.kv_pool, inp.page_table, inp.seq_lens, inp.scale,
+                                        inp.kv_scale)
+    mla.decode_combine(plan, inp.seq_lens, out2, lse2, workspace=ws)
+    torch.cuda.synchronize()
+    assert mla.get_status() == mla.MLA_OK
+    assert torch.equal(out1.view(torch.int16), out2.view(torch.int16))
+    assert torch.equal(lse1.view(torch.int32), lse2.view(torch.int32))
+
+
 def test_decode_page_shuffle_invariance_bitwise(mla):
     wl = DecodeWorkload("shuffle", 2, 4, 16, [1500, 777], seed=5, extra_pages=7)
     inp = make_decode_inputs(wl, "cpu")

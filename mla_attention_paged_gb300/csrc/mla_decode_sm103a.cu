@@ -663,6 +663,8 @@ decode_partial_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
   tc_fence_before();
   __syncthreads();
   if (threadIdx.x == 0 && ctrl->abort_flag) atomicOr(p.status, kStatusTimeout);
+  // every store of this CTA is issued: the combine grid may be scheduled now
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (warp == 5) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
@@ -671,19 +673,24 @@ decode_partial_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
 
 // --------------------------------------------------------------------------------------
 // Combine: out[b, row] = sum_s exp(lse_s - lse) * O_s,  lse = log sum_s exp(lse_s).
-// One 128-thread CTA per (request, folded row); thread i owns value columns 4i..4i+3.
-// Splits are taken in batches of kCombineBatch (16, or 64 when a request has more than 16
-// splits): every partial row of a batch and its log-sum-exp are loaded before any is used
-// (one memory round trip per batch), each warp reduces the batch's weights with shuffles
-// (no block-wide synchronisation), and a running maximum rescales what earlier batches
-// accumulated.  The small batch keeps registers low so that many CTAs share an SM.
+// One 128-thread CTA per (request, kCombineRows folded rows).  One thread copies the rows'
+// partials of a batch of splits (each a contiguous 1 KB per row) into shared memory with
+// bulk copies, so that the TMA engine rather than per-thread loads moves them; meanwhile
+// each warp loads its row's log-sum-exps and reduces the weights with shuffles.  Thread t
+// then accumulates value columns 8(t%64)..8(t%64)+7 of row t/64 from shared memory.  A
+// running maximum rescales earlier batches when a request has more than kCombineBatch
+// splits.
 // --------------------------------------------------------------------------------------
-constexpr int kCombineThreads = 128;
+constexpr int kCombineRows = 2;
+constexpr int kCombineThreads = 64 * kCombineRows;
+constexpr int kCombineBatch = 32;  // splits staged per round (lane l holds split s0 + l)
+constexpr int kCombineRowBytes = kValueDim * 2;
 
-template <int kCombineBatch>
 __global__ void __launch_bounds__(kCombineThreads) decode_combine_kernel(const DecodeParams p) {
-  static_assert(kCombineBatch <= 64, "a lane holds at most two splits' log-sum-exp");
-  const int row = blockIdx.x;
+  extern __shared__ __align__(128) uint8_t cs[];  // [split][row][512] bf16
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  const int row0 = blockIdx.x * kCombineRows;
   const int b = blockIdx.y;
   const int tid = threadIdx.x;
   const int lane = tid & 31;
@@ -691,60 +698,91 @@ __global__ void __launch_bounds__(kCombineThreads) decode_combine_kernel(const D
   if (L < p.T || L > p.max_seq) return;
   const int ns = (L + p.chunk - 1) / p.chunk;
   if (ns <= 1) return;
+  const int nr = min(kCombineRows, p.R - row0);
+  const int r = tid / 64;   // row of this thread within the CTA
+  const int c8 = tid % 64;  // value columns 8*c8 .. 8*c8+7
+  const bool active = r < nr;
+  if (tid == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    fence_mbarrier_init();
+  }
+  __syncthreads();
+  // launched as a programmatic dependent of the partial kernel: wait for its results
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int64_t base = static_cast<int64_t>(b) * p.max_splits;
-  const float* lse_s = p.ws_lse + base * p.R + row;
-  // thread tid owns value columns 4*tid .. 4*tid+3: one 8-byte bf16 load per split
-  const uint2* src = reinterpret_cast<const uint2*>(p.ws_o + (base * p.R + row) * kValueDim) + tid;
-  const int64_t stride2 = static_cast<int64_t>(p.R) * kValueDim / 4;  // uint2s between splits
+  const float* lse_s = p.ws_lse + base * p.R + row0 + (active ? r : 0);
   float m_run = -INFINITY, w_run = 0.f;
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int s0 = 0; s0 < ns; s0 += kCombineBatch) {
-    const int nb = min(kCombineBatch, ns - s0);
-    uint2 v[kCombineBatch];
+  float acc[8];
 #pragma unroll
-    for (int u = 0; u < kCombineBatch; ++u)
-      v[u] = (u < nb) ? __ldg(src + (s0 + u) * stride2) : make_uint2(0u, 0u);
-    // lane l holds the log-sum-exp of splits s0 + l and s0 + 32 + l
-    const float l0 = (lane < nb) ? __ldg(lse_s + static_cast<int64_t>(s0 + lane) * p.R) : -INFINITY;
-    const float l1 = (kCombineBatch > 32 && lane + 32 < nb) ? __ldg(lse_s + static_cast<int64_t>(s0 + 32 + lane) * p.R) : -INFINITY;
-    float bm = fmaxf(l0, l1);
+  for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+  bool ok = true;
+  uint32_t phase = 0;
+  for (int s0 = 0; s0 < ns && ok; s0 += kCombineBatch) {
+    const int nb = min(kCombineBatch, ns - s0);
+    if (tid == 0) {
+      mbar_arrive_expect_tx(&bar, static_cast<uint32_t>(nb * nr * kCombineRowBytes));
+      const uint64_t pol = policy_evict_first();
+      for (int s = 0; s < nb; ++s)
+        bulk_load(cs + s * nr * kCombineRowBytes, p.ws_o + ((base + s0 + s) * p.R + row0) * kValueDim,
+                  static_cast<uint32_t>(nr * kCombineRowBytes), &bar, pol);
+    }
+    const float l = (lane < nb) ? __ldg(lse_s + static_cast<int64_t>(s0 + lane) * p.R) : -INFINITY;
+    float bm = l;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, o));
     const float m_new = fmaxf(m_run, bm);
     if (m_new != -INFINITY) {
       const float c = __expf(m_run - m_new);  // 0 while nothing has been accumulated
-      acc.x *= c;
-      acc.y *= c;
-      acc.z *= c;
-      acc.w *= c;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[i] *= c;
       w_run *= c;
       m_run = m_new;
     }
-    const float w0 = (m_new == -INFINITY) ? 0.f : __expf(l0 - m_new);
-    const float w1 = (m_new == -INFINITY) ? 0.f : __expf(l1 - m_new);
-    float ws = w0 + w1;
+    const float w = (m_new == -INFINITY) ? 0.f : __expf(l - m_new);
+    float ws = w;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) ws += __shfl_xor_sync(0xffffffffu, ws, o);
     w_run += ws;
+    ok = mbar_wait(&bar, phase, &abort_flag);
+    phase ^= 1u;
+    if (ok) {
+      const uint32_t src = smem_u32(cs) + (active ? r : 0) * kCombineRowBytes + c8 * 16;
+      for (int s = 0; s < nb; ++s) {
+        const float ws_s = __shfl_sync(0xffffffffu, w, s);
+        uint32_t v0, v1, v2, v3;
+        asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(v0), "=r"(v1), "=r"(v2), "=r"(v3)
+                     : "r"(src + s * nr * kCombineRowBytes));
+        const uint32_t vv[4] = {v0, v1, v2, v3};
 #pragma unroll
-    for (int u = 0; u < kCombineBatch; ++u) {
-      if (u < nb) {  // nb is uniform across the CTA
-        const float w = __shfl_sync(0xffffffffu, u < 32 ? w0 : w1, u & 31);
-        const float2 lo = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v[u].x));
-        const float2 hi = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v[u].y));
-        acc.x += w * lo.x;
-        acc.y += w * lo.y;
-        acc.z += w * hi.x;
-        acc.w += w * hi.y;
+        for (int i = 0; i < 4; ++i) {
+          const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&vv[i]));
+          acc[2 * i] += ws_s * f.x;
+          acc[2 * i + 1] += ws_s * f.y;
+        }
       }
     }
+    ok = __syncthreads_and(ok) != 0;  // the staging area is reused by the next batch
   }
-  const float inv = w_run > 0.f ? 1.f / w_run : 0.f;
-  uint2 pk;
-  pk.x = pack_bf16x2(acc.x * inv, acc.y * inv);
-  pk.y = pack_bf16x2(acc.z * inv, acc.w * inv);
-  *reinterpret_cast<uint2*>(p.out + (static_cast<int64_t>(b) * p.R + row) * kValueDim + tid * 4) = pk;
-  if (tid == 0) p.lse[static_cast<int64_t>(b) * p.R + row] = (w_run > 0.f) ? (m_run + __logf(w_run)) : -INFINITY;
+  if (!ok) {
+    if (tid == 0) {
+      atomicOr(p.status, kStatusTimeout);
+      drain_wait(&bar, phase ^ 1u);  // copies still in flight land before the CTA exits
+    }
+    return;
+  }
+  if (active) {
+    const float inv = w_run > 0.f ? 1.f / w_run : 0.f;
+    uint4 pk;
+    pk.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+    pk.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
+    pk.z = pack_bf16x2(acc[4] * inv, acc[5] * inv);
+    pk.w = pack_bf16x2(acc[6] * inv, acc[7] * inv);
+    const int64_t orow = static_cast<int64_t>(b) * p.R + row0 + r;
+    *reinterpret_cast<uint4*>(p.out + orow * kValueDim + c8 * 8) = pk;
+    if (c8 == 0) p.lse[orow] = (w_run > 0.f) ? (m_run + __logf(w_run)) : -INFINITY;
+  }
 }
 
 // Watchdog self-test: wait on an mbarrier that nothing ever arrives on, through the same
@@ -794,12 +832,26 @@ cudaError_t launch_selftest_timeout(unsigned* status, cudaStream_t stream) {
 }
 
 cudaError_t launch_decode_combine(const DecodeParams& p, cudaStream_t stream) {
-  dim3 grid(p.R, p.B);
-  if (p.max_splits <= 16)
-    decode_combine_kernel<16><<<grid, kCombineThreads, 0, stream>>>(p);
-  else
-    decode_combine_kernel<64><<<grid, kCombineThreads, 0, stream>>>(p);
-  return cudaGetLastError();
+  const dim3 grid((p.R + kCombineRows - 1) / kCombineRows, p.B);
+  const int smem = min(p.max_splits, kCombineBatch) * kCombineRows * kCombineRowBytes;
+  static bool attr_set = false;
+  if (!attr_set) {
+    const cudaError_t e = cudaFuncSetAttribute(decode_combine_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               kCombineBatch * kCombineRows * kCombineRowBytes);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(kCombineThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, decode_combine_kernel, p);
 }
 
 }  // namespace mla

@@ -11,7 +11,8 @@
 // padding); launch-blog repost "英偉達力薦，小團隊兩個月開源一款「光速級」智能體推理引擎",
 // section "TokenSpeed 性能預覽" (prefill with a long prefix KV cache, tuned softmax).
 //
-// Design on sm_103a (one CTA per (128-row query block, head, request), one CTA per SM):
+// Design on sm_103a (one CTA per (128-row query block, head, request), one CTA per SM,
+// 320 threads: softmax warps 0-7, producer warp 8, MMA warp 9):
 //  * Producer warp: TMA (128-byte swizzled, 4-D maps over (columns, token, column block,
 //    head), one box per operand tile) loads the query block once and streams 128-key K (192
 //    wide) and V (128 wide) tiles of the same head through two separate 2-stage mbarrier
@@ -20,12 +21,15 @@
 //  * MMA warp (uniform control flow, one elected thread issues): S = Q . K^T (M=128 rows,
 //    N=128 keys, K=192) into one of two TMEM S buffers; O += P . V (M=128, N=128, K=128)
 //    with P read straight from TMEM (the A operand) and V MN-major from shared memory.
-//  * Softmax warps (4, one thread per query row = TMEM lane): causal mask offset by the
-//    prefix only on tiles that cross the diagonal, running max in the log2 domain with a
-//    lazy rescale of the thread's own O row (only when the max grows by more than 2^8),
-//    exp2 on the MUFU unit; P (bf16) is written back into the first 64 columns of the
-//    tile's own S buffer, so it never touches shared memory.
-//  * Epilogue: O / l to bf16 and the natural-log LSE, straight from TMEM.
+//  * Softmax warps (8: two per TMEM lane quadrant, each row = TMEM lane split between a
+//    warp for keys 0-63 and one for keys 64-127 of every tile, which swap their partial
+//    row maxima through shared memory): causal mask offset by the prefix only on tiles
+//    that cross the diagonal, running max in the log2 domain with a lazy rescale of the
+//    thread's half of its O row (only when the max grows by more than 2^8), exp2 on the
+//    MUFU unit; P (bf16) is written back into the first 64 columns of the tile's own S
+//    buffer, so it never touches shared memory.
+//  * Epilogue: O / l to bf16 and the natural-log LSE, straight from TMEM (each half of a
+//    row writes its 64 value columns; the row sum is the two halves' partial sums).
 // Every wait is bounded; on expiry the CTA records a timeout in the status word, drains
 // its in-flight copies and MMAs, frees TMEM and returns.
 #include "mla_internal.h"
@@ -39,7 +43,11 @@ constexpr int kDv = 128;
 constexpr int kBM = 128;     // query rows per CTA
 constexpr int kBN = 128;     // keys per tile
 constexpr int kStages = 2;
-constexpr int kThreads = 192;
+constexpr int kSoftmaxWarps = 8;  // two per TMEM lane quadrant, one per half of the key tile
+constexpr int kSoftmaxThreads = 32 * kSoftmaxWarps;
+constexpr int kProducerWarp = kSoftmaxWarps;
+constexpr int kMmaWarp = kSoftmaxWarps + 1;
+constexpr int kThreads = 32 * (kSoftmaxWarps + 2);
 
 constexpr int kQBlockBytes = kBM * 128;                // 16 KB per 64-column block
 constexpr int kQBytes = (kDqk / 64) * kQBlockBytes;    // 48 KB
@@ -65,9 +73,11 @@ struct PrefillCtrl {
   uint64_t mma_drain;
   uint32_t tmem_base;
   int abort_flag;
+  float row_max[2][kBM];   // per half of the key tile: this tile's partial row maxima
+  float row_sum[2][kBM];   // per half: partial row sums (epilogue)
 };
-constexpr int kSmemBytes = kOffCtrl + 1024 + 1024;
-static_assert(sizeof(PrefillCtrl) <= 1024, "control block");
+constexpr int kSmemBytes = kOffCtrl + 4096 + 1024;
+static_assert(sizeof(PrefillCtrl) <= 4096, "control block");
 
 constexpr uint32_t kTmemCols = 512;  // O at 0..127, S/P buffers at 128..255 and 256..383
 constexpr uint32_t kTmemO = 0;
@@ -166,17 +176,17 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       mbar_init(&ctrl->s_full[i], 1);
       mbar_init(&ctrl->s_consumed[i], 1);
     }
-    mbar_init(&ctrl->p_full, 128);
+    mbar_init(&ctrl->p_full, kSoftmaxThreads);
     mbar_init(&ctrl->o_done, 1);
     mbar_init(&ctrl->mma_drain, 1);
     ctrl->abort_flag = 0;
     fence_mbarrier_init();
   }
-  if (warp == 5) {
+  if (warp == kMmaWarp) {
     tmem_alloc(&ctrl->tmem_base, kTmemCols);
     tmem_relinquish();
   }
-  if (warp == 4 && lane == 0) {
+  if (warp == kProducerWarp && lane == 0) {
     tma_prefetch_desc(&tm_q);
     tma_prefetch_desc(&tm_k);
     tma_prefetch_desc(&tm_v);
@@ -187,7 +197,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
   const uint32_t tmem = ctrl->tmem_base;
   volatile int* abort_flag = &ctrl->abort_flag;
 
-  if (warp == 4) {
+  if (warp == kProducerWarp) {
     // ------------------------------------------------------------------ TMA producer
     // lane 0 streams the K ring, lane 1 the V ring (independent waits in divergent lanes)
     if (lane < 2) {
@@ -225,7 +235,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       }
     }
     __syncwarp();
-  } else if (warp == 5) {
+  } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------------ MMA issuer (whole warp,
     // uniform control flow; one elected thread issues each GEMM's MMAs and their commits)
     const uint32_t idesc1 = make_idesc_bf16(kBM, kBN, false, false);
@@ -308,35 +318,87 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     }
     __syncwarp();
   } else {
-    // ------------------------------------------------------------------ softmax + epilogue (warps 0-3)
-    const int r = warp * 32 + lane;          // query row within the block = TMEM lane
+    // ------------------------------------------------------------------ softmax + epilogue (warps 0-7)
+    // Warp w serves TMEM lane quadrant w%4 (query rows 32(w%4) .. +31) and half hf = w/4 of
+    // every key tile (keys 64hf .. 64hf+63); the two warps of a quadrant swap their partial
+    // row maxima through shared memory (a 64-thread named barrier per quadrant) so that both
+    // halves scale P by the same running maximum.
+    const int quad = warp & 3;
+    const int hf = warp >> 2;
+    const int r = quad * 32 + lane;            // query row within the block = TMEM lane
     const bool row_active = r < rows;
     const int vis_last = pre + row_begin + r;  // last visible key of this row
-    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
+    const int pair_bar = 2 + quad;
     float m_used = -INFINITY;
-    float l_sum = 0.f;
+    float l_sum = 0.f;  // this half's share of the row sum
     bool failed = false;
     for (int j = 0; j < ntiles; ++j) {
       const int sb = j & 1;
-      const int k0 = j * kBN;
+      const int k0 = j * kBN + 64 * hf;
       const uint32_t s_tmem = tmem + lane_base + kTmemS + sb * 128;
       bool fail = !mbar_wait(&ctrl->s_full[sb], (j >> 1) & 1, abort_flag);
       fail = __any_sync(0xffffffffu, fail);
       bool need_rescale = false;
       float alpha = 1.f;
+      uint32_t sr[64];
+      int lim = -1;
       if (!fail) {
         tc_fence_after();
-        uint32_t sr[128];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) tmem_ld32(s_tmem + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32 * c]));
+        tmem_ld32(s_tmem + 64 * hf, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
+        tmem_ld32(s_tmem + 64 * hf + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
         tmem_ld_wait();
-        const int lim = (j >= diag_tile) ? (row_active ? vis_last - k0 : -1) : (row_active ? kBN - 1 : -1);
-        uint32_t packed[64];
-        online_softmax_step<128>(sr, lim, p.scale_log2, kRescaleThreshold, m_used, l_sum, packed, alpha,
-                                 need_rescale);
-        // P (bf16 pairs) over the first 64 columns of this tile's S buffer
-        tmem_st32(s_tmem, *reinterpret_cast<uint32_t(*)[32]>(&packed[0]));
-        tmem_st32(s_tmem + 32, *reinterpret_cast<uint32_t(*)[32]>(&packed[32]));
+        lim = (j >= diag_tile) ? (row_active ? vis_last - k0 : -1) : (row_active ? 63 : -1);
+        float mx = -INFINITY;
+        if (lim >= 63) {
+#pragma unroll
+          for (int i = 0; i < 64; ++i) mx = fmaxf(mx, __uint_as_float(sr[i]));
+        } else {
+#pragma unroll
+          for (int i = 0; i < 64; ++i)
+            if (i <= lim) mx = fmaxf(mx, __uint_as_float(sr[i]));
+        }
+        ctrl->row_max[hf][r] = mx;
+      }
+      // both halves have loaded their S columns (P below overwrites columns 0..63) and
+      // published their partial maxima
+      named_bar_sync(pair_bar, 64);
+      if (!fail) {
+        const float mx = fmaxf(ctrl->row_max[0][r], ctrl->row_max[1][r]);
+        const float mt = mx * p.scale_log2;
+        if (m_used == -INFINITY) {
+          m_used = mt;
+        } else if (mt > m_used + kRescaleThreshold) {
+          alpha = ex2_approx(m_used - mt);
+          need_rescale = true;
+          l_sum *= alpha;
+          m_used = mt;
+        }
+        const float neg_m = (m_used == -INFINITY) ? 0.f : -m_used;
+        uint32_t packed[32];
+        float l0 = 0.f, l1 = 0.f;
+        if (lim >= 63) {
+#pragma unroll
+          for (int i = 0; i < 64; i += 2) {
+            const float p0 = ex2_approx(fmaf(__uint_as_float(sr[i]), p.scale_log2, neg_m));
+            const float p1 = ex2_approx(fmaf(__uint_as_float(sr[i + 1]), p.scale_log2, neg_m));
+            l0 += p0;
+            l1 += p1;
+            packed[i >> 1] = pack_bf16x2(p0, p1);
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < 64; i += 2) {
+            const float p0 = (i <= lim) ? ex2_approx(fmaf(__uint_as_float(sr[i]), p.scale_log2, neg_m)) : 0.f;
+            const float p1 = (i + 1 <= lim) ? ex2_approx(fmaf(__uint_as_float(sr[i + 1]), p.scale_log2, neg_m)) : 0.f;
+            l0 += p0;
+            l1 += p1;
+            packed[i >> 1] = pack_bf16x2(p0, p1);
+          }
+        }
+        l_sum += l0 + l1;
+        // P (bf16 pairs) of this half over columns 32hf .. 32hf+31 of the tile's S buffer
+        tmem_st32(s_tmem + 32 * hf, packed);
       }
       if (!fail && j >= 1) {
         // O may only be rescaled once BMM2(j-1) has finished accumulating into it
@@ -344,20 +406,21 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         fail = __any_sync(0xffffffffu, fail);
       }
       if (!fail && __any_sync(0xffffffffu, need_rescale) && j >= 1) {
-        // rescale this thread's own O row (TMEM lane r, 128 columns)
+        // rescale this thread's half of its O row (TMEM lane r, columns 64hf .. 64hf+63)
         tc_fence_after();
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
+        for (int c = 0; c < 2; ++c) {
           uint32_t v[32];
-          tmem_ld32(tmem + lane_base + kTmemO + c * 32, v);
+          const uint32_t addr = tmem + lane_base + kTmemO + 64 * hf + c * 32;
+          tmem_ld32(addr, v);
           tmem_ld_wait();
 #pragma unroll
           for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
-          tmem_st32(tmem + lane_base + kTmemO + c * 32, v);
+          tmem_st32(addr, v);
         }
       }
       tmem_st_wait();
-      if (bar_or(1, 128, fail || (*abort_flag != 0))) {
+      if (bar_or(1, kSoftmaxThreads, fail || (*abort_flag != 0))) {
         failed = true;
         break;
       }
@@ -365,17 +428,19 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       mbar_arrive(&ctrl->p_full);
     }
     if (!failed) failed = !mbar_wait(&ctrl->o_done, (ntiles - 1) & 1, abort_flag);
-    if (!bar_or(1, 128, failed || (*abort_flag != 0))) {
+    if (!failed) ctrl->row_sum[hf][r] = l_sum;
+    if (!bar_or(1, kSoftmaxThreads, failed || (*abort_flag != 0))) {
       tc_fence_after();
-      const float inv = (l_sum > 0.f) ? 1.f / l_sum : 0.f;
+      const float l_tot = ctrl->row_sum[0][r] + ctrl->row_sum[1][r];
+      const float inv = (l_tot > 0.f) ? 1.f / l_tot : 0.f;
       const int64_t tok = static_cast<int64_t>(q_start) + row_begin + r;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < 2; ++c) {
         uint32_t v[32];
-        tmem_ld32(tmem + lane_base + kTmemO + c * 32, v);
+        tmem_ld32(tmem + lane_base + kTmemO + 64 * hf + c * 32, v);
         tmem_ld_wait();
         if (row_active) {
-          uint4* dst = reinterpret_cast<uint4*>(p.out + (tok * p.H + h) * kDv + c * 32);
+          uint4* dst = reinterpret_cast<uint4*>(p.out + (tok * p.H + h) * kDv + 64 * hf + c * 32);
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
             dst[i] = make_uint4(pack_bf16x2(__uint_as_float(v[8 * i + 0]) * inv, __uint_as_float(v[8 * i + 1]) * inv),
@@ -385,8 +450,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
           }
         }
       }
-      if (row_active) {
-        const float lse2 = (l_sum > 0.f) ? (m_used + __log2f(l_sum)) : -INFINITY;
+      if (row_active && hf == 0) {
+        const float lse2 = (l_tot > 0.f) ? (m_used + __log2f(l_tot)) : -INFINITY;
         p.lse[tok * p.H + h] = lse2 * 0.69314718055994530942f;
       }
     }
@@ -395,7 +460,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
   tc_fence_before();
   __syncthreads();
   if (threadIdx.x == 0 && ctrl->abort_flag) atomicOr(p.status, kStatusTimeout);
-  if (warp == 5) {
+  if (warp == kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }

@@ -192,7 +192,13 @@ decode_partial_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
   const int nq = (nrows + 15) & ~15;  // BMM2 N (multiple of 16)
 
   if (threadIdx.x == 0) {
+    // Q (nine 64-column blocks of the 64 folded rows) is requested first, by the thread that
+    // initialises q_full, so the barrier is armed only after its initialisation
+    tma_prefetch_desc(&tm_q);
     mbar_init(&ctrl->q_full, 1);
+    fence_mbarrier_init();
+    mbar_arrive_expect_tx(&ctrl->q_full, kTileBytes);
+    tma_load_3d(smem + kOffQ, &tm_q, &ctrl->q_full, 0, b * p.R + row0, 0, policy_evict_last());
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&ctrl->kv_full[s], kFp8 ? kDequantThreads : 1);
       mbar_init(&ctrl->kv_empty[s], 1);
@@ -213,12 +219,7 @@ decode_partial_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
     tmem_alloc(&ctrl->tmem_base, kTmemCols);
     tmem_relinquish();
   }
-  if (warp == 4 && lane == 0) {
-    tma_prefetch_desc(&tm_q);
-    if (!kFp8) tma_prefetch_desc(&tm_kv);
-    mbar_arrive_expect_tx(&ctrl->q_full, kTileBytes);
-    tma_load_3d(smem + kOffQ, &tm_q, &ctrl->q_full, 0, b * p.R + row0, 0, policy_evict_last());  // 9 blocks
-  }
+  if (warp == 4 && lane == 0 && !kFp8) tma_prefetch_desc(&tm_kv);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();

@@ -127,7 +127,9 @@ def measure_decode_extra(mla, name, dev, steps=200):
     return {"workload": name, "us_per_call": call_ms * 1e3, "kv_gbs": kv_bytes / (call_ms / 1e3) / 1e9,
             "partial_us": part_ms * 1e3, "partial_gbs": alg_bytes / (part_ms / 1e3) / 1e9,
             "hbm_frac": alg_bytes / (part_ms / 1e3) / 1e9 / peak["hbm_gbs"],
-            "tflops": decode_flops(wl) / (call_ms / 1e3) / 1e12, "splits": plan.max_splits,
+            "tflops": decode_flops(wl) / (call_ms / 1e3) / 1e12,
+            "partial_tflops_frac": decode_flops(wl) / (part_ms / 1e3) / 1e12 / peak["bf16_tflops"],
+            "splits": plan.max_splits,
             "timing": "CUDA graph of back-to-back calls (partial: of partial-kernel launches alone), "
                       "L2 " + ("rotated sets" if n_sets > 1 else "inputs > L2")}
 
@@ -501,7 +503,8 @@ def main():
         del sets, host_in, dev_in, host_out, graph, kgraph
         torch.cuda.empty_cache()
         line["extra"] = {"prefill": measure_prefill(mla, dev)}
-        for name in ["decode_bf16_b16_q4_h16_l64k", "decode_fp8_b16_q4_h16_l64k"]:
+        for name in ["decode_bf16_b16_q4_h16_l64k", "decode_fp8_b16_q4_h16_l64k", "decode_fp8_b8_q4_h16_l64k",
+                     "decode_b16_q2_h16_ragged", "decode_b16_q2_h128_ragged", "decode_b1_q1_h16_l1024"]:
             line["extra"][name] = measure_decode_extra(mla, name, dev)
             torch.cuda.empty_cache()
     if rank == 0:

@@ -13,6 +13,7 @@ is not available; these synthetic draws stand in for it.
 Recipe (all draws from one torch.Generator seeded per workload):
   * decode Q and latent KV: N(0, 1) / sqrt(576), bf16; scale 1/sqrt(192).
   * FP8 KV: latent N(0, 1), kv_scale = amax|x| / 448, codes = e4m3fn(x / kv_scale).
+  * INT8 KV: latent N(0, 1), kv_scale = amax|x| / 127, codes = round(x / kv_scale) as int8.
   * pages: 64-token pages; each request owns ceil(L_b / 64) pages taken from one shared
     pool in a random permutation.
   * "peaked" variants multiply Q by 30 and plant near-copies of a query direction into
@@ -40,7 +41,7 @@ class DecodeWorkload:
     heads: int
     seq_lens: list            # per request, drafts included
     page_size: int = 64
-    kv_dtype: str = "bf16"    # "bf16" or "e4m3"
+    kv_dtype: str = "bf16"    # "bf16", "e4m3" or "int8"
     seed: int = 0
     peaked: bool = False
     extra_pages: int = 0      # unused pool pages (pool larger than needed)
@@ -75,6 +76,8 @@ def decode_workloads():
             "decode_fp8_b16_q4_h16_l64k", 16, 4, 16, [65536] * 16, kv_dtype="e4m3", seed=1003),
         "decode_bf16_b16_q4_h16_l64k": DecodeWorkload(
             "decode_bf16_b16_q4_h16_l64k", 16, 4, 16, [65536] * 16, seed=1003),
+        "decode_int8_b16_q4_h16_l64k": DecodeWorkload(
+            "decode_int8_b16_q4_h16_l64k", 16, 4, 16, [65536] * 16, kv_dtype="int8", seed=1003),
     }
 
 
@@ -88,7 +91,7 @@ def prefill_workloads():
 @dataclass
 class DecodeInputs:
     q: torch.Tensor            # [B, T, H, 576] bf16
-    kv_pool: torch.Tensor      # [n_pages, page, 576] bf16, or uint8 e4m3 codes
+    kv_pool: torch.Tensor      # [n_pages, page, 576] bf16, uint8 e4m3 codes or int8 codes
     page_table: torch.Tensor   # [B, max_pages] int32
     seq_lens: torch.Tensor     # [B] int32
     kv_scale: float
@@ -134,6 +137,19 @@ def make_decode_inputs(wl: DecodeWorkload, device="cpu", max_pages=None) -> Deco
             e = min(n_pages, s + step)
             pool[s:e] = (raw[s:e] / kv_scale).clamp_(-448.0, 448.0).to(torch.float8_e4m3fn).view(torch.uint8)
         del raw
+    elif wl.kv_dtype == "int8":
+        raw = torch.empty(n_pages, P, D_LATENT, dtype=torch.float32, device=dev)
+        step = max(1, (1 << 27) // (P * D_LATENT))
+        for s in range(0, n_pages, step):
+            e = min(n_pages, s + step)
+            raw[s:e] = torch.randn(e - s, P, D_LATENT, generator=g, device=dev)
+        amax = float(raw.abs().max())
+        kv_scale = amax / 127.0
+        pool = torch.empty(n_pages, P, D_LATENT, dtype=torch.int8, device=dev)
+        for s in range(0, n_pages, step):
+            e = min(n_pages, s + step)
+            pool[s:e] = torch.round(raw[s:e] / kv_scale).clamp_(-127.0, 127.0).to(torch.int8)
+        del raw
     else:
         raise ValueError(wl.kv_dtype)
     if wl.peaked:
@@ -162,6 +178,8 @@ def _plant_near_duplicates(q, pool, page_table, wl, g, kv_scale):
             page = int(page_table[b, j // P])
             if pool.dtype == torch.uint8:
                 pool[page, j % P] = (row / kv_scale).clamp(-448.0, 448.0).to(torch.float8_e4m3fn).view(torch.uint8)
+            elif pool.dtype == torch.int8:
+                pool[page, j % P] = torch.round(row / kv_scale).clamp(-127.0, 127.0).to(torch.int8)
             else:
                 pool[page, j % P] = row.to(torch.bfloat16)
 

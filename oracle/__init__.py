@@ -91,8 +91,8 @@ def mla_decode(q: torch.Tensor, kv_pool: torch.Tensor, page_table, seq_lens, sca
                kv_scale: float = 1.0, dv: int = 512, rows=None, lens_include_drafts: bool = True):
     """Absorbed MLA decode over a paged latent cache, in fp64.
 
-    q: [B, T, H, D] bf16.  kv_pool: [n_pages, page_size, D] bf16, or uint8 e4m3 codes
-    (then each element is decoded and multiplied by kv_scale).  page_table: [B, max_pages]
+    q: [B, T, H, D] bf16.  kv_pool: [n_pages, page_size, D] bf16, uint8 e4m3 codes or
+    int8 codes (then each element is decoded and multiplied by kv_scale).  page_table: [B, max_pages]
     int32.  seq_lens: [B] (tokens cached per request, drafts included).
     Returns (out [B,T,H,dv] float64, lse [B,T,H] float64) or, with ``rows`` (flat ids
     (b*T + t)*H + h), (out [n, dv], lse [n]).
@@ -107,8 +107,11 @@ def mla_decode(q: torch.Tensor, kv_pool: torch.Tensor, page_table, seq_lens, sca
     elif kv_pool.dtype == torch.uint8:
         pool = np.ascontiguousarray(kv_pool.cpu().numpy())
         kv_dtype = 1
+    elif kv_pool.dtype == torch.int8:
+        pool = np.ascontiguousarray(kv_pool.cpu().numpy())
+        kv_dtype = 2
     else:
-        raise TypeError("kv_pool must be bf16 or uint8 e4m3 codes")
+        raise TypeError("kv_pool must be bf16, uint8 e4m3 codes or int8 codes")
     qb = _bits16(q)
     pt = _i32(page_table)
     sl = _i32(seq_lens)

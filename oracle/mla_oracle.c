@@ -26,6 +26,9 @@
  *  - lse is the natural log of sum_j exp(s_j) with s_j the scaled score.
  *  - FP8 KV is OCP e4m3fn (bias 7, no infinities, S.1111.111 is NaN) times one
  *    per-tensor scale; the decode table below is built from that format definition.
+ *  - INT8 KV (the talk's section "Kernel：让 MLA 真正跑满 GPU" names INT8 among the KV
+ *    quantisations that stay bandwidth-bound) is read as two's-complement int8 codes
+ *    times one per-tensor scale, the plainest form the talk leaves open.
  *  - Prefill: request b has prefix_lens[b] cached tokens followed by its new tokens;
  *    new token i (0-based) sees keys 0 .. prefix_lens[b] + i.
  *
@@ -70,9 +73,11 @@ double oracle_e4m3_to_double(uint8_t code) {
   return s ? -v : v;
 }
 
-/* kv_dtype: 0 = bf16 (uint16 bit patterns), 1 = e4m3 bytes times kv_scale. */
+/* kv_dtype: 0 = bf16 (uint16 bit patterns), 1 = e4m3 bytes times kv_scale,
+ * 2 = int8 (two's complement) codes times kv_scale. */
 static double kv_elem(const void* pool, int kv_dtype, int64_t idx, double kv_scale) {
   if (kv_dtype == 0) return bf16_bits_to_double(((const uint16_t*)pool)[idx]);
+  if (kv_dtype == 2) return (double)((const int8_t*)pool)[idx] * kv_scale;
   return oracle_e4m3_to_double(((const uint8_t*)pool)[idx]) * kv_scale;
 }
 

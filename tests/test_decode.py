@@ -94,6 +94,8 @@ SMALL = [
     ("fp8_page16", 2, 2, 16, [77, 500], 16, "e4m3"),
     ("fp8_page128", 1, 3, 16, [700], 128, "e4m3"),
     ("fp8_h128", 1, 2, 128, [900], 64, "e4m3"),
+    ("mtp8", 2, 8, 16, [700, 2000], 64, "bf16"),   # q_len 8: 128 folded rows, two row groups
+    ("fp8_mtp8", 2, 8, 16, [333, 1500], 64, "e4m3"),
 ]
 
 
@@ -142,6 +144,21 @@ def test_decode_stages_equal_decode_bitwise(mla, kv, num_sms):
     assert mla.get_status() == mla.MLA_OK
     assert torch.equal(out1.view(torch.int16), out2.view(torch.int16))
     assert torch.equal(lse1.view(torch.int32), lse2.view(torch.int32))
+
+
+@pytest.mark.parametrize("kv", ["bf16", "e4m3"])
+def test_decode_one_million_keys_sampled(mla, oracle_mod, kv):
+    """A 2^20-key context (16384 pages of 64): the planner's split count and the kernels at
+    the long end, checked on sampled rows the oracle computes one by one."""
+    wl = DecodeWorkload("l1m", 1, 2, 16, [1 << 20], kv_dtype=kv, seed=80)
+    inp = make_decode_inputs(wl, "cuda")
+    out, lse, plan = run_gpu(mla, inp)
+    assert plan.max_splits > 1
+    rows = [0, 5, 16, 31]
+    ref_out, ref_lse = oracle_mod.mla_decode(inp.q.cpu(), inp.kv_pool.cpu(), inp.page_table.cpu(),
+                                             inp.seq_lens.cpu(), inp.scale, kv_scale=inp.kv_scale, rows=rows)
+    check(out.reshape(-1, 512)[rows], lse.reshape(-1)[rows], ref_out, ref_lse, fp8=(kv == "e4m3"))
+    assert np.isfinite(out).all() and np.isfinite(lse).all()
 
 
 def test_decode_page_shuffle_invariance_bitwise(mla):

@@ -8,7 +8,10 @@ The pages print no worked example, so the oracle is pinned to things outside its
   * invariants of the method: physical page order does not matter, split + LSE merge
     equals the unsplit result, folding draft tokens into rows is result-neutral;
   * the e4m3 decode table against torch's float8_e4m3fn conversion on all 256 codes and
-    against points the format definition fixes.
+    against points the format definition fixes;
+  * int8 codes: with a power-of-two scale the decoded values are exact in bf16, so the
+    int8 pool must give bit-for-bit the bf16 pool's result; the extreme codes decode to
+    -128 and 127 times the scale.
 Each is chosen so that a plausible slip (dropped term, wrong causal index, wrong value
 columns, transposed operand, wrong log base) fails at least one of them.
 """
@@ -38,6 +41,8 @@ def _dense_kv(inp, b, L):
     rows = inp.kv_pool[pages, idx % P]
     if rows.dtype == torch.uint8:
         rows = rows.view(torch.float8_e4m3fn).to(torch.float64) * inp.kv_scale
+    elif rows.dtype == torch.int8:
+        rows = rows.to(torch.float64) * inp.kv_scale
     else:
         rows = rows.to(torch.float64)
     return rows
@@ -69,6 +74,8 @@ CASES = [
     (2, 2, 4, [65, 64], 64, "bf16"),
     (2, 3, 2, [33, 9], 4, "e4m3"),
     (1, 4, 4, [70], 64, "e4m3"),
+    (2, 3, 2, [33, 9], 4, "int8"),
+    (1, 4, 4, [70], 64, "int8"),
 ]
 
 
@@ -213,6 +220,28 @@ def test_e4m3_format_points(oracle_mod):
     assert f(0x00) == 0.0 and math.copysign(1.0, f(0x80)) == -1.0
     finite = [c for c in range(256) if not math.isnan(f(c))]
     assert len(finite) == 254
+
+
+def test_int8_pool_equals_bf16_pool_of_its_values(oracle_mod):
+    inp = _paged(2, 3, 4, [70, 13], 16, seed=21, kv="int8")
+    scale = 2.0 ** -5  # codes * 2^-5 (|code| <= 127, seven bits) are exact in bf16
+    vals = (inp.kv_pool.to(torch.float64) * scale).to(torch.bfloat16)
+    assert torch.equal(vals.to(torch.float64), inp.kv_pool.to(torch.float64) * scale)
+    o8, l8 = oracle_mod.mla_decode(inp.q, inp.kv_pool, inp.page_table, inp.seq_lens, inp.scale, kv_scale=scale)
+    ob, lb = oracle_mod.mla_decode(inp.q, vals, inp.page_table, inp.seq_lens, inp.scale)
+    np.testing.assert_array_equal(o8, ob)
+    np.testing.assert_array_equal(l8, lb)
+
+
+def test_int8_extreme_codes(oracle_mod):
+    # one visible key: the output is that key's value row, i.e. the decoded codes
+    q = torch.zeros(1, 1, 1, D, dtype=torch.bfloat16)
+    pool = torch.zeros(1, 1, D, dtype=torch.int8)
+    pool[0, 0, :4] = torch.tensor([-128, 127, -1, 1], dtype=torch.int8)
+    out, lse = oracle_mod.mla_decode(q, pool, torch.zeros(1, 1, dtype=torch.int32), torch.ones(1, dtype=torch.int32),
+                                     0.1, kv_scale=0.5)
+    assert out[0, 0, 0, :4].tolist() == [-64.0, 63.5, -0.5, 0.5]
+    assert lse[0, 0, 0] == 0.0
 
 
 # ------------------------------------------------------------------------------------

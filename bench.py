@@ -49,7 +49,7 @@ def _peaks():
 def decode_bytes(wl):
     """Algorithmic bytes of one decode call: each request's latent rows once, its page-table
     entries, and the query / output / lse rows."""
-    e = 1 if wl.kv_dtype == "e4m3" else 2
+    e = 1 if wl.kv_dtype in ("e4m3", "int8") else 2
     kv = sum(L * 576 * e for L in wl.seq_lens)
     pt = sum(((L + wl.page_size - 1) // wl.page_size) * 4 for L in wl.seq_lens)
     io = wl.batch * wl.q_len * wl.heads * (576 * 2 + 512 * 2 + 4)
@@ -97,7 +97,7 @@ def measure_decode_extra(mla, name, dev, steps=200):
         w = decode_workloads()[name]
         w.seed = replica_seed(wl.seed, i, 0)
         sets.append(make_decode_inputs(w, dev))
-    kvd = mla.MLA_KV_E4M3 if wl.kv_dtype == "e4m3" else mla.MLA_KV_BF16
+    kvd = {"e4m3": mla.MLA_KV_E4M3, "int8": mla.MLA_KV_INT8}.get(wl.kv_dtype, mla.MLA_KV_BF16)
     plan = mla.decode_plan(wl.seq_lens, wl.q_len, wl.heads, wl.page_size, sets[0].page_table.shape[1],
                            sets[0].kv_pool.shape[0], kvd)
     ws_buf = mla.workspace_for(plan, dev)
@@ -503,7 +503,8 @@ def main():
         del sets, host_in, dev_in, host_out, graph, kgraph
         torch.cuda.empty_cache()
         line["extra"] = {"prefill": measure_prefill(mla, dev)}
-        for name in ["decode_bf16_b16_q4_h16_l64k", "decode_fp8_b16_q4_h16_l64k", "decode_fp8_b8_q4_h16_l64k",
+        for name in ["decode_bf16_b16_q4_h16_l64k", "decode_fp8_b16_q4_h16_l64k", "decode_int8_b16_q4_h16_l64k",
+                     "decode_fp8_b8_q4_h16_l64k",
                      "decode_b16_q2_h16_ragged", "decode_b16_q2_h128_ragged", "decode_b1_q1_h16_l1024"]:
             line["extra"][name] = measure_decode_extra(mla, name, dev)
             torch.cuda.empty_cache()

@@ -59,7 +59,11 @@ typedef enum mla_status_t {
 
 typedef enum mla_kv_dtype_t {
   MLA_KV_BF16 = 0, /* latent pool stored as bfloat16                                     */
-  MLA_KV_E4M3 = 1  /* latent pool stored as OCP FP8 e4m3fn codes times one kv_scale      */
+  MLA_KV_E4M3 = 1, /* latent pool stored as OCP FP8 e4m3fn codes times one kv_scale      */
+  MLA_KV_INT8 = 2  /* latent pool stored as two's-complement int8 codes times one kv_scale.
+                    * (The TokenSpeed talk, section "Kernel：让 MLA 真正跑满 GPU", names INT8
+                    * among the KV quantisations that keep decode bandwidth-bound; a
+                    * per-tensor scale is the plainest form it leaves open.)               */
 } mla_kv_dtype_t;
 
 /* Decode plan: a plain value struct filled by mla_decode_plan(); callers treat the
@@ -98,12 +102,12 @@ int mla_decode_plan(int batch, const int32_t* seq_lens_host, int q_len, int num_
 
 /* Absorbed MLA decode with speculative draft tokens over the paged latent cache.
  *   q          : [B, T, H, 576] bf16.  Folded row m = t*H + h of request b.
- *   kv_pages   : [num_pages, page_size, 576] bf16 or e4m3 bytes (plan->kv_dtype).
+ *   kv_pages   : [num_pages, page_size, 576] bf16, e4m3 or int8 bytes (plan->kv_dtype).
  *   page_table : [B, max_pages_per_seq] int32; latent row j of request b is
  *                kv_pages[page_table[b, j / page_size], j % page_size, :].
  *   seq_lens   : [B] int32 device copy of the planned lengths (each <= max_seq_len).
  *   scale      : softmax scale applied to q . k.
- *   kv_scale   : per-tensor dequantisation scale of an e4m3 pool (ignored for bf16).
+ *   kv_scale   : per-tensor dequantisation scale of an 8-bit pool (ignored for bf16).
  *   out        : [B, T, H, 512] bf16, out[b,t,h] = sum_j softmax_j(scale q.k_j) v_j with
  *                draft t seeing keys 0 .. L_b - T + t and v_j = k_j[:512].
  *   lse        : [B, T, H] fp32, natural-log log-sum-exp of the scaled scores.

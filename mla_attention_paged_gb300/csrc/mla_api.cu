@@ -145,7 +145,7 @@ int mla_decode_plan(int batch, const int32_t* seq_lens_host, int q_len, int num_
   if (!seq_lens_host || !plan_out || batch < 1 || q_len < 1 || num_heads < 1 || max_pages_per_seq < 1 ||
       num_pages < 1)
     return MLA_ERR_INVALID_ARG;
-  if (kv_dtype != MLA_KV_BF16 && kv_dtype != MLA_KV_E4M3) return MLA_ERR_INVALID_ARG;
+  if (kv_dtype != MLA_KV_BF16 && kv_dtype != MLA_KV_E4M3 && kv_dtype != MLA_KV_INT8) return MLA_ERR_INVALID_ARG;
   if (q_len > 8 || !page_size_ok(page_size) || q_len * num_heads > 1024) return MLA_ERR_UNSUPPORTED;
   if (batch > 65535) return MLA_ERR_UNSUPPORTED;
   std::vector<int> lens(seq_lens_host, seq_lens_host + batch);
@@ -248,7 +248,7 @@ int decode_stages(const mla_decode_plan_t* plan, const void* q, const void* kv_p
     if (!make_map(&tm_q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, q, dims, strides, box)) return MLA_ERR_CUDA;
   }
   memset(&tm_kv, 0, sizeof tm_kv);
-  if (partial && plan->kv_dtype == MLA_KV_BF16) {  // e4m3 pages are fetched with untiled bulk copies
+  if (partial && plan->kv_dtype == MLA_KV_BF16) {  // 8-bit pages are read row by row by the decode warps
     const uint64_t rows = static_cast<uint64_t>(plan->num_pages) * plan->page_size;
     if (plan->page_size >= kTileKeys) {  // a 64-key tile is one row range of one page
       const uint64_t dims[3] = {64, rows, kLatentDim / 64};
@@ -273,9 +273,10 @@ int decode_stages(const mla_decode_plan_t* plan, const void* q, const void* kv_p
   p.chunk = plan->chunk_tokens;
   p.max_splits = plan->max_splits;
   p.max_seq = plan->max_seq_len;
-  p.kv_fp8 = plan->kv_dtype == MLA_KV_E4M3;
-  p.scale_log2 = scale * 1.4426950408889634f * (p.kv_fp8 ? kv_scale : 1.f);
-  p.v_scale = p.kv_fp8 ? kv_scale : 1.f;
+  p.kv_dtype = plan->kv_dtype;
+  const bool kv8 = plan->kv_dtype != MLA_KV_BF16;
+  p.scale_log2 = scale * 1.4426950408889634f * (kv8 ? kv_scale : 1.f);
+  p.v_scale = kv8 ? kv_scale : 1.f;
   p.page_table = page_table;
   p.seq_lens = seq_lens;
   p.kv_pool = static_cast<const uint8_t*>(kv_pages);

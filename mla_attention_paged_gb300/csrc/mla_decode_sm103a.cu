@@ -162,11 +162,40 @@ __device__ __forceinline__ void store_f16_chunk(uint32_t rbase, int sw, uint4 w)
   st_shared_v4(row0 + ((c0 + 16) ^ sw), o[4], o[5], o[6], o[7]);
 }
 
+// Four int8 codes (bytes of w) -> four f16 holding the codes' values exactly: the top bit
+// of each byte is flipped (code + 128 as an unsigned byte u), u is placed under the f16
+// pattern 0x64 (the value 1024 + u, exact since u < 1024) by two byte permutes, and 1152
+// is subtracted in f16 (exact: the result is a small integer).
+__device__ __forceinline__ void int8x4_to_f16x4(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  const uint32_t x = w ^ 0x80808080u;
+  uint32_t a, b;
+  asm("prmt.b32 %0, %1, %2, 0x5140;" : "=r"(a) : "r"(x), "r"(0x64646464u));
+  asm("prmt.b32 %0, %1, %2, 0x7362;" : "=r"(b) : "r"(x), "r"(0x64646464u));
+  asm("sub.f16x2 %0, %1, %2;" : "=r"(lo) : "r"(a), "r"(0x64806480u));
+  asm("sub.f16x2 %0, %1, %2;" : "=r"(hi) : "r"(b), "r"(0x64806480u));
+}
 
-template <bool kFp8>
-__global__ void __launch_bounds__(threads_for(kFp8), 1)
+// Sixteen int8 codes -> sixteen f16 stored like store_f16_chunk.
+__device__ __forceinline__ void store_f16_chunk_int8(uint32_t rbase, int sw, uint4 w) {
+  uint32_t o[8];
+  int8x4_to_f16x4(w.x, o[0], o[1]);
+  int8x4_to_f16x4(w.y, o[2], o[3]);
+  int8x4_to_f16x4(w.z, o[4], o[5]);
+  int8x4_to_f16x4(w.w, o[6], o[7]);
+  const uint32_t row0 = rbase & ~127u;
+  const uint32_t c0 = (rbase & 127u);
+  st_shared_v4(row0 + (c0 ^ sw), o[0], o[1], o[2], o[3]);
+  st_shared_v4(row0 + ((c0 + 16) ^ sw), o[4], o[5], o[6], o[7]);
+}
+
+
+// kKv: pool format (kKvBf16, kKvE4m3, kKvInt8).  The two 8-bit formats share one path
+// (kFp8 below: decode warps, f16 GEMMs) and differ only in the byte -> f16 step.
+template <int kKv>
+__global__ void __launch_bounds__(threads_for(kKv != kKvBf16), 1)
 decode_partial_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kv,
                       const DecodeParams p) {
+  constexpr bool kFp8 = kKv != kKvBf16;  // an 8-bit pool (e4m3 or int8)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   DecodeCtrl* ctrl = reinterpret_cast<DecodeCtrl*>(smem + kOffCtrl);
@@ -483,7 +512,12 @@ decode_partial_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
         const uint32_t rbase = st + row * 128;
         const int sw = (row & 7) << 4;
 #pragma unroll
-        for (int m = 0; m < 3; ++m) store_f16_chunk(rbase + (dw + 3 * m) * kBlockBytes, sw, w[m][i]);
+        for (int m = 0; m < 3; ++m) {
+          if constexpr (kKv == kKvInt8)
+            store_f16_chunk_int8(rbase + (dw + 3 * m) * kBlockBytes, sw, w[m][i]);
+          else
+            store_f16_chunk(rbase + (dw + 3 * m) * kBlockBytes, sw, w[m][i]);
+        }
       }
       fence_proxy_async_smem();
       mbar_arrive(&ctrl->kv_full[s]);
@@ -505,9 +539,11 @@ decode_partial_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
     float m_used = -INFINITY;
     float l_sum = 0.f;
     bool failed = false;
-    // e4m3 tiles are decoded as values times 2^-8 (exact); the factor returns here
-    const float scale_log2 = kFp8 ? p.scale_log2 * 256.f : p.scale_log2;
-    const float v_scale = kFp8 ? p.v_scale * 256.f : p.v_scale;
+    // e4m3 tiles are decoded as values times 2^-8 (exact); the factor returns here (int8
+    // codes are decoded to their exact values)
+    constexpr float kDecodeFactor = (kKv == kKvE4m3) ? 256.f : 1.f;
+    const float scale_log2 = p.scale_log2 * kDecodeFactor;
+    const float v_scale = p.v_scale * kDecodeFactor;
 
     for (int j = 0; j < ntiles; ++j) {
       const int sb = j & 1;
@@ -802,7 +838,7 @@ __global__ void selftest_timeout_kernel(unsigned* status) {
   if (threadIdx.x == 0 && (!ok || abort_flag)) atomicOr(status, kStatusTimeout);
 }
 
-template <bool kFp8>
+template <int kKv>
 cudaError_t launch_partial_impl(const DecodeParams& p, const CUtensorMap& tm_q, const CUtensorMap& tm_kv,
                                 int head_groups, cudaStream_t stream) {
   static thread_local int configured_device = -1;
@@ -810,12 +846,12 @@ cudaError_t launch_partial_impl(const DecodeParams& p, const CUtensorMap& tm_q, 
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (configured_device != dev) {
-    e = cudaFuncSetAttribute(decode_partial_kernel<kFp8>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    e = cudaFuncSetAttribute(decode_partial_kernel<kKv>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return e;
     configured_device = dev;
   }
   dim3 grid(head_groups, p.max_splits, p.B);
-  decode_partial_kernel<kFp8><<<grid, threads_for(kFp8), kSmemBytes, stream>>>(tm_q, tm_kv, p);
+  decode_partial_kernel<kKv><<<grid, threads_for(kKv != kKvBf16), kSmemBytes, stream>>>(tm_q, tm_kv, p);
   return cudaGetLastError();
 }
 
@@ -823,8 +859,11 @@ cudaError_t launch_partial_impl(const DecodeParams& p, const CUtensorMap& tm_q, 
 
 cudaError_t launch_decode_partial(const DecodeParams& p, const CUtensorMap& tm_q, const CUtensorMap& tm_kv,
                                   int head_groups, cudaStream_t stream) {
-  return p.kv_fp8 ? launch_partial_impl<true>(p, tm_q, tm_kv, head_groups, stream)
-                  : launch_partial_impl<false>(p, tm_q, tm_kv, head_groups, stream);
+  switch (p.kv_dtype) {
+    case kKvE4m3: return launch_partial_impl<kKvE4m3>(p, tm_q, tm_kv, head_groups, stream);
+    case kKvInt8: return launch_partial_impl<kKvInt8>(p, tm_q, tm_kv, head_groups, stream);
+    default: return launch_partial_impl<kKvBf16>(p, tm_q, tm_kv, head_groups, stream);
+  }
 }
 
 cudaError_t launch_selftest_timeout(unsigned* status, cudaStream_t stream) {

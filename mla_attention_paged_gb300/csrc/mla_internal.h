@@ -14,6 +14,11 @@ constexpr int kValueDim = 512;   // value = first 512 latent columns
 constexpr int kTileKeys = 64;    // keys per decode tile
 constexpr int kGroupRows = 64;   // folded query rows per decode CTA
 
+// Pool formats of the decode kernel (the values of mla_kv_dtype_t).
+constexpr int kKvBf16 = 0;
+constexpr int kKvE4m3 = 1;
+constexpr int kKvInt8 = 2;
+
 // Device status word bits (OR-ed by kernels, read and cleared by mla_get_status).
 constexpr unsigned kStatusTimeout = 1u;
 constexpr unsigned kStatusDeviceArg = 2u;
@@ -22,12 +27,12 @@ struct DecodeParams {
   int B, T, H, R;               // R = T*H folded rows per request
   int page_size, max_pages;     // page geometry and page_table row stride
   int chunk, max_splits, max_seq;
-  int kv_fp8;                   // 0: bf16 pool, 1: e4m3 pool
-  float scale_log2;             // softmax scale * log2(e) (* kv_scale for e4m3)
-  float v_scale;                // 1, or kv_scale for e4m3 (applied in the epilogue)
+  int kv_dtype;                 // kKvBf16, kKvE4m3 or kKvInt8
+  float scale_log2;             // softmax scale * log2(e) (* kv_scale for an 8-bit pool)
+  float v_scale;                // 1, or kv_scale for an 8-bit pool (applied in the epilogue)
   const int32_t* page_table;
   const int32_t* seq_lens;
-  const uint8_t* kv_pool;       // pool base (e4m3 path copies raw pages from here)
+  const uint8_t* kv_pool;       // pool base (the 8-bit path reads raw rows from here)
   __nv_bfloat16* out;           // [B, T, H, 512]
   float* lse;                   // [B, T, H]
   __nv_bfloat16* ws_o;          // [B, max_splits, R, 512] partial outputs (normalised, bf16)

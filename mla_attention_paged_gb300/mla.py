@@ -23,6 +23,7 @@ MLA_ERR_TIMEOUT = 5
 MLA_ERR_DEVICE_ARG = 6
 MLA_KV_BF16 = 0
 MLA_KV_E4M3 = 1
+MLA_KV_INT8 = 2
 
 EXPORTED = ["mla_decode_plan", "mla_decode", "mla_decode_partial", "mla_decode_combine", "mla_prefill_varlen", "mla_get_status",
             "mla_status_string", "mla_version", "mla_set_profile_events", "mla_profile_elapsed_ms",

@@ -1,8 +1,8 @@
 """GPU parity of mla_decode (through the C ABI) against the fp64 CPU oracle.
 
 Tolerances (bf16 output): max-abs 2e-2 and relative L2 5e-3 over the compared outputs,
-LSE within 1e-3 absolute; FP8 KV: max-abs 6e-2 against the oracle run on the same e4m3
-codes and scale.  Small cases are compared element by element over every output; the
+LSE within 1e-3 absolute; 8-bit KV (e4m3 or int8): max-abs 6e-2 against the oracle run on
+the same codes and scale.  Small cases are compared element by element over every output; the
 full-size workloads are compared on sampled rows the oracle computes one by one, in the
 same launch configuration the benchmark times.
 """
@@ -38,7 +38,7 @@ def run_gpu(mla, inp, num_sms=0, dev="cuda"):
     pool = inp.kv_pool.to(dev)
     pt = inp.page_table.to(dev)
     sl = inp.seq_lens.to(dev)
-    kvd = mla.MLA_KV_E4M3 if pool.dtype == torch.uint8 else mla.MLA_KV_BF16
+    kvd = {torch.uint8: mla.MLA_KV_E4M3, torch.int8: mla.MLA_KV_INT8}.get(pool.dtype, mla.MLA_KV_BF16)
     plan = mla.decode_plan(inp.seq_lens.cpu(), wl.q_len, wl.heads, wl.page_size, pt.shape[1], pool.shape[0],
                            kvd, num_sms)
     out, lse = mla.decode(plan, q, pool, pt, sl, inp.scale, inp.kv_scale)
@@ -67,7 +67,7 @@ def _full_check(mla, oracle_mod, wl, num_sms=0):
     out, lse, plan = run_gpu(mla, inp, num_sms)
     ref_out, ref_lse = oracle_mod.mla_decode(inp.q, inp.kv_pool, inp.page_table, inp.seq_lens, inp.scale,
                                              kv_scale=inp.kv_scale)
-    check(out, lse, ref_out, ref_lse, fp8=(wl.kv_dtype == "e4m3"))
+    check(out, lse, ref_out, ref_lse, fp8=(wl.kv_dtype != "bf16"))
     return out, lse, plan
 
 
@@ -96,6 +96,11 @@ SMALL = [
     ("fp8_h128", 1, 2, 128, [900], 64, "e4m3"),
     ("mtp8", 2, 8, 16, [700, 2000], 64, "bf16"),   # q_len 8: 128 folded rows, two row groups
     ("fp8_mtp8", 2, 8, 16, [333, 1500], 64, "e4m3"),
+    ("int8_drafts4", 2, 4, 16, [300, 1000], 64, "int8"),
+    ("int8_ragged", 3, 1, 16, [1, 65, 130], 64, "int8"),
+    ("int8_page16", 2, 2, 16, [77, 500], 16, "int8"),
+    ("int8_page128", 1, 3, 16, [700], 128, "int8"),
+    ("int8_h128", 1, 2, 128, [900], 64, "int8"),
 ]
 
 
@@ -117,7 +122,7 @@ def test_decode_split_counts_agree(mla, oracle_mod, num_sms):
         assert plan.max_splits > 1
 
 
-@pytest.mark.parametrize("kv", ["bf16", "e4m3"])
+@pytest.mark.parametrize("kv", ["bf16", "e4m3", "int8"])
 def test_decode_combine_many_splits(mla, oracle_mod, kv):
     """More than 64 splits per request: the combine takes its splits in several batches and
     rescales the running sum between them; a ragged batch mixes 2 to ~80 splits."""
@@ -126,13 +131,14 @@ def test_decode_combine_many_splits(mla, oracle_mod, kv):
     assert plan.max_splits > 64
 
 
-@pytest.mark.parametrize("kv,num_sms", [("bf16", 0), ("e4m3", 0), ("bf16", 1)], ids=["bf16", "e4m3", "one_split"])
+@pytest.mark.parametrize("kv,num_sms", [("bf16", 0), ("e4m3", 0), ("int8", 0), ("bf16", 1)],
+                         ids=["bf16", "e4m3", "int8", "one_split"])
 def test_decode_stages_equal_decode_bitwise(mla, kv, num_sms):
     """mla_decode_partial then mla_decode_combine gives mla_decode's bits (multi-split and
     single-split plans; the combine enqueues nothing for the latter)."""
     wl = DecodeWorkload("stages", 3, 4, 16, [5000, 130, 2999], kv_dtype=kv, seed=79, peaked=True)
     inp = make_decode_inputs(wl, "cuda")
-    kvd = mla.MLA_KV_E4M3 if kv == "e4m3" else mla.MLA_KV_BF16
+    kvd = {"e4m3": mla.MLA_KV_E4M3, "int8": mla.MLA_KV_INT8}.get(kv, mla.MLA_KV_BF16)
     plan = mla.decode_plan(wl.seq_lens, wl.q_len, wl.heads, wl.page_size, inp.page_table.shape[1],
                            inp.kv_pool.shape[0], kvd, num_sms)
     assert (plan.max_splits > 1) == (num_sms == 0)
@@ -146,7 +152,7 @@ def test_decode_stages_equal_decode_bitwise(mla, kv, num_sms):
     assert torch.equal(lse1.view(torch.int32), lse2.view(torch.int32))
 
 
-@pytest.mark.parametrize("kv", ["bf16", "e4m3"])
+@pytest.mark.parametrize("kv", ["bf16", "e4m3", "int8"])
 def test_decode_one_million_keys_sampled(mla, oracle_mod, kv):
     """A 2^20-key context (16384 pages of 64): the planner's split count and the kernels at
     the long end, checked on sampled rows the oracle computes one by one."""
@@ -157,7 +163,7 @@ def test_decode_one_million_keys_sampled(mla, oracle_mod, kv):
     rows = [0, 5, 16, 31]
     ref_out, ref_lse = oracle_mod.mla_decode(inp.q.cpu(), inp.kv_pool.cpu(), inp.page_table.cpu(),
                                              inp.seq_lens.cpu(), inp.scale, kv_scale=inp.kv_scale, rows=rows)
-    check(out.reshape(-1, 512)[rows], lse.reshape(-1)[rows], ref_out, ref_lse, fp8=(kv == "e4m3"))
+    check(out.reshape(-1, 512)[rows], lse.reshape(-1)[rows], ref_out, ref_lse, fp8=(kv != "bf16"))
     assert np.isfinite(out).all() and np.isfinite(lse).all()
 
 
@@ -216,6 +222,6 @@ def test_decode_full_size_sampled(mla, oracle_mod, name):
     rows = _sample_rows(wl, per_request=16 if wl.batch <= 4 else 6)
     ref_out, ref_lse = oracle_mod.mla_decode(inp.q.cpu(), inp.kv_pool.cpu(), inp.page_table.cpu(),
                                              inp.seq_lens.cpu(), inp.scale, kv_scale=inp.kv_scale, rows=rows)
-    check(out.reshape(-1, 512)[rows], lse.reshape(-1)[rows], ref_out, ref_lse, fp8=(wl.kv_dtype == "e4m3"))
+    check(out.reshape(-1, 512)[rows], lse.reshape(-1)[rows], ref_out, ref_lse, fp8=(wl.kv_dtype != "bf16"))
     # every output finite, including rows not sampled
     assert np.isfinite(out).all() and np.isfinite(lse).all()

@@ -505,7 +505,8 @@ def main():
         line["extra"] = {"prefill": measure_prefill(mla, dev)}
         for name in ["decode_bf16_b16_q4_h16_l64k", "decode_fp8_b16_q4_h16_l64k", "decode_int8_b16_q4_h16_l64k",
                      "decode_fp8_b8_q4_h16_l64k",
-                     "decode_b16_q2_h16_ragged", "decode_b16_q2_h128_ragged", "decode_b1_q1_h16_l1024"]:
+                     "decode_b16_q2_h16_ragged", "decode_b16_q2_h128_ragged", "decode_b1_q1_h16_l1024",
+                     "decode_b4_q512_h16_l32k"]:
             line["extra"][name] = measure_decode_extra(mla, name, dev)
             torch.cuda.empty_cache()
     if rank == 0:

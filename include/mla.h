@@ -21,7 +21,8 @@
  *  [READ]  "TokenSpeed 深度解析" (gitread.org), section "核心技术揭秘": KV is managed in
  *          fixed-size blocks reached through a table (paged KV).
  *
- * Shapes used throughout: B requests, T = q_len draft tokens per request (1..8), H heads,
+ * Shapes used throughout: B requests, T = q_len draft tokens per request (1..8192; beyond
+ * a few drafts this is the prefill of T new tokens over a paged prefix, absorbed form), H heads,
  * D = 576 latent columns (512 latent + 64 rope), Dv = 512 (the value is the first 512
  * latent columns).  Prefill: 16-bit q/k with Dqk = 192 and v with Dv' = 128.
  *
@@ -94,8 +95,8 @@ typedef struct mla_decode_plan_t {
  *                   draft tokens (the drafts are the last q_len positions).
  *   num_sms       : SMs to plan for; 0 = query the current device.
  * Errors: MLA_ERR_INVALID_ARG (null pointers, batch < 1, a length < q_len or beyond
- * max_pages_per_seq*page_size), MLA_ERR_UNSUPPORTED (q_len > 8, page_size not one of
- * 8,16,32,64,128,256, or more than 1024 folded rows), MLA_ERR_CUDA (device query). */
+ * max_pages_per_seq*page_size), MLA_ERR_UNSUPPORTED (q_len > 8192, page_size not one
+ * of 8,16,32,64,128,256, or more than 131072 folded rows), MLA_ERR_CUDA (device query). */
 int mla_decode_plan(int batch, const int32_t* seq_lens_host, int q_len, int num_heads,
                     int page_size, int max_pages_per_seq, int64_t num_pages, int kv_dtype,
                     int num_sms, mla_decode_plan_t* plan_out);

@@ -146,7 +146,10 @@ int mla_decode_plan(int batch, const int32_t* seq_lens_host, int q_len, int num_
       num_pages < 1)
     return MLA_ERR_INVALID_ARG;
   if (kv_dtype != MLA_KV_BF16 && kv_dtype != MLA_KV_E4M3 && kv_dtype != MLA_KV_INT8) return MLA_ERR_INVALID_ARG;
-  if (q_len > 8 || !page_size_ok(page_size) || q_len * num_heads > 1024) return MLA_ERR_UNSUPPORTED;
+  // q_len beyond a few drafts is the prefill of q_len new tokens over a paged prefix in
+  // absorbed form (the same computation: new token t sees keys 0 .. L - q_len + t)
+  if (q_len > 8192 || !page_size_ok(page_size) || static_cast<int64_t>(q_len) * num_heads > 131072)
+    return MLA_ERR_UNSUPPORTED;
   if (batch > 65535) return MLA_ERR_UNSUPPORTED;
   std::vector<int> lens(seq_lens_host, seq_lens_host + batch);
   int max_len = 0;

@@ -78,6 +78,9 @@ def decode_workloads():
             "decode_bf16_b16_q4_h16_l64k", 16, 4, 16, [65536] * 16, seed=1003),
         "decode_int8_b16_q4_h16_l64k": DecodeWorkload(
             "decode_int8_b16_q4_h16_l64k", 16, 4, 16, [65536] * 16, kv_dtype="int8", seed=1003),
+        # prefill in absorbed form over a paged prefix: 512 new tokens on 32K cached ones
+        "decode_b4_q512_h16_l32k": DecodeWorkload(
+            "decode_b4_q512_h16_l32k", 4, 512, 16, [32768 + 512] * 4, seed=1005),
     }
 
 

@@ -93,12 +93,13 @@ def test_plan_is_memoised_and_deterministic(mla):
 @pytest.mark.parametrize("kw,code", [
     (dict(seq_lens=[3], q_len=4), 1),                 # fewer cached tokens than drafts
     (dict(seq_lens=[10000], max_pages=10), 1),        # beyond the table
-    (dict(q_len=9), 2),                               # more than 8 drafts
+    (dict(seq_lens=[10000], q_len=8193), 2),          # more new tokens than the absorbed prefill takes
+    (dict(seq_lens=[10000], q_len=2048, heads=128), 2),  # more than 131072 folded rows
     (dict(page_size=48), 2),                          # unsupported page size
     (dict(kv_dtype=7), 1),
 ])
 def test_plan_rejects_bad_arguments(mla, kw, code):
-    args = dict(seq_lens=[100], q_len=1, heads=16, page_size=64, max_pages=10, pages=10, kv_dtype=0)
+    args = dict(seq_lens=[100], q_len=1, heads=16, page_size=64, max_pages=200, pages=200, kv_dtype=0)
     args.update(kw)
     lens = torch.tensor(args["seq_lens"], dtype=torch.int32)
     plan = mla.DecodePlan()

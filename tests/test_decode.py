@@ -167,6 +167,16 @@ def test_decode_one_million_keys_sampled(mla, oracle_mod, kv):
     assert np.isfinite(out).all() and np.isfinite(lse).all()
 
 
+@pytest.mark.parametrize("kv,T,lens", [("bf16", 64, [200, 1000]), ("bf16", 300, [4400]), ("e4m3", 128, [129, 3000])],
+                         ids=["bf16_t64", "bf16_t300", "e4m3_t128"])
+def test_decode_absorbed_prefill_over_paged_prefix(mla, oracle_mod, kv, T, lens):
+    """Prefill of T new tokens over a paged prefix in absorbed form: the decode call with
+    q_len = T (new token t sees the prefix and new tokens 0..t), T*H folded rows in many
+    64-row groups; every output compared."""
+    wl = DecodeWorkload("absorbed_prefill", len(lens), T, 16, lens, kv_dtype=kv, seed=81 + T)
+    _full_check(mla, oracle_mod, wl)
+
+
 def test_decode_page_shuffle_invariance_bitwise(mla):
     wl = DecodeWorkload("shuffle", 2, 4, 16, [1500, 777], seed=5, extra_pages=7)
     inp = make_decode_inputs(wl, "cpu")

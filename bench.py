@@ -328,6 +328,32 @@ def run_reference(args, ws, rank):
     print(json.dumps(line), flush=True)
 
 
+def run_profile_case(name):
+    """Three calls of one workload, for a profiler to capture (no timing, no JSON line)."""
+    from mla_attention_paged_gb300 import build
+    from mla_attention_paged_gb300.inputs import make_prefill_inputs, prefill_workloads
+    build.build()
+    from mla_attention_paged_gb300 import mla
+    if name in prefill_workloads():
+        inp = make_prefill_inputs(prefill_workloads()[name], "cuda")
+        for _ in range(3):
+            mla.prefill_varlen(inp.q, inp.k, inp.v, inp.cu_seqlens_q, inp.cu_seqlens_kv, inp.prefix_lens,
+                               inp.max_seqlen_q, inp.scale)
+    else:
+        wl = decode_workloads()[name]
+        inp = make_decode_inputs(wl, "cuda")
+        kvd = {"e4m3": mla.MLA_KV_E4M3, "int8": mla.MLA_KV_INT8}.get(wl.kv_dtype, mla.MLA_KV_BF16)
+        plan = mla.decode_plan(wl.seq_lens, wl.q_len, wl.heads, wl.page_size, inp.page_table.shape[1],
+                               inp.kv_pool.shape[0], kvd)
+        for _ in range(3):
+            mla.decode(plan, inp.q, inp.kv_pool, inp.page_table, inp.seq_lens, inp.scale, inp.kv_scale)
+    torch.cuda.synchronize()
+    status = mla.get_status()
+    if status != mla.MLA_OK:
+        raise RuntimeError(f"device status {mla.status_string(status)}")
+    print(f"profile case {name}: ok", flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -336,7 +362,12 @@ def main():
     ap.add_argument("--impl", default="mine", choices=["mine", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extra", action="store_true", help="skip the secondary prefill / batch-16 decode lines")
+    ap.add_argument("--profile-case", default=None,
+                    help="run three calls of one named workload (a profiler target) and exit without timing")
     args = ap.parse_args()
+    if args.profile_case:
+        run_profile_case(args.profile_case)
+        return
     args.warmup = max(args.warmup, 3)
     ws, rank, local = _dist()
     if args.impl == "reference":

@@ -3,8 +3,9 @@
 // What it computes (per request b, draft t, head h; keys j = 0 .. L_b - T + t):
 //   out[b,t,h,:] = sum_j softmax_j(scale * q[b,t,h,:] . k_j) * k_j[:512]
 // where k_j is the 576-wide latent row j of request b, found through the page table (an
-// e4m3 pool is decoded exactly to bf16 and its per-tensor scale folded into the softmax
-// scale and the output).  TokenSpeed pages: "构建面向 Agentic 推理的下一代 LLM 推理引擎"
+// e4m3 or int8 pool is decoded exactly to f16 and its per-tensor scale folded into the
+// softmax scale and the output).  With T beyond a few drafts the same computation is the
+// prefill of T new tokens over a paged prefix in absorbed form.  TokenSpeed pages: "构建面向 Agentic 推理的下一代 LLM 推理引擎"
 // (AICon talk), section "Kernel：让 MLA 真正跑满 GPU" (latent state shared by all heads,
 // fold factor, split-KV partial + reduction stages, TMEM accumulators, KV bandwidth as the
 // limit even with 8-bit KV); launch-blog repost "英偉達力薦，小團隊兩個月開源一款「光速級」
@@ -16,11 +17,12 @@
 //    takes 64 consecutive rows, so all heads and drafts share each latent tile load.
 //  * Producer warp: bf16 pools are gathered by TMA (one 3-D box per 64-key tile: 64 rows x
 //    nine 128-byte-swizzled column blocks) from the pages named by the page table, into a
-//    2-stage ring.  For e4m3 pools, three dequant warps (4, 6, 7) read each tile's rows
+//    2-stage ring.  For 8-bit pools, three dequant warps (4, 6, 7) read each tile's rows
 //    from the page pool into registers, wait for the stage, and write them as f16 into the
-//    same swizzled layout (exact decode, values times 2^-8; the factor is folded into the
-//    scales); the MMA warp prefetches rows into L2 a few tiles ahead of them.  The e4m3
-//    GEMMs run on f16 operands (Q converted once per CTA, P in f16).
+//    same swizzled layout (exact decode: e4m3 values times 2^-8, the factor folded into
+//    the scales; int8 codes as themselves); the MMA warp prefetches rows into L2 a few
+//    tiles ahead of them.  The 8-bit GEMMs run on f16 operands (Q converted once per CTA,
+//    P in f16).
 //  * MMA warp (uniform control flow, one elected thread issues): BMM1  S[rows, keys] =
 //    Q . K^T  (M=64, N=64, K=576) into TMEM, double-buffered; BMM2  O^T[dims, rows] +=
 //    V^T . P^T  (M=128 per 128 value columns, N=rows, K=64 keys) with V^T read MN-major
@@ -34,7 +36,8 @@
 //    (bf16) to shared memory as the K-major B operand of BMM2.
 //  * Epilogue (4 warps over the 128 TMEM lanes = value columns): normalise by the row
 //    sum and write either the final bf16 output (single split) or the bf16 partial and
-//    its fp32 log-sum-exp for the combine kernel.
+//    its fp32 log-sum-exp for the combine kernel, which runs as a programmatic dependent
+//    launch triggered after each CTA's last store.
 // Every wait is bounded; on expiry the CTA records a timeout in the status word, drains
 // its in-flight copies and MMAs, frees TMEM and returns.
 #include <cuda_fp16.h>

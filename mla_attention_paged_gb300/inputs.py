@@ -88,7 +88,10 @@ def prefill_workloads():
     g = torch.Generator().manual_seed(1004)
     prefix = [int(x) for x in torch.randint(20000, 100001, (5,), generator=g)]
     new = [int(x) for x in torch.randint(256, 2049, (5,), generator=g)]
-    return {"prefill_b5_h16_prefix": PrefillWorkload("prefill_b5_h16_prefix", prefix, new, 16, seed=1004)}
+    return {"prefill_b5_h16_prefix": PrefillWorkload("prefill_b5_h16_prefix", prefix, new, 16, seed=1004),
+            # a smaller case of the same kernel (K/V ~1 GB, above L2) for profiler captures
+            "prefill_b2_h16_prefix24k": PrefillWorkload("prefill_b2_h16_prefix24k", [24000, 23000], [1024, 1024], 16,
+                                                        seed=1006)}
 
 
 @dataclass

@@ -103,7 +103,9 @@ int mla_decode_plan(int batch, const int32_t* seq_lens_host, int q_len, int num_
 
 /* Absorbed MLA decode with speculative draft tokens over the paged latent cache.
  *   q          : [B, T, H, 576] bf16.  Folded row m = t*H + h of request b.
- *   kv_pages   : [num_pages, page_size, 576] bf16, e4m3 or int8 bytes (plan->kv_dtype).
+ *   kv_pages   : [num_pages, page_size, 576] bf16, e4m3 or int8 bytes (plan->kv_dtype);
+ *                the allocation must hold all num_pages pages in the plan's format (the
+ *                library cannot check it: a pool of another format is read out of bounds).
  *   page_table : [B, max_pages_per_seq] int32; latent row j of request b is
  *                kv_pages[page_table[b, j / page_size], j % page_size, :].
  *   seq_lens   : [B] int32 device copy of the planned lengths (each <= max_seq_len).

@@ -53,15 +53,16 @@ constexpr int kDimBlocks = kLatentDim / 64;          // 9 blocks of 64 columns (
 constexpr int kBlockBytes = 64 * 128;                // 64 rows x 128 bytes, swizzled
 constexpr int kTileBytes = kDimBlocks * kBlockBytes; // 73728: one bf16 64-key latent tile
 constexpr int kStages = 2;
-constexpr int kPrefetchTiles = 3;  // e4m3: tiles ahead of the decode that are prefetched into L2
-// Warps 0-3 softmax/epilogue, 5 MMA; bf16: warp 4 producer (192 threads); e4m3: warps 4, 6
-// and 7 decode (256 threads: eight warps keep the register budget at 255 per thread).
+constexpr int kPrefetchTiles = 3;  // 8-bit pools: tiles ahead of the decode that are prefetched into L2
+// Warps 0-3 softmax/epilogue, 5 MMA; bf16: warp 4 producer (192 threads); 8-bit pools:
+// warps 4, 6 and 7 decode (256 threads: eight warps keep the register budget at 255 per
+// thread).
 constexpr int kDequantThreads = 96;
 __host__ __device__ constexpr int threads_for(bool fp8) { return fp8 ? 256 : 192; }
 
 // Shared memory map: Q | stage0 | stage1 | P | ctrl.  A stage holds one 64-key tile as nine
-// 128-byte-swizzled column blocks: bf16 as loaded by TMA, or (e4m3) f16 as decoded by the
-// dequant warps from rows they read straight from global memory.
+// 128-byte-swizzled column blocks: bf16 as loaded by TMA, or (8-bit pools) f16 as decoded
+// by the dequant warps from rows they read straight from global memory.
 constexpr int kOffQ = 0;
 constexpr int kOffStages = kOffQ + kTileBytes;
 constexpr int kOffP = kOffStages + kStages * kTileBytes;
@@ -69,13 +70,13 @@ constexpr int kOffCtrl = kOffP + kBlockBytes;
 
 struct DecodeCtrl {
   uint64_t q_full;
-  uint64_t kv_full[kStages];   // tile landed (bf16: TMA bytes; e4m3: dequant threads)
+  uint64_t kv_full[kStages];   // tile landed (bf16: TMA bytes; 8-bit: dequant threads)
   uint64_t kv_empty[kStages];  // BMM2 of the tile in this stage completed
   uint64_t s_full[2];
   uint64_t s_free[2];
   uint64_t p_full;
   uint64_t o_done;
-  uint64_t q_ready;            // e4m3: Q converted to f16 in place
+  uint64_t q_ready;            // 8-bit pools: Q converted to f16 in place
   uint64_t mma_drain;
   uint32_t tmem_base;
   int abort_flag;
@@ -332,7 +333,7 @@ decode_partial_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
   } else if (warp == 5) {
     // ------------------------------------------------------------------ MMA issuer (whole warp,
     // uniform control flow; one elected thread issues each GEMM's MMAs and their commit)
-    // the e4m3 path multiplies f16 operands (Q converted once, K/V decoded to f16, P in f16)
+    // the 8-bit path multiplies f16 operands (Q converted once, K/V decoded to f16, P in f16)
     const uint32_t idesc1 = kFp8 ? make_idesc_f16(64, 64, false, false) : make_idesc_bf16(64, 64, false, false);
     const uint32_t idesc2 = kFp8 ? make_idesc_f16(128, nq, true, false) : make_idesc_bf16(128, nq, true, false);
     // Descriptors are built once; each MMA advances the start-address field by a
@@ -344,7 +345,7 @@ decode_partial_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
       if (lane == 0) v = mbar_test_wait(bar, parity) ? 1u : 0u;
       return __shfl_sync(0xffffffffu, v, 0) != 0;
     };
-    // e4m3: lanes < sub (pages per tile) prefetch their page of tile n1 + 1 + kPrefetchTiles
+    // 8-bit pools: lanes < sub (pages per tile) prefetch their page of tile n1 + 1 + kPrefetchTiles
     // into L2 each time BMM1(n1) is issued, with the page id looked up one BMM1 earlier.
     const int P = p.page_size;
     const int sub = P < kTileKeys ? kTileKeys / P : 1;
@@ -454,8 +455,8 @@ decode_partial_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
     }
     __syncwarp();
   } else if (kFp8 && warp >= 4) {
-    // ------------------------------------------------------------------ e4m3 dequant (warps 4, 6, 7):
-    // Q to f16 in place once; then, per tile, each lane reads its rows' e4m3 bytes straight
+    // ------------------------------------------------------------------ 8-bit dequant (warps 4, 6, 7):
+    // Q to f16 in place once; then, per tile, each lane reads its rows' e4m3 / int8 bytes straight
     // from the page pool into registers (issued before waiting for the stage, so the reads
     // overlap the previous tile's GEMMs), waits for the stage, and writes them as f16 into
     // the swizzled tile.  Lane dl of decode warp dw (0..2) owns rows dl/4 + 8i (i < 8) and
@@ -565,7 +566,7 @@ decode_partial_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
         mbar_arrive(&ctrl->s_free[sb]);
         // keys i <= lim of this lane's 32-key half are visible
         const int lim = row_active ? (min(kv_end - 1, lim_abs) - k0 - 32 * half) : -1;
-        // the e4m3 path multiplies P in f16 (P <= 2^8 here, where f16 keeps more bits than bf16)
+        // the 8-bit path multiplies P in f16 (P <= 2^8 here, where f16 keeps more bits than bf16)
         online_softmax_step<32, true, kFp8>(sr, lim, scale_log2, kRescaleThreshold, m_used, l_sum, packed, alpha,
                                             need_rescale);
       }

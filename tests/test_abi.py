@@ -5,6 +5,8 @@ import ctypes
 import os
 import re
 
+import numpy as np
+
 import pytest
 import torch
 
@@ -82,6 +84,40 @@ def test_plan_head_groups_for_many_heads(mla):
     plan = mla.decode_plan([8192, 131072], q_len=2, num_heads=128, page_size=64, max_pages_per_seq=2048,
                            num_pages=4096, num_sms=152)
     assert plan.rows == 256 and plan.head_groups == 4
+
+
+def test_plan_invariants_on_random_batches(mla):
+    """Seeded random batches (ragged lengths, 1-8 drafts or a long absorbed prefill, 16 or
+    128 heads, several SM counts): the split chunk is whole 64-key tiles and at least four
+    of them (or the whole of the longest request), one wave of CTAs whenever a request is
+    split, the smallest chunk with that property, and a workspace that fits every split."""
+    rng = np.random.default_rng(12)
+    for _ in range(60):
+        B = int(rng.integers(1, 40))
+        T = int(rng.choice([1, 2, 4, 8, 300]))
+        H = int(rng.choice([16, 128]))
+        if T * H > 131072:
+            continue
+        sms = int(rng.choice([16, 100, 152]))
+        lens = [int(x) for x in rng.integers(T, 200000, B)]
+        mp = (max(lens) + 63) // 64
+        plan = mla.decode_plan(lens, q_len=T, num_heads=H, page_size=64, max_pages_per_seq=mp,
+                               num_pages=B * mp, num_sms=sms)
+        tiles = [(L + 63) // 64 for L in lens]
+        ct = plan.chunk_tokens // 64
+        assert plan.chunk_tokens % 64 == 0 and ct >= min(4, max(tiles))
+        groups = (T * H + 63) // 64
+        assert plan.head_groups == groups
+        ctas = groups * sum((t + ct - 1) // ct for t in tiles)
+        assert plan.max_splits == (max(lens) + plan.chunk_tokens - 1) // plan.chunk_tokens
+        if plan.max_splits > 1:
+            assert ctas <= sms
+            if ct > min(4, max(tiles)):
+                assert groups * sum((t + ct - 2) // (ct - 1) for t in tiles) > sms
+            parts = B * plan.max_splits * T * H
+            assert plan.workspace_bytes == 256 + parts * 512 * 2 + parts * 4
+        else:
+            assert plan.workspace_bytes == 0
 
 
 def test_plan_is_memoised_and_deterministic(mla):

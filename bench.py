@@ -7,6 +7,15 @@ Inputs are rotated over several independent input sets whose KV totals more than
 the L2 size, so every step streams its KV from HBM.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+    python bench.py --profile-case <workload>     (three calls, for a profiler capture)
+
+Timing: `value` = KV bytes / time of one CUDA graph holding the K steps (no event nodes
+inside); the roofline's kernel time = one pair of CUDA events around a second graph of
+back-to-back launches of the split-KV partial kernel alone (mla_decode_partial); `e2e` =
+wall clock of K end-to-end steps (one packed H2D copy of q / page table / lengths, the
+decode call, one packed D2H copy of out / lse, copies on their own streams) replayed from
+one graph.  The extra lines (prefill, batch-16 bf16 / e4m3 / int8 decode, ragged and
+128-head decode, absorbed prefill, a latency case) are graph-timed the same way.
 
 N > 1 runs under torchrun: every rank runs an independent replica (the path has no
 exchange step); value = all ranks' KV bytes / max-over-ranks time.

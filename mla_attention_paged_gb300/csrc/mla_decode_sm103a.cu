@@ -210,28 +210,13 @@ decode_partial_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
   const int split = blockIdx.y;
   const int b = blockIdx.z;
 
-  const int L = p.seq_lens[b];
-  if (L < p.T || L > p.max_seq || L > p.max_pages * p.page_size) {
-    if (threadIdx.x == 0 && split == 0 && group == 0) atomicOr(p.status, kStatusDeviceArg);
-    return;
-  }
-  const int kv_start = split * p.chunk;
-  if (kv_start >= L) return;  // this request needs fewer splits
-  const int kv_end = min(L, kv_start + p.chunk);
-  const int ntiles = (kv_end - kv_start + kTileKeys - 1) / kTileKeys;
-  const int nsplit_b = (L + p.chunk - 1) / p.chunk;
-  const int row0 = group * kGroupRows;
-  const int nrows = min(kGroupRows, p.R - row0);
-  const int nq = (nrows + 15) & ~15;  // BMM2 N (multiple of 16)
-
+  // Set-up that reads no input of this call: barriers, TMEM, descriptor prefetch.  The
+  // kernel is launched as a programmatic dependent of the stream's previous kernel, so this
+  // part may overlap that kernel's tail; griddepcontrol.wait below then holds every thread
+  // until that kernel has completed and its writes are visible.
   if (threadIdx.x == 0) {
-    // Q (nine 64-column blocks of the 64 folded rows) is requested first, by the thread that
-    // initialises q_full, so the barrier is armed only after its initialisation
     tma_prefetch_desc(&tm_q);
     mbar_init(&ctrl->q_full, 1);
-    fence_mbarrier_init();
-    mbar_arrive_expect_tx(&ctrl->q_full, kTileBytes);
-    tma_load_3d(smem + kOffQ, &tm_q, &ctrl->q_full, 0, b * p.R + row0, 0, policy_evict_last());
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&ctrl->kv_full[s], kFp8 ? kDequantThreads : 1);
       mbar_init(&ctrl->kv_empty[s], 1);
@@ -257,6 +242,27 @@ decode_partial_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = ctrl->tmem_base;
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+
+  const int L = p.seq_lens[b];
+  const bool bad_len = L < p.T || L > p.max_seq || L > p.max_pages * p.page_size;
+  if (bad_len && threadIdx.x == 0 && split == 0 && group == 0) atomicOr(p.status, kStatusDeviceArg);
+  const int kv_start = split * p.chunk;
+  if (bad_len || kv_start >= L) {  // (CTA-uniform) a bad length, or this request needs fewer splits
+    if (warp == 5) tmem_dealloc(tmem, kTmemCols);  // no tensor-core work was issued
+    return;
+  }
+  const int kv_end = min(L, kv_start + p.chunk);
+  const int ntiles = (kv_end - kv_start + kTileKeys - 1) / kTileKeys;
+  const int nsplit_b = (L + p.chunk - 1) / p.chunk;
+  const int row0 = group * kGroupRows;
+  const int nrows = min(kGroupRows, p.R - row0);
+  const int nq = (nrows + 15) & ~15;  // BMM2 N (multiple of 16)
+  if (threadIdx.x == 0) {
+    // Q: nine 64-column blocks of the 64 folded rows
+    mbar_arrive_expect_tx(&ctrl->q_full, kTileBytes);
+    tma_load_3d(smem + kOffQ, &tm_q, &ctrl->q_full, 0, b * p.R + row0, 0, policy_evict_last());
+  }
   volatile int* abort_flag = &ctrl->abort_flag;
 
   if (warp == 4 && !kFp8) {
@@ -854,9 +860,19 @@ cudaError_t launch_partial_impl(const DecodeParams& p, const CUtensorMap& tm_q, 
     if (e != cudaSuccess) return e;
     configured_device = dev;
   }
-  dim3 grid(head_groups, p.max_splits, p.B);
-  decode_partial_kernel<kKv><<<grid, threads_for(kKv != kKvBf16), kSmemBytes, stream>>>(tm_q, tm_kv, p);
-  return cudaGetLastError();
+  // programmatic dependent launch: the kernel's set-up may overlap the previous kernel,
+  // whose completion it awaits (griddepcontrol.wait) before reading any input
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(head_groups, p.max_splits, p.B);
+  cfg.blockDim = dim3(threads_for(kKv != kKvBf16));
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, decode_partial_kernel<kKv>, tm_q, tm_kv, p);
 }
 
 }  // namespace

@@ -119,6 +119,11 @@ int mla_decode_plan(int batch, const int32_t* seq_lens_host, int q_len, int num_
  *                overwritten; calls that share one workspace must be stream-ordered.
  * Enqueues the split-KV partial kernel and, when any request has more than one split,
  * the LSE-merge combine kernel on `stream`.  No allocation, no host synchronisation.
+ * Both are programmatic dependent launches: the partial kernel may set itself up while the
+ * stream's previous kernel finishes, but reads no input before that kernel has completed;
+ * the combine waits in the same way for the partial kernel.  A kernel enqueued after this
+ * call as a programmatic dependent must itself wait (griddepcontrol.wait or
+ * cudaGridDependencySynchronize) before it reads out or lse.
  * Errors: MLA_ERR_INVALID_ARG (null pointers, q_len/num_heads differ from the plan,
  * misaligned pointers: q, kv_pages 16-byte, out 16-byte), MLA_ERR_WORKSPACE_TOO_SMALL,
  * MLA_ERR_CUDA (tensor-map encoding or launch failure). */

@@ -894,12 +894,16 @@ cudaError_t launch_selftest_timeout(unsigned* status, cudaStream_t stream) {
 cudaError_t launch_decode_combine(const DecodeParams& p, cudaStream_t stream) {
   const dim3 grid((p.R + kCombineRows - 1) / kCombineRows, p.B);
   const int smem = min(p.max_splits, kCombineBatch) * kCombineRows * kCombineRowBytes;
-  static bool attr_set = false;
-  if (!attr_set) {
-    const cudaError_t e = cudaFuncSetAttribute(decode_combine_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               kCombineBatch * kCombineRows * kCombineRowBytes);
+  // the shared-memory limit is a per-device attribute: set it once per device and thread
+  static thread_local int configured_device = -1;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (configured_device != dev) {
+    e = cudaFuncSetAttribute(decode_combine_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kCombineBatch * kCombineRows * kCombineRowBytes);
     if (e != cudaSuccess) return e;
-    attr_set = true;
+    configured_device = dev;
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;

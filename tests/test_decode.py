@@ -167,6 +167,23 @@ def test_decode_one_million_keys_sampled(mla, oracle_mod, kv):
     assert np.isfinite(out).all() and np.isfinite(lse).all()
 
 
+def test_decode_maximum_rows_sampled(mla, oracle_mod):
+    """The largest call the plan accepts: q_len 8192 new tokens x 16 heads = 131072 folded
+    rows (2048 row groups, more than one wave of CTAs) over a 640-token paged prefix;
+    sampled rows at the first and last tokens and at row-group boundaries against the
+    oracle, every output finite."""
+    T, H = 8192, 16
+    wl = DecodeWorkload("max_rows", 1, T, H, [T + 640], seed=83)
+    inp = make_decode_inputs(wl, "cuda")
+    out, lse, plan = run_gpu(mla, inp)
+    assert plan.rows == T * H == 131072 and plan.head_groups == 2048
+    rows = [0, 1, 15, 16, 63, 64, 65, 4095, 4096, 65535, 65536, 100000, 131007, 131008, 131070, 131071]
+    ref_out, ref_lse = oracle_mod.mla_decode(inp.q.cpu(), inp.kv_pool.cpu(), inp.page_table.cpu(),
+                                             inp.seq_lens.cpu(), inp.scale, kv_scale=inp.kv_scale, rows=rows)
+    check(out.reshape(-1, 512)[rows], lse.reshape(-1)[rows], ref_out, ref_lse, fp8=False)
+    assert np.isfinite(out).all() and np.isfinite(lse).all()
+
+
 @pytest.mark.parametrize("kv,T,lens", [("bf16", 64, [200, 1000]), ("bf16", 300, [4400]), ("e4m3", 128, [129, 3000])],
                          ids=["bf16_t64", "bf16_t300", "e4m3_t128"])
 def test_decode_absorbed_prefill_over_paged_prefix(mla, oracle_mod, kv, T, lens):

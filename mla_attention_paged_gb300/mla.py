@@ -25,9 +25,10 @@ MLA_KV_BF16 = 0
 MLA_KV_E4M3 = 1
 MLA_KV_INT8 = 2
 
-EXPORTED = ["mla_decode_plan", "mla_decode", "mla_decode_partial", "mla_decode_combine", "mla_prefill_varlen", "mla_get_status",
-            "mla_status_string", "mla_version", "mla_set_profile_events", "mla_profile_elapsed_ms",
-            "mla_selftest_wait_timeout"]
+# Every function include/mla.h declares; each is given its C signature in _load().
+EXPORTED = ["mla_decode_plan", "mla_decode", "mla_decode_partial", "mla_decode_combine", "mla_decode_noalloc",
+            "mla_prefill_varlen", "mla_get_status", "mla_status_string", "mla_version", "mla_set_profile_events",
+            "mla_profile_elapsed_ms", "mla_selftest_wait_timeout"]
 
 
 class MlaError(RuntimeError):
@@ -60,6 +61,8 @@ def _load() -> ctypes.CDLL:
     lib.mla_decode_partial.restype = i32
     lib.mla_decode_partial.argtypes = [ctypes.POINTER(DecodePlan), P, P, P, P, i32, i32, f32, f32, P, P, P, sz, P]
     lib.mla_decode_combine.restype = i32
+    lib.mla_decode_noalloc.restype = i32
+    lib.mla_decode_noalloc.argtypes = [ctypes.POINTER(DecodePlan), P, P, P, P, i32, i32, f32, f32, P, P, P]
     lib.mla_decode_combine.argtypes = [ctypes.POINTER(DecodePlan), P, i32, i32, P, P, P, sz, P]
     lib.mla_prefill_varlen.restype = i32
     lib.mla_prefill_varlen.argtypes = [P, P, P, P, P, P, i32, i32, i32, i32, i32, f32, P, P, P]
@@ -166,6 +169,22 @@ def decode_combine(plan: DecodePlan, seq_lens: torch.Tensor, out: torch.Tensor, 
     rc = lib.mla_decode_combine(ctypes.byref(plan), _ptr(seq_lens), int(T), int(H), _ptr(out), _ptr(lse),
                                 _ptr(workspace), int(ws_bytes), _stream_handle(stream))
     _check(rc, "mla_decode_combine")
+    return out, lse
+
+
+def decode_noalloc(plan: DecodePlan, q: torch.Tensor, kv_pages: torch.Tensor, page_table: torch.Tensor,
+                   seq_lens: torch.Tensor, scale: float, kv_scale: float = 1.0, out=None, lse=None, stream=None):
+    """mla_decode_noalloc through the C ABI: decode with the split-KV scratch in the
+    library's fixed 32 MiB device buffer instead of a workspace.  Returns (out, lse)."""
+    B, T, H, D = q.shape
+    if out is None:
+        out = torch.empty(B, T, H, 512, dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.empty(B, T, H, dtype=torch.float32, device=q.device)
+    rc = lib.mla_decode_noalloc(ctypes.byref(plan), _ptr(q), _ptr(kv_pages), _ptr(page_table), _ptr(seq_lens),
+                                int(T), int(H), float(scale), float(kv_scale), _ptr(out), _ptr(lse),
+                                _stream_handle(stream))
+    _check(rc, "mla_decode_noalloc")
     return out, lse
 
 

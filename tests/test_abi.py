@@ -46,6 +46,16 @@ def test_library_exports_every_declared_symbol(mla):
         assert hasattr(lib, name), f"libmla.so does not export {name}"
 
 
+def test_binding_covers_the_header(mla):
+    """The Python binding lists exactly the functions the header declares, and gives each
+    its C signature."""
+    assert sorted(mla.EXPORTED) == _declared_functions()
+    for name in mla.EXPORTED:
+        fn = getattr(mla.lib, name)
+        if name != "mla_version":  # the one function without arguments
+            assert fn.argtypes, f"{name} has no argument types set"
+
+
 def test_plan_struct_layout(mla):
     assert ctypes.sizeof(mla.DecodePlan) == 64
 

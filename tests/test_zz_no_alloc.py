@@ -67,6 +67,11 @@ def test_noalloc_matches_workspace_decode_on_two_calls_in_a_row(mla):
         assert np.abs(a - r).max() <= MAX_ABS
         assert np.linalg.norm(a - r) / np.linalg.norm(r) <= REL_L2
         assert np.abs(lse.cpu().numpy() - ref_lse.cpu().numpy()).max() <= LSE_ABS
+        # the binding's wrapper makes the same call
+        out2, lse2 = mla.decode_noalloc(plan, inp.q, inp.kv_pool, inp.page_table, inp.seq_lens, inp.scale)
+        torch.cuda.synchronize()
+        assert torch.equal(out2.view(torch.int16), out.view(torch.int16))
+        assert torch.equal(lse2.view(torch.int32), lse.view(torch.int32))
 
 
 def test_noalloc_rejects_plans_beyond_its_buffer(mla):

@@ -66,7 +66,11 @@ def decode_bytes(wl):
 
 
 def decode_flops(wl):
-    return 2 * sum(wl.q_len * wl.heads * L * (576 + 512) for L in wl.seq_lens)
+    """2 * H * (576 + 512) * sum over query tokens of the keys each one sees (token t of a
+    request of L keys sees keys 0 .. L - T + t)."""
+    T = wl.q_len
+    keys = sum(T * (L - T) + T * (T + 1) // 2 for L in wl.seq_lens)
+    return 2 * wl.heads * (576 + 512) * keys
 
 
 def prefill_flops(wl):

@@ -96,7 +96,10 @@ std::mutex g_plan_mu;
 std::unordered_map<std::string, mla_decode_plan_t> g_plan_cache;
 
 // Smallest keys-per-split chunk (whole 64-key tiles, at least 4 tiles when the request is
-// that long) for which the partial kernel needs no more CTAs than the GPU has SMs.
+// that long) for which the partial kernel needs no more CTAs than the GPU has SMs.  When one
+// split per request already needs more CTAs than that (many row groups), the chunk is the
+// whole request unless 2-4 splits lower the estimated makespan, waves x (tiles per CTA + 3
+// tiles of fixed cost per CTA), as they do when the last wave would run mostly empty.
 int choose_chunk_tiles(const std::vector<int>& lens, int groups, int sms) {
   int max_tiles = 1;
   for (int L : lens) max_tiles = std::max(max_tiles, (L + kTileKeys - 1) / kTileKeys);
@@ -106,7 +109,16 @@ int choose_chunk_tiles(const std::vector<int>& lens, int groups, int sms) {
     return n * groups;
   };
   int lo = std::min(4, max_tiles), hi = max_tiles;
-  if (ctas(hi) > sms) return hi;  // one split per request already exceeds one wave
+  if (ctas(hi) > sms) {
+    auto cost = [&](int ct) { return ((ctas(ct) + sms - 1) / sms) * static_cast<long long>(ct + 3); };
+    int best = hi;
+    for (int k = 2; k <= 4; ++k) {
+      const int ct = (max_tiles + k - 1) / k;
+      if (ct < 4) break;
+      if (cost(ct) < cost(best)) best = ct;
+    }
+    return best;
+  }
   while (lo < hi) {
     int mid = (lo + hi) / 2;
     if (ctas(mid) <= sms)

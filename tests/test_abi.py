@@ -98,8 +98,10 @@ def test_plan_head_groups_for_many_heads(mla):
 def test_plan_invariants_on_random_batches(mla):
     """Seeded random batches (ragged lengths, 1-8 drafts or a long absorbed prefill, 16 or
     128 heads, several SM counts): the split chunk is whole 64-key tiles and at least four
-    of them (or the whole of the longest request), one wave of CTAs whenever a request is
-    split, the smallest chunk with that property, and a workspace that fits every split."""
+    of them (or the whole of the longest request); while one split per request fits in one
+    wave of CTAs, one wave whenever a request is split and the smallest chunk with that
+    property; beyond one wave, the whole request or 2-4 splits, whichever has the lowest
+    waves x (tiles per CTA + 3); and a workspace that fits every split."""
     rng = np.random.default_rng(12)
     for _ in range(60):
         B = int(rng.integers(1, 40))
@@ -117,12 +119,18 @@ def test_plan_invariants_on_random_batches(mla):
         assert plan.chunk_tokens % 64 == 0 and ct >= min(4, max(tiles))
         groups = (T * H + 63) // 64
         assert plan.head_groups == groups
-        ctas = groups * sum((t + ct - 1) // ct for t in tiles)
+        n_ctas = lambda c: groups * sum((t + c - 1) // c for t in tiles)
+        ctas = n_ctas(ct)
         assert plan.max_splits == (max(lens) + plan.chunk_tokens - 1) // plan.chunk_tokens
-        if plan.max_splits > 1:
+        if n_ctas(max(tiles)) > sms:  # more than one wave even unsplit
+            cost = lambda c: -(-n_ctas(c) // sms) * (c + 3)
+            cands = [max(tiles)] + [c for c in (-(-max(tiles) // k) for k in (2, 3, 4)) if c >= 4]
+            assert ct in cands and cost(ct) == min(cost(c) for c in cands)
+        elif plan.max_splits > 1:
             assert ctas <= sms
             if ct > min(4, max(tiles)):
                 assert groups * sum((t + ct - 2) // (ct - 1) for t in tiles) > sms
+        if plan.max_splits > 1:
             parts = B * plan.max_splits * T * H
             assert plan.workspace_bytes == 256 + parts * 512 * 2 + parts * 4
         else:

@@ -95,6 +95,17 @@ def test_plan_head_groups_for_many_heads(mla):
     assert plan.rows == 256 and plan.head_groups == 4
 
 
+def test_plan_splits_a_multi_wave_absorbed_prefill(mla):
+    """4 requests x 512 new tokens x 16 heads on 32K keys: 128 row groups per request, 512
+    CTAs unsplit (3.4 waves of 152).  Two splits of 256 tiles give 7 waves x 259 = 1813
+    tile-times against 4 x 515 = 2060 unsplit (three: 11 x 174; four: 14 x 131)."""
+    plan = mla.decode_plan([32768] * 4, q_len=512, num_heads=16, page_size=64, max_pages_per_seq=512,
+                           num_pages=2048, num_sms=152)
+    assert plan.head_groups == 128
+    assert plan.chunk_tokens == 256 * 64 and plan.max_splits == 2
+    assert plan.workspace_bytes == 256 + 4 * 2 * 512 * 16 * (512 * 2 + 4)
+
+
 def test_plan_invariants_on_random_batches(mla):
     """Seeded random batches (ragged lengths, 1-8 drafts or a long absorbed prefill, 16 or
     128 heads, several SM counts): the split chunk is whole 64-key tiles and at least four

@@ -76,6 +76,8 @@ CASES = [
     (1, 4, 4, [70], 64, "e4m3"),
     (2, 3, 2, [33, 9], 4, "int8"),
     (1, 4, 4, [70], 64, "int8"),
+    (2, 2, 2, [300, 129], 128, "bf16"),   # pages larger than one tile, a request ending inside one
+    (1, 1, 2, [600], 256, "e4m3"),
 ]
 
 

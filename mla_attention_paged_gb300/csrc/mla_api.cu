@@ -9,7 +9,9 @@
 #include <algorithm>
 #include <cstdio>
 #include <cstring>
+#include <functional>
 #include <mutex>
+#include <queue>
 #include <string>
 #include <unordered_map>
 #include <vector>
@@ -95,38 +97,94 @@ cudaError_t record_event(cudaEvent_t ev, cudaStream_t s) {
 std::mutex g_plan_mu;
 std::unordered_map<std::string, mla_decode_plan_t> g_plan_cache;
 
-// Smallest keys-per-split chunk (whole 64-key tiles, at least 4 tiles when the request is
-// that long) for which the partial kernel needs no more CTAs than the GPU has SMs.  When one
-// split per request already needs more CTAs than that (many row groups), the chunk is the
-// whole request unless 2-4 splits lower the estimated makespan, waves x (tiles per CTA + 3
-// tiles of fixed cost per CTA), as they do when the last wave would run mostly empty.
+// Cost model of the planner, in units of one 64-key tile of one CTA: a CTA costs its tiles
+// plus kCtaFixedTiles (start-up until its first tile has landed, and the epilogue), and a
+// plan with more than one split pays kCombineTiles for the combine kernel.
+constexpr long long kCtaFixedTiles = 3;
+constexpr long long kCombineTiles = 2;
+
+// Estimated duration of a decode call whose splits are ct tiles long: the partial kernel's
+// CTAs (group fastest, then split, then request: the grid's launch order) are dispatched in
+// that order, each onto the SM that frees first; CTAs of splits a request does not have exit
+// at once and cost nothing.  Plus the combine, when some request is split.
+long long plan_cost(const std::vector<int>& tiles, int groups, int ct, int sms) {
+  int max_splits = 1;
+  long long n_ctas = 0, longest = 0;
+  for (int t : tiles) {
+    const int ns = (t + ct - 1) / ct;
+    max_splits = std::max(max_splits, ns);
+    n_ctas += static_cast<long long>(ns) * groups;
+    longest = std::max<long long>(longest, std::min(t, ct));
+  }
+  long long span;
+  if (n_ctas <= sms) {
+    span = longest + kCtaFixedTiles;  // one wave: the longest CTA
+  } else {
+    std::priority_queue<long long, std::vector<long long>, std::greater<long long>> free_at;
+    for (int i = 0; i < sms; ++i) free_at.push(0);
+    span = 0;
+    for (int t : tiles) {
+      const int ns = (t + ct - 1) / ct;
+      for (int s = 0; s < ns; ++s) {
+        const long long cost = std::min(ct, t - s * ct) + kCtaFixedTiles;
+        for (int g = 0; g < groups; ++g) {
+          const long long start = free_at.top();
+          free_at.pop();
+          free_at.push(start + cost);
+          span = std::max(span, start + cost);
+        }
+      }
+    }
+  }
+  return span + (max_splits > 1 ? kCombineTiles : 0);
+}
+
+// Keys-per-split chunk in whole 64-key tiles (at least 4 tiles, or the whole of the
+// longest request when it is shorter).  Candidates: the smallest chunk for which the
+// partial kernel needs no more CTAs than the GPU has SMs (one wave; when the unsplit call
+// already fits), and the longest request cut into 1-4 splits.  The candidate with the
+// lowest plan_cost wins, the one with fewer splits on a tie, so a split is only taken when
+// the model says it shortens the call.
 int choose_chunk_tiles(const std::vector<int>& lens, int groups, int sms) {
+  std::vector<int> tiles;
+  tiles.reserve(lens.size());
   int max_tiles = 1;
-  for (int L : lens) max_tiles = std::max(max_tiles, (L + kTileKeys - 1) / kTileKeys);
+  for (int L : lens) {
+    tiles.push_back((L + kTileKeys - 1) / kTileKeys);
+    max_tiles = std::max(max_tiles, tiles.back());
+  }
   auto ctas = [&](int ct) {
     long long n = 0;
-    for (int L : lens) n += ((L + kTileKeys - 1) / kTileKeys + ct - 1) / ct;
+    for (int t : tiles) n += (t + ct - 1) / ct;
     return n * groups;
   };
-  int lo = std::min(4, max_tiles), hi = max_tiles;
-  if (ctas(hi) > sms) {
-    auto cost = [&](int ct) { return ((ctas(ct) + sms - 1) / sms) * static_cast<long long>(ct + 3); };
-    int best = hi;
-    for (int k = 2; k <= 4; ++k) {
-      const int ct = (max_tiles + k - 1) / k;
-      if (ct < 4) break;
-      if (cost(ct) < cost(best)) best = ct;
+  const int lo = std::min(4, max_tiles);
+  std::vector<int> cands;
+  for (int k = 1; k <= 4; ++k) {
+    const int ct = (max_tiles + k - 1) / k;
+    if (ct >= lo) cands.push_back(ct);
+  }
+  if (ctas(max_tiles) <= sms) {
+    int a = lo, b = max_tiles;
+    while (a < b) {
+      const int mid = (a + b) / 2;
+      if (ctas(mid) <= sms)
+        b = mid;
+      else
+        a = mid + 1;
     }
-    return best;
+    cands.push_back(a);
   }
-  while (lo < hi) {
-    int mid = (lo + hi) / 2;
-    if (ctas(mid) <= sms)
-      hi = mid;
-    else
-      lo = mid + 1;
+  int best = max_tiles;
+  long long best_cost = plan_cost(tiles, groups, max_tiles, sms);
+  for (int ct : cands) {
+    const long long c = plan_cost(tiles, groups, ct, sms);
+    if (c < best_cost || (c == best_cost && ct > best)) {
+      best = ct;
+      best_cost = c;
+    }
   }
-  return lo;
+  return best;
 }
 
 }  // namespace
@@ -289,6 +347,7 @@ int decode_stages(const mla_decode_plan_t* plan, const void* q, const void* kv_p
   p.max_splits = plan->max_splits;
   p.max_seq = plan->max_seq_len;
   p.kv_dtype = plan->kv_dtype;
+  p.num_pages = plan->num_pages;
   const bool kv8 = plan->kv_dtype != MLA_KV_BF16;
   p.scale_log2 = scale * 1.4426950408889634f * (kv8 ? kv_scale : 1.f);
   p.v_scale = kv8 ? kv_scale : 1.f;
@@ -388,7 +447,9 @@ int mla_prefill_varlen(const void* q, const void* k, const void* v, const int32_
   p.prefix_lens = prefix_lens;
   p.out = static_cast<__nv_bfloat16*>(out);
   p.lse = lse;
+  p.max_seqlen_q = max_seqlen_q;
   p.total_q = total_q;
+  p.total_kv = total_kv;
   p.status = status;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (g_prof_start && record_event(g_prof_start, s) != cudaSuccess) return MLA_ERR_CUDA;

@@ -95,24 +95,70 @@ def test_plan_head_groups_for_many_heads(mla):
     assert plan.rows == 256 and plan.head_groups == 4
 
 
+def _plan_cost(tiles, groups, ct, sms):
+    """The planner's cost model, restated: CTAs (group fastest, then split, then request)
+    dispatched in that order onto the SM that frees first, each costing its tiles + 3; a
+    plan with more than one split adds 2 for the combine."""
+    import heapq
+    splits = [-(-t // ct) for t in tiles]
+    n_ctas = groups * sum(splits)
+    if n_ctas <= sms:
+        span = max(min(t, ct) for t in tiles) + 3
+    else:
+        free = [0] * sms
+        span = 0
+        for t, ns in zip(tiles, splits):
+            for s in range(ns):
+                cost = min(ct, t - s * ct) + 3
+                for _ in range(groups):
+                    start = heapq.heappop(free)
+                    heapq.heappush(free, start + cost)
+                    span = max(span, start + cost)
+    return span + (2 if max(splits) > 1 else 0)
+
+
 def test_plan_splits_a_multi_wave_absorbed_prefill(mla):
     """4 requests x 512 new tokens x 16 heads on 32K keys: 128 row groups per request, 512
-    CTAs unsplit (3.4 waves of 152).  Two splits of 256 tiles give 7 waves x 259 = 1813
-    tile-times against 4 x 515 = 2060 unsplit (three: 11 x 174; four: 14 x 131)."""
+    CTAs unsplit (3.4 waves of 152 SMs: 4 x 515 = 2060 tile-times).  Two splits of 256
+    tiles: 1024 CTAs in 6.7 waves, 7 x 259 + 2 = 1815 (three: 1536 CTAs of ~174, four:
+    2048 CTAs of 131, 14 x 131 + 2 = 1836)."""
     plan = mla.decode_plan([32768] * 4, q_len=512, num_heads=16, page_size=64, max_pages_per_seq=512,
                            num_pages=2048, num_sms=152)
     assert plan.head_groups == 128
     assert plan.chunk_tokens == 256 * 64 and plan.max_splits == 2
     assert plan.workspace_bytes == 256 + 4 * 2 * 512 * 16 * (512 * 2 + 4)
+    assert _plan_cost([512] * 4, 128, 256, 152) == 1815 and _plan_cost([512] * 4, 128, 512, 152) == 2060
+
+
+def test_plan_one_sm_never_splits(mla):
+    """On one SM every CTA runs after the previous one, so a split only adds per-CTA fixed
+    cost and a combine: the plan keeps one split per request, whatever the lengths.  (The
+    ragged batch [5000, 130, 2999]: 79 + 3 + 47 tiles; three-way splits of 27 tiles would
+    cost 147 + 2 tile-times against 138.)"""
+    plan = mla.decode_plan([5000, 130, 2999], q_len=4, num_heads=16, page_size=64, max_pages_per_seq=79,
+                           num_pages=300, num_sms=1)
+    assert plan.max_splits == 1 and plan.workspace_bytes == 0
+    assert _plan_cost([79, 3, 47], 1, 79, 1) == 138 < _plan_cost([79, 3, 47], 1, 27, 1) == 149
+    rng = np.random.default_rng(7)
+    for _ in range(30):
+        B = int(rng.integers(1, 12))
+        T = int(rng.choice([1, 2, 4, 8, 64]))
+        H = int(rng.choice([16, 128]))
+        lens = [int(x) for x in rng.integers(T, 300000, B)]
+        mp = (max(lens) + 63) // 64
+        plan = mla.decode_plan(lens, q_len=T, num_heads=H, page_size=64, max_pages_per_seq=mp,
+                               num_pages=B * mp, num_sms=1)
+        assert plan.max_splits == 1 and plan.chunk_tokens == mp * 64
 
 
 def test_plan_invariants_on_random_batches(mla):
     """Seeded random batches (ragged lengths, 1-8 drafts or a long absorbed prefill, 16 or
     128 heads, several SM counts): the split chunk is whole 64-key tiles and at least four
-    of them (or the whole of the longest request); while one split per request fits in one
-    wave of CTAs, one wave whenever a request is split and the smallest chunk with that
-    property; beyond one wave, the whole request or 2-4 splits, whichever has the lowest
-    waves x (tiles per CTA + 3); and a workspace that fits every split."""
+    of them (or the whole of the longest request); the plan's estimated duration is the
+    lowest over its candidates (1-4 splits of the longest request, and the smallest chunk
+    that keeps the call in one wave when the unsplit call fits one), so it is never longer
+    than the unsplit call's; a split that fits one wave is the smallest such chunk; and the
+    workspace fits every split."""
     rng = np.random.default_rng(12)
     for _ in range(60):
         B = int(rng.integers(1, 40))
@@ -120,27 +166,30 @@ def test_plan_invariants_on_random_batches(mla):
         H = int(rng.choice([16, 128]))
         if T * H > 131072:
             continue
-        sms = int(rng.choice([16, 100, 152]))
+        sms = int(rng.choice([1, 3, 16, 100, 152]))
         lens = [int(x) for x in rng.integers(T, 200000, B)]
         mp = (max(lens) + 63) // 64
         plan = mla.decode_plan(lens, q_len=T, num_heads=H, page_size=64, max_pages_per_seq=mp,
                                num_pages=B * mp, num_sms=sms)
         tiles = [(L + 63) // 64 for L in lens]
+        mt = max(tiles)
         ct = plan.chunk_tokens // 64
-        assert plan.chunk_tokens % 64 == 0 and ct >= min(4, max(tiles))
+        assert plan.chunk_tokens % 64 == 0 and ct >= min(4, mt)
         groups = (T * H + 63) // 64
         assert plan.head_groups == groups
         n_ctas = lambda c: groups * sum((t + c - 1) // c for t in tiles)
-        ctas = n_ctas(ct)
         assert plan.max_splits == (max(lens) + plan.chunk_tokens - 1) // plan.chunk_tokens
-        if n_ctas(max(tiles)) > sms:  # more than one wave even unsplit
-            cost = lambda c: -(-n_ctas(c) // sms) * (c + 3)
-            cands = [max(tiles)] + [c for c in (-(-max(tiles) // k) for k in (2, 3, 4)) if c >= 4]
-            assert ct in cands and cost(ct) == min(cost(c) for c in cands)
-        elif plan.max_splits > 1:
-            assert ctas <= sms
-            if ct > min(4, max(tiles)):
-                assert groups * sum((t + ct - 2) // (ct - 1) for t in tiles) > sms
+        cands = [c for c in (-(-mt // k) for k in (1, 2, 3, 4)) if c >= min(4, mt)]
+        one_wave = None
+        if n_ctas(mt) <= sms:
+            one_wave = min(c for c in range(min(4, mt), mt + 1) if n_ctas(c) <= sms)
+            cands.append(one_wave)
+        cost = lambda c: _plan_cost(tiles, groups, c, sms)
+        assert ct in cands + [mt]
+        assert cost(ct) == min(cost(c) for c in cands)
+        assert cost(ct) <= cost(mt)
+        if plan.max_splits > 1 and n_ctas(ct) <= sms and one_wave is not None:
+            assert ct == one_wave
         if plan.max_splits > 1:
             parts = B * plan.max_splits * T * H
             assert plan.workspace_bytes == 256 + parts * 512 * 2 + parts * 4

@@ -86,9 +86,15 @@ typedef struct mla_decode_plan_t {
   size_t workspace_bytes;    /* bytes mla_decode needs in `workspace` (0 = none)         */
 } mla_decode_plan_t;
 
-/* Plan one decode launch: pick the keys-per-split chunk so that the partial kernel
- * fills the GPU's SMs in one wave (one CTA per SM per (request, split, 64-row group)),
- * and size the workspace for the split partials.  Plans are memoised on all arguments
+/* Plan one decode launch: pick the keys-per-split chunk (whole 64-key tiles) and size the
+ * workspace for the split partials.  The partial kernel runs one CTA per (request, split,
+ * 64-row group); the plan estimates the call's duration by dispatching those CTAs in launch
+ * order onto the SM that frees first (each costing its tiles plus a fixed start-up and
+ * epilogue cost, plus the combine when a request is split), over these chunks: the
+ * longest request in 1-4 splits, and the smallest chunk that keeps the call in one wave of
+ * CTAs when the unsplit call fits one.  The chunk with the shortest estimate wins (fewer
+ * splits on a tie), so a split is never taken when it lengthens the call by that estimate.
+ * Plans are memoised on all arguments
  * (the split count and workspace are "computed automatically at run time and cached",
  * [TALK] Kernel section).
  *   seq_lens_host : HOST int32[batch], tokens cached per request INCLUDING the q_len
@@ -126,7 +132,11 @@ int mla_decode_plan(int batch, const int32_t* seq_lens_host, int q_len, int num_
  * cudaGridDependencySynchronize) before it reads out or lse.
  * Errors: MLA_ERR_INVALID_ARG (null pointers, q_len/num_heads differ from the plan,
  * misaligned pointers: q, kv_pages 16-byte, out 16-byte), MLA_ERR_WORKSPACE_TOO_SMALL,
- * MLA_ERR_CUDA (tensor-map encoding or launch failure). */
+ * MLA_ERR_CUDA (tensor-map encoding or launch failure).  Device-side, recorded in the
+ * status word as MLA_ERR_DEVICE_ARG (read by mla_get_status): a length below q_len or
+ * beyond the plan (that request is skipped, its out/lse rows left unwritten), and a page
+ * id outside [0, num_pages) (the rows it names are read as zeros, never from outside the
+ * pool). */
 int mla_decode(const mla_decode_plan_t* plan, const void* q, const void* kv_pages,
                const int32_t* page_table, const int32_t* seq_lens, int q_len, int num_heads,
                float scale, float kv_scale, void* out, float* lse, void* workspace,
@@ -194,7 +204,10 @@ int mla_decode_noalloc(const mla_decode_plan_t* plan, const void* q, const void*
  *                   0 .. p_b + i of its own request.
  *   lse           : [total_q, H] fp32 natural-log log-sum-exp.
  * Errors: MLA_ERR_INVALID_ARG, MLA_ERR_UNSUPPORTED (num_heads < 1 or > 256),
- * MLA_ERR_CUDA. */
+ * MLA_ERR_CUDA.  Device-side, recorded in the status word as MLA_ERR_DEVICE_ARG (read by
+ * mla_get_status) before any load or store of the request: its kv length differs from
+ * p_b + n_b, n_b > max_seqlen_q, or its rows reach beyond total_q / total_kv.  That
+ * request is skipped and its out/lse rows are left unwritten. */
 int mla_prefill_varlen(const void* q, const void* k, const void* v, const int32_t* cu_seqlens_q,
                        const int32_t* cu_seqlens_kv, const int32_t* prefix_lens, int batch,
                        int num_heads, int max_seqlen_q, int total_q, int total_kv, float scale,

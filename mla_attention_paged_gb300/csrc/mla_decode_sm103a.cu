@@ -301,6 +301,17 @@ decode_partial_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
           pids[pp] = 0;
         }
       }
+      // A page id outside the pool is reported and replaced by -1: its box then lies
+      // wholly before the first row, and TMA fills it with zeros instead of reading.
+      bool bad_pid = false;
+#pragma unroll
+      for (int pp = 0; pp < 8; ++pp) {
+        if (pp < npg && (pids[pp] < 0 || static_cast<int64_t>(pids[pp]) >= p.num_pages)) {
+          bad_pid = true;
+          pids[pp] = -1;
+        }
+      }
+      if (bad_pid && lane == 0) atomicOr(p.status, kStatusDeviceArg);
       // The page ids above are resolved before waiting for the stage, so that only the
       // copies are left once it frees up (resolving them after the wait was measured to
       // delay each tile's copies by ~1.5k cycles).
@@ -361,7 +372,7 @@ decode_partial_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
       return (lane < sub && jt < ntiles && k < kv_end) ? k / P : -1;
     };
     auto prefetch = [&](int jt, int pid) {
-      if (pid < 0) return;
+      if (pid < 0 || static_cast<int64_t>(pid) >= p.num_pages) return;  // (a bad id is reported by the decode warps)
       const int k = kv_start + jt * kTileKeys + lane * P;
       const int rows = min(min(P, kTileKeys), kv_end - k);
       prefetch_l2_bulk(p.kv_pool + (static_cast<int64_t>(pid) * P + k % P) * kLatentDim,
@@ -487,12 +498,21 @@ decode_partial_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
     }
     const int P = p.page_size;
     const int32_t* pt = p.page_table + static_cast<int64_t>(b) * p.max_pages;
-    // page id of each owned row of tile j (0 past the request end: the row is not read)
+    // page id of each owned row of tile j (-1 past the request end, or for an id outside
+    // the pool, which is reported: the row is not read and counts as zeros)
     auto row_pids = [&](int j, int (&pid)[8]) {
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         const int k = kv_start + j * kTileKeys + (dl >> 2) + 8 * i;
-        pid[i] = (k < L) ? __ldg(pt + k / P) : 0;
+        int v = -1;
+        if (k < L) {
+          v = __ldg(pt + k / P);
+          if (v < 0 || static_cast<int64_t>(v) >= p.num_pages) {
+            atomicOr(p.status, kStatusDeviceArg);
+            v = -1;
+          }
+        }
+        pid[i] = v;
       }
     };
     int pid_cur[8];
@@ -504,8 +524,9 @@ decode_partial_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         const int k = k0 + (dl >> 2) + 8 * i;
-        const uint8_t* row = p.kv_pool + (static_cast<int64_t>(pid_cur[i]) * P + k % P) * kLatentDim + (dl & 3) * 16;
-        const bool valid = k < L;
+        const bool valid = pid_cur[i] >= 0;
+        const uint8_t* row =
+            p.kv_pool + (static_cast<int64_t>(valid ? pid_cur[i] : 0) * P + k % P) * kLatentDim + (dl & 3) * 16;
 #pragma unroll
         for (int m = 0; m < 3; ++m)
           w[m][i] = valid ? __ldg(reinterpret_cast<const uint4*>(row + (dw + 3 * m) * 64)) : make_uint4(0u, 0u, 0u, 0u);
@@ -741,10 +762,6 @@ __global__ void __launch_bounds__(kCombineThreads) decode_combine_kernel(const D
   const int b = blockIdx.y;
   const int tid = threadIdx.x;
   const int lane = tid & 31;
-  const int L = p.seq_lens[b];
-  if (L < p.T || L > p.max_seq) return;
-  const int ns = (L + p.chunk - 1) / p.chunk;
-  if (ns <= 1) return;
   const int nr = min(kCombineRows, p.R - row0);
   const int r = tid / 64;   // row of this thread within the CTA
   const int c8 = tid % 64;  // value columns 8*c8 .. 8*c8+7
@@ -755,8 +772,14 @@ __global__ void __launch_bounds__(kCombineThreads) decode_combine_kernel(const D
     fence_mbarrier_init();
   }
   __syncthreads();
-  // launched as a programmatic dependent of the partial kernel: wait for its results
+  // Launched as a programmatic dependent of the stream's previous kernel (the partial
+  // kernel inside mla_decode): wait for it to complete before reading any input, the
+  // lengths included, since a caller's own kernel between the two stages may write them.
   asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int L = p.seq_lens[b];
+  if (L < p.T || L > p.max_seq) return;  // (CTA-uniform; the partial kernel reported it)
+  const int ns = (L + p.chunk - 1) / p.chunk;
+  if (ns <= 1) return;
   const int64_t base = static_cast<int64_t>(b) * p.max_splits;
   const float* lse_s = p.ws_lse + base * p.R + row0 + (active ? r : 0);
   float m_run = -INFINITY, w_run = 0.f;

@@ -28,6 +28,7 @@ struct DecodeParams {
   int page_size, max_pages;     // page geometry and page_table row stride
   int chunk, max_splits, max_seq;
   int kv_dtype;                 // kKvBf16, kKvE4m3 or kKvInt8
+  int64_t num_pages;            // pages in the pool: a page id outside [0, num_pages) is reported
   float scale_log2;             // softmax scale * log2(e) (* kv_scale for an 8-bit pool)
   float v_scale;                // 1, or kv_scale for an 8-bit pool (applied in the epilogue)
   const int32_t* page_table;
@@ -42,13 +43,14 @@ struct DecodeParams {
 
 struct PrefillParams {
   int B, H, max_q_blocks;
+  int max_seqlen_q;             // host bound on new tokens per request (sizes the grid)
   float scale_log2;
   const int32_t* cu_q;
   const int32_t* cu_kv;
   const int32_t* prefix_lens;
   __nv_bfloat16* out;           // [total_q, H, 128]
   float* lse;                   // [total_q, H]
-  int total_q;
+  int total_q, total_kv;        // rows of q/out/lse and of k/v
   unsigned* status;
 };
 

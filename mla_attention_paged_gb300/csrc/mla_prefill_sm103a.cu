@@ -153,7 +153,13 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
   const int kv_start = p.cu_kv[b];
   const int kv_total = p.cu_kv[b + 1] - kv_start;
   const int pre = p.prefix_lens[b];
-  if (n_b < 0 || pre < 0 || kv_total != pre + n_b) {
+  // Device-side argument checks, before any load or store: the request's rows lie inside
+  // q/out/lse and k/v, its kv length is prefix + new tokens, and its new tokens fit the
+  // grid the host sized from max_seqlen_q (rows beyond it would be left unwritten).
+  const bool bad = n_b < 0 || pre < 0 || kv_total != pre + n_b || n_b > p.max_seqlen_q || q_start < 0 ||
+                   kv_start < 0 || static_cast<int64_t>(q_start) + n_b > p.total_q ||
+                   static_cast<int64_t>(kv_start) + kv_total > p.total_kv;
+  if (bad) {
     if (threadIdx.x == 0 && qb == 0 && h == 0) atomicOr(p.status, kStatusDeviceArg);
     return;
   }

@@ -1,8 +1,8 @@
 """GPU parity of mla_decode (through the C ABI) against the fp64 CPU oracle.
 
 Tolerances (bf16 output): max-abs 2e-2 and relative L2 5e-3 over the compared outputs,
-LSE within 1e-3 absolute; 8-bit KV (e4m3 or int8): max-abs 6e-2 against the oracle run on
-the same codes and scale.  Small cases are compared element by element over every output; the
+LSE within 1e-3 absolute; 8-bit KV (e4m3 or int8): the same relative-L2 and LSE bounds,
+with max-abs 6e-2, against the oracle run on the same codes and scale.  Small cases are compared element by element over every output; the
 full-size workloads are compared on sampled rows the oracle computes one by one, in the
 same launch configuration the benchmark times.
 """
@@ -54,10 +54,7 @@ def check(out, lse, ref_out, ref_lse, fp8=False):
     err = np.abs(out - ref_out)
     assert err.max() <= (MAX_ABS_FP8 if fp8 else MAX_ABS), f"max-abs {err.max():.3e}"
     rel = np.linalg.norm(out - ref_out) / max(np.linalg.norm(ref_out), 1e-30)
-    if not fp8:
-        assert rel <= REL_L2, f"rel-L2 {rel:.3e}"
-    else:
-        assert rel <= 2 * REL_L2, f"rel-L2 {rel:.3e}"
+    assert rel <= REL_L2, f"rel-L2 {rel:.3e}"
     lerr = np.abs(lse - ref_lse).max()
     assert lerr <= LSE_ABS, f"lse abs {lerr:.3e}"
 
@@ -211,19 +208,25 @@ def test_decode_page_shuffle_invariance_bitwise(mla):
 
 def test_decode_fold_neutrality(mla):
     """T drafts folded into one launch equal T single-token launches whose cache ends at
-    each draft's own position."""
-    wl = DecodeWorkload("fold", 2, 4, 16, [700, 1300], seed=9)
+    each draft's own position.  Peaked inputs (a few keys dominate each row, outputs of
+    the size of a value row) so that a row mixed up between the folded and the separate
+    launches shows far above the relative-L2 bound."""
+    wl = DecodeWorkload("fold", 2, 4, 16, [700, 1300], seed=9, peaked=True)
     inp = make_decode_inputs(wl, "cpu")
     out, lse, _ = run_gpu(mla, inp)
     out = out.reshape(2, 4, 16, 512)
+    lse = lse.reshape(2, 4, 16)
+    assert np.linalg.norm(out) > 1.0  # outputs are dominated by planted rows, not ~1e-4 means
     for t in range(4):
         w1 = DecodeWorkload("fold1", 2, 1, 16, [700 - 3 + t, 1300 - 3 + t], seed=9)
         one = make_decode_inputs(w1, "cpu")
         one.q = inp.q[:, t:t + 1].contiguous()
         one.kv_pool, one.page_table = inp.kv_pool, inp.page_table
         o1, l1, _ = run_gpu(mla, one)
-        err = np.abs(o1.reshape(2, 1, 16, 512)[:, 0] - out[:, t]).max()
-        assert err <= MAX_ABS / 4
+        a = o1.reshape(2, 16, 512)
+        b = out[:, t]
+        assert np.linalg.norm(a - b) / np.linalg.norm(b) <= REL_L2
+        assert np.abs(l1.reshape(2, 16) - lse[:, t]).max() <= LSE_ABS
 
 
 # ------------------------------------------------------------------------------------

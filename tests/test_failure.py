@@ -3,8 +3,11 @@
 * The bounded mbarrier wait every kernel uses gives up after its limit and records
   MLA_ERR_TIMEOUT in the status word (a self-test kernel waits on a barrier that nothing
   arrives on); the context stays usable afterwards.
-* A device-side argument check (a request longer than the plan allows) is caught by the
-  kernel before any access that depends on it and reported as MLA_ERR_DEVICE_ARG.
+* Device-side argument checks are caught by the kernels before any access that depends
+  on them and reported as MLA_ERR_DEVICE_ARG: a decode request longer than the plan
+  allows, a page id outside the pool (on the bf16 path, whose TMA reads zero-fill outside
+  the pool even without the check), and a prefill request with more new tokens than the
+  host's max_seqlen_q sized the grid for.
 """
 import time
 
@@ -56,4 +59,33 @@ def test_length_beyond_plan_is_reported(mla):
     mla.decode(plan, inp.q.cuda(), inp.kv_pool.cuda(), inp.page_table.cuda(), bad.cuda(), inp.scale)
     torch.cuda.synchronize()
     assert mla.get_status() == mla.MLA_ERR_DEVICE_ARG
+    assert mla.get_status() == mla.MLA_OK
+
+
+@pytest.mark.parametrize("bad_id", [-1, 10**6], ids=["negative", "past_pool"])
+def test_page_id_outside_pool_is_reported(mla, bad_id):
+    wl = DecodeWorkload("bad_page", 2, 2, 16, [700, 300], seed=6)
+    inp = make_decode_inputs(wl, "cpu")
+    plan = mla.decode_plan([700, 300], 2, 16, 64, inp.page_table.shape[1], inp.kv_pool.shape[0])
+    pt = inp.page_table.clone()
+    pt[0, 3] = bad_id
+    mla.decode(plan, inp.q.cuda(), inp.kv_pool.cuda(), pt.cuda(), inp.seq_lens.cuda(), inp.scale)
+    torch.cuda.synchronize()
+    assert mla.get_status() == mla.MLA_ERR_DEVICE_ARG
+    # the valid table runs clean afterwards
+    mla.decode(plan, inp.q.cuda(), inp.kv_pool.cuda(), inp.page_table.cuda(), inp.seq_lens.cuda(), inp.scale)
+    torch.cuda.synchronize()
+    assert mla.get_status() == mla.MLA_OK
+
+
+def test_prefill_request_beyond_max_seqlen_is_reported(mla):
+    """max_seqlen_q below a request's new-token count: the grid covers only its first
+    query block, so the kernel reports the request instead of leaving rows unwritten."""
+    from mla_attention_paged_gb300.inputs import PrefillWorkload, make_prefill_inputs
+    pi = make_prefill_inputs(PrefillWorkload("too_many_new", [100, 50], [300, 40], 2, seed=7), "cuda")
+    mla.prefill_varlen(pi.q, pi.k, pi.v, pi.cu_seqlens_q, pi.cu_seqlens_kv, pi.prefix_lens, 128, pi.scale)
+    torch.cuda.synchronize()
+    assert mla.get_status() == mla.MLA_ERR_DEVICE_ARG
+    mla.prefill_varlen(pi.q, pi.k, pi.v, pi.cu_seqlens_q, pi.cu_seqlens_kv, pi.prefix_lens, 300, pi.scale)
+    torch.cuda.synchronize()
     assert mla.get_status() == mla.MLA_OK

@@ -1,10 +1,10 @@
 """Benchmark of the MLA hot path on GB300 (one JSON line on rank 0).
 
-Workload: absorbed MLA speculative decode, batch 4, q_len 4, 16 heads, 32768 cached tokens
-per request, 64-token pages scattered in a shared pool, bf16 (synthetic, seeded).  One
-step = one mla_decode call (plan cached; split-KV partial kernel + LSE combine kernel).
-Inputs are rotated over several independent input sets whose KV totals more than twice
-the L2 size, so every step streams its KV from HBM.
+Headline workload: absorbed MLA speculative decode, batch 16, q_len 2, 16 heads, per-request
+cached lengths drawn uniformly from [8192, 131072] (seeded), 64-token pages shuffled in a
+shared pool, bf16 (synthetic, seeded): the largest decode configuration on one GPU, 1.28 GB
+of latent KV, which exceeds L2, so every step streams its KV from HBM.  One step = one
+mla_decode call (plan cached; split-KV partial kernel + LSE combine kernel).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
     python bench.py --profile-case <workload>     (three calls, for a profiler capture)
@@ -14,8 +14,8 @@ inside); the roofline's kernel time = one pair of CUDA events around a second gr
 back-to-back launches of the split-KV partial kernel alone (mla_decode_partial); `e2e` =
 wall clock of K end-to-end steps (one packed H2D copy of q / page table / lengths, the
 decode call, one packed D2H copy of out / lse, copies on their own streams) replayed from
-one graph.  The extra lines (prefill, batch-16 bf16 / e4m3 / int8 decode, ragged and
-128-head decode, absorbed prefill, a latency case) are graph-timed the same way.
+one graph.  The extra lines (the other decode workloads, the absorbed prefill over a paged
+prefix and the varlen prefill) are graph-timed the same way and printed last, compactly.
 
 N > 1 runs under torchrun: every rank runs an independent replica (the path has no
 exchange step); value = all ranks' KV bytes / max-over-ranks time.
@@ -39,7 +39,7 @@ sys.path.insert(0, ROOT)
 from mla_attention_paged_gb300.inputs import decode_workloads, make_decode_inputs  # noqa: E402
 
 METRIC = "MLA decode KV-read GB/s & µs/call vs 8 TB/s; varlen prefill TFLOP/s"
-WORKLOAD = "decode_b4_q4_h16_l32k"
+WORKLOAD = "decode_b16_q2_h16_ragged"
 L2_BYTES = 129 * 1024 * 1024
 
 
@@ -100,16 +100,38 @@ def graph_ms_per_call(fn, n, stream):
     return ms
 
 
-def measure_decode_extra(mla, name, dev, steps=200):
-    """Secondary decode measurement (device time per call, partial-kernel roofline)."""
+# Workloads whose decode sits above the tensor ridge (flops per KV byte): their fraction is
+# taken against the bf16 tensor peak, the others against HBM bandwidth.
+TENSOR_BOUND = ("decode_b16_q2_h128_ragged", "decode_b4_q512_h16_l32k")
+# The extra lines, in print order: the last ones are the configurations the targets are
+# quoted on (batch 16 / 64K prefix, and the varlen prefill), so they end the JSON line.
+EXTRA_DECODE = ["decode_b4_q4_h16_l32k", "decode_b1_q1_h16_l1024", "decode_b16_q2_h128_ragged",
+                "decode_b4_q512_h16_l32k", "decode_int8_b16_q4_h16_l64k", "decode_fp8_b8_q4_h16_l64k",
+                "decode_bf16_b16_q4_h16_l64k", "decode_fp8_b16_q4_h16_l64k"]
+
+
+def decode_sets(name, dev, rank=0):
+    """Input sets of one decode workload: enough independent sets that their KV exceeds 2.5x
+    L2 (rotated between calls so that every call reads its KV from HBM), or one set when the
+    workload alone is larger than that."""
     wl = decode_workloads()[name]
-    kv_bytes, alg_bytes = decode_bytes(wl)
-    n_sets = max(2, math.ceil(2.5 * L2_BYTES / kv_bytes) + 1) if kv_bytes < 2.5 * L2_BYTES else 1
+    kv_bytes, _ = decode_bytes(wl)
+    n_sets = 1 if kv_bytes >= 2.5 * L2_BYTES else max(2, math.ceil(2.5 * L2_BYTES / kv_bytes) + 1)
     sets = []
     for i in range(n_sets):
         w = decode_workloads()[name]
-        w.seed = replica_seed(wl.seed, i, 0)
+        w.seed = replica_seed(wl.seed, i, rank)
         sets.append(make_decode_inputs(w, dev))
+    return wl, sets
+
+
+def measure_decode_extra(mla, name, dev, steps=200):
+    """Secondary decode line: device time per call (graph of back-to-back calls) and the
+    partial kernel's own rate (graph of back-to-back partial launches), as a fraction of the
+    binding roofline."""
+    wl, sets = decode_sets(name, dev)
+    n_sets = len(sets)
+    kv_bytes, alg_bytes = decode_bytes(wl)
     kvd = {"e4m3": mla.MLA_KV_E4M3, "int8": mla.MLA_KV_INT8}.get(wl.kv_dtype, mla.MLA_KV_BF16)
     plan = mla.decode_plan(wl.seq_lens, wl.q_len, wl.heads, wl.page_size, sets[0].page_table.shape[1],
                            sets[0].kv_pool.shape[0], kvd)
@@ -137,14 +159,14 @@ def measure_decode_extra(mla, name, dev, steps=200):
     assert mla.get_status(st) == mla.MLA_OK
     peak = _peaks()
     del sets
-    return {"workload": name, "us_per_call": call_ms * 1e3, "kv_gbs": kv_bytes / (call_ms / 1e3) / 1e9,
-            "partial_us": part_ms * 1e3, "partial_gbs": alg_bytes / (part_ms / 1e3) / 1e9,
-            "hbm_frac": alg_bytes / (part_ms / 1e3) / 1e9 / peak["hbm_gbs"],
-            "tflops": decode_flops(wl) / (call_ms / 1e3) / 1e12,
-            "partial_tflops_frac": decode_flops(wl) / (part_ms / 1e3) / 1e12 / peak["bf16_tflops"],
-            "splits": plan.max_splits,
-            "timing": "CUDA graph of back-to-back calls (partial: of partial-kernel launches alone), "
-                      "L2 " + ("rotated sets" if n_sets > 1 else "inputs > L2")}
+    rec = {"us": round(call_ms * 1e3, 2), "kernel_us": round(part_ms * 1e3, 2), "splits": plan.max_splits}
+    if name in TENSOR_BOUND:
+        tf = decode_flops(wl) / (part_ms / 1e3) / 1e12
+        rec.update(bound="tensor", tflops=round(tf, 1), frac=round(tf / peak["bf16_tflops"], 3))
+    else:
+        gbs = alg_bytes / (part_ms / 1e3) / 1e9
+        rec.update(bound="hbm", gbs=round(gbs, 1), frac=round(gbs / peak["hbm_gbs"], 3))
+    return rec
 
 
 def measure_prefill(mla, dev, steps=10):
@@ -165,12 +187,10 @@ def measure_prefill(mla, dev, steps=10):
     st.synchronize()
     ms = graph_ms_per_call(call, steps, st)
     assert mla.get_status(st) == mla.MLA_OK
-    fl = prefill_flops(wl)
+    tf = prefill_flops(wl) / (ms / 1e3) / 1e12
     peak = _peaks()
-    tf = fl / (ms / 1e3) / 1e12
-    return {"workload": wl.name, "ms_per_call": ms, "tflops": tf, "flops_per_call": fl,
-            "roofline": {"bound": "tensor", "achieved": tf, "peak": peak["bf16_tflops"], "unit": "TFLOP/s",
-                         "frac": tf / peak["bf16_tflops"], "peak_source": peak["source"] + " bf16 dense burst"}}
+    return {"us": round(ms * 1e3, 1), "bound": "tensor", "tflops": round(tf, 1),
+            "frac": round(tf / peak["bf16_tflops"], 3)}
 
 
 class ClockSampler:
@@ -254,33 +274,30 @@ def replica_seed(base_seed, set_index, rank):
     return base_seed + 97 * set_index + 100003 * rank
 
 
-def _traffic_record(kernel_src):
-    """DRAM bytes per launch from the committed ncu summary, if it was taken on the
-    current kernel source; otherwise None."""
+def _traffic_record(kernel_src, workload):
+    """DRAM bytes per launch of the partial kernel on `workload` from the committed ncu
+    summary, if it was taken on the current kernel source; otherwise None."""
     import hashlib
     path = os.path.join(ROOT, "profiles", "decode_partial_traffic.json")
     try:
         with open(path) as f:
             rec = json.load(f)
         src = open(os.path.join(ROOT, "mla_attention_paged_gb300", "csrc", kernel_src), "rb").read()
-        if rec.get("source_sha256") != hashlib.sha256(src).hexdigest():
+        if rec.get("source_sha256") != hashlib.sha256(src).hexdigest() or rec.get("workload") != workload:
             return None
         return rec
     except Exception:
         return None
 
 
-def cpu_baseline(wl, inp_cpu, seconds=10.0):
-    """The fp64 oracle, as it stands, on a bounded sample of this workload's rows: random
-    row subsets (whole passes over the workload when it is small) until about `seconds` of
-    oracle time have been spent."""
+def _oracle_rows_for(inp_cpu, rows_total, seconds, seed):
+    """Run the oracle on random row subsets of one decode workload until about `seconds` of
+    oracle time are spent; returns (rows done, seconds)."""
     import numpy as np
 
     import oracle
-    oracle.build()
-    rows_total = wl.batch * wl.q_len * wl.heads
-    rng = np.random.default_rng(0)
-    n = 8
+    rng = np.random.default_rng(seed)
+    n = 1
     done_rows, elapsed = 0, 0.0
     while elapsed < seconds:
         rows = rng.choice(rows_total, size=min(n, rows_total), replace=False)
@@ -290,17 +307,38 @@ def cpu_baseline(wl, inp_cpu, seconds=10.0):
         elapsed += time.perf_counter() - t0
         done_rows += len(rows)
         per_row = elapsed / done_rows
-        n = int(max(8, min(rows_total, (seconds - elapsed) / max(per_row, 1e-9))))
+        n = int(max(1, min(rows_total, (seconds - elapsed) / max(per_row, 1e-9))))
+    return done_rows, elapsed
+
+
+def cpu_baseline(wl, inp_cpu, seconds=10.0, single_seconds=4.0):
+    """The fp64 oracle, as it stands, on a bounded sample of this workload's rows: random
+    row subsets until about `seconds` of oracle time on every host thread, then about
+    `single_seconds` on one thread.  Each figure is the workload's KV bytes over the time a
+    whole pass would take at the sampled rate (rows of one workload cost about the same)."""
+    import oracle
+    oracle.build()
+    rows_total = wl.batch * wl.q_len * wl.heads
     kv_bytes, _ = decode_bytes(wl)
-    step_s = elapsed * rows_total / done_rows
-    return {"value": kv_bytes / step_s / 1e9, "unit": "GB/s", "cores": oracle.num_threads(), "kind": "oracle",
-            "sample": f"{done_rows} (request, draft, head) rows drawn from the {rows_total} of {wl.name} "
-                      f"({done_rows / rows_total:.2f} passes), fp64, {elapsed:.1f} s; step time scaled by rows",
-            "seconds": round(elapsed, 2)}
+    threads = oracle.num_threads()
+    done, el = _oracle_rows_for(inp_cpu, rows_total, seconds, 0)
+    oracle.set_num_threads(1)
+    try:
+        done1, el1 = _oracle_rows_for(inp_cpu, rows_total, single_seconds, 1)
+    finally:
+        oracle.set_num_threads(threads)
+    return {"value": kv_bytes / (el * rows_total / done) / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
+            "sample": f"{done} of the {rows_total} (request, draft, head) rows of {wl.name}, fp64, {el:.1f} s; "
+                      f"pass time scaled by rows",
+            "single_thread": {"value": kv_bytes / (el1 * rows_total / done1) / 1e9, "unit": "GB/s",
+                              "rows": done1, "seconds": round(el1, 2)}}
 
 
 def run_reference(args, ws, rank):
-    """Reference arm: the CPU fp64 oracle timed on bounded samples of the same workload."""
+    """Reference arm: the CPU fp64 oracle, as it stands, on the host cores.  Each step is a
+    bounded sample of the headline workload's rows (sized so the whole run takes about a
+    minute); ms_per_step is the sample's measured time and value the workload's KV bytes
+    over the time a whole pass would take at that rate."""
     if rank != 0:
         return
     import numpy as np
@@ -311,13 +349,13 @@ def run_reference(args, ws, rank):
     inp = make_decode_inputs(wl, "cpu")
     rows_total = wl.batch * wl.q_len * wl.heads
     rng = np.random.default_rng(1)
-    # size each step's row sample so that warm-up + K steps take about a minute
-    t0 = time.perf_counter()
-    oracle.mla_decode(inp.q, inp.kv_pool, inp.page_table, inp.seq_lens, inp.scale, rows=[0])
-    per_row = max(time.perf_counter() - t0, 1e-4)
     threads = oracle.num_threads()
+    t0 = time.perf_counter()
+    oracle.mla_decode(inp.q, inp.kv_pool, inp.page_table, inp.seq_lens, inp.scale,
+                      rows=rng.choice(rows_total, min(threads, rows_total), replace=False))
+    per_row = max((time.perf_counter() - t0) / threads, 1e-5)
     budget = 60.0 / max(1, args.steps + args.warmup)
-    rows_per_step = int(max(1, min(threads, rows_total, budget / per_row * threads)))
+    rows_per_step = int(max(1, min(rows_total, budget / per_row)))
     for _ in range(args.warmup):
         oracle.mla_decode(inp.q, inp.kv_pool, inp.page_table, inp.seq_lens, inp.scale,
                           rows=rng.choice(rows_total, rows_per_step, replace=False))
@@ -327,15 +365,16 @@ def run_reference(args, ws, rank):
                           rows=rng.choice(rows_total, rows_per_step, replace=False))
     el = time.perf_counter() - t0
     kv_bytes, _ = decode_bytes(wl)
-    step_s = el / args.steps * rows_total / rows_per_step
-    val = kv_bytes / step_s / 1e9
+    step_s = el / args.steps
+    val = kv_bytes * rows_per_step / rows_total / step_s / 1e9
+    sample = (f"each step: {rows_per_step} of the {rows_total} (request, draft, head) rows of {WORKLOAD}, fp64; "
+              f"value = KV bytes x sampled fraction / step time")
     line = {"impl": "reference", "metric": METRIC, "value": val, "unit": "GB/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_s * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": WORKLOAD, "batch": wl.batch, "q_len": wl.q_len, "heads": wl.heads,
-                       "kv_len": wl.seq_lens[0], "page_size": wl.page_size, "kv_dtype": wl.kv_dtype},
-            "cpu_baseline": {"value": val, "unit": "GB/s", "cores": oracle.num_threads(), "kind": "oracle",
-                             "sample": f"{rows_per_step} of {rows_total} rows per step, step time scaled by rows"},
+                       "kv_len": "U[8192,131072]", "page_size": wl.page_size, "kv_dtype": wl.kv_dtype},
+            "cpu_baseline": {"value": val, "unit": "GB/s", "cores": threads, "kind": "oracle", "sample": sample},
             "e2e": {"value": val, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -369,11 +408,11 @@ def run_profile_case(name):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
-    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="mine", choices=["mine", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--no-extra", action="store_true", help="skip the secondary prefill / batch-16 decode lines")
+    ap.add_argument("--no-extra", action="store_true", help="skip the secondary decode / prefill lines")
     ap.add_argument("--profile-case", default=None,
                     help="run three calls of one named workload (a profiler target) and exit without timing")
     args = ap.parse_args()
@@ -394,14 +433,9 @@ def main():
 
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    wl = decode_workloads()[WORKLOAD]
+    wl, sets = decode_sets(WORKLOAD, dev, rank)
+    n_sets = len(sets)
     kv_bytes, alg_bytes = decode_bytes(wl)
-    n_sets = max(2, math.ceil(2.5 * L2_BYTES / kv_bytes) + 1)
-    sets = []
-    for i in range(n_sets):
-        wl_i = decode_workloads()[WORKLOAD]
-        wl_i.seed = replica_seed(wl.seed, i, rank)
-        sets.append(make_decode_inputs(wl_i, dev))
     s0 = sets[0]
     plan = mla.decode_plan(wl.seq_lens, wl.q_len, wl.heads, wl.page_size, s0.page_table.shape[1],
                            s0.kv_pool.shape[0], mla.MLA_KV_BF16)
@@ -430,9 +464,9 @@ def main():
     stream.synchronize()
 
     # Duration of the dominant kernel: the split-KV partial kernel alone, launched back to
-    # back (same rotated inputs) in a second graph, timed between one pair of CUDA events on
-    # the launch stream, right after the timed replay and under the same clock sampling.
-    n_k = min(args.steps, 400)
+    # back (same inputs) in a second graph, timed between one pair of CUDA events on the
+    # launch stream, right after the timed replay and under the same clock sampling.
+    n_k = max(20, min(args.steps, 400))
 
     def partial_step(i):
         s = sets[i % n_sets]
@@ -479,12 +513,13 @@ def main():
     part_ms = kstart.elapsed_time(kstop) / n_k
     peaks = _peaks()
     achieved = alg_bytes / (part_ms / 1e3) / 1e9
-    traffic = _traffic_record("mla_decode_sm103a.cu")
+    traffic = _traffic_record("mla_decode_sm103a.cu", WORKLOAD)
 
     # End to end through the public API: each step copies that step's q, page table and
     # lengths from pinned host memory to the device (packed in one buffer: one copy), calls
     # mla_decode, and copies out + lse back to pinned host memory (one packed buffer, one
-    # copy).  The latent cache is device-resident.
+    # copy).  The latent cache is device-resident.  Two I/O slots (or one per input set)
+    # alternate, so that step i+1's inputs and step i-1's results move while step i computes.
     def _packed(tensors):
         offs, off = [], 0
         for t in tensors:
@@ -496,10 +531,12 @@ def main():
         n = like.numel() * like.element_size()
         return buf[off:off + n].view(like.dtype).view(like.shape)
 
+    n_io = max(2, n_sets)
     in_offs, in_bytes = _packed([sets[0].q, sets[0].page_table, sets[0].seq_lens])
     out_offs, out_bytes = _packed([outs[0], lses[0]])
     host_in, dev_in, host_out, dev_out = [], [], [], []
-    for k, s in enumerate(sets):
+    for k in range(n_io):
+        s = sets[k % n_sets]
         hb = torch.empty(in_bytes, dtype=torch.uint8).pin_memory()
         for t, off in zip((s.q, s.page_table, s.seq_lens), in_offs):
             _view(hb, off, t).copy_(t.cpu())
@@ -508,28 +545,25 @@ def main():
         dev_in.append((db, _view(db, in_offs[0], s.q), _view(db, in_offs[1], s.page_table),
                        _view(db, in_offs[2], s.seq_lens)))
         ob = torch.empty(out_bytes, dtype=torch.uint8, device=dev)
-        dev_out.append((ob, _view(ob, out_offs[0], outs[k]), _view(ob, out_offs[1], lses[k])))
+        dev_out.append((ob, _view(ob, out_offs[0], outs[0]), _view(ob, out_offs[1], lses[0])))
         host_out.append(torch.empty(out_bytes, dtype=torch.uint8).pin_memory())
     h2d = sum(t.numel() * t.element_size() for t in (sets[0].q, sets[0].page_table, sets[0].seq_lens))
     d2h = sum(t.numel() * t.element_size() for t in (outs[0], lses[0]))
     e2e_steps = min(args.steps, 500)
 
-    # Copies run on their own streams so that step i+1's inputs and step i-1's results move
-    # while step i computes (each set's buffers are reused only after the step that last
-    # used them is done with them).
     s_h2d = torch.cuda.Stream(device=dev)
     s_d2h = torch.cuda.Stream(device=dev)
-    ev_in = [torch.cuda.Event() for _ in sets]
-    ev_done = [torch.cuda.Event() for _ in sets]
-    ev_read = [torch.cuda.Event() for _ in sets]
+    ev_in = [torch.cuda.Event() for _ in range(n_io)]
+    ev_done = [torch.cuda.Event() for _ in range(n_io)]
+    ev_read = [torch.cuda.Event() for _ in range(n_io)]
 
     def e2e_step(i):
-        k = i % n_sets
-        s = sets[k]
+        k = i % n_io
+        s = sets[k % n_sets]
         db, q_d, pt_d, sl_d = dev_in[k]
         ob, out_d, lse_d = dev_out[k]
         with torch.cuda.stream(s_h2d):
-            s_h2d.wait_event(ev_done[k])       # the last step on this set has consumed its inputs
+            s_h2d.wait_event(ev_done[k])       # the last step on this slot has consumed its inputs
             db.copy_(host_in[k], non_blocking=True)
             ev_in[k].record(s_h2d)
         stream.wait_event(ev_in[k])
@@ -550,7 +584,7 @@ def main():
             ev_start.record(stream)
             s_h2d.wait_event(ev_start)
             s_d2h.wait_event(ev_start)
-            for k in range(n_sets):  # nothing pending on any set at the start
+            for k in range(n_io):  # nothing pending on any slot at the start
                 ev_done[k].record(stream)
                 ev_read[k].record(s_d2h)
             for i in range(n):
@@ -584,41 +618,40 @@ def main():
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded N(0,1)/sqrt(576) latents, shuffled 64-token pages)",
         "config": {"workload": WORKLOAD, "batch": wl.batch, "q_len": wl.q_len, "heads": wl.heads,
-                   "kv_len": wl.seq_lens[0], "page_size": wl.page_size, "kv_dtype": wl.kv_dtype,
-                   "parallelism": f"replicas x{ws}", "l2": f"inputs rotated over {n_sets} sets "
-                   f"({n_sets * kv_bytes / 2**20:.0f} MiB KV > 2.5x L2)",
-                   "timing": "one CUDA graph of K steps, CUDA events on the launch stream",
-                   "splits": plan.max_splits, "chunk_tokens": plan.chunk_tokens},
+                   "kv_len": "U[8192,131072]", "page_size": wl.page_size, "kv_dtype": wl.kv_dtype,
+                   "parallelism": f"replicas x{ws}",
+                   "l2": (f"inputs rotated over {n_sets} sets" if n_sets > 1 else
+                          f"inputs larger than L2 ({kv_bytes / 2**20:.0f} MiB KV)"),
+                   "splits": plan.max_splits},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": achieved / peaks["hbm_gbs"],
                      "traffic": (traffic["dram_bytes_per_launch"] if traffic else None),
-                     "kernel": "decode_partial_bf16_kernel", "kernel_us": part_ms * 1e3,
-                     "kernel_timing": f"{n_k} back-to-back launches of the partial kernel in one CUDA graph "
-                                      "between two CUDA events on the launch stream",
-                     "alg_bytes_per_launch": alg_bytes, "peak_source": peaks["source"]},
+                     "kernel": "decode_partial_kernel<bf16>", "kernel_us": part_ms * 1e3,
+                     "alg_bytes_per_launch": alg_bytes, "peak_source": peaks["source"] + " copy bandwidth"},
         "e2e": {"value": e2e_val, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "steps": e2e_steps, "us_per_call": e2e_s / e2e_steps * 1e6,
-                "host_enqueue_us_per_call": enqueue_s / e2e_steps * 1e6,
-                "copies_per_step": "1 H2D (q, page table, lengths packed) + 1 D2H (out, lse packed), "
-                                   "on copy streams overlapping the neighbouring steps' compute",
-                "timing": "wall clock around one replay of a CUDA graph of the steps"},
+                "host_enqueue_us_per_call": enqueue_s / e2e_steps * 1e6},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks,
+        "timing": "value: one CUDA graph of K steps between CUDA events on the launch stream; kernel: "
+                  f"{n_k} back-to-back partial-kernel launches in one graph; e2e: wall clock of one graph of "
+                  "steps with packed H2D/D2H copies on copy streams",
     }
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         inp_cpu = make_decode_inputs(decode_workloads()[WORKLOAD], "cpu")
         line["cpu_baseline"] = cpu_baseline(wl, inp_cpu)
+        del inp_cpu
     if not args.no_extra:
-        # the other hot-path rows, measured on their own (not part of `value`)
+        # the other hot-path rows, each measured on its own (not part of `value`): per call
+        # (us), partial kernel alone (kernel_us) and its fraction of the binding roofline
         del sets, host_in, dev_in, host_out, dev_out, graph, kgraph
         torch.cuda.empty_cache()
-        line["extra"] = {"prefill": measure_prefill(mla, dev)}
-        for name in ["decode_bf16_b16_q4_h16_l64k", "decode_fp8_b16_q4_h16_l64k", "decode_int8_b16_q4_h16_l64k",
-                     "decode_fp8_b8_q4_h16_l64k",
-                     "decode_b16_q2_h16_ragged", "decode_b16_q2_h128_ragged", "decode_b1_q1_h16_l1024",
-                     "decode_b4_q512_h16_l32k"]:
-            line["extra"][name] = measure_decode_extra(mla, name, dev)
+        extra = {}
+        for name in EXTRA_DECODE:
+            extra[name] = measure_decode_extra(mla, name, dev)
             torch.cuda.empty_cache()
+        extra["prefill_b5_h16_prefix"] = measure_prefill(mla, dev)
+        line["extra"] = extra
     if rank == 0:
         print(json.dumps(line), flush=True)
     if ws > 1:

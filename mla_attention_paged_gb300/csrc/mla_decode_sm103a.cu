@@ -87,6 +87,10 @@ struct DecodeCtrl {
 constexpr int kSmemBytes = kOffCtrl + 1024 + 1024;  // + control block + alignment slack
 static_assert(sizeof(DecodeCtrl) <= 1024, "control block");
 
+// Values of the CTA's abort flag: a bounded wait ran out, or a device argument check failed.
+constexpr int kAbortTimeout = 1;
+constexpr int kAbortBadArg = 2;
+
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemS = 256;   // S buffers at columns 256 and 320; O^T chunks at 0,64,128,192
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
@@ -277,6 +281,8 @@ decode_partial_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
     int cur = (first_page + lane <= last_page) ? __ldg(pt + first_page + lane) : 0;
     int nxt = (first_page + 32 + lane <= last_page) ? __ldg(pt + first_page + 32 + lane) : 0;
     const uint64_t pol_kv = policy_evict_first();
+    const unsigned n_pages = static_cast<unsigned>(min(p.num_pages, static_cast<int64_t>(0x7fffffff)));
+    bool bad_pid = false;
     int last_issued[kStages] = {-1, -1};
     bool ok = true;
     for (int j = 0; j < ntiles; ++j) {
@@ -301,17 +307,14 @@ decode_partial_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
           pids[pp] = 0;
         }
       }
-      // A page id outside the pool is reported and replaced by -1: its box then lies
-      // wholly before the first row, and TMA fills it with zeros instead of reading.
-      bool bad_pid = false;
+      // A page id outside the pool is replaced by -1 (reported after the loop): its box
+      // then lies wholly before the first row, and TMA fills it with zeros instead of reading.
 #pragma unroll
       for (int pp = 0; pp < 8; ++pp) {
-        if (pp < npg && (pids[pp] < 0 || static_cast<int64_t>(pids[pp]) >= p.num_pages)) {
-          bad_pid = true;
-          pids[pp] = -1;
-        }
+        const bool outside = pp < npg && static_cast<unsigned>(pids[pp]) >= n_pages;
+        bad_pid |= outside;
+        pids[pp] = outside ? -1 : pids[pp];
       }
-      if (bad_pid && lane == 0) atomicOr(p.status, kStatusDeviceArg);
       // The page ids above are resolved before waiting for the stage, so that only the
       // copies are left once it frees up (resolving them after the wait was measured to
       // delay each tile's copies by ~1.5k cycles).
@@ -341,6 +344,7 @@ decode_partial_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
       last_issued[s] = j;
       __syncwarp();
     }
+    if (bad_pid && lane == 0) atomicOr(p.status, kStatusDeviceArg);
     if (!ok && lane == 0) {
       // drain copies still in flight before the CTA exits
       drain_wait(&ctrl->q_full, 0);
@@ -371,8 +375,9 @@ decode_partial_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
       const int k = kv_start + jt * kTileKeys + lane * P;
       return (lane < sub && jt < ntiles && k < kv_end) ? k / P : -1;
     };
+    const unsigned n_pages = static_cast<unsigned>(min(p.num_pages, static_cast<int64_t>(0x7fffffff)));
     auto prefetch = [&](int jt, int pid) {
-      if (pid < 0 || static_cast<int64_t>(pid) >= p.num_pages) return;  // (a bad id is reported by the decode warps)
+      if (static_cast<unsigned>(pid) >= n_pages) return;  // none, or outside the pool (the decode warps report it)
       const int k = kv_start + jt * kTileKeys + lane * P;
       const int rows = min(min(P, kTileKeys), kv_end - k);
       prefetch_l2_bulk(p.kv_pool + (static_cast<int64_t>(pid) * P + k % P) * kLatentDim,
@@ -457,8 +462,10 @@ decode_partial_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
           const unsigned long long now = global_timer_ns();
           if (idle_since == 0) {
             idle_since = now;
-          } else if (*abort_flag || now - idle_since > kWaitLimitNs) {
-            *abort_flag = 1;
+          } else if (*abort_flag) {
+            give_up = 1;
+          } else if (now - idle_since > kWaitLimitNs) {
+            *abort_flag = kAbortTimeout;
             give_up = 1;
           }
         }
@@ -482,6 +489,18 @@ decode_partial_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
     const int dw = (warp == 4) ? 0 : warp - 5;
     const int dl = lane;
     const int td = dw * 32 + dl;
+    const int P = p.page_size;
+    const int32_t* pt = p.page_table + static_cast<int64_t>(b) * p.max_pages;
+    // Every page id this split reads (rows kv_start .. kv_end - 1) is checked once, before
+    // any row is read; the loads are issued here and overlap the Q conversion.  An id
+    // outside the pool stops the CTA (reported as a device argument error below).  The
+    // check stays out of the tile loop, whose loads it would otherwise delay.
+    bool bad_id = false;
+    {
+      const unsigned n_pages = static_cast<unsigned>(min(p.num_pages, static_cast<int64_t>(0x7fffffff)));
+      for (int pg = kv_start / P + td; pg <= (kv_end - 1) / P; pg += kDequantThreads)
+        bad_id |= static_cast<unsigned>(__ldg(pt + pg)) >= n_pages;
+    }
     bool ok = mbar_wait(&ctrl->q_full, 0, abort_flag);
     if (ok) {
       const uint32_t q_s = smem_u32(smem + kOffQ);
@@ -496,23 +515,19 @@ decode_partial_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
       fence_proxy_async_smem();
       mbar_arrive(&ctrl->q_ready);
     }
-    const int P = p.page_size;
-    const int32_t* pt = p.page_table + static_cast<int64_t>(b) * p.max_pages;
-    // page id of each owned row of tile j (-1 past the request end, or for an id outside
-    // the pool, which is reported: the row is not read and counts as zeros)
+    if (bar_or(2, kDequantThreads, bad_id)) {
+      if (td == 0) {
+        atomicOr(p.status, kStatusDeviceArg);
+        *abort_flag = kAbortBadArg;  // the other roles leave their loops at their next wait
+      }
+      ok = false;
+    }
+    // page id of each owned row of tile j (0 past the request end: the row is not read)
     auto row_pids = [&](int j, int (&pid)[8]) {
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         const int k = kv_start + j * kTileKeys + (dl >> 2) + 8 * i;
-        int v = -1;
-        if (k < L) {
-          v = __ldg(pt + k / P);
-          if (v < 0 || static_cast<int64_t>(v) >= p.num_pages) {
-            atomicOr(p.status, kStatusDeviceArg);
-            v = -1;
-          }
-        }
-        pid[i] = v;
+        pid[i] = (k < L) ? __ldg(pt + k / P) : 0;
       }
     };
     int pid_cur[8];
@@ -524,9 +539,8 @@ decode_partial_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         const int k = k0 + (dl >> 2) + 8 * i;
-        const bool valid = pid_cur[i] >= 0;
-        const uint8_t* row =
-            p.kv_pool + (static_cast<int64_t>(valid ? pid_cur[i] : 0) * P + k % P) * kLatentDim + (dl & 3) * 16;
+        const uint8_t* row = p.kv_pool + (static_cast<int64_t>(pid_cur[i]) * P + k % P) * kLatentDim + (dl & 3) * 16;
+        const bool valid = k < L;
 #pragma unroll
         for (int m = 0; m < 3; ++m)
           w[m][i] = valid ? __ldg(reinterpret_cast<const uint4*>(row + (dw + 3 * m) * 64)) : make_uint4(0u, 0u, 0u, 0u);
@@ -730,7 +744,7 @@ decode_partial_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
 
   tc_fence_before();
   __syncthreads();
-  if (threadIdx.x == 0 && ctrl->abort_flag) atomicOr(p.status, kStatusTimeout);
+  if (threadIdx.x == 0 && ctrl->abort_flag == kAbortTimeout) atomicOr(p.status, kStatusTimeout);
   // every store of this CTA is issued: the combine grid may be scheduled now
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (warp == 5) {

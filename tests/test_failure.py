@@ -5,9 +5,8 @@
   arrives on); the context stays usable afterwards.
 * Device-side argument checks are caught by the kernels before any access that depends
   on them and reported as MLA_ERR_DEVICE_ARG: a decode request longer than the plan
-  allows, a page id outside the pool (on the bf16 path, whose TMA reads zero-fill outside
-  the pool even without the check), and a prefill request with more new tokens than the
-  host's max_seqlen_q sized the grid for.
+  allows, a page id outside the pool (bf16, e4m3 and int8 pools), and a prefill request
+  with more new tokens than the host's max_seqlen_q sized the grid for.
 """
 import time
 
@@ -62,18 +61,28 @@ def test_length_beyond_plan_is_reported(mla):
     assert mla.get_status() == mla.MLA_OK
 
 
-@pytest.mark.parametrize("bad_id", [-1, 10**6], ids=["negative", "past_pool"])
-def test_page_id_outside_pool_is_reported(mla, bad_id):
-    wl = DecodeWorkload("bad_page", 2, 2, 16, [700, 300], seed=6)
+@pytest.mark.parametrize("kv", ["bf16", "e4m3", "int8"])
+@pytest.mark.parametrize("bad", ["negative", "past_pool"])
+def test_page_id_outside_pool_is_reported(mla, kv, bad):
+    """A page id outside [0, num_pages) is reported as MLA_ERR_DEVICE_ARG.  The pool given
+    to the call is a view into a larger allocation (16 spare pages on each side), so the
+    ids used here (-1 and num_pages + 5) still name allocated memory: the test checks the
+    report without any read outside an allocation, whatever the kernel does."""
+    wl = DecodeWorkload("bad_page", 2, 2, 16, [700, 300], kv_dtype=kv, seed=6)
     inp = make_decode_inputs(wl, "cpu")
-    plan = mla.decode_plan([700, 300], 2, 16, 64, inp.page_table.shape[1], inp.kv_pool.shape[0])
+    n = inp.kv_pool.shape[0]
+    big = torch.zeros((n + 32,) + tuple(inp.kv_pool.shape[1:]), dtype=inp.kv_pool.dtype, device="cuda")
+    big[16:16 + n] = inp.kv_pool.cuda()
+    pool = big[16:16 + n]
+    kvd = {"e4m3": mla.MLA_KV_E4M3, "int8": mla.MLA_KV_INT8}.get(kv, mla.MLA_KV_BF16)
+    plan = mla.decode_plan([700, 300], 2, 16, 64, inp.page_table.shape[1], n, kvd)
     pt = inp.page_table.clone()
-    pt[0, 3] = bad_id
-    mla.decode(plan, inp.q.cuda(), inp.kv_pool.cuda(), pt.cuda(), inp.seq_lens.cuda(), inp.scale)
+    pt[0, 3] = -1 if bad == "negative" else n + 5
+    mla.decode(plan, inp.q.cuda(), pool, pt.cuda(), inp.seq_lens.cuda(), inp.scale, inp.kv_scale)
     torch.cuda.synchronize()
     assert mla.get_status() == mla.MLA_ERR_DEVICE_ARG
     # the valid table runs clean afterwards
-    mla.decode(plan, inp.q.cuda(), inp.kv_pool.cuda(), inp.page_table.cuda(), inp.seq_lens.cuda(), inp.scale)
+    mla.decode(plan, inp.q.cuda(), pool, inp.page_table.cuda(), inp.seq_lens.cuda(), inp.scale, inp.kv_scale)
     torch.cuda.synchronize()
     assert mla.get_status() == mla.MLA_OK
 

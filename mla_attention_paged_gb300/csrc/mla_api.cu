@@ -55,10 +55,11 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// Tiled tensor map with 128-byte swizzle.  dims/strides innermost first; strides in bytes
-// for dims 1..rank-1.
+// Tiled tensor map (128-byte swizzle unless given).  dims/strides innermost first; strides
+// in bytes for dims 1..rank-1.
 bool make_map(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void* base, const uint64_t* dims,
-              const uint64_t* strides, const uint32_t* box) {
+              const uint64_t* strides, const uint32_t* box,
+              CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
   PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
   if (!fn) return false;
   cuuint64_t d[5];
@@ -72,7 +73,7 @@ bool make_map(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void* base
     if (i + 1 < rank) s[i] = strides[i];
   }
   CUresult r = fn(m, dt, static_cast<cuuint32_t>(rank), const_cast<void*>(base), d, s, bx, es,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
@@ -321,7 +322,25 @@ int decode_stages(const mla_decode_plan_t* plan, const void* q, const void* kv_p
     if (!make_map(&tm_q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, q, dims, strides, box)) return MLA_ERR_CUDA;
   }
   memset(&tm_kv, 0, sizeof tm_kv);
-  if (partial && plan->kv_dtype == MLA_KV_BF16) {  // 8-bit pages are read row by row by the decode warps
+  if (partial && plan->kv_dtype == MLA_KV_E4M3) {
+    // e4m3 codes, 576 bytes per row, viewed as [rows][9 blocks][64 bytes] with 64-byte
+    // swizzle: one box lands a 64-key tile as the K-major layout the 8-bit MMAs read.
+    const uint64_t rows = static_cast<uint64_t>(plan->num_pages) * plan->page_size;
+    if (plan->page_size >= kTileKeys) {
+      const uint64_t dims[3] = {64, rows, kLatentDim / 64};
+      const uint64_t strides[2] = {static_cast<uint64_t>(kLatentDim), 64};
+      const uint32_t box[3] = {64, static_cast<uint32_t>(kTileKeys), kLatentDim / 64};
+      if (!make_map(&tm_kv, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, kv_pages, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_64B))
+        return MLA_ERR_CUDA;
+    } else {  // smaller pages: one 2-D box per (page, column block)
+      const uint64_t dims[2] = {static_cast<uint64_t>(kLatentDim), rows};
+      const uint64_t strides[1] = {static_cast<uint64_t>(kLatentDim)};
+      const uint32_t box[2] = {64, static_cast<uint32_t>(plan->page_size)};
+      if (!make_map(&tm_kv, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, kv_pages, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_64B))
+        return MLA_ERR_CUDA;
+    }
+  }
+  if (partial && plan->kv_dtype == MLA_KV_BF16) {  // int8 pages are read row by row by the decode warps
     const uint64_t rows = static_cast<uint64_t>(plan->num_pages) * plan->page_size;
     if (plan->page_size >= kTileKeys) {  // a 64-key tile is one row range of one page
       const uint64_t dims[3] = {64, rows, kLatentDim / 64};

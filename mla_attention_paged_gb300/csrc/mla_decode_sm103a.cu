@@ -1,10 +1,11 @@
-// mla_decode_sm103a.cu -- absorbed MLA decode over a paged latent KV cache, sm_103a.
+// mla_decode_sm103a.cu -- absorbed MLA decode over a paged latent KV cache (bf16 or int8
+// pool), sm_103a.  (An e4m3 pool runs decode_partial_e4m3_kernel, mla_decode_e4m3_sm103a.cu.)
 //
 // What it computes (per request b, draft t, head h; keys j = 0 .. L_b - T + t):
 //   out[b,t,h,:] = sum_j softmax_j(scale * q[b,t,h,:] . k_j) * k_j[:512]
 // where k_j is the 576-wide latent row j of request b, found through the page table (an
-// e4m3 or int8 pool is decoded exactly to f16 and its per-tensor scale folded into the
-// softmax scale and the output).  With T beyond a few drafts the same computation is the
+// int8 pool is decoded exactly to f16 and its per-tensor scale folded into the softmax
+// scale and the output).  With T beyond a few drafts the same computation is the
 // prefill of T new tokens over a paged prefix in absorbed form.  TokenSpeed pages: "构建面向 Agentic 推理的下一代 LLM 推理引擎"
 // (AICon talk), section "Kernel：让 MLA 真正跑满 GPU" (latent state shared by all heads,
 // fold factor, split-KV partial + reduction stages, TMEM accumulators, KV bandwidth as the
@@ -17,32 +18,15 @@
 //    takes 64 consecutive rows, so all heads and drafts share each latent tile load.
 //  * Producer warp: bf16 pools are gathered by TMA (one 3-D box per 64-key tile: 64 rows x
 //    nine 128-byte-swizzled column blocks) from the pages named by the page table, into a
-//    2-stage ring.  For 8-bit pools, three dequant warps (4, 6, 7) read each tile's rows
+//    2-stage ring.  For int8 pools, three dequant warps (4, 6, 7) read each tile's rows
 //    from the page pool into registers, wait for the stage, and write them as f16 into the
-//    same swizzled layout (exact decode: e4m3 values times 2^-8, the factor folded into
-//    the scales; int8 codes as themselves); the MMA warp prefetches rows into L2 a few
-//    tiles ahead of them.  The 8-bit GEMMs run on f16 operands (Q converted once per CTA,
-//    P in f16).
-//  * MMA warp (uniform control flow, one elected thread issues): BMM1  S[rows, keys] =
-//    Q . K^T  (M=64, N=64, K=576) into TMEM, double-buffered; BMM2  O^T[dims, rows] +=
-//    V^T . P^T  (M=128 per 128 value columns, N=rows, K=64 keys) with V^T read MN-major
-//    from the same shared-memory tile as K.  O^T lives in TMEM for the whole split (256
-//    columns); S takes 2 x 64 columns.  GEMMs are issued in whichever order their inputs
-//    become ready.
-//  * Softmax warps (4): the M=64 accumulator puts row 16w+i in TMEM lane 32w+i, so each
-//    warp serves 16 rows, each row split between lanes i and i+16 (32 keys apiece); it
-//    applies the causal/length mask, keeps a running max in the log2 domain with a lazy
-//    rescale (O is rescaled only when the max grows by more than 2^8), and writes P
-//    (bf16) to shared memory as the K-major B operand of BMM2.
-//  * Epilogue (4 warps over the 128 TMEM lanes = value columns): normalise by the row
-//    sum and write either the final bf16 output (single split) or the bf16 partial and
-//    its fp32 log-sum-exp for the combine kernel, which runs as a programmatic dependent
-//    launch triggered after each CTA's last store.
-// Every wait is bounded; on expiry the CTA records a timeout in the status word, drains
-// its in-flight copies and MMAs, frees TMEM and returns.
+//    same swizzled layout (exact decode: int8 codes as themselves); the MMA warp prefetches
+//    rows into L2 a few tiles ahead of them.  The int8 GEMMs run on f16 operands (Q
+//    converted once per CTA, P in f16).
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
 
+#include "kv8_decode.cuh"
 #include "mla_internal.h"
 #include "sm103a_ptx.cuh"
 
@@ -53,15 +37,15 @@ constexpr int kDimBlocks = kLatentDim / 64;          // 9 blocks of 64 columns (
 constexpr int kBlockBytes = 64 * 128;                // 64 rows x 128 bytes, swizzled
 constexpr int kTileBytes = kDimBlocks * kBlockBytes; // 73728: one bf16 64-key latent tile
 constexpr int kStages = 2;
-constexpr int kPrefetchTiles = 3;  // 8-bit pools: tiles ahead of the decode that are prefetched into L2
-// Warps 0-3 softmax/epilogue, 5 MMA; bf16: warp 4 producer (192 threads); 8-bit pools:
+constexpr int kPrefetchTiles = 3;  // int8 pools: tiles ahead of the decode that are prefetched into L2
+// Warps 0-3 softmax/epilogue, 5 MMA; bf16: warp 4 producer (192 threads); int8 pools:
 // warps 4, 6 and 7 decode (256 threads: eight warps keep the register budget at 255 per
 // thread).
 constexpr int kDequantThreads = 96;
 __host__ __device__ constexpr int threads_for(bool fp8) { return fp8 ? 256 : 192; }
 
 // Shared memory map: Q | stage0 | stage1 | P | ctrl.  A stage holds one 64-key tile as nine
-// 128-byte-swizzled column blocks: bf16 as loaded by TMA, or (8-bit pools) f16 as decoded
+// 128-byte-swizzled column blocks: bf16 as loaded by TMA, or (int8 pools) f16 as decoded
 // by the dequant warps from rows they read straight from global memory.
 constexpr int kOffQ = 0;
 constexpr int kOffStages = kOffQ + kTileBytes;
@@ -70,13 +54,13 @@ constexpr int kOffCtrl = kOffP + kBlockBytes;
 
 struct DecodeCtrl {
   uint64_t q_full;
-  uint64_t kv_full[kStages];   // tile landed (bf16: TMA bytes; 8-bit: dequant threads)
+  uint64_t kv_full[kStages];   // tile landed (bf16: TMA bytes; int8: dequant threads)
   uint64_t kv_empty[kStages];  // BMM2 of the tile in this stage completed
   uint64_t s_full[2];
   uint64_t s_free[2];
   uint64_t p_full;
   uint64_t o_done;
-  uint64_t q_ready;            // 8-bit pools: Q converted to f16 in place
+  uint64_t q_ready;            // int8 pools: Q converted to f16 in place
   uint64_t mma_drain;
   uint32_t tmem_base;
   int abort_flag;
@@ -95,115 +79,13 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemS = 256;   // S buffers at columns 256 and 320; O^T chunks at 0,64,128,192
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
-__device__ __forceinline__ bool bar_or(int id, int nthreads, bool pred) {
-  uint32_t r;
-  asm volatile(
-      "{\n\t.reg .pred p, q;\n\t"
-      "setp.ne.u32 q, %1, 0;\n\t"
-      "bar.red.or.pred p, %2, %3, q;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(r)
-      : "r"(static_cast<uint32_t>(pred)), "r"(id), "r"(nthreads)
-      : "memory");
-  return r != 0;
-}
-
-// Bounded wait that ignores the abort flag: used only to drain work already in flight.
-__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
-  const unsigned long long t0 = global_timer_ns();
-  while (!mbar_try_wait(bar, parity)) {
-    if (global_timer_ns() - t0 > kWaitLimitNs) return;
-  }
-}
-
-// Four e4m3 codes (bytes of w) -> four f16 holding the codes' values times 2^-8, exactly,
-// with integer ops only.  An e4m3 code s.eeee.mmm moved to f16 bit positions s.0eeee.mmm0000000
-// reads as the same significand with exponent bias 15 instead of 7, i.e. the value times
-// 2^-8; e4m3 subnormals land on f16 subnormals with the same factor.  (The finite e4m3 range,
-// |v| <= 448, becomes |v| <= 1.75.)  The kernel folds 2^8 back into the softmax and output
-// scales.
-__device__ __forceinline__ void e4m3x4_to_f16x4_scaled(uint32_t w, uint32_t& lo, uint32_t& hi) {
-  const uint32_t h0 = __byte_perm(w, 0u, 0x1404);  // code 0 in bits 8-15, code 1 in bits 24-31
-  const uint32_t h1 = __byte_perm(w, 0u, 0x3424);  // codes 2 and 3
-  lo = (h0 & 0x80008000u) | ((h0 >> 1) & 0x3F803F80u);
-  hi = (h1 & 0x80008000u) | ((h1 >> 1) & 0x3F803F80u);
-}
-
-// The same four codes through the conversion unit (cvt e4m3x2 -> f16x2, exact), scaled by
-// 2^-8 on the FMA pipe (exact: a power of two, and every result stays an f16 value).  The
-// dequant warps decode half of each chunk this way and half with the integer ops above, so
-// that the conversion and integer pipes share the work.
-__device__ __forceinline__ void e4m3x4_to_f16x4_scaled_cvt(uint32_t w, uint32_t& lo, uint32_t& hi) {
-  uint32_t a, b;
-  asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
-      "cvt.rn.f16x2.e4m3x2 %0, l;\n\tcvt.rn.f16x2.e4m3x2 %1, h;\n\t}"
-      : "=r"(a), "=r"(b)
-      : "r"(w));
-  const __half2 k = __half2half2(__ushort_as_half(0x1C00));  // 2^-8
-  const __half2 ra = __hmul2(*reinterpret_cast<const __half2*>(&a), k);
-  const __half2 rb = __hmul2(*reinterpret_cast<const __half2*>(&b), k);
-  lo = *reinterpret_cast<const uint32_t*>(&ra);
-  hi = *reinterpret_cast<const uint32_t*>(&rb);
-}
-
-// Two bf16 -> two f16, round to nearest (exact for magnitudes in f16's normal range).
-__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t v) {
-  return pack_f16x2(__uint_as_float(v << 16), __uint_as_float(v & 0xFFFF0000u));
-}
-
-// Decode 16 e4m3 codes (one 16-byte chunk of a row: 16 consecutive columns) into two 16-byte
-// f16 chunks (values times 2^-8) of a 128-byte-swizzled row.  rbase: shared address of the
-// row's 128-byte line plus 32 bytes per chunk index (chunk pair 2m, 2m+1 of the row);
-// sw: the row's swizzle (row mod 8, times 16).  Half of the codes go through the conversion
-// unit, half through the integer path, so that both pipes share the work.
-__device__ __forceinline__ void store_f16_chunk(uint32_t rbase, int sw, uint4 w) {
-  uint32_t o[8];
-  e4m3x4_to_f16x4_scaled_cvt(w.x, o[0], o[1]);
-  e4m3x4_to_f16x4_scaled_cvt(w.y, o[2], o[3]);
-  e4m3x4_to_f16x4_scaled(w.z, o[4], o[5]);
-  e4m3x4_to_f16x4_scaled(w.w, o[6], o[7]);
-  // the chunk pair sits at byte offsets 32m and 32m + 16 of the unswizzled row; rbase
-  // already holds row base + 32m
-  const uint32_t row0 = rbase & ~127u;
-  const uint32_t c0 = (rbase & 127u);
-  st_shared_v4(row0 + (c0 ^ sw), o[0], o[1], o[2], o[3]);
-  st_shared_v4(row0 + ((c0 + 16) ^ sw), o[4], o[5], o[6], o[7]);
-}
-
-// Four int8 codes (bytes of w) -> four f16 holding the codes' values exactly: the top bit
-// of each byte is flipped (code + 128 as an unsigned byte u), u is placed under the f16
-// pattern 0x64 (the value 1024 + u, exact since u < 1024) by two byte permutes, and 1152
-// is subtracted in f16 (exact: the result is a small integer).
-__device__ __forceinline__ void int8x4_to_f16x4(uint32_t w, uint32_t& lo, uint32_t& hi) {
-  const uint32_t x = w ^ 0x80808080u;
-  uint32_t a, b;
-  asm("prmt.b32 %0, %1, %2, 0x5140;" : "=r"(a) : "r"(x), "r"(0x64646464u));
-  asm("prmt.b32 %0, %1, %2, 0x7362;" : "=r"(b) : "r"(x), "r"(0x64646464u));
-  asm("sub.f16x2 %0, %1, %2;" : "=r"(lo) : "r"(a), "r"(0x64806480u));
-  asm("sub.f16x2 %0, %1, %2;" : "=r"(hi) : "r"(b), "r"(0x64806480u));
-}
-
-// Sixteen int8 codes -> sixteen f16 stored like store_f16_chunk.
-__device__ __forceinline__ void store_f16_chunk_int8(uint32_t rbase, int sw, uint4 w) {
-  uint32_t o[8];
-  int8x4_to_f16x4(w.x, o[0], o[1]);
-  int8x4_to_f16x4(w.y, o[2], o[3]);
-  int8x4_to_f16x4(w.z, o[4], o[5]);
-  int8x4_to_f16x4(w.w, o[6], o[7]);
-  const uint32_t row0 = rbase & ~127u;
-  const uint32_t c0 = (rbase & 127u);
-  st_shared_v4(row0 + (c0 ^ sw), o[0], o[1], o[2], o[3]);
-  st_shared_v4(row0 + ((c0 + 16) ^ sw), o[4], o[5], o[6], o[7]);
-}
-
-
-// kKv: pool format (kKvBf16, kKvE4m3, kKvInt8).  The two 8-bit formats share one path
-// (kFp8 below: decode warps, f16 GEMMs) and differ only in the byte -> f16 step.
+// kKv: pool format (kKvBf16 or kKvInt8; kInt8 below selects the decode warps and f16
+// GEMMs of the int8 path).
 template <int kKv>
 __global__ void __launch_bounds__(threads_for(kKv != kKvBf16), 1)
 decode_partial_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kv,
                       const DecodeParams p) {
-  constexpr bool kFp8 = kKv != kKvBf16;  // an 8-bit pool (e4m3 or int8)
+  constexpr bool kInt8 = kKv == kKvInt8;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   DecodeCtrl* ctrl = reinterpret_cast<DecodeCtrl*>(smem + kOffCtrl);
@@ -222,7 +104,7 @@ decode_partial_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
     tma_prefetch_desc(&tm_q);
     mbar_init(&ctrl->q_full, 1);
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(&ctrl->kv_full[s], kFp8 ? kDequantThreads : 1);
+      mbar_init(&ctrl->kv_full[s], kInt8 ? kDequantThreads : 1);
       mbar_init(&ctrl->kv_empty[s], 1);
     }
     for (int i = 0; i < 2; ++i) {
@@ -241,7 +123,7 @@ decode_partial_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
     tmem_alloc(&ctrl->tmem_base, kTmemCols);
     tmem_relinquish();
   }
-  if (warp == 4 && lane == 0 && !kFp8) tma_prefetch_desc(&tm_kv);
+  if (warp == 4 && lane == 0 && !kInt8) tma_prefetch_desc(&tm_kv);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -269,7 +151,7 @@ decode_partial_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
   }
   volatile int* abort_flag = &ctrl->abort_flag;
 
-  if (warp == 4 && !kFp8) {
+  if (warp == 4 && !kInt8) {
     // ------------------------------------------------------------------ producer (bf16)
     const int P = p.page_size;
     const int sub = P < kTileKeys ? kTileKeys / P : 1;  // pages per tile
@@ -354,9 +236,9 @@ decode_partial_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
   } else if (warp == 5) {
     // ------------------------------------------------------------------ MMA issuer (whole warp,
     // uniform control flow; one elected thread issues each GEMM's MMAs and their commit)
-    // the 8-bit path multiplies f16 operands (Q converted once, K/V decoded to f16, P in f16)
-    const uint32_t idesc1 = kFp8 ? make_idesc_f16(64, 64, false, false) : make_idesc_bf16(64, 64, false, false);
-    const uint32_t idesc2 = kFp8 ? make_idesc_f16(128, nq, true, false) : make_idesc_bf16(128, nq, true, false);
+    // the int8 path multiplies f16 operands (Q converted once, K/V decoded to f16, P in f16)
+    const uint32_t idesc1 = kInt8 ? make_idesc_f16(64, 64, false, false) : make_idesc_bf16(64, 64, false, false);
+    const uint32_t idesc2 = kInt8 ? make_idesc_f16(128, nq, true, false) : make_idesc_bf16(128, nq, true, false);
     // Descriptors are built once; each MMA advances the start-address field by a
     // compile-time offset (addresses stay below 256 KB, so no carry leaves the field).
     const uint64_t q_desc = make_smem_desc(smem_u32(smem + kOffQ), 16, 1024);
@@ -366,7 +248,7 @@ decode_partial_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
       if (lane == 0) v = mbar_test_wait(bar, parity) ? 1u : 0u;
       return __shfl_sync(0xffffffffu, v, 0) != 0;
     };
-    // 8-bit pools: lanes < sub (pages per tile) prefetch their page of tile n1 + 1 + kPrefetchTiles
+    // int8 pools: lanes < sub (pages per tile) prefetch their page of tile n1 + 1 + kPrefetchTiles
     // into L2 each time BMM1(n1) is issued, with the page id looked up one BMM1 earlier.
     const int P = p.page_size;
     const int sub = P < kTileKeys ? kTileKeys / P : 1;
@@ -384,7 +266,7 @@ decode_partial_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
                        static_cast<uint32_t>(rows * kLatentDim));
     };
     int pf_pid = -1;
-    if (kFp8) {
+    if (kInt8) {
       for (int jt = 1; jt <= kPrefetchTiles; ++jt) {
         const int pg = page_of(jt);
         if (pg >= 0) prefetch(jt, __ldg(pt + pg));
@@ -393,7 +275,7 @@ decode_partial_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
       pf_pid = (pg >= 0) ? __ldg(pt + pg) : -1;
       __syncwarp();
     }
-    bool ok = kFp8 ? mbar_wait(&ctrl->q_ready, 0, abort_flag) : mbar_wait(&ctrl->q_full, 0, abort_flag);
+    bool ok = kInt8 ? mbar_wait(&ctrl->q_ready, 0, abort_flag) : mbar_wait(&ctrl->q_full, 0, abort_flag);
     ok = __all_sync(0xffffffffu, ok);
     // Issue whichever GEMM is ready: BMM2(n2) first (it frees a stage), else BMM1(n1) for a
     // tile whose data has landed and whose S buffer is free.  BMM1 runs at most two tiles
@@ -444,7 +326,7 @@ decode_partial_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
             umma_commit(&ctrl->s_full[sb]);
           }
           __syncwarp();
-          if (kFp8) {
+          if (kInt8) {
             prefetch(n1 + 1 + kPrefetchTiles, pf_pid);
             const int pg = page_of(n1 + 2 + kPrefetchTiles);
             pf_pid = (pg >= 0) ? __ldg(pt + pg) : -1;
@@ -478,9 +360,9 @@ decode_partial_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
       drain_wait(&ctrl->mma_drain, 0);
     }
     __syncwarp();
-  } else if (kFp8 && warp >= 4) {
-    // ------------------------------------------------------------------ 8-bit dequant (warps 4, 6, 7):
-    // Q to f16 in place once; then, per tile, each lane reads its rows' e4m3 / int8 bytes straight
+  } else if (kInt8 && warp >= 4) {
+    // ------------------------------------------------------------------ int8 dequant (warps 4, 6, 7):
+    // Q to f16 in place once; then, per tile, each lane reads its rows' int8 bytes straight
     // from the page pool into registers (issued before waiting for the stage, so the reads
     // overlap the previous tile's GEMMs), waits for the stage, and writes them as f16 into
     // the swizzled tile.  Lane dl of decode warp dw (0..2) owns rows dl/4 + 8i (i < 8) and
@@ -557,12 +439,7 @@ decode_partial_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
         const uint32_t rbase = st + row * 128;
         const int sw = (row & 7) << 4;
 #pragma unroll
-        for (int m = 0; m < 3; ++m) {
-          if constexpr (kKv == kKvInt8)
-            store_f16_chunk_int8(rbase + (dw + 3 * m) * kBlockBytes, sw, w[m][i]);
-          else
-            store_f16_chunk(rbase + (dw + 3 * m) * kBlockBytes, sw, w[m][i]);
-        }
+        for (int m = 0; m < 3; ++m) store_f16_chunk_int8(rbase + (dw + 3 * m) * kBlockBytes, sw, w[m][i]);
       }
       fence_proxy_async_smem();
       mbar_arrive(&ctrl->kv_full[s]);
@@ -584,11 +461,9 @@ decode_partial_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
     float m_used = -INFINITY;
     float l_sum = 0.f;
     bool failed = false;
-    // e4m3 tiles are decoded as values times 2^-8 (exact); the factor returns here (int8
-    // codes are decoded to their exact values)
-    constexpr float kDecodeFactor = (kKv == kKvE4m3) ? 256.f : 1.f;
-    const float scale_log2 = p.scale_log2 * kDecodeFactor;
-    const float v_scale = p.v_scale * kDecodeFactor;
+    // (int8 codes are decoded to their exact values: the scales apply as they are)
+    const float scale_log2 = p.scale_log2;
+    const float v_scale = p.v_scale;
 
     for (int j = 0; j < ntiles; ++j) {
       const int sb = j & 1;
@@ -607,8 +482,8 @@ decode_partial_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
         mbar_arrive(&ctrl->s_free[sb]);
         // keys i <= lim of this lane's 32-key half are visible
         const int lim = row_active ? (min(kv_end - 1, lim_abs) - k0 - 32 * half) : -1;
-        // the 8-bit path multiplies P in f16 (P <= 2^8 here, where f16 keeps more bits than bf16)
-        online_softmax_step<32, true, kFp8>(sr, lim, scale_log2, kRescaleThreshold, m_used, l_sum, packed, alpha,
+        // the int8 path multiplies P in f16 (P <= 2^8 here, where f16 keeps more bits than bf16)
+        online_softmax_step<32, true, kInt8>(sr, lim, scale_log2, kRescaleThreshold, m_used, l_sum, packed, alpha,
                                             need_rescale);
       }
       if (!fail && j >= 1) {
@@ -634,7 +509,7 @@ decode_partial_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
         failed = true;
         break;
       }
-      if (!kFp8) {
+      if (!kInt8) {
         // zero value rows past the request's end in the last tile (stale or unloaded rows
         // would otherwise meet P = 0 in BMM2 and could carry NaN/Inf bit patterns)
         const int valid_rows = L - k0;
@@ -917,7 +792,7 @@ cudaError_t launch_partial_impl(const DecodeParams& p, const CUtensorMap& tm_q, 
 cudaError_t launch_decode_partial(const DecodeParams& p, const CUtensorMap& tm_q, const CUtensorMap& tm_kv,
                                   int head_groups, cudaStream_t stream) {
   switch (p.kv_dtype) {
-    case kKvE4m3: return launch_partial_impl<kKvE4m3>(p, tm_q, tm_kv, head_groups, stream);
+    case kKvE4m3: return launch_decode_partial_e4m3(p, tm_q, tm_kv, head_groups, stream);
     case kKvInt8: return launch_partial_impl<kKvInt8>(p, tm_q, tm_kv, head_groups, stream);
     default: return launch_partial_impl<kKvBf16>(p, tm_q, tm_kv, head_groups, stream);
   }

@@ -57,6 +57,9 @@ struct PrefillParams {
 // Decode: split-KV partial kernel (tensor maps over q and the latent pool).
 cudaError_t launch_decode_partial(const DecodeParams& p, const CUtensorMap& tm_q, const CUtensorMap& tm_kv,
                                   int head_groups, cudaStream_t stream);
+// Decode over an e4m3 pool: the split-KV partial kernel that runs BMM1 on the raw codes.
+cudaError_t launch_decode_partial_e4m3(const DecodeParams& p, const CUtensorMap& tm_q, const CUtensorMap& tm_kv,
+                                       int head_groups, cudaStream_t stream);
 // Decode: LSE-merge of the split partials for requests with more than one split.
 cudaError_t launch_decode_combine(const DecodeParams& p, cudaStream_t stream);
 // Watchdog self-test kernel (a wait nothing satisfies; must time out and report).

@@ -84,26 +84,6 @@ constexpr uint32_t kTmemO = 0;
 constexpr uint32_t kTmemS = 128;
 constexpr float kRescaleThreshold = 8.0f;
 
-__device__ __forceinline__ bool bar_or(int id, int nthreads, bool pred) {
-  uint32_t r;
-  asm volatile(
-      "{\n\t.reg .pred p, q;\n\t"
-      "setp.ne.u32 q, %1, 0;\n\t"
-      "bar.red.or.pred p, %2, %3, q;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(r)
-      : "r"(static_cast<uint32_t>(pred)), "r"(id), "r"(nthreads)
-      : "memory");
-  return r != 0;
-}
-
-__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
-  const unsigned long long t0 = global_timer_ns();
-  while (!mbar_try_wait(bar, parity)) {
-    if (global_timer_ns() - t0 > kWaitLimitNs) return;
-  }
-}
-
 // D[tmem] (+)= A[tmem] * B[smem desc]: the A operand (M rows x 16 K elements, bf16 packed
 // two per 32-bit column, row = lane) is read from Tensor Memory.
 __device__ __forceinline__ void umma_ts_bf16(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,

@@ -14,12 +14,13 @@
 //  * The raw e4m3 tile (64 keys x 576 codes, 36 KB) arrives by TMA (64-byte swizzle) in a
 //    2-stage ring, its rows prefetched into L2 a few tiles earlier, and is the B operand of
 //    BMM1 as it is: BMM1 runs on 8-bit operands
-//    (kind::f8f6f4).  Q stays exact: each bf16 query row, scaled by a power of two 2^s that
-//    brings its largest element into [128, 256), is split into q_hi = e4m3(q 2^s) and
-//    q_lo = e4m3(q 2^s - q_hi), which together hold the bf16 value (an 8-bit significand
-//    in two 4-bit halves; only elements below 2^-2 of that scaled range, 2^-9 of the row's
-//    largest, can lose low bits to e4m3's subnormal floor).  S = (q_hi + q_lo) . k_code
-//    takes two passes of MMAs into one fp32 accumulator, and 2^-s returns in the softmax.
+//    (kind::f8f6f4).  Q keeps its bf16 value: each query row, scaled by a power of two 2^s
+//    that brings its largest element into [128, 256), is split into q_hi = e4m3(q 2^s) and
+//    q_lo = e4m3(q 2^s - q_hi), an 8-bit significand in two 4-bit halves.  This is exact
+//    for every element within 2^9 of the row's largest |q|; smaller elements fall under
+//    e4m3's subnormal floor (2^-9 at that scale) and carry an absolute error of at most
+//    2^-17 of the row's largest |q|.  S = (q_hi + q_lo) . k_code takes two passes of MMAs
+//    into one fp32 accumulator, and 2^-s returns in the softmax.
 //  * Only V (the first 512 columns) is decoded to f16 (exactly: codes times 2^-8), from the
 //    raw stage in shared memory into one f16 V stage, by the decode warps, while the
 //    tensor core runs BMM1 of the next tile on its raw stage.  BMM2 (O^T += V^T . P^T,

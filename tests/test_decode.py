@@ -191,6 +191,50 @@ def test_decode_absorbed_prefill_over_paged_prefix(mla, oracle_mod, kv, T, lens)
     _full_check(mla, oracle_mod, wl)
 
 
+def _wide_range_queries(seed, outlier):
+    wl = DecodeWorkload("wide_q", 2, 4, 16, [700, 1500], kv_dtype="e4m3", seed=91)
+    inp = make_decode_inputs(wl, "cpu")
+    g = torch.Generator().manual_seed(seed)
+    q = inp.q.float()
+    q = q * torch.pow(2.0, torch.randint(-16, 5, q.shape, generator=g).float())
+    q[0, 0, 0] = 0.0
+    q[0, 1, 3, 17] = outlier
+    inp.q = q.to(torch.bfloat16)
+    return inp
+
+
+def test_decode_e4m3_queries_over_many_binades(mla, oracle_mod):
+    """The e4m3 kernel splits each bf16 query row into two e4m3 parts under a per-row
+    power-of-two scale.  Rows whose elements span 2^-16 .. 2^4 of their typical size, an
+    all-zero row and a row with one element 1000x its neighbours: parity with the oracle
+    (on the same bf16 queries) within the usual bounds."""
+    inp = _wide_range_queries(5, 40.0)
+    out, lse, _ = run_gpu(mla, inp)
+    ref_out, ref_lse = oracle_mod.mla_decode(inp.q, inp.kv_pool, inp.page_table, inp.seq_lens, inp.scale,
+                                             kv_scale=inp.kv_scale)
+    check(out, lse, ref_out, ref_lse, fp8=True)
+
+
+def test_decode_e4m3_query_split_error_bound(mla, oracle_mod):
+    """The split is exact for elements within 2^9 of their row's largest |q|; smaller
+    elements carry an absolute error of at most 2^-17 of it (e4m3's subnormal floor under
+    the row scale).  A row with one element of 3e4 among elements near 1e-2 has scores in
+    the thousands: its log-sum-exp stays within scale * 2^-17 * max|q| * max_j sum_i |k_ji|
+    of the oracle's, every other row within 1e-3, and the outputs within the usual bounds."""
+    inp = _wide_range_queries(5, 3.0e4)
+    out, lse, _ = run_gpu(mla, inp)
+    ref_out, ref_lse = oracle_mod.mla_decode(inp.q, inp.kv_pool, inp.page_table, inp.seq_lens, inp.scale,
+                                             kv_scale=inp.kv_scale)
+    out = out.reshape(ref_out.shape)
+    lse = lse.reshape(ref_lse.shape)
+    rel = np.linalg.norm(out - ref_out) / np.linalg.norm(ref_out)
+    assert np.isfinite(out).all() and rel <= REL_L2 and np.abs(out - ref_out).max() <= MAX_ABS_FP8
+    keys = inp.kv_pool.view(torch.float8_e4m3fn).double().abs().sum(-1).max().item() * inp.kv_scale
+    qmax = inp.q.float().abs().amax(-1).double().numpy()
+    bound = np.maximum(inp.scale * 2.0 ** -17 * qmax * keys, LSE_ABS)
+    assert (np.abs(lse - ref_lse) <= bound).all()
+
+
 def test_decode_page_shuffle_invariance_bitwise(mla):
     wl = DecodeWorkload("shuffle", 2, 4, 16, [1500, 777], seed=5, extra_pages=7)
     inp = make_decode_inputs(wl, "cpu")

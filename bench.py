@@ -7,7 +7,8 @@ of latent KV, which exceeds L2, so every step streams its KV from HBM.  One step
 mla_decode call (plan cached; split-KV partial kernel + LSE combine kernel).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
-    python bench.py --profile-case <workload>     (three calls, for a profiler capture)
+    python bench.py --profile-case <workload>     (three calls, for a profiler capture;
+                                                   paged_p64:<prefill workload> for the paged prefill)
 
 Timing: `value` = KV bytes / time of one CUDA graph holding the K steps (no event nodes
 inside); the roofline's kernel time = one pair of CUDA events around a second graph of
@@ -15,7 +16,8 @@ back-to-back launches of the split-KV partial kernel alone (mla_decode_partial);
 wall clock of K end-to-end steps (one packed H2D copy of q / page table / lengths, the
 decode call, one packed D2H copy of out / lse, copies on their own streams) replayed from
 one graph.  The extra lines (the other decode workloads, the absorbed prefill over a paged
-prefix and the varlen prefill) are graph-timed the same way and printed last, compactly.
+prefix, the varlen prefill over a paged cache and over contiguous K/V) are graph-timed the
+same way and printed last, compactly.
 
 N > 1 runs under torchrun: every rank runs an independent replica (the path has no
 exchange step); value = all ranks' KV bytes / max-over-ranks time.
@@ -169,17 +171,27 @@ def measure_decode_extra(mla, name, dev, steps=200):
     return rec
 
 
-def measure_prefill(mla, dev, steps=10):
-    from mla_attention_paged_gb300.inputs import make_prefill_inputs, prefill_workloads
+def measure_prefill(mla, dev, steps=10, page_size=None):
+    """The varlen prefill line (5 requests, prefix 20K-100K, 256-2048 new tokens, 16 heads):
+    contiguous K/V, or (page_size given) the same K/V laid out in a shuffled paged cache and
+    read through the page table."""
+    from mla_attention_paged_gb300.inputs import make_prefill_inputs, page_prefill_kv, prefill_workloads
     wl = prefill_workloads()["prefill_b5_h16_prefix"]
     inp = make_prefill_inputs(wl, dev)
     out = torch.empty(inp.q.shape[0], wl.heads, 128, dtype=torch.bfloat16, device=dev)
     lse = torch.empty(inp.q.shape[0], wl.heads, dtype=torch.float32, device=dev)
     st = torch.cuda.Stream(device=dev)
+    if page_size:
+        pk = page_prefill_kv(inp, page_size, seed=wl.seed + 1)
+        inp.k = inp.v = None  # only the paged copy is read
 
-    def call(i=0):
-        mla.prefill_varlen(inp.q, inp.k, inp.v, inp.cu_seqlens_q, inp.cu_seqlens_kv, inp.prefix_lens,
-                           inp.max_seqlen_q, inp.scale, out=out, lse=lse, stream=st)
+        def call(i=0):
+            mla.prefill_paged(inp.q, pk.k_pages, pk.v_pages, pk.page_table, inp.cu_seqlens_q, pk.kv_lens,
+                              inp.max_seqlen_q, inp.scale, out=out, lse=lse, stream=st)
+    else:
+        def call(i=0):
+            mla.prefill_varlen(inp.q, inp.k, inp.v, inp.cu_seqlens_q, inp.cu_seqlens_kv, inp.prefix_lens,
+                               inp.max_seqlen_q, inp.scale, out=out, lse=lse, stream=st)
 
     with torch.cuda.stream(st):
         for _ in range(2):
@@ -385,7 +397,15 @@ def run_profile_case(name):
     from mla_attention_paged_gb300.inputs import make_prefill_inputs, prefill_workloads
     build.build()
     from mla_attention_paged_gb300 import mla
-    if name in prefill_workloads():
+    if name.startswith("paged_p64:") and name.split(":", 1)[1] in prefill_workloads():
+        from mla_attention_paged_gb300.inputs import page_prefill_kv
+        wl = prefill_workloads()[name.split(":", 1)[1]]
+        inp = make_prefill_inputs(wl, "cuda")
+        pk = page_prefill_kv(inp, 64, seed=wl.seed + 1)
+        for _ in range(3):
+            mla.prefill_paged(inp.q, pk.k_pages, pk.v_pages, pk.page_table, inp.cu_seqlens_q, pk.kv_lens,
+                              inp.max_seqlen_q, inp.scale)
+    elif name in prefill_workloads():
         inp = make_prefill_inputs(prefill_workloads()[name], "cuda")
         for _ in range(3):
             mla.prefill_varlen(inp.q, inp.k, inp.v, inp.cu_seqlens_q, inp.cu_seqlens_kv, inp.prefix_lens,
@@ -650,6 +670,8 @@ def main():
         for name in EXTRA_DECODE:
             extra[name] = measure_decode_extra(mla, name, dev)
             torch.cuda.empty_cache()
+        extra["prefill_paged_p64_b5_h16_prefix"] = measure_prefill(mla, dev, page_size=64)
+        torch.cuda.empty_cache()
         extra["prefill_b5_h16_prefix"] = measure_prefill(mla, dev)
         line["extra"] = extra
     if rank == 0:

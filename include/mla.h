@@ -29,7 +29,7 @@
  * Conventions shared by every call:
  *  - Every pointer argument that is not documented as host memory is DEVICE memory owned
  *    by the caller.  The library never allocates or frees device memory and never
- *    synchronises the stream in mla_decode / mla_prefill_varlen.
+ *    synchronises the stream in mla_decode / mla_prefill_varlen / mla_prefill_paged.
  *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
  *  - Tensors are dense and row-major (last index fastest), with the layouts given below.
  *  - Every call returns an mla_status_t code; no C++ exception crosses this ABI.
@@ -212,6 +212,34 @@ int mla_prefill_varlen(const void* q, const void* k, const void* v, const int32_
                        const int32_t* cu_seqlens_kv, const int32_t* prefix_lens, int batch,
                        int num_heads, int max_seqlen_q, int total_q, int total_kv, float scale,
                        void* out, float* lse, void* stream);
+
+/* The same prefill with K/V read from a paged cache of per-head k/v rows instead of
+ * contiguous per-request rows.  The TokenSpeed pages describe the prefill as "prefill with a
+ * long prefix KV cache" ([BLOG] "TokenSpeed 性能預覽"; [TALK] "Kernel：让 MLA 真正跑满 GPU",
+ * last paragraph) and keep KV in fixed-size blocks behind a table ([READ] "核心技术揭秘");
+ * this call reads both the cached prefix and the new tokens' k/v from such blocks.
+ *   q             : [total_q, H, 192] bf16; request b's n_b new tokens are rows
+ *                   cu_seqlens_q[b] .. cu_seqlens_q[b+1]-1.
+ *   k_pages       : [num_pages, page_size, H, 192] bf16.
+ *   v_pages       : [num_pages, page_size, H, 128] bf16.
+ *   page_table    : [batch, max_pages_per_seq] int32; key j of request b (prefix first,
+ *                   then its new tokens) is row j % page_size of page
+ *                   page_table[b, j / page_size] of k_pages / v_pages.
+ *   kv_lens       : [batch] int32 (device), p_b + n_b: the request's cached prefix plus
+ *                   its new tokens, whose k/v are the last n_b positions.
+ *   page_size     : 16, 32, 64, 128 or 256 tokens.
+ *   num_pages     : pages in each pool (num_pages * page_size < 2^31).
+ *   out, lse      : as mla_prefill_varlen: new token i of request b attends to keys
+ *                   0 .. p_b + i.
+ * Errors: MLA_ERR_INVALID_ARG, MLA_ERR_UNSUPPORTED (num_heads outside 1..256, another page
+ * size, too many pool rows), MLA_ERR_CUDA.  Device-side, recorded in the status word as
+ * MLA_ERR_DEVICE_ARG: n_b > max_seqlen_q, kv_lens[b] < n_b or beyond the table row, q rows
+ * beyond total_q (the request is skipped, before any access), and a page id outside
+ * [0, num_pages) (its rows are read as zeros, never from outside the pools). */
+int mla_prefill_paged(const void* q, const void* k_pages, const void* v_pages, const int32_t* page_table,
+                      const int32_t* cu_seqlens_q, const int32_t* kv_lens, int batch, int num_heads,
+                      int page_size, int max_pages_per_seq, int64_t num_pages, int max_seqlen_q,
+                      int total_q, float scale, void* out, float* lse, void* stream);
 
 /* Read and clear the current device's status word after synchronising `stream`.
  * Returns MLA_OK, MLA_ERR_TIMEOUT or MLA_ERR_DEVICE_ARG (first recorded), or

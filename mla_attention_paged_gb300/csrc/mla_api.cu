@@ -477,6 +477,75 @@ int mla_prefill_varlen(const void* q, const void* k, const void* v, const int32_
   return MLA_OK;
 }
 
+int mla_prefill_paged(const void* q, const void* k_pages, const void* v_pages, const int32_t* page_table,
+                      const int32_t* cu_seqlens_q, const int32_t* kv_lens, int batch, int num_heads, int page_size,
+                      int max_pages_per_seq, int64_t num_pages, int max_seqlen_q, int total_q, float scale,
+                      void* out, float* lse, void* stream) {
+  if (batch < 1 || batch > 65535 || max_seqlen_q < 0 || total_q < 0 || max_pages_per_seq < 1 || num_pages < 1)
+    return MLA_ERR_INVALID_ARG;
+  if (num_heads < 1 || num_heads > 256) return MLA_ERR_UNSUPPORTED;
+  if (page_size != 16 && page_size != 32 && page_size != 64 && page_size != 128 && page_size != 256)
+    return MLA_ERR_UNSUPPORTED;
+  if (num_pages * page_size >= (int64_t(1) << 31)) return MLA_ERR_UNSUPPORTED;  // TMA row coordinates are int32
+  if (!(scale > 0.f)) return MLA_ERR_INVALID_ARG;
+  if (total_q == 0 || max_seqlen_q == 0) return MLA_OK;  // no new tokens: nothing to compute
+  if (!q || !k_pages || !v_pages || !page_table || !cu_seqlens_q || !kv_lens || !out || !lse)
+    return MLA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k_pages, 16) || !aligned(v_pages, 16) || !aligned(out, 16) || !aligned(lse, 4))
+    return MLA_ERR_INVALID_ARG;
+  unsigned* status = status_ptr();
+  if (!status) return MLA_ERR_CUDA;
+  const uint64_t H = static_cast<uint64_t>(num_heads);
+  const uint64_t rows = static_cast<uint64_t>(num_pages) * page_size;
+  // The pools are [num_pages * page_size rows][H][192 | 128]: the same 4-D view as the
+  // contiguous prefill.  Pages of 128 or 256 keys take one box per 128-key tile; smaller
+  // pages one box per (page, 64-column block).
+  const uint32_t box_rows = static_cast<uint32_t>(page_size < 128 ? page_size : 128);
+  const bool whole = page_size >= 128;
+  CUtensorMap tm_q, tm_k, tm_v;
+  {
+    const uint64_t dims[4] = {64, static_cast<uint64_t>(total_q), 3, H};
+    const uint64_t strides[3] = {H * 192 * 2, 128, 192 * 2};
+    const uint32_t box[4] = {64, 128, 3, 1};
+    if (!make_map(&tm_q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, q, dims, strides, box)) return MLA_ERR_CUDA;
+  }
+  {
+    const uint64_t dims[4] = {64, rows, 3, H};
+    const uint64_t strides[3] = {H * 192 * 2, 128, 192 * 2};
+    const uint32_t box[4] = {64, box_rows, whole ? 3u : 1u, 1};
+    if (!make_map(&tm_k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, k_pages, dims, strides, box)) return MLA_ERR_CUDA;
+  }
+  {
+    const uint64_t dims[4] = {64, rows, 2, H};
+    const uint64_t strides[3] = {H * 128 * 2, 128, 128 * 2};
+    const uint32_t box[4] = {64, box_rows, whole ? 2u : 1u, 1};
+    if (!make_map(&tm_v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, v_pages, dims, strides, box)) return MLA_ERR_CUDA;
+  }
+  PrefillParams p;
+  memset(&p, 0, sizeof p);
+  p.B = batch;
+  p.H = num_heads;
+  p.max_q_blocks = (max_seqlen_q + 127) / 128;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.cu_q = cu_seqlens_q;
+  p.out = static_cast<__nv_bfloat16*>(out);
+  p.lse = lse;
+  p.max_seqlen_q = max_seqlen_q;
+  p.total_q = total_q;
+  p.total_kv = static_cast<int>(rows);
+  p.status = status;
+  p.page_table = page_table;
+  p.kv_lens = kv_lens;
+  p.page_size = page_size;
+  p.max_pages = max_pages_per_seq;
+  p.num_pages = num_pages;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (g_prof_start && record_event(g_prof_start, s) != cudaSuccess) return MLA_ERR_CUDA;
+  if (launch_prefill(p, tm_q, tm_k, tm_v, s) != cudaSuccess) return MLA_ERR_CUDA;
+  if (g_prof_stop && record_event(g_prof_stop, s) != cudaSuccess) return MLA_ERR_CUDA;
+  return MLA_OK;
+}
+
 int mla_set_profile_events(void* start_event, void* stop_event) {
   g_prof_start = static_cast<cudaEvent_t>(start_event);
   g_prof_stop = static_cast<cudaEvent_t>(stop_event);

@@ -52,6 +52,12 @@ struct PrefillParams {
   float* lse;                   // [total_q, H]
   int total_q, total_kv;        // rows of q/out/lse and of k/v
   unsigned* status;
+  // paged K/V (page_table non-null): row j of request b is row j % page_size of page
+  // page_table[b * max_pages + j / page_size]; kv_lens[b] = prefix + new tokens
+  const int32_t* page_table;
+  const int32_t* kv_lens;
+  int page_size, max_pages;
+  int64_t num_pages;
 };
 
 // Decode: split-KV partial kernel (tensor maps over q and the latent pool).
@@ -64,7 +70,7 @@ cudaError_t launch_decode_partial_e4m3(const DecodeParams& p, const CUtensorMap&
 cudaError_t launch_decode_combine(const DecodeParams& p, cudaStream_t stream);
 // Watchdog self-test kernel (a wait nothing satisfies; must time out and report).
 cudaError_t launch_selftest_timeout(unsigned* status, cudaStream_t stream);
-// Prefill: ragged causal prefill with prefix offset.
+// Prefill: ragged causal prefill with prefix offset (contiguous or paged K/V, by p.page_table).
 cudaError_t launch_prefill(const PrefillParams& p, const CUtensorMap& tm_q, const CUtensorMap& tm_k,
                            const CUtensorMap& tm_v, cudaStream_t stream);
 

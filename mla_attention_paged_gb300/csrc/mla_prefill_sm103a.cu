@@ -1,5 +1,6 @@
 // mla_prefill_sm103a.cu -- ragged (no padding) causal MLA prefill on top of a cached
-// prefix, sm_103a.
+// prefix, sm_103a.  K/V come either as contiguous per-request rows or from a paged cache
+// (per-head k/v pages behind a page table; the same kernel, a different producer).
 //
 // What it computes: request b has p_b cached prefix tokens followed by n_b new tokens; for
 // new token i and head h,
@@ -96,6 +97,9 @@ __device__ __forceinline__ void umma_ts_bf16(uint32_t d_tmem, uint32_t a_tmem, u
       : "memory");
 }
 
+// kPaged: K/V rows of request b come from a paged cache (row j of the request is row j % P
+// of page page_table[b][j / P] of the pools) instead of contiguous rows at cu_kv[b].
+template <bool kPaged>
 __global__ void __launch_bounds__(kThreads, 1)
 prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const PrefillParams p) {
@@ -115,10 +119,10 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
   if (p.B <= kThreads) {
     if (threadIdx.x < p.B) {
       const int t = threadIdx.x;
-      const int len_t = p.cu_kv[t + 1] - p.cu_kv[t];
+      const int len_t = kPaged ? p.kv_lens[t] : p.cu_kv[t + 1] - p.cu_kv[t];
       int rank = 0;
       for (int u = 0; u < p.B; ++u) {
-        const int len_u = p.cu_kv[u + 1] - p.cu_kv[u];
+        const int len_u = kPaged ? p.kv_lens[u] : p.cu_kv[u + 1] - p.cu_kv[u];
         rank += (len_u > len_t || (len_u == len_t && u < t)) ? 1 : 0;
       }
       if (rank == static_cast<int>(blockIdx.z)) s_req = t;
@@ -130,15 +134,17 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
 
   const int q_start = p.cu_q[b];
   const int n_b = p.cu_q[b + 1] - q_start;
-  const int kv_start = p.cu_kv[b];
-  const int kv_total = p.cu_kv[b + 1] - kv_start;
-  const int pre = p.prefix_lens[b];
   // Device-side argument checks, before any load or store: the request's rows lie inside
-  // q/out/lse and k/v, its kv length is prefix + new tokens, and its new tokens fit the
-  // grid the host sized from max_seqlen_q (rows beyond it would be left unwritten).
+  // q/out/lse and k/v (paged: its length fits its page-table row), its kv length is prefix
+  // + new tokens, and its new tokens fit the grid the host sized from max_seqlen_q (rows
+  // beyond it would be left unwritten).
+  const int kv_start = kPaged ? 0 : p.cu_kv[b];
+  const int kv_total = kPaged ? p.kv_lens[b] : p.cu_kv[b + 1] - kv_start;
+  const int pre = kPaged ? kv_total - n_b : p.prefix_lens[b];
   const bool bad = n_b < 0 || pre < 0 || kv_total != pre + n_b || n_b > p.max_seqlen_q || q_start < 0 ||
                    kv_start < 0 || static_cast<int64_t>(q_start) + n_b > p.total_q ||
-                   static_cast<int64_t>(kv_start) + kv_total > p.total_kv;
+                   (kPaged ? static_cast<int64_t>(kv_total) > static_cast<int64_t>(p.max_pages) * p.page_size
+                           : static_cast<int64_t>(kv_start) + kv_total > p.total_kv);
   if (bad) {
     if (threadIdx.x == 0 && qb == 0 && h == 0) atomicOr(p.status, kStatusDeviceArg);
     return;
@@ -185,36 +191,117 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
 
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------------ TMA producer
-    // lane 0 streams the K ring, lane 1 the V ring (independent waits in divergent lanes)
-    if (lane < 2) {
-      const bool is_k = lane == 0;
+    // contiguous K/V: lane 0 streams the K ring, lane 1 the V ring (independent waits in
+    // divergent lanes)
+    if constexpr (!kPaged) {
+      if (lane < 2) {
+        const bool is_k = lane == 0;
+        const uint64_t pol_kv = policy_evict_last();  // re-read by the other query blocks of this head
+        if (is_k) {
+          mbar_arrive_expect_tx(&ctrl->q_full, kQBytes);
+          // one box: 128 rows x all three 64-column blocks of head h
+          tma_load_4d(smem + kOffQ, &tm_q, &ctrl->q_full, 0, q_start + row_begin, 0, h, policy_evict_first());
+        }
+        uint64_t* full = is_k ? ctrl->k_full : ctrl->v_full;
+        uint64_t* empty = is_k ? ctrl->k_empty : ctrl->v_empty;
+        int last_issued[kStages] = {-1, -1};
+        bool ok = true;
+        for (int j = 0; j < ntiles; ++j) {
+          const int s = j % kStages;
+          if (j >= kStages) {
+            ok = mbar_wait(&empty[s], ((j / kStages) - 1) & 1, abort_flag);
+            if (!ok) break;
+          }
+          const int row = kv_start + j * kBN;
+          if (is_k) {
+            mbar_arrive_expect_tx(&full[s], kKBytes);
+            tma_load_4d(smem + kOffK + s * kKBytes, &tm_k, &full[s], 0, row, 0, h, pol_kv);  // 128 rows x 3 blocks
+          } else {
+            mbar_arrive_expect_tx(&full[s], kVBytes);
+            tma_load_4d(smem + kOffV + s * kVBytes, &tm_v, &full[s], 0, row, 0, h, pol_kv);  // 128 rows x 2 blocks
+          }
+          last_issued[s] = j;
+        }
+        if (!ok) {
+          if (is_k) drain_wait(&ctrl->q_full, 0);
+          for (int s = 0; s < kStages; ++s)
+            if (last_issued[s] >= 0) drain_wait(&full[s], (last_issued[s] / kStages) & 1);
+        }
+      }
+    } else {
+      // Paged: lanes 0-15 stream the K ring, lanes 16-31 the V ring.  A tile of 128 keys is
+      // one box per operand when a page holds 128 or 256 keys, else one box per (page,
+      // 64-column block) of its 128 / P pages; the group's lanes take those boxes round-robin,
+      // so that they are issued in parallel.  The group's first lane waits for the stage and
+      // arms its barrier.  Page ids of the next tile are read before that wait.  An id
+      // outside the pool, or a page past the request's end, becomes -1: its boxes lie before
+      // the first row and TMA fills them with zeros (an id outside the pool is reported).
+      const bool is_k = lane < 16;
+      const int gl = lane & 15;
+      const int leader = is_k ? 0 : 16;
+      const unsigned gmask = is_k ? 0x0000FFFFu : 0xFFFF0000u;
       const uint64_t pol_kv = policy_evict_last();  // re-read by the other query blocks of this head
-      if (is_k) {
+      if (lane == 0) {
         mbar_arrive_expect_tx(&ctrl->q_full, kQBytes);
-        // one box: 128 rows x all three 64-column blocks of head h
         tma_load_4d(smem + kOffQ, &tm_q, &ctrl->q_full, 0, q_start + row_begin, 0, h, policy_evict_first());
       }
       uint64_t* full = is_k ? ctrl->k_full : ctrl->v_full;
       uint64_t* empty = is_k ? ctrl->k_empty : ctrl->v_empty;
+      const int P = p.page_size;
+      const int npt = P >= kBN ? 1 : kBN / P;          // pages per tile: 1, 2, 4 or 8
+      const int nblk = is_k ? kDqk / 64 : kDv / 64;     // boxes per page when P < 128
+      const int nbox = P >= kBN ? 1 : npt * nblk;       // boxes per tile: at most 24, two per lane
+      const int pages_b = (kv_total + P - 1) / P;
+      const int32_t* pt = p.page_table + static_cast<int64_t>(b) * p.max_pages;
+      const unsigned n_pages = static_cast<unsigned>(min(p.num_pages, static_cast<int64_t>(0x7fffffff)));
+      bool bad_pid = false;
+      auto page_id = [&](int jt, int bx) -> int {  // page of box bx of tile jt, or -1
+        const int pg = jt * kBN / P + (P >= kBN ? 0 : bx / nblk);
+        int v = -1;
+        if (bx < nbox && jt < ntiles && pg < pages_b) {
+          v = __ldg(pt + pg);
+          if (static_cast<unsigned>(v) >= n_pages) {
+            bad_pid = true;
+            v = -1;
+          }
+        }
+        return v;
+      };
+      const CUtensorMap* map = is_k ? &tm_k : &tm_v;
       int last_issued[kStages] = {-1, -1};
       bool ok = true;
+      int cur0 = page_id(0, gl), cur1 = page_id(0, gl + 16);
       for (int j = 0; j < ntiles; ++j) {
         const int s = j % kStages;
+        const int nxt0 = page_id(j + 1, gl), nxt1 = page_id(j + 1, gl + 16);
         if (j >= kStages) {
-          ok = mbar_wait(&empty[s], ((j / kStages) - 1) & 1, abort_flag);
+          bool w = true;
+          if (gl == 0) w = mbar_wait(&empty[s], ((j / kStages) - 1) & 1, abort_flag);
+          ok = __shfl_sync(gmask, w, leader);
           if (!ok) break;
         }
-        const int row = kv_start + j * kBN;
-        if (is_k) {
-          mbar_arrive_expect_tx(&full[s], kKBytes);
-          tma_load_4d(smem + kOffK + s * kKBytes, &tm_k, &full[s], 0, row, 0, h, pol_kv);  // 128 rows x 3 blocks
+        uint8_t* dst = smem + (is_k ? kOffK + s * kKBytes : kOffV + s * kVBytes);
+        if (gl == 0) mbar_arrive_expect_tx(&full[s], is_k ? kKBytes : kVBytes);
+        __syncwarp(gmask);  // the barrier is armed before any of the group's copies can land
+        if (P >= kBN) {
+          if (gl == 0) tma_load_4d(dst, map, &full[s], 0, cur0 * P + (j * kBN) % P, 0, h, pol_kv);
         } else {
-          mbar_arrive_expect_tx(&full[s], kVBytes);
-          tma_load_4d(smem + kOffV + s * kVBytes, &tm_v, &full[s], 0, row, 0, h, pol_kv);  // 128 rows x 2 blocks
+#pragma unroll
+          for (int k = 0; k < 2; ++k) {
+            const int bx = gl + 16 * k;
+            if (bx < nbox) {
+              const int pp = bx / nblk, blk = bx % nblk;
+              tma_load_4d(dst + blk * kKVBlockBytes + pp * P * 128, map, &full[s], 0, (k ? cur1 : cur0) * P, blk, h,
+                          pol_kv);
+            }
+          }
         }
         last_issued[s] = j;
+        cur0 = nxt0;
+        cur1 = nxt1;
       }
-      if (!ok) {
+      if (__any_sync(gmask, bad_pid) && gl == 0) atomicOr(p.status, kStatusDeviceArg);
+      if (!ok && gl == 0) {
         if (is_k) drain_wait(&ctrl->q_full, 0);
         for (int s = 0; s < kStages; ++s)
           if (last_issued[s] >= 0) drain_wait(&full[s], (last_issued[s] / kStages) & 1);
@@ -456,18 +543,24 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
 
 cudaError_t launch_prefill(const PrefillParams& p, const CUtensorMap& tm_q, const CUtensorMap& tm_k,
                            const CUtensorMap& tm_v, cudaStream_t stream) {
-  static thread_local int configured_device = -1;
+  // the shared-memory limit is a per-device attribute: set it once per device, thread and instance
+  static thread_local int configured_device[2] = {-1, -1};
+  const bool paged = p.page_table != nullptr;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (configured_device != dev) {
-    e = cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (configured_device[paged] != dev) {
+    e = paged ? cudaFuncSetAttribute(prefill_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes)
+              : cudaFuncSetAttribute(prefill_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return e;
-    configured_device = dev;
+    configured_device[paged] = dev;
   }
   if (p.max_q_blocks < 1) return cudaSuccess;
   dim3 grid(p.max_q_blocks, p.H, p.B);
-  prefill_kernel<<<grid, kThreads, kSmemBytes, stream>>>(tm_q, tm_k, tm_v, p);
+  if (paged)
+    prefill_kernel<true><<<grid, kThreads, kSmemBytes, stream>>>(tm_q, tm_k, tm_v, p);
+  else
+    prefill_kernel<false><<<grid, kThreads, kSmemBytes, stream>>>(tm_q, tm_k, tm_v, p);
   return cudaGetLastError();
 }
 

@@ -228,3 +228,44 @@ def make_prefill_inputs(wl: PrefillWorkload, device="cpu") -> PrefillInputs:
                          torch.tensor(wl.prefix_lens, dtype=torch.int32, device=dev),
                          max(wl.new_lens) if wl.new_lens else 0,
                          1.0 / math.sqrt(D_QK_PREFILL), wl)
+
+
+@dataclass
+class PagedKV:
+    k_pages: torch.Tensor      # [num_pages, page_size, H, 192] bf16
+    v_pages: torch.Tensor      # [num_pages, page_size, H, 128] bf16
+    page_table: torch.Tensor   # [B, max_pages] int32
+    kv_lens: torch.Tensor      # [B] int32: prefix + new tokens
+
+
+def page_prefill_kv(inp: PrefillInputs, page_size: int, seed: int, extra_pages: int = 0) -> PagedKV:
+    """Lay a prefill batch's contiguous per-request K/V rows out in a paged cache (layout
+    only): request b's p_b + n_b rows fill ceil((p_b + n_b) / page_size) pages taken from
+    one shared pool in a random permutation; the rest of each request's last page and
+    ``extra_pages`` unused pages hold random values."""
+    dev = inp.k.device
+    g = torch.Generator(device=dev).manual_seed(seed)
+    H = inp.k.shape[1]
+    P = page_size
+    cu = [int(x) for x in inp.cu_seqlens_kv.cpu()]
+    lens = [cu[b + 1] - cu[b] for b in range(len(cu) - 1)]
+    pages_per = [(L + P - 1) // P for L in lens]
+    n_pages = sum(pages_per) + extra_pages
+    mp = max(1, max(pages_per))
+    k_pages = torch.randn(n_pages, P, H, D_QK_PREFILL, generator=g, device=dev).to(torch.bfloat16)
+    v_pages = torch.randn(n_pages, P, H, D_V_PREFILL, generator=g, device=dev).to(torch.bfloat16)
+    perm = torch.randperm(n_pages, generator=g, device=dev).to(torch.int32)
+    page_table = torch.zeros(len(lens), mp, dtype=torch.int32, device=dev)
+    kf = k_pages.view(n_pages * P, H, D_QK_PREFILL)
+    vf = v_pages.view(n_pages * P, H, D_V_PREFILL)
+    off = 0
+    for b, (L, n) in enumerate(zip(lens, pages_per)):
+        page_table[b, :n] = perm[off:off + n]
+        off += n
+        if L == 0:
+            continue
+        j = torch.arange(L, device=dev)
+        dst = page_table[b, j // P].long() * P + j % P
+        kf[dst] = inp.k[cu[b]:cu[b + 1]]
+        vf[dst] = inp.v[cu[b]:cu[b + 1]]
+    return PagedKV(k_pages, v_pages, page_table, torch.tensor(lens, dtype=torch.int32, device=dev))

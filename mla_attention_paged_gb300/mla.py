@@ -27,7 +27,7 @@ MLA_KV_INT8 = 2
 
 # Every function include/mla.h declares; each is given its C signature in _load().
 EXPORTED = ["mla_decode_plan", "mla_decode", "mla_decode_partial", "mla_decode_combine", "mla_decode_noalloc",
-            "mla_prefill_varlen", "mla_get_status", "mla_status_string", "mla_version", "mla_set_profile_events",
+            "mla_prefill_varlen", "mla_prefill_paged", "mla_get_status", "mla_status_string", "mla_version", "mla_set_profile_events",
             "mla_profile_elapsed_ms", "mla_selftest_wait_timeout"]
 
 
@@ -66,6 +66,8 @@ def _load() -> ctypes.CDLL:
     lib.mla_decode_combine.argtypes = [ctypes.POINTER(DecodePlan), P, i32, i32, P, P, P, sz, P]
     lib.mla_prefill_varlen.restype = i32
     lib.mla_prefill_varlen.argtypes = [P, P, P, P, P, P, i32, i32, i32, i32, i32, f32, P, P, P]
+    lib.mla_prefill_paged.restype = i32
+    lib.mla_prefill_paged.argtypes = [P, P, P, P, P, P, i32, i32, i32, i32, i64, i32, i32, f32, P, P, P]
     lib.mla_get_status.restype = i32
     lib.mla_get_status.argtypes = [P]
     lib.mla_status_string.restype = ctypes.c_char_p
@@ -201,6 +203,25 @@ def prefill_varlen(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_seqlens
                                 int(prefix_lens.numel()), int(H), int(max_seqlen_q), int(Nq), int(k.shape[0]),
                                 float(scale), _ptr(out), _ptr(lse), _stream_handle(stream))
     _check(rc, "mla_prefill_varlen")
+    return out, lse
+
+
+def prefill_paged(q: torch.Tensor, k_pages: torch.Tensor, v_pages: torch.Tensor, page_table: torch.Tensor,
+                  cu_seqlens_q: torch.Tensor, kv_lens: torch.Tensor, max_seqlen_q: int, scale: float, out=None,
+                  lse=None, stream=None):
+    """mla_prefill_paged through the C ABI: the varlen prefill with K/V read through a page
+    table from [num_pages, page_size, H, 192 | 128] pools.  Returns (out, lse)."""
+    Nq, H, _ = q.shape
+    num_pages, page_size = k_pages.shape[0], k_pages.shape[1]
+    if out is None:
+        out = torch.empty(Nq, H, v_pages.shape[3], dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.empty(Nq, H, dtype=torch.float32, device=q.device)
+    rc = lib.mla_prefill_paged(_ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(page_table), _ptr(cu_seqlens_q),
+                               _ptr(kv_lens), int(kv_lens.numel()), int(H), int(page_size), int(page_table.shape[1]),
+                               int(num_pages), int(max_seqlen_q), int(Nq), float(scale), _ptr(out), _ptr(lse),
+                               _stream_handle(stream))
+    _check(rc, "mla_prefill_paged")
     return out, lse
 
 

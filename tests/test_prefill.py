@@ -1,4 +1,5 @@
-"""GPU parity of mla_prefill_varlen (through the C ABI) against the fp64 CPU oracle.
+"""GPU parity of mla_prefill_varlen and mla_prefill_paged (through the C ABI) against the
+fp64 CPU oracle.
 
 Tolerances: max-abs 2e-2 and relative L2 5e-3 over the compared outputs, LSE within 1e-3
 absolute.  Small ragged batches are compared element by element; the full-size workload
@@ -10,7 +11,7 @@ import numpy as np
 import pytest
 import torch
 
-from mla_attention_paged_gb300.inputs import PrefillWorkload, make_prefill_inputs, prefill_workloads
+from mla_attention_paged_gb300.inputs import PrefillWorkload, make_prefill_inputs, page_prefill_kv, prefill_workloads
 
 pytestmark = pytest.mark.gpu
 
@@ -111,3 +112,97 @@ def test_prefill_full_size_sampled(mla, oracle_mod, name):
                                               inp.cu_seqlens_kv.cpu(), inp.prefix_lens.cpu(), inp.scale, rows=rows)
     check(out.reshape(-1, 128)[rows], lse.reshape(-1)[rows], ref_out, ref_lse)
     assert np.isfinite(out).all() and np.isfinite(lse).all()
+
+
+# ------------------------------------------------------------------------------------
+# paged K/V: the same prefill reading every key (prefix and new tokens) through a page table
+# ------------------------------------------------------------------------------------
+def run_gpu_paged(mla, inp, pk):
+    d = "cuda"
+    out, lse = mla.prefill_paged(inp.q.to(d), pk.k_pages.to(d), pk.v_pages.to(d), pk.page_table.to(d),
+                                 inp.cu_seqlens_q.to(d), pk.kv_lens.to(d), inp.max_seqlen_q, inp.scale)
+    torch.cuda.synchronize()
+    assert mla.get_status() == mla.MLA_OK
+    return out.float().cpu().numpy(), lse.cpu().numpy()
+
+
+PAGED = [
+    ("ragged_p16", [1, 63, 65, 300], [300, 1, 64, 17], 3, 16),
+    ("ragged_p64", [1, 63, 65, 300], [300, 1, 64, 17], 3, 64),
+    ("empty_request_p32", [10, 40], [0, 77], 8, 32),
+    ("long_prefix_p128", [5000], [260], 16, 128),
+    ("tile_crossing_p256", [200, 700], [129, 333], 4, 256),
+]
+
+
+@pytest.mark.parametrize("name,prefix,new,H,P", PAGED, ids=[c[0] for c in PAGED])
+def test_prefill_paged_small(mla, oracle_mod, name, prefix, new, H, P):
+    """Every output against the oracle run on the contiguous rows the pages were built from."""
+    wl = PrefillWorkload(name, prefix, new, H, seed=300 + len(name))
+    inp = make_prefill_inputs(wl, "cpu")
+    pk = page_prefill_kv(inp, P, seed=7, extra_pages=3)
+    out, lse = run_gpu_paged(mla, inp, pk)
+    ref_out, ref_lse = oracle_mod.mla_prefill(inp.q, inp.k, inp.v, inp.cu_seqlens_q, inp.cu_seqlens_kv,
+                                              inp.prefix_lens, inp.scale)
+    check(out, lse, ref_out, ref_lse)
+
+
+@pytest.mark.parametrize("P", [16, 64, 256])
+def test_prefill_paged_equals_contiguous_bitwise(mla, P):
+    """The paged call gives the contiguous call's bits: the same keys in the same tiles, and
+    the rows a tile holds past a request's end are masked either way (P = 0 times finite
+    values)."""
+    wl = PrefillWorkload("paged_vs_contiguous", [700, 90, 1500], [150, 333, 64], 4, seed=12)
+    inp = make_prefill_inputs(wl, "cpu")
+    pk = page_prefill_kv(inp, P, seed=8)
+    out_c, lse_c = run_gpu(mla, inp)
+    out_p, lse_p = run_gpu_paged(mla, inp, pk)
+    np.testing.assert_array_equal(out_c, out_p)
+    np.testing.assert_array_equal(lse_c, lse_p)
+
+
+def test_prefill_paged_full_size_sampled(mla, oracle_mod):
+    """The 5-request workload (prefix 20K-100K, 256-2048 new tokens, 16 heads) with its K/V in
+    64-token pages, sampled rows against the oracle."""
+    wl = prefill_workloads()["prefill_b5_h16_prefix"]
+    inp = make_prefill_inputs(wl, "cuda")
+    pk = page_prefill_kv(inp, 64, seed=9)
+    out, lse = run_gpu_paged(mla, inp, pk)
+    H = wl.heads
+    g = np.random.default_rng(6)
+    rows = []
+    off = 0
+    for n in wl.new_lens:
+        toks = {off, off + n - 1} | set(int(x) for x in g.integers(off, off + n, 6))
+        for t in sorted(toks):
+            for h in (0, H - 1, int(g.integers(H))):
+                rows.append(t * H + h)
+        off += n
+    rows = sorted(set(rows))
+    ref_out, ref_lse = oracle_mod.mla_prefill(inp.q.cpu(), inp.k.cpu(), inp.v.cpu(), inp.cu_seqlens_q.cpu(),
+                                              inp.cu_seqlens_kv.cpu(), inp.prefix_lens.cpu(), inp.scale, rows=rows)
+    check(out.reshape(-1, 128)[rows], lse.reshape(-1)[rows], ref_out, ref_lse)
+    assert np.isfinite(out).all() and np.isfinite(lse).all()
+
+
+def test_prefill_paged_bad_page_id_is_reported(mla):
+    """A page id outside [0, num_pages) is reported as MLA_ERR_DEVICE_ARG.  The pools given to
+    the call are views into larger allocations (8 spare pages on each side), so the id used
+    here still names allocated memory."""
+    wl = PrefillWorkload("paged_bad", [300, 40], [100, 20], 2, seed=13)
+    inp = make_prefill_inputs(wl, "cuda")
+    pk = page_prefill_kv(inp, 64, seed=10)
+    n = pk.k_pages.shape[0]
+    kb = torch.zeros((n + 16,) + tuple(pk.k_pages.shape[1:]), dtype=torch.bfloat16, device="cuda")
+    vb = torch.zeros((n + 16,) + tuple(pk.v_pages.shape[1:]), dtype=torch.bfloat16, device="cuda")
+    kb[8:8 + n] = pk.k_pages
+    vb[8:8 + n] = pk.v_pages
+    pt = pk.page_table.clone()
+    pt[0, 2] = n + 3
+    mla.prefill_paged(inp.q, kb[8:8 + n], vb[8:8 + n], pt, inp.cu_seqlens_q, pk.kv_lens, inp.max_seqlen_q, inp.scale)
+    torch.cuda.synchronize()
+    assert mla.get_status() == mla.MLA_ERR_DEVICE_ARG
+    mla.prefill_paged(inp.q, kb[8:8 + n], vb[8:8 + n], pk.page_table, inp.cu_seqlens_q, pk.kv_lens,
+                      inp.max_seqlen_q, inp.scale)
+    torch.cuda.synchronize()
+    assert mla.get_status() == mla.MLA_OK

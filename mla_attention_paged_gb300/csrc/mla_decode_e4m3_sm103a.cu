@@ -9,8 +9,8 @@
 // bandwidth-bound); launch-blog repost "英偉達力薦，小團隊兩個月開源一款「光速級」智能體推理引擎",
 // section "TokenSpeed 性能預覽" (query-sequence axis folded into the head axis).
 //
-// Design on sm_103a (one CTA per (64-row group, split, request); one CTA per SM; 448
-// threads: softmax warps 0-3, producer warp 4, MMA warp 5, decode warps 6-13):
+// Design on sm_103a (one CTA per (64-row group, split, request); one CTA per SM; 480
+// threads: softmax warps 0-3, producer warp 4, BMM1 warp 5, decode warps 6-13, BMM2 warp 14):
 //  * The raw e4m3 tile (64 keys x 576 codes, 36 KB) arrives by TMA (64-byte swizzle) in a
 //    2-stage ring, its rows prefetched into L2 a few tiles earlier, and is the B operand of
 //    BMM1 as it is: BMM1 runs on 8-bit operands
@@ -23,8 +23,13 @@
 //    into one fp32 accumulator, and 2^-s returns in the softmax.
 //  * Only V (the first 512 columns) is decoded to f16 (exactly: codes times 2^-8), from the
 //    raw stage in shared memory into one f16 V stage, by the decode warps, while the
-//    tensor core runs BMM1 of the next tile on its raw stage.  BMM2 (O^T += V^T . P^T,
-//    M = 128 value columns, N = rows, K = 64 keys) reads that stage with f16 P.
+//    tensor core runs BMM1 of the next tile on its raw stage.  The decode warps take a
+//    tile's raw V bytes into registers as soon as it lands and release the raw stage at
+//    once, so its refill does not wait for the V stage.  BMM2 (O^T += V^T . P^T, M = 128
+//    value columns, N = rows, K = 64 keys) reads that stage with f16 P.
+//  * BMM1 and BMM2 are issued by two warps, each waiting on its own inputs: issuing blocks
+//    while the tensor pipe is busy, and one warp issuing both held each BMM2 behind the
+//    next BMM1's issue loop.
 //  * Shared memory: q_hi | q_lo (2 x 36 KB) | raw ring (2 x 36 KB) | f16 V stage (64 KB) |
 //    P (8 KB).  The bf16 Q tile lands by TMA on the V stage and P (72 KB) and is split
 //    from there before the first V decode.
@@ -60,7 +65,8 @@ static_assert(kOffQBf16 + kQBf16Bytes == kOffCtrl, "bf16 Q staging spans V and P
 constexpr int kDecodeWarps = 8;
 constexpr int kDecodeWarp0 = 6;
 constexpr int kDecodeThreads = 32 * kDecodeWarps;
-constexpr int kThreads = 32 * kDecodeWarp0 + kDecodeThreads;
+constexpr int kBmm2Warp = kDecodeWarp0 + kDecodeWarps;  // issues BMM2 (warp 5 issues BMM1)
+constexpr int kThreads = 32 * (kBmm2Warp + 1);
 constexpr int kSoftmaxThreads = 128;
 constexpr int kQThreadsPerRow = kDecodeThreads / kGroupRows;  // 1, 2 or 4 adjacent lanes per Q row
 static_assert(kQThreadsPerRow == 1 || kQThreadsPerRow == 2 || kQThreadsPerRow == 4, "Q split threads per row");
@@ -77,6 +83,7 @@ struct Ctrl {
   uint64_t p_full;
   uint64_t o_done;
   uint64_t mma_drain;
+  uint64_t mma_drain2;         // the BMM2 warp's MMAs
   uint32_t tmem_base;
   int abort_flag;
   int rescale_flag[4];
@@ -136,6 +143,7 @@ decode_partial_e4m3_kernel(const __grid_constant__ CUtensorMap tm_q, const __gri
     mbar_init(&ctrl->p_full, kSoftmaxThreads);
     mbar_init(&ctrl->o_done, 1);
     mbar_init(&ctrl->mma_drain, 1);
+    mbar_init(&ctrl->mma_drain2, 1);
     ctrl->abort_flag = 0;
     for (int w = 0; w < 4; ++w) ctrl->rescale_flag[w] = 0;
     fence_mbarrier_init();
@@ -262,100 +270,83 @@ decode_partial_e4m3_kernel(const __grid_constant__ CUtensorMap tm_q, const __gri
         if (last_issued[s] >= 0) drain_wait(&ctrl->raw_full[s], (last_issued[s] >> 1) & 1);
     }
   } else if (warp == 5) {
-    // ------------------------------------------------------------------ MMA issuer
+    // ------------------------------------------------------------------ BMM1 issuer (whole warp,
+    // uniform control flow; one elected thread issues the MMAs and their commits)
     const uint32_t idesc1 = make_idesc_e4m3(64, 64);
-    const uint32_t idesc2 = make_idesc_f16(128, nq, true, false);
     const uint64_t qhi_desc = make_smem_desc_sw64(smem_u32(smem + kOffQ8));
     const uint64_t qlo_desc = make_smem_desc_sw64(smem_u32(smem + kOffQ8 + kQPart));
-    const uint64_t p_desc = make_smem_desc(smem_u32(smem + kOffP), 16, 1024);
-    const uint64_t v_desc = make_smem_desc(smem_u32(smem + kOffV), kF16Block, 1024);
-    auto poll = [&](uint64_t* bar, uint32_t parity) -> bool {
-      uint32_t v = 0;
-      if (lane == 0) v = mbar_test_wait(bar, parity) ? 1u : 0u;
-      return __shfl_sync(0xffffffffu, v, 0) != 0;
-    };
     bool ok = mbar_wait(&ctrl->q_ready, 0, abort_flag);
-    ok = __all_sync(0xffffffffu, ok);
-    // BMM2(n2) once P(n2) and the V stage hold tile n2 (it frees the V stage), else BMM1(n1)
-    // once raw tile n1 has landed and its S buffer is free; BMM1 runs at most two tiles ahead.
-    int n1 = 0, n2 = 0;
-    unsigned long long idle_since = 0;
-    while (ok && n2 < ntiles) {
-      bool progressed = false;
-      if (n2 < n1 && poll(&ctrl->p_full, n2 & 1) && poll(&ctrl->v_full, n2 & 1)) {
-        tc_fence_after();
-        if (elect_one()) {
+    // BMM1(j) as soon as raw tile j has landed and its S buffer is free.  Issuing blocks
+    // while the tensor pipe is busy, so BMM2 has a warp of its own and is never held behind
+    // this warp's issue loop.
+    for (int j = 0; j < ntiles; ++j) {
+      const int s = j & 1, sb = j & 1;
+      if (ok) ok = mbar_wait(&ctrl->raw_full[s], (j >> 1) & 1, abort_flag);
+      if (ok && j >= 2) ok = mbar_wait(&ctrl->s_free[sb], ((j - 2) >> 1) & 1, abort_flag);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      tc_fence_after();
+      const uint64_t k_desc = make_smem_desc_sw64(smem_u32(smem + kOffRaw + s * kRawTile));
+      const uint32_t d = tmem + kTmemS + sb * 64;
+      // the q descriptors pass through an empty asm on every issue, so that the compiler
+      // adds the 36 offsets here instead of keeping 36 precomputed descriptors live
+      uint64_t qh = qhi_desc, ql = qlo_desc;
+      asm volatile("" : "+l"(qh), "+l"(ql));
+      if (elect_one()) {
+        // S = q_hi . k + q_lo . k: 2 x 9 blocks x 2 K-steps of 32 codes
 #pragma unroll
-          for (int qc = 0; qc < 4; ++qc) {
+        for (int part = 0; part < 2; ++part) {
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-              const uint64_t voff = static_cast<uint64_t>((2 * qc * kF16Block + kk * 2048) >> 4);
-              const uint64_t poff = static_cast<uint64_t>((kk * 32) >> 4);
-              umma_bf16(tmem + qc * 64, v_desc + voff, p_desc + poff, idesc2, (n2 > 0 || kk > 0) ? 1u : 0u);
+          for (int c = 0; c < kBlocks; ++c) {
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+              const uint64_t off = static_cast<uint64_t>((c * kRawBlock + k * 32) >> 4);
+              umma_e4m3(d, (part == 0 ? qh : ql) + off, k_desc + off, idesc1, (part | c | k) != 0 ? 1u : 0u);
             }
           }
-          umma_commit(&ctrl->o_done);
-          umma_commit(&ctrl->v_empty);
         }
-        __syncwarp();
-        ++n2;
-        progressed = true;
-      } else if (n1 < ntiles && n1 < n2 + 2) {
-        const int s = n1 & 1, sb = n1 & 1;
-        if (poll(&ctrl->raw_full[s], (n1 >> 1) & 1) && (n1 < 2 || poll(&ctrl->s_free[sb], ((n1 - 2) >> 1) & 1))) {
-          tc_fence_after();
-          const uint64_t k_desc = make_smem_desc_sw64(smem_u32(smem + kOffRaw + s * kRawTile));
-          const uint32_t d = tmem + kTmemS + sb * 64;
-          // the q descriptors pass through an empty asm on every issue, so that the compiler
-          // adds the 36 offsets here instead of keeping 36 precomputed descriptors live
-          uint64_t qh = qhi_desc, ql = qlo_desc;
-          asm volatile("" : "+l"(qh), "+l"(ql));
-          if (elect_one()) {
-            // S = q_hi . k + q_lo . k: 2 x 9 blocks x 2 K-steps of 32 codes
-#pragma unroll
-            for (int part = 0; part < 2; ++part) {
-#pragma unroll
-              for (int c = 0; c < kBlocks; ++c) {
-#pragma unroll
-                for (int k = 0; k < 2; ++k) {
-                  const uint64_t off = static_cast<uint64_t>((c * kRawBlock + k * 32) >> 4);
-                  umma_e4m3(d, (part == 0 ? qh : ql) + off, k_desc + off, idesc1,
-                            (part | c | k) != 0 ? 1u : 0u);
-                }
-              }
-            }
-            umma_commit(&ctrl->s_full[sb]);
-            umma_commit(&ctrl->raw_empty[s]);
-          }
-          __syncwarp();
-          ++n1;
-          progressed = true;
-        }
+        umma_commit(&ctrl->s_full[sb]);
+        umma_commit(&ctrl->raw_empty[s]);
       }
-      if (progressed) {
-        idle_since = 0;
-      } else {
-        uint32_t give_up = 0;
-        if (lane == 0) {
-          const unsigned long long now = global_timer_ns();
-          if (idle_since == 0) {
-            idle_since = now;
-          } else if (*abort_flag) {
-            give_up = 1;
-          } else if (now - idle_since > kWaitLimitNs) {
-            *abort_flag = kAbortTimeout;
-            give_up = 1;
-          }
-        }
-        ok = __shfl_sync(0xffffffffu, give_up, 0) == 0;
-      }
+      __syncwarp();
     }
+    // every MMA this warp issued completes before TMEM is released
     if (elect_one()) {
       umma_commit(&ctrl->mma_drain);
       drain_wait(&ctrl->mma_drain, 0);
     }
     __syncwarp();
-  } else if (warp >= kDecodeWarp0) {
+  } else if (warp == kBmm2Warp) {
+    // ------------------------------------------------------------------ BMM2 issuer
+    const uint32_t idesc2 = make_idesc_f16(128, nq, true, false);
+    const uint64_t p_desc = make_smem_desc(smem_u32(smem + kOffP), 16, 1024);
+    const uint64_t v_desc = make_smem_desc(smem_u32(smem + kOffV), kF16Block, 1024);
+    bool ok = true;
+    for (int j = 0; j < ntiles; ++j) {
+      if (ok) ok = mbar_wait(&ctrl->p_full, j & 1, abort_flag);
+      if (ok) ok = mbar_wait(&ctrl->v_full, j & 1, abort_flag);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      tc_fence_after();
+      if (elect_one()) {
+#pragma unroll
+        for (int qc = 0; qc < 4; ++qc) {
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint64_t voff = static_cast<uint64_t>((2 * qc * kF16Block + kk * 2048) >> 4);
+            const uint64_t poff = static_cast<uint64_t>((kk * 32) >> 4);
+            umma_bf16(tmem + qc * 64, v_desc + voff, p_desc + poff, idesc2, (j > 0 || kk > 0) ? 1u : 0u);
+          }
+        }
+        umma_commit(&ctrl->o_done);
+        umma_commit(&ctrl->v_empty);
+      }
+      __syncwarp();
+    }
+    if (elect_one()) {
+      umma_commit(&ctrl->mma_drain2);
+      drain_wait(&ctrl->mma_drain2, 0);
+    }
+    __syncwarp();
+  } else if (warp >= kDecodeWarp0 && warp < kBmm2Warp) {
     // ------------------------------------------------------------------ decode warps
     const int dt = threadIdx.x - kDecodeWarp0 * 32;
     bool ok = mbar_wait(&ctrl->q_full, 0, abort_flag);
@@ -424,29 +415,40 @@ decode_partial_e4m3_kernel(const __grid_constant__ CUtensorMap tm_q, const __gri
     // V decode: raw chunk q = dt + kDecodeThreads i of the tile's eight value blocks (2048
     // chunks): block q / 256, row (q % 256) / 4, 16-code chunk q % 4 -> two 16-byte f16
     // chunks of the row.
+    // The raw V bytes of tile j go to registers as soon as the tile lands, and the raw stage
+    // is released at once (BMM1 releases it too): its refill need not wait for the V stage,
+    // which frees only when BMM2(j - 1) completes.  Then the f16 values are written.
+    constexpr int kPerThread = 2048 / kDecodeThreads;
     for (int j = 0; ok && j < ntiles; ++j) {
       const int s = j & 1;
       ok = mbar_wait(&ctrl->raw_full[s], (j >> 1) & 1, abort_flag);
-      if (ok && j >= 1) ok = mbar_wait(&ctrl->v_empty, (j - 1) & 1, abort_flag);
       if (!ok) break;
       const int valid_rows = L - (kv_start + j * kTileKeys);  // rows past the request end become zeros
       const uint32_t raw = smem_u32(smem + kOffRaw + s * kRawTile);
-      const uint32_t vst = smem_u32(smem + kOffV);
-#pragma unroll 4
-      for (int i = 0; i < 2048 / kDecodeThreads; ++i) {
+      uint4 w[kPerThread];
+#pragma unroll
+      for (int i = 0; i < kPerThread; ++i) {
         const int q = dt + kDecodeThreads * i;
         const int blk = q >> 8, row = (q >> 2) & 63, jc = q & 3;
-        uint4 w = make_uint4(0u, 0u, 0u, 0u);
+        w[i] = make_uint4(0u, 0u, 0u, 0u);
         if (row < valid_rows) {
           asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                       : "=r"(w.x), "=r"(w.y), "=r"(w.z), "=r"(w.w)
+                       : "=r"(w[i].x), "=r"(w[i].y), "=r"(w[i].z), "=r"(w[i].w)
                        : "r"(raw + blk * kRawBlock + row * 64 + ((jc ^ ((row >> 1) & 3)) << 4)));
         }
-        store_f16_chunk(vst + blk * kF16Block + row * 128 + jc * 32, (row & 7) << 4, w);
+      }
+      mbar_arrive(&ctrl->raw_empty[s]);
+      if (j >= 1) ok = mbar_wait(&ctrl->v_empty, (j - 1) & 1, abort_flag);
+      if (!ok) break;
+      const uint32_t vst = smem_u32(smem + kOffV);
+#pragma unroll
+      for (int i = 0; i < kPerThread; ++i) {
+        const int q = dt + kDecodeThreads * i;
+        const int blk = q >> 8, row = (q >> 2) & 63, jc = q & 3;
+        store_f16_chunk(vst + blk * kF16Block + row * 128 + jc * 32, (row & 7) << 4, w[i]);
       }
       fence_proxy_async_smem();
       mbar_arrive(&ctrl->v_full);
-      mbar_arrive(&ctrl->raw_empty[s]);
     }
   } else {
     // ------------------------------------------------------------------ softmax + epilogue (warps 0-3)

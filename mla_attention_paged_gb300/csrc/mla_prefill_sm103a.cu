@@ -13,15 +13,17 @@
 // section "TokenSpeed 性能預覽" (prefill with a long prefix KV cache, tuned softmax).
 //
 // Design on sm_103a (one CTA per (128-row query block, head, request), one CTA per SM,
-// 320 threads: softmax warps 0-7, producer warp 8, MMA warp 9):
+// 352 threads: softmax warps 0-7, producer warp 8, BMM1 warp 9, BMM2 warp 10):
 //  * Producer warp: TMA (128-byte swizzled, 4-D maps over (columns, token, column block,
 //    head), one box per operand tile) loads the query block once and streams 128-key K (192
 //    wide) and V (128 wide) tiles of the same head through two separate 2-stage mbarrier
 //    rings: a K stage is refilled as soon as its BMM1 is done, a V stage once its BMM2 is,
 //    so the K loads run ahead of the softmax instead of waiting for the whole tile.
-//  * MMA warp (uniform control flow, one elected thread issues): S = Q . K^T (M=128 rows,
-//    N=128 keys, K=192) into one of two TMEM S buffers; O += P . V (M=128, N=128, K=128)
-//    with P read straight from TMEM (the A operand) and V MN-major from shared memory.
+//  * Two MMA warps (uniform control flow, one elected thread issues): the BMM1 warp puts
+//    S = Q . K^T (M=128 rows, N=128 keys, K=192) into one of two TMEM S buffers; the BMM2
+//    warp adds O += P . V (M=128, N=128, K=128) with P read straight from TMEM (the A
+//    operand) and V MN-major from shared memory.  Issuing an MMA stalls while the tensor
+//    pipe is busy, so with one issuer a ready BMM2 waited behind the next BMM1's 12 MMAs.
 //  * Softmax warps (8: two per TMEM lane quadrant, each row = TMEM lane split between a
 //    warp for keys 0-63 and one for keys 64-127 of every tile, which swap their partial
 //    row maxima through shared memory): causal mask offset by the prefix only on tiles
@@ -47,8 +49,9 @@ constexpr int kStages = 2;
 constexpr int kSoftmaxWarps = 8;  // two per TMEM lane quadrant, one per half of the key tile
 constexpr int kSoftmaxThreads = 32 * kSoftmaxWarps;
 constexpr int kProducerWarp = kSoftmaxWarps;
-constexpr int kMmaWarp = kSoftmaxWarps + 1;
-constexpr int kThreads = 32 * (kSoftmaxWarps + 2);
+constexpr int kMmaWarp = kSoftmaxWarps + 1;   // issues BMM1 (and owns TMEM)
+constexpr int kBmm2Warp = kSoftmaxWarps + 2;  // issues BMM2
+constexpr int kThreads = 32 * (kSoftmaxWarps + 3);
 
 constexpr int kQBlockBytes = kBM * 128;                // 16 KB per 64-column block
 constexpr int kQBytes = (kDqk / 64) * kQBlockBytes;    // 48 KB
@@ -72,6 +75,7 @@ struct PrefillCtrl {
   uint64_t p_full;
   uint64_t o_done;
   uint64_t mma_drain;
+  uint64_t mma_drain2;     // the BMM2 warp's MMAs
   uint32_t tmem_base;
   int abort_flag;
   float row_max[2][kBM];   // per half of the key tile: this tile's partial row maxima
@@ -171,6 +175,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     mbar_init(&ctrl->p_full, kSoftmaxThreads);
     mbar_init(&ctrl->o_done, 1);
     mbar_init(&ctrl->mma_drain, 1);
+    mbar_init(&ctrl->mma_drain2, 1);
     ctrl->abort_flag = 0;
     fence_mbarrier_init();
   }
@@ -309,85 +314,68 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     }
     __syncwarp();
   } else if (warp == kMmaWarp) {
-    // ------------------------------------------------------------------ MMA issuer (whole warp,
-    // uniform control flow; one elected thread issues each GEMM's MMAs and their commits)
+    // ------------------------------------------------------------------ BMM1 issuer (whole warp,
+    // uniform control flow; one elected thread issues the MMAs and their commits).  Issuing
+    // blocks while the tensor pipe is busy, so BMM2 has a warp of its own: neither GEMM
+    // waits behind the other's issue loop.
     const uint32_t idesc1 = make_idesc_bf16(kBM, kBN, false, false);
-    const uint32_t idesc2 = make_idesc_bf16(kBM, kDv, false, true);
     const uint64_t q_desc = make_smem_desc(smem_u32(smem + kOffQ), 16, 1024);
-    auto poll = [&](uint64_t* bar, uint32_t parity) -> bool {
-      uint32_t v = 0;
-      if (lane == 0) v = mbar_test_wait(bar, parity) ? 1u : 0u;
-      return __shfl_sync(0xffffffffu, v, 0) != 0;
-    };
     bool ok = mbar_wait(&ctrl->q_full, 0, abort_flag);
-    ok = __all_sync(0xffffffffu, ok);
-    // BMM2(n2) as soon as P(n2) and V(n2) are ready (it frees a V stage and an S buffer),
-    // else BMM1(n1) once K(n1) has landed and BMM2(n1-2) has read the P in its S buffer.
-    int n1 = 0, n2 = 0;
-    unsigned long long idle_since = 0;
-    while (ok && n2 < ntiles) {
-      bool progressed = false;
-      if (n2 < n1 && poll(&ctrl->p_full, n2 & 1) && poll(&ctrl->v_full[n2 % kStages], (n2 / kStages) & 1)) {
-        tc_fence_after();
-        const int s = n2 % kStages, sb = n2 & 1;
-        // P: 128 rows x 16 keys per MMA, 8 TMEM columns apart.  V: 16 keys (two 8-key groups,
-        // SBO apart) x 128 value columns (two 64-column blocks, LBO apart), MN-major.
-        const uint64_t v_desc =
-            make_smem_desc(smem_u32(smem + kOffV + s * kVBytes), kKVBlockBytes, 1024);
-        const uint32_t p_tmem = tmem + kTmemS + sb * 128;
-        if (elect_one()) {
+    // BMM1(j) once K(j) has landed and BMM2(j-2) has read the P in its S buffer
+    for (int j = 0; j < ntiles; ++j) {
+      const int s = j % kStages, sb = j & 1;
+      if (ok) ok = mbar_wait(&ctrl->k_full[s], (j / kStages) & 1, abort_flag);
+      if (ok && j >= 2) ok = mbar_wait(&ctrl->s_consumed[sb], ((j - 2) >> 1) & 1, abort_flag);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      tc_fence_after();
+      const uint64_t k_desc = make_smem_desc(smem_u32(smem + kOffK + s * kKBytes), 16, 1024);
+      if (elect_one()) {
 #pragma unroll
-          for (int kk = 0; kk < kBN / 16; ++kk)
-            umma_ts_bf16(tmem + kTmemO, p_tmem + kk * 8, v_desc + static_cast<uint64_t>((kk * 2048) >> 4), idesc2,
-                         (n2 > 0 || kk > 0) ? 1u : 0u);
-          umma_commit(&ctrl->o_done);
-          umma_commit(&ctrl->v_empty[s]);
-          umma_commit(&ctrl->s_consumed[sb]);
+        for (int c = 0; c < kDqk / 64; ++c) {
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            umma_bf16(tmem + kTmemS + sb * 128, q_desc + static_cast<uint64_t>((c * kQBlockBytes + k * 32) >> 4),
+                      k_desc + static_cast<uint64_t>((c * kKVBlockBytes + k * 32) >> 4), idesc1, (c | k) != 0);
         }
-        __syncwarp();
-        ++n2;
-        progressed = true;
-      } else if (n1 < ntiles && n1 < n2 + 2) {
-        const int s = n1 % kStages, sb = n1 & 1;
-        if (poll(&ctrl->k_full[s], (n1 / kStages) & 1) &&
-            (n1 < 2 || poll(&ctrl->s_consumed[sb], ((n1 - 2) >> 1) & 1))) {
-          tc_fence_after();
-          const uint64_t k_desc = make_smem_desc(smem_u32(smem + kOffK + s * kKBytes), 16, 1024);
-          if (elect_one()) {
-#pragma unroll
-            for (int c = 0; c < kDqk / 64; ++c) {
-#pragma unroll
-              for (int k = 0; k < 4; ++k)
-                umma_bf16(tmem + kTmemS + sb * 128, q_desc + static_cast<uint64_t>((c * kQBlockBytes + k * 32) >> 4),
-                          k_desc + static_cast<uint64_t>((c * kKVBlockBytes + k * 32) >> 4), idesc1, (c | k) != 0);
-            }
-            umma_commit(&ctrl->s_full[sb]);
-            umma_commit(&ctrl->k_empty[s]);
-          }
-          __syncwarp();
-          ++n1;
-          progressed = true;
-        }
+        umma_commit(&ctrl->s_full[sb]);
+        umma_commit(&ctrl->k_empty[s]);
       }
-      if (progressed) {
-        idle_since = 0;
-      } else {
-        uint32_t give_up = 0;
-        if (lane == 0) {
-          const unsigned long long now = global_timer_ns();
-          if (idle_since == 0) {
-            idle_since = now;
-          } else if (*abort_flag || now - idle_since > kWaitLimitNs) {
-            *abort_flag = 1;
-            give_up = 1;
-          }
-        }
-        ok = __shfl_sync(0xffffffffu, give_up, 0) == 0;
-      }
+      __syncwarp();
     }
     if (elect_one()) {
       umma_commit(&ctrl->mma_drain);
       drain_wait(&ctrl->mma_drain, 0);
+    }
+    __syncwarp();
+  } else if (warp == kBmm2Warp) {
+    // ------------------------------------------------------------------ BMM2 issuer: O += P . V
+    // as soon as P(j) and V(j) are ready (it frees a V stage and an S buffer)
+    const uint32_t idesc2 = make_idesc_bf16(kBM, kDv, false, true);
+    bool ok = true;
+    for (int j = 0; j < ntiles; ++j) {
+      const int s = j % kStages, sb = j & 1;
+      if (ok) ok = mbar_wait(&ctrl->p_full, j & 1, abort_flag);
+      if (ok) ok = mbar_wait(&ctrl->v_full[s], (j / kStages) & 1, abort_flag);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      tc_fence_after();
+      // P: 128 rows x 16 keys per MMA, 8 TMEM columns apart.  V: 16 keys (two 8-key groups,
+      // SBO apart) x 128 value columns (two 64-column blocks, LBO apart), MN-major.
+      const uint64_t v_desc = make_smem_desc(smem_u32(smem + kOffV + s * kVBytes), kKVBlockBytes, 1024);
+      const uint32_t p_tmem = tmem + kTmemS + sb * 128;
+      if (elect_one()) {
+#pragma unroll
+        for (int kk = 0; kk < kBN / 16; ++kk)
+          umma_ts_bf16(tmem + kTmemO, p_tmem + kk * 8, v_desc + static_cast<uint64_t>((kk * 2048) >> 4), idesc2,
+                       (j > 0 || kk > 0) ? 1u : 0u);
+        umma_commit(&ctrl->o_done);
+        umma_commit(&ctrl->v_empty[s]);
+        umma_commit(&ctrl->s_consumed[sb]);
+      }
+      __syncwarp();
+    }
+    if (elect_one()) {
+      umma_commit(&ctrl->mma_drain2);
+      drain_wait(&ctrl->mma_drain2, 0);
     }
     __syncwarp();
   } else {

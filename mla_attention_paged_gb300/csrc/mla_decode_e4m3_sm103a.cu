@@ -9,38 +9,47 @@
 // bandwidth-bound); launch-blog repost "英偉達力薦，小團隊兩個月開源一款「光速級」智能體推理引擎",
 // section "TokenSpeed 性能預覽" (query-sequence axis folded into the head axis).
 //
-// Design on sm_103a (one CTA per (64-row group, split, request); one CTA per SM; 480
-// threads: softmax warps 0-3, producer warp 4, BMM1 warp 5, decode warps 6-13, BMM2 warp 14):
+// Design on sm_103a (one CTA per (64-row group, split, request); one CTA per SM; 224
+// threads: softmax warps 0-3, producer warp 4, BMM1 warp 5, BMM2 warp 6).  Both GEMMs run on
+// the 8-bit codes as they arrive (kind::f8f6f4); nothing is decoded to a wider type:
 //  * The raw e4m3 tile (64 keys x 576 codes, 36 KB) arrives by TMA (64-byte swizzle) in a
-//    2-stage ring, its rows prefetched into L2 a few tiles earlier, and is the B operand of
-//    BMM1 as it is: BMM1 runs on 8-bit operands
-//    (kind::f8f6f4).  Q keeps its bf16 value: each query row, scaled by a power of two 2^s
-//    that brings its largest element into [128, 256), is split into q_hi = e4m3(q 2^s) and
+//    4-stage ring, its rows prefetched into L2 ahead of the load.
+//  * Q keeps its bf16 value: each query row, scaled by a power of two 2^s that brings its
+//    largest element into [128, 256), is split into q_hi = e4m3(q 2^s) and
 //    q_lo = e4m3(q 2^s - q_hi), an 8-bit significand in two 4-bit halves.  This is exact
 //    for every element within 2^9 of the row's largest |q|; smaller elements fall under
 //    e4m3's subnormal floor (2^-9 at that scale) and carry an absolute error of at most
-//    2^-17 of the row's largest |q|.  S = (q_hi + q_lo) . k_code takes two passes of MMAs
-//    into one fp32 accumulator, and 2^-s returns in the softmax.
-//  * Only V (the first 512 columns) is decoded to f16 (exactly: codes times 2^-8), from the
-//    raw stage in shared memory into one f16 V stage, by the decode warps, while the
-//    tensor core runs BMM1 of the next tile on its raw stage.  The decode warps take a
-//    tile's raw V bytes into registers as soon as it lands and release the raw stage at
-//    once, so its refill does not wait for the V stage.  BMM2 (O^T += V^T . P^T, M = 128
-//    value columns, N = rows, K = 64 keys) reads that stage with f16 P.
+//    2^-17 of the row's largest |q|.
+//  * BMM1 (M = 128, N = 64 keys, K = 576): the A operand stacks q_hi and q_lo, 16 rows of
+//    each in turn, so that row r's hi and lo partial scores land in TMEM lanes i and i + 16
+//    of the same warp (i = 32 (r / 16) + r % 16).  One shuffle adds them; each lane then
+//    holds half the row's keys.  One pass of full-rate MMAs reads the K tile once.
+//  * BMM2 (O^T += V^T . P^T, M = 128 value columns, N = rows, K = 64 keys) takes V straight
+//    from the raw stage as an MN-major e4m3 operand.  P is split in two 8-bit parts: the
+//    softmax forms P 2^6 (at most 2^8, because the running max moves once a tile's max
+//    exceeds it by more than 2 in the log2 domain) and writes p_hi = e4m3(P 2^6) and
+//    p_lo = e5m2(P 2^6 - p_hi); two MMA passes (e4m3 x e4m3, e4m3 x e5m2) add both.  Their
+//    sum carries P 2^6 to within 2^-8 relative from 2^-6 up (e4m3's normal range) and to
+//    within 2^-14 absolute below.  p_lo is e5m2 for its range: a P below e4m3's subnormal
+//    floor (2^-9 of 2^6, i.e. 2^-15 of the running max) would flush to zero, and behind one
+//    dominant key a long tail of such keys is a mass that O would lose; e5m2 keeps every
+//    key down to 2^-22 of the running max.  The output is normalised by the sum of
+//    p_hi + p_lo (the values the MMAs use), the LSE taken from the fp32 P.
+//  * A raw stage is released when BMM1 and BMM2 of its tile have both completed.  Rows of
+//    the request's last tile past its end are zeroed in the stage before BMM2 reads them
+//    (stale codes there could be NaN, and 0 * NaN is NaN).
 //  * BMM1 and BMM2 are issued by two warps, each waiting on its own inputs: issuing blocks
-//    while the tensor pipe is busy, and one warp issuing both held each BMM2 behind the
-//    next BMM1's issue loop.
-//  * Shared memory: q_hi | q_lo (2 x 36 KB) | raw ring (2 x 36 KB) | f16 V stage (64 KB) |
-//    P (8 KB).  The bf16 Q tile lands by TMA on the V stage and P (72 KB) and is split
-//    from there before the first V decode.
-//  * Softmax and epilogue as in the bf16/int8 kernel: M = 64 rows in TMEM lanes
-//    32*(r/16) + r%16, each row split over two lanes, lazy rescale, f16 P, bf16 output or
-//    split partial for the combine kernel (a programmatic dependent launch).
+//    while the tensor pipe is busy.
+//  * Shared memory: stacked q_hi / q_lo (72 KB) | raw ring (4 x 36 KB) | p_hi, p_lo
+//    (2 x 4 KB).  The bf16 Q tile lands by TMA on ring stages 2-3 and is split from there
+//    before their first load; the epilogue stages the bf16 output in stages 0-1.
+//  * Softmax and epilogue: each row split over two lanes of a warp (keys 0-31, 32-63),
+//    lazy rescale, bf16 output or split partial for the combine kernel (a programmatic
+//    dependent launch).
 // Every wait is bounded; on expiry the CTA records a timeout in the status word, drains
 // its in-flight copies and MMAs, frees TMEM and returns.
 #include <cuda_fp16.h>
 
-#include "kv8_decode.cuh"
 #include "mla_internal.h"
 #include "sm103a_ptx.cuh"
 
@@ -48,36 +57,36 @@ namespace mla {
 namespace {
 
 constexpr int kBlocks = kLatentDim / 64;           // 9 column blocks of 64
+constexpr int kStages = 4;                         // raw ring depth
 constexpr int kRawBlock = 64 * 64;                 // 64 keys x 64 one-byte codes (64-byte swizzle)
 constexpr int kRawTile = kBlocks * kRawBlock;      // 36864
-constexpr int kQPart = kBlocks * kRawBlock;        // 64 rows x 576 e4m3 codes
+constexpr int kQ8Block = 128 * 64;                 // 128 stacked hi/lo rows x 64 codes
+constexpr int kQ8Bytes = kBlocks * kQ8Block;       // 73728
 constexpr int kF16Block = 64 * 128;                // 64 rows x 64 16-bit columns (128-byte swizzle)
-constexpr int kVBytes = (kValueDim / 64) * kF16Block;  // 65536
 constexpr int kQBf16Bytes = kBlocks * kF16Block;   // 73728
-constexpr int kOffQ8 = 0;                          // q_hi, then q_lo
-constexpr int kOffRaw = 2 * kQPart;                // raw ring
-constexpr int kOffV = kOffRaw + 2 * kRawTile;      // f16 V stage
-constexpr int kOffP = kOffV + kVBytes;             // P [64 rows][64 keys] f16
-constexpr int kOffQBf16 = kOffV;                   // the bf16 Q tile lands on V and P
-constexpr int kOffCtrl = kOffP + kF16Block;
-static_assert(kOffQBf16 + kQBf16Bytes == kOffCtrl, "bf16 Q staging spans V and P exactly");
+constexpr int kPPart = 64 * 64;                    // p_hi (e4m3) or p_lo (e5m2): 64 rows x 64 keys
+constexpr int kOffQ8 = 0;
+constexpr int kOffRaw = kQ8Bytes;                  // raw ring
+constexpr int kOffP = kOffRaw + kStages * kRawTile;
+constexpr int kOffCtrl = kOffP + 2 * kPPart;
+constexpr int kOffQBf16 = kOffRaw + 2 * kRawTile;  // the bf16 Q tile lands on ring stages 2-3
+constexpr int kOffOStage = kOffRaw;                // [64][512] bf16 output staging (stages 0-1)
+static_assert(kOffQBf16 + kQBf16Bytes == kOffP, "bf16 Q staging spans ring stages 2-3 exactly");
+static_assert(kGroupRows * kValueDim * 2 <= 2 * kRawTile, "output staging fits ring stages 0-1");
 
-constexpr int kDecodeWarps = 8;
-constexpr int kDecodeWarp0 = 6;
-constexpr int kDecodeThreads = 32 * kDecodeWarps;
-constexpr int kBmm2Warp = kDecodeWarp0 + kDecodeWarps;  // issues BMM2 (warp 5 issues BMM1)
-constexpr int kThreads = 32 * (kBmm2Warp + 1);
 constexpr int kSoftmaxThreads = 128;
-constexpr int kQThreadsPerRow = kDecodeThreads / kGroupRows;  // 1, 2 or 4 adjacent lanes per Q row
-static_assert(kQThreadsPerRow == 1 || kQThreadsPerRow == 2 || kQThreadsPerRow == 4, "Q split threads per row");
+constexpr int kProducerWarp = 4;
+constexpr int kBmm1Warp = 5;
+constexpr int kBmm2Warp = 6;
+constexpr int kThreads = 32 * (kBmm2Warp + 1);
+constexpr int kQThreadsPerRow = kSoftmaxThreads / kGroupRows;  // 2 adjacent threads per Q row
+static_assert(kQThreadsPerRow == 2, "Q split threads per row");
 
 struct Ctrl {
   uint64_t q_full;             // bf16 Q tile landed (TMA)
-  uint64_t q_ready;            // q_hi / q_lo written (decode threads)
-  uint64_t raw_full[2];        // raw tile landed (TMA)
-  uint64_t raw_empty[2];       // BMM1 of the tile done (commit) and its V decoded (decode threads)
-  uint64_t v_full;             // f16 V stage written (decode threads)
-  uint64_t v_empty;            // BMM2 of the V stage's tile done (commit)
+  uint64_t q_ready;            // stacked q_hi / q_lo written (softmax threads)
+  uint64_t raw_full[kStages];  // raw tile landed (TMA)
+  uint64_t raw_empty[kStages]; // BMM1 and BMM2 of the tile done (two commits)
   uint64_t s_full[2];
   uint64_t s_free[2];
   uint64_t p_full;
@@ -94,11 +103,15 @@ struct Ctrl {
 constexpr int kSmemBytes = kOffCtrl + 1024 + 1024;  // + control block + alignment slack
 static_assert(sizeof(Ctrl) <= 1024, "control block");
 
-constexpr int kPrefetchAhead = 3;  // raw tiles are prefetched into L2 this many tiles before their TMA load
+constexpr int kPrefetchAhead = 2;  // raw tiles are prefetched into L2 this many tiles beyond the ring
 constexpr int kAbortTimeout = 1;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemS = 256;  // S buffers at columns 256 and 320; O^T chunks at 0,64,128,192
-constexpr float kRescaleThreshold = 8.0f;
+// The running max (log2 domain) moves once a tile's max exceeds it by more than this, and
+// P is formed times 2^kPShift: P 2^kPShift <= 2^(threshold + shift) = 256 < 448 (e4m3 max),
+// and e4m3's subnormal floor (2^-9) sits 2^-15 below a P of 1.
+constexpr float kRescaleThreshold = 2.0f;
+constexpr float kPShift = 6.0f;
 
 // Two floats -> two e4m3 codes (round to nearest even, saturating), `lo` in the low byte.
 __device__ __forceinline__ uint32_t f32x2_to_e4m3x2(float lo, float hi) {
@@ -112,6 +125,66 @@ __device__ __forceinline__ float2 e4m3x2_to_f32x2(uint32_t codes) {
   uint32_t h2;
   asm("{\n\t.reg .b16 c;\n\tcvt.u16.u32 c, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, c;\n\t}" : "=r"(h2) : "r"(codes));
   return __half22float2(*reinterpret_cast<const __half2*>(&h2));
+}
+
+// The same pair of conversions for e5m2.
+__device__ __forceinline__ uint32_t f32x2_to_e5m2x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e5m2x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+__device__ __forceinline__ float2 e5m2x2_to_f32x2(uint32_t codes) {
+  uint32_t h2;
+  asm("{\n\t.reg .b16 c;\n\tcvt.u16.u32 c, %1;\n\tcvt.rn.f16x2.e5m2x2 %0, c;\n\t}" : "=r"(h2) : "r"(codes));
+  return __half22float2(*reinterpret_cast<const __half2*>(&h2));
+}
+
+// One online-softmax step over this lane's 32 scores x[] of its row (the row's other 32
+// keys are in lane ^ 16, which takes the same running-state decisions).  Keys i <= lim are
+// visible.  P 2^kPShift goes out as e4m3 hi and e5m2 lo codes (4 per word, key order).  l_sum
+// accumulates the fp32 P (for the LSE), l_use the hi + lo values the MMAs take (for the
+// output's normalisation, so that the split's rounding of a dominant key cancels in O / l).
+__device__ __forceinline__ void softmax_step_e4m3(const float (&x)[32], int lim, float scale_log2, float& m_used,
+                                                  float& l_sum, float& l_use, uint32_t (&phi)[8],
+                                                  uint32_t (&plo)[8], float& alpha, bool& need_rescale) {
+  float mx = -INFINITY;
+#pragma unroll
+  for (int i = 0; i < 32; ++i)
+    if (i <= lim) mx = fmaxf(mx, x[i]);
+  mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+  const float mt = mx * scale_log2;  // scale > 0: max commutes with the scaling; -inf stays -inf
+  alpha = 1.f;
+  need_rescale = false;
+  if (m_used == -INFINITY) {
+    m_used = mt;  // first contributing tile: nothing accumulated yet
+  } else if (mt > m_used + kRescaleThreshold) {
+    alpha = ex2_approx(m_used - mt);
+    need_rescale = true;
+    l_sum *= alpha;
+    l_use *= alpha;
+    m_used = mt;
+  }
+  const float off = (m_used == -INFINITY) ? 0.f : (kPShift - m_used);
+  float l0 = 0.f, u0 = 0.f, u1 = 0.f;
+#pragma unroll
+  for (int i = 0; i < 32; i += 4) {
+    float pv[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) pv[u] = (i + u <= lim) ? ex2_approx(fmaf(x[i + u], scale_log2, off)) : 0.f;
+    const uint32_t h01 = f32x2_to_e4m3x2(pv[0], pv[1]), h23 = f32x2_to_e4m3x2(pv[2], pv[3]);
+    const float2 a01 = e4m3x2_to_f32x2(h01), a23 = e4m3x2_to_f32x2(h23);
+    const uint32_t l01 = f32x2_to_e5m2x2(pv[0] - a01.x, pv[1] - a01.y);
+    const uint32_t l23 = f32x2_to_e5m2x2(pv[2] - a23.x, pv[3] - a23.y);
+    const float2 b01 = e5m2x2_to_f32x2(l01), b23 = e5m2x2_to_f32x2(l23);
+    l0 += (pv[0] + pv[1]) + (pv[2] + pv[3]);
+    u0 += (a01.x + b01.x) + (a23.x + b23.x);
+    u1 += (a01.y + b01.y) + (a23.y + b23.y);
+    phi[i >> 2] = h01 | (h23 << 16);
+    plo[i >> 2] = l01 | (l23 << 16);
+  }
+  l_sum += l0;
+  l_use += u0 + u1;
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -131,15 +204,15 @@ decode_partial_e4m3_kernel(const __grid_constant__ CUtensorMap tm_q, const __gri
   // programmatic dependent launch; griddepcontrol.wait below orders every input read).
   if (threadIdx.x == 0) {
     mbar_init(&ctrl->q_full, 1);
-    mbar_init(&ctrl->q_ready, kDecodeThreads);
-    for (int s = 0; s < 2; ++s) {
+    mbar_init(&ctrl->q_ready, kSoftmaxThreads);
+    for (int s = 0; s < kStages; ++s) {
       mbar_init(&ctrl->raw_full[s], 1);
-      mbar_init(&ctrl->raw_empty[s], 1 + kDecodeThreads);
+      mbar_init(&ctrl->raw_empty[s], 2);
+    }
+    for (int s = 0; s < 2; ++s) {
       mbar_init(&ctrl->s_full[s], 1);
       mbar_init(&ctrl->s_free[s], kSoftmaxThreads);
     }
-    mbar_init(&ctrl->v_full, kDecodeThreads);
-    mbar_init(&ctrl->v_empty, 1);
     mbar_init(&ctrl->p_full, kSoftmaxThreads);
     mbar_init(&ctrl->o_done, 1);
     mbar_init(&ctrl->mma_drain, 1);
@@ -148,11 +221,11 @@ decode_partial_e4m3_kernel(const __grid_constant__ CUtensorMap tm_q, const __gri
     for (int w = 0; w < 4; ++w) ctrl->rescale_flag[w] = 0;
     fence_mbarrier_init();
   }
-  if (warp == 5) {
+  if (warp == kBmm1Warp) {
     tmem_alloc(&ctrl->tmem_base, kTmemCols);
     tmem_relinquish();
   }
-  if (warp == 4 && lane == 0) {
+  if (warp == kProducerWarp && lane == 0) {
     tma_prefetch_desc(&tm_q);
     tma_prefetch_desc(&tm_kv);
   }
@@ -167,7 +240,7 @@ decode_partial_e4m3_kernel(const __grid_constant__ CUtensorMap tm_q, const __gri
   if (bad_len && threadIdx.x == 0 && split == 0 && group == 0) atomicOr(p.status, kStatusDeviceArg);
   const int kv_start = split * p.chunk;
   if (bad_len || kv_start >= L) {  // (CTA-uniform) a bad length, or this request needs fewer splits
-    if (warp == 5) tmem_dealloc(tmem, kTmemCols);
+    if (warp == kBmm1Warp) tmem_dealloc(tmem, kTmemCols);
     return;
   }
   const int kv_end = min(L, kv_start + p.chunk);
@@ -178,7 +251,7 @@ decode_partial_e4m3_kernel(const __grid_constant__ CUtensorMap tm_q, const __gri
   const int nq = (nrows + 15) & ~15;  // BMM2 N (multiple of 16)
   volatile int* abort_flag = &ctrl->abort_flag;
 
-  if (warp == 4) {
+  if (warp == kProducerWarp) {
     // ------------------------------------------------------------------ producer: Q, then raw tiles
     const int P = p.page_size;
     const int sub = P < kTileKeys ? kTileKeys / P : 1;  // pages per tile
@@ -192,8 +265,11 @@ decode_partial_e4m3_kernel(const __grid_constant__ CUtensorMap tm_q, const __gri
     const uint64_t pol_kv = policy_evict_first();
     const unsigned n_pages = static_cast<unsigned>(min(p.num_pages, static_cast<int64_t>(0x7fffffff)));
     bool bad_pid = false;
-    int last_issued[2] = {-1, -1};
+    int last_issued[kStages];
+#pragma unroll
+    for (int s = 0; s < kStages; ++s) last_issued[s] = -1;
     bool ok = true;
+    bool q_waited = false;
     if (lane == 0) {
       mbar_arrive_expect_tx(&ctrl->q_full, kQBf16Bytes);
       tma_load_3d(smem + kOffQBf16, &tm_q, &ctrl->q_full, 0, b * p.R + row0, 0, policy_evict_last());
@@ -209,9 +285,9 @@ decode_partial_e4m3_kernel(const __grid_constant__ CUtensorMap tm_q, const __gri
       prefetch_l2_bulk(p.kv_pool + (static_cast<int64_t>(pid) * P + k % P) * kLatentDim,
                        static_cast<uint32_t>(rows * kLatentDim));
     };
-    for (int jt = 2; jt < 2 + kPrefetchAhead; ++jt) prefetch_tile(jt);
+    for (int jt = kStages; jt < kStages + kPrefetchAhead; ++jt) prefetch_tile(jt);
     for (int j = 0; j < ntiles; ++j) {
-      const int s = j & 1;
+      const int s = j % kStages;
       const int k0 = kv_start + j * kTileKeys;
       const int pg0 = k0 / P;
       const int tile_end = min(k0 + kTileKeys, L);
@@ -240,9 +316,16 @@ decode_partial_e4m3_kernel(const __grid_constant__ CUtensorMap tm_q, const __gri
         bad_pid |= outside;
         pids[pp] = outside ? -1 : pids[pp];
       }
-      if (j >= 2) {
+      if (s >= 2 && !q_waited) {  // stages 2-3 hold the bf16 Q tile until it has been split
         bool w = true;
-        if (lane == 0) w = mbar_wait(&ctrl->raw_empty[s], ((j >> 1) - 1) & 1, abort_flag);
+        if (lane == 0) w = mbar_wait(&ctrl->q_ready, 0, abort_flag);
+        ok = __shfl_sync(0xffffffffu, w, 0);
+        q_waited = true;
+        if (!ok) break;
+      }
+      if (j >= kStages) {
+        bool w = true;
+        if (lane == 0) w = mbar_wait(&ctrl->raw_empty[s], ((j / kStages) - 1) & 1, abort_flag);
         ok = __shfl_sync(0xffffffffu, w, 0);
         if (!ok) break;
       }
@@ -260,49 +343,38 @@ decode_partial_e4m3_kernel(const __grid_constant__ CUtensorMap tm_q, const __gri
         }
       }
       last_issued[s] = j;
-      prefetch_tile(j + 2 + kPrefetchAhead);
+      prefetch_tile(j + kStages + kPrefetchAhead);
       __syncwarp();
     }
     if (bad_pid && lane == 0) atomicOr(p.status, kStatusDeviceArg);
     if (!ok && lane == 0) {
       drain_wait(&ctrl->q_full, 0);
-      for (int s = 0; s < 2; ++s)
-        if (last_issued[s] >= 0) drain_wait(&ctrl->raw_full[s], (last_issued[s] >> 1) & 1);
+      for (int s = 0; s < kStages; ++s)
+        if (last_issued[s] >= 0) drain_wait(&ctrl->raw_full[s], (last_issued[s] / kStages) & 1);
     }
-  } else if (warp == 5) {
+  } else if (warp == kBmm1Warp) {
     // ------------------------------------------------------------------ BMM1 issuer (whole warp,
     // uniform control flow; one elected thread issues the MMAs and their commits)
-    const uint32_t idesc1 = make_idesc_e4m3(64, 64);
-    const uint64_t qhi_desc = make_smem_desc_sw64(smem_u32(smem + kOffQ8));
-    const uint64_t qlo_desc = make_smem_desc_sw64(smem_u32(smem + kOffQ8 + kQPart));
+    const uint32_t idesc1 = make_idesc_e4m3(128, 64);
+    const uint64_t q_desc = make_smem_desc_sw64(smem_u32(smem + kOffQ8));
     bool ok = mbar_wait(&ctrl->q_ready, 0, abort_flag);
-    // BMM1(j) as soon as raw tile j has landed and its S buffer is free.  Issuing blocks
-    // while the tensor pipe is busy, so BMM2 has a warp of its own and is never held behind
-    // this warp's issue loop.
+    // BMM1(j) as soon as raw tile j has landed and its S buffer is free
     for (int j = 0; j < ntiles; ++j) {
-      const int s = j & 1, sb = j & 1;
-      if (ok) ok = mbar_wait(&ctrl->raw_full[s], (j >> 1) & 1, abort_flag);
+      const int s = j % kStages, sb = j & 1;
+      if (ok) ok = mbar_wait(&ctrl->raw_full[s], (j / kStages) & 1, abort_flag);
       if (ok && j >= 2) ok = mbar_wait(&ctrl->s_free[sb], ((j - 2) >> 1) & 1, abort_flag);
       if (!__all_sync(0xffffffffu, ok)) break;
       tc_fence_after();
       const uint64_t k_desc = make_smem_desc_sw64(smem_u32(smem + kOffRaw + s * kRawTile));
       const uint32_t d = tmem + kTmemS + sb * 64;
-      // the q descriptors pass through an empty asm on every issue, so that the compiler
-      // adds the 36 offsets here instead of keeping 36 precomputed descriptors live
-      uint64_t qh = qhi_desc, ql = qlo_desc;
-      asm volatile("" : "+l"(qh), "+l"(ql));
       if (elect_one()) {
-        // S = q_hi . k + q_lo . k: 2 x 9 blocks x 2 K-steps of 32 codes
+        // S_hi / S_lo (stacked rows) = [q_hi; q_lo] . k: 9 blocks x 2 K-steps of 32 codes
 #pragma unroll
-        for (int part = 0; part < 2; ++part) {
+        for (int c = 0; c < kBlocks; ++c) {
 #pragma unroll
-          for (int c = 0; c < kBlocks; ++c) {
-#pragma unroll
-            for (int k = 0; k < 2; ++k) {
-              const uint64_t off = static_cast<uint64_t>((c * kRawBlock + k * 32) >> 4);
-              umma_e4m3(d, (part == 0 ? qh : ql) + off, k_desc + off, idesc1, (part | c | k) != 0 ? 1u : 0u);
-            }
-          }
+          for (int k = 0; k < 2; ++k)
+            umma_f8(d, q_desc + static_cast<uint64_t>((c * kQ8Block + k * 32) >> 4),
+                      k_desc + static_cast<uint64_t>((c * kRawBlock + k * 32) >> 4), idesc1, (c | k) != 0 ? 1u : 0u);
         }
         umma_commit(&ctrl->s_full[sb]);
         umma_commit(&ctrl->raw_empty[s]);
@@ -317,27 +389,34 @@ decode_partial_e4m3_kernel(const __grid_constant__ CUtensorMap tm_q, const __gri
     __syncwarp();
   } else if (warp == kBmm2Warp) {
     // ------------------------------------------------------------------ BMM2 issuer
-    const uint32_t idesc2 = make_idesc_f16(128, nq, true, false);
-    const uint64_t p_desc = make_smem_desc(smem_u32(smem + kOffP), 16, 1024);
-    const uint64_t v_desc = make_smem_desc(smem_u32(smem + kOffV), kF16Block, 1024);
+    // O^T[value col, row] += V^T . P^T: A = V^T, MN-major straight from the raw stage (two
+    // 64-column blocks of 4 KB per 128-column chunk, 8-key groups 512 bytes apart); B = p_hi
+    // (e4m3) then p_lo (e5m2), K-major rows of 64 keys.
+    const uint32_t idesc2_hi = make_idesc_f8(128, nq, kF8E4M3, kF8E4M3, true, false);
+    const uint32_t idesc2_lo = make_idesc_f8(128, nq, kF8E4M3, kF8E5M2, true, false);
+    const uint64_t phi_desc = make_smem_desc_sw64(smem_u32(smem + kOffP));
+    const uint64_t plo_desc = make_smem_desc_sw64(smem_u32(smem + kOffP + kPPart));
     bool ok = true;
     for (int j = 0; j < ntiles; ++j) {
+      const int s = j % kStages;
       if (ok) ok = mbar_wait(&ctrl->p_full, j & 1, abort_flag);
-      if (ok) ok = mbar_wait(&ctrl->v_full, j & 1, abort_flag);
+      if (ok) ok = mbar_wait(&ctrl->raw_full[s], (j / kStages) & 1, abort_flag);
       if (!__all_sync(0xffffffffu, ok)) break;
       tc_fence_after();
+      const uint64_t v_desc = make_smem_desc_sw64(smem_u32(smem + kOffRaw + s * kRawTile), kRawBlock, 512);
       if (elect_one()) {
 #pragma unroll
         for (int qc = 0; qc < 4; ++qc) {
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const uint64_t voff = static_cast<uint64_t>((2 * qc * kF16Block + kk * 2048) >> 4);
+          for (int kk = 0; kk < 2; ++kk) {
+            const uint64_t voff = static_cast<uint64_t>((2 * qc * kRawBlock + kk * 2048) >> 4);
             const uint64_t poff = static_cast<uint64_t>((kk * 32) >> 4);
-            umma_bf16(tmem + qc * 64, v_desc + voff, p_desc + poff, idesc2, (j > 0 || kk > 0) ? 1u : 0u);
+            umma_f8(tmem + qc * 64, v_desc + voff, phi_desc + poff, idesc2_hi, (j > 0 || kk > 0) ? 1u : 0u);
+            umma_f8(tmem + qc * 64, v_desc + voff, plo_desc + poff, idesc2_lo, 1u);
           }
         }
         umma_commit(&ctrl->o_done);
-        umma_commit(&ctrl->v_empty);
+        umma_commit(&ctrl->raw_empty[s]);
       }
       __syncwarp();
     }
@@ -346,41 +425,41 @@ decode_partial_e4m3_kernel(const __grid_constant__ CUtensorMap tm_q, const __gri
       drain_wait(&ctrl->mma_drain2, 0);
     }
     __syncwarp();
-  } else if (warp >= kDecodeWarp0 && warp < kBmm2Warp) {
-    // ------------------------------------------------------------------ decode warps
-    const int dt = threadIdx.x - kDecodeWarp0 * 32;
-    bool ok = mbar_wait(&ctrl->q_full, 0, abort_flag);
-    if (ok) {
-      // Q split: row r is taken by kQThreadsPerRow adjacent threads; thread h of them takes
-      // bf16 chunks [8h/n, 8(h+1)/n) of every 64-column block (e4m3 chunks [4h/n, 4(h+1)/n)).
-      constexpr int kE8 = 4 / kQThreadsPerRow;  // e4m3 chunks (16 codes) per block for this thread
-      const int r = dt / kQThreadsPerRow, h = dt % kQThreadsPerRow;
+  } else if (warp < 4) {
+    // ------------------------------------------------------------------ softmax + epilogue (warps 0-3)
+    // Q split first: row r is taken by threads 2r and 2r+1; thread h of them takes bf16
+    // chunks [4h, 4h+4) of every 64-column block (e4m3 chunks 2h, 2h+1).  q_hi of row r goes
+    // to stacked row 32 (r / 16) + r % 16, q_lo 16 rows further.
+    bool failed = bar_or(1, kSoftmaxThreads, !mbar_wait(&ctrl->q_full, 0, abort_flag));
+    if (!failed) {
+      const int r = threadIdx.x >> 1, h = threadIdx.x & 1;
       const uint32_t qb = smem_u32(smem + kOffQBf16) + r * 128;
       float mx = 0.f;
       for (int c = 0; c < kBlocks; ++c) {
 #pragma unroll
-        for (int jj = 0; jj < 2 * kE8; ++jj) {
+        for (int jj = 0; jj < 4; ++jj) {
           uint32_t w[4];
           asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
                        : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
-                       : "r"(qb + c * kF16Block + (((2 * kE8 * h + jj) ^ (r & 7)) << 4)));
+                       : "r"(qb + c * kF16Block + (((4 * h + jj) ^ (r & 7)) << 4)));
 #pragma unroll
           for (int i = 0; i < 4; ++i)
             mx = fmaxf(mx, fmaxf(fabsf(__uint_as_float(w[i] << 16)), fabsf(__uint_as_float(w[i] & 0xFFFF0000u))));
         }
       }
-#pragma unroll
-      for (int o = 1; o < kQThreadsPerRow; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
       int sh = 0;  // the row's power-of-two scale: its largest |q| lands in [128, 256)
       if (mx > 0.f) sh = min(126, max(-120, 7 - (static_cast<int>((__float_as_uint(mx) >> 23) & 0xFFu) - 127)));
       const float mult = __uint_as_float(static_cast<uint32_t>(sh + 127) << 23);
       if (h == 0) ctrl->q_unscale[r] = __uint_as_float(static_cast<uint32_t>(127 - sh) << 23);
-      const uint32_t qhi = smem_u32(smem + kOffQ8) + r * 64;
-      const int sw8 = (r >> 1) & 3;  // the 64-byte swizzle of row r
+      const int m_hi = 32 * (r >> 4) + (r & 15);  // stacked row of q_hi (q_lo: m_hi + 16)
+      const uint32_t qhi = smem_u32(smem + kOffQ8) + m_hi * 64;
+      const uint32_t qlo = qhi + 16 * 64;
+      const int sw8 = (m_hi >> 1) & 3;  // the 64-byte swizzle of both stacked rows
       for (int c = 0; c < kBlocks; ++c) {
 #pragma unroll
-        for (int e2 = 0; e2 < kE8; ++e2) {
-          const int e = kE8 * h + e2;  // e4m3 chunk (16 codes) = bf16 chunks 2e and 2e+1
+        for (int e2 = 0; e2 < 2; ++e2) {
+          const int e = 2 * h + e2;  // e4m3 chunk (16 codes) = bf16 chunks 2e and 2e+1
           uint32_t w[8];
           asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
                        : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
@@ -402,59 +481,20 @@ decode_partial_e4m3_kernel(const __grid_constant__ CUtensorMap tm_q, const __gri
             hi4[i >> 1] = h01 | (h23 << 16);
             lo4[i >> 1] = l01 | (l23 << 16);
           }
-          const uint32_t off = c * kRawBlock + ((e ^ sw8) << 4);
+          const uint32_t off = c * kQ8Block + ((e ^ sw8) << 4);
           st_shared_v4(qhi + off, hi4[0], hi4[1], hi4[2], hi4[3]);
-          st_shared_v4(qhi + kQPart + off, lo4[0], lo4[1], lo4[2], lo4[3]);
+          st_shared_v4(qlo + off, lo4[0], lo4[1], lo4[2], lo4[3]);
         }
       }
       fence_proxy_async_smem();
     }
-    // every decode thread has read the bf16 Q tile before any writes the V stage over it
-    named_bar_sync(2, kDecodeThreads);
-    if (ok) mbar_arrive(&ctrl->q_ready);
-    // V decode: raw chunk q = dt + kDecodeThreads i of the tile's eight value blocks (2048
-    // chunks): block q / 256, row (q % 256) / 4, 16-code chunk q % 4 -> two 16-byte f16
-    // chunks of the row.
-    // The raw V bytes of tile j go to registers as soon as the tile lands, and the raw stage
-    // is released at once (BMM1 releases it too): its refill need not wait for the V stage,
-    // which frees only when BMM2(j - 1) completes.  Then the f16 values are written.
-    constexpr int kPerThread = 2048 / kDecodeThreads;
-    for (int j = 0; ok && j < ntiles; ++j) {
-      const int s = j & 1;
-      ok = mbar_wait(&ctrl->raw_full[s], (j >> 1) & 1, abort_flag);
-      if (!ok) break;
-      const int valid_rows = L - (kv_start + j * kTileKeys);  // rows past the request end become zeros
-      const uint32_t raw = smem_u32(smem + kOffRaw + s * kRawTile);
-      uint4 w[kPerThread];
-#pragma unroll
-      for (int i = 0; i < kPerThread; ++i) {
-        const int q = dt + kDecodeThreads * i;
-        const int blk = q >> 8, row = (q >> 2) & 63, jc = q & 3;
-        w[i] = make_uint4(0u, 0u, 0u, 0u);
-        if (row < valid_rows) {
-          asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                       : "=r"(w[i].x), "=r"(w[i].y), "=r"(w[i].z), "=r"(w[i].w)
-                       : "r"(raw + blk * kRawBlock + row * 64 + ((jc ^ ((row >> 1) & 3)) << 4)));
-        }
-      }
-      mbar_arrive(&ctrl->raw_empty[s]);
-      if (j >= 1) ok = mbar_wait(&ctrl->v_empty, (j - 1) & 1, abort_flag);
-      if (!ok) break;
-      const uint32_t vst = smem_u32(smem + kOffV);
-#pragma unroll
-      for (int i = 0; i < kPerThread; ++i) {
-        const int q = dt + kDecodeThreads * i;
-        const int blk = q >> 8, row = (q >> 2) & 63, jc = q & 3;
-        store_f16_chunk(vst + blk * kF16Block + row * 128 + jc * 32, (row & 7) << 4, w[i]);
-      }
-      fence_proxy_async_smem();
-      mbar_arrive(&ctrl->v_full);
-    }
-  } else {
-    // ------------------------------------------------------------------ softmax + epilogue (warps 0-3)
-    // BMM1 runs with M = 64: folded row r lives in TMEM lane 32*(r/16) + r%16, so warp w
-    // owns rows 16w .. 16w+15.  Each row is split between lanes i and i+16 of its warp:
-    // lane i takes keys 0-31 of every tile, lane i+16 keys 32-63.
+    // every softmax thread has read the bf16 Q tile (ring stages 2-3) and written its split
+    named_bar_sync(1, kSoftmaxThreads);
+    if (!failed) mbar_arrive(&ctrl->q_ready);
+
+    // BMM1 (M = 128) puts row r's hi / lo partial scores in TMEM lanes 32*(r/16) + r%16 and
+    // 16 further, so warp w owns rows 16w .. 16w+15.  Lane i (< 16) keeps keys 0-31 of its
+    // row, lane i+16 keys 32-63; each takes the other half's partial scores by a shuffle.
     const int half = lane >> 4;
     const bool row_lane = half == 0;
     const int r = warp * 16 + (lane & 15);
@@ -463,49 +503,66 @@ decode_partial_e4m3_kernel(const __grid_constant__ CUtensorMap tm_q, const __gri
     const int lim_abs = L - p.T + t;  // last visible key of this row
     const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
     float m_used = -INFINITY;
-    float l_sum = 0.f;
-    // the rows' 2^-s are written once q_ready completes (CTA-uniform over the four warps,
-    // since every later barrier among them counts all 128 threads)
-    bool failed = bar_or(1, kSoftmaxThreads, !mbar_wait(&ctrl->q_ready, 0, abort_flag));
-    // S holds (q 2^s) . k_code: the row's 2^-s and kv_scale (in p.scale_log2) return here.
-    // V is decoded as codes times 2^-8 (exact); that factor returns in the output scale.
+    float l_sum = 0.f, l_use = 0.f;
+    // S holds (q 2^s) . k_code: the row's 2^-s and kv_scale (in p.scale_log2) return here;
+    // P carries 2^kPShift, which cancels in O / l and returns in the LSE.
     const float scale_log2 = failed ? 0.f : p.scale_log2 * ctrl->q_unscale[r];
-    const float v_scale = p.v_scale * 256.f;
+    const float v_scale = p.v_scale;
+    const uint32_t p_row = smem_u32(smem + kOffP) + r * 64;
+    const int p_sw = (r >> 1) & 3;
 
     for (int j = 0; !failed && j < ntiles; ++j) {
       const int sb = j & 1;
+      const int s = j % kStages;
       const int k0 = kv_start + j * kTileKeys;
       bool need_rescale = false;
       float alpha = 1.f;
-      uint32_t packed[16];
+      uint32_t phi[8], plo[8];
       bool fail = !mbar_wait(&ctrl->s_full[sb], (j >> 1) & 1, abort_flag);
       fail = __any_sync(0xffffffffu, fail);
       if (!fail) {
         tc_fence_after();
-        uint32_t sr[32];
-        tmem_ld16x32bx2_32(tmem + lane_base + kTmemS + sb * 64, sr);
+        uint32_t sa[32], sz[32];
+        tmem_ld32(tmem + lane_base + kTmemS + sb * 64, sa);
+        tmem_ld32(tmem + lane_base + kTmemS + sb * 64 + 32, sz);
         tmem_ld_wait();
         tc_fence_before();
         mbar_arrive(&ctrl->s_free[sb]);
+        float x[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const uint32_t mine = half ? sz[i] : sa[i];
+          const uint32_t other = __shfl_xor_sync(0xffffffffu, half ? sa[i] : sz[i], 16);
+          x[i] = __uint_as_float(mine) + __uint_as_float(other);
+        }
         const int lim = row_active ? (min(kv_end - 1, lim_abs) - k0 - 32 * half) : -1;
-        online_softmax_step<32, true, true>(sr, lim, scale_log2, kRescaleThreshold, m_used, l_sum, packed, alpha,
-                                            need_rescale);
+        softmax_step_e4m3(x, lim, scale_log2, m_used, l_sum, l_use, phi, plo, alpha, need_rescale);
       }
       if (!fail && j >= 1) {
         fail = !mbar_wait(&ctrl->o_done, (j - 1) & 1, abort_flag);
         fail = __any_sync(0xffffffffu, fail);
       }
       if (!fail) {
-        const uint32_t row_addr = smem_u32(smem + kOffP) + r * 128;
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const int chunk = 4 * half + c;
-          st_shared_v4(row_addr + ((chunk ^ (r & 7)) << 4), packed[4 * c], packed[4 * c + 1], packed[4 * c + 2],
-                       packed[4 * c + 3]);
+        for (int c = 0; c < 2; ++c) {
+          const uint32_t off = ((2 * half + c) ^ p_sw) << 4;
+          st_shared_v4(p_row + off, phi[4 * c], phi[4 * c + 1], phi[4 * c + 2], phi[4 * c + 3]);
+          st_shared_v4(p_row + kPPart + off, plo[4 * c], plo[4 * c + 1], plo[4 * c + 2], plo[4 * c + 3]);
         }
         if (row_lane) ctrl->alpha[r] = alpha;
         const bool any = __any_sync(0xffffffffu, need_rescale);
         if (lane == 0) ctrl->rescale_flag[warp] = any ? 1 : 0;
+        // the request's last tile: rows past its end are zeroed in the V blocks (BMM1 of this
+        // tile has completed; BMM2 reads them only after p_full)
+        const int valid_rows = L - k0;
+        if (valid_rows < kTileKeys) {
+          const uint32_t stage = smem_u32(smem + kOffRaw + s * kRawTile);
+          const int n16 = (kTileKeys - valid_rows) * 4 * (kValueDim / 64);  // 16-byte pieces
+          for (int i = threadIdx.x; i < n16; i += kSoftmaxThreads) {
+            const int row = valid_rows + (i >> 5), blk = (i >> 2) & 7, piece = i & 3;
+            st_shared_v4(stage + blk * kRawBlock + row * 64 + piece * 16, 0u, 0u, 0u, 0u);
+          }
+        }
       }
       fence_proxy_async_smem();
       if (bar_or(1, kSoftmaxThreads, fail || (*abort_flag != 0))) {
@@ -552,10 +609,11 @@ decode_partial_e4m3_kernel(const __grid_constant__ CUtensorMap tm_q, const __gri
       tc_fence_after();
       const bool final_out = (nsplit_b == 1);
       l_sum += __shfl_xor_sync(0xffffffffu, l_sum, 16);  // the two halves' partial row sums
+      l_use += __shfl_xor_sync(0xffffffffu, l_use, 16);
       if (row_lane) {
-        const float lse2 = (l_sum > 0.f) ? (m_used + __log2f(l_sum)) : -INFINITY;
+        const float lse2 = (l_sum > 0.f) ? (m_used + __log2f(l_sum) - kPShift) : -INFINITY;
         const float lse_nat = lse2 * 0.69314718055994530942f;
-        ctrl->row_scale[r] = (l_sum > 0.f) ? (v_scale / l_sum) : 0.f;
+        ctrl->row_scale[r] = (l_use > 0.f) ? (v_scale / l_use) : 0.f;
         if (row_active) {
           const int64_t grow = static_cast<int64_t>(b) * p.R + row0 + r;
           if (final_out)
@@ -565,9 +623,9 @@ decode_partial_e4m3_kernel(const __grid_constant__ CUtensorMap tm_q, const __gri
         }
       }
       named_bar_sync(1, kSoftmaxThreads);
-      // Normalised O (bf16) is transposed through the V stage (free once the last BMM2 has
-      // completed) so that global stores are whole 16-byte row chunks.
-      const uint32_t stage_s = smem_u32(smem + kOffV);  // [64][512] bf16
+      // Normalised O (bf16) is transposed through ring stages 0-1 (free once the last BMM2
+      // has completed) so that global stores are whole 16-byte row chunks.
+      const uint32_t stage_s = smem_u32(smem + kOffOStage);  // [64][512] bf16
       // rows 32hh .. 32hh+31 at a time: their 32 scales stay in registers (shared-memory
       // loads interleaved with the staging stores would each wait for the stores before them)
 #pragma unroll 1
@@ -595,7 +653,7 @@ decode_partial_e4m3_kernel(const __grid_constant__ CUtensorMap tm_q, const __gri
           }
         }
       }
-      const __nv_bfloat16* stage_h = reinterpret_cast<const __nv_bfloat16*>(smem + kOffV);
+      const __nv_bfloat16* stage_h = reinterpret_cast<const __nv_bfloat16*>(smem + kOffOStage);
       named_bar_sync(1, kSoftmaxThreads);
       constexpr int kChunksPerRow = kValueDim * 2 / 16;
       __nv_bfloat16* dst = final_out
@@ -614,7 +672,7 @@ decode_partial_e4m3_kernel(const __grid_constant__ CUtensorMap tm_q, const __gri
   if (threadIdx.x == 0 && ctrl->abort_flag == kAbortTimeout) atomicOr(p.status, kStatusTimeout);
   // every store of this CTA is issued: the combine grid may be scheduled now
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  if (warp == 5) {
+  if (warp == kBmm1Warp) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }

@@ -215,28 +215,44 @@ __device__ __forceinline__ uint64_t make_smem_desc(uint32_t saddr, uint32_t lbo_
   return d;
 }
 
-// The same with 64-byte swizzle (layout code 4): K-major tiles of 8-bit elements, 64 bytes
-// per row, whose 8-row core-matrix groups are 512 bytes apart.
+// The same with 64-byte swizzle (layout code 4), for 8-bit elements in 64-byte rows.
+// K-major (the defaults): 8-row core-matrix groups 512 bytes apart, LBO unused.  MN-major
+// (64 MN-contiguous elements per row, one row per K index): LBO = the byte stride between
+// 64-element MN blocks, SBO = the stride between groups of 8 K rows.
 constexpr uint32_t kSwizzle64B = 4;
 
-__device__ __forceinline__ uint64_t make_smem_desc_sw64(uint32_t saddr) {
+__device__ __forceinline__ uint64_t make_smem_desc_sw64(uint32_t saddr, uint32_t lbo_bytes = 16,
+                                                        uint32_t sbo_bytes = 512) {
   uint64_t d = 0;
   d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
-  d |= static_cast<uint64_t>(16 >> 4) << 16;
-  d |= static_cast<uint64_t>(512 >> 4) << 32;
+  d |= static_cast<uint64_t>((lbo_bytes >> 4) & 0x3FFFu) << 16;
+  d |= static_cast<uint64_t>((sbo_bytes >> 4) & 0x3FFFu) << 32;
   d |= static_cast<uint64_t>(1) << 46;
   d |= static_cast<uint64_t>(kSwizzle64B) << 61;
   return d;
 }
 
-// kind::f8f6f4 instruction descriptor: fp32 accumulator, e4m3 A and B (format code 0 in
-// bits 7-9 and 10-12), both K-major, dense; K = 32 elements per MMA.
-__host__ __device__ constexpr uint32_t make_idesc_e4m3(int M, int N) {
-  return (1u << 4) | (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+// kind::f8f6f4 instruction descriptor: fp32 accumulator, dense; K = 32 elements per MMA.
+// Bits 7-9 / 10-12: A / B format (0 = e4m3, 1 = e5m2; the two may differ in this kind);
+// bits 15 / 16: A / B MN-major.
+constexpr uint32_t kF8E4M3 = 0;
+constexpr uint32_t kF8E5M2 = 1;
+
+__host__ __device__ constexpr uint32_t make_idesc_f8(int M, int N, uint32_t a_fmt, uint32_t b_fmt,
+                                                     bool a_mn_major = false, bool b_mn_major = false) {
+  return (1u << 4) | (a_fmt << 7) | (b_fmt << 10) | ((a_mn_major ? 1u : 0u) << 15) |
+         ((b_mn_major ? 1u : 0u) << 16) | (static_cast<uint32_t>(N >> 3) << 17) |
+         (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// e4m3 A and B.
+__host__ __device__ constexpr uint32_t make_idesc_e4m3(int M, int N, bool a_mn_major = false,
+                                                       bool b_mn_major = false) {
+  return make_idesc_f8(M, N, kF8E4M3, kF8E4M3, a_mn_major, b_mn_major);
 }
 
 // D[tmem] (+)= A[smem desc] * B[smem desc] on 8-bit operands (kind::f8f6f4).
-__device__ __forceinline__ void umma_e4m3(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+__device__ __forceinline__ void umma_f8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                                           uint32_t accumulate) {
   asm volatile(
       "{\n\t.reg .pred p;\n\t"

@@ -235,6 +235,35 @@ def test_decode_e4m3_query_split_error_bound(mla, oracle_mod):
     assert (np.abs(lse - ref_lse) <= bound).all()
 
 
+def test_decode_e4m3_dominant_key_over_long_tail(mla, oracle_mod):
+    """The e4m3 kernel feeds P to its second GEMM in two 8-bit parts (e4m3 hi, e5m2 lo).
+    Each head's query points at one key of its request, so that key's score stands 12 to
+    19.5 above the others in the log2 domain (head h: 12 + h/2) and thousands of keys sit
+    near 2^-12 .. 2^-19.5 of the row max: a tail that holds up to a few percent of the row's
+    mass, which an e4m3 low part would flush to zero below 2^-15.  Every row's output
+    within the relative-L2 bound of the oracle's, and the usual bounds overall."""
+    wl = DecodeWorkload("long_tail", 2, 2, 16, [4096, 3000], kv_dtype="e4m3", seed=97)
+    inp = make_decode_inputs(wl, "cpu")
+    P = wl.page_size
+    keys = inp.kv_pool.view(torch.float8_e4m3fn).double() * inp.kv_scale
+    q = torch.empty(2, 2, 16, 576, dtype=torch.float64)
+    for b, L in enumerate(wl.seq_lens):
+        pos = L // 3
+        kd = keys[int(inp.page_table[b, pos // P]), pos % P]
+        for h in range(16):
+            gap_log2 = 12.0 + 0.5 * h
+            q[b, :, h] = kd * (gap_log2 * math.log(2.0) / (inp.scale * float(kd @ kd)))
+    inp.q = q.to(torch.bfloat16)
+    out, lse, _ = run_gpu(mla, inp)
+    ref_out, ref_lse = oracle_mod.mla_decode(inp.q, inp.kv_pool, inp.page_table, inp.seq_lens, inp.scale,
+                                             kv_scale=inp.kv_scale)
+    check(out, lse, ref_out, ref_lse, fp8=True)
+    o = out.reshape(-1, 512)
+    r = ref_out.reshape(-1, 512)
+    row_rel = np.linalg.norm(o - r, axis=1) / np.linalg.norm(r, axis=1)
+    assert row_rel.max() <= REL_L2, f"worst row rel-L2 {row_rel.max():.3e}"
+
+
 def test_decode_page_shuffle_invariance_bitwise(mla):
     wl = DecodeWorkload("shuffle", 2, 4, 16, [1500, 777], seed=5, extra_pages=7)
     inp = make_decode_inputs(wl, "cpu")

@@ -9,8 +9,8 @@
 // bandwidth-bound); launch-blog repost "英偉達力薦，小團隊兩個月開源一款「光速級」智能體推理引擎",
 // section "TokenSpeed 性能預覽" (query-sequence axis folded into the head axis).
 //
-// Design on sm_103a (one CTA per (64-row group, split, request); one CTA per SM; 224
-// threads: softmax warps 0-3, producer warp 4, BMM1 warp 5, BMM2 warp 6).  Both GEMMs run on
+// Design on sm_103a (one CTA per (64-row group, split, request); one CTA per SM; 352
+// threads: softmax warps 0-7, producer warp 8, BMM1 warp 9, BMM2 warp 10).  Both GEMMs run on
 // the 8-bit codes as they arrive (kind::f8f6f4); nothing is decoded to a wider type:
 //  * The raw e4m3 tile (64 keys x 576 codes, 36 KB) arrives by TMA (64-byte swizzle) in a
 //    4-stage ring, its rows prefetched into L2 ahead of the load.
@@ -41,10 +41,12 @@
 //  * BMM1 and BMM2 are issued by two warps, each waiting on its own inputs: issuing blocks
 //    while the tensor pipe is busy.
 //  * Shared memory: stacked q_hi / q_lo (72 KB) | raw ring (4 x 36 KB) | p_hi, p_lo
-//    (2 x 4 KB).  The bf16 Q tile lands by TMA on ring stages 2-3 and is split from there
+//    (2 x 4 KB) | control (2 KB): 227 KB.  The bf16 Q tile lands by TMA on ring stages 2-3 and is split from there
 //    before their first load; the epilogue stages the bf16 output in stages 0-1.
-//  * Softmax and epilogue: each row split over two lanes of a warp (keys 0-31, 32-63),
-//    lazy rescale, bf16 output or split partial for the combine kernel (a programmatic
+//  * Softmax and epilogue: eight warps, two per TMEM lane quadrant, so that two warps share
+//    each scheduler (one alone left most of its cycles to latency).  Each row's 64 keys are
+//    spread over four threads (16 each); P is formed and split in f16x2 arithmetic; lazy
+//    rescale; bf16 output or split partial for the combine kernel (a programmatic
 //    dependent launch).
 // Every wait is bounded; on expiry the CTA records a timeout in the status word, drains
 // its in-flight copies and MMAs, frees TMEM and returns.
@@ -74,13 +76,14 @@ constexpr int kOffOStage = kOffRaw;                // [64][512] bf16 output stag
 static_assert(kOffQBf16 + kQBf16Bytes == kOffP, "bf16 Q staging spans ring stages 2-3 exactly");
 static_assert(kGroupRows * kValueDim * 2 <= 2 * kRawTile, "output staging fits ring stages 0-1");
 
-constexpr int kSoftmaxThreads = 128;
-constexpr int kProducerWarp = 4;
-constexpr int kBmm1Warp = 5;
-constexpr int kBmm2Warp = 6;
+constexpr int kSoftmaxWarps = 8;  // two per TMEM lane quadrant, one per half of the key tile
+constexpr int kSoftmaxThreads = 32 * kSoftmaxWarps;
+constexpr int kProducerWarp = kSoftmaxWarps;
+constexpr int kBmm1Warp = kSoftmaxWarps + 1;
+constexpr int kBmm2Warp = kSoftmaxWarps + 2;
 constexpr int kThreads = 32 * (kBmm2Warp + 1);
-constexpr int kQThreadsPerRow = kSoftmaxThreads / kGroupRows;  // 2 adjacent threads per Q row
-static_assert(kQThreadsPerRow == 2, "Q split threads per row");
+constexpr int kQThreadsPerRow = kSoftmaxThreads / kGroupRows;  // 4 adjacent threads per Q row
+static_assert(kQThreadsPerRow == 4, "Q split threads per row");
 
 struct Ctrl {
   uint64_t q_full;             // bf16 Q tile landed (TMA)
@@ -95,13 +98,18 @@ struct Ctrl {
   uint64_t mma_drain2;         // the BMM2 warp's MMAs
   uint32_t tmem_base;
   int abort_flag;
-  int rescale_flag[4];
+  alignas(16) int rescale_flag[kSoftmaxWarps];
   alignas(16) float alpha[kGroupRows];
+  // [0][half of the key tile][row]: partial row maxima of a tile, swapped between the two
+  // warps of a lane quadrant; at the end [0] and [1] hold the halves' row sums l / l_use
+  float red[2][2][kGroupRows];
   alignas(16) float row_scale[kGroupRows];
   alignas(16) float q_unscale[kGroupRows];  // 2^-s of each row's Q split
 };
-constexpr int kSmemBytes = kOffCtrl + 1024 + 1024;  // + control block + alignment slack
-static_assert(sizeof(Ctrl) <= 1024, "control block");
+constexpr int kCtrlBytes = 2048;
+constexpr int kSmemBytes = kOffCtrl + kCtrlBytes + 1024;  // + control block + alignment slack
+static_assert(sizeof(Ctrl) <= kCtrlBytes, "control block");
+static_assert(kSmemBytes <= 232448, "shared memory per block");
 
 constexpr int kPrefetchAhead = 2;  // raw tiles are prefetched into L2 this many tiles beyond the ring
 constexpr int kAbortTimeout = 1;
@@ -127,64 +135,65 @@ __device__ __forceinline__ float2 e4m3x2_to_f32x2(uint32_t codes) {
   return __half22float2(*reinterpret_cast<const __half2*>(&h2));
 }
 
-// The same pair of conversions for e5m2.
-__device__ __forceinline__ uint32_t f32x2_to_e5m2x2(float lo, float hi) {
+__device__ __forceinline__ uint32_t f16x2_to_e4m3x2(uint32_t h) {
   uint16_t r;
-  asm("cvt.rn.satfinite.e5m2x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(r) : "r"(h));
   return r;
 }
 
-__device__ __forceinline__ float2 e5m2x2_to_f32x2(uint32_t codes) {
-  uint32_t h2;
-  asm("{\n\t.reg .b16 c;\n\tcvt.u16.u32 c, %1;\n\tcvt.rn.f16x2.e5m2x2 %0, c;\n\t}" : "=r"(h2) : "r"(codes));
-  return __half22float2(*reinterpret_cast<const __half2*>(&h2));
+__device__ __forceinline__ uint32_t f16x2_to_e5m2x2(uint32_t h) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e5m2x2.f16x2 %0, %1;" : "=h"(r) : "r"(h));
+  return r;
 }
 
-// One online-softmax step over this lane's 32 scores x[] of its row (the row's other 32
-// keys are in lane ^ 16, which takes the same running-state decisions).  Keys i <= lim are
-// visible.  P 2^kPShift goes out as e4m3 hi and e5m2 lo codes (4 per word, key order).  l_sum
-// accumulates the fp32 P (for the LSE), l_use the hi + lo values the MMAs take (for the
-// output's normalisation, so that the split's rounding of a dominant key cancels in O / l).
-__device__ __forceinline__ void softmax_step_e4m3(const float (&x)[32], int lim, float scale_log2, float& m_used,
-                                                  float& l_sum, float& l_use, uint32_t (&phi)[8],
-                                                  uint32_t (&plo)[8], float& alpha, bool& need_rescale) {
-  float mx = -INFINITY;
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t codes) {
+  uint32_t h2;
+  asm("{\n\t.reg .b16 c;\n\tcvt.u16.u32 c, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, c;\n\t}" : "=r"(h2) : "r"(codes));
+  return h2;
+}
+
+__device__ __forceinline__ uint32_t e5m2x2_to_f16x2(uint32_t codes) {
+  uint32_t h2;
+  asm("{\n\t.reg .b16 c;\n\tcvt.u16.u32 c, %1;\n\tcvt.rn.f16x2.e5m2x2 %0, c;\n\t}" : "=r"(h2) : "r"(codes));
+  return h2;
+}
+
+// P 2^kPShift for this thread's 16 keys of its row (keys i <= lim visible; kAll: all of
+// them), split into e4m3 hi and e5m2 lo codes (4 per word, key order) through f16: the f16
+// value keeps 11 bits, and hi, the residual (exact in f16: hi is within a factor of 2 of
+// the value, or zero) and lo are formed there.  l_sum accumulates the fp32 P 2^kPShift (for
+// the LSE), l_use the hi + lo values the MMAs take (for the output's normalisation, so that
+// the split's rounding of a dominant key cancels in O / l).
+template <bool kAll>
+__device__ __forceinline__ void p_split16(const float (&x)[16], int lim, float scale_log2, float off, float& l_sum,
+                                          float& l_use, uint32_t (&phi)[4], uint32_t (&plo)[4]) {
+  float ls = 0.f, lu = 0.f;
 #pragma unroll
-  for (int i = 0; i < 32; ++i)
-    if (i <= lim) mx = fmaxf(mx, x[i]);
-  mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-  const float mt = mx * scale_log2;  // scale > 0: max commutes with the scaling; -inf stays -inf
-  alpha = 1.f;
-  need_rescale = false;
-  if (m_used == -INFINITY) {
-    m_used = mt;  // first contributing tile: nothing accumulated yet
-  } else if (mt > m_used + kRescaleThreshold) {
-    alpha = ex2_approx(m_used - mt);
-    need_rescale = true;
-    l_sum *= alpha;
-    l_use *= alpha;
-    m_used = mt;
+  for (int i = 0; i < 16; i += 4) {
+    uint32_t h8[2], l8[2];
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const int k = i + 2 * u;
+      const float p0 = (kAll || k <= lim) ? ex2_approx(fmaf(x[k], scale_log2, off)) : 0.f;
+      const float p1 = (kAll || k + 1 <= lim) ? ex2_approx(fmaf(x[k + 1], scale_log2, off)) : 0.f;
+      ls += p0 + p1;
+      const uint32_t ph = pack_f16x2(p0, p1);
+      h8[u] = f16x2_to_e4m3x2(ph);
+      const uint32_t hb = e4m3x2_to_f16x2(h8[u]);
+      uint32_t d, sum;
+      asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(ph), "r"(hb));
+      l8[u] = f16x2_to_e5m2x2(d);
+      const uint32_t lb = e5m2x2_to_f16x2(l8[u]);
+      asm("add.rn.f16x2 %0, %1, %2;" : "=r"(sum) : "r"(hb), "r"(lb));
+      const float2 uf = __half22float2(*reinterpret_cast<const __half2*>(&sum));
+      lu += uf.x + uf.y;
+    }
+    phi[i >> 2] = h8[0] | (h8[1] << 16);
+    plo[i >> 2] = l8[0] | (l8[1] << 16);
   }
-  const float off = (m_used == -INFINITY) ? 0.f : (kPShift - m_used);
-  float l0 = 0.f, u0 = 0.f, u1 = 0.f;
-#pragma unroll
-  for (int i = 0; i < 32; i += 4) {
-    float pv[4];
-#pragma unroll
-    for (int u = 0; u < 4; ++u) pv[u] = (i + u <= lim) ? ex2_approx(fmaf(x[i + u], scale_log2, off)) : 0.f;
-    const uint32_t h01 = f32x2_to_e4m3x2(pv[0], pv[1]), h23 = f32x2_to_e4m3x2(pv[2], pv[3]);
-    const float2 a01 = e4m3x2_to_f32x2(h01), a23 = e4m3x2_to_f32x2(h23);
-    const uint32_t l01 = f32x2_to_e5m2x2(pv[0] - a01.x, pv[1] - a01.y);
-    const uint32_t l23 = f32x2_to_e5m2x2(pv[2] - a23.x, pv[3] - a23.y);
-    const float2 b01 = e5m2x2_to_f32x2(l01), b23 = e5m2x2_to_f32x2(l23);
-    l0 += (pv[0] + pv[1]) + (pv[2] + pv[3]);
-    u0 += (a01.x + b01.x) + (a23.x + b23.x);
-    u1 += (a01.y + b01.y) + (a23.y + b23.y);
-    phi[i >> 2] = h01 | (h23 << 16);
-    plo[i >> 2] = l01 | (l23 << 16);
-  }
-  l_sum += l0;
-  l_use += u0 + u1;
+  l_sum += ls;
+  l_use += lu;
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -218,7 +227,7 @@ decode_partial_e4m3_kernel(const __grid_constant__ CUtensorMap tm_q, const __gri
     mbar_init(&ctrl->mma_drain, 1);
     mbar_init(&ctrl->mma_drain2, 1);
     ctrl->abort_flag = 0;
-    for (int w = 0; w < 4; ++w) ctrl->rescale_flag[w] = 0;
+    for (int w = 0; w < kSoftmaxWarps; ++w) ctrl->rescale_flag[w] = 0;
     fence_mbarrier_init();
   }
   if (warp == kBmm1Warp) {
@@ -425,29 +434,30 @@ decode_partial_e4m3_kernel(const __grid_constant__ CUtensorMap tm_q, const __gri
       drain_wait(&ctrl->mma_drain2, 0);
     }
     __syncwarp();
-  } else if (warp < 4) {
-    // ------------------------------------------------------------------ softmax + epilogue (warps 0-3)
-    // Q split first: row r is taken by threads 2r and 2r+1; thread h of them takes bf16
-    // chunks [4h, 4h+4) of every 64-column block (e4m3 chunks 2h, 2h+1).  q_hi of row r goes
-    // to stacked row 32 (r / 16) + r % 16, q_lo 16 rows further.
+  } else if (warp < kSoftmaxWarps) {
+    // ------------------------------------------------------------------ softmax + epilogue (warps 0-7)
+    // Q split first: row r is taken by threads 4r .. 4r+3; thread h of them takes bf16
+    // chunks 2h, 2h+1 of every 64-column block (e4m3 chunk h).  q_hi of row r goes to stacked
+    // row 32 (r / 16) + r % 16, q_lo 16 rows further.
     bool failed = bar_or(1, kSoftmaxThreads, !mbar_wait(&ctrl->q_full, 0, abort_flag));
     if (!failed) {
-      const int r = threadIdx.x >> 1, h = threadIdx.x & 1;
+      const int r = threadIdx.x >> 2, h = threadIdx.x & 3;
       const uint32_t qb = smem_u32(smem + kOffQBf16) + r * 128;
       float mx = 0.f;
       for (int c = 0; c < kBlocks; ++c) {
 #pragma unroll
-        for (int jj = 0; jj < 4; ++jj) {
+        for (int jj = 0; jj < 2; ++jj) {
           uint32_t w[4];
           asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
                        : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
-                       : "r"(qb + c * kF16Block + (((4 * h + jj) ^ (r & 7)) << 4)));
+                       : "r"(qb + c * kF16Block + (((2 * h + jj) ^ (r & 7)) << 4)));
 #pragma unroll
           for (int i = 0; i < 4; ++i)
             mx = fmaxf(mx, fmaxf(fabsf(__uint_as_float(w[i] << 16)), fabsf(__uint_as_float(w[i] & 0xFFFF0000u))));
         }
       }
       mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
       int sh = 0;  // the row's power-of-two scale: its largest |q| lands in [128, 256)
       if (mx > 0.f) sh = min(126, max(-120, 7 - (static_cast<int>((__float_as_uint(mx) >> 23) & 0xFFu) - 127)));
       const float mult = __uint_as_float(static_cast<uint32_t>(sh + 127) << 23);
@@ -455,36 +465,31 @@ decode_partial_e4m3_kernel(const __grid_constant__ CUtensorMap tm_q, const __gri
       const int m_hi = 32 * (r >> 4) + (r & 15);  // stacked row of q_hi (q_lo: m_hi + 16)
       const uint32_t qhi = smem_u32(smem + kOffQ8) + m_hi * 64;
       const uint32_t qlo = qhi + 16 * 64;
-      const int sw8 = (m_hi >> 1) & 3;  // the 64-byte swizzle of both stacked rows
+      const uint32_t e_off = (h ^ ((m_hi >> 1) & 3)) << 4;  // chunk h under both rows' 64-byte swizzle
       for (int c = 0; c < kBlocks; ++c) {
+        uint32_t w[8];
+        asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
+                     : "r"(qb + c * kF16Block + (((2 * h) ^ (r & 7)) << 4)));
+        asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(w[4]), "=r"(w[5]), "=r"(w[6]), "=r"(w[7])
+                     : "r"(qb + c * kF16Block + (((2 * h + 1) ^ (r & 7)) << 4)));
+        uint32_t hi4[4], lo4[4];
 #pragma unroll
-        for (int e2 = 0; e2 < 2; ++e2) {
-          const int e = 2 * h + e2;  // e4m3 chunk (16 codes) = bf16 chunks 2e and 2e+1
-          uint32_t w[8];
-          asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                       : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
-                       : "r"(qb + c * kF16Block + (((2 * e) ^ (r & 7)) << 4)));
-          asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                       : "=r"(w[4]), "=r"(w[5]), "=r"(w[6]), "=r"(w[7])
-                       : "r"(qb + c * kF16Block + (((2 * e + 1) ^ (r & 7)) << 4)));
-          uint32_t hi4[4], lo4[4];
-#pragma unroll
-          for (int i = 0; i < 8; i += 2) {
-            // four values: w[i] = (x0, x1), w[i+1] = (x2, x3), bf16 pairs low half first
-            const float x0 = __uint_as_float(w[i] << 16) * mult, x1 = __uint_as_float(w[i] & 0xFFFF0000u) * mult;
-            const float x2 = __uint_as_float(w[i + 1] << 16) * mult;
-            const float x3 = __uint_as_float(w[i + 1] & 0xFFFF0000u) * mult;
-            const uint32_t h01 = f32x2_to_e4m3x2(x0, x1), h23 = f32x2_to_e4m3x2(x2, x3);
-            const float2 v01 = e4m3x2_to_f32x2(h01), v23 = e4m3x2_to_f32x2(h23);
-            const uint32_t l01 = f32x2_to_e4m3x2(x0 - v01.x, x1 - v01.y);
-            const uint32_t l23 = f32x2_to_e4m3x2(x2 - v23.x, x3 - v23.y);
-            hi4[i >> 1] = h01 | (h23 << 16);
-            lo4[i >> 1] = l01 | (l23 << 16);
-          }
-          const uint32_t off = c * kQ8Block + ((e ^ sw8) << 4);
-          st_shared_v4(qhi + off, hi4[0], hi4[1], hi4[2], hi4[3]);
-          st_shared_v4(qlo + off, lo4[0], lo4[1], lo4[2], lo4[3]);
+        for (int i = 0; i < 8; i += 2) {
+          // four values: w[i] = (x0, x1), w[i+1] = (x2, x3), bf16 pairs low half first
+          const float x0 = __uint_as_float(w[i] << 16) * mult, x1 = __uint_as_float(w[i] & 0xFFFF0000u) * mult;
+          const float x2 = __uint_as_float(w[i + 1] << 16) * mult;
+          const float x3 = __uint_as_float(w[i + 1] & 0xFFFF0000u) * mult;
+          const uint32_t h01 = f32x2_to_e4m3x2(x0, x1), h23 = f32x2_to_e4m3x2(x2, x3);
+          const float2 v01 = e4m3x2_to_f32x2(h01), v23 = e4m3x2_to_f32x2(h23);
+          const uint32_t l01 = f32x2_to_e4m3x2(x0 - v01.x, x1 - v01.y);
+          const uint32_t l23 = f32x2_to_e4m3x2(x2 - v23.x, x3 - v23.y);
+          hi4[i >> 1] = h01 | (h23 << 16);
+          lo4[i >> 1] = l01 | (l23 << 16);
         }
+        st_shared_v4(qhi + c * kQ8Block + e_off, hi4[0], hi4[1], hi4[2], hi4[3]);
+        st_shared_v4(qlo + c * kQ8Block + e_off, lo4[0], lo4[1], lo4[2], lo4[3]);
       }
       fence_proxy_async_smem();
     }
@@ -493,63 +498,92 @@ decode_partial_e4m3_kernel(const __grid_constant__ CUtensorMap tm_q, const __gri
     if (!failed) mbar_arrive(&ctrl->q_ready);
 
     // BMM1 (M = 128) puts row r's hi / lo partial scores in TMEM lanes 32*(r/16) + r%16 and
-    // 16 further, so warp w owns rows 16w .. 16w+15.  Lane i (< 16) keeps keys 0-31 of its
-    // row, lane i+16 keys 32-63; each takes the other half's partial scores by a shuffle.
+    // 16 further: warps w and w+4 serve lane quadrant w%4 (rows 16(w%4) .. +15), warp w the
+    // tile's keys 0-31 and warp w+4 keys 32-63.  Lanes i and i+16 hold the hi and lo parts
+    // of one row; after a shuffle lane i keeps the sum for the first 16 of its warp's keys,
+    // lane i+16 for the last 16.  The two warps of a quadrant swap their partial row maxima
+    // through shared memory (a 64-thread named barrier per quadrant).
+    const int quad = warp & 3, kh = warp >> 2;
     const int half = lane >> 4;
-    const bool row_lane = half == 0;
-    const int r = warp * 16 + (lane & 15);
+    const int r = quad * 16 + (lane & 15);
     const bool row_active = r < nrows;
     const int t = (row0 + r) / p.H;
     const int lim_abs = L - p.T + t;  // last visible key of this row
-    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
+    const int pair_bar = 2 + quad;
+    const int kb = 32 * kh + 16 * half;  // this thread's first key of every tile
     float m_used = -INFINITY;
     float l_sum = 0.f, l_use = 0.f;
     // S holds (q 2^s) . k_code: the row's 2^-s and kv_scale (in p.scale_log2) return here;
     // P carries 2^kPShift, which cancels in O / l and returns in the LSE.
     const float scale_log2 = failed ? 0.f : p.scale_log2 * ctrl->q_unscale[r];
     const float v_scale = p.v_scale;
-    const uint32_t p_row = smem_u32(smem + kOffP) + r * 64;
-    const int p_sw = (r >> 1) & 3;
+    const uint32_t p_addr = smem_u32(smem + kOffP) + r * 64 + (((2 * kh + half) ^ ((r >> 1) & 3)) << 4);
 
     for (int j = 0; !failed && j < ntiles; ++j) {
       const int sb = j & 1;
       const int s = j % kStages;
       const int k0 = kv_start + j * kTileKeys;
-      bool need_rescale = false;
-      float alpha = 1.f;
-      uint32_t phi[8], plo[8];
       bool fail = !mbar_wait(&ctrl->s_full[sb], (j >> 1) & 1, abort_flag);
       fail = __any_sync(0xffffffffu, fail);
+      float x[16];
+      int lim = -1;
       if (!fail) {
         tc_fence_after();
-        uint32_t sa[32], sz[32];
-        tmem_ld32(tmem + lane_base + kTmemS + sb * 64, sa);
-        tmem_ld32(tmem + lane_base + kTmemS + sb * 64 + 32, sz);
+        uint32_t v[32];
+        tmem_ld32(tmem + lane_base + kTmemS + sb * 64 + 32 * kh, v);
         tmem_ld_wait();
         tc_fence_before();
         mbar_arrive(&ctrl->s_free[sb]);
-        float x[32];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const uint32_t mine = half ? sz[i] : sa[i];
-          const uint32_t other = __shfl_xor_sync(0xffffffffu, half ? sa[i] : sz[i], 16);
-          x[i] = __uint_as_float(mine) + __uint_as_float(other);
+        for (int k = 0; k < 16; ++k) {
+          const uint32_t mine = half ? v[16 + k] : v[k];
+          const uint32_t other = __shfl_xor_sync(0xffffffffu, half ? v[k] : v[16 + k], 16);
+          x[k] = __uint_as_float(mine) + __uint_as_float(other);
         }
-        const int lim = row_active ? (min(kv_end - 1, lim_abs) - k0 - 32 * half) : -1;
-        softmax_step_e4m3(x, lim, scale_log2, m_used, l_sum, l_use, phi, plo, alpha, need_rescale);
+        lim = row_active ? (min(kv_end - 1, lim_abs) - k0 - kb) : -1;
+        float mx = -INFINITY;
+        if (lim >= 15) {
+#pragma unroll
+          for (int k = 0; k < 16; ++k) mx = fmaxf(mx, x[k]);
+        } else {
+#pragma unroll
+          for (int k = 0; k < 16; ++k)
+            if (k <= lim) mx = fmaxf(mx, x[k]);
+        }
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+        if (half == 0) ctrl->red[0][kh][r] = mx;
+      }
+      named_bar_sync(pair_bar, 64);
+      uint32_t phi[4], plo[4];
+      float alpha = 1.f;
+      bool need_rescale = false;
+      if (!fail) {
+        // scale > 0: max commutes with the scaling; -inf stays -inf
+        const float mt = fmaxf(ctrl->red[0][0][r], ctrl->red[0][1][r]) * scale_log2;
+        if (m_used == -INFINITY) {
+          m_used = mt;  // first contributing tile: nothing accumulated yet
+        } else if (mt > m_used + kRescaleThreshold) {
+          alpha = ex2_approx(m_used - mt);
+          need_rescale = true;
+          l_sum *= alpha;
+          l_use *= alpha;
+          m_used = mt;
+        }
+        const float off = (m_used == -INFINITY) ? 0.f : (kPShift - m_used);
+        if (lim >= 15)
+          p_split16<true>(x, lim, scale_log2, off, l_sum, l_use, phi, plo);
+        else
+          p_split16<false>(x, lim, scale_log2, off, l_sum, l_use, phi, plo);
       }
       if (!fail && j >= 1) {
         fail = !mbar_wait(&ctrl->o_done, (j - 1) & 1, abort_flag);
         fail = __any_sync(0xffffffffu, fail);
       }
       if (!fail) {
-#pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          const uint32_t off = ((2 * half + c) ^ p_sw) << 4;
-          st_shared_v4(p_row + off, phi[4 * c], phi[4 * c + 1], phi[4 * c + 2], phi[4 * c + 3]);
-          st_shared_v4(p_row + kPPart + off, plo[4 * c], plo[4 * c + 1], plo[4 * c + 2], plo[4 * c + 3]);
-        }
-        if (row_lane) ctrl->alpha[r] = alpha;
+        st_shared_v4(p_addr, phi[0], phi[1], phi[2], phi[3]);
+        st_shared_v4(p_addr + kPPart, plo[0], plo[1], plo[2], plo[3]);
+        if (kh == 0 && half == 0) ctrl->alpha[r] = alpha;
         const bool any = __any_sync(0xffffffffu, need_rescale);
         if (lane == 0) ctrl->rescale_flag[warp] = any ? 1 : 0;
         // the request's last tile: rows past its end are zeroed in the V blocks (BMM1 of this
@@ -569,32 +603,30 @@ decode_partial_e4m3_kernel(const __grid_constant__ CUtensorMap tm_q, const __gri
         failed = true;
         break;
       }
-      if (ctrl->rescale_flag[0] | ctrl->rescale_flag[1] | ctrl->rescale_flag[2] | ctrl->rescale_flag[3]) {
+      const int4 f0 = *reinterpret_cast<const int4*>(&ctrl->rescale_flag[0]);
+      const int4 f1 = *reinterpret_cast<const int4*>(&ctrl->rescale_flag[4]);
+      if (f0.x | f0.y | f0.z | f0.w | f1.x | f1.y | f1.z | f1.w) {
         // O^T[dim, row] *= alpha[row] for all 512 value columns; this thread owns TMEM lane
-        // (warp*32 + lane) of each 128-column chunk.  Rows 32hh .. 32hh+31 at a time, so
-        // that only their 32 factors are held in registers.
+        // (32 quad + lane) of each 128-column chunk, rows 32kh .. 32kh+31.
         tc_fence_after();
-#pragma unroll 1
-        for (int hh = 0; hh < 2; ++hh) {
-          float al[32];
+        float al[32];
 #pragma unroll
-          for (int i = 0; i < 32; i += 4) {
-            const float4 f = *reinterpret_cast<const float4*>(&ctrl->alpha[hh * 32 + i]);
-            al[i] = f.x;
-            al[i + 1] = f.y;
-            al[i + 2] = f.z;
-            al[i + 3] = f.w;
-          }
+        for (int i = 0; i < 32; i += 4) {
+          const float4 f = *reinterpret_cast<const float4*>(&ctrl->alpha[kh * 32 + i]);
+          al[i] = f.x;
+          al[i + 1] = f.y;
+          al[i + 2] = f.z;
+          al[i + 3] = f.w;
+        }
 #pragma unroll 1
-          for (int qc = 0; qc < 4; ++qc) {
-            uint32_t v[32];
-            const uint32_t addr = tmem + lane_base + qc * 64 + hh * 32;
-            tmem_ld32(addr, v);
-            tmem_ld_wait();
+        for (int qc = 0; qc < 4; ++qc) {
+          uint32_t v[32];
+          const uint32_t addr = tmem + lane_base + qc * 64 + kh * 32;
+          tmem_ld32(addr, v);
+          tmem_ld_wait();
 #pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * al[i]);
-            tmem_st32(addr, v);
-          }
+          for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * al[i]);
+          tmem_st32(addr, v);
         }
         tmem_st_wait();
       }
@@ -603,17 +635,24 @@ decode_partial_e4m3_kernel(const __grid_constant__ CUtensorMap tm_q, const __gri
     }
 
     if (!failed) failed = !mbar_wait(&ctrl->o_done, (ntiles - 1) & 1, abort_flag);
+    // this thread's partial row sums -> its warp's half of the row -> shared with the other half
+    l_sum += __shfl_xor_sync(0xffffffffu, l_sum, 16);
+    l_use += __shfl_xor_sync(0xffffffffu, l_use, 16);
+    if (half == 0) {
+      ctrl->red[0][kh][r] = l_sum;
+      ctrl->red[1][kh][r] = l_use;
+    }
     if (bar_or(1, kSoftmaxThreads, failed || (*abort_flag != 0))) {
       failed = true;
     } else {
       tc_fence_after();
       const bool final_out = (nsplit_b == 1);
-      l_sum += __shfl_xor_sync(0xffffffffu, l_sum, 16);  // the two halves' partial row sums
-      l_use += __shfl_xor_sync(0xffffffffu, l_use, 16);
-      if (row_lane) {
-        const float lse2 = (l_sum > 0.f) ? (m_used + __log2f(l_sum) - kPShift) : -INFINITY;
+      if (kh == 0 && half == 0) {
+        const float ls = ctrl->red[0][0][r] + ctrl->red[0][1][r];
+        const float lu = ctrl->red[1][0][r] + ctrl->red[1][1][r];
+        const float lse2 = (ls > 0.f) ? (m_used + __log2f(ls) - kPShift) : -INFINITY;
         const float lse_nat = lse2 * 0.69314718055994530942f;
-        ctrl->row_scale[r] = (l_use > 0.f) ? (v_scale / l_use) : 0.f;
+        ctrl->row_scale[r] = (lu > 0.f) ? (v_scale / lu) : 0.f;
         if (row_active) {
           const int64_t grow = static_cast<int64_t>(b) * p.R + row0 + r;
           if (final_out)
@@ -624,33 +663,30 @@ decode_partial_e4m3_kernel(const __grid_constant__ CUtensorMap tm_q, const __gri
       }
       named_bar_sync(1, kSoftmaxThreads);
       // Normalised O (bf16) is transposed through ring stages 0-1 (free once the last BMM2
-      // has completed) so that global stores are whole 16-byte row chunks.
+      // has completed) so that global stores are whole 16-byte row chunks.  This thread:
+      // value column 32 quad + lane of each 128-column chunk, rows 32kh .. 32kh+31, whose
+      // scales stay in registers.
       const uint32_t stage_s = smem_u32(smem + kOffOStage);  // [64][512] bf16
-      // rows 32hh .. 32hh+31 at a time: their 32 scales stay in registers (shared-memory
-      // loads interleaved with the staging stores would each wait for the stores before them)
-#pragma unroll 1
-      for (int hh = 0; hh < 2; ++hh) {
-        float rs[32];
+      float rs[32];
 #pragma unroll
-        for (int i = 0; i < 32; i += 4) {
-          const float4 f = *reinterpret_cast<const float4*>(&ctrl->row_scale[hh * 32 + i]);
-          rs[i] = f.x;
-          rs[i + 1] = f.y;
-          rs[i + 2] = f.z;
-          rs[i + 3] = f.w;
-        }
+      for (int i = 0; i < 32; i += 4) {
+        const float4 f = *reinterpret_cast<const float4*>(&ctrl->row_scale[kh * 32 + i]);
+        rs[i] = f.x;
+        rs[i + 1] = f.y;
+        rs[i + 2] = f.z;
+        rs[i + 3] = f.w;
+      }
 #pragma unroll 1
-        for (int qc = 0; qc < 4; ++qc) {
-          const int dim = qc * 128 + warp * 32 + lane;
-          uint32_t v[32];
-          tmem_ld32(tmem + lane_base + qc * 64 + hh * 32, v);
-          tmem_ld_wait();
+      for (int qc = 0; qc < 4; ++qc) {
+        const int dim = qc * 128 + quad * 32 + lane;
+        uint32_t v[32];
+        tmem_ld32(tmem + lane_base + qc * 64 + kh * 32, v);
+        tmem_ld_wait();
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const __nv_bfloat16 o = __float2bfloat16_rn(__uint_as_float(v[i]) * rs[i]);
-            asm volatile("st.shared.b16 [%0], %1;" ::"r"(stage_s + ((hh * 32 + i) * kValueDim + dim) * 2),
-                         "h"(*reinterpret_cast<const uint16_t*>(&o)));
-          }
+        for (int i = 0; i < 32; ++i) {
+          const __nv_bfloat16 o = __float2bfloat16_rn(__uint_as_float(v[i]) * rs[i]);
+          asm volatile("st.shared.b16 [%0], %1;" ::"r"(stage_s + ((kh * 32 + i) * kValueDim + dim) * 2),
+                       "h"(*reinterpret_cast<const uint16_t*>(&o)));
         }
       }
       const __nv_bfloat16* stage_h = reinterpret_cast<const __nv_bfloat16*>(smem + kOffOStage);

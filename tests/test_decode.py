@@ -264,6 +264,45 @@ def test_decode_e4m3_dominant_key_over_long_tail(mla, oracle_mod):
     assert row_rel.max() <= REL_L2, f"worst row rel-L2 {row_rel.max():.3e}"
 
 
+@pytest.mark.parametrize("kv", ["bf16", "e4m3", "int8"])
+def test_decode_running_max_rises_every_tile(mla, oracle_mod, kv):
+    """Keys built so that each row's scores climb 4 to 7 (head h: 4 (1 + h/20)) in the log2
+    domain every 64 keys: the running max moves on every tile of the e4m3 kernel (threshold
+    2) and every second or third tile of the others (threshold 8), so O is rescaled again and
+    again while BMM2s are in flight.  The climb lives in the 64 rope columns, which take part
+    in the scores but not in V, so the outputs keep the usual size.  Parity with the oracle
+    on every output."""
+    wl = DecodeWorkload("rising", 2, 2, 16, [1000, 2100], kv_dtype=kv, seed=61)
+    inp = make_decode_inputs(wl, "cpu")
+    n_pages, P, _ = inp.kv_pool.shape
+    g = torch.Generator().manual_seed(62)
+    u = torch.zeros(576, dtype=torch.float64)
+    u[512:] = torch.randn(64, generator=g, dtype=torch.float64)
+    u /= u.norm()
+    x = torch.randn(n_pages, P, 576, generator=g, dtype=torch.float64) * 0.5
+    for b, L in enumerate(wl.seq_lens):
+        idx = torch.arange(L)
+        pages = inp.page_table[b, idx // P].long()
+        x[pages, idx % P] += (4.0 * idx.double() / 64.0)[:, None] * u
+    if kv == "bf16":
+        inp.kv_pool, inp.kv_scale = x.to(torch.bfloat16), 1.0
+    elif kv == "e4m3":
+        inp.kv_scale = float(x.abs().max()) / 448.0
+        inp.kv_pool = (x / inp.kv_scale).clamp(-448.0, 448.0).float().to(torch.float8_e4m3fn).view(torch.uint8)
+    else:
+        inp.kv_scale = float(x.abs().max()) / 127.0
+        inp.kv_pool = torch.round(x / inp.kv_scale).clamp(-127.0, 127.0).to(torch.int8)
+    c = math.log(2.0) / inp.scale  # a key's score in the log2 domain is then its k . u
+    q = torch.empty(2, 2, 16, 576, dtype=torch.float64)
+    for h in range(16):
+        q[:, :, h] = c * (1.0 + h / 20.0) * u
+    inp.q = q.to(torch.bfloat16)
+    out, lse, _ = run_gpu(mla, inp)
+    ref_out, ref_lse = oracle_mod.mla_decode(inp.q, inp.kv_pool, inp.page_table, inp.seq_lens, inp.scale,
+                                             kv_scale=inp.kv_scale)
+    check(out, lse, ref_out, ref_lse, fp8=(kv != "bf16"))
+
+
 def test_decode_page_shuffle_invariance_bitwise(mla):
     wl = DecodeWorkload("shuffle", 2, 4, 16, [1500, 777], seed=5, extra_pages=7)
     inp = make_decode_inputs(wl, "cpu")

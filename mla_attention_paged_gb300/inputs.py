@@ -14,6 +14,8 @@ Recipe (all draws from one torch.Generator seeded per workload):
   * decode Q and latent KV: N(0, 1) / sqrt(576), bf16; scale 1/sqrt(192).
   * FP8 KV: latent N(0, 1), kv_scale = amax|x| / 448, codes = e4m3fn(x / kv_scale).
   * INT8 KV: latent N(0, 1), kv_scale = amax|x| / 127, codes = round(x / kv_scale) as int8.
+  * INT8 KV with a scale per page: each page's N(0, 1) latents times 2^U(-3, 3), encoded with
+    that page's amax / 127; kv_scale = the largest page scale.
   * pages: 64-token pages; each request owns ceil(L_b / 64) pages taken from one shared
     pool in a random permutation.
   * "peaked" variants multiply Q by 30 and plant near-copies of a query direction into
@@ -41,7 +43,7 @@ class DecodeWorkload:
     heads: int
     seq_lens: list            # per request, drafts included
     page_size: int = 64
-    kv_dtype: str = "bf16"    # "bf16", "e4m3" or "int8"
+    kv_dtype: str = "bf16"    # "bf16", "e4m3", "int8" or "int8page"
     seed: int = 0
     peaked: bool = False
     extra_pages: int = 0      # unused pool pages (pool larger than needed)
@@ -103,6 +105,7 @@ class DecodeInputs:
     kv_scale: float
     scale: float
     wl: DecodeWorkload = field(repr=False, default=None)
+    page_scales: torch.Tensor = None  # [n_pages] float32 (int8 pools with a scale per page)
 
 
 def make_decode_inputs(wl: DecodeWorkload, device="cpu", max_pages=None) -> DecodeInputs:
@@ -156,18 +159,37 @@ def make_decode_inputs(wl: DecodeWorkload, device="cpu", max_pages=None) -> Deco
             e = min(n_pages, s + step)
             pool[s:e] = torch.round(raw[s:e] / kv_scale).clamp_(-127.0, 127.0).to(torch.int8)
         del raw
+    elif wl.kv_dtype == "int8page":
+        # a scale per page: each page's N(0,1) latents times a spread factor 2^U(-3,3), so
+        # that pages differ in range, encoded as round(x / s_page) with s_page = its amax / 127
+        raw = torch.empty(n_pages, P, D_LATENT, dtype=torch.float32, device=dev)
+        step = max(1, (1 << 27) // (P * D_LATENT))
+        spread = torch.pow(2.0, torch.rand(n_pages, generator=g, device=dev) * 6.0 - 3.0)
+        for s in range(0, n_pages, step):
+            e = min(n_pages, s + step)
+            raw[s:e] = torch.randn(e - s, P, D_LATENT, generator=g, device=dev) * spread[s:e, None, None]
+        page_scales = (raw.abs().amax(dim=(1, 2)) / 127.0).clamp_(min=1e-30)
+        pool = torch.empty(n_pages, P, D_LATENT, dtype=torch.int8, device=dev)
+        for s in range(0, n_pages, step):
+            e = min(n_pages, s + step)
+            pool[s:e] = torch.round(raw[s:e] / page_scales[s:e, None, None]).clamp_(-127.0, 127.0).to(torch.int8)
+        kv_scale = float(page_scales.max())
+        del raw
     else:
         raise ValueError(wl.kv_dtype)
     if wl.peaked:
-        _plant_near_duplicates(q, pool, page_table, wl, g, kv_scale)
+        _plant_near_duplicates(q, pool, page_table, wl, g, kv_scale,
+                               page_scales if wl.kv_dtype == "int8page" else None)
     seq_lens = torch.tensor(wl.seq_lens, dtype=torch.int32, device=dev)
     return DecodeInputs(q.to(torch.bfloat16), pool, page_table, seq_lens, kv_scale,
-                        1.0 / math.sqrt(D_QK_PREFILL), wl)
+                        1.0 / math.sqrt(D_QK_PREFILL), wl,
+                        page_scales if wl.kv_dtype == "int8page" else None)
 
 
-def _plant_near_duplicates(q, pool, page_table, wl, g, kv_scale):
+def _plant_near_duplicates(q, pool, page_table, wl, g, kv_scale, page_scales=None):
     """Overwrite a few random key rows of each request with a scaled copy of one of its
-    query directions plus noise, so that a handful of keys dominate the softmax."""
+    query directions plus noise, so that a handful of keys dominate the softmax.  (int8
+    rows are encoded with their page's scale when the pool has one per page.)"""
     dev = q.device
     B, T, H, P = wl.batch, wl.q_len, wl.heads, wl.page_size
     for b in range(B):
@@ -185,7 +207,8 @@ def _plant_near_duplicates(q, pool, page_table, wl, g, kv_scale):
             if pool.dtype == torch.uint8:
                 pool[page, j % P] = (row / kv_scale).clamp(-448.0, 448.0).to(torch.float8_e4m3fn).view(torch.uint8)
             elif pool.dtype == torch.int8:
-                pool[page, j % P] = torch.round(row / kv_scale).clamp(-127.0, 127.0).to(torch.int8)
+                sc = float(page_scales[page]) if page_scales is not None else kv_scale
+                pool[page, j % P] = torch.round(row / sc).clamp(-127.0, 127.0).to(torch.int8)
             else:
                 pool[page, j % P] = row.to(torch.bfloat16)
 

@@ -46,7 +46,7 @@ def _load():
             P = ctypes.c_void_p
             i32, i64, dbl = ctypes.c_int, ctypes.c_int64, ctypes.c_double
             lib.oracle_mla_decode.restype = ctypes.c_int
-            lib.oracle_mla_decode.argtypes = [i32, i32, i32, i32, i32, i32, P, P, i32, dbl, i64,
+            lib.oracle_mla_decode.argtypes = [i32, i32, i32, i32, i32, i32, P, P, i32, dbl, P, i64,
                                               P, i32, P, dbl, i32, P, i64, P, P]
             lib.oracle_mla_prefill.restype = ctypes.c_int
             lib.oracle_mla_prefill.argtypes = [i32, i32, i32, i32, P, P, P, P, P, P, dbl, P, i64, P, P]
@@ -88,12 +88,14 @@ def e4m3_to_double(codes) -> np.ndarray:
 
 
 def mla_decode(q: torch.Tensor, kv_pool: torch.Tensor, page_table, seq_lens, scale: float,
-               kv_scale: float = 1.0, dv: int = 512, rows=None, lens_include_drafts: bool = True):
+               kv_scale: float = 1.0, dv: int = 512, rows=None, lens_include_drafts: bool = True,
+               page_scales=None):
     """Absorbed MLA decode over a paged latent cache, in fp64.
 
     q: [B, T, H, D] bf16.  kv_pool: [n_pages, page_size, D] bf16, uint8 e4m3 codes or
-    int8 codes (then each element is decoded and multiplied by kv_scale).  page_table: [B, max_pages]
-    int32.  seq_lens: [B] (tokens cached per request, drafts included).
+    int8 codes (then each element is decoded and multiplied by kv_scale, or, for int8 codes
+    with ``page_scales`` [n_pages], by the scale of the page that holds it).  page_table:
+    [B, max_pages] int32.  seq_lens: [B] (tokens cached per request, drafts included).
     Returns (out [B,T,H,dv] float64, lse [B,T,H] float64) or, with ``rows`` (flat ids
     (b*T + t)*H + h), (out [n, dv], lse [n]).
     """
@@ -112,6 +114,13 @@ def mla_decode(q: torch.Tensor, kv_pool: torch.Tensor, page_table, seq_lens, sca
         kv_dtype = 2
     else:
         raise TypeError("kv_pool must be bf16, uint8 e4m3 codes or int8 codes")
+    ps = None
+    if page_scales is not None:
+        if kv_dtype != 2:
+            raise TypeError("page_scales apply to int8 pools only")
+        ps = np.ascontiguousarray(torch.as_tensor(page_scales).detach().cpu().double().numpy().reshape(-1))
+        if ps.size != n_pages:
+            raise ValueError("page_scales must hold one scale per page")
     qb = _bits16(q)
     pt = _i32(page_table)
     sl = _i32(seq_lens)
@@ -126,7 +135,8 @@ def mla_decode(q: torch.Tensor, kv_pool: torch.Tensor, page_table, seq_lens, sca
         out = np.zeros((n_rows, dv), dtype=np.float64)
         lse = np.zeros((n_rows,), dtype=np.float64)
     rc = lib.oracle_mla_decode(B, T, H, D, dv, page_size, _ptr(qb), _ptr(pool), kv_dtype,
-                               float(kv_scale), n_pages, _ptr(pt), max_pages, _ptr(sl), float(scale),
+                               float(kv_scale), _ptr(ps) if ps is not None else None, n_pages, _ptr(pt),
+                               max_pages, _ptr(sl), float(scale),
                                1 if lens_include_drafts else 0,
                                _ptr(rows_arr) if rows_arr is not None else None, n_rows,
                                _ptr(out), _ptr(lse))

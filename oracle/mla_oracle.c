@@ -28,7 +28,8 @@
  *    per-tensor scale; the decode table below is built from that format definition.
  *  - INT8 KV (the talk's section "Kernel：让 MLA 真正跑满 GPU" names INT8 among the KV
  *    quantisations that stay bandwidth-bound) is read as two's-complement int8 codes
- *    times one per-tensor scale, the plainest form the talk leaves open.
+ *    times one per-tensor scale, the plainest form the talk leaves open; or, with a
+ *    scale per page, each code times the scale of the page that holds its row.
  *  - Prefill: request b has prefix_lens[b] cached tokens followed by its new tokens;
  *    new token i (0-based) sees keys 0 .. prefix_lens[b] + i.
  *
@@ -74,7 +75,8 @@ double oracle_e4m3_to_double(uint8_t code) {
 }
 
 /* kv_dtype: 0 = bf16 (uint16 bit patterns), 1 = e4m3 bytes times kv_scale,
- * 2 = int8 (two's complement) codes times kv_scale. */
+ * 2 = int8 (two's complement) codes times kv_scale (the caller passes the scale of the
+ * element's page when the pool has one per page). */
 static double kv_elem(const void* pool, int kv_dtype, int64_t idx, double kv_scale) {
   if (kv_dtype == 0) return bf16_bits_to_double(((const uint16_t*)pool)[idx]);
   if (kv_dtype == 2) return (double)((const int8_t*)pool)[idx] * kv_scale;
@@ -89,7 +91,9 @@ static double kv_elem(const void* pool, int kv_dtype, int64_t idx, double kv_sca
 /* Decode: absorbed MLA over the paged latent cache.
  *
  *   q          [B, T, H, D] bf16 bits                 (D = 576 latent + rope columns)
- *   kv_pool    [n_pages, page_size, D] bf16 bits or e4m3 bytes
+ *   kv_pool    [n_pages, page_size, D] bf16 bits, e4m3 bytes or int8 codes
+ *   page_scales optional [n_pages] double (int8 pools only): the scale of each page's
+ *              codes, used instead of kv_scale; NULL = one kv_scale for the pool
  *   page_table [B, max_pages] int32: latent row j of request b lives at
  *              kv_pool[page_table[b, j / page_size], j % page_size, :]
  *   seq_lens   [B] int32 cached tokens per request
@@ -100,12 +104,13 @@ static double kv_elem(const void* pool, int kv_dtype, int64_t idx, double kv_sca
  * Returns 0, or -1 on an argument error (a row with no visible key, a page id out of
  * range, a length beyond the table).                                                   */
 int oracle_mla_decode(int B, int T, int H, int D, int Dv, int page_size, const uint16_t* q,
-                      const void* kv_pool, int kv_dtype, double kv_scale, int64_t n_pages,
-                      const int32_t* page_table, int max_pages, const int32_t* seq_lens,
+                      const void* kv_pool, int kv_dtype, double kv_scale, const double* page_scales,
+                      int64_t n_pages, const int32_t* page_table, int max_pages, const int32_t* seq_lens,
                       double scale, int lens_include_drafts, const int64_t* rows,
                       int64_t n_rows, double* out, double* lse) {
   int64_t total = rows ? n_rows : (int64_t)B * T * H;
   int err = 0;
+  if (page_scales && kv_dtype != 2) return -1;
   /* argument checks first, serially */
   for (int b = 0; b < B; ++b) {
     int64_t L = seq_lens[b] + (lens_include_drafts ? 0 : T);
@@ -131,10 +136,11 @@ int oracle_mla_decode(int B, int T, int H, int D, int Dv, int page_size, const u
     if (!s) { err |= 1; continue; }
     /* scores */
     for (int64_t j = 0; j < nvis; ++j) {
-      int64_t base = ((int64_t)page_table[(int64_t)b * max_pages + j / page_size] * page_size +
-                      j % page_size) * D;
+      int32_t pid = page_table[(int64_t)b * max_pages + j / page_size];
+      int64_t base = ((int64_t)pid * page_size + j % page_size) * D;
+      double sc = page_scales ? page_scales[pid] : kv_scale;
       double acc = 0.0;
-      for (int c = 0; c < D; ++c) acc += bf16_bits_to_double(qrow[c]) * kv_elem(kv_pool, kv_dtype, base + c, kv_scale);
+      for (int c = 0; c < D; ++c) acc += bf16_bits_to_double(qrow[c]) * kv_elem(kv_pool, kv_dtype, base + c, sc);
       s[j] = scale * acc;
     }
     /* softmax normaliser */
@@ -145,10 +151,11 @@ int oracle_mla_decode(int B, int T, int H, int D, int Dv, int page_size, const u
     /* weighted sum of values */
     for (int c = 0; c < Dv; ++c) o[c] = 0.0;
     for (int64_t j = 0; j < nvis; ++j) {
-      int64_t base = ((int64_t)page_table[(int64_t)b * max_pages + j / page_size] * page_size +
-                      j % page_size) * D;
+      int32_t pid = page_table[(int64_t)b * max_pages + j / page_size];
+      int64_t base = ((int64_t)pid * page_size + j % page_size) * D;
+      double sc = page_scales ? page_scales[pid] : kv_scale;
       double w = s[j];
-      for (int c = 0; c < Dv; ++c) o[c] += w * kv_elem(kv_pool, kv_dtype, base + c, kv_scale);
+      for (int c = 0; c < Dv; ++c) o[c] += w * kv_elem(kv_pool, kv_dtype, base + c, sc);
     }
     for (int c = 0; c < Dv; ++c) o[c] /= Z;
     lse[i] = m + log(Z);

@@ -11,7 +11,10 @@ The pages print no worked example, so the oracle is pinned to things outside its
     against points the format definition fixes;
   * int8 codes: with a power-of-two scale the decoded values are exact in bf16, so the
     int8 pool must give bit-for-bit the bf16 pool's result; the extreme codes decode to
-    -128 and 127 times the scale.
+    -128 and 127 times the scale;
+  * int8 codes with a scale per page: library SDPA on the rows dequantised page by page;
+    equal page scales give bit-for-bit the per-tensor result; one visible key in a page
+    whose id differs from its table slot returns its codes times that page's scale.
 Each is chosen so that a plausible slip (dropped term, wrong causal index, wrong value
 columns, transposed operand, wrong log base) fails at least one of them.
 """
@@ -42,7 +45,10 @@ def _dense_kv(inp, b, L):
     if rows.dtype == torch.uint8:
         rows = rows.view(torch.float8_e4m3fn).to(torch.float64) * inp.kv_scale
     elif rows.dtype == torch.int8:
-        rows = rows.to(torch.float64) * inp.kv_scale
+        if inp.page_scales is not None:
+            rows = rows.to(torch.float64) * inp.page_scales.double()[pages][:, None]
+        else:
+            rows = rows.to(torch.float64) * inp.kv_scale
     else:
         rows = rows.to(torch.float64)
     return rows
@@ -76,6 +82,8 @@ CASES = [
     (1, 4, 4, [70], 64, "e4m3"),
     (2, 3, 2, [33, 9], 4, "int8"),
     (1, 4, 4, [70], 64, "int8"),
+    (2, 3, 2, [33, 9], 4, "int8page"),
+    (2, 2, 3, [70, 130], 64, "int8page"),
     (2, 2, 2, [300, 129], 128, "bf16"),   # pages larger than one tile, a request ending inside one
     (1, 1, 2, [600], 256, "e4m3"),
 ]
@@ -86,7 +94,7 @@ CASES = [
 def test_decode_matches_library_sdpa(oracle_mod, B, T, H, lens, P, kv, peaked):
     inp = _paged(B, T, H, lens, P, seed=7 + B + T + P, kv=kv, peaked=peaked)
     out, lse = oracle_mod.mla_decode(inp.q, inp.kv_pool, inp.page_table, inp.seq_lens, inp.scale,
-                                     kv_scale=inp.kv_scale)
+                                     kv_scale=inp.kv_scale, page_scales=inp.page_scales)
     ref_out, ref_lse = _sdpa_decode(inp)
     np.testing.assert_allclose(out, ref_out, rtol=1e-10, atol=1e-13)
     np.testing.assert_allclose(lse, ref_lse, rtol=1e-12, atol=1e-12)
@@ -244,6 +252,37 @@ def test_int8_extreme_codes(oracle_mod):
                                      0.1, kv_scale=0.5)
     assert out[0, 0, 0, :4].tolist() == [-64.0, 63.5, -0.5, 0.5]
     assert lse[0, 0, 0] == 0.0
+
+
+def test_int8_equal_page_scales_equal_per_tensor_bitwise(oracle_mod):
+    inp = _paged(2, 3, 4, [70, 13], 16, seed=23, kv="int8")
+    n_pages = inp.kv_pool.shape[0]
+    o1, l1 = oracle_mod.mla_decode(inp.q, inp.kv_pool, inp.page_table, inp.seq_lens, inp.scale, kv_scale=0.037)
+    o2, l2 = oracle_mod.mla_decode(inp.q, inp.kv_pool, inp.page_table, inp.seq_lens, inp.scale,
+                                   page_scales=torch.full((n_pages,), 0.037, dtype=torch.float64))
+    np.testing.assert_array_equal(o1, o2)
+    np.testing.assert_array_equal(l1, l2)
+
+
+def test_int8_page_scale_is_that_of_the_rows_page(oracle_mod):
+    # one visible key, in physical page 1 named by table slot 0: the output is its codes
+    # times page 1's scale (not slot 0's, not page 0's)
+    q = torch.zeros(1, 1, 1, D, dtype=torch.bfloat16)
+    pool = torch.zeros(2, 1, D, dtype=torch.int8)
+    pool[1, 0, :4] = torch.tensor([-128, 127, -1, 1], dtype=torch.int8)
+    pool[0, 0, :4] = torch.tensor([5, 5, 5, 5], dtype=torch.int8)
+    table = torch.tensor([[1, 0]], dtype=torch.int32)
+    out, lse = oracle_mod.mla_decode(q, pool, table, torch.ones(1, dtype=torch.int32), 0.1,
+                                     page_scales=torch.tensor([0.5, 0.25], dtype=torch.float64))
+    assert out[0, 0, 0, :4].tolist() == [-32.0, 31.75, -0.25, 0.25]
+    assert lse[0, 0, 0] == 0.0
+
+
+def test_page_scales_rejected_for_non_int8_pools(oracle_mod):
+    inp = _paged(1, 1, 2, [5], 4, seed=3)
+    with pytest.raises(TypeError):
+        oracle_mod.mla_decode(inp.q, inp.kv_pool, inp.page_table, inp.seq_lens, inp.scale,
+                              page_scales=torch.ones(inp.kv_pool.shape[0]))
 
 
 # ------------------------------------------------------------------------------------

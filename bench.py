@@ -60,9 +60,11 @@ def _peaks():
 def decode_bytes(wl):
     """Algorithmic bytes of one decode call: each request's latent rows once, its page-table
     entries, and the query / output / lse rows."""
-    e = 1 if wl.kv_dtype in ("e4m3", "int8") else 2
+    e = 1 if wl.kv_dtype in ("e4m3", "int8", "int8page") else 2
     kv = sum(L * 576 * e for L in wl.seq_lens)
-    pt = sum(((L + wl.page_size - 1) // wl.page_size) * 4 for L in wl.seq_lens)
+    # page-table entries (and, for a pool with a scale per page, the pages' fp32 scales)
+    per_page = 8 if wl.kv_dtype == "int8page" else 4
+    pt = sum(((L + wl.page_size - 1) // wl.page_size) * per_page for L in wl.seq_lens)
     io = wl.batch * wl.q_len * wl.heads * (576 * 2 + 512 * 2 + 4)
     return kv, kv + pt + io
 
@@ -108,7 +110,8 @@ TENSOR_BOUND = ("decode_b16_q2_h128_ragged", "decode_b4_q512_h16_l32k")
 # The extra lines, in print order: the last ones are the configurations the targets are
 # quoted on (batch 16 / 64K prefix, and the varlen prefill), so they end the JSON line.
 EXTRA_DECODE = ["decode_b4_q4_h16_l32k", "decode_b1_q1_h16_l1024", "decode_b16_q2_h128_ragged",
-                "decode_b4_q512_h16_l32k", "decode_int8_b16_q4_h16_l64k", "decode_fp8_b8_q4_h16_l64k",
+                "decode_b4_q512_h16_l32k", "decode_int8_b16_q4_h16_l64k", "decode_int8page_b16_q4_h16_l64k",
+                "decode_fp8_b8_q4_h16_l64k",
                 "decode_bf16_b16_q4_h16_l64k", "decode_fp8_b16_q4_h16_l64k"]
 
 
@@ -134,7 +137,8 @@ def measure_decode_extra(mla, name, dev, steps=200):
     wl, sets = decode_sets(name, dev)
     n_sets = len(sets)
     kv_bytes, alg_bytes = decode_bytes(wl)
-    kvd = {"e4m3": mla.MLA_KV_E4M3, "int8": mla.MLA_KV_INT8}.get(wl.kv_dtype, mla.MLA_KV_BF16)
+    kvd = {"e4m3": mla.MLA_KV_E4M3, "int8": mla.MLA_KV_INT8,
+           "int8page": mla.MLA_KV_INT8_PAGE}.get(wl.kv_dtype, mla.MLA_KV_BF16)
     plan = mla.decode_plan(wl.seq_lens, wl.q_len, wl.heads, wl.page_size, sets[0].page_table.shape[1],
                            sets[0].kv_pool.shape[0], kvd)
     ws_buf = mla.workspace_for(plan, dev)
@@ -144,11 +148,19 @@ def measure_decode_extra(mla, name, dev, steps=200):
 
     def call(i):
         s = sets[i % n_sets]
-        mla.decode(plan, s.q, s.kv_pool, s.page_table, s.seq_lens, s.scale, s.kv_scale, out=out, lse=lse,
-                   workspace=ws_buf, stream=st)
+        if s.page_scales is not None:
+            mla.decode_int8_paged(plan, s.q, s.kv_pool, s.page_scales, s.page_table, s.seq_lens, s.scale,
+                                  s.kv_scale, out=out, lse=lse, workspace=ws_buf, stream=st)
+        else:
+            mla.decode(plan, s.q, s.kv_pool, s.page_table, s.seq_lens, s.scale, s.kv_scale, out=out, lse=lse,
+                       workspace=ws_buf, stream=st)
 
     def partial(i):
+        # (a pool with a scale per page has no partial-only entry point: its line times whole calls)
         s = sets[i % n_sets]
+        if s.page_scales is not None:
+            call(i)
+            return
         mla.decode_partial(plan, s.q, s.kv_pool, s.page_table, s.seq_lens, s.scale, s.kv_scale, out=out, lse=lse,
                            workspace=ws_buf, stream=st)
 
@@ -413,11 +425,16 @@ def run_profile_case(name):
     else:
         wl = decode_workloads()[name]
         inp = make_decode_inputs(wl, "cuda")
-        kvd = {"e4m3": mla.MLA_KV_E4M3, "int8": mla.MLA_KV_INT8}.get(wl.kv_dtype, mla.MLA_KV_BF16)
+        kvd = {"e4m3": mla.MLA_KV_E4M3, "int8": mla.MLA_KV_INT8,
+               "int8page": mla.MLA_KV_INT8_PAGE}.get(wl.kv_dtype, mla.MLA_KV_BF16)
         plan = mla.decode_plan(wl.seq_lens, wl.q_len, wl.heads, wl.page_size, inp.page_table.shape[1],
                                inp.kv_pool.shape[0], kvd)
         for _ in range(3):
-            mla.decode(plan, inp.q, inp.kv_pool, inp.page_table, inp.seq_lens, inp.scale, inp.kv_scale)
+            if inp.page_scales is not None:
+                mla.decode_int8_paged(plan, inp.q, inp.kv_pool, inp.page_scales, inp.page_table, inp.seq_lens,
+                                      inp.scale, inp.kv_scale)
+            else:
+                mla.decode(plan, inp.q, inp.kv_pool, inp.page_table, inp.seq_lens, inp.scale, inp.kv_scale)
     torch.cuda.synchronize()
     status = mla.get_status()
     if status != mla.MLA_OK:

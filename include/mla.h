@@ -61,10 +61,13 @@ typedef enum mla_status_t {
 typedef enum mla_kv_dtype_t {
   MLA_KV_BF16 = 0, /* latent pool stored as bfloat16                                     */
   MLA_KV_E4M3 = 1, /* latent pool stored as OCP FP8 e4m3fn codes times one kv_scale      */
-  MLA_KV_INT8 = 2  /* latent pool stored as two's-complement int8 codes times one kv_scale.
+  MLA_KV_INT8 = 2, /* latent pool stored as two's-complement int8 codes times one kv_scale.
                     * (The TokenSpeed talk, section "Kernel：让 MLA 真正跑满 GPU", names INT8
                     * among the KV quantisations that keep decode bandwidth-bound; a
                     * per-tensor scale is the plainest form it leaves open.)               */
+  MLA_KV_INT8_PAGE = 3 /* int8 codes, each page with its own scale: a latent element is its
+                        * code times the scale of the page that holds its row (the other
+                        * INT8 form the talk leaves open); decoded by mla_decode_int8_paged  */
 } mla_kv_dtype_t;
 
 /* Decode plan: a plain value struct filled by mla_decode_plan(); callers treat the
@@ -141,6 +144,25 @@ int mla_decode(const mla_decode_plan_t* plan, const void* q, const void* kv_page
                const int32_t* page_table, const int32_t* seq_lens, int q_len, int num_heads,
                float scale, float kv_scale, void* out, float* lse, void* workspace,
                size_t workspace_bytes, void* stream);
+
+/* mla_decode over an int8 pool with one scale per page (plan->kv_dtype ==
+ * MLA_KV_INT8_PAGE; mla_decode and mla_decode_partial reject such plans).  Arguments,
+ * layouts and errors as mla_decode, with:
+ *   kv_pages    : [num_pages, page_size, 576] int8 codes.
+ *   page_scales : [num_pages] fp32 on the device, 4-byte aligned: the scale of each page's
+ *                 codes (element = code * page_scales[page]).
+ *   kv_scale    : a reference scale > 0 (the largest page scale is the natural choice).
+ *                 Each page scale must lie in [0, 255 * kv_scale]; a page scale outside it
+ *                 (or not finite) on a page a request reads is reported as
+ *                 MLA_ERR_DEVICE_ARG and that request's split is skipped.
+ * The codes are multiplied exactly as int8 values; each key's page scale relative to
+ * kv_scale multiplies its score (in fp32) and the softmax weight its value row receives,
+ * and kv_scale itself is folded into the softmax scale and the output.  The combine
+ * stage is the one of mla_decode: mla_decode_combine accepts these plans. */
+int mla_decode_int8_paged(const mla_decode_plan_t* plan, const void* q, const void* kv_pages,
+                          const float* page_scales, const int32_t* page_table, const int32_t* seq_lens,
+                          int q_len, int num_heads, float scale, float kv_scale, void* out, float* lse,
+                          void* workspace, size_t workspace_bytes, void* stream);
 
 /* The two stages of mla_decode, for callers that schedule them apart (e.g. to put other
  * work between them, or to time the split-KV partial kernel on its own).  The TokenSpeed

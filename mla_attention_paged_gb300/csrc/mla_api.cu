@@ -216,7 +216,8 @@ int mla_decode_plan(int batch, const int32_t* seq_lens_host, int q_len, int num_
   if (!seq_lens_host || !plan_out || batch < 1 || q_len < 1 || num_heads < 1 || max_pages_per_seq < 1 ||
       num_pages < 1)
     return MLA_ERR_INVALID_ARG;
-  if (kv_dtype != MLA_KV_BF16 && kv_dtype != MLA_KV_E4M3 && kv_dtype != MLA_KV_INT8) return MLA_ERR_INVALID_ARG;
+  if (kv_dtype != MLA_KV_BF16 && kv_dtype != MLA_KV_E4M3 && kv_dtype != MLA_KV_INT8 && kv_dtype != MLA_KV_INT8_PAGE)
+    return MLA_ERR_INVALID_ARG;
   // q_len beyond a few drafts is the prefill of q_len new tokens over a paged prefix in
   // absorbed form (the same computation: new token t sees keys 0 .. L - q_len + t)
   if (q_len > 8192 || !page_size_ok(page_size) || static_cast<int64_t>(q_len) * num_heads > 131072)
@@ -290,12 +291,16 @@ constexpr int kStageCombine = 2;
 
 // The two stages of a decode call.  The partial stage needs q, the pages and the page table;
 // the combine stage reads only the lengths, the workspace and writes out/lse.
-int decode_stages(const mla_decode_plan_t* plan, const void* q, const void* kv_pages, const int32_t* page_table,
+int decode_stages(const mla_decode_plan_t* plan, const void* q, const void* kv_pages, const float* page_scales,
+                  const int32_t* page_table,
                   const int32_t* seq_lens, int q_len, int num_heads, float scale, float kv_scale, void* out,
                   float* lse, void* workspace, size_t workspace_bytes, void* stream, int stages) {
   const bool partial = (stages & kStagePartial) != 0;
   if (!plan || !seq_lens || !out || !lse) return MLA_ERR_INVALID_ARG;
   if (partial && (!q || !kv_pages || !page_table)) return MLA_ERR_INVALID_ARG;
+  // a pool with a scale per page needs the scales; no other pool takes them
+  if (partial && (plan->kv_dtype == MLA_KV_INT8_PAGE) != (page_scales != nullptr)) return MLA_ERR_INVALID_ARG;
+  if (page_scales && !aligned(page_scales, 4)) return MLA_ERR_INVALID_ARG;
   if (q_len != plan->q_len || num_heads != plan->num_heads || plan->rows != q_len * num_heads)
     return MLA_ERR_INVALID_ARG;
   if (!aligned(out, 16) || !aligned(lse, 4)) return MLA_ERR_INVALID_ARG;
@@ -373,6 +378,8 @@ int decode_stages(const mla_decode_plan_t* plan, const void* q, const void* kv_p
   p.page_table = page_table;
   p.seq_lens = seq_lens;
   p.kv_pool = static_cast<const uint8_t*>(kv_pages);
+  p.page_scales = page_scales;
+  p.inv_ref_scale = 1.f / kv_scale;
   p.out = static_cast<__nv_bfloat16*>(out);
   p.lse = lse;
   if (plan->max_splits > 1) {
@@ -400,22 +407,31 @@ extern "C" {
 int mla_decode(const mla_decode_plan_t* plan, const void* q, const void* kv_pages, const int32_t* page_table,
                const int32_t* seq_lens, int q_len, int num_heads, float scale, float kv_scale, void* out,
                float* lse, void* workspace, size_t workspace_bytes, void* stream) {
-  return decode_stages(plan, q, kv_pages, page_table, seq_lens, q_len, num_heads, scale, kv_scale, out, lse,
-                       workspace, workspace_bytes, stream, kStagePartial | kStageCombine);
+  return decode_stages(plan, q, kv_pages, nullptr, page_table, seq_lens, q_len, num_heads, scale, kv_scale, out,
+                       lse, workspace, workspace_bytes, stream, kStagePartial | kStageCombine);
+}
+
+int mla_decode_int8_paged(const mla_decode_plan_t* plan, const void* q, const void* kv_pages, const float* page_scales,
+                          const int32_t* page_table, const int32_t* seq_lens, int q_len, int num_heads, float scale,
+                          float kv_scale, void* out, float* lse, void* workspace, size_t workspace_bytes,
+                          void* stream) {
+  if (!plan || plan->kv_dtype != MLA_KV_INT8_PAGE || !page_scales) return MLA_ERR_INVALID_ARG;
+  return decode_stages(plan, q, kv_pages, page_scales, page_table, seq_lens, q_len, num_heads, scale, kv_scale, out,
+                       lse, workspace, workspace_bytes, stream, kStagePartial | kStageCombine);
 }
 
 int mla_decode_partial(const mla_decode_plan_t* plan, const void* q, const void* kv_pages,
                        const int32_t* page_table, const int32_t* seq_lens, int q_len, int num_heads, float scale,
                        float kv_scale, void* out, float* lse, void* workspace, size_t workspace_bytes,
                        void* stream) {
-  return decode_stages(plan, q, kv_pages, page_table, seq_lens, q_len, num_heads, scale, kv_scale, out, lse,
-                       workspace, workspace_bytes, stream, kStagePartial);
+  return decode_stages(plan, q, kv_pages, nullptr, page_table, seq_lens, q_len, num_heads, scale, kv_scale, out,
+                       lse, workspace, workspace_bytes, stream, kStagePartial);
 }
 
 int mla_decode_combine(const mla_decode_plan_t* plan, const int32_t* seq_lens, int q_len, int num_heads,
                        void* out, float* lse, void* workspace, size_t workspace_bytes, void* stream) {
-  return decode_stages(plan, nullptr, nullptr, nullptr, seq_lens, q_len, num_heads, 1.f, 1.f, out, lse, workspace,
-                       workspace_bytes, stream, kStageCombine);
+  return decode_stages(plan, nullptr, nullptr, nullptr, nullptr, seq_lens, q_len, num_heads, 1.f, 1.f, out, lse,
+                       workspace, workspace_bytes, stream, kStageCombine);
 }
 
 int mla_prefill_varlen(const void* q, const void* k, const void* v, const int32_t* cu_seqlens_q,

@@ -67,9 +67,13 @@ struct DecodeCtrl {
   int rescale_flag[4];
   alignas(16) float alpha[kGroupRows];
   alignas(16) float row_scale[kGroupRows];
+  // int8 pools with a scale per page: each key's scale relative to kv_scale, per stage
+  alignas(16) float key_scale[kStages][kTileKeys];
 };
-constexpr int kSmemBytes = kOffCtrl + 1024 + 1024;  // + control block + alignment slack
-static_assert(sizeof(DecodeCtrl) <= 1024, "control block");
+constexpr int kCtrlBytes = 2048;
+constexpr int kSmemBytes = kOffCtrl + kCtrlBytes + 1024;  // + control block + alignment slack
+static_assert(sizeof(DecodeCtrl) <= kCtrlBytes, "control block");
+static_assert(kSmemBytes <= 232448, "shared memory per block");
 
 // Values of the CTA's abort flag: a bounded wait ran out, or a device argument check failed.
 constexpr int kAbortTimeout = 1;
@@ -79,13 +83,14 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemS = 256;   // S buffers at columns 256 and 320; O^T chunks at 0,64,128,192
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
-// kKv: pool format (kKvBf16 or kKvInt8; kInt8 below selects the decode warps and f16
-// GEMMs of the int8 path).
+// kKv: pool format (kKvBf16, kKvInt8 or kKvInt8Page; kInt8 below selects the decode warps
+// and f16 GEMMs of the int8 paths, kPageScales the per-key scales of kKvInt8Page).
 template <int kKv>
 __global__ void __launch_bounds__(threads_for(kKv != kKvBf16), 1)
 decode_partial_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kv,
                       const DecodeParams p) {
-  constexpr bool kInt8 = kKv == kKvInt8;
+  constexpr bool kInt8 = kKv == kKvInt8 || kKv == kKvInt8Page;
+  constexpr bool kPageScales = kKv == kKvInt8Page;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   DecodeCtrl* ctrl = reinterpret_cast<DecodeCtrl*>(smem + kOffCtrl);
@@ -380,8 +385,16 @@ decode_partial_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
     bool bad_id = false;
     {
       const unsigned n_pages = static_cast<unsigned>(min(p.num_pages, static_cast<int64_t>(0x7fffffff)));
-      for (int pg = kv_start / P + td; pg <= (kv_end - 1) / P; pg += kDequantThreads)
-        bad_id |= static_cast<unsigned>(__ldg(pt + pg)) >= n_pages;
+      for (int pg = kv_start / P + td; pg <= (kv_end - 1) / P; pg += kDequantThreads) {
+        const unsigned pid = static_cast<unsigned>(__ldg(pt + pg));
+        bad_id |= pid >= n_pages;
+        if (kPageScales && pid < n_pages) {
+          // a page's scale relative to kv_scale must be finite and in [0, 255], so that
+          // P times it stays within f16's range
+          const float rel = __ldg(p.page_scales + pid) * p.inv_ref_scale;
+          bad_id |= !(rel >= 0.f && rel <= 255.f);
+        }
+      }
     }
     bool ok = mbar_wait(&ctrl->q_full, 0, abort_flag);
     if (ok) {
@@ -414,6 +427,19 @@ decode_partial_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
     };
     int pid_cur[8];
     row_pids(0, pid_cur);
+    // per-page scales: eight lanes of the first decode warp hold the scale (relative to
+    // kv_scale) of each of a tile's 64 rows, loaded one tile ahead; rows past the request
+    // end get 0
+    const bool scale_lane = kPageScales && dw == 0 && (dl & 3) == 0;
+    auto row_rels = [&](int j, const int (&pid)[8], float (&rel)[8]) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int k = kv_start + j * kTileKeys + (dl >> 2) + 8 * i;
+        rel[i] = (scale_lane && k < L) ? __ldg(p.page_scales + pid[i]) * p.inv_ref_scale : 0.f;
+      }
+    };
+    float rel_cur[8];
+    if (kPageScales) row_rels(0, pid_cur, rel_cur);
     for (int j = 0; ok && j < ntiles; ++j) {
       const int s = j % kStages;
       const int k0 = kv_start + j * kTileKeys;
@@ -428,10 +454,18 @@ decode_partial_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
           w[m][i] = valid ? __ldg(reinterpret_cast<const uint4*>(row + (dw + 3 * m) * 64)) : make_uint4(0u, 0u, 0u, 0u);
       }
       int pid_nxt[8];
-      if (j + 1 < ntiles) row_pids(j + 1, pid_nxt);
+      float rel_nxt[8];
+      if (j + 1 < ntiles) {
+        row_pids(j + 1, pid_nxt);
+        if (kPageScales) row_rels(j + 1, pid_nxt, rel_nxt);
+      }
       // the stage is free once BMM2(j - 2) has completed
       if (j >= kStages) ok = mbar_wait(&ctrl->kv_empty[s], ((j / kStages) - 1) & 1, abort_flag);
       if (!ok) break;
+      if (scale_lane) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) ctrl->key_scale[s][(dl >> 2) + 8 * i] = rel_cur[i];
+      }
       const uint32_t st = smem_u32(smem + kOffStages + s * kTileBytes) + (dl & 3) * 32;
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
@@ -444,7 +478,10 @@ decode_partial_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
       fence_proxy_async_smem();
       mbar_arrive(&ctrl->kv_full[s]);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) pid_cur[i] = pid_nxt[i];
+      for (int i = 0; i < 8; ++i) {
+        pid_cur[i] = pid_nxt[i];
+        if (kPageScales) rel_cur[i] = rel_nxt[i];
+      }
     }
   } else {
     // ------------------------------------------------------------------ softmax + epilogue (warps 0-3)
@@ -482,9 +519,26 @@ decode_partial_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
         mbar_arrive(&ctrl->s_free[sb]);
         // keys i <= lim of this lane's 32-key half are visible
         const int lim = row_active ? (min(kv_end - 1, lim_abs) - k0 - 32 * half) : -1;
-        // the int8 path multiplies P in f16 (P <= 2^8 here, where f16 keeps more bits than bf16)
-        online_softmax_step<32, true, kInt8>(sr, lim, scale_log2, kRescaleThreshold, m_used, l_sum, packed, alpha,
-                                            need_rescale);
+        if constexpr (kPageScales) {
+          // the keys' scales relative to kv_scale (written by the decode warps before they
+          // released the tile: waiting on that release orders their writes before the reads)
+          fail = __any_sync(0xffffffffu, !mbar_wait(&ctrl->kv_full[j % kStages], (j / kStages) & 1, abort_flag));
+          float ks[32];
+#pragma unroll
+          for (int i = 0; i < 32; i += 4) {
+            const float4 f = *reinterpret_cast<const float4*>(&ctrl->key_scale[j % kStages][32 * half + i]);
+            ks[i] = f.x;
+            ks[i + 1] = f.y;
+            ks[i + 2] = f.z;
+            ks[i + 3] = f.w;
+          }
+          online_softmax_step<32, true, true, true>(sr, lim, scale_log2, kRescaleThreshold, m_used, l_sum, packed,
+                                                    alpha, need_rescale, ks);
+        } else {
+          // the int8 path multiplies P in f16 (P <= 2^8 here, where f16 keeps more bits than bf16)
+          online_softmax_step<32, true, kInt8>(sr, lim, scale_log2, kRescaleThreshold, m_used, l_sum, packed,
+                                              alpha, need_rescale);
+        }
       }
       if (!fail && j >= 1) {
         fail = !mbar_wait(&ctrl->o_done, (j - 1) & 1, abort_flag);
@@ -794,6 +848,7 @@ cudaError_t launch_decode_partial(const DecodeParams& p, const CUtensorMap& tm_q
   switch (p.kv_dtype) {
     case kKvE4m3: return launch_decode_partial_e4m3(p, tm_q, tm_kv, head_groups, stream);
     case kKvInt8: return launch_partial_impl<kKvInt8>(p, tm_q, tm_kv, head_groups, stream);
+    case kKvInt8Page: return launch_partial_impl<kKvInt8Page>(p, tm_q, tm_kv, head_groups, stream);
     default: return launch_partial_impl<kKvBf16>(p, tm_q, tm_kv, head_groups, stream);
   }
 }

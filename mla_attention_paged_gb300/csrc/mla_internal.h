@@ -18,6 +18,7 @@ constexpr int kGroupRows = 64;   // folded query rows per decode CTA
 constexpr int kKvBf16 = 0;
 constexpr int kKvE4m3 = 1;
 constexpr int kKvInt8 = 2;
+constexpr int kKvInt8Page = 3;  // int8 codes times a scale per page
 
 // Device status word bits (OR-ed by kernels, read and cleared by mla_get_status).
 constexpr unsigned kStatusTimeout = 1u;
@@ -27,13 +28,15 @@ struct DecodeParams {
   int B, T, H, R;               // R = T*H folded rows per request
   int page_size, max_pages;     // page geometry and page_table row stride
   int chunk, max_splits, max_seq;
-  int kv_dtype;                 // kKvBf16, kKvE4m3 or kKvInt8
+  int kv_dtype;                 // kKvBf16, kKvE4m3, kKvInt8 or kKvInt8Page
   int64_t num_pages;            // pages in the pool: a page id outside [0, num_pages) is reported
   float scale_log2;             // softmax scale * log2(e) (* kv_scale for an 8-bit pool)
   float v_scale;                // 1, or kv_scale for an 8-bit pool (applied in the epilogue)
   const int32_t* page_table;
   const int32_t* seq_lens;
   const uint8_t* kv_pool;       // pool base (the 8-bit path reads raw rows from here)
+  const float* page_scales;     // kKvInt8Page: [num_pages] scale of each page's codes
+  float inv_ref_scale;          // kKvInt8Page: 1 / kv_scale (page scales are applied relative to it)
   __nv_bfloat16* out;           // [B, T, H, 512]
   float* lse;                   // [B, T, H]
   __nv_bfloat16* ws_o;          // [B, max_splits, R, 512] partial outputs (normalised, bf16)

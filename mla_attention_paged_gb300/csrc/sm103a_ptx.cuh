@@ -397,19 +397,25 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
 // kPairMax: the row is split between lanes l and l^16 (each holds N of its scores); the
 // tile max is exchanged between them, so both take identical running-state decisions and
 // each keeps the partial row sum of its own half.
-template <int N, bool kPairMax = false, bool kHalfP = false>
+// kScaled: key i carries a scale ks[i] (keys stored with a scale per page, relative to the
+// reference folded into scale_log2 and the output): its score is s[i] * ks[i], and the P
+// multiplied into its stored value row is P_i * ks[i], while l_sum takes P_i.
+template <int N, bool kPairMax = false, bool kHalfP = false, bool kScaled = false>
 __device__ __forceinline__ void online_softmax_step(const uint32_t (&s)[N], int lim, float scale_log2,
                                                     float threshold, float& m_used, float& l_sum,
-                                                    uint32_t (&packed)[N / 2], float& alpha, bool& need_rescale) {
+                                                    uint32_t (&packed)[N / 2], float& alpha, bool& need_rescale,
+                                                    const float* ks = nullptr) {
+  auto score = [&](int i) -> float { return kScaled ? __uint_as_float(s[i]) * ks[i] : __uint_as_float(s[i]); };
+  auto vw = [&](int i, float pi) -> float { return kScaled ? pi * ks[i] : pi; };
   const bool all = lim >= N - 1;
   float mx = -INFINITY;
   if (all) {
 #pragma unroll
-    for (int i = 0; i < N; ++i) mx = fmaxf(mx, __uint_as_float(s[i]));
+    for (int i = 0; i < N; ++i) mx = fmaxf(mx, score(i));
   } else {
 #pragma unroll
     for (int i = 0; i < N; ++i)
-      if (i <= lim) mx = fmaxf(mx, __uint_as_float(s[i]));
+      if (i <= lim) mx = fmaxf(mx, score(i));
   }
   if (kPairMax) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
   const float mt = mx * scale_log2;  // scale > 0: max commutes with the scaling; -inf stays -inf
@@ -428,20 +434,20 @@ __device__ __forceinline__ void online_softmax_step(const uint32_t (&s)[N], int 
   if (all) {
 #pragma unroll
     for (int i = 0; i < N; i += 2) {
-      const float p0 = ex2_approx(fmaf(__uint_as_float(s[i]), scale_log2, neg_m));
-      const float p1 = ex2_approx(fmaf(__uint_as_float(s[i + 1]), scale_log2, neg_m));
+      const float p0 = ex2_approx(fmaf(score(i), scale_log2, neg_m));
+      const float p1 = ex2_approx(fmaf(score(i + 1), scale_log2, neg_m));
       l0 += p0;
       l1 += p1;
-      packed[i >> 1] = kHalfP ? pack_f16x2(p0, p1) : pack_bf16x2(p0, p1);
+      packed[i >> 1] = kHalfP ? pack_f16x2(vw(i, p0), vw(i + 1, p1)) : pack_bf16x2(vw(i, p0), vw(i + 1, p1));
     }
   } else {
 #pragma unroll
     for (int i = 0; i < N; i += 2) {
-      const float p0 = (i <= lim) ? ex2_approx(fmaf(__uint_as_float(s[i]), scale_log2, neg_m)) : 0.f;
-      const float p1 = (i + 1 <= lim) ? ex2_approx(fmaf(__uint_as_float(s[i + 1]), scale_log2, neg_m)) : 0.f;
+      const float p0 = (i <= lim) ? ex2_approx(fmaf(score(i), scale_log2, neg_m)) : 0.f;
+      const float p1 = (i + 1 <= lim) ? ex2_approx(fmaf(score(i + 1), scale_log2, neg_m)) : 0.f;
       l0 += p0;
       l1 += p1;
-      packed[i >> 1] = kHalfP ? pack_f16x2(p0, p1) : pack_bf16x2(p0, p1);
+      packed[i >> 1] = kHalfP ? pack_f16x2(vw(i, p0), vw(i + 1, p1)) : pack_bf16x2(vw(i, p0), vw(i + 1, p1));
     }
   }
   l_sum += l0 + l1;

@@ -14,7 +14,7 @@ Recipe (all draws from one torch.Generator seeded per workload):
   * decode Q and latent KV: N(0, 1) / sqrt(576), bf16; scale 1/sqrt(192).
   * FP8 KV: latent N(0, 1), kv_scale = amax|x| / 448, codes = e4m3fn(x / kv_scale).
   * INT8 KV: latent N(0, 1), kv_scale = amax|x| / 127, codes = round(x / kv_scale) as int8.
-  * INT8 KV with a scale per page: each page's N(0, 1) latents times 2^U(-3, 3), encoded with
+  * INT8 KV with a scale per page: each page's N(0, 1) latents times 2^U(-2, 0), encoded with
     that page's amax / 127; kv_scale = the largest page scale.
   * pages: 64-token pages; each request owns ceil(L_b / 64) pages taken from one shared
     pool in a random permutation.
@@ -80,6 +80,8 @@ def decode_workloads():
             "decode_bf16_b16_q4_h16_l64k", 16, 4, 16, [65536] * 16, seed=1003),
         "decode_int8_b16_q4_h16_l64k": DecodeWorkload(
             "decode_int8_b16_q4_h16_l64k", 16, 4, 16, [65536] * 16, kv_dtype="int8", seed=1003),
+        "decode_int8page_b16_q4_h16_l64k": DecodeWorkload(
+            "decode_int8page_b16_q4_h16_l64k", 16, 4, 16, [65536] * 16, kv_dtype="int8page", seed=1003),
         # prefill in absorbed form over a paged prefix: 512 new tokens on 32K cached ones
         "decode_b4_q512_h16_l32k": DecodeWorkload(
             "decode_b4_q512_h16_l32k", 4, 512, 16, [32768 + 512] * 4, seed=1005),
@@ -160,11 +162,12 @@ def make_decode_inputs(wl: DecodeWorkload, device="cpu", max_pages=None) -> Deco
             pool[s:e] = torch.round(raw[s:e] / kv_scale).clamp_(-127.0, 127.0).to(torch.int8)
         del raw
     elif wl.kv_dtype == "int8page":
-        # a scale per page: each page's N(0,1) latents times a spread factor 2^U(-3,3), so
-        # that pages differ in range, encoded as round(x / s_page) with s_page = its amax / 127
+        # a scale per page: each page's N(0,1) latents times a spread factor 2^U(-2,0), so
+        # that pages differ in range (up to 4x) while values keep the other pools' size,
+        # encoded as round(x / s_page) with s_page = its amax / 127
         raw = torch.empty(n_pages, P, D_LATENT, dtype=torch.float32, device=dev)
         step = max(1, (1 << 27) // (P * D_LATENT))
-        spread = torch.pow(2.0, torch.rand(n_pages, generator=g, device=dev) * 6.0 - 3.0)
+        spread = torch.pow(2.0, torch.rand(n_pages, generator=g, device=dev) * 2.0 - 2.0)
         for s in range(0, n_pages, step):
             e = min(n_pages, s + step)
             raw[s:e] = torch.randn(e - s, P, D_LATENT, generator=g, device=dev) * spread[s:e, None, None]

@@ -24,9 +24,11 @@ MLA_ERR_DEVICE_ARG = 6
 MLA_KV_BF16 = 0
 MLA_KV_E4M3 = 1
 MLA_KV_INT8 = 2
+MLA_KV_INT8_PAGE = 3
 
 # Every function include/mla.h declares; each is given its C signature in _load().
 EXPORTED = ["mla_decode_plan", "mla_decode", "mla_decode_partial", "mla_decode_combine", "mla_decode_noalloc",
+            "mla_decode_int8_paged",
             "mla_prefill_varlen", "mla_prefill_paged", "mla_get_status", "mla_status_string", "mla_version", "mla_set_profile_events",
             "mla_profile_elapsed_ms", "mla_selftest_wait_timeout"]
 
@@ -64,6 +66,9 @@ def _load() -> ctypes.CDLL:
     lib.mla_decode_noalloc.restype = i32
     lib.mla_decode_noalloc.argtypes = [ctypes.POINTER(DecodePlan), P, P, P, P, i32, i32, f32, f32, P, P, P]
     lib.mla_decode_combine.argtypes = [ctypes.POINTER(DecodePlan), P, i32, i32, P, P, P, sz, P]
+    lib.mla_decode_int8_paged.restype = i32
+    lib.mla_decode_int8_paged.argtypes = [ctypes.POINTER(DecodePlan), P, P, P, P, P, i32, i32, f32, f32, P, P, P,
+                                          sz, P]
     lib.mla_prefill_varlen.restype = i32
     lib.mla_prefill_varlen.argtypes = [P, P, P, P, P, P, i32, i32, i32, i32, i32, f32, P, P, P]
     lib.mla_prefill_paged.restype = i32
@@ -139,6 +144,26 @@ def decode(plan: DecodePlan, q: torch.Tensor, kv_pages: torch.Tensor, page_table
                         int(H), float(scale), float(kv_scale), _ptr(out), _ptr(lse), _ptr(workspace),
                         int(ws_bytes), _stream_handle(stream))
     _check(rc, "mla_decode")
+    return out, lse
+
+
+def decode_int8_paged(plan: DecodePlan, q: torch.Tensor, kv_pages: torch.Tensor, page_scales: torch.Tensor,
+                      page_table: torch.Tensor, seq_lens: torch.Tensor, scale: float, kv_scale: float, out=None,
+                      lse=None, workspace=None, stream=None):
+    """mla_decode_int8_paged through the C ABI: an int8 pool with one fp32 scale per page
+    (page_scales [num_pages] on the device).  Returns (out [B,T,H,512] bf16, lse [B,T,H] fp32)."""
+    B, T, H, D = q.shape
+    if out is None:
+        out = torch.empty(B, T, H, 512, dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.empty(B, T, H, dtype=torch.float32, device=q.device)
+    if workspace is None and plan.workspace_bytes:
+        workspace = workspace_for(plan, q.device)
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    rc = lib.mla_decode_int8_paged(ctypes.byref(plan), _ptr(q), _ptr(kv_pages), _ptr(page_scales), _ptr(page_table),
+                                   _ptr(seq_lens), int(T), int(H), float(scale), float(kv_scale), _ptr(out),
+                                   _ptr(lse), _ptr(workspace), int(ws_bytes), _stream_handle(stream))
+    _check(rc, "mla_decode_int8_paged")
     return out, lse
 
 

@@ -247,3 +247,28 @@ def test_decode_validates_before_touching_the_device(mla):
     rc = mla.lib.mla_decode(ctypes.byref(plan), fake, fake, fake, fake, 4, 16, 0.0, 1.0, fake, fake, fake,
                             plan.workspace_bytes, None)
     assert rc == mla.MLA_ERR_INVALID_ARG
+
+
+def test_int8_paged_entry_validates_before_touching_the_device(mla):
+    """A pool with a scale per page goes through mla_decode_int8_paged only, with its scales;
+    no other pool takes scales.  Every call below fails validation on the host."""
+    paged = mla.decode_plan([4096] * 2, 2, 16, 64, 64, 256, mla.MLA_KV_INT8_PAGE, num_sms=152)
+    plain = mla.decode_plan([4096] * 2, 2, 16, 64, 64, 256, mla.MLA_KV_INT8, num_sms=152)
+    fake = ctypes.c_void_p(1 << 20)  # never dereferenced
+    ws = max(paged.workspace_bytes, plain.workspace_bytes)
+    # mla_decode has no scales for a per-page pool
+    rc = mla.lib.mla_decode(ctypes.byref(paged), fake, fake, fake, fake, 2, 16, 0.07, 1.0, fake, fake, fake, ws, None)
+    assert rc == mla.MLA_ERR_INVALID_ARG
+    rc = mla.lib.mla_decode_partial(ctypes.byref(paged), fake, fake, fake, fake, 2, 16, 0.07, 1.0, fake, fake, fake,
+                                    ws, None)
+    assert rc == mla.MLA_ERR_INVALID_ARG
+    # the per-page entry point refuses other plans, null scales and misaligned scales
+    rc = mla.lib.mla_decode_int8_paged(ctypes.byref(plain), fake, fake, fake, fake, fake, 2, 16, 0.07, 1.0, fake,
+                                       fake, fake, ws, None)
+    assert rc == mla.MLA_ERR_INVALID_ARG
+    rc = mla.lib.mla_decode_int8_paged(ctypes.byref(paged), fake, fake, None, fake, fake, 2, 16, 0.07, 1.0, fake,
+                                       fake, fake, ws, None)
+    assert rc == mla.MLA_ERR_INVALID_ARG
+    rc = mla.lib.mla_decode_int8_paged(ctypes.byref(paged), fake, fake, ctypes.c_void_p((1 << 20) + 2), fake, fake,
+                                       2, 16, 0.07, 1.0, fake, fake, fake, ws, None)
+    assert rc == mla.MLA_ERR_INVALID_ARG

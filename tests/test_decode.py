@@ -39,9 +39,15 @@ def run_gpu(mla, inp, num_sms=0, dev="cuda"):
     pt = inp.page_table.to(dev)
     sl = inp.seq_lens.to(dev)
     kvd = {torch.uint8: mla.MLA_KV_E4M3, torch.int8: mla.MLA_KV_INT8}.get(pool.dtype, mla.MLA_KV_BF16)
+    if inp.page_scales is not None:
+        kvd = mla.MLA_KV_INT8_PAGE
     plan = mla.decode_plan(inp.seq_lens.cpu(), wl.q_len, wl.heads, wl.page_size, pt.shape[1], pool.shape[0],
                            kvd, num_sms)
-    out, lse = mla.decode(plan, q, pool, pt, sl, inp.scale, inp.kv_scale)
+    if inp.page_scales is not None:
+        out, lse = mla.decode_int8_paged(plan, q, pool, inp.page_scales.to(dev).float(), pt, sl, inp.scale,
+                                         inp.kv_scale)
+    else:
+        out, lse = mla.decode(plan, q, pool, pt, sl, inp.scale, inp.kv_scale)
     torch.cuda.synchronize()
     assert mla.get_status() == mla.MLA_OK
     return out.float().cpu().numpy(), lse.cpu().numpy(), plan
@@ -63,7 +69,7 @@ def _full_check(mla, oracle_mod, wl, num_sms=0):
     inp = make_decode_inputs(wl, "cpu")
     out, lse, plan = run_gpu(mla, inp, num_sms)
     ref_out, ref_lse = oracle_mod.mla_decode(inp.q, inp.kv_pool, inp.page_table, inp.seq_lens, inp.scale,
-                                             kv_scale=inp.kv_scale)
+                                             kv_scale=inp.kv_scale, page_scales=inp.page_scales)
     check(out, lse, ref_out, ref_lse, fp8=(wl.kv_dtype != "bf16"))
     return out, lse, plan
 
@@ -98,6 +104,10 @@ SMALL = [
     ("int8_page16", 2, 2, 16, [77, 500], 16, "int8"),
     ("int8_page128", 1, 3, 16, [700], 128, "int8"),
     ("int8_h128", 1, 2, 128, [900], 64, "int8"),
+    ("int8page_drafts4", 2, 4, 16, [300, 1000], 64, "int8page"),
+    ("int8page_ragged", 3, 1, 16, [1, 65, 130], 64, "int8page"),
+    ("int8page_page16", 2, 2, 16, [77, 500], 16, "int8page"),
+    ("int8page_page128", 1, 3, 16, [700], 128, "int8page"),
 ]
 
 
@@ -264,7 +274,7 @@ def test_decode_e4m3_dominant_key_over_long_tail(mla, oracle_mod):
     assert row_rel.max() <= REL_L2, f"worst row rel-L2 {row_rel.max():.3e}"
 
 
-@pytest.mark.parametrize("kv", ["bf16", "e4m3", "int8"])
+@pytest.mark.parametrize("kv", ["bf16", "e4m3", "int8", "int8page"])
 def test_decode_running_max_rises_every_tile(mla, oracle_mod, kv):
     """Keys built so that each row's scores climb 4 to 7 (head h: 4 (1 + h/20)) in the log2
     domain every 64 keys: the running max moves on every tile of the e4m3 kernel (threshold
@@ -289,9 +299,13 @@ def test_decode_running_max_rises_every_tile(mla, oracle_mod, kv):
     elif kv == "e4m3":
         inp.kv_scale = float(x.abs().max()) / 448.0
         inp.kv_pool = (x / inp.kv_scale).clamp(-448.0, 448.0).float().to(torch.float8_e4m3fn).view(torch.uint8)
-    else:
+    elif kv == "int8":
         inp.kv_scale = float(x.abs().max()) / 127.0
         inp.kv_pool = torch.round(x / inp.kv_scale).clamp(-127.0, 127.0).to(torch.int8)
+    else:
+        inp.page_scales = x.abs().amax(dim=(1, 2)).clamp(min=1e-30) / 127.0
+        inp.kv_scale = float(inp.page_scales.max())
+        inp.kv_pool = torch.round(x / inp.page_scales[:, None, None]).clamp(-127.0, 127.0).to(torch.int8)
     c = math.log(2.0) / inp.scale  # a key's score in the log2 domain is then its k . u
     q = torch.empty(2, 2, 16, 576, dtype=torch.float64)
     for h in range(16):
@@ -299,7 +313,7 @@ def test_decode_running_max_rises_every_tile(mla, oracle_mod, kv):
     inp.q = q.to(torch.bfloat16)
     out, lse, _ = run_gpu(mla, inp)
     ref_out, ref_lse = oracle_mod.mla_decode(inp.q, inp.kv_pool, inp.page_table, inp.seq_lens, inp.scale,
-                                             kv_scale=inp.kv_scale)
+                                             kv_scale=inp.kv_scale, page_scales=inp.page_scales)
     check(out, lse, ref_out, ref_lse, fp8=(kv != "bf16"))
 
 
@@ -363,7 +377,8 @@ def test_decode_full_size_sampled(mla, oracle_mod, name):
     out, lse, plan = run_gpu(mla, inp)
     rows = _sample_rows(wl, per_request=16 if wl.batch <= 4 else 6)
     ref_out, ref_lse = oracle_mod.mla_decode(inp.q.cpu(), inp.kv_pool.cpu(), inp.page_table.cpu(),
-                                             inp.seq_lens.cpu(), inp.scale, kv_scale=inp.kv_scale, rows=rows)
+                                             inp.seq_lens.cpu(), inp.scale, kv_scale=inp.kv_scale, rows=rows,
+                                             page_scales=inp.page_scales)
     check(out.reshape(-1, 512)[rows], lse.reshape(-1)[rows], ref_out, ref_lse, fp8=(wl.kv_dtype != "bf16"))
     # every output finite, including rows not sampled
     assert np.isfinite(out).all() and np.isfinite(lse).all()

@@ -61,7 +61,13 @@ def test_length_beyond_plan_is_reported(mla):
     assert mla.get_status() == mla.MLA_OK
 
 
-@pytest.mark.parametrize("kv", ["bf16", "e4m3", "int8"])
+def _decode_any(mla, plan, q, pool, scales, pt, sl, scale, kv_scale):
+    if scales is not None:
+        return mla.decode_int8_paged(plan, q, pool, scales, pt, sl, scale, kv_scale)
+    return mla.decode(plan, q, pool, pt, sl, scale, kv_scale)
+
+
+@pytest.mark.parametrize("kv", ["bf16", "e4m3", "int8", "int8page"])
 @pytest.mark.parametrize("bad", ["negative", "past_pool"])
 def test_page_id_outside_pool_is_reported(mla, kv, bad):
     """A page id outside [0, num_pages) is reported as MLA_ERR_DEVICE_ARG.  The pool given
@@ -74,15 +80,37 @@ def test_page_id_outside_pool_is_reported(mla, kv, bad):
     big = torch.zeros((n + 32,) + tuple(inp.kv_pool.shape[1:]), dtype=inp.kv_pool.dtype, device="cuda")
     big[16:16 + n] = inp.kv_pool.cuda()
     pool = big[16:16 + n]
-    kvd = {"e4m3": mla.MLA_KV_E4M3, "int8": mla.MLA_KV_INT8}.get(kv, mla.MLA_KV_BF16)
+    kvd = {"e4m3": mla.MLA_KV_E4M3, "int8": mla.MLA_KV_INT8,
+           "int8page": mla.MLA_KV_INT8_PAGE}.get(kv, mla.MLA_KV_BF16)
     plan = mla.decode_plan([700, 300], 2, 16, 64, inp.page_table.shape[1], n, kvd)
+    scales = inp.page_scales.cuda().float() if inp.page_scales is not None else None
     pt = inp.page_table.clone()
     pt[0, 3] = -1 if bad == "negative" else n + 5
-    mla.decode(plan, inp.q.cuda(), pool, pt.cuda(), inp.seq_lens.cuda(), inp.scale, inp.kv_scale)
+    _decode_any(mla, plan, inp.q.cuda(), pool, scales, pt.cuda(), inp.seq_lens.cuda(), inp.scale, inp.kv_scale)
     torch.cuda.synchronize()
     assert mla.get_status() == mla.MLA_ERR_DEVICE_ARG
     # the valid table runs clean afterwards
-    mla.decode(plan, inp.q.cuda(), pool, inp.page_table.cuda(), inp.seq_lens.cuda(), inp.scale, inp.kv_scale)
+    _decode_any(mla, plan, inp.q.cuda(), pool, scales, inp.page_table.cuda(), inp.seq_lens.cuda(), inp.scale,
+                inp.kv_scale)
+    torch.cuda.synchronize()
+    assert mla.get_status() == mla.MLA_OK
+
+
+@pytest.mark.parametrize("bad", [-1.0, float("nan"), 300.0])
+def test_page_scale_outside_range_is_reported(mla, bad):
+    """A page scale (relative to kv_scale) that is negative, not finite or above 255, on a
+    page a request reads, is reported as MLA_ERR_DEVICE_ARG; valid scales run clean after."""
+    wl = DecodeWorkload("bad_scale", 2, 2, 16, [700, 300], kv_dtype="int8page", seed=8)
+    inp = make_decode_inputs(wl, "cuda")
+    n = inp.kv_pool.shape[0]
+    plan = mla.decode_plan([700, 300], 2, 16, 64, inp.page_table.shape[1], n, mla.MLA_KV_INT8_PAGE)
+    scales = inp.page_scales.float().clone()
+    scales[int(inp.page_table[1, 2])] = bad * inp.kv_scale
+    mla.decode_int8_paged(plan, inp.q, inp.kv_pool, scales, inp.page_table, inp.seq_lens, inp.scale, inp.kv_scale)
+    torch.cuda.synchronize()
+    assert mla.get_status() == mla.MLA_ERR_DEVICE_ARG
+    mla.decode_int8_paged(plan, inp.q, inp.kv_pool, inp.page_scales.float(), inp.page_table, inp.seq_lens,
+                          inp.scale, inp.kv_scale)
     torch.cuda.synchronize()
     assert mla.get_status() == mla.MLA_OK
 

@@ -39,10 +39,13 @@ constexpr int kTileBytes = kDimBlocks * kBlockBytes; // 73728: one bf16 64-key l
 constexpr int kStages = 2;
 constexpr int kPrefetchTiles = 3;  // int8 pools: tiles ahead of the decode that are prefetched into L2
 // Warps 0-3 softmax/epilogue, 5 MMA; bf16: warp 4 producer (192 threads); int8 pools:
-// warps 4, 6 and 7 decode (256 threads: eight warps keep the register budget at 255 per
-// thread).
-constexpr int kDequantThreads = 96;
-__host__ __device__ constexpr int threads_for(bool fp8) { return fp8 ? 256 : 192; }
+// warps 4 and 6-10 decode (352 threads), each lane holding four rows' codes of its tile.
+constexpr int kDecodeWarps = 6;
+constexpr int kDequantThreads = 32 * kDecodeWarps;
+// int8: softmax warps 0-3, decode warp 4, MMA warp 5, decode warps 6 .. 4 + kDecodeWarps
+__host__ __device__ constexpr int threads_for(bool fp8) { return fp8 ? 32 * (5 + kDecodeWarps) : 192; }
+static_assert(threads_for(true) / 32 - 1 == 4 + kDecodeWarps, "the last int8 warp is the last decode warp");
+static_assert(1 + (threads_for(true) / 32 - 6) == kDecodeWarps, "decode warps: 4 and 6 ..");
 
 // Shared memory map: Q | stage0 | stage1 | P | ctrl.  A stage holds one 64-key tile as nine
 // 128-byte-swizzled column blocks: bf16 as loaded by TMA, or (int8 pools) f16 as decoded
@@ -366,16 +369,18 @@ decode_partial_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
     }
     __syncwarp();
   } else if (kInt8 && warp >= 4) {
-    // ------------------------------------------------------------------ int8 dequant (warps 4, 6, 7):
+    // ------------------------------------------------------------------ int8 dequant (warps 4, 6-10):
     // Q to f16 in place once; then, per tile, each lane reads its rows' int8 bytes straight
     // from the page pool into registers (issued before waiting for the stage, so the reads
     // overlap the previous tile's GEMMs), waits for the stage, and writes them as f16 into
-    // the swizzled tile.  Lane dl of decode warp dw (0..2) owns rows dl/4 + 8i (i < 8) and
-    // 16-byte chunk dl % 4 of column blocks dw, dw + 3 and dw + 6.  (The MMA warp prefetches
+    // the swizzled tile.  Lane dl of decode warp dw (0..5) owns rows 32 (dw / 3) + dl/4 + 8i
+    // (i < 4) and 16-byte chunk dl % 4 of column blocks dw % 3, + 3 and + 6.  (The MMA warp prefetches
     // the rows into L2 kPrefetchTiles tiles ahead.)
     const int dw = (warp == 4) ? 0 : warp - 5;
     const int dl = lane;
     const int td = dw * 32 + dl;
+    const int bg = dw % 3;                        // column blocks bg, bg + 3, bg + 6
+    const int rbase0 = 32 * (dw / 3) + (dl >> 2);  // first owned row; then every 8th, four in all
     const int P = p.page_size;
     const int32_t* pt = p.page_table + static_cast<int64_t>(b) * p.max_pages;
     // Every page id this split reads (rows kv_start .. kv_end - 1) is checked once, before
@@ -418,43 +423,43 @@ decode_partial_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
       ok = false;
     }
     // page id of each owned row of tile j (0 past the request end: the row is not read)
-    auto row_pids = [&](int j, int (&pid)[8]) {
+    auto row_pids = [&](int j, int (&pid)[4]) {
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int k = kv_start + j * kTileKeys + (dl >> 2) + 8 * i;
+      for (int i = 0; i < 4; ++i) {
+        const int k = kv_start + j * kTileKeys + rbase0 + 8 * i;
         pid[i] = (k < L) ? __ldg(pt + k / P) : 0;
       }
     };
-    int pid_cur[8];
+    int pid_cur[4];
     row_pids(0, pid_cur);
-    // per-page scales: eight lanes of the first decode warp hold the scale (relative to
-    // kv_scale) of each of a tile's 64 rows, loaded one tile ahead; rows past the request
-    // end get 0
-    const bool scale_lane = kPageScales && dw == 0 && (dl & 3) == 0;
-    auto row_rels = [&](int j, const int (&pid)[8], float (&rel)[8]) {
+    // per-page scales: eight lanes of each of decode warps 0 and 3 hold the scale (relative
+    // to kv_scale) of each of their 32 rows of a tile, loaded one tile ahead; rows past the
+    // request end get 0
+    const bool scale_lane = kPageScales && bg == 0 && (dl & 3) == 0;
+    auto row_rels = [&](int j, const int (&pid)[4], float (&rel)[4]) {
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int k = kv_start + j * kTileKeys + (dl >> 2) + 8 * i;
+      for (int i = 0; i < 4; ++i) {
+        const int k = kv_start + j * kTileKeys + rbase0 + 8 * i;
         rel[i] = (scale_lane && k < L) ? __ldg(p.page_scales + pid[i]) * p.inv_ref_scale : 0.f;
       }
     };
-    float rel_cur[8];
+    float rel_cur[4];
     if (kPageScales) row_rels(0, pid_cur, rel_cur);
     for (int j = 0; ok && j < ntiles; ++j) {
       const int s = j % kStages;
       const int k0 = kv_start + j * kTileKeys;
-      uint4 w[3][8];
+      uint4 w[3][4];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int k = k0 + (dl >> 2) + 8 * i;
+      for (int i = 0; i < 4; ++i) {
+        const int k = k0 + rbase0 + 8 * i;
         const uint8_t* row = p.kv_pool + (static_cast<int64_t>(pid_cur[i]) * P + k % P) * kLatentDim + (dl & 3) * 16;
         const bool valid = k < L;
 #pragma unroll
         for (int m = 0; m < 3; ++m)
-          w[m][i] = valid ? __ldg(reinterpret_cast<const uint4*>(row + (dw + 3 * m) * 64)) : make_uint4(0u, 0u, 0u, 0u);
+          w[m][i] = valid ? __ldg(reinterpret_cast<const uint4*>(row + (bg + 3 * m) * 64)) : make_uint4(0u, 0u, 0u, 0u);
       }
-      int pid_nxt[8];
-      float rel_nxt[8];
+      int pid_nxt[4];
+      float rel_nxt[4];
       if (j + 1 < ntiles) {
         row_pids(j + 1, pid_nxt);
         if (kPageScales) row_rels(j + 1, pid_nxt, rel_nxt);
@@ -464,21 +469,21 @@ decode_partial_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
       if (!ok) break;
       if (scale_lane) {
 #pragma unroll
-        for (int i = 0; i < 8; ++i) ctrl->key_scale[s][(dl >> 2) + 8 * i] = rel_cur[i];
+        for (int i = 0; i < 4; ++i) ctrl->key_scale[s][rbase0 + 8 * i] = rel_cur[i];
       }
       const uint32_t st = smem_u32(smem + kOffStages + s * kTileBytes) + (dl & 3) * 32;
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int row = (dl >> 2) + 8 * i;
+      for (int i = 0; i < 4; ++i) {
+        const int row = rbase0 + 8 * i;
         const uint32_t rbase = st + row * 128;
         const int sw = (row & 7) << 4;
 #pragma unroll
-        for (int m = 0; m < 3; ++m) store_f16_chunk_int8(rbase + (dw + 3 * m) * kBlockBytes, sw, w[m][i]);
+        for (int m = 0; m < 3; ++m) store_f16_chunk_int8(rbase + (bg + 3 * m) * kBlockBytes, sw, w[m][i]);
       }
       fence_proxy_async_smem();
       mbar_arrive(&ctrl->kv_full[s]);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
+      for (int i = 0; i < 4; ++i) {
         pid_cur[i] = pid_nxt[i];
         if (kPageScales) rel_cur[i] = rel_nxt[i];
       }
@@ -583,17 +588,44 @@ decode_partial_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
         // O^T[dim, row] *= alpha[row] for all 512 value columns; this thread owns TMEM lane
         // (warp*32 + lane) of each 128-column chunk.
         tc_fence_after();
+        if constexpr (kInt8) {
+          // (the int8 kernels run at a lower register cap: rows 32hh .. 32hh+31 at a time,
+          // so that only their 32 factors are held in registers)
 #pragma unroll 1
-        for (int qc = 0; qc < 4; ++qc) {
-#pragma unroll
           for (int hh = 0; hh < 2; ++hh) {
-            uint32_t v[32];
-            const uint32_t addr = tmem + lane_base + qc * 64 + hh * 32;
-            tmem_ld32(addr, v);
-            tmem_ld_wait();
+            float al[32];
 #pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * ctrl->alpha[hh * 32 + i]);
-            tmem_st32(addr, v);
+            for (int i = 0; i < 32; i += 4) {
+              const float4 f = *reinterpret_cast<const float4*>(&ctrl->alpha[hh * 32 + i]);
+              al[i] = f.x;
+              al[i + 1] = f.y;
+              al[i + 2] = f.z;
+              al[i + 3] = f.w;
+            }
+#pragma unroll 1
+            for (int qc = 0; qc < 4; ++qc) {
+              uint32_t v[32];
+              const uint32_t addr = tmem + lane_base + qc * 64 + hh * 32;
+              tmem_ld32(addr, v);
+              tmem_ld_wait();
+#pragma unroll
+              for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * al[i]);
+              tmem_st32(addr, v);
+            }
+          }
+        } else {
+#pragma unroll 1
+          for (int qc = 0; qc < 4; ++qc) {
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+              uint32_t v[32];
+              const uint32_t addr = tmem + lane_base + qc * 64 + hh * 32;
+              tmem_ld32(addr, v);
+              tmem_ld_wait();
+#pragma unroll
+              for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * ctrl->alpha[hh * 32 + i]);
+              tmem_st32(addr, v);
+            }
           }
         }
         tmem_st_wait();
@@ -630,30 +662,60 @@ decode_partial_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
       // rounded to the bf16 output anyway, and half the bytes is half the extra traffic.
       // The 64 row scales go to registers first: shared-memory loads interleaved with the
       // staging stores below would each have to wait for the stores before them.
-      float rs[kGroupRows];
-#pragma unroll
-      for (int i = 0; i < kGroupRows; i += 4) {
-        const float4 f = *reinterpret_cast<const float4*>(&ctrl->row_scale[i]);
-        rs[i] = f.x;
-        rs[i + 1] = f.y;
-        rs[i + 2] = f.z;
-        rs[i + 3] = f.w;
-      }
       const uint32_t stage_s = smem_u32(smem + kOffStages);  // [64][512] bf16
+      if constexpr (kInt8) {
+        // (the int8 kernels run at a lower register cap: rows 32hh .. 32hh+31 at a time,
+        // their 32 scales in registers)
 #pragma unroll 1
-      for (int qc = 0; qc < 4; ++qc) {
-        const int dim = qc * 128 + warp * 32 + lane;
-#pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
-          uint32_t v[32];
-          tmem_ld32(tmem + lane_base + qc * 64 + hh * 32, v);
-          tmem_ld_wait();
+          float rs[32];
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const int rr = hh * 32 + i;
-            const __nv_bfloat16 o = __float2bfloat16_rn(__uint_as_float(v[i]) * rs[rr]);
-            asm volatile("st.shared.b16 [%0], %1;" ::"r"(stage_s + (rr * kValueDim + dim) * 2),
-                         "h"(*reinterpret_cast<const uint16_t*>(&o)));
+          for (int i = 0; i < 32; i += 4) {
+            const float4 f = *reinterpret_cast<const float4*>(&ctrl->row_scale[hh * 32 + i]);
+            rs[i] = f.x;
+            rs[i + 1] = f.y;
+            rs[i + 2] = f.z;
+            rs[i + 3] = f.w;
+          }
+#pragma unroll 1
+          for (int qc = 0; qc < 4; ++qc) {
+            const int dim = qc * 128 + warp * 32 + lane;
+            uint32_t v[32];
+            tmem_ld32(tmem + lane_base + qc * 64 + hh * 32, v);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              const __nv_bfloat16 o = __float2bfloat16_rn(__uint_as_float(v[i]) * rs[i]);
+              asm volatile("st.shared.b16 [%0], %1;" ::"r"(stage_s + ((hh * 32 + i) * kValueDim + dim) * 2),
+                           "h"(*reinterpret_cast<const uint16_t*>(&o)));
+            }
+          }
+        }
+      } else {
+        float rs[kGroupRows];
+#pragma unroll
+        for (int i = 0; i < kGroupRows; i += 4) {
+          const float4 f = *reinterpret_cast<const float4*>(&ctrl->row_scale[i]);
+          rs[i] = f.x;
+          rs[i + 1] = f.y;
+          rs[i + 2] = f.z;
+          rs[i + 3] = f.w;
+        }
+#pragma unroll 1
+        for (int qc = 0; qc < 4; ++qc) {
+          const int dim = qc * 128 + warp * 32 + lane;
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            uint32_t v[32];
+            tmem_ld32(tmem + lane_base + qc * 64 + hh * 32, v);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              const int rr = hh * 32 + i;
+              const __nv_bfloat16 o = __float2bfloat16_rn(__uint_as_float(v[i]) * rs[rr]);
+              asm volatile("st.shared.b16 [%0], %1;" ::"r"(stage_s + (rr * kValueDim + dim) * 2),
+                           "h"(*reinterpret_cast<const uint16_t*>(&o)));
+            }
           }
         }
       }

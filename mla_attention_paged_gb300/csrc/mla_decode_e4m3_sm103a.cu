@@ -13,7 +13,7 @@
 // threads: softmax warps 0-7, producer warp 8, BMM1 warp 9, BMM2 warp 10).  Both GEMMs run on
 // the 8-bit codes as they arrive (kind::f8f6f4); nothing is decoded to a wider type:
 //  * The raw e4m3 tile (64 keys x 576 codes, 36 KB) arrives by TMA (64-byte swizzle) in a
-//    4-stage ring, its rows prefetched into L2 ahead of the load.
+//    5-stage ring, its rows prefetched into L2 ahead of the load.
 //  * Q keeps its bf16 value: each query row, scaled by a power of two 2^s that brings its
 //    largest element into [128, 256), is split into q_hi = e4m3(q 2^s) and
 //    q_lo = e4m3(q 2^s - q_hi), an 8-bit significand in two 4-bit halves.  This is exact
@@ -22,8 +22,11 @@
 //    2^-17 of the row's largest |q|.
 //  * BMM1 (M = 128, N = 64 keys, K = 576): the A operand stacks q_hi and q_lo, 16 rows of
 //    each in turn, so that row r's hi and lo partial scores land in TMEM lanes i and i + 16
-//    of the same warp (i = 32 (r / 16) + r % 16).  One shuffle adds them; each lane then
-//    holds half the row's keys.  One pass of full-rate MMAs reads the K tile once.
+//    of the same warp (i = 32 (r / 16) + r % 16), and one shuffle between the two lanes
+//    adds them.  One pass of full-rate MMAs reads the K tile once.  The split's column
+//    blocks 0-7 sit in TMEM (the A operand from tensor memory: stacked row = lane, four
+//    codes per 32-bit column), the rope block 8 in shared memory; the stacked Q is then not
+//    re-read from shared memory on every tile.
 //  * BMM2 (O^T += V^T . P^T, M = 128 value columns, N = rows, K = 64 keys) takes V straight
 //    from the raw stage as an MN-major e4m3 operand.  P is split in two 8-bit parts: the
 //    softmax forms P 2^6 (at most 2^8, because the running max moves once a tile's max
@@ -40,9 +43,13 @@
 //    (stale codes there could be NaN, and 0 * NaN is NaN).
 //  * BMM1 and BMM2 are issued by two warps, each waiting on its own inputs: issuing blocks
 //    while the tensor pipe is busy.
-//  * Shared memory: stacked q_hi / q_lo (72 KB) | raw ring (4 x 36 KB) | p_hi, p_lo
-//    (2 x 4 KB) | control (2 KB): 227 KB.  The bf16 Q tile lands by TMA on ring stages 2-3 and is split from there
-//    before their first load; the epilogue stages the bf16 output in stages 0-1.
+//  * P is double-buffered by tile parity: the softmax of tile j waits only for BMM2 of tile
+//    j-2 (which read its buffer).
+//  * TMEM: O^T (256 columns) | two S buffers (2 x 64) | split blocks 0-7 (128).  Shared
+//    memory: the split's rope block (8 KB) | raw ring (5 x 36 KB) | two P buffers (p_hi |
+//    p_lo, 2 x 8 KB) | control.  The bf16 Q tile lands by TMA on ring stages 1-2 and is
+//    split from there before their first load; the epilogue stages the bf16 output in
+//    stages 0-1.
 //  * Softmax and epilogue: eight warps, two per TMEM lane quadrant, so that two warps share
 //    each scheduler (one alone left most of its cycles to latency).  Each row's 64 keys are
 //    spread over four threads (16 each); P is formed and split in f16x2 arithmetic; lazy
@@ -59,21 +66,21 @@ namespace mla {
 namespace {
 
 constexpr int kBlocks = kLatentDim / 64;           // 9 column blocks of 64
-constexpr int kStages = 4;                         // raw ring depth
+constexpr int kStages = 5;                         // raw ring depth
 constexpr int kRawBlock = 64 * 64;                 // 64 keys x 64 one-byte codes (64-byte swizzle)
 constexpr int kRawTile = kBlocks * kRawBlock;      // 36864
-constexpr int kQ8Block = 128 * 64;                 // 128 stacked hi/lo rows x 64 codes
-constexpr int kQ8Bytes = kBlocks * kQ8Block;       // 73728
+constexpr int kQRBytes = 128 * 64;                 // the split's rope block: 128 stacked rows x 64 codes
 constexpr int kF16Block = 64 * 128;                // 64 rows x 64 16-bit columns (128-byte swizzle)
 constexpr int kQBf16Bytes = kBlocks * kF16Block;   // 73728
 constexpr int kPPart = 64 * 64;                    // p_hi (e4m3) or p_lo (e5m2): 64 rows x 64 keys
-constexpr int kOffQ8 = 0;
-constexpr int kOffRaw = kQ8Bytes;                  // raw ring
-constexpr int kOffP = kOffRaw + kStages * kRawTile;
-constexpr int kOffCtrl = kOffP + 2 * kPPart;
-constexpr int kOffQBf16 = kOffRaw + 2 * kRawTile;  // the bf16 Q tile lands on ring stages 2-3
+constexpr int kPBuf = 2 * kPPart;                  // one P buffer: p_hi | p_lo
+constexpr int kOffQR = 0;
+constexpr int kOffRaw = kQRBytes;                  // raw ring
+constexpr int kOffP = kOffRaw + kStages * kRawTile;  // two P buffers (tile parity)
+constexpr int kOffCtrl = kOffP + 2 * kPBuf;
+constexpr int kOffQBf16 = kOffRaw + kRawTile;      // the bf16 Q tile lands on ring stages 1-2
 constexpr int kOffOStage = kOffRaw;                // [64][512] bf16 output staging (stages 0-1)
-static_assert(kOffQBf16 + kQBf16Bytes == kOffP, "bf16 Q staging spans ring stages 2-3 exactly");
+static_assert(kQBf16Bytes == 2 * kRawTile, "bf16 Q staging spans ring stages 1-2 exactly");
 static_assert(kGroupRows * kValueDim * 2 <= 2 * kRawTile, "output staging fits ring stages 0-1");
 
 constexpr int kSoftmaxWarps = 8;  // two per TMEM lane quadrant, one per half of the key tile
@@ -92,21 +99,24 @@ struct Ctrl {
   uint64_t raw_empty[kStages]; // BMM1 and BMM2 of the tile done (two commits)
   uint64_t s_full[2];
   uint64_t s_free[2];
-  uint64_t p_full;
-  uint64_t o_done;
+  uint64_t p_full[2];          // P buffer written (softmax threads), by tile parity
+  uint64_t o_done[2];          // BMM2 of the tile done (commit), by tile parity
   uint64_t mma_drain;
   uint64_t mma_drain2;         // the BMM2 warp's MMAs
   uint32_t tmem_base;
   int abort_flag;
-  alignas(16) int rescale_flag[kSoftmaxWarps];
-  alignas(16) float alpha[kGroupRows];
+  // by tile parity: written before a tile's closing barrier and read after it, while the
+  // next tile's writes may already run (it waits only for the BMM2 two tiles back)
+  alignas(16) int rescale_flag[2][kSoftmaxWarps];
+  alignas(16) float alpha[2][kGroupRows];
+  alignas(16) float q_mult[kGroupRows];     // 2^s of each row's Q split
   // [0][half of the key tile][row]: partial row maxima of a tile, swapped between the two
   // warps of a lane quadrant; at the end [0] and [1] hold the halves' row sums l / l_use
   float red[2][2][kGroupRows];
   alignas(16) float row_scale[kGroupRows];
   alignas(16) float q_unscale[kGroupRows];  // 2^-s of each row's Q split
 };
-constexpr int kCtrlBytes = 2048;
+constexpr int kCtrlBytes = 3072;
 constexpr int kSmemBytes = kOffCtrl + kCtrlBytes + 1024;  // + control block + alignment slack
 static_assert(sizeof(Ctrl) <= kCtrlBytes, "control block");
 static_assert(kSmemBytes <= 232448, "shared memory per block");
@@ -115,6 +125,10 @@ constexpr int kPrefetchAhead = 2;  // raw tiles are prefetched into L2 this many
 constexpr int kAbortTimeout = 1;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemS = 256;  // S buffers at columns 256 and 320; O^T chunks at 0,64,128,192
+// Column blocks 0-7 of the stacked split (BMM1's A operand): 128 lanes (stacked rows) x 512
+// codes, four per 32-bit column, at columns 384-511.  (The rope block, 8, stays in shared
+// memory: with two S buffers and O^T there is no room for it.)
+constexpr uint32_t kTmemQ = 384;
 // The running max (log2 domain) moves once a tile's max exceeds it by more than this, and
 // P is formed times 2^kPShift: P 2^kPShift <= 2^(threshold + shift) = 256 < 448 (e4m3 max),
 // and e4m3's subnormal floor (2^-9) sits 2^-15 below a P of 1.
@@ -222,12 +236,14 @@ decode_partial_e4m3_kernel(const __grid_constant__ CUtensorMap tm_q, const __gri
       mbar_init(&ctrl->s_full[s], 1);
       mbar_init(&ctrl->s_free[s], kSoftmaxThreads);
     }
-    mbar_init(&ctrl->p_full, kSoftmaxThreads);
-    mbar_init(&ctrl->o_done, 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&ctrl->p_full[s], kSoftmaxThreads);
+      mbar_init(&ctrl->o_done[s], 1);
+    }
     mbar_init(&ctrl->mma_drain, 1);
     mbar_init(&ctrl->mma_drain2, 1);
     ctrl->abort_flag = 0;
-    for (int w = 0; w < kSoftmaxWarps; ++w) ctrl->rescale_flag[w] = 0;
+    for (int w = 0; w < kSoftmaxWarps; ++w) ctrl->rescale_flag[0][w] = ctrl->rescale_flag[1][w] = 0;
     fence_mbarrier_init();
   }
   if (warp == kBmm1Warp) {
@@ -325,7 +341,7 @@ decode_partial_e4m3_kernel(const __grid_constant__ CUtensorMap tm_q, const __gri
         bad_pid |= outside;
         pids[pp] = outside ? -1 : pids[pp];
       }
-      if (s >= 2 && !q_waited) {  // stages 2-3 hold the bf16 Q tile until it has been split
+      if (s >= 1 && !q_waited) {  // stages 1-2 hold the bf16 Q tile until it has been split
         bool w = true;
         if (lane == 0) w = mbar_wait(&ctrl->q_ready, 0, abort_flag);
         ok = __shfl_sync(0xffffffffu, w, 0);
@@ -365,7 +381,7 @@ decode_partial_e4m3_kernel(const __grid_constant__ CUtensorMap tm_q, const __gri
     // ------------------------------------------------------------------ BMM1 issuer (whole warp,
     // uniform control flow; one elected thread issues the MMAs and their commits)
     const uint32_t idesc1 = make_idesc_e4m3(128, 64);
-    const uint64_t q_desc = make_smem_desc_sw64(smem_u32(smem + kOffQ8));
+    const uint64_t qr_desc = make_smem_desc_sw64(smem_u32(smem + kOffQR));
     bool ok = mbar_wait(&ctrl->q_ready, 0, abort_flag);
     // BMM1(j) as soon as raw tile j has landed and its S buffer is free
     for (int j = 0; j < ntiles; ++j) {
@@ -377,14 +393,19 @@ decode_partial_e4m3_kernel(const __grid_constant__ CUtensorMap tm_q, const __gri
       const uint64_t k_desc = make_smem_desc_sw64(smem_u32(smem + kOffRaw + s * kRawTile));
       const uint32_t d = tmem + kTmemS + sb * 64;
       if (elect_one()) {
-        // S_hi / S_lo (stacked rows) = [q_hi; q_lo] . k: 9 blocks x 2 K-steps of 32 codes
+        // S_hi / S_lo (stacked rows) = [q_hi; q_lo] . k: 9 blocks x 2 K-steps of 32 codes,
+        // A from TMEM for blocks 0-7 (8 columns per K-step), from shared memory for block 8
 #pragma unroll
-        for (int c = 0; c < kBlocks; ++c) {
+        for (int c = 0; c < kBlocks - 1; ++c) {
 #pragma unroll
           for (int k = 0; k < 2; ++k)
-            umma_f8(d, q_desc + static_cast<uint64_t>((c * kQ8Block + k * 32) >> 4),
-                      k_desc + static_cast<uint64_t>((c * kRawBlock + k * 32) >> 4), idesc1, (c | k) != 0 ? 1u : 0u);
+            umma_f8_ts(d, tmem + kTmemQ + c * 16 + k * 8, k_desc + static_cast<uint64_t>((c * kRawBlock + k * 32) >> 4),
+                       idesc1, (c | k) != 0 ? 1u : 0u);
         }
+#pragma unroll
+        for (int k = 0; k < 2; ++k)
+          umma_f8(d, qr_desc + static_cast<uint64_t>((k * 32) >> 4),
+                  k_desc + static_cast<uint64_t>(((kBlocks - 1) * kRawBlock + k * 32) >> 4), idesc1, 1u);
         umma_commit(&ctrl->s_full[sb]);
         umma_commit(&ctrl->raw_empty[s]);
       }
@@ -403,16 +424,16 @@ decode_partial_e4m3_kernel(const __grid_constant__ CUtensorMap tm_q, const __gri
     // (e4m3) then p_lo (e5m2), K-major rows of 64 keys.
     const uint32_t idesc2_hi = make_idesc_f8(128, nq, kF8E4M3, kF8E4M3, true, false);
     const uint32_t idesc2_lo = make_idesc_f8(128, nq, kF8E4M3, kF8E5M2, true, false);
-    const uint64_t phi_desc = make_smem_desc_sw64(smem_u32(smem + kOffP));
-    const uint64_t plo_desc = make_smem_desc_sw64(smem_u32(smem + kOffP + kPPart));
     bool ok = true;
     for (int j = 0; j < ntiles; ++j) {
-      const int s = j % kStages;
-      if (ok) ok = mbar_wait(&ctrl->p_full, j & 1, abort_flag);
+      const int s = j % kStages, pb = j & 1;
+      if (ok) ok = mbar_wait(&ctrl->p_full[pb], (j >> 1) & 1, abort_flag);
       if (ok) ok = mbar_wait(&ctrl->raw_full[s], (j / kStages) & 1, abort_flag);
       if (!__all_sync(0xffffffffu, ok)) break;
       tc_fence_after();
       const uint64_t v_desc = make_smem_desc_sw64(smem_u32(smem + kOffRaw + s * kRawTile), kRawBlock, 512);
+      const uint64_t phi_desc = make_smem_desc_sw64(smem_u32(smem + kOffP + pb * kPBuf));
+      const uint64_t plo_desc = make_smem_desc_sw64(smem_u32(smem + kOffP + pb * kPBuf + kPPart));
       if (elect_one()) {
 #pragma unroll
         for (int qc = 0; qc < 4; ++qc) {
@@ -424,7 +445,7 @@ decode_partial_e4m3_kernel(const __grid_constant__ CUtensorMap tm_q, const __gri
             umma_f8(tmem + qc * 64, v_desc + voff, plo_desc + poff, idesc2_lo, 1u);
           }
         }
-        umma_commit(&ctrl->o_done);
+        umma_commit(&ctrl->o_done[pb]);
         umma_commit(&ctrl->raw_empty[s]);
       }
       __syncwarp();
@@ -436,13 +457,18 @@ decode_partial_e4m3_kernel(const __grid_constant__ CUtensorMap tm_q, const __gri
     __syncwarp();
   } else if (warp < kSoftmaxWarps) {
     // ------------------------------------------------------------------ softmax + epilogue (warps 0-7)
-    // Q split first: row r is taken by threads 4r .. 4r+3; thread h of them takes bf16
-    // chunks 2h, 2h+1 of every 64-column block (e4m3 chunk h).  q_hi of row r goes to stacked
-    // row 32 (r / 16) + r % 16, q_lo 16 rows further.
+    // Q split, in two passes over the bf16 tile (ring stages 1-2).  First, row r's largest
+    // |q| (threads 4r .. 4r+3, each over bf16 chunks 2h, 2h+1 of every 64-column block) sets
+    // its power-of-two scale, and the same threads write the rope block's q_hi / q_lo
+    // (e4m3 chunk h) to shared memory: q_hi of row r as stacked row 32 (r / 16) + r % 16,
+    // q_lo 16 rows further.  Then each thread writes one stacked row's codes of four column
+    // blocks into TMEM (its lane quadrant's lane = the stacked row; blocks 4kh .. 4kh+3):
+    // lanes i < 16 the q_hi of row 16 quad + i, lanes i >= 16 the q_lo.
     bool failed = bar_or(1, kSoftmaxThreads, !mbar_wait(&ctrl->q_full, 0, abort_flag));
+    const uint32_t qb0 = smem_u32(smem + kOffQBf16);
     if (!failed) {
       const int r = threadIdx.x >> 2, h = threadIdx.x & 3;
-      const uint32_t qb = smem_u32(smem + kOffQBf16) + r * 128;
+      const uint32_t qb = qb0 + r * 128;
       float mx = 0.f;
       for (int c = 0; c < kBlocks; ++c) {
 #pragma unroll
@@ -461,39 +487,79 @@ decode_partial_e4m3_kernel(const __grid_constant__ CUtensorMap tm_q, const __gri
       int sh = 0;  // the row's power-of-two scale: its largest |q| lands in [128, 256)
       if (mx > 0.f) sh = min(126, max(-120, 7 - (static_cast<int>((__float_as_uint(mx) >> 23) & 0xFFu) - 127)));
       const float mult = __uint_as_float(static_cast<uint32_t>(sh + 127) << 23);
-      if (h == 0) ctrl->q_unscale[r] = __uint_as_float(static_cast<uint32_t>(127 - sh) << 23);
+      if (h == 0) {
+        ctrl->q_unscale[r] = __uint_as_float(static_cast<uint32_t>(127 - sh) << 23);
+        ctrl->q_mult[r] = mult;
+      }
       const int m_hi = 32 * (r >> 4) + (r & 15);  // stacked row of q_hi (q_lo: m_hi + 16)
-      const uint32_t qhi = smem_u32(smem + kOffQ8) + m_hi * 64;
+      const uint32_t qhi = smem_u32(smem + kOffQR) + m_hi * 64;
       const uint32_t qlo = qhi + 16 * 64;
       const uint32_t e_off = (h ^ ((m_hi >> 1) & 3)) << 4;  // chunk h under both rows' 64-byte swizzle
-      for (int c = 0; c < kBlocks; ++c) {
-        uint32_t w[8];
-        asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                     : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
-                     : "r"(qb + c * kF16Block + (((2 * h) ^ (r & 7)) << 4)));
-        asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                     : "=r"(w[4]), "=r"(w[5]), "=r"(w[6]), "=r"(w[7])
-                     : "r"(qb + c * kF16Block + (((2 * h + 1) ^ (r & 7)) << 4)));
-        uint32_t hi4[4], lo4[4];
+      constexpr int c = kBlocks - 1;  // the rope block
+      uint32_t w[8];
+      asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                   : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
+                   : "r"(qb + c * kF16Block + (((2 * h) ^ (r & 7)) << 4)));
+      asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                   : "=r"(w[4]), "=r"(w[5]), "=r"(w[6]), "=r"(w[7])
+                   : "r"(qb + c * kF16Block + (((2 * h + 1) ^ (r & 7)) << 4)));
+      uint32_t hi4[4], lo4[4];
 #pragma unroll
-        for (int i = 0; i < 8; i += 2) {
-          // four values: w[i] = (x0, x1), w[i+1] = (x2, x3), bf16 pairs low half first
-          const float x0 = __uint_as_float(w[i] << 16) * mult, x1 = __uint_as_float(w[i] & 0xFFFF0000u) * mult;
-          const float x2 = __uint_as_float(w[i + 1] << 16) * mult;
-          const float x3 = __uint_as_float(w[i + 1] & 0xFFFF0000u) * mult;
-          const uint32_t h01 = f32x2_to_e4m3x2(x0, x1), h23 = f32x2_to_e4m3x2(x2, x3);
-          const float2 v01 = e4m3x2_to_f32x2(h01), v23 = e4m3x2_to_f32x2(h23);
-          const uint32_t l01 = f32x2_to_e4m3x2(x0 - v01.x, x1 - v01.y);
-          const uint32_t l23 = f32x2_to_e4m3x2(x2 - v23.x, x3 - v23.y);
-          hi4[i >> 1] = h01 | (h23 << 16);
-          lo4[i >> 1] = l01 | (l23 << 16);
-        }
-        st_shared_v4(qhi + c * kQ8Block + e_off, hi4[0], hi4[1], hi4[2], hi4[3]);
-        st_shared_v4(qlo + c * kQ8Block + e_off, lo4[0], lo4[1], lo4[2], lo4[3]);
+      for (int i = 0; i < 8; i += 2) {
+        // four values: w[i] = (x0, x1), w[i+1] = (x2, x3), bf16 pairs low half first
+        const float x0 = __uint_as_float(w[i] << 16) * mult, x1 = __uint_as_float(w[i] & 0xFFFF0000u) * mult;
+        const float x2 = __uint_as_float(w[i + 1] << 16) * mult;
+        const float x3 = __uint_as_float(w[i + 1] & 0xFFFF0000u) * mult;
+        const uint32_t h01 = f32x2_to_e4m3x2(x0, x1), h23 = f32x2_to_e4m3x2(x2, x3);
+        const float2 v01 = e4m3x2_to_f32x2(h01), v23 = e4m3x2_to_f32x2(h23);
+        const uint32_t l01 = f32x2_to_e4m3x2(x0 - v01.x, x1 - v01.y);
+        const uint32_t l23 = f32x2_to_e4m3x2(x2 - v23.x, x3 - v23.y);
+        hi4[i >> 1] = h01 | (h23 << 16);
+        lo4[i >> 1] = l01 | (l23 << 16);
       }
+      st_shared_v4(qhi + e_off, hi4[0], hi4[1], hi4[2], hi4[3]);
+      st_shared_v4(qlo + e_off, lo4[0], lo4[1], lo4[2], lo4[3]);
       fence_proxy_async_smem();
     }
-    // every softmax thread has read the bf16 Q tile (ring stages 2-3) and written its split
+    named_bar_sync(1, kSoftmaxThreads);  // the rows' scales are written
+    if (!failed) {
+      const int quad_q = warp & 3, kh_q = warp >> 2;
+      const bool lo_part = (lane >> 4) != 0;
+      const int r = quad_q * 16 + (lane & 15);
+      const float mult = ctrl->q_mult[r];
+      const uint32_t qb = qb0 + r * 128;
+      const uint32_t lane_q = static_cast<uint32_t>(quad_q * 32) << 16;
+#pragma unroll 1
+      for (int cb = 0; cb < 4; ++cb) {
+        const int c = 4 * kh_q + cb;
+        uint32_t codes[16];  // 64 codes of block c, four per word, column order
+#pragma unroll
+        for (int ch = 0; ch < 8; ++ch) {  // bf16 chunk ch = columns 8ch .. 8ch+7
+          uint32_t w[4];
+          asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                       : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
+                       : "r"(qb + c * kF16Block + ((ch ^ (r & 7)) << 4)));
+#pragma unroll
+          for (int i = 0; i < 4; i += 2) {
+            const float x0 = __uint_as_float(w[i] << 16) * mult, x1 = __uint_as_float(w[i] & 0xFFFF0000u) * mult;
+            const float x2 = __uint_as_float(w[i + 1] << 16) * mult;
+            const float x3 = __uint_as_float(w[i + 1] & 0xFFFF0000u) * mult;
+            uint32_t c01 = f32x2_to_e4m3x2(x0, x1), c23 = f32x2_to_e4m3x2(x2, x3);
+            if (lo_part) {
+              const float2 v01 = e4m3x2_to_f32x2(c01), v23 = e4m3x2_to_f32x2(c23);
+              c01 = f32x2_to_e4m3x2(x0 - v01.x, x1 - v01.y);
+              c23 = f32x2_to_e4m3x2(x2 - v23.x, x3 - v23.y);
+            }
+            codes[2 * ch + (i >> 1)] = c01 | (c23 << 16);
+          }
+        }
+        tmem_st16(tmem + lane_q + kTmemQ + c * 16, codes);
+      }
+      tmem_st_wait();
+    }
+    // every softmax thread has read its part of the bf16 tile (ring stages 1-2) and written
+    // its part of the split
+    tc_fence_before();
     named_bar_sync(1, kSoftmaxThreads);
     if (!failed) mbar_arrive(&ctrl->q_ready);
 
@@ -521,7 +587,7 @@ decode_partial_e4m3_kernel(const __grid_constant__ CUtensorMap tm_q, const __gri
     const uint32_t p_addr = smem_u32(smem + kOffP) + r * 64 + (((2 * kh + half) ^ ((r >> 1) & 3)) << 4);
 
     for (int j = 0; !failed && j < ntiles; ++j) {
-      const int sb = j & 1;
+      const int sb = j & 1, pb = j & 1;
       const int s = j % kStages;
       const int k0 = kv_start + j * kTileKeys;
       bool fail = !mbar_wait(&ctrl->s_full[sb], (j >> 1) & 1, abort_flag);
@@ -576,16 +642,16 @@ decode_partial_e4m3_kernel(const __grid_constant__ CUtensorMap tm_q, const __gri
         else
           p_split16<false>(x, lim, scale_log2, off, l_sum, l_use, phi, plo);
       }
-      if (!fail && j >= 1) {
-        fail = !mbar_wait(&ctrl->o_done, (j - 1) & 1, abort_flag);
+      if (!fail && j >= 2) {  // the P buffer is free once BMM2 of tile j-2 has completed
+        fail = !mbar_wait(&ctrl->o_done[pb], ((j - 2) >> 1) & 1, abort_flag);
         fail = __any_sync(0xffffffffu, fail);
       }
       if (!fail) {
-        st_shared_v4(p_addr, phi[0], phi[1], phi[2], phi[3]);
-        st_shared_v4(p_addr + kPPart, plo[0], plo[1], plo[2], plo[3]);
-        if (kh == 0 && half == 0) ctrl->alpha[r] = alpha;
+        st_shared_v4(p_addr + pb * kPBuf, phi[0], phi[1], phi[2], phi[3]);
+        st_shared_v4(p_addr + pb * kPBuf + kPPart, plo[0], plo[1], plo[2], plo[3]);
+        if (kh == 0 && half == 0) ctrl->alpha[pb][r] = alpha;
         const bool any = __any_sync(0xffffffffu, need_rescale);
-        if (lane == 0) ctrl->rescale_flag[warp] = any ? 1 : 0;
+        if (lane == 0) ctrl->rescale_flag[pb][warp] = any ? 1 : 0;
         // the request's last tile: rows past its end are zeroed in the V blocks (BMM1 of this
         // tile has completed; BMM2 reads them only after p_full)
         const int valid_rows = L - k0;
@@ -603,16 +669,19 @@ decode_partial_e4m3_kernel(const __grid_constant__ CUtensorMap tm_q, const __gri
         failed = true;
         break;
       }
-      const int4 f0 = *reinterpret_cast<const int4*>(&ctrl->rescale_flag[0]);
-      const int4 f1 = *reinterpret_cast<const int4*>(&ctrl->rescale_flag[4]);
+      const int4 f0 = *reinterpret_cast<const int4*>(&ctrl->rescale_flag[pb][0]);
+      const int4 f1 = *reinterpret_cast<const int4*>(&ctrl->rescale_flag[pb][4]);
       if (f0.x | f0.y | f0.z | f0.w | f1.x | f1.y | f1.z | f1.w) {
-        // O^T[dim, row] *= alpha[row] for all 512 value columns; this thread owns TMEM lane
-        // (32 quad + lane) of each 128-column chunk, rows 32kh .. 32kh+31.
+        // O^T[dim, row] *= alpha[row] for all 512 value columns, once BMM2 of tile j-1 has
+        // completed; this thread owns TMEM lane (32 quad + lane) of each 128-column chunk,
+        // rows 32kh .. 32kh+31.  (A wait that gives up raises the abort flag, which the next
+        // closing barrier reports.)
+        if (j >= 1) mbar_wait(&ctrl->o_done[pb ^ 1], ((j - 1) >> 1) & 1, abort_flag);
         tc_fence_after();
         float al[32];
 #pragma unroll
         for (int i = 0; i < 32; i += 4) {
-          const float4 f = *reinterpret_cast<const float4*>(&ctrl->alpha[kh * 32 + i]);
+          const float4 f = *reinterpret_cast<const float4*>(&ctrl->alpha[pb][kh * 32 + i]);
           al[i] = f.x;
           al[i + 1] = f.y;
           al[i + 2] = f.z;
@@ -631,10 +700,10 @@ decode_partial_e4m3_kernel(const __grid_constant__ CUtensorMap tm_q, const __gri
         tmem_st_wait();
       }
       tc_fence_before();
-      mbar_arrive(&ctrl->p_full);
+      mbar_arrive(&ctrl->p_full[pb]);
     }
 
-    if (!failed) failed = !mbar_wait(&ctrl->o_done, (ntiles - 1) & 1, abort_flag);
+    if (!failed) failed = !mbar_wait(&ctrl->o_done[(ntiles - 1) & 1], ((ntiles - 1) >> 1) & 1, abort_flag);
     // this thread's partial row sums -> its warp's half of the row -> shared with the other half
     l_sum += __shfl_xor_sync(0xffffffffu, l_sum, 16);
     l_use += __shfl_xor_sync(0xffffffffu, l_use, 16);

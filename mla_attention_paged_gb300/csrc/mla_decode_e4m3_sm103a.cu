@@ -20,10 +20,11 @@
 //    for every element within 2^9 of the row's largest |q|; smaller elements fall under
 //    e4m3's subnormal floor (2^-9 at that scale) and carry an absolute error of at most
 //    2^-17 of the row's largest |q|.
-//  * BMM1 (M = 128, N = 64 keys, K = 576): the A operand stacks q_hi and q_lo, 16 rows of
-//    each in turn, so that row r's hi and lo partial scores land in TMEM lanes i and i + 16
-//    of the same warp (i = 32 (r / 16) + r % 16), and one shuffle between the two lanes
-//    adds them.  One pass of full-rate MMAs reads the K tile once.  The split's column
+//  * BMM1 (M = 128, N = 64 keys, K = 576): the A operand stacks q_hi and q_lo, 8 rows of
+//    each in turn, so that row r's hi and lo partial scores land in TMEM lanes i and i + 8
+//    (i = 16 (r / 8) + r % 8).  The 16x256b load shape hands both lanes' values for the
+//    same columns to one thread, which adds them.  One pass of full-rate MMAs reads the K
+//    tile once.  The split's column
 //    blocks 0-7 sit in TMEM (the A operand from tensor memory: stacked row = lane, four
 //    codes per 32-bit column), the rope block 8 in shared memory; the stacked Q is then not
 //    re-read from shared memory on every tile.
@@ -51,8 +52,9 @@
 //    split from there before their first load; the epilogue stages the bf16 output in
 //    stages 0-1.
 //  * Softmax and epilogue: eight warps, two per TMEM lane quadrant, so that two warps share
-//    each scheduler (one alone left most of its cycles to latency).  Each row's 64 keys are
-//    spread over four threads (16 each); P is formed and split in f16x2 arithmetic; lazy
+//    each scheduler (one alone left most of its cycles to latency).  Each warp owns 8 whole
+//    rows; a row's 64 keys are spread over four adjacent threads (16 each), which combine
+//    their maxima and sums by shuffles.  P is formed and split in f16x2 arithmetic; lazy
 //    rescale; bf16 output or split partial for the combine kernel (a programmatic
 //    dependent launch).
 // Every wait is bounded; on expiry the CTA records a timeout in the status word, drains
@@ -83,7 +85,7 @@ constexpr int kOffOStage = kOffRaw;                // [64][512] bf16 output stag
 static_assert(kQBf16Bytes == 2 * kRawTile, "bf16 Q staging spans ring stages 1-2 exactly");
 static_assert(kGroupRows * kValueDim * 2 <= 2 * kRawTile, "output staging fits ring stages 0-1");
 
-constexpr int kSoftmaxWarps = 8;  // two per TMEM lane quadrant, one per half of the key tile
+constexpr int kSoftmaxWarps = 8;  // two per TMEM lane quadrant, 8 rows each
 constexpr int kSoftmaxThreads = 32 * kSoftmaxWarps;
 constexpr int kProducerWarp = kSoftmaxWarps;
 constexpr int kBmm1Warp = kSoftmaxWarps + 1;
@@ -110,9 +112,6 @@ struct Ctrl {
   alignas(16) int rescale_flag[2][kSoftmaxWarps];
   alignas(16) float alpha[2][kGroupRows];
   alignas(16) float q_mult[kGroupRows];     // 2^s of each row's Q split
-  // [0][half of the key tile][row]: partial row maxima of a tile, swapped between the two
-  // warps of a lane quadrant; at the end [0] and [1] hold the halves' row sums l / l_use
-  float red[2][2][kGroupRows];
   alignas(16) float row_scale[kGroupRows];
   alignas(16) float q_unscale[kGroupRows];  // 2^-s of each row's Q split
 };
@@ -173,38 +172,32 @@ __device__ __forceinline__ uint32_t e5m2x2_to_f16x2(uint32_t codes) {
   return h2;
 }
 
-// P 2^kPShift for this thread's 16 keys of its row (keys i <= lim visible; kAll: all of
-// them), split into e4m3 hi and e5m2 lo codes (4 per word, key order) through f16: the f16
+// P 2^kPShift for this thread's 16 keys of its row, eight pairs: x[2i], x[2i+1] are the
+// keys 8i and 8i + 1 past the thread's first key (visible while <= lim; kAll: all of them).
+// Each pair is split into two e4m3 hi and two e5m2 lo codes (low byte first) through f16: the f16
 // value keeps 11 bits, and hi, the residual (exact in f16: hi is within a factor of 2 of
 // the value, or zero) and lo are formed there.  l_sum accumulates the fp32 P 2^kPShift (for
 // the LSE), l_use the hi + lo values the MMAs take (for the output's normalisation, so that
 // the split's rounding of a dominant key cancels in O / l).
 template <bool kAll>
 __device__ __forceinline__ void p_split16(const float (&x)[16], int lim, float scale_log2, float off, float& l_sum,
-                                          float& l_use, uint32_t (&phi)[4], uint32_t (&plo)[4]) {
+                                          float& l_use, uint32_t (&phi)[8], uint32_t (&plo)[8]) {
   float ls = 0.f, lu = 0.f;
 #pragma unroll
-  for (int i = 0; i < 16; i += 4) {
-    uint32_t h8[2], l8[2];
-#pragma unroll
-    for (int u = 0; u < 2; ++u) {
-      const int k = i + 2 * u;
-      const float p0 = (kAll || k <= lim) ? ex2_approx(fmaf(x[k], scale_log2, off)) : 0.f;
-      const float p1 = (kAll || k + 1 <= lim) ? ex2_approx(fmaf(x[k + 1], scale_log2, off)) : 0.f;
-      ls += p0 + p1;
-      const uint32_t ph = pack_f16x2(p0, p1);
-      h8[u] = f16x2_to_e4m3x2(ph);
-      const uint32_t hb = e4m3x2_to_f16x2(h8[u]);
-      uint32_t d, sum;
-      asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(ph), "r"(hb));
-      l8[u] = f16x2_to_e5m2x2(d);
-      const uint32_t lb = e5m2x2_to_f16x2(l8[u]);
-      asm("add.rn.f16x2 %0, %1, %2;" : "=r"(sum) : "r"(hb), "r"(lb));
-      const float2 uf = __half22float2(*reinterpret_cast<const __half2*>(&sum));
-      lu += uf.x + uf.y;
-    }
-    phi[i >> 2] = h8[0] | (h8[1] << 16);
-    plo[i >> 2] = l8[0] | (l8[1] << 16);
+  for (int i = 0; i < 8; ++i) {
+    const float p0 = (kAll || 8 * i <= lim) ? ex2_approx(fmaf(x[2 * i], scale_log2, off)) : 0.f;
+    const float p1 = (kAll || 8 * i + 1 <= lim) ? ex2_approx(fmaf(x[2 * i + 1], scale_log2, off)) : 0.f;
+    ls += p0 + p1;
+    const uint32_t ph = pack_f16x2(p0, p1);
+    phi[i] = f16x2_to_e4m3x2(ph);
+    const uint32_t hb = e4m3x2_to_f16x2(phi[i]);
+    uint32_t d, sum;
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(ph), "r"(hb));
+    plo[i] = f16x2_to_e5m2x2(d);
+    const uint32_t lb = e5m2x2_to_f16x2(plo[i]);
+    asm("add.rn.f16x2 %0, %1, %2;" : "=r"(sum) : "r"(hb), "r"(lb));
+    const float2 uf = __half22float2(*reinterpret_cast<const __half2*>(&sum));
+    lu += uf.x + uf.y;
   }
   l_sum += ls;
   l_use += lu;
@@ -460,10 +453,10 @@ decode_partial_e4m3_kernel(const __grid_constant__ CUtensorMap tm_q, const __gri
     // Q split, in two passes over the bf16 tile (ring stages 1-2).  First, row r's largest
     // |q| (threads 4r .. 4r+3, each over bf16 chunks 2h, 2h+1 of every 64-column block) sets
     // its power-of-two scale, and the same threads write the rope block's q_hi / q_lo
-    // (e4m3 chunk h) to shared memory: q_hi of row r as stacked row 32 (r / 16) + r % 16,
-    // q_lo 16 rows further.  Then each thread writes one stacked row's codes of four column
+    // (e4m3 chunk h) to shared memory: q_hi of row r as stacked row 16 (r / 8) + r % 8,
+    // q_lo 8 rows further.  Then each thread writes one stacked row's codes of four column
     // blocks into TMEM (its lane quadrant's lane = the stacked row; blocks 4kh .. 4kh+3):
-    // lanes i < 16 the q_hi of row 16 quad + i, lanes i >= 16 the q_lo.
+    // lane i holds row 16 quad + 8 (i / 16) + i % 8, its q_hi for i % 16 < 8, else its q_lo.
     bool failed = bar_or(1, kSoftmaxThreads, !mbar_wait(&ctrl->q_full, 0, abort_flag));
     const uint32_t qb0 = smem_u32(smem + kOffQBf16);
     if (!failed) {
@@ -491,9 +484,9 @@ decode_partial_e4m3_kernel(const __grid_constant__ CUtensorMap tm_q, const __gri
         ctrl->q_unscale[r] = __uint_as_float(static_cast<uint32_t>(127 - sh) << 23);
         ctrl->q_mult[r] = mult;
       }
-      const int m_hi = 32 * (r >> 4) + (r & 15);  // stacked row of q_hi (q_lo: m_hi + 16)
+      const int m_hi = 16 * (r >> 3) + (r & 7);  // stacked row of q_hi (q_lo: m_hi + 8)
       const uint32_t qhi = smem_u32(smem + kOffQR) + m_hi * 64;
-      const uint32_t qlo = qhi + 16 * 64;
+      const uint32_t qlo = qhi + 8 * 64;
       const uint32_t e_off = (h ^ ((m_hi >> 1) & 3)) << 4;  // chunk h under both rows' 64-byte swizzle
       constexpr int c = kBlocks - 1;  // the rope block
       uint32_t w[8];
@@ -524,8 +517,8 @@ decode_partial_e4m3_kernel(const __grid_constant__ CUtensorMap tm_q, const __gri
     named_bar_sync(1, kSoftmaxThreads);  // the rows' scales are written
     if (!failed) {
       const int quad_q = warp & 3, kh_q = warp >> 2;
-      const bool lo_part = (lane >> 4) != 0;
-      const int r = quad_q * 16 + (lane & 15);
+      const bool lo_part = ((lane >> 3) & 1) != 0;
+      const int r = quad_q * 16 + 8 * (lane >> 4) + (lane & 7);
       const float mult = ctrl->q_mult[r];
       const uint32_t qb = qb0 + r * 128;
       const uint32_t lane_q = static_cast<uint32_t>(quad_q * 32) << 16;
@@ -563,28 +556,29 @@ decode_partial_e4m3_kernel(const __grid_constant__ CUtensorMap tm_q, const __gri
     named_bar_sync(1, kSoftmaxThreads);
     if (!failed) mbar_arrive(&ctrl->q_ready);
 
-    // BMM1 (M = 128) puts row r's hi / lo partial scores in TMEM lanes 32*(r/16) + r%16 and
-    // 16 further: warps w and w+4 serve lane quadrant w%4 (rows 16(w%4) .. +15), warp w the
-    // tile's keys 0-31 and warp w+4 keys 32-63.  Lanes i and i+16 hold the hi and lo parts
-    // of one row; after a shuffle lane i keeps the sum for the first 16 of its warp's keys,
-    // lane i+16 for the last 16.  The two warps of a quadrant swap their partial row maxima
-    // through shared memory (a 64-thread named barrier per quadrant).
+    // BMM1 (M = 128) puts row r's hi / lo partial scores in TMEM lanes 16 (r / 8) + r % 8 and
+    // 8 further.  Warp w (quad = w % 4, kh = w / 4) reads lanes 32 quad + 16 kh .. +15 with
+    // the 16x256b shape: rows 16 quad + 8 kh .. +7, each row's hi and lo partial in the same
+    // thread.  Thread 4g + c holds row 16 quad + 8 kh + g, keys 8i + 2c and 8i + 2c + 1
+    // (i < 8) of every tile; the row's four threads combine their maxima by two shuffles.
     const int quad = warp & 3, kh = warp >> 2;
-    const int half = lane >> 4;
-    const int r = quad * 16 + (lane & 15);
+    const int cq = lane & 3;
+    const int r = quad * 16 + kh * 8 + (lane >> 2);
     const bool row_active = r < nrows;
     const int t = (row0 + r) / p.H;
     const int lim_abs = L - p.T + t;  // last visible key of this row
     const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
-    const int pair_bar = 2 + quad;
-    const int kb = 32 * kh + 16 * half;  // this thread's first key of every tile
+    const uint32_t s_lane = static_cast<uint32_t>(quad * 32 + kh * 16) << 16;
     float m_used = -INFINITY;
     float l_sum = 0.f, l_use = 0.f;
     // S holds (q 2^s) . k_code: the row's 2^-s and kv_scale (in p.scale_log2) return here;
     // P carries 2^kPShift, which cancels in O / l and returns in the LSE.
     const float scale_log2 = failed ? 0.f : p.scale_log2 * ctrl->q_unscale[r];
     const float v_scale = p.v_scale;
-    const uint32_t p_addr = smem_u32(smem + kOffP) + r * 64 + (((2 * kh + half) ^ ((r >> 1) & 3)) << 4);
+    // key pair i of this thread in a P buffer: row r (64 bytes), 16-byte chunk i / 2 under
+    // the 64-byte swizzle, bytes 8 (i % 2) + 2c, +1
+    const uint32_t p_row = smem_u32(smem + kOffP) + r * 64 + 2 * cq;
+    const uint32_t p_sw = (r >> 1) & 3;
 
     for (int j = 0; !failed && j < ntiles; ++j) {
       const int sb = j & 1, pb = j & 1;
@@ -594,39 +588,40 @@ decode_partial_e4m3_kernel(const __grid_constant__ CUtensorMap tm_q, const __gri
       fail = __any_sync(0xffffffffu, fail);
       float x[16];
       int lim = -1;
+      float mx = -INFINITY;
       if (!fail) {
         tc_fence_after();
         uint32_t v[32];
-        tmem_ld32(tmem + lane_base + kTmemS + sb * 64 + 32 * kh, v);
+        tmem_ld16x256b_x8(tmem + s_lane + kTmemS + sb * 64, v);
         tmem_ld_wait();
         tc_fence_before();
         mbar_arrive(&ctrl->s_free[sb]);
 #pragma unroll
-        for (int k = 0; k < 16; ++k) {
-          const uint32_t mine = half ? v[16 + k] : v[k];
-          const uint32_t other = __shfl_xor_sync(0xffffffffu, half ? v[k] : v[16 + k], 16);
-          x[k] = __uint_as_float(mine) + __uint_as_float(other);
+        for (int i = 0; i < 8; ++i) {
+          x[2 * i] = __uint_as_float(v[4 * i]) + __uint_as_float(v[4 * i + 2]);
+          x[2 * i + 1] = __uint_as_float(v[4 * i + 1]) + __uint_as_float(v[4 * i + 3]);
         }
-        lim = row_active ? (min(kv_end - 1, lim_abs) - k0 - kb) : -1;
-        float mx = -INFINITY;
-        if (lim >= 15) {
+        // the row's last visible key in this tile, counted from this thread's first key 2c
+        lim = row_active ? (min(kv_end - 1, lim_abs) - k0 - 2 * cq) : -1;
+        if (lim >= 57) {
 #pragma unroll
           for (int k = 0; k < 16; ++k) mx = fmaxf(mx, x[k]);
         } else {
 #pragma unroll
-          for (int k = 0; k < 16; ++k)
-            if (k <= lim) mx = fmaxf(mx, x[k]);
+          for (int i = 0; i < 8; ++i) {
+            if (8 * i <= lim) mx = fmaxf(mx, x[2 * i]);
+            if (8 * i + 1 <= lim) mx = fmaxf(mx, x[2 * i + 1]);
+          }
         }
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-        if (half == 0) ctrl->red[0][kh][r] = mx;
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
       }
-      named_bar_sync(pair_bar, 64);
-      uint32_t phi[4], plo[4];
+      uint32_t phi[8], plo[8];
       float alpha = 1.f;
       bool need_rescale = false;
       if (!fail) {
         // scale > 0: max commutes with the scaling; -inf stays -inf
-        const float mt = fmaxf(ctrl->red[0][0][r], ctrl->red[0][1][r]) * scale_log2;
+        const float mt = mx * scale_log2;
         if (m_used == -INFINITY) {
           m_used = mt;  // first contributing tile: nothing accumulated yet
         } else if (mt > m_used + kRescaleThreshold) {
@@ -637,7 +632,7 @@ decode_partial_e4m3_kernel(const __grid_constant__ CUtensorMap tm_q, const __gri
           m_used = mt;
         }
         const float off = (m_used == -INFINITY) ? 0.f : (kPShift - m_used);
-        if (lim >= 15)
+        if (lim >= 57)
           p_split16<true>(x, lim, scale_log2, off, l_sum, l_use, phi, plo);
         else
           p_split16<false>(x, lim, scale_log2, off, l_sum, l_use, phi, plo);
@@ -647,9 +642,13 @@ decode_partial_e4m3_kernel(const __grid_constant__ CUtensorMap tm_q, const __gri
         fail = __any_sync(0xffffffffu, fail);
       }
       if (!fail) {
-        st_shared_v4(p_addr + pb * kPBuf, phi[0], phi[1], phi[2], phi[3]);
-        st_shared_v4(p_addr + pb * kPBuf + kPPart, plo[0], plo[1], plo[2], plo[3]);
-        if (kh == 0 && half == 0) ctrl->alpha[pb][r] = alpha;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const uint32_t a = p_row + pb * kPBuf + ((((i >> 1) ^ p_sw) << 4) | ((i & 1) << 3));
+          st_shared_u16(a, phi[i]);
+          st_shared_u16(a + kPPart, plo[i]);
+        }
+        if (cq == 0) ctrl->alpha[pb][r] = alpha;
         const bool any = __any_sync(0xffffffffu, need_rescale);
         if (lane == 0) ctrl->rescale_flag[pb][warp] = any ? 1 : 0;
         // the request's last tile: rows past its end are zeroed in the V blocks (BMM1 of this
@@ -704,21 +703,19 @@ decode_partial_e4m3_kernel(const __grid_constant__ CUtensorMap tm_q, const __gri
     }
 
     if (!failed) failed = !mbar_wait(&ctrl->o_done[(ntiles - 1) & 1], ((ntiles - 1) >> 1) & 1, abort_flag);
-    // this thread's partial row sums -> its warp's half of the row -> shared with the other half
-    l_sum += __shfl_xor_sync(0xffffffffu, l_sum, 16);
-    l_use += __shfl_xor_sync(0xffffffffu, l_use, 16);
-    if (half == 0) {
-      ctrl->red[0][kh][r] = l_sum;
-      ctrl->red[1][kh][r] = l_use;
-    }
+    // the row's four threads' partial sums
+    l_sum += __shfl_xor_sync(0xffffffffu, l_sum, 1);
+    l_sum += __shfl_xor_sync(0xffffffffu, l_sum, 2);
+    l_use += __shfl_xor_sync(0xffffffffu, l_use, 1);
+    l_use += __shfl_xor_sync(0xffffffffu, l_use, 2);
     if (bar_or(1, kSoftmaxThreads, failed || (*abort_flag != 0))) {
       failed = true;
     } else {
       tc_fence_after();
       const bool final_out = (nsplit_b == 1);
-      if (kh == 0 && half == 0) {
-        const float ls = ctrl->red[0][0][r] + ctrl->red[0][1][r];
-        const float lu = ctrl->red[1][0][r] + ctrl->red[1][1][r];
+      if (cq == 0) {
+        const float ls = l_sum;
+        const float lu = l_use;
         const float lse2 = (ls > 0.f) ? (m_used + __log2f(ls) - kPShift) : -INFINITY;
         const float lse_nat = lse2 * 0.69314718055994530942f;
         ctrl->row_scale[r] = (lu > 0.f) ? (v_scale / lu) : 0.f;

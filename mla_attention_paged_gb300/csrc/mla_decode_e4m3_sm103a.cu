@@ -13,7 +13,8 @@
 // threads: softmax warps 0-7, producer warp 8, BMM1 warp 9, BMM2 warp 10).  Both GEMMs run on
 // the 8-bit codes as they arrive (kind::f8f6f4); nothing is decoded to a wider type:
 //  * The raw e4m3 tile (64 keys x 576 codes, 36 KB) arrives by TMA (64-byte swizzle) in a
-//    5-stage ring, its rows prefetched into L2 ahead of the load.
+//    5-stage ring.  (Five stages cover the load latency: an L2 prefetch ahead of the ring,
+//    which an earlier 4-stage ring needed, now only delayed the producer's loads.)
 //  * Q keeps its bf16 value: each query row, scaled by a power of two 2^s that brings its
 //    largest element into [128, 256), is split into q_hi = e4m3(q 2^s) and
 //    q_lo = e4m3(q 2^s - q_hi), an 8-bit significand in two 4-bit halves.  This is exact
@@ -120,7 +121,6 @@ constexpr int kSmemBytes = kOffCtrl + kCtrlBytes + 1024;  // + control block + a
 static_assert(sizeof(Ctrl) <= kCtrlBytes, "control block");
 static_assert(kSmemBytes <= 232448, "shared memory per block");
 
-constexpr int kPrefetchAhead = 2;  // raw tiles are prefetched into L2 this many tiles beyond the ring
 constexpr int kAbortTimeout = 1;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemS = 256;  // S buffers at columns 256 and 320; O^T chunks at 0,64,128,192
@@ -220,17 +220,17 @@ decode_partial_e4m3_kernel(const __grid_constant__ CUtensorMap tm_q, const __gri
   // programmatic dependent launch; griddepcontrol.wait below orders every input read).
   if (threadIdx.x == 0) {
     mbar_init(&ctrl->q_full, 1);
-    mbar_init(&ctrl->q_ready, kSoftmaxThreads);
+    mbar_init(&ctrl->q_ready, kSoftmaxWarps);
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&ctrl->raw_full[s], 1);
       mbar_init(&ctrl->raw_empty[s], 2);
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&ctrl->s_full[s], 1);
-      mbar_init(&ctrl->s_free[s], kSoftmaxThreads);
+      mbar_init(&ctrl->s_free[s], kSoftmaxWarps);
     }
     for (int s = 0; s < 2; ++s) {
-      mbar_init(&ctrl->p_full[s], kSoftmaxThreads);
+      mbar_init(&ctrl->p_full[s], kSoftmaxWarps);
       mbar_init(&ctrl->o_done[s], 1);
     }
     mbar_init(&ctrl->mma_drain, 1);
@@ -292,18 +292,6 @@ decode_partial_e4m3_kernel(const __grid_constant__ CUtensorMap tm_q, const __gri
       mbar_arrive_expect_tx(&ctrl->q_full, kQBf16Bytes);
       tma_load_3d(smem + kOffQBf16, &tm_q, &ctrl->q_full, 0, b * p.R + row0, 0, policy_evict_last());
     }
-    // L2 prefetch of tile jt's rows (lane l < pages per tile: the rows of its page in the
-    // tile), so that each TMA load, issued only once its ring stage frees up, finds them in L2.
-    auto prefetch_tile = [&](int jt) {
-      const int k = kv_start + jt * kTileKeys + lane * box_rows;
-      if (jt >= ntiles || lane >= sub || k >= kv_end) return;
-      const unsigned pid = static_cast<unsigned>(__ldg(pt + k / P));
-      if (pid >= n_pages) return;  // (reported when its TMA load is issued)
-      const int rows = min(box_rows, kv_end - k);
-      prefetch_l2_bulk(p.kv_pool + (static_cast<int64_t>(pid) * P + k % P) * kLatentDim,
-                       static_cast<uint32_t>(rows * kLatentDim));
-    };
-    for (int jt = kStages; jt < kStages + kPrefetchAhead; ++jt) prefetch_tile(jt);
     for (int j = 0; j < ntiles; ++j) {
       const int s = j % kStages;
       const int k0 = kv_start + j * kTileKeys;
@@ -361,7 +349,6 @@ decode_partial_e4m3_kernel(const __grid_constant__ CUtensorMap tm_q, const __gri
         }
       }
       last_issued[s] = j;
-      prefetch_tile(j + kStages + kPrefetchAhead);
       __syncwarp();
     }
     if (bad_pid && lane == 0) atomicOr(p.status, kStatusDeviceArg);
@@ -554,7 +541,8 @@ decode_partial_e4m3_kernel(const __grid_constant__ CUtensorMap tm_q, const __gri
     // its part of the split
     tc_fence_before();
     named_bar_sync(1, kSoftmaxThreads);
-    if (!failed) mbar_arrive(&ctrl->q_ready);
+    __syncwarp();
+    if (!failed && lane == 0) mbar_arrive(&ctrl->q_ready);
 
     // BMM1 (M = 128) puts row r's hi / lo partial scores in TMEM lanes 16 (r / 8) + r % 8 and
     // 8 further.  Warp w (quad = w % 4, kh = w / 4) reads lanes 32 quad + 16 kh .. +15 with
@@ -595,7 +583,8 @@ decode_partial_e4m3_kernel(const __grid_constant__ CUtensorMap tm_q, const __gri
         tmem_ld16x256b_x8(tmem + s_lane + kTmemS + sb * 64, v);
         tmem_ld_wait();
         tc_fence_before();
-        mbar_arrive(&ctrl->s_free[sb]);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ctrl->s_free[sb]);
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           x[2 * i] = __uint_as_float(v[4 * i]) + __uint_as_float(v[4 * i + 2]);
@@ -699,7 +688,8 @@ decode_partial_e4m3_kernel(const __grid_constant__ CUtensorMap tm_q, const __gri
         tmem_st_wait();
       }
       tc_fence_before();
-      mbar_arrive(&ctrl->p_full[pb]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ctrl->p_full[pb]);
     }
 
     if (!failed) failed = !mbar_wait(&ctrl->o_done[(ntiles - 1) & 1], ((ntiles - 1) >> 1) & 1, abort_flag);

@@ -53,11 +53,13 @@
 //    split from there before their first load; the epilogue stages the bf16 output in
 //    stages 0-1.
 //  * Softmax and epilogue: eight warps, two per TMEM lane quadrant, so that two warps share
-//    each scheduler (one alone left most of its cycles to latency).  Each warp owns 8 whole
-//    rows; a row's 64 keys are spread over four adjacent threads (16 each), which combine
-//    their maxima and sums by shuffles.  P is formed and split in f16x2 arithmetic; lazy
-//    rescale; bf16 output or split partial for the combine kernel (a programmatic
-//    dependent launch).
+//    each scheduler (one alone left most of its cycles to latency).  They ping-pong: the
+//    two warps of a quadrant take alternate tiles, each owning the quadrant's 16 rows; a
+//    row's 64 keys are spread over four adjacent threads (16 each), which combine their
+//    maxima by shuffles.  A tile's running max is handed to the other warp through a named
+//    barrier as soon as it is known, so each warp has two tile periods for its per-tile
+//    waits and hand-offs.  P is formed and split in f16x2 arithmetic; lazy rescale; bf16
+//    output or split partial for the combine kernel (a programmatic dependent launch).
 // Every wait is bounded; on expiry the CTA records a timeout in the status word, drains
 // its in-flight copies and MMAs, frees TMEM and returns.
 #include <cuda_fp16.h>
@@ -86,7 +88,7 @@ constexpr int kOffOStage = kOffRaw;                // [64][512] bf16 output stag
 static_assert(kQBf16Bytes == 2 * kRawTile, "bf16 Q staging spans ring stages 1-2 exactly");
 static_assert(kGroupRows * kValueDim * 2 <= 2 * kRawTile, "output staging fits ring stages 0-1");
 
-constexpr int kSoftmaxWarps = 8;  // two per TMEM lane quadrant, 8 rows each
+constexpr int kSoftmaxWarps = 8;  // two per TMEM lane quadrant, alternating tiles
 constexpr int kSoftmaxThreads = 32 * kSoftmaxWarps;
 constexpr int kProducerWarp = kSoftmaxWarps;
 constexpr int kBmm1Warp = kSoftmaxWarps + 1;
@@ -114,9 +116,15 @@ struct Ctrl {
   alignas(16) float alpha[2][kGroupRows];
   alignas(16) float q_mult[kGroupRows];     // 2^s of each row's Q split
   alignas(16) float row_scale[kGroupRows];
+  // ping-pong softmax: the running max each tile hands to the other parity's warps (by
+  // sender parity), a stop mark per (sender parity, quadrant), and each parity's final
+  // (reference max, row sum, row sum of the split values) per row
+  alignas(16) float tok_m[2][kGroupRows];
+  int tok_stop[2][4];
+  alignas(16) float fin[2][3][kGroupRows];
   alignas(16) float q_unscale[kGroupRows];  // 2^-s of each row's Q split
 };
-constexpr int kCtrlBytes = 3072;
+constexpr int kCtrlBytes = 4096;
 constexpr int kSmemBytes = kOffCtrl + kCtrlBytes + 1024;  // + control block + alignment slack
 static_assert(sizeof(Ctrl) <= kCtrlBytes, "control block");
 static_assert(kSmemBytes <= 232448, "shared memory per block");
@@ -227,16 +235,17 @@ decode_partial_e4m3_kernel(const __grid_constant__ CUtensorMap tm_q, const __gri
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&ctrl->s_full[s], 1);
-      mbar_init(&ctrl->s_free[s], kSoftmaxWarps);
+      mbar_init(&ctrl->s_free[s], kSoftmaxWarps / 2);
     }
     for (int s = 0; s < 2; ++s) {
-      mbar_init(&ctrl->p_full[s], kSoftmaxWarps);
+      mbar_init(&ctrl->p_full[s], kSoftmaxWarps / 2);
       mbar_init(&ctrl->o_done[s], 1);
     }
     mbar_init(&ctrl->mma_drain, 1);
     mbar_init(&ctrl->mma_drain2, 1);
     ctrl->abort_flag = 0;
     for (int w = 0; w < kSoftmaxWarps; ++w) ctrl->rescale_flag[0][w] = ctrl->rescale_flag[1][w] = 0;
+    for (int q = 0; q < 4; ++q) ctrl->tok_stop[0][q] = ctrl->tok_stop[1][q] = 0;
     fence_mbarrier_init();
   }
   if (warp == kBmm1Warp) {
@@ -545,86 +554,140 @@ decode_partial_e4m3_kernel(const __grid_constant__ CUtensorMap tm_q, const __gri
     if (!failed && lane == 0) mbar_arrive(&ctrl->q_ready);
 
     // BMM1 (M = 128) puts row r's hi / lo partial scores in TMEM lanes 16 (r / 8) + r % 8 and
-    // 8 further.  Warp w (quad = w % 4, kh = w / 4) reads lanes 32 quad + 16 kh .. +15 with
-    // the 16x256b shape: rows 16 quad + 8 kh .. +7, each row's hi and lo partial in the same
-    // thread.  Thread 4g + c holds row 16 quad + 8 kh + g, keys 8i + 2c and 8i + 2c + 1
-    // (i < 8) of every tile; the row's four threads combine their maxima by two shuffles.
-    const int quad = warp & 3, kh = warp >> 2;
+    // 8 further.  Warp w takes lane quadrant quad = w % 4, i.e. rows 16 quad .. +15, and the
+    // tiles of parity par = w / 4 (ping-pong: the two warps of a quadrant alternate tiles).
+    // Two 16x256b loads (lanes 32 quad .. +15 and 32 quad + 16 .. +31) give thread 4g + c
+    // rows 16 quad + g and 16 quad + 8 + g, each row's hi and lo partial in the same thread,
+    // keys 8i + 2c and 8i + 2c + 1 (i < 8) of its tiles; a row's four threads combine their
+    // maxima by two shuffles.  A tile's running max depends on the previous tile's, which the
+    // other parity's warp of the quadrant computed: it is handed over through shared memory
+    // and a named barrier (bar.arrive by the sender, bar.sync by the receiver) as soon as it
+    // is known, before either warp forms its P.  Each warp keeps its own row sums, relative
+    // to the reference max of its last tile; the two are combined after the loop.
+    const int quad = warp & 3, par = warp >> 2;
+    const int kh = par;  // (the epilogue's rows 32 kh .. +31)
     const int cq = lane & 3;
-    const int r = quad * 16 + kh * 8 + (lane >> 2);
-    const bool row_active = r < nrows;
-    const int t = (row0 + r) / p.H;
-    const int lim_abs = L - p.T + t;  // last visible key of this row
+    const int rr0 = quad * 16 + (lane >> 2);  // rows rr0 and rr0 + 8
     const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
-    const uint32_t s_lane = static_cast<uint32_t>(quad * 32 + kh * 16) << 16;
-    float m_used = -INFINITY;
-    float l_sum = 0.f, l_use = 0.f;
+    const float v_scale = p.v_scale;
+    int lim_abs[2];
+    bool row_active[2];
+    float scale_log2[2];
     // S holds (q 2^s) . k_code: the row's 2^-s and kv_scale (in p.scale_log2) return here;
     // P carries 2^kPShift, which cancels in O / l and returns in the LSE.
-    const float scale_log2 = failed ? 0.f : p.scale_log2 * ctrl->q_unscale[r];
-    const float v_scale = p.v_scale;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int r = rr0 + 8 * h;
+      row_active[h] = r < nrows;
+      lim_abs[h] = L - p.T + (row0 + r) / p.H;  // last visible key of the row
+      scale_log2[h] = failed ? 0.f : p.scale_log2 * ctrl->q_unscale[r];
+    }
+    float m_w[2] = {-INFINITY, -INFINITY};  // reference max of this warp's last tile
+    float l_sum[2] = {0.f, 0.f}, l_use[2] = {0.f, 0.f};
     // key pair i of this thread in a P buffer: row r (64 bytes), 16-byte chunk i / 2 under
     // the 64-byte swizzle, bytes 8 (i % 2) + 2c, +1
-    const uint32_t p_row = smem_u32(smem + kOffP) + r * 64 + 2 * cq;
-    const uint32_t p_sw = (r >> 1) & 3;
+    const uint32_t p_base = smem_u32(smem + kOffP) + 2 * cq;
+    const int bar_par = 2 + par;                   // the four warps of this parity (128 threads)
+    const int tok_in = 4 + 2 * quad + (par ^ 1);   // handed over by the other parity
+    const int tok_out = 4 + 2 * quad + par;        // handed over to it
+    // A parity whose closing barrier reports a failure drains: at its next tile it takes the
+    // other parity's hand-over and hands one back marked stop, then leaves; a warp that
+    // receives a stop mark leaves without handing over.  Every hand-over thus has a receiver.
+    bool draining = false;
 
-    for (int j = 0; !failed && j < ntiles; ++j) {
-      const int sb = j & 1, pb = j & 1;
+    for (int j = par; !failed && j < ntiles; j += 2) {
+      const int pb = j & 1;  // S buffer, P buffer and flags of this tile (= par)
       const int s = j % kStages;
       const int k0 = kv_start + j * kTileKeys;
-      bool fail = !mbar_wait(&ctrl->s_full[sb], (j >> 1) & 1, abort_flag);
-      fail = __any_sync(0xffffffffu, fail);
-      float x[16];
-      int lim = -1;
-      float mx = -INFINITY;
+      bool fail = draining;
+      float x[2][16];
+      int lim[2] = {-1, -1};
+      float mx[2] = {-INFINITY, -INFINITY};
+      if (!fail) fail = __any_sync(0xffffffffu, !mbar_wait(&ctrl->s_full[pb], (j >> 1) & 1, abort_flag));
       if (!fail) {
         tc_fence_after();
-        uint32_t v[32];
-        tmem_ld16x256b_x8(tmem + s_lane + kTmemS + sb * 64, v);
+        uint32_t v0[32], v1[32];
+        tmem_ld16x256b_x8(tmem + lane_base + kTmemS + pb * 64, v0);
+        tmem_ld16x256b_x8(tmem + lane_base + (16u << 16) + kTmemS + pb * 64, v1);
         tmem_ld_wait();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&ctrl->s_free[sb]);
+        if (lane == 0) mbar_arrive(&ctrl->s_free[pb]);
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-          x[2 * i] = __uint_as_float(v[4 * i]) + __uint_as_float(v[4 * i + 2]);
-          x[2 * i + 1] = __uint_as_float(v[4 * i + 1]) + __uint_as_float(v[4 * i + 3]);
+          x[0][2 * i] = __uint_as_float(v0[4 * i]) + __uint_as_float(v0[4 * i + 2]);
+          x[0][2 * i + 1] = __uint_as_float(v0[4 * i + 1]) + __uint_as_float(v0[4 * i + 3]);
+          x[1][2 * i] = __uint_as_float(v1[4 * i]) + __uint_as_float(v1[4 * i + 2]);
+          x[1][2 * i + 1] = __uint_as_float(v1[4 * i + 1]) + __uint_as_float(v1[4 * i + 3]);
         }
-        // the row's last visible key in this tile, counted from this thread's first key 2c
-        lim = row_active ? (min(kv_end - 1, lim_abs) - k0 - 2 * cq) : -1;
-        if (lim >= 57) {
 #pragma unroll
-          for (int k = 0; k < 16; ++k) mx = fmaxf(mx, x[k]);
-        } else {
+        for (int h = 0; h < 2; ++h) {
+          // the row's last visible key in this tile, counted from this thread's first key 2c
+          lim[h] = row_active[h] ? (min(kv_end - 1, lim_abs[h]) - k0 - 2 * cq) : -1;
+          if (lim[h] >= 57) {
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            if (8 * i <= lim) mx = fmaxf(mx, x[2 * i]);
-            if (8 * i + 1 <= lim) mx = fmaxf(mx, x[2 * i + 1]);
+            for (int k = 0; k < 16; ++k) mx[h] = fmaxf(mx[h], x[h][k]);
+          } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              if (8 * i <= lim[h]) mx[h] = fmaxf(mx[h], x[h][2 * i]);
+              if (8 * i + 1 <= lim[h]) mx[h] = fmaxf(mx[h], x[h][2 * i + 1]);
+            }
           }
+          mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 1));
+          mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 2));
         }
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
       }
-      uint32_t phi[8], plo[8];
-      float alpha = 1.f;
-      bool need_rescale = false;
-      if (!fail) {
-        // scale > 0: max commutes with the scaling; -inf stays -inf
-        const float mt = mx * scale_log2;
-        if (m_used == -INFINITY) {
-          m_used = mt;  // first contributing tile: nothing accumulated yet
-        } else if (mt > m_used + kRescaleThreshold) {
-          alpha = ex2_approx(m_used - mt);
-          need_rescale = true;
-          l_sum *= alpha;
-          l_use *= alpha;
-          m_used = mt;
+      // the previous tile's reference max, handed over by the other parity
+      float mprev[2] = {-INFINITY, -INFINITY};
+      if (j >= 1) {
+        named_bar_sync(tok_in, 64);
+        if (ctrl->tok_stop[par ^ 1][quad] != 0) {  // the other parity has left
+          failed = true;
+          break;
         }
-        const float off = (m_used == -INFINITY) ? 0.f : (kPShift - m_used);
-        if (lim >= 57)
-          p_split16<true>(x, lim, scale_log2, off, l_sum, l_use, phi, plo);
-        else
-          p_split16<false>(x, lim, scale_log2, off, l_sum, l_use, phi, plo);
+        mprev[0] = ctrl->tok_m[par ^ 1][rr0];
+        mprev[1] = ctrl->tok_m[par ^ 1][rr0 + 8];
+      }
+      float alpha[2] = {1.f, 1.f}, m_new[2];
+      bool need_rescale = false;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        // scale > 0: max commutes with the scaling; -inf stays -inf
+        const float mt = mx[h] * scale_log2[h];
+        m_new[h] = mprev[h];
+        if (fail) {
+        } else if (mprev[h] == -INFINITY) {
+          m_new[h] = mt;  // first contributing tile: nothing accumulated yet
+        } else if (mt > mprev[h] + kRescaleThreshold) {
+          alpha[h] = ex2_approx(mprev[h] - mt);
+          need_rescale = true;
+          m_new[h] = mt;
+        }
+      }
+      if (j + 1 < ntiles) {  // hand this tile's reference max to the other parity
+        if (cq == 0) {
+          ctrl->tok_m[par][rr0] = m_new[0];
+          ctrl->tok_m[par][rr0 + 8] = m_new[1];
+        }
+        if (lane == 0) ctrl->tok_stop[par][quad] = draining ? 1 : 0;
+        asm volatile("bar.arrive %0, %1;" ::"r"(tok_out), "r"(64) : "memory");
+      }
+      if (draining) {
+        failed = true;
+        break;
+      }
+      float off[2];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        // this warp's sums move from its previous reference to this tile's
+        if (!fail && m_w[h] != m_new[h] && m_w[h] != -INFINITY) {
+          const float f = ex2_approx(m_w[h] - m_new[h]);
+          l_sum[h] *= f;
+          l_use[h] *= f;
+        }
+        if (!fail) m_w[h] = m_new[h];
+        off[h] = (m_new[h] == -INFINITY) ? 0.f : (kPShift - m_new[h]);
       }
       if (!fail && j >= 2) {  // the P buffer is free once BMM2 of tile j-2 has completed
         fail = !mbar_wait(&ctrl->o_done[pb], ((j - 2) >> 1) & 1, abort_flag);
@@ -632,58 +695,71 @@ decode_partial_e4m3_kernel(const __grid_constant__ CUtensorMap tm_q, const __gri
       }
       if (!fail) {
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const uint32_t a = p_row + pb * kPBuf + ((((i >> 1) ^ p_sw) << 4) | ((i & 1) << 3));
-          st_shared_u16(a, phi[i]);
-          st_shared_u16(a + kPPart, plo[i]);
+        for (int h = 0; h < 2; ++h) {
+          const int r = rr0 + 8 * h;
+          uint32_t phi[8], plo[8];
+          if (lim[h] >= 57)
+            p_split16<true>(x[h], lim[h], scale_log2[h], off[h], l_sum[h], l_use[h], phi, plo);
+          else
+            p_split16<false>(x[h], lim[h], scale_log2[h], off[h], l_sum[h], l_use[h], phi, plo);
+          const uint32_t p_row = p_base + pb * kPBuf + r * 64;
+          const uint32_t p_sw = (r >> 1) & 3;
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const uint32_t a = p_row + ((((i >> 1) ^ p_sw) << 4) | ((i & 1) << 3));
+            st_shared_u16(a, phi[i]);
+            st_shared_u16(a + kPPart, plo[i]);
+          }
+          if (cq == 0) ctrl->alpha[pb][r] = alpha[h];
         }
-        if (cq == 0) ctrl->alpha[pb][r] = alpha;
         const bool any = __any_sync(0xffffffffu, need_rescale);
-        if (lane == 0) ctrl->rescale_flag[pb][warp] = any ? 1 : 0;
+        if (lane == 0) ctrl->rescale_flag[pb][quad] = any ? 1 : 0;
         // the request's last tile: rows past its end are zeroed in the V blocks (BMM1 of this
         // tile has completed; BMM2 reads them only after p_full)
         const int valid_rows = L - k0;
         if (valid_rows < kTileKeys) {
           const uint32_t stage = smem_u32(smem + kOffRaw + s * kRawTile);
           const int n16 = (kTileKeys - valid_rows) * 4 * (kValueDim / 64);  // 16-byte pieces
-          for (int i = threadIdx.x; i < n16; i += kSoftmaxThreads) {
+          for (int i = quad * 32 + lane; i < n16; i += kSoftmaxThreads / 2) {
             const int row = valid_rows + (i >> 5), blk = (i >> 2) & 7, piece = i & 3;
             st_shared_v4(stage + blk * kRawBlock + row * 64 + piece * 16, 0u, 0u, 0u, 0u);
           }
         }
       }
       fence_proxy_async_smem();
-      if (bar_or(1, kSoftmaxThreads, fail || (*abort_flag != 0))) {
-        failed = true;
-        break;
+      if (bar_or(bar_par, kSoftmaxThreads / 2, fail || (*abort_flag != 0))) {
+        draining = true;  // leave at this parity's next tile (or now, if it has none)
+        continue;
       }
       const int4 f0 = *reinterpret_cast<const int4*>(&ctrl->rescale_flag[pb][0]);
-      const int4 f1 = *reinterpret_cast<const int4*>(&ctrl->rescale_flag[pb][4]);
-      if (f0.x | f0.y | f0.z | f0.w | f1.x | f1.y | f1.z | f1.w) {
+      if (f0.x | f0.y | f0.z | f0.w) {
         // O^T[dim, row] *= alpha[row] for all 512 value columns, once BMM2 of tile j-1 has
         // completed; this thread owns TMEM lane (32 quad + lane) of each 128-column chunk,
-        // rows 32kh .. 32kh+31.  (A wait that gives up raises the abort flag, which the next
-        // closing barrier reports.)
+        // all 64 rows.  (A wait that gives up raises the abort flag, which the next closing
+        // barrier reports.)
         if (j >= 1) mbar_wait(&ctrl->o_done[pb ^ 1], ((j - 1) >> 1) & 1, abort_flag);
         tc_fence_after();
-        float al[32];
-#pragma unroll
-        for (int i = 0; i < 32; i += 4) {
-          const float4 f = *reinterpret_cast<const float4*>(&ctrl->alpha[pb][kh * 32 + i]);
-          al[i] = f.x;
-          al[i + 1] = f.y;
-          al[i + 2] = f.z;
-          al[i + 3] = f.w;
-        }
 #pragma unroll 1
-        for (int qc = 0; qc < 4; ++qc) {
-          uint32_t v[32];
-          const uint32_t addr = tmem + lane_base + qc * 64 + kh * 32;
-          tmem_ld32(addr, v);
-          tmem_ld_wait();
+        for (int hh = 0; hh < 2; ++hh) {
+          float al[32];
 #pragma unroll
-          for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * al[i]);
-          tmem_st32(addr, v);
+          for (int i = 0; i < 32; i += 4) {
+            const float4 f = *reinterpret_cast<const float4*>(&ctrl->alpha[pb][hh * 32 + i]);
+            al[i] = f.x;
+            al[i + 1] = f.y;
+            al[i + 2] = f.z;
+            al[i + 3] = f.w;
+          }
+#pragma unroll 1
+          for (int qc = 0; qc < 4; ++qc) {
+            uint32_t v[32];
+            const uint32_t addr = tmem + lane_base + qc * 64 + hh * 32;
+            tmem_ld32(addr, v);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * al[i]);
+            tmem_st32(addr, v);
+          }
         }
         tmem_st_wait();
       }
@@ -691,30 +767,49 @@ decode_partial_e4m3_kernel(const __grid_constant__ CUtensorMap tm_q, const __gri
       __syncwarp();
       if (lane == 0) mbar_arrive(&ctrl->p_full[pb]);
     }
+    if (draining) failed = true;
 
     if (!failed) failed = !mbar_wait(&ctrl->o_done[(ntiles - 1) & 1], ((ntiles - 1) >> 1) & 1, abort_flag);
-    // the row's four threads' partial sums
-    l_sum += __shfl_xor_sync(0xffffffffu, l_sum, 1);
-    l_sum += __shfl_xor_sync(0xffffffffu, l_sum, 2);
-    l_use += __shfl_xor_sync(0xffffffffu, l_use, 1);
-    l_use += __shfl_xor_sync(0xffffffffu, l_use, 2);
+    // this warp's partial row sums (its four threads per row), relative to m_w, to shared
+    // memory; the two parities' parts are combined below
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      l_sum[h] += __shfl_xor_sync(0xffffffffu, l_sum[h], 1);
+      l_sum[h] += __shfl_xor_sync(0xffffffffu, l_sum[h], 2);
+      l_use[h] += __shfl_xor_sync(0xffffffffu, l_use[h], 1);
+      l_use[h] += __shfl_xor_sync(0xffffffffu, l_use[h], 2);
+      if (cq == 0) {
+        ctrl->fin[par][0][rr0 + 8 * h] = m_w[h];
+        ctrl->fin[par][1][rr0 + 8 * h] = l_sum[h];
+        ctrl->fin[par][2][rr0 + 8 * h] = l_use[h];
+      }
+    }
     if (bar_or(1, kSoftmaxThreads, failed || (*abort_flag != 0))) {
       failed = true;
     } else {
       tc_fence_after();
       const bool final_out = (nsplit_b == 1);
-      if (cq == 0) {
-        const float ls = l_sum;
-        const float lu = l_use;
-        const float lse2 = (ls > 0.f) ? (m_used + __log2f(ls) - kPShift) : -INFINITY;
-        const float lse_nat = lse2 * 0.69314718055994530942f;
-        ctrl->row_scale[r] = (lu > 0.f) ? (v_scale / lu) : 0.f;
-        if (row_active) {
-          const int64_t grow = static_cast<int64_t>(b) * p.R + row0 + r;
-          if (final_out)
-            p.lse[grow] = lse_nat;
-          else
-            p.ws_lse[(static_cast<int64_t>(b) * p.max_splits + split) * p.R + row0 + r] = lse_nat;
+      if (par == 0 && cq == 0) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int r = rr0 + 8 * h;
+          // O is relative to the last tile's max, the larger of the two parities' last
+          const float ma = ctrl->fin[0][0][r], mb = ctrl->fin[1][0][r];
+          const float m = fmaxf(ma, mb);
+          const float fa = (ma == -INFINITY) ? 0.f : ex2_approx(ma - m);
+          const float fb = (mb == -INFINITY) ? 0.f : ex2_approx(mb - m);
+          const float ls = ctrl->fin[0][1][r] * fa + ctrl->fin[1][1][r] * fb;
+          const float lu = ctrl->fin[0][2][r] * fa + ctrl->fin[1][2][r] * fb;
+          const float lse2 = (ls > 0.f) ? (m + __log2f(ls) - kPShift) : -INFINITY;
+          const float lse_nat = lse2 * 0.69314718055994530942f;
+          ctrl->row_scale[r] = (lu > 0.f) ? (v_scale / lu) : 0.f;
+          if (row_active[h]) {
+            const int64_t grow = static_cast<int64_t>(b) * p.R + row0 + r;
+            if (final_out)
+              p.lse[grow] = lse_nat;
+            else
+              p.ws_lse[(static_cast<int64_t>(b) * p.max_splits + split) * p.R + row0 + r] = lse_nat;
+          }
         }
       }
       named_bar_sync(1, kSoftmaxThreads);

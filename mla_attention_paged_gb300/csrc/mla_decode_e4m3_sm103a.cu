@@ -25,10 +25,9 @@
 //    each in turn, so that row r's hi and lo partial scores land in TMEM lanes i and i + 8
 //    (i = 16 (r / 8) + r % 8).  The 16x256b load shape hands both lanes' values for the
 //    same columns to one thread, which adds them.  One pass of full-rate MMAs reads the K
-//    tile once.  The split's column
-//    blocks 0-7 sit in TMEM (the A operand from tensor memory: stacked row = lane, four
-//    codes per 32-bit column), the rope block 8 in shared memory; the stacked Q is then not
-//    re-read from shared memory on every tile.
+//    tile once.  The split's column blocks 0-7 sit in TMEM (the A operand from tensor
+//    memory: stacked row = lane, four codes per 32-bit column), the rope block 8 in shared
+//    memory; the stacked Q is then not re-read from shared memory on every tile.
 //  * BMM2 (O^T += V^T . P^T, M = 128 value columns, N = rows, K = 64 keys) takes V straight
 //    from the raw stage as an MN-major e4m3 operand.  P is split in two 8-bit parts: the
 //    softmax forms P 2^6 (at most 2^8, because the running max moves once a tile's max

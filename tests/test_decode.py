@@ -96,6 +96,10 @@ SMALL = [
     ("fp8_ragged", 3, 1, 16, [1, 65, 130], 64, "e4m3"),
     ("fp8_page16", 2, 2, 16, [77, 500], 16, "e4m3"),
     ("fp8_page128", 1, 3, 16, [700], 128, "e4m3"),
+    ("fp8_page8", 2, 4, 16, [45, 300], 8, "e4m3"),      # eight page boxes per tile
+    ("fp8_page32", 1, 4, 16, [1025], 32, "e4m3"),
+    ("fp8_page256", 1, 2, 16, [2000], 256, "e4m3"),
+    ("fp8_tails", 5, 1, 16, [2, 64, 127, 128, 129], 64, "e4m3"),  # tile counts 1-3 and full tails
     ("fp8_h128", 1, 2, 128, [900], 64, "e4m3"),
     ("mtp8", 2, 8, 16, [700, 2000], 64, "bf16"),   # q_len 8: 128 folded rows, two row groups
     ("fp8_mtp8", 2, 8, 16, [333, 1500], 64, "e4m3"),

@@ -18,11 +18,14 @@
 //    takes 64 consecutive rows, so all heads and drafts share each latent tile load.
 //  * Producer warp: bf16 pools are gathered by TMA (one 3-D box per 64-key tile: 64 rows x
 //    nine 128-byte-swizzled column blocks) from the pages named by the page table, into a
-//    2-stage ring.  For int8 pools, three dequant warps (4, 6, 7) read each tile's rows
+//    2-stage ring.  For int8 pools, six decode warps (4 and 6-10) read each tile's rows
 //    from the page pool into registers, wait for the stage, and write them as f16 into the
-//    same swizzled layout (exact decode: int8 codes as themselves); the MMA warp prefetches
+//    same swizzled layout (exact decode: int8 codes as themselves); the BMM1 warp prefetches
 //    rows into L2 a few tiles ahead of them.  The int8 GEMMs run on f16 operands (Q
-//    converted once per CTA, P in f16).
+//    converted once per CTA, P in f16), issued by two warps (BMM1 by warp 5, BMM2 by the
+//    last warp), each waiting on its own inputs; one polling warp for both left each GEMM
+//    waiting behind the other's issue.  (The bf16 path keeps one issuer for both: split,
+//    it measured slower there.)
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
 
@@ -42,10 +45,12 @@ constexpr int kPrefetchTiles = 3;  // int8 pools: tiles ahead of the decode that
 // warps 4 and 6-10 decode (352 threads), each lane holding four rows' codes of its tile.
 constexpr int kDecodeWarps = 6;
 constexpr int kDequantThreads = 32 * kDecodeWarps;
-// int8: softmax warps 0-3, decode warp 4, MMA warp 5, decode warps 6 .. 4 + kDecodeWarps
-__host__ __device__ constexpr int threads_for(bool fp8) { return fp8 ? 32 * (5 + kDecodeWarps) : 192; }
-static_assert(threads_for(true) / 32 - 1 == 4 + kDecodeWarps, "the last int8 warp is the last decode warp");
-static_assert(1 + (threads_for(true) / 32 - 6) == kDecodeWarps, "decode warps: 4 and 6 ..");
+// int8: softmax warps 0-3, decode warp 4, BMM1 warp 5, decode warps 6 .. 4 + kDecodeWarps,
+// BMM2 warp 5 + kDecodeWarps
+__host__ __device__ constexpr int threads_for(bool fp8) { return fp8 ? 32 * (6 + kDecodeWarps) : 192; }
+constexpr int kBmm2WarpInt8 = 5 + kDecodeWarps;
+static_assert(threads_for(true) / 32 - 1 == kBmm2WarpInt8, "the last int8 warp is the BMM2 issuer");
+static_assert(1 + (kBmm2WarpInt8 - 6) == kDecodeWarps, "decode warps: 4 and 6 .. kBmm2WarpInt8 - 1");
 
 // Shared memory map: Q | stage0 | stage1 | P | ctrl.  A stage holds one 64-key tile as nine
 // 128-byte-swizzled column blocks: bf16 as loaded by TMA, or (int8 pools) f16 as decoded
@@ -65,6 +70,7 @@ struct DecodeCtrl {
   uint64_t o_done;
   uint64_t q_ready;            // int8 pools: Q converted to f16 in place
   uint64_t mma_drain;
+  uint64_t mma_drain2;         // int8: the BMM2 warp's MMAs
   uint32_t tmem_base;
   int abort_flag;
   int rescale_flag[4];
@@ -113,7 +119,7 @@ decode_partial_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
     mbar_init(&ctrl->q_full, 1);
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&ctrl->kv_full[s], kInt8 ? kDequantThreads : 1);
-      mbar_init(&ctrl->kv_empty[s], 1);
+      mbar_init(&ctrl->kv_empty[s], kInt8 ? 2 : 1);  // int8: BMM1 and BMM2 come from two warps
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&ctrl->s_full[i], 1);
@@ -123,6 +129,7 @@ decode_partial_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
     mbar_init(&ctrl->o_done, 1);
     mbar_init(&ctrl->q_ready, kDequantThreads);
     mbar_init(&ctrl->mma_drain, 1);
+    mbar_init(&ctrl->mma_drain2, 1);
     ctrl->abort_flag = 0;
     for (int w = 0; w < 4; ++w) ctrl->rescale_flag[w] = 0;
     fence_mbarrier_init();
@@ -285,6 +292,39 @@ decode_partial_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
     }
     bool ok = kInt8 ? mbar_wait(&ctrl->q_ready, 0, abort_flag) : mbar_wait(&ctrl->q_full, 0, abort_flag);
     ok = __all_sync(0xffffffffu, ok);
+    if constexpr (kInt8) {
+      // int8 pools: this warp issues BMM1 only (BMM2 has its own warp): BMM1(n1) once tile
+      // n1 has been decoded and its S buffer is free.  Its commit on the stage's empty
+      // barrier is the first of two (the BMM2 warp's is the other).
+      for (int n1 = 0; ok && n1 < ntiles; ++n1) {
+        const int s = n1 % kStages, sb = n1 & 1;
+        bool w = mbar_wait(&ctrl->kv_full[s], (n1 / kStages) & 1, abort_flag);
+        if (w && n1 >= 2) w = mbar_wait(&ctrl->s_free[sb], ((n1 - 2) >> 1) & 1, abort_flag);
+        ok = __all_sync(0xffffffffu, w);
+        if (!ok) break;
+        tc_fence_after();
+        const uint64_t k_desc = make_smem_desc(smem_u32(smem + kOffStages + s * kTileBytes), 16, 1024);
+        const uint32_t d = tmem + kTmemS + sb * 64;
+        if (elect_one()) {
+#pragma unroll
+          for (int c = 0; c < kDimBlocks; ++c) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const uint64_t off = static_cast<uint64_t>((c * kBlockBytes + k * 32) >> 4);
+              umma_bf16(d, q_desc + off, k_desc + off, idesc1, (c | k) != 0);
+            }
+          }
+          umma_commit(&ctrl->s_full[sb]);
+          umma_commit(&ctrl->kv_empty[s]);
+        }
+        __syncwarp();
+        prefetch(n1 + 1 + kPrefetchTiles, pf_pid);
+        const int pg = page_of(n1 + 2 + kPrefetchTiles);
+        pf_pid = (pg >= 0) ? __ldg(pt + pg) : -1;
+        __syncwarp();
+      }
+      ok = false;  // (the loop below is the bf16 path's)
+    }
     // Issue whichever GEMM is ready: BMM2(n2) first (it frees a stage), else BMM1(n1) for a
     // tile whose data has landed and whose S buffer is free.  BMM1 runs at most two tiles
     // ahead of BMM2 (double-buffered S).
@@ -366,6 +406,42 @@ decode_partial_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
     if (elect_one()) {
       umma_commit(&ctrl->mma_drain);
       drain_wait(&ctrl->mma_drain, 0);
+    }
+    __syncwarp();
+  } else if (kInt8 && warp == kBmm2WarpInt8) {
+    // ------------------------------------------------------------------ int8 pools: BMM2 issuer
+    // O^T += V^T . P^T once the softmax has written P(n2); V from the decoded stage (waited
+    // for here too, so that this warp orders its reads after the decode warps' writes).
+    const uint32_t idesc2 = make_idesc_f16(128, nq, true, false);
+    const uint64_t p_desc = make_smem_desc(smem_u32(smem + kOffP), 16, 1024);
+    bool ok = true;
+    for (int n2 = 0; ok && n2 < ntiles; ++n2) {
+      const int s = n2 % kStages;
+      bool w = mbar_wait(&ctrl->p_full, n2 & 1, abort_flag);
+      if (w) w = mbar_wait(&ctrl->kv_full[s], (n2 / kStages) & 1, abort_flag);
+      ok = __all_sync(0xffffffffu, w);
+      if (!ok) break;
+      tc_fence_after();
+      const uint64_t v_desc = make_smem_desc(smem_u32(smem + kOffStages + s * kTileBytes), kBlockBytes, 1024);
+      if (elect_one()) {
+#pragma unroll
+        for (int qc = 0; qc < 4; ++qc) {
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint64_t voff = static_cast<uint64_t>((2 * qc * kBlockBytes + kk * 2048) >> 4);
+            const uint64_t poff = static_cast<uint64_t>((kk * 32) >> 4);
+            umma_bf16(tmem + qc * 64, v_desc + voff, p_desc + poff, idesc2, (n2 > 0 || kk > 0) ? 1u : 0u);
+          }
+        }
+        umma_commit(&ctrl->o_done);
+        umma_commit(&ctrl->kv_empty[s]);
+      }
+      __syncwarp();
+    }
+    // every MMA this warp issued completes before TMEM is released
+    if (elect_one()) {
+      umma_commit(&ctrl->mma_drain2);
+      drain_wait(&ctrl->mma_drain2, 0);
     }
     __syncwarp();
   } else if (kInt8 && warp >= 4) {

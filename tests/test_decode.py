@@ -108,10 +108,15 @@ SMALL = [
     ("int8_page16", 2, 2, 16, [77, 500], 16, "int8"),
     ("int8_page128", 1, 3, 16, [700], 128, "int8"),
     ("int8_h128", 1, 2, 128, [900], 64, "int8"),
+    ("int8_page8", 2, 4, 16, [45, 300], 8, "int8"),
+    ("int8_page32", 1, 4, 16, [1025], 32, "int8"),
+    ("int8_page256", 1, 2, 16, [2000], 256, "int8"),
+    ("int8_tails", 5, 1, 16, [2, 64, 127, 128, 129], 64, "int8"),
     ("int8page_drafts4", 2, 4, 16, [300, 1000], 64, "int8page"),
     ("int8page_ragged", 3, 1, 16, [1, 65, 130], 64, "int8page"),
     ("int8page_page16", 2, 2, 16, [77, 500], 16, "int8page"),
     ("int8page_page128", 1, 3, 16, [700], 128, "int8page"),
+    ("int8page_page8", 2, 4, 16, [45, 300], 8, "int8page"),
 ]
 
 

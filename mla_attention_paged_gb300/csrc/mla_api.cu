@@ -159,7 +159,9 @@ int choose_chunk_tiles(const std::vector<int>& lens, int groups, int sms) {
     for (int t : tiles) n += (t + ct - 1) / ct;
     return n * groups;
   };
-  const int lo = std::min(4, max_tiles);
+  // smallest chunk: 4 tiles; fewer (down to one) only where the longest request still needs
+  // at most 32 splits, one round of the combine (which stages up to 32 splits at a time)
+  const int lo = std::min(4, std::max(1, (max_tiles + 31) / 32));
   std::vector<int> cands;
   for (int k = 1; k <= 4; ++k) {
     const int ct = (max_tiles + k - 1) / k;

@@ -153,8 +153,9 @@ def test_plan_one_sm_never_splits(mla):
 
 def test_plan_invariants_on_random_batches(mla):
     """Seeded random batches (ragged lengths, 1-8 drafts or a long absorbed prefill, 16 or
-    128 heads, several SM counts): the split chunk is whole 64-key tiles and at least four
-    of them (or the whole of the longest request); the plan's estimated duration is the
+    128 heads, several SM counts): the split chunk is whole 64-key tiles, at least four of
+    them (or the whole of the longest request), or fewer where the longest request still
+    takes at most 32 splits (one round of the combine); the plan's estimated duration is the
     lowest over its candidates (1-4 splits of the longest request, and the smallest chunk
     that keeps the call in one wave when the unsplit call fits one), so it is never longer
     than the unsplit call's; a split that fits one wave is the smallest such chunk; and the
@@ -174,15 +175,16 @@ def test_plan_invariants_on_random_batches(mla):
         tiles = [(L + 63) // 64 for L in lens]
         mt = max(tiles)
         ct = plan.chunk_tokens // 64
-        assert plan.chunk_tokens % 64 == 0 and ct >= min(4, mt)
+        lo = min(4, max(1, -(-mt // 32)))
+        assert plan.chunk_tokens % 64 == 0 and ct >= lo
         groups = (T * H + 63) // 64
         assert plan.head_groups == groups
         n_ctas = lambda c: groups * sum((t + c - 1) // c for t in tiles)
         assert plan.max_splits == (max(lens) + plan.chunk_tokens - 1) // plan.chunk_tokens
-        cands = [c for c in (-(-mt // k) for k in (1, 2, 3, 4)) if c >= min(4, mt)]
+        cands = [c for c in (-(-mt // k) for k in (1, 2, 3, 4)) if c >= lo]
         one_wave = None
         if n_ctas(mt) <= sms:
-            one_wave = min(c for c in range(min(4, mt), mt + 1) if n_ctas(c) <= sms)
+            one_wave = min(c for c in range(lo, mt + 1) if n_ctas(c) <= sms)
             cands.append(one_wave)
         cost = lambda c: _plan_cost(tiles, groups, c, sms)
         assert ct in cands + [mt]

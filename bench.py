@@ -298,16 +298,26 @@ def replica_seed(base_seed, set_index, rank):
     return base_seed + 97 * set_index + 100003 * rank
 
 
-def _traffic_record(kernel_src, workload):
-    """DRAM bytes per launch of the partial kernel on `workload` from the committed ncu
-    summary, if it was taken on the current kernel source; otherwise None."""
+TRAFFIC_SOURCES = ("mla_decode_narrow_sm103a.cu", "sm103a_ptx.cuh")  # the headline's partial kernel
+
+
+def _sources_sha256(names):
     import hashlib
+    h = hashlib.sha256()
+    for n in names:
+        with open(os.path.join(ROOT, "mla_attention_paged_gb300", "csrc", n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def _traffic_record(workload):
+    """DRAM bytes per launch of the partial kernel on `workload` from the committed ncu
+    summary, if it was taken on the current kernel sources; otherwise None."""
     path = os.path.join(ROOT, "profiles", "decode_partial_traffic.json")
     try:
         with open(path) as f:
             rec = json.load(f)
-        src = open(os.path.join(ROOT, "mla_attention_paged_gb300", "csrc", kernel_src), "rb").read()
-        if rec.get("source_sha256") != hashlib.sha256(src).hexdigest() or rec.get("workload") != workload:
+        if rec.get("source_sha256") != _sources_sha256(TRAFFIC_SOURCES) or rec.get("workload") != workload:
             return None
         return rec
     except Exception:
@@ -550,7 +560,7 @@ def main():
     part_ms = kstart.elapsed_time(kstop) / n_k
     peaks = _peaks()
     achieved = alg_bytes / (part_ms / 1e3) / 1e9
-    traffic = _traffic_record("mla_decode_sm103a.cu", WORKLOAD)
+    traffic = _traffic_record(WORKLOAD)
 
     # End to end through the public API: each step copies that step's q, page table and
     # lengths from pinned host memory to the device (packed in one buffer: one copy), calls
@@ -663,7 +673,7 @@ def main():
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": achieved / peaks["hbm_gbs"],
                      "traffic": (traffic["dram_bytes_per_launch"] if traffic else None),
-                     "kernel": "decode_partial_kernel<bf16>", "kernel_us": part_ms * 1e3,
+                     "kernel": "decode_partial_narrow_kernel", "kernel_us": part_ms * 1e3,
                      "alg_bytes_per_launch": alg_bytes, "peak_source": peaks["source"] + " copy bandwidth"},
         "e2e": {"value": e2e_val, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "steps": e2e_steps, "us_per_call": e2e_s / e2e_steps * 1e6,

@@ -16,8 +16,8 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libmla.so")
-SOURCES = ["mla_api.cu", "mla_decode_sm103a.cu", "mla_decode_e4m3_sm103a.cu", "mla_prefill_sm103a.cu",
-           "mla_noalloc.cu"]
+SOURCES = ["mla_api.cu", "mla_decode_sm103a.cu", "mla_decode_e4m3_sm103a.cu", "mla_decode_narrow_sm103a.cu",
+           "mla_prefill_sm103a.cu", "mla_noalloc.cu"]
 HEADERS = ["mla_internal.h", "sm103a_ptx.cuh", "kv8_decode.cuh", os.path.join("..", "..", "include", "mla.h")]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -987,7 +987,10 @@ cudaError_t launch_decode_partial(const DecodeParams& p, const CUtensorMap& tm_q
     case kKvE4m3: return launch_decode_partial_e4m3(p, tm_q, tm_kv, head_groups, stream);
     case kKvInt8: return launch_partial_impl<kKvInt8>(p, tm_q, tm_kv, head_groups, stream);
     case kKvInt8Page: return launch_partial_impl<kKvInt8Page>(p, tm_q, tm_kv, head_groups, stream);
-    default: return launch_partial_impl<kKvBf16>(p, tm_q, tm_kv, head_groups, stream);
+    default:
+      // at most 32 folded rows: Q fits in tensor memory, and shared memory takes three tiles
+      if (p.R <= 32) return launch_decode_partial_narrow(p, tm_q, tm_kv, stream);
+      return launch_partial_impl<kKvBf16>(p, tm_q, tm_kv, head_groups, stream);
   }
 }
 

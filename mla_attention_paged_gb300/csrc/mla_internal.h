@@ -69,6 +69,10 @@ cudaError_t launch_decode_partial(const DecodeParams& p, const CUtensorMap& tm_q
 // Decode over an e4m3 pool: the split-KV partial kernel that runs BMM1 on the raw codes.
 cudaError_t launch_decode_partial_e4m3(const DecodeParams& p, const CUtensorMap& tm_q, const CUtensorMap& tm_kv,
                                        int head_groups, cudaStream_t stream);
+// Decode over a bf16 pool for requests of at most 32 folded rows (R <= 32): Q held in
+// tensor memory, a three-tile ring (mla_decode_narrow_sm103a.cu).
+cudaError_t launch_decode_partial_narrow(const DecodeParams& p, const CUtensorMap& tm_q, const CUtensorMap& tm_kv,
+                                         cudaStream_t stream);
 // Decode: LSE-merge of the split partials for requests with more than one split.
 cudaError_t launch_decode_combine(const DecodeParams& p, cudaStream_t stream);
 // Watchdog self-test kernel (a wait nothing satisfies; must time out and report).

@@ -92,6 +92,15 @@ SMALL = [
     ("page128", 2, 1, 16, [700, 129], 128, "bf16"),
     ("page256", 1, 4, 16, [2000], 256, "bf16"),
     ("long_single", 1, 1, 16, [20000], 64, "bf16"),
+    # at most 32 folded rows (the bf16 kernel with Q in tensor memory and a three-tile ring):
+    # page geometries, 1-4 tiles (the first tile in the stage Q arrived in is tile 2), 24
+    # rows (the second row warp half full), 32 rows over many tiles
+    ("narrow_page8", 2, 2, 16, [45, 300], 8, "bf16"),
+    ("narrow_page32", 1, 2, 16, [1025], 32, "bf16"),
+    ("narrow_page256", 1, 1, 16, [2000], 256, "bf16"),
+    ("narrow_tails", 7, 2, 16, [2, 64, 127, 128, 129, 192, 193], 64, "bf16"),
+    ("narrow_rows24", 2, 3, 8, [500, 1300], 64, "bf16"),
+    ("narrow_rows32", 2, 2, 16, [4000, 9000], 64, "bf16"),
     ("fp8_drafts4", 2, 4, 16, [300, 1000], 64, "e4m3"),
     ("fp8_ragged", 3, 1, 16, [1, 65, 130], 64, "e4m3"),
     ("fp8_page16", 2, 2, 16, [77, 500], 16, "e4m3"),

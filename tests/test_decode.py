@@ -101,6 +101,14 @@ SMALL = [
     ("narrow_tails", 7, 2, 16, [2, 64, 127, 128, 129, 192, 193], 64, "bf16"),
     ("narrow_rows24", 2, 3, 8, [500, 1300], 64, "bf16"),
     ("narrow_rows32", 2, 2, 16, [4000, 9000], 64, "bf16"),
+    # 33-64 folded rows in one group: pages of 16 and 128 keys, lengths around tile
+    # boundaries, 40 and 48 rows, long requests over many splits
+    ("rows64_page16", 2, 4, 16, [300, 97], 16, "bf16"),
+    ("rows64_page128", 2, 4, 16, [700, 129], 128, "bf16"),
+    ("rows64_tails", 8, 4, 16, [4, 47, 48, 49, 96, 97, 191, 240], 64, "bf16"),
+    ("rows40", 2, 5, 8, [500, 1300], 64, "bf16"),
+    ("rows48", 2, 3, 16, [777, 2049], 32, "bf16"),
+    ("rows64_long", 2, 4, 16, [9000, 17000], 64, "bf16"),
     ("fp8_drafts4", 2, 4, 16, [300, 1000], 64, "e4m3"),
     ("fp8_ragged", 3, 1, 16, [1, 65, 130], 64, "e4m3"),
     ("fp8_page16", 2, 2, 16, [77, 500], 16, "e4m3"),

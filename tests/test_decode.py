@@ -164,12 +164,14 @@ def test_decode_combine_many_splits(mla, oracle_mod, kv):
     assert plan.max_splits > 64
 
 
-@pytest.mark.parametrize("kv,num_sms", [("bf16", 0), ("e4m3", 0), ("int8", 0), ("bf16", 1)],
-                         ids=["bf16", "e4m3", "int8", "one_split"])
-def test_decode_stages_equal_decode_bitwise(mla, kv, num_sms):
+@pytest.mark.parametrize("kv,num_sms,q_len", [("bf16", 0, 4), ("e4m3", 0, 4), ("int8", 0, 4), ("bf16", 1, 4),
+                                              ("bf16", 0, 2), ("bf16", 1, 2)],
+                         ids=["bf16", "e4m3", "int8", "one_split", "bf16_rows32", "one_split_rows32"])
+def test_decode_stages_equal_decode_bitwise(mla, kv, num_sms, q_len):
     """mla_decode_partial then mla_decode_combine gives mla_decode's bits (multi-split and
-    single-split plans; the combine enqueues nothing for the latter)."""
-    wl = DecodeWorkload("stages", 3, 4, 16, [5000, 130, 2999], kv_dtype=kv, seed=79, peaked=True)
+    single-split plans; the combine enqueues nothing for the latter).  q_len 2 x 16 heads
+    runs the kernel that keeps Q in tensor memory."""
+    wl = DecodeWorkload("stages", 3, q_len, 16, [5000, 130, 2999], kv_dtype=kv, seed=79, peaked=True)
     inp = make_decode_inputs(wl, "cuda")
     kvd = {"e4m3": mla.MLA_KV_E4M3, "int8": mla.MLA_KV_INT8}.get(kv, mla.MLA_KV_BF16)
     plan = mla.decode_plan(wl.seq_lens, wl.q_len, wl.heads, wl.page_size, inp.page_table.shape[1],

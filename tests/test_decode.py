@@ -101,6 +101,8 @@ SMALL = [
     ("narrow_tails", 7, 2, 16, [2, 64, 127, 128, 129, 192, 193], 64, "bf16"),
     ("narrow_rows24", 2, 3, 8, [500, 1300], 64, "bf16"),
     ("narrow_rows32", 2, 2, 16, [4000, 9000], 64, "bf16"),
+    ("narrow_one_row", 2, 1, 1, [100, 7], 64, "bf16"),   # one folded row: BMM2 N = 16
+    ("narrow_rows17", 2, 1, 17, [300, 65], 64, "bf16"),  # the second row warp holds one row
     # 33-64 folded rows in one group: pages of 16 and 128 keys, lengths around tile
     # boundaries, 40 and 48 rows, long requests over many splits
     ("rows64_page16", 2, 4, 16, [300, 97], 16, "bf16"),

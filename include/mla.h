@@ -86,17 +86,24 @@ typedef struct mla_decode_plan_t {
   int32_t chunk_tokens;      /* keys per split (multiple of 64)                          */
   int32_t max_splits;        /* splits of the longest request                            */
   int32_t max_seq_len;       /* longest planned request; device seq_lens must not exceed */
+  int32_t split_major;       /* launch order of the partial kernel's CTAs: 1 = split by
+                                split (plans of more than one wave), 0 = request by request */
   size_t workspace_bytes;    /* bytes mla_decode needs in `workspace` (0 = none)         */
 } mla_decode_plan_t;
 
 /* Plan one decode launch: pick the keys-per-split chunk (whole 64-key tiles) and size the
  * workspace for the split partials.  The partial kernel runs one CTA per (request, split,
- * 64-row group); the plan estimates the call's duration by dispatching those CTAs in launch
- * order onto the SM that frees first (each costing its tiles plus a fixed start-up and
- * epilogue cost, plus the combine when a request is split), over these chunks: the
- * longest request in 1-4 splits, and the smallest chunk that keeps the call in one wave of
- * CTAs when the unsplit call fits one.  The chunk with the shortest estimate wins (fewer
- * splits on a tie), so a split is never taken when it lengthens the call by that estimate.
+ * 64-row group); the plan estimates the call's duration by dispatching those CTAs in
+ * launch order onto the SM that frees first (each costing its tiles plus a fixed
+ * start-up and epilogue cost that depends on the pool format, plus the combine when a
+ * request is split), over these chunks: the longest request in 1-4 splits, the smallest
+ * chunk that keeps the call in one wave of CTAs when the unsplit call fits one, and, with
+ * one row group, the chunks that share all tiles evenly over one or two waves.  The chunk
+ * with the shortest estimate wins (fewer splits on a tie), so a split is never taken when
+ * it lengthens the call by that estimate.  A plan of one row group and more than one wave
+ * launches its CTAs split by split (every request's first split, then every request's
+ * second, ...: split_major = 1), so that short remainders go last; every other plan
+ * launches them request by request.
  * Plans are memoised on all arguments
  * (the split count and workspace are "computed automatically at run time and cached",
  * [TALK] Kernel section).

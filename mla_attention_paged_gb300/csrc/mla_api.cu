@@ -99,16 +99,25 @@ std::mutex g_plan_mu;
 std::unordered_map<std::string, mla_decode_plan_t> g_plan_cache;
 
 // Cost model of the planner, in units of one 64-key tile of one CTA: a CTA costs its tiles
-// plus kCtaFixedTiles (start-up until its first tile has landed, and the epilogue), and a
-// plan with more than one split pays kCombineTiles for the combine kernel.
-constexpr long long kCtaFixedTiles = 3;
+// plus a fixed part (start-up until its first tile has landed, and the epilogue), and a
+// plan with more than one split pays kCombineTiles for the combine kernel.  The fixed part
+// in tile units depends on the pool format: an e4m3 tile holds half the bytes of a bf16 or
+// int8 one and streams in about half the time, while the start-up (Q load and split, the
+// first tiles' latency) and the epilogue take about as long.
 constexpr long long kCombineTiles = 2;
+long long cta_fixed_tiles(int kv_dtype) { return kv_dtype == MLA_KV_E4M3 ? 10 : 3; }
+
+// Launch order of a multi-wave plan: split by split (every request's split s before any
+// split s + 1, so that short remainders go last) for one row group; request by request
+// for several, whose row groups share each tile through L2 and so run best side by side
+// on one request's keys.
+bool split_major_order(int groups) { return groups == 1; }
 
 // Estimated duration of a decode call whose splits are ct tiles long: the partial kernel's
-// CTAs (group fastest, then split, then request: the grid's launch order) are dispatched in
-// that order, each onto the SM that frees first; CTAs of splits a request does not have exit
-// at once and cost nothing.  Plus the combine, when some request is split.
-long long plan_cost(const std::vector<int>& tiles, int groups, int ct, int sms) {
+// CTAs, in the grid's launch order (group fastest, then split_major_order's), are
+// dispatched each onto the SM that frees first; CTAs of splits a request does not have
+// exit at once and cost nothing.  Plus the combine, when some request is split.
+long long plan_cost(const std::vector<int>& tiles, int groups, int ct, int sms, long long fixed) {
   int max_splits = 1;
   long long n_ctas = 0, longest = 0;
   for (int t : tiles) {
@@ -119,22 +128,27 @@ long long plan_cost(const std::vector<int>& tiles, int groups, int ct, int sms) 
   }
   long long span;
   if (n_ctas <= sms) {
-    span = longest + kCtaFixedTiles;  // one wave: the longest CTA
+    span = longest + fixed;  // one wave: the longest CTA
   } else {
     std::priority_queue<long long, std::vector<long long>, std::greater<long long>> free_at;
     for (int i = 0; i < sms; ++i) free_at.push(0);
     span = 0;
-    for (int t : tiles) {
-      const int ns = (t + ct - 1) / ct;
-      for (int s = 0; s < ns; ++s) {
-        const long long cost = std::min(ct, t - s * ct) + kCtaFixedTiles;
-        for (int g = 0; g < groups; ++g) {
-          const long long start = free_at.top();
-          free_at.pop();
-          free_at.push(start + cost);
-          span = std::max(span, start + cost);
-        }
+    auto dispatch = [&](int t, int s) {
+      const long long cost = std::min<long long>(ct, t - static_cast<long long>(s) * ct) + fixed;
+      for (int g = 0; g < groups; ++g) {
+        const long long start = free_at.top();
+        free_at.pop();
+        free_at.push(start + cost);
+        span = std::max(span, start + cost);
       }
+    };
+    if (split_major_order(groups)) {
+      for (int s = 0; s < max_splits; ++s)
+        for (int t : tiles)
+          if (s * static_cast<long long>(ct) < t) dispatch(t, s);
+    } else {
+      for (int t : tiles)
+        for (int s = 0; s * static_cast<long long>(ct) < t; ++s) dispatch(t, s);
     }
   }
   return span + (max_splits > 1 ? kCombineTiles : 0);
@@ -143,10 +157,14 @@ long long plan_cost(const std::vector<int>& tiles, int groups, int ct, int sms) 
 // Keys-per-split chunk in whole 64-key tiles (at least 4 tiles, or the whole of the
 // longest request when it is shorter).  Candidates: the smallest chunk for which the
 // partial kernel needs no more CTAs than the GPU has SMs (one wave; when the unsplit call
-// already fits), and the longest request cut into 1-4 splits.  The candidate with the
-// lowest plan_cost wins, the one with fewer splits on a tie, so a split is only taken when
-// the model says it shortens the call.
-int choose_chunk_tiles(const std::vector<int>& lens, int groups, int sms) {
+// already fits), the longest request cut into 1-4 splits, and, for calls of one row group,
+// the chunks that share all tiles evenly over one or two waves of SMs.  (A batch of equal
+// requests that one wave leaves a few SMs short of, e.g. 16 x 1024 tiles on 152 SMs as 144
+// CTAs of 114, then runs as 144 CTAs of 108 plus 16 remainders of 52, the remainders
+// launched last and paired up on the SMs that free first.)  The candidate with the lowest
+// plan_cost wins, the one with fewer splits on a tie, so a split is only taken when the
+// model says it shortens the call.
+int choose_chunk_tiles(const std::vector<int>& lens, int groups, int sms, long long fixed) {
   std::vector<int> tiles;
   tiles.reserve(lens.size());
   int max_tiles = 1;
@@ -178,10 +196,18 @@ int choose_chunk_tiles(const std::vector<int>& lens, int groups, int sms) {
     }
     cands.push_back(a);
   }
+  if (groups == 1) {
+    long long total = 0;
+    for (int t : tiles) total += t;
+    for (int waves = 1; waves <= 2; ++waves) {
+      const long long ct = (total + static_cast<long long>(waves) * sms - 1) / (static_cast<long long>(waves) * sms);
+      if (ct >= lo && ct < max_tiles) cands.push_back(static_cast<int>(ct));
+    }
+  }
   int best = max_tiles;
-  long long best_cost = plan_cost(tiles, groups, max_tiles, sms);
+  long long best_cost = plan_cost(tiles, groups, max_tiles, sms, fixed);
   for (int ct : cands) {
-    const long long c = plan_cost(tiles, groups, ct, sms);
+    const long long c = plan_cost(tiles, groups, ct, sms, fixed);
     if (c < best_cost || (c == best_cost && ct > best)) {
       best = ct;
       best_cost = c;
@@ -197,7 +223,7 @@ using namespace mla;
 
 extern "C" {
 
-int mla_version(void) { return 100; }
+int mla_version(void) { return 101; }
 
 const char* mla_status_string(int status) {
   switch (status) {
@@ -264,11 +290,17 @@ int mla_decode_plan(int batch, const int32_t* seq_lens_host, int q_len, int num_
   pl.num_sms = num_sms;
   pl.rows = q_len * num_heads;
   pl.head_groups = (pl.rows + kGroupRows - 1) / kGroupRows;
-  const int ct = choose_chunk_tiles(lens, pl.head_groups, num_sms);
+  const int ct = choose_chunk_tiles(lens, pl.head_groups, num_sms, cta_fixed_tiles(kv_dtype));
   pl.chunk_tokens = ct * kTileKeys;
   pl.max_seq_len = max_len;
   pl.max_splits = (max_len + pl.chunk_tokens - 1) / pl.chunk_tokens;
   if (pl.max_splits > 65535) return MLA_ERR_UNSUPPORTED;
+  {
+    // more CTAs with work than SMs, one row group: launch split by split, as the cost model assumed
+    long long n_ctas = 0;
+    for (int L : lens) n_ctas += (L + pl.chunk_tokens - 1) / pl.chunk_tokens;
+    pl.split_major = (n_ctas * pl.head_groups > num_sms && split_major_order(pl.head_groups)) ? 1 : 0;
+  }
   if (pl.max_splits > 1) {
     const size_t parts = static_cast<size_t>(batch) * pl.max_splits * pl.rows;
     pl.workspace_bytes = 256 + parts * kValueDim * sizeof(__nv_bfloat16) + parts * sizeof(float);
@@ -372,6 +404,7 @@ int decode_stages(const mla_decode_plan_t* plan, const void* q, const void* kv_p
   p.chunk = plan->chunk_tokens;
   p.max_splits = plan->max_splits;
   p.max_seq = plan->max_seq_len;
+  p.split_major = plan->split_major;
   p.kv_dtype = plan->kv_dtype;
   p.num_pages = plan->num_pages;
   const bool kv8 = plan->kv_dtype != MLA_KV_BF16;

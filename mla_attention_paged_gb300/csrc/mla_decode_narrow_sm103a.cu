@@ -82,8 +82,11 @@ decode_partial_narrow_kernel(const __grid_constant__ CUtensorMap tm_q, const __g
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int split = blockIdx.y;
-  const int b = blockIdx.z;
+  // grid (row groups, requests, splits) for a multi-wave plan: the hardware starts CTAs in
+  // linear block order, so every request's first split is dispatched before any second
+  // split; (row groups, splits, requests) otherwise
+  const int b = p.split_major ? blockIdx.y : blockIdx.z;
+  const int split = p.split_major ? blockIdx.z : blockIdx.y;
 
   // Set-up that reads no input of this call (overlaps the previous kernel's tail under
   // programmatic dependent launch; griddepcontrol.wait then orders every input read).
@@ -529,7 +532,7 @@ cudaError_t launch_decode_partial_narrow(const DecodeParams& p, const CUtensorMa
   }
   // programmatic dependent launch, as for the general kernel
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(1, p.max_splits, p.B);
+  cfg.gridDim = p.split_major ? dim3(1, p.B, p.max_splits) : dim3(1, p.max_splits, p.B);
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = kSmemBytes;
   cfg.stream = stream;

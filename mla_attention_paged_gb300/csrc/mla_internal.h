@@ -28,6 +28,7 @@ struct DecodeParams {
   int B, T, H, R;               // R = T*H folded rows per request
   int page_size, max_pages;     // page geometry and page_table row stride
   int chunk, max_splits, max_seq;
+  int split_major;              // grid (groups, B, splits) when set, else (groups, splits, B)
   int kv_dtype;                 // kKvBf16, kKvE4m3, kKvInt8 or kKvInt8Page
   int64_t num_pages;            // pages in the pool: a page id outside [0, num_pages) is reported
   float scale_log2;             // softmax scale * log2(e) (* kv_scale for an 8-bit pool)

@@ -44,7 +44,7 @@ class DecodePlan(ctypes.Structure):
                 ("page_size", ctypes.c_int32), ("max_pages_per_seq", ctypes.c_int32),
                 ("kv_dtype", ctypes.c_int32), ("num_pages", ctypes.c_int64), ("num_sms", ctypes.c_int32),
                 ("rows", ctypes.c_int32), ("head_groups", ctypes.c_int32), ("chunk_tokens", ctypes.c_int32),
-                ("max_splits", ctypes.c_int32), ("max_seq_len", ctypes.c_int32),
+                ("max_splits", ctypes.c_int32), ("max_seq_len", ctypes.c_int32), ("split_major", ctypes.c_int32),
                 ("workspace_bytes", ctypes.c_size_t)]
 
     def as_dict(self):

@@ -57,7 +57,8 @@ def test_binding_covers_the_header(mla):
 
 
 def test_plan_struct_layout(mla):
-    assert ctypes.sizeof(mla.DecodePlan) == 64
+    assert ctypes.sizeof(mla.DecodePlan) == 72
+    assert mla.DecodePlan.workspace_bytes.offset == 64 and mla.DecodePlan.split_major.offset == 56
 
 
 def test_status_strings(mla):
@@ -68,9 +69,15 @@ def test_status_strings(mla):
 
 
 def test_plan_fills_one_wave_and_sizes_workspace(mla):
+    """16 requests of 1024 tiles on 152 SMs.  An e4m3 pool (fixed cost 10 tile-times per
+    CTA) keeps the one-wave plan: 144 CTAs of 114 tiles, 124 + 2 for the combine; 108-tile
+    chunks tie at 126 (two remainders of 52 + 10 on each of the 8 free SMs), and a tie goes
+    to fewer splits.  A bf16 pool (fixed cost 3) takes the chunk that shares the tiles
+    evenly over the SMs: 108 tiles, 144 CTAs of 108 and 16 remainders of 52 launched last,
+    two of them on each of the 8 SMs left free (111 + 2 against 117 + 2)."""
     lens = [65536] * 16
     plan = mla.decode_plan(lens, q_len=4, num_heads=16, page_size=64, max_pages_per_seq=1024,
-                           num_pages=16 * 1024, num_sms=152)
+                           num_pages=16 * 1024, kv_dtype=mla.MLA_KV_E4M3, num_sms=152)
     assert plan.rows == 64 and plan.head_groups == 1
     assert plan.chunk_tokens % 64 == 0
     ctas = sum((L + plan.chunk_tokens - 1) // plan.chunk_tokens for L in lens) * plan.head_groups
@@ -81,6 +88,12 @@ def test_plan_fills_one_wave_and_sizes_workspace(mla):
     assert plan.max_splits == (65536 + plan.chunk_tokens - 1) // plan.chunk_tokens
     parts = 16 * plan.max_splits * 64
     assert plan.workspace_bytes == 256 + parts * 512 * 2 + parts * 4  # bf16 partial rows + fp32 lse
+    assert _plan_cost([1024] * 16, 1, 114, 152, fixed=10) == 126 == _plan_cost([1024] * 16, 1, 108, 152, fixed=10)
+    bf = mla.decode_plan(lens, q_len=4, num_heads=16, page_size=64, max_pages_per_seq=1024,
+                         num_pages=16 * 1024, num_sms=152)
+    assert bf.chunk_tokens == 108 * 64 and bf.max_splits == 10
+    assert bf.split_major == 1 and plan.split_major == 0  # 160 CTAs with work on 152 SMs; 144
+    assert _plan_cost([1024] * 16, 1, 108, 152) == 113 < _plan_cost([1024] * 16, 1, 114, 152) == 119
 
 
 def test_plan_single_split_needs_no_workspace(mla):
@@ -95,25 +108,30 @@ def test_plan_head_groups_for_many_heads(mla):
     assert plan.rows == 256 and plan.head_groups == 4
 
 
-def _plan_cost(tiles, groups, ct, sms):
-    """The planner's cost model, restated: CTAs (group fastest, then split, then request)
-    dispatched in that order onto the SM that frees first, each costing its tiles + 3; a
-    plan with more than one split adds 2 for the combine."""
+def _plan_cost(tiles, groups, ct, sms, fixed=3):
+    """The planner's cost model, restated: CTAs in launch order (group fastest; with one
+    row group split by split, every request's split s before any split s + 1; with several
+    request by request) dispatched onto the SM that frees first, each costing its tiles + a
+    fixed part (3 tile-times, 10 for an e4m3 pool); a plan with more than one split adds 2
+    for the combine."""
     import heapq
     splits = [-(-t // ct) for t in tiles]
     n_ctas = groups * sum(splits)
     if n_ctas <= sms:
-        span = max(min(t, ct) for t in tiles) + 3
+        span = max(min(t, ct) for t in tiles) + fixed
     else:
         free = [0] * sms
         span = 0
-        for t, ns in zip(tiles, splits):
-            for s in range(ns):
-                cost = min(ct, t - s * ct) + 3
-                for _ in range(groups):
-                    start = heapq.heappop(free)
-                    heapq.heappush(free, start + cost)
-                    span = max(span, start + cost)
+        if groups == 1:
+            order = [(t, s) for s in range(max(splits)) for t, ns in zip(tiles, splits) if s < ns]
+        else:
+            order = [(t, s) for t, ns in zip(tiles, splits) for s in range(ns)]
+        for t, s in order:
+            cost = min(ct, t - s * ct) + fixed
+            for _ in range(groups):
+                start = heapq.heappop(free)
+                heapq.heappush(free, start + cost)
+                span = max(span, start + cost)
     return span + (2 if max(splits) > 1 else 0)
 
 
@@ -156,8 +174,9 @@ def test_plan_invariants_on_random_batches(mla):
     128 heads, several SM counts): the split chunk is whole 64-key tiles, at least four of
     them (or the whole of the longest request), or fewer where the longest request still
     takes at most 32 splits (one round of the combine); the plan's estimated duration is the
-    lowest over its candidates (1-4 splits of the longest request, and the smallest chunk
-    that keeps the call in one wave when the unsplit call fits one), so it is never longer
+    lowest over its candidates (1-4 splits of the longest request, the smallest chunk that
+    keeps the call in one wave when the unsplit call fits one, and with one row group the
+    chunks that share all tiles evenly over one or two waves), so it is never longer
     than the unsplit call's; a split that fits one wave is the smallest such chunk; and the
     workspace fits every split."""
     rng = np.random.default_rng(12)
@@ -186,6 +205,8 @@ def test_plan_invariants_on_random_batches(mla):
         if n_ctas(mt) <= sms:
             one_wave = min(c for c in range(lo, mt + 1) if n_ctas(c) <= sms)
             cands.append(one_wave)
+        if groups == 1:
+            cands += [c for c in (-(-sum(tiles) // (w * sms)) for w in (1, 2)) if lo <= c < mt]
         cost = lambda c: _plan_cost(tiles, groups, c, sms)
         assert ct in cands + [mt]
         assert cost(ct) == min(cost(c) for c in cands)

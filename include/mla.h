@@ -98,7 +98,8 @@ typedef struct mla_decode_plan_t {
  * start-up and epilogue cost that depends on the pool format, plus the combine when a
  * request is split), over these chunks: the longest request in 1-4 splits, the smallest
  * chunk that keeps the call in one wave of CTAs when the unsplit call fits one, and, with
- * one row group, the chunks that share all tiles evenly over one or two waves.  The chunk
+ * one row group, the chunks that share all tiles evenly over one or two waves (and up to
+ * 8 tiles more than the one-wave one).  The chunk
  * with the shortest estimate wins (fewer splits on a tie), so a split is never taken when
  * it lengthens the call by that estimate.  A plan of one row group and more than one wave
  * launches its CTAs split by split (every request's first split, then every request's

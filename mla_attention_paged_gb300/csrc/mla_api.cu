@@ -158,10 +158,11 @@ long long plan_cost(const std::vector<int>& tiles, int groups, int ct, int sms, 
 // longest request when it is shorter).  Candidates: the smallest chunk for which the
 // partial kernel needs no more CTAs than the GPU has SMs (one wave; when the unsplit call
 // already fits), the longest request cut into 1-4 splits, and, for calls of one row group,
-// the chunks that share all tiles evenly over one or two waves of SMs.  (A batch of equal
-// requests that one wave leaves a few SMs short of, e.g. 16 x 1024 tiles on 152 SMs as 144
-// CTAs of 114, then runs as 144 CTAs of 108 plus 16 remainders of 52, the remainders
-// launched last and paired up on the SMs that free first.)  The candidate with the lowest
+// the chunks that share all tiles evenly over one or two waves of SMs (the one-wave one and
+// up to 8 tiles more).  (A batch of equal requests that one wave leaves a few SMs short of,
+// e.g. 16 x 1024 tiles on 152 SMs as 144 CTAs of 114, then runs as 144 CTAs of 108 plus 16
+// remainders of 52, the remainders launched last and paired up on the SMs that free first;
+// with an e4m3 pool's larger fixed cost, 109 and remainders of 43.)  The candidate with the lowest
 // plan_cost wins, the one with fewer splits on a tie, so a split is only taken when the
 // model says it shortens the call.
 int choose_chunk_tiles(const std::vector<int>& lens, int groups, int sms, long long fixed) {
@@ -200,8 +201,13 @@ int choose_chunk_tiles(const std::vector<int>& lens, int groups, int sms, long l
     long long total = 0;
     for (int t : tiles) total += t;
     for (int waves = 1; waves <= 2; ++waves) {
-      const long long ct = (total + static_cast<long long>(waves) * sms - 1) / (static_cast<long long>(waves) * sms);
-      if (ct >= lo && ct < max_tiles) cands.push_back(static_cast<int>(ct));
+      const long long base = (total + static_cast<long long>(waves) * sms - 1) / (static_cast<long long>(waves) * sms);
+      // one wave: also up to 8 tiles longer, which shortens the remainders that run two to
+      // an SM (a larger fixed cost per CTA wants shorter remainders)
+      for (int d = 0; d <= (waves == 1 ? 8 : 0); ++d) {
+        const long long ct = base + d;
+        if (ct >= lo && ct < max_tiles) cands.push_back(static_cast<int>(ct));
+      }
     }
   }
   int best = max_tiles;

@@ -69,31 +69,34 @@ def test_status_strings(mla):
 
 
 def test_plan_fills_one_wave_and_sizes_workspace(mla):
-    """16 requests of 1024 tiles on 152 SMs.  An e4m3 pool (fixed cost 10 tile-times per
-    CTA) keeps the one-wave plan: 144 CTAs of 114 tiles, 124 + 2 for the combine; 108-tile
-    chunks tie at 126 (two remainders of 52 + 10 on each of the 8 free SMs), and a tie goes
-    to fewer splits.  A bf16 pool (fixed cost 3) takes the chunk that shares the tiles
-    evenly over the SMs: 108 tiles, 144 CTAs of 108 and 16 remainders of 52 launched last,
-    two of them on each of the 8 SMs left free (111 + 2 against 117 + 2)."""
+    """16 requests of 1024 tiles on 152 SMs.  A bf16 pool (fixed cost 3 tile-times per CTA)
+    takes the chunk that shares the tiles evenly over the SMs: 108 tiles, 144 CTAs of 108
+    and 16 remainders of 52 launched last, two of them on each of the 8 SMs left free
+    (111 + 2 for the combine, against 117 + 2 for the one-wave plan of 114).  An e4m3 pool
+    (fixed cost 10) would tie there (two remainders of 52 + 10 on an SM: 124 + 2, as the
+    one-wave plan) and takes 109: remainders of 43, 2 x 53 < 119.  A batch that fits one
+    wave at the balanced chunk keeps the one-wave plan: the smallest chunk that fits."""
     lens = [65536] * 16
-    plan = mla.decode_plan(lens, q_len=4, num_heads=16, page_size=64, max_pages_per_seq=1024,
-                           num_pages=16 * 1024, kv_dtype=mla.MLA_KV_E4M3, num_sms=152)
-    assert plan.rows == 64 and plan.head_groups == 1
-    assert plan.chunk_tokens % 64 == 0
+    bf = mla.decode_plan(lens, q_len=4, num_heads=16, page_size=64, max_pages_per_seq=1024,
+                         num_pages=16 * 1024, num_sms=152)
+    assert bf.rows == 64 and bf.head_groups == 1
+    assert bf.chunk_tokens == 108 * 64 and bf.max_splits == 10 and bf.split_major == 1
+    parts = 16 * bf.max_splits * 64
+    assert bf.workspace_bytes == 256 + parts * 512 * 2 + parts * 4  # bf16 partial rows + fp32 lse
+    assert _plan_cost([1024] * 16, 1, 108, 152) == 113 < _plan_cost([1024] * 16, 1, 114, 152) == 119
+    f8 = mla.decode_plan(lens, q_len=4, num_heads=16, page_size=64, max_pages_per_seq=1024,
+                         num_pages=16 * 1024, kv_dtype=mla.MLA_KV_E4M3, num_sms=152)
+    assert f8.chunk_tokens == 109 * 64 and f8.max_splits == 10 and f8.split_major == 1
+    assert (_plan_cost([1024] * 16, 1, 109, 152, fixed=10) == 121
+            < _plan_cost([1024] * 16, 1, 108, 152, fixed=10) == 126 == _plan_cost([1024] * 16, 1, 114, 152, fixed=10))
+    lens = [60000] * 8  # 938 tiles: 8 x 19 = 152 CTAs of 50 fill one wave exactly
+    plan = mla.decode_plan(lens, q_len=4, num_heads=16, page_size=64, max_pages_per_seq=938,
+                           num_pages=8 * 938, num_sms=152)
     ctas = sum((L + plan.chunk_tokens - 1) // plan.chunk_tokens for L in lens) * plan.head_groups
-    assert ctas <= 152
+    assert ctas <= 152 and plan.split_major == 0
     # the next smaller chunk would overflow one wave
     smaller = plan.chunk_tokens - 64
     assert sum((L + smaller - 1) // smaller for L in lens) > 152
-    assert plan.max_splits == (65536 + plan.chunk_tokens - 1) // plan.chunk_tokens
-    parts = 16 * plan.max_splits * 64
-    assert plan.workspace_bytes == 256 + parts * 512 * 2 + parts * 4  # bf16 partial rows + fp32 lse
-    assert _plan_cost([1024] * 16, 1, 114, 152, fixed=10) == 126 == _plan_cost([1024] * 16, 1, 108, 152, fixed=10)
-    bf = mla.decode_plan(lens, q_len=4, num_heads=16, page_size=64, max_pages_per_seq=1024,
-                         num_pages=16 * 1024, num_sms=152)
-    assert bf.chunk_tokens == 108 * 64 and bf.max_splits == 10
-    assert bf.split_major == 1 and plan.split_major == 0  # 160 CTAs with work on 152 SMs; 144
-    assert _plan_cost([1024] * 16, 1, 108, 152) == 113 < _plan_cost([1024] * 16, 1, 114, 152) == 119
 
 
 def test_plan_single_split_needs_no_workspace(mla):
@@ -206,7 +209,8 @@ def test_plan_invariants_on_random_batches(mla):
             one_wave = min(c for c in range(lo, mt + 1) if n_ctas(c) <= sms)
             cands.append(one_wave)
         if groups == 1:
-            cands += [c for c in (-(-sum(tiles) // (w * sms)) for w in (1, 2)) if lo <= c < mt]
+            base1, base2 = -(-sum(tiles) // sms), -(-sum(tiles) // (2 * sms))
+            cands += [c for c in [base1 + d for d in range(9)] + [base2] if lo <= c < mt]
         cost = lambda c: _plan_cost(tiles, groups, c, sms)
         assert ct in cands + [mt]
         assert cost(ct) == min(cost(c) for c in cands)

@@ -147,14 +147,18 @@ def test_decode_small(mla, oracle_mod, name, B, T, H, lens, P, kv, peaked):
     _full_check(mla, oracle_mod, wl)
 
 
+@pytest.mark.parametrize("q_len", [4, 2], ids=["rows64", "rows32"])
 @pytest.mark.parametrize("num_sms", [1, 3, 16, 152, 100000])
-def test_decode_split_counts_agree(mla, oracle_mod, num_sms):
+def test_decode_split_counts_agree(mla, oracle_mod, num_sms, q_len):
     """Different split counts (one split per request up to the minimum chunk) give the
-    oracle's result; the LSE merge of the partials is exercised whenever splits > 1."""
-    wl = DecodeWorkload("splits", 3, 4, 16, [3000, 65, 9000], seed=77, peaked=True)
+    oracle's result; the LSE merge of the partials is exercised whenever splits > 1.  On 1
+    and 3 SMs the plans take more than one wave and launch split by split; q_len 2 x 16
+    heads runs the kernel with Q in tensor memory."""
+    wl = DecodeWorkload("splits", 3, q_len, 16, [3000, 65, 9000], seed=77, peaked=True)
     _, _, plan = _full_check(mla, oracle_mod, wl, num_sms=num_sms)
     if num_sms >= 152:
         assert plan.max_splits > 1
+    assert plan.split_major == (1 if num_sms <= 3 else 0)
 
 
 @pytest.mark.parametrize("kv", ["bf16", "e4m3", "int8"])

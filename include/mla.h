@@ -96,7 +96,9 @@ typedef struct mla_decode_plan_t {
  * 64-row group); the plan estimates the call's duration by dispatching those CTAs in
  * launch order onto the SM that frees first (each costing its tiles plus a fixed
  * start-up and epilogue cost that depends on the pool format, plus the combine when a
- * request is split), over these chunks: the longest request in 1-4 splits, the smallest
+ * request is split), over these chunks: the longest request in 1-4 splits (1-32 with more
+ * than one row group when the others leave the SMs idle over a tenth of the call), the
+ * smallest
  * chunk that keeps the call in one wave of CTAs when the unsplit call fits one, and, with
  * one row group, the chunks that share all tiles evenly over one or two waves (and up to
  * 8 tiles more than the one-wave one).  The chunk

@@ -11,6 +11,7 @@
 #include <cstring>
 #include <functional>
 #include <mutex>
+#include <limits>
 #include <queue>
 #include <string>
 #include <unordered_map>
@@ -117,19 +118,28 @@ bool split_major_order(int groups) { return groups == 1; }
 // CTAs, in the grid's launch order (group fastest, then split_major_order's), are
 // dispatched each onto the SM that frees first; CTAs of splits a request does not have
 // exit at once and cost nothing.  Plus the combine, when some request is split.
-long long plan_cost(const std::vector<int>& tiles, int groups, int ct, int sms, long long fixed) {
+// `bound`: the caller only needs costs up to it; once the estimate is known to exceed it,
+// some value above it is returned without finishing the schedule.  A negative bound
+// returns a lower bound on the estimate (exact for a one-wave plan).
+long long plan_cost(const std::vector<int>& tiles, int groups, int ct, int sms, long long fixed,
+                    long long bound = std::numeric_limits<long long>::max()) {
   int max_splits = 1;
-  long long n_ctas = 0, longest = 0;
+  long long n_ctas = 0, longest = 0, work = 0;
   for (int t : tiles) {
     const int ns = (t + ct - 1) / ct;
     max_splits = std::max(max_splits, ns);
     n_ctas += static_cast<long long>(ns) * groups;
     longest = std::max<long long>(longest, std::min(t, ct));
+    work += (static_cast<long long>(t) + static_cast<long long>(ns) * fixed) * groups;
   }
+  const long long combine = max_splits > 1 ? kCombineTiles : 0;
   long long span;
   if (n_ctas <= sms) {
     span = longest + fixed;  // one wave: the longest CTA
   } else {
+    // no schedule is shorter than its longest CTA or than the work spread over every SM
+    const long long lower = std::max(longest + fixed, (work + sms - 1) / sms) + combine;
+    if (lower > bound) return lower;  // (with bound < 0: the lower bound itself)
     std::priority_queue<long long, std::vector<long long>, std::greater<long long>> free_at;
     for (int i = 0; i < sms; ++i) free_at.push(0);
     span = 0;
@@ -141,23 +151,26 @@ long long plan_cost(const std::vector<int>& tiles, int groups, int ct, int sms, 
         free_at.push(start + cost);
         span = std::max(span, start + cost);
       }
+      return span + combine <= bound;  // (the span only grows)
     };
+    bool go = true;
     if (split_major_order(groups)) {
-      for (int s = 0; s < max_splits; ++s)
-        for (int t : tiles)
-          if (s * static_cast<long long>(ct) < t) dispatch(t, s);
+      for (int s = 0; go && s < max_splits; ++s)
+        for (size_t i = 0; go && i < tiles.size(); ++i)
+          if (s * static_cast<long long>(ct) < tiles[i]) go = dispatch(tiles[i], s);
     } else {
-      for (int t : tiles)
-        for (int s = 0; s * static_cast<long long>(ct) < t; ++s) dispatch(t, s);
+      for (size_t i = 0; go && i < tiles.size(); ++i)
+        for (int s = 0; go && s * static_cast<long long>(ct) < tiles[i]; ++s) go = dispatch(tiles[i], s);
     }
   }
-  return span + (max_splits > 1 ? kCombineTiles : 0);
+  return span + combine;
 }
 
 // Keys-per-split chunk in whole 64-key tiles (at least 4 tiles, or the whole of the
 // longest request when it is shorter).  Candidates: the smallest chunk for which the
 // partial kernel needs no more CTAs than the GPU has SMs (one wave; when the unsplit call
-// already fits), the longest request cut into 1-4 splits, and, for calls of one row group,
+// already fits), the longest request cut into 1-4 splits (1-32 with several row groups
+// that the others leave badly balanced, below), and, for calls of one row group,
 // the chunks that share all tiles evenly over one or two waves of SMs (the one-wave one and
 // up to 8 tiles more).  (A batch of equal requests that one wave leaves a few SMs short of,
 // e.g. 16 x 1024 tiles on 152 SMs as 144 CTAs of 114, then runs as 144 CTAs of 108 plus 16
@@ -210,13 +223,31 @@ int choose_chunk_tiles(const std::vector<int>& lens, int groups, int sms, long l
       }
     }
   }
+  // A candidate wins with a lower cost, or an equal one and fewer splits (a longer chunk),
+  // so costs above the best so far need not be finished.
   int best = max_tiles;
   long long best_cost = plan_cost(tiles, groups, max_tiles, sms, fixed);
-  for (int ct : cands) {
-    const long long c = plan_cost(tiles, groups, ct, sms, fixed);
+  auto consider = [&](int ct) {
+    const long long c = plan_cost(tiles, groups, ct, sms, fixed, best_cost);
     if (c < best_cost || (c == best_cost && ct > best)) {
       best = ct;
       best_cost = c;
+    }
+  };
+  for (int ct : cands) consider(ct);
+  // Several row groups (tensor-bound; each tile shared through L2) whose best plan so far
+  // leaves the SMs idle more than a tenth of it (its cost above 1.1 x the work spread over
+  // every SM, e.g. a ragged batch cut into one wave): also the longest request in 5-32
+  // splits, whose shorter CTAs even the load out over several waves.
+  if (groups > 1) {
+    long long work = 0;
+    for (int t : tiles) work += (static_cast<long long>(t) + fixed) * groups;
+    const long long spread = (work + sms - 1) / sms;
+    if (10 * best_cost > 11 * spread) {
+      for (int k = 5; k <= 32; ++k) {
+        const int ct = (max_tiles + k - 1) / k;
+        if (ct >= lo) consider(ct);
+      }
     }
   }
   return best;

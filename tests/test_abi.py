@@ -142,13 +142,35 @@ def test_plan_splits_a_multi_wave_absorbed_prefill(mla):
     """4 requests x 512 new tokens x 16 heads on 32K keys: 128 row groups per request, 512
     CTAs unsplit (3.4 waves of 152 SMs: 4 x 515 = 2060 tile-times).  Two splits of 256
     tiles: 1024 CTAs in 6.7 waves, 7 x 259 + 2 = 1815 (three: 1536 CTAs of ~174, four:
-    2048 CTAs of 131, 14 x 131 + 2 = 1836)."""
+    2048 CTAs of 131, 14 x 131 + 2 = 1836).  1815 is within 1.1 x the work spread over the
+    SMs (4 x 128 x 515 / 152 = 1735), so the wider scan of 5-32 splits does not run."""
     plan = mla.decode_plan([32768] * 4, q_len=512, num_heads=16, page_size=64, max_pages_per_seq=512,
                            num_pages=2048, num_sms=152)
-    assert plan.head_groups == 128
+    assert plan.head_groups == 128 and plan.split_major == 0
     assert plan.chunk_tokens == 256 * 64 and plan.max_splits == 2
     assert plan.workspace_bytes == 256 + 4 * 2 * 512 * 16 * (512 * 2 + 4)
     assert _plan_cost([512] * 4, 128, 256, 152) == 1815 and _plan_cost([512] * 4, 128, 512, 152) == 2060
+    assert 10 * 1815 <= 11 * -(-4 * 128 * 515 // 152)
+
+
+def test_plan_evens_out_a_ragged_many_head_batch(mla):
+    """16 requests of 8K-128K keys at q_len 2 x 128 heads (four row groups): the one-wave
+    plan (4 splits of the longest request, 152 CTAs) leaves the SMs far less work on
+    average than its longest CTA, over 1.1 x the spread, so the planner also tries 5-32
+    splits; one of those wins, its shorter CTAs evened out over several waves."""
+    rng = np.random.default_rng(2026)
+    lens = [int(x) for x in rng.integers(8192, 131073, 16)]
+    tiles = [(L + 63) // 64 for L in lens]
+    mp = max(tiles)
+    plan = mla.decode_plan(lens, q_len=2, num_heads=128, page_size=64, max_pages_per_seq=mp, num_pages=16 * mp,
+                           num_sms=152)
+    ct = plan.chunk_tokens // 64
+    assert plan.head_groups == 4 and plan.split_major == 0
+    one_wave = min(c for c in range(4, mp + 1) if 4 * sum(-(-t // c) for t in tiles) <= 152)
+    spread = -(-sum((t + 3) * 4 for t in tiles) // 152)
+    assert 10 * _plan_cost(tiles, 4, one_wave, 152) > 11 * spread
+    assert -(-mp // ct) > 4 and _plan_cost(tiles, 4, ct, 152) < _plan_cost(tiles, 4, one_wave, 152)
+    assert _plan_cost(tiles, 4, ct, 152) == min(_plan_cost(tiles, 4, -(-mp // k), 152) for k in range(1, 33))
 
 
 def test_plan_one_sm_never_splits(mla):
@@ -177,8 +199,10 @@ def test_plan_invariants_on_random_batches(mla):
     128 heads, several SM counts): the split chunk is whole 64-key tiles, at least four of
     them (or the whole of the longest request), or fewer where the longest request still
     takes at most 32 splits (one round of the combine); the plan's estimated duration is the
-    lowest over its candidates (1-4 splits of the longest request, the smallest chunk that
-    keeps the call in one wave when the unsplit call fits one, and with one row group the
+    lowest over its candidates (1-4 splits of the longest request, 1-32 with several row
+    groups when the others cost over 1.1 x the work spread over the SMs, the smallest chunk
+    that keeps the call in one wave when the unsplit call fits one, and with one row group
+    the
     chunks that share all tiles evenly over one or two waves), so it is never longer
     than the unsplit call's; a split that fits one wave is the smallest such chunk; and the
     workspace fits every split."""
@@ -203,7 +227,7 @@ def test_plan_invariants_on_random_batches(mla):
         assert plan.head_groups == groups
         n_ctas = lambda c: groups * sum((t + c - 1) // c for t in tiles)
         assert plan.max_splits == (max(lens) + plan.chunk_tokens - 1) // plan.chunk_tokens
-        cands = [c for c in (-(-mt // k) for k in (1, 2, 3, 4)) if c >= lo]
+        cands = [c for c in (-(-mt // k) for k in range(1, 5)) if c >= lo]
         one_wave = None
         if n_ctas(mt) <= sms:
             one_wave = min(c for c in range(lo, mt + 1) if n_ctas(c) <= sms)
@@ -212,6 +236,10 @@ def test_plan_invariants_on_random_batches(mla):
             base1, base2 = -(-sum(tiles) // sms), -(-sum(tiles) // (2 * sms))
             cands += [c for c in [base1 + d for d in range(9)] + [base2] if lo <= c < mt]
         cost = lambda c: _plan_cost(tiles, groups, c, sms)
+        if groups > 1:
+            spread = -(-sum((t + 3) * groups for t in tiles) // sms)
+            if 10 * min(cost(c) for c in cands + [mt]) > 11 * spread:
+                cands += [c for c in (-(-mt // k) for k in range(5, 33)) if c >= lo]
         assert ct in cands + [mt]
         assert cost(ct) == min(cost(c) for c in cands)
         assert cost(ct) <= cost(mt)

@@ -33,12 +33,29 @@
 //    buffer, so it never touches shared memory.
 //  * Epilogue: O / l to bf16 and the natural-log LSE, straight from TMEM (each half of a
 //    row writes its 64 value columns; the row sum is the two halves' partial sums).
+//  * Key-range split: a (request, head, q block) of at least kMinSplitTiles key tiles runs
+//    as two CTAs over the first and second half of its tiles, so that the grid's CTAs are
+//    small enough to even out over the SMs (a few hundred to ~750 tiles each, 3-4 per SM
+//    otherwise, left SMs idle ~10 % of the call at its end).  Each half writes its
+//    normalised partial and LSE (the first half into out / lse, the second into a scratch
+//    slot), fences, and counts itself on the pair's counter; the half that arrives second
+//    merges the two (weights exp(lse_i - max)) into out / lse and clears the counter.
+//    Neither half ever waits for the other.
 // Every wait is bounded; on expiry the CTA records a timeout in the status word, drains
 // its in-flight copies and MMAs, frees TMEM and returns.
 #include "mla_internal.h"
 #include "sm103a_ptx.cuh"
 
 namespace mla {
+
+// Scratch of the key-range split: the second half's partial output (bf16, 128 rows x 128
+// value columns) and LSE per slot, and each slot's arrival counter (cleared before every
+// launch).
+constexpr int kSplitSlots = 1024;
+__device__ uint4 g_split_o[kSplitSlots * 128 * 128 * 2 / 16];
+__device__ float g_split_lse[kSplitSlots * 128];
+__device__ int g_split_count[kSplitSlots];
+
 namespace {
 
 constexpr int kDqk = 192;
@@ -52,6 +69,9 @@ constexpr int kProducerWarp = kSoftmaxWarps;
 constexpr int kMmaWarp = kSoftmaxWarps + 1;   // issues BMM1 (and owns TMEM)
 constexpr int kBmm2Warp = kSoftmaxWarps + 2;  // issues BMM2
 constexpr int kThreads = 32 * (kSoftmaxWarps + 3);
+
+constexpr int kMinSplitTiles = 8;     // key tiles from which a q block is split in two
+constexpr int kMaxSplitPairs = kSplitSlots;  // q blocks past the scratch slots are not split
 
 constexpr int kQBlockBytes = kBM * 128;                // 16 KB per 64-column block
 constexpr int kQBytes = (kDqk / 64) * kQBlockBytes;    // 48 KB
@@ -78,6 +98,7 @@ struct PrefillCtrl {
   uint64_t mma_drain2;     // the BMM2 warp's MMAs
   uint32_t tmem_base;
   int abort_flag;
+  int split_arrival;       // key-range split: 0 if this half finished first, 1 if second
   float row_max[2][kBM];   // per half of the key tile: this tile's partial row maxima
   float row_sum[2][kBM];   // per half: partial row sums (epilogue)
 };
@@ -115,9 +136,10 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
   const int lane = threadIdx.x & 31;
   const int h = blockIdx.y;
   // Longest work first: blockIdx.z is the rank of the request by its key count (descending,
-  // ties by index) and blockIdx.x counts q blocks down from the last one, so the in-order
-  // dispatch of the grid starts the longest CTAs first and the shorter ones fill in behind
-  // them (per-CTA work spans a few hundred to a few thousand tiles across requests).
+  // ties by index) and blockIdx.x / 2 counts q blocks down from the last one, so the
+  // in-order dispatch of the grid starts the longest CTAs first and the shorter ones fill
+  // in behind them (per-CTA work spans a few hundred to a few thousand tiles across
+  // requests).  blockIdx.x % 2 is the half of a split key range.
   __shared__ int s_req;
   int b = blockIdx.z;
   if (p.B <= kThreads) {
@@ -134,7 +156,9 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     __syncthreads();
     b = s_req;
   }
-  const int qb = static_cast<int>(gridDim.x) - 1 - static_cast<int>(blockIdx.x);
+  const int n_qb = static_cast<int>(gridDim.x >> 1);
+  const int qb = n_qb - 1 - static_cast<int>(blockIdx.x >> 1);
+  const int part = static_cast<int>(blockIdx.x & 1u);
 
   const int q_start = p.cu_q[b];
   const int n_b = p.cu_q[b + 1] - q_start;
@@ -150,7 +174,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                    (kPaged ? static_cast<int64_t>(kv_total) > static_cast<int64_t>(p.max_pages) * p.page_size
                            : static_cast<int64_t>(kv_start) + kv_total > p.total_kv);
   if (bad) {
-    if (threadIdx.x == 0 && qb == 0 && h == 0) atomicOr(p.status, kStatusDeviceArg);
+    if (threadIdx.x == 0 && qb == 0 && h == 0 && part == 0) atomicOr(p.status, kStatusDeviceArg);
     return;
   }
   const int row_begin = qb * kBM;
@@ -159,6 +183,12 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
   const int kv_len = pre + row_begin + rows;  // keys any row of this block can see
   const int ntiles = (kv_len + kBN - 1) / kBN;
   const int diag_tile = (pre + row_begin) / kBN;  // first tile that may need the causal mask
+  // key-range split: this CTA takes tiles [t_lo, t_lo + nloc) of the q block's ntiles
+  const int slot = (static_cast<int>(blockIdx.z) * p.H + h) * n_qb + (n_qb - 1 - qb);
+  const bool split = ntiles >= kMinSplitTiles && slot < kMaxSplitPairs;
+  if (part == 1 && !split) return;  // (CTA-uniform, before any set-up)
+  const int t_lo = (split && part == 1) ? ntiles / 2 : 0;
+  const int nloc = split ? (part == 0 ? ntiles / 2 : ntiles - ntiles / 2) : ntiles;
 
   if (threadIdx.x == 0) {
     mbar_init(&ctrl->q_full, 1);
@@ -211,13 +241,13 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         uint64_t* empty = is_k ? ctrl->k_empty : ctrl->v_empty;
         int last_issued[kStages] = {-1, -1};
         bool ok = true;
-        for (int j = 0; j < ntiles; ++j) {
+        for (int j = 0; j < nloc; ++j) {
           const int s = j % kStages;
           if (j >= kStages) {
             ok = mbar_wait(&empty[s], ((j / kStages) - 1) & 1, abort_flag);
             if (!ok) break;
           }
-          const int row = kv_start + j * kBN;
+          const int row = kv_start + (t_lo + j) * kBN;
           if (is_k) {
             mbar_arrive_expect_tx(&full[s], kKBytes);
             tma_load_4d(smem + kOffK + s * kKBytes, &tm_k, &full[s], 0, row, 0, h, pol_kv);  // 128 rows x 3 blocks
@@ -260,10 +290,10 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       const int32_t* pt = p.page_table + static_cast<int64_t>(b) * p.max_pages;
       const unsigned n_pages = static_cast<unsigned>(min(p.num_pages, static_cast<int64_t>(0x7fffffff)));
       bool bad_pid = false;
-      auto page_id = [&](int jt, int bx) -> int {  // page of box bx of tile jt, or -1
+      auto page_id = [&](int jt, int bx) -> int {  // page of box bx of (absolute) tile jt, or -1
         const int pg = jt * kBN / P + (P >= kBN ? 0 : bx / nblk);
         int v = -1;
-        if (bx < nbox && jt < ntiles && pg < pages_b) {
+        if (bx < nbox && jt < t_lo + nloc && pg < pages_b) {
           v = __ldg(pt + pg);
           if (static_cast<unsigned>(v) >= n_pages) {
             bad_pid = true;
@@ -275,10 +305,10 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       const CUtensorMap* map = is_k ? &tm_k : &tm_v;
       int last_issued[kStages] = {-1, -1};
       bool ok = true;
-      int cur0 = page_id(0, gl), cur1 = page_id(0, gl + 16);
-      for (int j = 0; j < ntiles; ++j) {
+      int cur0 = page_id(t_lo, gl), cur1 = page_id(t_lo, gl + 16);
+      for (int j = 0; j < nloc; ++j) {
         const int s = j % kStages;
-        const int nxt0 = page_id(j + 1, gl), nxt1 = page_id(j + 1, gl + 16);
+        const int nxt0 = page_id(t_lo + j + 1, gl), nxt1 = page_id(t_lo + j + 1, gl + 16);
         if (j >= kStages) {
           bool w = true;
           if (gl == 0) w = mbar_wait(&empty[s], ((j / kStages) - 1) & 1, abort_flag);
@@ -289,7 +319,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         if (gl == 0) mbar_arrive_expect_tx(&full[s], is_k ? kKBytes : kVBytes);
         __syncwarp(gmask);  // the barrier is armed before any of the group's copies can land
         if (P >= kBN) {
-          if (gl == 0) tma_load_4d(dst, map, &full[s], 0, cur0 * P + (j * kBN) % P, 0, h, pol_kv);
+          if (gl == 0) tma_load_4d(dst, map, &full[s], 0, cur0 * P + ((t_lo + j) * kBN) % P, 0, h, pol_kv);
         } else {
 #pragma unroll
           for (int k = 0; k < 2; ++k) {
@@ -321,8 +351,9 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     const uint32_t idesc1 = make_idesc_bf16(kBM, kBN, false, false);
     const uint64_t q_desc = make_smem_desc(smem_u32(smem + kOffQ), 16, 1024);
     bool ok = mbar_wait(&ctrl->q_full, 0, abort_flag);
-    // BMM1(j) once K(j) has landed and BMM2(j-2) has read the P in its S buffer
-    for (int j = 0; j < ntiles; ++j) {
+    // BMM1(j) once K(j) has landed and BMM2(j-2) has read the P in its S buffer (j counts
+    // this CTA's tiles)
+    for (int j = 0; j < nloc; ++j) {
       const int s = j % kStages, sb = j & 1;
       if (ok) ok = mbar_wait(&ctrl->k_full[s], (j / kStages) & 1, abort_flag);
       if (ok && j >= 2) ok = mbar_wait(&ctrl->s_consumed[sb], ((j - 2) >> 1) & 1, abort_flag);
@@ -352,7 +383,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     // as soon as P(j) and V(j) are ready (it frees a V stage and an S buffer)
     const uint32_t idesc2 = make_idesc_bf16(kBM, kDv, false, true);
     bool ok = true;
-    for (int j = 0; j < ntiles; ++j) {
+    for (int j = 0; j < nloc; ++j) {
       const int s = j % kStages, sb = j & 1;
       if (ok) ok = mbar_wait(&ctrl->p_full, j & 1, abort_flag);
       if (ok) ok = mbar_wait(&ctrl->v_full[s], (j / kStages) & 1, abort_flag);
@@ -394,9 +425,9 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     float m_used = -INFINITY;
     float l_sum = 0.f;  // this half's share of the row sum
     bool failed = false;
-    for (int j = 0; j < ntiles; ++j) {
+    for (int j = 0; j < nloc; ++j) {
       const int sb = j & 1;
-      const int k0 = j * kBN + 64 * hf;
+      const int k0 = (t_lo + j) * kBN + 64 * hf;  // absolute key of this half's first column
       const uint32_t s_tmem = tmem + lane_base + kTmemS + sb * 128;
       bool fail = !mbar_wait(&ctrl->s_full[sb], (j >> 1) & 1, abort_flag);
       fail = __any_sync(0xffffffffu, fail);
@@ -409,7 +440,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         tmem_ld32(s_tmem + 64 * hf, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
         tmem_ld32(s_tmem + 64 * hf + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
         tmem_ld_wait();
-        lim = (j >= diag_tile) ? (row_active ? vis_last - k0 : -1) : (row_active ? 63 : -1);
+        lim = (t_lo + j >= diag_tile) ? (row_active ? vis_last - k0 : -1) : (row_active ? 63 : -1);
         float mx = -INFINITY;
         if (lim >= 63) {
 #pragma unroll
@@ -488,32 +519,83 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       tc_fence_before();
       mbar_arrive(&ctrl->p_full);
     }
-    if (!failed) failed = !mbar_wait(&ctrl->o_done, (ntiles - 1) & 1, abort_flag);
+    if (!failed) failed = !mbar_wait(&ctrl->o_done, (nloc - 1) & 1, abort_flag);
     if (!failed) ctrl->row_sum[hf][r] = l_sum;
     if (!bar_or(1, kSoftmaxThreads, failed || (*abort_flag != 0))) {
       tc_fence_after();
       const float l_tot = ctrl->row_sum[0][r] + ctrl->row_sum[1][r];
       const float inv = (l_tot > 0.f) ? 1.f / l_tot : 0.f;
       const int64_t tok = static_cast<int64_t>(q_start) + row_begin + r;
+      const float lse_own = (l_tot > 0.f) ? (m_used + __log2f(l_tot)) * 0.69314718055994530942f : -INFINITY;
+      // this thread's 64 value columns of its row: in out, or (second half of a split) in
+      // the slot's scratch row
+      uint4* const out_row = reinterpret_cast<uint4*>(p.out + (tok * p.H + h) * kDv + 64 * hf);
+      uint4* const scratch_row = g_split_o + (static_cast<int64_t>(slot) * kBM + r) * (kDv * 2 / 16) + hf * 8;
+      uint4* const dst = (split && part == 1) ? scratch_row : out_row;
+      float o[64];  // normalised O of this thread's columns (kept for a merge)
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
         uint32_t v[32];
         tmem_ld32(tmem + lane_base + kTmemO + 64 * hf + c * 32, v);
         tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) o[32 * c + i] = __uint_as_float(v[i]) * inv;
         if (row_active) {
-          uint4* dst = reinterpret_cast<uint4*>(p.out + (tok * p.H + h) * kDv + 64 * hf + c * 32);
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
-            dst[i] = make_uint4(pack_bf16x2(__uint_as_float(v[8 * i + 0]) * inv, __uint_as_float(v[8 * i + 1]) * inv),
-                                pack_bf16x2(__uint_as_float(v[8 * i + 2]) * inv, __uint_as_float(v[8 * i + 3]) * inv),
-                                pack_bf16x2(__uint_as_float(v[8 * i + 4]) * inv, __uint_as_float(v[8 * i + 5]) * inv),
-                                pack_bf16x2(__uint_as_float(v[8 * i + 6]) * inv, __uint_as_float(v[8 * i + 7]) * inv));
+            const float* f = &o[32 * c + 8 * i];
+            dst[4 * c + i] = make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]), pack_bf16x2(f[4], f[5]),
+                                        pack_bf16x2(f[6], f[7]));
           }
         }
       }
       if (row_active && hf == 0) {
-        const float lse2 = (l_tot > 0.f) ? (m_used + __log2f(l_tot)) : -INFINITY;
-        p.lse[tok * p.H + h] = lse2 * 0.69314718055994530942f;
+        if (split && part == 1)
+          g_split_lse[slot * kBM + r] = lse_own;
+        else
+          p.lse[tok * p.H + h] = lse_own;
+      }
+      if (split) {
+        // publish this half's partial, then count it; the half that counts second merges
+        __threadfence();
+        named_bar_sync(1, kSoftmaxThreads);
+        if (threadIdx.x == 0) ctrl->split_arrival = atomicAdd(&g_split_count[slot], 1);
+        named_bar_sync(1, kSoftmaxThreads);
+        if (ctrl->split_arrival == 1) {
+          __threadfence();
+          if (row_active) {
+            // The same arithmetic whichever half arrives second: both halves' bf16 partials
+            // (this half's as it wrote them), combined first half first.
+            const float lse_oth = (part == 1) ? __ldcg(p.lse + tok * p.H + h) : __ldcg(g_split_lse + slot * kBM + r);
+            const uint4* const oth = (part == 1) ? out_row : scratch_row;
+            const float lse0 = part == 0 ? lse_own : lse_oth;
+            const float lse1 = part == 0 ? lse_oth : lse_own;
+            const float m = fmaxf(lse0, lse1);
+            const float w0 = (lse0 == -INFINITY) ? 0.f : __expf(lse0 - m);
+            const float w1 = (lse1 == -INFINITY) ? 0.f : __expf(lse1 - m);
+            const float tot = w0 + w1;
+            const float a0 = (tot > 0.f) ? w0 / tot : 0.f;
+            const float a1 = (tot > 0.f) ? w1 / tot : 0.f;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const uint4 u = __ldcg(oth + i);
+              const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+              uint32_t pk[4];
+#pragma unroll
+              for (int k = 0; k < 4; ++k) {
+                const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[k]));
+                const float own_x = __bfloat162float(__float2bfloat16_rn(o[8 * i + 2 * k]));
+                const float own_y = __bfloat162float(__float2bfloat16_rn(o[8 * i + 2 * k + 1]));
+                const float x0 = part == 0 ? own_x : f.x, x1 = part == 0 ? f.x : own_x;
+                const float y0 = part == 0 ? own_y : f.y, y1 = part == 0 ? f.y : own_y;
+                pk[k] = pack_bf16x2(__fmaf_rn(a1, x1, __fmul_rn(a0, x0)), __fmaf_rn(a1, y1, __fmul_rn(a0, y0)));
+              }
+              out_row[i] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            }
+            if (hf == 0) p.lse[tok * p.H + h] = (tot > 0.f) ? m + __logf(tot) : -INFINITY;
+          }
+          if (threadIdx.x == 0) g_split_count[slot] = 0;
+        }
       }
     }
   }
@@ -544,7 +626,20 @@ cudaError_t launch_prefill(const PrefillParams& p, const CUtensorMap& tm_q, cons
     configured_device[paged] = dev;
   }
   if (p.max_q_blocks < 1) return cudaSuccess;
-  dim3 grid(p.max_q_blocks, p.H, p.B);
+  // the split counters start at zero (the merging half clears its own; a launch that gave
+  // up part-way may not have)
+  static thread_local int count_device = -1;
+  static thread_local void* count_ptr = nullptr;
+  if (count_device != dev) {
+    e = cudaGetSymbolAddress(&count_ptr, g_split_count);
+    if (e != cudaSuccess) return e;
+    count_device = dev;
+  }
+  const long long slots = static_cast<long long>(p.B) * p.H * p.max_q_blocks;
+  e = cudaMemsetAsync(count_ptr, 0, sizeof(int) * static_cast<size_t>(slots < kSplitSlots ? slots : kSplitSlots),
+                      stream);
+  if (e != cudaSuccess) return e;
+  dim3 grid(2 * p.max_q_blocks, p.H, p.B);
   if (paged)
     prefill_kernel<true><<<grid, kThreads, kSmemBytes, stream>>>(tm_q, tm_k, tm_v, p);
   else

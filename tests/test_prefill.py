@@ -59,6 +59,9 @@ SMALL = [
     ("empty_request", [10, 40], [0, 77], 16),
     ("long_prefix", [5000], [260], 16),
     ("many_heads", [100], [200], 32),
+    # q blocks with at least 8 key tiles run as two CTAs over the two halves of their keys
+    ("causal_split", [0], [1300], 4),          # no prefix: the causal diagonal in both halves
+    ("prefix_split", [1500, 3000], [200, 40], 8),
 ]
 
 
@@ -82,6 +85,24 @@ def test_prefill_peaked_scores(mla, oracle_mod):
     ref_out, ref_lse = oracle_mod.mla_prefill(inp.q, inp.k, inp.v, inp.cu_seqlens_q, inp.cu_seqlens_kv,
                                               inp.prefix_lens, inp.scale)
     check(out, lse, ref_out, ref_lse)
+
+
+def test_prefill_split_halves_are_deterministic(mla):
+    """Two CTAs share a q block's keys and the one that finishes second merges: the result
+    must not depend on which that is.  Five runs of a prefill whose q blocks all split
+    give the same bits."""
+    wl = PrefillWorkload("split_repeat", [2000, 4000], [300, 700], 8, seed=21)
+    inp = make_prefill_inputs(wl, "cpu")
+    dev = "cuda"
+    outs = []
+    for _ in range(5):
+        out, lse = mla.prefill_varlen(inp.q.to(dev), inp.k.to(dev), inp.v.to(dev), inp.cu_seqlens_q.to(dev),
+                                      inp.cu_seqlens_kv.to(dev), inp.prefix_lens.to(dev), inp.max_seqlen_q, inp.scale)
+        torch.cuda.synchronize()
+        assert mla.get_status() == mla.MLA_OK
+        outs.append((out.view(torch.int16).cpu(), lse.view(torch.int32).cpu()))
+    for o, l in outs[1:]:
+        assert torch.equal(o, outs[0][0]) and torch.equal(l, outs[0][1])
 
 
 def test_prefill_no_new_tokens_is_a_no_op(mla):

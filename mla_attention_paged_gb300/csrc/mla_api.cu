@@ -119,8 +119,7 @@ bool split_major_order(int groups) { return groups == 1; }
 // dispatched each onto the SM that frees first; CTAs of splits a request does not have
 // exit at once and cost nothing.  Plus the combine, when some request is split.
 // `bound`: the caller only needs costs up to it; once the estimate is known to exceed it,
-// some value above it is returned without finishing the schedule.  A negative bound
-// returns a lower bound on the estimate (exact for a one-wave plan).
+// some value above it is returned without finishing the schedule.
 long long plan_cost(const std::vector<int>& tiles, int groups, int ct, int sms, long long fixed,
                     long long bound = std::numeric_limits<long long>::max()) {
   int max_splits = 1;
@@ -139,7 +138,7 @@ long long plan_cost(const std::vector<int>& tiles, int groups, int ct, int sms, 
   } else {
     // no schedule is shorter than its longest CTA or than the work spread over every SM
     const long long lower = std::max(longest + fixed, (work + sms - 1) / sms) + combine;
-    if (lower > bound) return lower;  // (with bound < 0: the lower bound itself)
+    if (lower > bound) return lower;
     std::priority_queue<long long, std::vector<long long>, std::greater<long long>> free_at;
     for (int i = 0; i < sms; ++i) free_at.push(0);
     span = 0;
@@ -175,9 +174,9 @@ long long plan_cost(const std::vector<int>& tiles, int groups, int ct, int sms, 
 // up to 8 tiles more).  (A batch of equal requests that one wave leaves a few SMs short of,
 // e.g. 16 x 1024 tiles on 152 SMs as 144 CTAs of 114, then runs as 144 CTAs of 108 plus 16
 // remainders of 52, the remainders launched last and paired up on the SMs that free first;
-// with an e4m3 pool's larger fixed cost, 109 and remainders of 43.)  The candidate with the lowest
-// plan_cost wins, the one with fewer splits on a tie, so a split is only taken when the
-// model says it shortens the call.
+// with an e4m3 pool's larger fixed cost, 109 and remainders of 43.)  The candidate with the
+// lowest plan_cost wins, the one with fewer splits on a tie, so a split is only taken when
+// the model says it shortens the call.
 int choose_chunk_tiles(const std::vector<int>& lens, int groups, int sms, long long fixed) {
   std::vector<int> tiles;
   tiles.reserve(lens.size());

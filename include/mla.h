@@ -239,7 +239,13 @@ int mla_decode_noalloc(const mla_decode_plan_t* plan, const void* q, const void*
  * MLA_ERR_CUDA.  Device-side, recorded in the status word as MLA_ERR_DEVICE_ARG (read by
  * mla_get_status) before any load or store of the request: its kv length differs from
  * p_b + n_b, n_b > max_seqlen_q, or its rows reach beyond total_q / total_kv.  That
- * request is skipped and its out/lse rows are left unwritten. */
+ * request is skipped and its out/lse rows are left unwritten.
+ * Scratch: a q block with 8 or more tiles of 128 keys runs as two CTAs over the halves of
+ * its keys, which merge through this library's own device scratch (32 MiB per GPU, 1024
+ * slots; q blocks past them are not split).  Prefill calls whose kernels overlap on the
+ * GPU (other streams, other threads) race on it: order them on one stream.  The first
+ * call on each device and host thread looks the scratch up; make it before any stream
+ * capture. */
 int mla_prefill_varlen(const void* q, const void* k, const void* v, const int32_t* cu_seqlens_q,
                        const int32_t* cu_seqlens_kv, const int32_t* prefix_lens, int batch,
                        int num_heads, int max_seqlen_q, int total_q, int total_kv, float scale,
@@ -267,7 +273,9 @@ int mla_prefill_varlen(const void* q, const void* k, const void* v, const int32_
  * size, too many pool rows), MLA_ERR_CUDA.  Device-side, recorded in the status word as
  * MLA_ERR_DEVICE_ARG: n_b > max_seqlen_q, kv_lens[b] < n_b or beyond the table row, q rows
  * beyond total_q (the request is skipped, before any access), and a page id outside
- * [0, num_pages) (its rows are read as zeros, never from outside the pools). */
+ * [0, num_pages) (its rows are read as zeros, never from outside the pools).
+ * Scratch: as mla_prefill_varlen (the same library-owned scratch: order every prefill
+ * call, contiguous or paged, on one stream). */
 int mla_prefill_paged(const void* q, const void* k_pages, const void* v_pages, const int32_t* page_table,
                       const int32_t* cu_seqlens_q, const int32_t* kv_lens, int batch, int num_heads,
                       int page_size, int max_pages_per_seq, int64_t num_pages, int max_seqlen_q,

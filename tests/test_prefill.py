@@ -105,6 +105,22 @@ def test_prefill_split_halves_are_deterministic(mla):
         assert torch.equal(o, outs[0][0]) and torch.equal(l, outs[0][1])
 
 
+def test_prefill_more_q_blocks_than_split_slots(mla, oracle_mod):
+    """128 heads x 9 q blocks = 1152 (request, head, q block) slots, past the 1024 scratch
+    slots of the key-range split: the first 1024 q blocks of 8+ key tiles split, the rest
+    run whole, in one launch.  Sampled rows of heads on both sides of the boundary (slots
+    are numbered head-major, so heads 113 and up hold slots past 1024) against the oracle."""
+    wl = PrefillWorkload("slots", [900], [1100], 128, seed=23)
+    inp = make_prefill_inputs(wl, "cuda")
+    out, lse = run_gpu(mla, inp)
+    H = wl.heads
+    rows = [t * H + h for t in (0, 127, 128, 700, 1023, 1024, 1099) for h in (0, 64, 112, 113, 127)]
+    ref_out, ref_lse = oracle_mod.mla_prefill(inp.q.cpu(), inp.k.cpu(), inp.v.cpu(), inp.cu_seqlens_q.cpu(),
+                                              inp.cu_seqlens_kv.cpu(), inp.prefix_lens.cpu(), inp.scale, rows=rows)
+    check(out.reshape(-1, 128)[rows], lse.reshape(-1)[rows], ref_out, ref_lse)
+    assert np.isfinite(out).all() and np.isfinite(lse).all()
+
+
 def test_prefill_no_new_tokens_is_a_no_op(mla):
     wl = PrefillWorkload("none", [10], [0], 2, seed=1)
     inp = make_prefill_inputs(wl, "cpu")

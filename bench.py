@@ -111,7 +111,7 @@ TENSOR_BOUND = ("decode_b16_q2_h128_ragged", "decode_b4_q512_h16_l32k")
 # quoted on (batch 16 / 64K prefix, and the varlen prefill), so they end the JSON line.
 EXTRA_DECODE = ["decode_b4_q4_h16_l32k", "decode_b1_q1_h16_l1024", "decode_b16_q2_h128_ragged",
                 "decode_b4_q512_h16_l32k", "decode_int8_b16_q4_h16_l64k", "decode_int8page_b16_q4_h16_l64k",
-                "decode_fp8_b8_q4_h16_l64k",
+                "decode_fp8_b8_q4_h16_l64k", "decode_fp8_b16_q2_h16_ragged",
                 "decode_bf16_b16_q4_h16_l64k", "decode_fp8_b16_q4_h16_l64k"]
 
 

@@ -210,6 +210,10 @@ __device__ __forceinline__ void p_split16(const float (&x)[16], int lim, float s
   l_use += lu;
 }
 
+// kMayIdle: q_len * heads is not a multiple of 64, so a row group may hold 48 rows or fewer
+// and a softmax warp may own no row; such warps then skip their S reads and P writes.  (A
+// compile-time choice: the check alone measured 1.2 % slower on full 64-row groups.)
+template <bool kMayIdle>
 __global__ void __launch_bounds__(kThreads, 1)
 decode_partial_e4m3_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kv,
                            const DecodeParams p) {
@@ -596,6 +600,10 @@ decode_partial_e4m3_kernel(const __grid_constant__ CUtensorMap tm_q, const __gri
     // other parity's hand-over and hands one back marked stop, then leaves; a warp that
     // receives a stop mark leaves without handing over.  Every hand-over thus has a receiver.
     bool draining = false;
+    // A warp whose 16 rows are all past the group's rows reads no S and writes no P (BMM2
+    // reads only the first nq rows of P, and nq <= 16 quad then); it keeps every barrier
+    // arrival and the hand-over, and its rows' alpha stays 1.
+    const bool idle = kMayIdle && __all_sync(0xffffffffu, !row_active[0] && !row_active[1]);
 
     for (int j = par; !failed && j < ntiles; j += 2) {
       const int pb = j & 1;  // S buffer, P buffer and flags of this tile (= par)
@@ -606,7 +614,12 @@ decode_partial_e4m3_kernel(const __grid_constant__ CUtensorMap tm_q, const __gri
       int lim[2] = {-1, -1};
       float mx[2] = {-INFINITY, -INFINITY};
       if (!fail) fail = __any_sync(0xffffffffu, !mbar_wait(&ctrl->s_full[pb], (j >> 1) & 1, abort_flag));
-      if (!fail) {
+      if (!fail && idle) {
+        tc_fence_after();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ctrl->s_free[pb]);
+      } else if (!fail) {
         tc_fence_after();
         uint32_t v0[32], v1[32];
         tmem_ld16x256b_x8(tmem + lane_base + kTmemS + pb * 64, v0);
@@ -697,7 +710,7 @@ decode_partial_e4m3_kernel(const __grid_constant__ CUtensorMap tm_q, const __gri
       }
       if (!fail) {
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
+        for (int h = 0; h < 2 && !idle; ++h) {
           const int r = rr0 + 8 * h;
           uint32_t phi[8], plo[8];
           if (lim[h] >= 57)
@@ -714,6 +727,7 @@ decode_partial_e4m3_kernel(const __grid_constant__ CUtensorMap tm_q, const __gri
           }
           if (cq == 0) ctrl->alpha[pb][r] = alpha[h];
         }
+        if (idle && cq == 0) ctrl->alpha[pb][rr0] = ctrl->alpha[pb][rr0 + 8] = 1.f;
         const bool any = __any_sync(0xffffffffu, need_rescale);
         if (lane == 0) ctrl->rescale_flag[pb][quad] = any ? 1 : 0;
         // the request's last tile: rows past its end are zeroed in the V blocks (BMM1 of this
@@ -876,7 +890,11 @@ cudaError_t launch_decode_partial_e4m3(const DecodeParams& p, const CUtensorMap&
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (configured_device != dev) {
-    e = cudaFuncSetAttribute(decode_partial_e4m3_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    e = cudaFuncSetAttribute(decode_partial_e4m3_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kSmemBytes);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(decode_partial_e4m3_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kSmemBytes);
     if (e != cudaSuccess) return e;
     configured_device = dev;
   }
@@ -890,7 +908,9 @@ cudaError_t launch_decode_partial_e4m3(const DecodeParams& p, const CUtensorMap&
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, decode_partial_e4m3_kernel, tm_q, tm_kv, p);
+  // a group of 48 rows or fewer exists when R is not a multiple of 64
+  return (p.R % kGroupRows != 0) ? cudaLaunchKernelEx(&cfg, decode_partial_e4m3_kernel<true>, tm_q, tm_kv, p)
+                                 : cudaLaunchKernelEx(&cfg, decode_partial_e4m3_kernel<false>, tm_q, tm_kv, p);
 }
 
 }  // namespace mla

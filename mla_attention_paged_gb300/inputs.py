@@ -64,7 +64,8 @@ def _ragged_lens(batch, lo, hi, seed):
 
 
 def decode_workloads():
-    """The decode workloads: small, speculative, ragged (16 and 128 heads), FP8 and its bf16 twin."""
+    """The decode workloads: small, speculative, ragged (16 and 128 heads), FP8 (q_len 4, and the
+    ragged shape) and its bf16 twin."""
     return {
         "decode_b1_q1_h16_l1024": DecodeWorkload("decode_b1_q1_h16_l1024", 1, 1, 16, [1024], seed=1000),
         "decode_b4_q4_h16_l32k": DecodeWorkload("decode_b4_q4_h16_l32k", 4, 4, 16, [32768] * 4, seed=1001),
@@ -76,6 +77,10 @@ def decode_workloads():
             "decode_fp8_b8_q4_h16_l64k", 8, 4, 16, [65536] * 8, kv_dtype="e4m3", seed=1003),
         "decode_fp8_b16_q4_h16_l64k": DecodeWorkload(
             "decode_fp8_b16_q4_h16_l64k", 16, 4, 16, [65536] * 16, kv_dtype="e4m3", seed=1003),
+        # the headline's shape over an e4m3 pool (32 folded rows per request)
+        "decode_fp8_b16_q2_h16_ragged": DecodeWorkload(
+            "decode_fp8_b16_q2_h16_ragged", 16, 2, 16, _ragged_lens(16, 8192, 131072, 1002), kv_dtype="e4m3",
+            seed=1002),
         "decode_bf16_b16_q4_h16_l64k": DecodeWorkload(
             "decode_bf16_b16_q4_h16_l64k", 16, 4, 16, [65536] * 16, seed=1003),
         "decode_int8_b16_q4_h16_l64k": DecodeWorkload(
